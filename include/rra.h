@@ -1,0 +1,218 @@
+/*
+ * rra.h -- barrier-free AllReduce over N virtual ranks on one GPU (C ABI).
+ *
+ * The operation is the AllReduce of "Every Microsecond Matters: Achieving
+ * Near Speed-of-Light Latency in GPU Collectives" (arXiv 2607.16100),
+ * Sec. III-A: every rank r contributes a vector send[r] of `count` elements
+ * and receives, in recv[r], the element-wise sum over all ranks.  The four
+ * algorithms are the paper's barrier-free designs (Sec. IV): one-shot push
+ * with the LL protocol, one-shot push with sentinel-initialised scratch,
+ * two-shot (ReduceScatter + AllGather) with bidirectional double buffering,
+ * and the two-shot LL128-atomic variant (Fig. 5).  No global barrier is used:
+ * every wait is on the arrival of data.
+ *
+ * Virtual ranks.  The N ranks live on ONE GPU.  Rank r is a group of CTAs
+ * that owns window r of one symmetric device allocation (window r starts
+ * `stride` bytes after window r-1), the single-GPU analogue of the symmetric
+ * memory windows of Sec. II-B.  A rank reads only its own input and its own
+ * window and writes only peers' windows and its own output; L2 is the point
+ * of coherence between ranks.  All CTAs of a call are launched cooperatively
+ * so that every polling CTA is co-resident with the CTAs it waits for.
+ *
+ * Results.  recv[r][i] = send[0][i] + send[1][i] + ... + send[N-1][i], the
+ * same value for every r.  One-shot and two-shot add in rank order 0..N-1
+ * with a binary32 running value for RRA_FP32/RRA_BF16 (bfloat16 results are
+ * rounded to nearest-even once at the end) and binary64 for RRA_FP64; they
+ * are bit-for-bit deterministic.  RRA_LL128_ATOMIC adds with hardware
+ * atomics in an unspecified order into binary32 (binary64 for RRA_FP64)
+ * accumulators; every rank still receives the identical bit pattern.
+ *
+ * Streams and graphs.  A call only enqueues work on `stream` (no host
+ * synchronisation, no host-to-device copies), so it can be captured into a
+ * CUDA graph; the per-call epoch lives in device memory and advances on every
+ * replay.  Calls on one communicator must be ordered on one stream.
+ *
+ * Errors.  Every function returns an rra_status_t.  Argument and CUDA launch
+ * errors are returned directly.  Errors found on the device (a poll that ran
+ * past its time limit) are recorded in a device status word: they do not
+ * fault the GPU, later calls on the same communicator become no-ops on the
+ * device, rra_comm_status() reports them, and the communicator stays
+ * poisoned (RRA_ERR_POISONED) until rra_comm_reset().
+ */
+#ifndef RRA_H
+#define RRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                     /* same type as cudaStream_t */
+typedef struct CUstream_st* rra_stream_t;
+
+typedef struct rra_comm* rra_comm_t;    /* opaque communicator */
+
+#define RRA_MAX_RANKS 64
+
+typedef enum {
+    RRA_OK = 0,
+    RRA_ERR_INVALID_ARG = 1,     /* bad pointer, size, dtype, algo, alignment */
+    RRA_ERR_CUDA = 2,            /* a CUDA runtime call failed */
+    RRA_ERR_OOM = 3,             /* device allocation failed */
+    RRA_ERR_NOT_CORESIDENT = 4,  /* N ranks cannot all be resident at once */
+    RRA_ERR_TIMEOUT = 5,         /* a device-side poll gave up (see status) */
+    RRA_ERR_POISONED = 6,        /* an earlier device error; call rra_comm_reset */
+    RRA_ERR_EPOCH = 7            /* epoch counter near wrap; call rra_comm_reset */
+} rra_status_t;
+
+typedef enum { RRA_FP32 = 0, RRA_BF16 = 1, RRA_FP64 = 2 } rra_dtype_t;
+
+typedef enum {
+    RRA_ONESHOT_LL = 0,        /* Sec. IV "LL": data and epoch flag share one atomic word */
+    RRA_ONESHOT_SENTINEL = 1,  /* Sec. IV "Sentinel": scratch pre-filled with -NaN, polled */
+    RRA_TWOSHOT_DBUF = 2,      /* Sec. III-A two-shot + Sec. IV double buffering, Fig. 4 */
+    RRA_LL128_ATOMIC = 3       /* Fig. 5: atomic adds into the owner's lines, counter == N-1 */
+} rra_algo_t;
+
+/* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
+typedef enum {
+    RRA_ATTR_CTAS_PER_RANK = 0,    /* 0 = chosen per call from the message size */
+    RRA_ATTR_POLL_TIMEOUT_MS = 1,  /* limit of every device-side wait (default 1000) */
+    RRA_ATTR_THREADS = 2,          /* threads per CTA: 128, 256, 512 or 1024 (default 512) */
+    RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step, 0 = largest that fits */
+    RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step, 0 = largest */
+    RRA_ATTR_ONESHOT_CHUNK = 5     /* bytes per rank per one-shot step, 0 = largest */
+} rra_attr_t;
+
+/* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
+ * The per-algorithm caps default to the paper's scratch sizes (Sec. VII,
+ * Fig. 12): 4 MiB for one-shot, 64 MiB for two-shot and LL128-atomic. */
+typedef struct {
+    int nranks;
+    size_t max_bytes;
+    size_t ll_chunk;        /* one-shot LL payload bytes per rank per step */
+    size_t ll_bytes;        /* LL region: 2 parities x N slots x 2*ll_chunk */
+    size_t os_chunk;        /* one-shot sentinel payload bytes per rank per step */
+    size_t os_bytes;        /* sentinel region: 2 x N x os_chunk */
+    size_t ts_part;         /* two-shot partition bytes per owner per step */
+    size_t ts_bytes;        /* RS + AG regions: 2 x (2 x N x ts_part) */
+    size_t la_part;         /* LL128-atomic partition payload bytes per owner per step */
+    size_t la_bytes;        /* accumulators + counters + LL-encoded AllGather slots */
+    size_t window_stride;   /* bytes between consecutive windows */
+    size_t ctrl_bytes;      /* control block before window 0 */
+    size_t total_bytes;     /* ctrl_bytes + nranks * window_stride */
+} rra_layout_t;
+
+/*
+ * rra_comm_create: allocate the symmetric windows and initialise them.
+ *   nranks     number of virtual ranks, 2 <= nranks <= RRA_MAX_RANKS.
+ *   max_bytes  largest message (count * element size) a call may pass, > 0.
+ *   out        receives the communicator; unchanged on error.
+ * Uses the current CUDA device.  Allocates once (cudaMalloc of
+ * layout.total_bytes); fills sentinel regions with all-one bytes, LL flags,
+ * accumulators and counters with zero, sets the epoch to 1 and synchronises.
+ * Environment overrides read here: RRA_POLL_TIMEOUT_MS, RRA_CTAS_PER_RANK,
+ * RRA_THREADS, RRA_SCRATCH_ONESHOT, RRA_SCRATCH_TWOSHOT (bytes).
+ * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_OOM, RRA_ERR_CUDA,
+ * RRA_ERR_NOT_CORESIDENT (fewer than nranks CTAs fit on the GPU at once).
+ */
+rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out);
+
+/*
+ * rra_allreduce: enqueue one AllReduce-sum on `stream` (Sec. III-A).
+ *   send[r]  device pointer to rank r's `count` input elements (r < nranks).
+ *   recv[r]  device pointer to rank r's `count` output elements.
+ *            send and recv are host arrays of nranks device pointers; they are
+ *            copied into the kernel's parameters, so they may be freed on
+ *            return.  Every pointer must be 16-byte aligned.  recv[r] may equal
+ *            send[r] (in place); buffers of different ranks must not overlap.
+ *   count    elements per rank; count == 0 returns RRA_OK without a launch;
+ *            count * element size must not exceed max_bytes.
+ *   dtype    element type; algo: one of rra_algo_t.
+ *   stream   CUDA stream (NULL = legacy default stream).
+ * The caller owns all buffers and must keep them alive until the work on
+ * `stream` completes.  RRA_ONESHOT_SENTINEL and RRA_TWOSHOT_DBUF require
+ * that no input element has the all-ones bit pattern (the sentinel, a
+ * negative NaN, Sec. IV "Sentinel"); such an input makes the call time out.
+ * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_POISONED, RRA_ERR_CUDA.
+ */
+rra_status_t rra_allreduce(rra_comm_t comm, const void* const send[], void* const recv[],
+                           size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                           rra_stream_t stream);
+
+/*
+ * rra_allreduce_host: the same operation on HOST buffers, end to end.
+ * send[r]/recv[r] are host pointers (pinned memory gives the fastest copies).
+ * The call copies every send[r] to device staging buffers owned by the
+ * communicator (allocated on the first call: 2 * nranks * max_bytes), runs
+ * rra_allreduce on `stream`, copies every recv[r] back and synchronises
+ * `stream` before returning.  One cudaMemcpyAsync per rank and direction.
+ * Errors: as rra_allreduce, plus RRA_ERR_OOM for the staging buffers, plus
+ * any device-side error of this call (the status word is read after the
+ * synchronisation).
+ */
+rra_status_t rra_allreduce_host(rra_comm_t comm, const void* const send[], void* const recv[],
+                                size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                                rra_stream_t stream);
+
+/* Synchronise the device and return the device status word: RRA_OK, or the
+ * first device-side error (e.g. RRA_ERR_TIMEOUT).  A device error poisons the
+ * communicator until rra_comm_reset().  If `rank`/`step` are non-NULL they
+ * receive the virtual rank and step that recorded the error (-1 if none). */
+rra_status_t rra_comm_status(rra_comm_t comm, int* rank, int* step);
+
+/* Synchronise the device, re-initialise every window (sentinels, flags,
+ * accumulators, counters), the epoch and the status word, and clear the
+ * poison and any injected fault. */
+rra_status_t rra_comm_reset(rra_comm_t comm);
+
+/* Synchronise the device and free everything the communicator owns. */
+rra_status_t rra_comm_destroy(rra_comm_t comm);
+
+/* Attributes: see rra_attr_t.  Invalid values return RRA_ERR_INVALID_ARG. */
+rra_status_t rra_comm_set_attr(rra_comm_t comm, rra_attr_t attr, int64_t value);
+rra_status_t rra_comm_get_attr(rra_comm_t comm, rra_attr_t attr, int64_t* value);
+
+/* The window layout of an existing communicator. */
+rra_status_t rra_comm_layout(rra_comm_t comm, rra_layout_t* out);
+
+/* Plan a layout without a GPU (pure host arithmetic).  scratch_oneshot and
+ * scratch_twoshot are the per-window caps in bytes (0 = the paper's 4 MiB /
+ * 64 MiB).  Errors: RRA_ERR_INVALID_ARG. */
+rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_oneshot,
+                             size_t scratch_twoshot, rra_layout_t* out);
+
+/* Number of CTAs the next call of (count, dtype, algo) would launch, and the
+ * number of chunk steps it would take; pure host arithmetic. */
+rra_status_t rra_comm_plan_call(rra_comm_t comm, size_t count, rra_dtype_t dtype,
+                                rra_algo_t algo, int* grid_ctas, int* steps);
+
+/* Largest number of CTAs of (dtype, algo) that can be resident at once. */
+rra_status_t rra_comm_max_coresident(rra_comm_t comm, rra_dtype_t dtype, rra_algo_t algo,
+                                     int* ctas);
+
+/* Optional in-kernel timing.  `dev_buf` is a device buffer of at least
+ * 2 * (largest grid) uint64_t; while set, every CTA of every call writes its
+ * %globaltimer start and end (ns) at dev_buf[2*cta] and dev_buf[2*cta+1].
+ * NULL switches timing off.  The caller owns the buffer. */
+rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
+
+/* Fault injection for tests (host-side injection only; no GPU fault): while
+ * set, virtual rank `rank` skips every store to its peers, so the peers'
+ * polls run into their time limit and record RRA_ERR_TIMEOUT.  rank = -1
+ * clears it; rra_comm_reset also clears it.  Synchronises the device. */
+rra_status_t rra_comm_inject_drop(rra_comm_t comm, int rank);
+
+/* Text for a status code (static storage). */
+const char* rra_status_string(rra_status_t status);
+
+/* Library version, e.g. "0.1.0". */
+const char* rra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RRA_H */

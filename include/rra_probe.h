@@ -1,0 +1,58 @@
+/*
+ * rra_probe.h -- single-GPU latency-floor probes (C ABI).
+ *
+ * "Every Microsecond Matters", Sec. VI, models the speed-of-light latency of
+ * a small push AllReduce as L_SoL = 2 * L_L2_RTT + L_remote_store: one L2
+ * round trip to load the input, one store into the peer's scratch, one L2
+ * round trip to read it back (the output store is not waited on).  On one GPU
+ * the "remote" store is a store from one SM that another SM observes through
+ * L2.  These probes measure both terms on the GPU they run on:
+ *
+ *  - L_L2_RTT by a dependent pointer chase through an L2-resident buffer that
+ *    is larger than L1 (not by a memory fence, whose latency includes draining
+ *    the memory pipeline);
+ *  - L_store->poll as half the round trip of a fence-free ping-pong between
+ *    two CTAs that sit on different SMs.
+ *
+ * All waits are bounded by a time limit; a probe that gives up returns
+ * RRA_ERR_TIMEOUT instead of hanging.
+ */
+#ifndef RRA_PROBE_H
+#define RRA_PROBE_H
+
+#include "rra.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Dependent-load chase over a random cycle of 8-byte words in a device
+ * buffer of `buf_bytes` (allocated and freed here; >= 64 KiB).  One warm pass
+ * brings the buffer into L2, then one thread follows `hops` pointers with
+ * L1-bypassing loads.  Output: mean ns per hop.  `seed` picks the cycle.
+ * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_OOM, RRA_ERR_CUDA. */
+rra_status_t rra_probe_l2_chase(size_t buf_bytes, uint64_t hops, uint64_t seed,
+                                double* ns_per_hop);
+
+/* Fence-free ping-pong between CTA `cta_a` and CTA `cta_b` of a grid that
+ * holds one CTA per SM (cooperative launch, so both are resident).  CTA a
+ * stores i to a flag; CTA b polls until it sees i and stores i to a second
+ * flag; CTA a polls that.  Output: mean ns per round trip over `iters`
+ * exchanges after `iters`/8 warm-up exchanges, and the SM ids the two CTAs ran
+ * on (they differ: one CTA per SM).  Errors: RRA_ERR_INVALID_ARG,
+ * RRA_ERR_TIMEOUT (a wait passed 1 s), RRA_ERR_CUDA. */
+rra_status_t rra_probe_pingpong(int cta_a, int cta_b, int iters,
+                                double* ns_round_trip, int* sm_a, int* sm_b);
+
+/* Launch one empty kernel (1 CTA, 32 threads) on `stream`, to measure launch
+ * and graph-node overhead next to the AllReduce. */
+rra_status_t rra_probe_empty_kernel(rra_stream_t stream);
+
+/* Number of SMs of the current device. */
+rra_status_t rra_probe_sm_count(int* sms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RRA_PROBE_H */

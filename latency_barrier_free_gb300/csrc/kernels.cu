@@ -1,0 +1,698 @@
+// kernels.cu -- the four barrier-free AllReduce kernels and the window
+// initialiser.
+//
+// Source: "Every Microsecond Matters: Achieving Near Speed-of-Light Latency in
+// GPU Collectives" (arXiv 2607.16100): Sec. III-A (one-shot push and two-shot
+// AllReduce), Sec. IV (LL, sentinel, bidirectional double buffering, Fig. 4)
+// and Fig. 5 (two-shot LL128 atomic AllReduce).
+//
+// Execution model.  One cooperative launch of N * C CTAs; CTA b is sub-slice
+// c = b % C of virtual rank r = b / C.  Rank r reads only send[r] and its own
+// window, and writes only peers' windows and recv[r].  All scratch traffic is
+// 16-byte vectors.  No CTA ever waits at a grid-wide barrier: every wait is a
+// poll on data (LL flag, sentinel, or LL128 line counter), bounded in time.
+//
+// Credit (double buffering, Sec. IV).  Step k of a call uses scratch parity
+// (epoch + k) & 1, so a slot is reused two steps later.  The position -> thread
+// map is the same in every step of a call, so the thread that fills slot
+// position v of peer p at step k+2 is the thread that, at step k+1, received
+// p's data for position v -- which p's corresponding thread sent only after it
+// had consumed (and, for sentinels, reset) position v of step k.  A
+// fence.acq_rel.gpu at the start of every step (when a call has >= 3 steps)
+// turns that chain into release/acquire pairs.  Between calls, the kernel
+// boundary orders everything.
+//
+// Summation order.  One-shot and two-shot add the N contributions of an
+// element in rank order 0..N-1 (binary32 running value for binary32 and
+// bfloat16, binary64 for binary64): the result is deterministic and equals the
+// fixed-order definition bit for bit.  LL128-atomic adds with L2 atomics in
+// arrival order (the paper notes the non-determinism).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "prims.cuh"
+#include "rra_internal.h"
+
+namespace rra {
+
+// ------------------------------------------------------------ helpers ----
+__device__ __forceinline__ char* window(const Params& p, int r) {
+    return p.win0 + (uint64_t)r * p.stride;
+}
+
+// Input vector `vec` of a rank's buffer; elements at or beyond `count` read
+// as zero (never the sentinel).
+template <typename T>
+__device__ __forceinline__ uint4 load_input(const void* base, uint64_t vec, uint64_t count) {
+    constexpr int VE = VecMath<T>::kElems;
+    const uint64_t e0 = vec * VE;
+    if (e0 + VE <= count) return ld_input_v4((const char*)base + vec * kVecBytes);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    const int n = (int)(count - e0);
+    if (sizeof(T) == 2) {
+        const uint16_t* s = (const uint16_t*)base + e0;
+        for (int i = 0; i < n; ++i) w[i >> 1] |= (uint32_t)s[i] << (16 * (i & 1));
+    } else if (sizeof(T) == 4) {
+        const uint32_t* s = (const uint32_t*)base + e0;
+        for (int i = 0; i < n; ++i) w[i] = s[i];
+    } else {
+        const uint32_t* s = (const uint32_t*)base + 2 * e0;
+        for (int i = 0; i < 2 * n; ++i) w[i] = s[i];
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Output vector `vec`; only elements below `count` are written.
+template <typename T>
+__device__ __forceinline__ void store_output(void* base, uint64_t vec, uint64_t count, uint4 v) {
+    constexpr int VE = VecMath<T>::kElems;
+    const uint64_t e0 = vec * VE;
+    if (e0 + VE <= count) {
+        st_output_v4((char*)base + vec * kVecBytes, v);
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int n = (int)(count - e0);
+    if (sizeof(T) == 2) {
+        uint16_t* d = (uint16_t*)base + e0;
+        for (int i = 0; i < n; ++i) d[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
+    } else if (sizeof(T) == 4) {
+        uint32_t* d = (uint32_t*)base + e0;
+        for (int i = 0; i < n; ++i) d[i] = w[i];
+    } else {
+        uint32_t* d = (uint32_t*)base + 2 * e0;
+        for (int i = 0; i < 2 * n; ++i) d[i] = w[i];
+    }
+}
+
+// Per-CTA prologue/epilogue shared by all kernels.
+struct CtaState {
+    uint64_t epoch;  // epoch of step 0 of this call
+    uint64_t t_start;
+    int rank, sub;
+    bool skip;       // earlier device error, or epoch wrap: do nothing
+    bool drop;       // injected fault: do not store to peers
+};
+
+__device__ __forceinline__ CtaState cta_prologue(const Params& p) {
+    __shared__ uint64_t s_epoch;
+    __shared__ int s_flags;
+    CtaState s;
+    s.t_start = globaltimer_ns();
+    s.rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
+    s.sub = (int)(blockIdx.x % (unsigned)p.ctas_per_rank);
+    if (threadIdx.x == 0) {
+        if (p.timing != nullptr) p.timing[2 * blockIdx.x] = s.t_start;
+        const uint64_t e = *(volatile const uint64_t*)&p.ctrl->epoch[blockIdx.x];
+        int flags = 0;
+        if (ld_relaxed_u32(&p.ctrl->status) != 0u) flags |= 1;
+        // 32-bit LL flags must not wrap inside the live window of epochs.
+        if ((e & 0xFFFFFFFFull) + (uint64_t)p.nsteps + 2ull > 0xFFFFFFFFull) {
+            record_error(p.ctrl, RRA_ERR_EPOCH, s.rank, 0);
+            flags |= 1;
+        }
+        if (*(volatile const int32_t*)&p.ctrl->drop_rank == s.rank) flags |= 2;
+        s_epoch = e;
+        s_flags = flags;
+    }
+    __syncthreads();
+    s.epoch = s_epoch;
+    s.skip = (s_flags & 1) != 0;
+    s.drop = (s_flags & 2) != 0;
+    return s;
+}
+
+__device__ __forceinline__ void cta_epilogue(const Params& p, const CtaState& s) {
+    if (!s.skip) {
+        // Advance every epoch slot this CTA owns: slots b, b + G, b + 2G, ...
+        const uint64_t next = s.epoch + p.nsteps;
+        const unsigned G = gridDim.x;
+        for (unsigned slot = blockIdx.x + threadIdx.x * G; slot < (unsigned)p.epoch_slots;
+             slot += blockDim.x * G) {
+            *(volatile uint64_t*)&p.ctrl->epoch[slot] = next;
+        }
+    }
+    if (p.timing != nullptr) {
+        __syncthreads();
+        if (threadIdx.x == 0) p.timing[2 * blockIdx.x + 1] = globaltimer_ns();
+    }
+}
+
+constexpr int kBatch = 8;  // sources polled with loads in flight at once
+
+// Poll one scratch vector once.  LL: both LL lines carry `ep` in all four
+// flags.  Sentinel: no atomic unit still holds the sentinel.
+template <typename T, bool kLL>
+__device__ __forceinline__ bool poll_once(const char* slot_pos, uint32_t ep, uint4& out) {
+    if (kLL) return ll_load(slot_pos, ep, out);
+    out = ld_scratch<VecMath<T>::kUnitBytes>(slot_pos);
+    return sentinel_arrived<VecMath<T>::kUnitBytes>(out);
+}
+
+// ---------------------------------------------------- one-shot (push) ----
+// Sec. III-A "One-shot" in push mode + Sec. IV "LL" / "Sentinel"; the
+// bcast() of Fig. 9: each rank stores its chunk into every peer's slot, then
+// polls its own window for the N-1 incoming slots and reduces.
+template <typename T, bool kLL>
+__device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s) {
+    using M = VecMath<T>;
+    constexpr int U = M::kUnitBytes;
+    constexpr uint64_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
+    const int N = p.nranks, r = s.rank;
+    const uint64_t pos0 = (uint64_t)s.sub * p.per_cta;
+    const uint64_t pos1 = pos0 + p.per_cta;
+    char* const mine = window(p, r) + p.region_off;
+    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint32_t ep = (uint32_t)e;
+        const uint64_t par_off = (e & 1ull) * p.parity_bytes;
+        const uint64_t base = (uint64_t)k * p.chunk_vecs;
+        const uint64_t nv = min(p.chunk_vecs, p.nvec - base);
+        const uint64_t end = min(pos1, nv);
+        w.step = (int)k;
+        if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
+
+        // push: my chunk into slot [parity][r] of every peer
+        if (!s.drop) {
+            for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+                const uint4 x = load_input<T>(p.send[r], base + v, p.count);
+                const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + v * kPosBytes;
+                for (int q = 0; q < N; ++q) {
+                    if (q == r) continue;
+                    char* dst = window(p, q) + off;
+                    if (kLL) ll_store(dst, x, ep);
+                    else st_scratch<U>(dst, x);
+                }
+            }
+        }
+        // receive: poll the N-1 incoming slots, reduce in rank order
+        for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+            const uint4 own = load_input<T>(p.send[r], base + v, p.count);
+            const char* const slot0 = mine + par_off + v * kPosBytes;
+            typename M::Acc acc;
+            for (int q0 = 0; q0 < N; q0 += kBatch) {
+                uint4 val[kBatch];
+                bool ok[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    ok[j] = true;
+                    if (q < N && q != r) ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * p.slot_bytes, ep, val[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    while (!ok[j]) {
+                        if (waiter_expired(w)) return false;
+                        ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * p.slot_bytes, ep, val[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q >= N) break;
+                    const uint4 x = (q == r) ? own : val[j];
+                    if (q == 0) acc = M::load(x);
+                    else M::add(acc, x);
+                }
+                if (!kLL) {
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j) {
+                        const int q = q0 + j;
+                        if (q < N && q != r)
+                            st_scratch<U>((char*)slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    }
+                }
+            }
+            store_output<T>(p.recv[r], base + v, p.count, M::store(acc));
+        }
+    }
+    return true;
+}
+
+template <typename T, bool kLL>
+__global__ void __launch_bounds__(512) oneshot_kernel(const __grid_constant__ Params p) {
+    const CtaState s = cta_prologue(p);
+    if (!s.skip) (void)oneshot_body<T, kLL>(p, s);
+    cta_epilogue(p, s);
+}
+
+// ------------------------------------------ two-shot, double buffered ----
+// Sec. III-A "Two-shot" (ReduceScatter then AllGather, both push) with
+// sentinel synchronisation and the bidirectional double buffering of Sec. IV /
+// Fig. 4.  Step k covers N partitions of `part` vectors; rank q owns
+// partition q.  RS: every rank stores its part q into owner q's RS slot
+// [parity][r].  Owner: polls the N-1 RS slots, reduces in rank order, stores
+// the result into every peer's AG slot [parity][owner] and its own output.
+// AG: every rank polls the N-1 AG slots and writes its output.
+struct Split {
+    uint64_t base;  // first vector of the step
+    uint64_t part;  // vectors per partition in this step
+    uint64_t rem;   // vectors left from `base` to the end of the message
+    __device__ __forceinline__ uint64_t valid(int q) const {  // vectors of partition q
+        const uint64_t lo = (uint64_t)q * part;
+        return rem > lo ? min(part, rem - lo) : 0ull;
+    }
+    __device__ __forceinline__ uint64_t vec(int q, uint64_t v) const {
+        return base + (uint64_t)q * part + v;
+    }
+};
+
+// The last step shrinks its partitions so the remaining vectors spread over
+// all owners; positions stay a prefix of the full-step positions.
+__device__ __forceinline__ Split split_step(const Params& p, uint32_t k) {
+    Split sp;
+    const uint64_t full = (uint64_t)p.nranks * p.chunk_vecs;
+    sp.base = (uint64_t)k * full;
+    sp.rem = p.nvec - sp.base;
+    sp.part = sp.rem >= full ? p.chunk_vecs : (sp.rem + p.nranks - 1) / p.nranks;
+    return sp;
+}
+
+template <typename T>
+__device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s) {
+    using M = VecMath<T>;
+    constexpr int U = M::kUnitBytes;
+    const int N = p.nranks, r = s.rank;
+    const uint64_t pos0 = (uint64_t)s.sub * p.per_cta;
+    const uint64_t pos1 = pos0 + p.per_cta;
+    char* const mine = window(p, r);
+    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint64_t par_off = (e & 1ull) * p.parity_bytes;
+        const Split sp = split_step(p, k);
+        const uint64_t end = min(pos1, sp.part);
+        w.step = (int)k;
+        if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
+
+        // ReduceScatter push: part q of my input -> owner q's RS slot [r]
+        if (!s.drop) {
+            for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+                const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + v * kVecBytes;
+                for (int q = 0; q < N; ++q) {
+                    if (q == r || v >= sp.valid(q)) continue;
+                    const uint4 x = load_input<T>(p.send[r], sp.vec(q, v), p.count);
+                    st_scratch<U>(window(p, q) + off, x);
+                }
+            }
+        }
+        // Owner: reduce my partition in rank order, push it to every AG slot
+        const uint64_t my_valid = sp.valid(r);
+        for (uint64_t v = pos0 + threadIdx.x; v < end && v < my_valid; v += blockDim.x) {
+            const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
+            const char* const slot0 = mine + p.region_off + par_off + v * kVecBytes;
+            typename M::Acc acc;
+            for (int q0 = 0; q0 < N; q0 += kBatch) {
+                uint4 val[kBatch];
+                bool ok[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    ok[j] = true;
+                    if (q < N && q != r) {
+                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
+                        ok[j] = sentinel_arrived<U>(val[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    while (!ok[j]) {
+                        if (waiter_expired(w)) return false;
+                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
+                        ok[j] = sentinel_arrived<U>(val[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q >= N) break;
+                    const uint4 x = (q == r) ? own : val[j];
+                    if (q == 0) acc = M::load(x);
+                    else M::add(acc, x);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q < N && q != r)
+                        st_scratch<U>((char*)slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                }
+            }
+            const uint4 red = M::store(acc);
+            if (!s.drop) {
+                const uint64_t off = p.aux_off + par_off + (uint64_t)r * p.slot_bytes + v * kVecBytes;
+                for (int q = 0; q < N; ++q) {
+                    if (q == r) continue;
+                    st_scratch<U>(window(p, q) + off, red);
+                }
+            }
+            store_output<T>(p.recv[r], sp.vec(r, v), p.count, red);
+        }
+        // AllGather receive: the N-1 reduced partitions of the other owners
+        for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+            const char* const slot0 = mine + p.aux_off + par_off + v * kVecBytes;
+            for (int q0 = 0; q0 < N; q0 += kBatch) {
+                uint4 val[kBatch];
+                bool ok[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    ok[j] = true;
+                    if (q < N && q != r && v < sp.valid(q)) {
+                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
+                        ok[j] = sentinel_arrived<U>(val[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    while (!ok[j]) {
+                        if (waiter_expired(w)) return false;
+                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
+                        ok[j] = sentinel_arrived<U>(val[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q < N && q != r && v < sp.valid(q)) {
+                        store_output<T>(p.recv[r], sp.vec(q, v), p.count, val[j]);
+                        st_scratch<U>((char*)slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    }
+                }
+            }
+        }
+    }
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) twoshot_kernel(const __grid_constant__ Params p) {
+    const CtaState s = cta_prologue(p);
+    if (!s.skip) (void)twoshot_body<T>(p, s);
+    cta_epilogue(p, s);
+}
+
+// ------------------------------------------------ two-shot LL128 atomic ----
+// Fig. 5: the ReduceScatter adds straight into the owner's destination lines
+// with atomic additions and raises a per-line counter; the owner consumes a
+// line when its counter shows every contribution (here: the N-1 peers, the
+// owner adds its own part in registers), re-zeroes line and counter for the
+// next use of the parity, and the AllGather pushes the result with epoch
+// flags (LL encoding) to every peer.
+//
+// Single-GPU reading of the line atomicity the paper takes from NVLink: L2
+// atomics are per element, so a contributor warp first issues all its
+// red.add operations for a group of 32 vectors, synchronises the warp, and
+// every lane issues fence.acq_rel.gpu before the counter increments (release);
+// the owner reads the counter, then fences (acquire) before reading the lines.
+template <typename T>
+struct Acc128;
+template <>
+struct Acc128<float> {          // binary32 -> binary32 accumulators
+    static constexpr int kRatio = 1;
+    __device__ __forceinline__ static void red(char* dst, uint4 x) {
+        red_add_v4f32(dst, __uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                      __uint_as_float(x.w));
+    }
+    __device__ __forceinline__ static uint4 finish(const char* src, uint4 own) {
+        const uint4 a = ld_relaxed_v4(src);
+        return make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(a.x), __uint_as_float(own.x))),
+                          __float_as_uint(__fadd_rn(__uint_as_float(a.y), __uint_as_float(own.y))),
+                          __float_as_uint(__fadd_rn(__uint_as_float(a.z), __uint_as_float(own.z))),
+                          __float_as_uint(__fadd_rn(__uint_as_float(a.w), __uint_as_float(own.w))));
+    }
+    __device__ __forceinline__ static void zero(char* src) { st_relaxed_v4(src, make_uint4(0, 0, 0, 0)); }
+};
+template <>
+struct Acc128<__nv_bfloat16> {  // bfloat16 -> binary32 accumulators (2 x 16 B per vector)
+    static constexpr int kRatio = 2;
+    using VM = VecMath<__nv_bfloat16>;
+    __device__ __forceinline__ static void red(char* dst, uint4 x) {
+        red_add_v4f32(dst, VM::lo(x.x), VM::hi(x.x), VM::lo(x.y), VM::hi(x.y));
+        red_add_v4f32(dst + 16, VM::lo(x.z), VM::hi(x.z), VM::lo(x.w), VM::hi(x.w));
+    }
+    __device__ __forceinline__ static uint4 finish(const char* src, uint4 own) {
+        const uint4 a = ld_relaxed_v4(src);
+        const uint4 b = ld_relaxed_v4(src + 16);
+        const float f0 = __fadd_rn(__uint_as_float(a.x), VM::lo(own.x));
+        const float f1 = __fadd_rn(__uint_as_float(a.y), VM::hi(own.x));
+        const float f2 = __fadd_rn(__uint_as_float(a.z), VM::lo(own.y));
+        const float f3 = __fadd_rn(__uint_as_float(a.w), VM::hi(own.y));
+        const float f4 = __fadd_rn(__uint_as_float(b.x), VM::lo(own.z));
+        const float f5 = __fadd_rn(__uint_as_float(b.y), VM::hi(own.z));
+        const float f6 = __fadd_rn(__uint_as_float(b.z), VM::lo(own.w));
+        const float f7 = __fadd_rn(__uint_as_float(b.w), VM::hi(own.w));
+        return make_uint4(VM::pack(f0, f1), VM::pack(f2, f3), VM::pack(f4, f5), VM::pack(f6, f7));
+    }
+    __device__ __forceinline__ static void zero(char* src) {
+        st_relaxed_v4(src, make_uint4(0, 0, 0, 0));
+        st_relaxed_v4(src + 16, make_uint4(0, 0, 0, 0));
+    }
+};
+template <>
+struct Acc128<double> {         // binary64 -> binary64 accumulators
+    static constexpr int kRatio = 1;
+    using VM = VecMath<double>;
+    __device__ __forceinline__ static void red(char* dst, uint4 x) {
+        red_add_f64(dst, VM::d(x.x, x.y));
+        red_add_f64(dst + 8, VM::d(x.z, x.w));
+    }
+    __device__ __forceinline__ static uint4 finish(const char* src, uint4 own) {
+        uint64_t a, b;
+        ld_relaxed_v2u64(src, a, b);
+        const double d0 = __dadd_rn(__longlong_as_double((long long)a), VM::d(own.x, own.y));
+        const double d1 = __dadd_rn(__longlong_as_double((long long)b), VM::d(own.z, own.w));
+        return make_uint4((uint32_t)__double2loint(d0), (uint32_t)__double2hiint(d0),
+                          (uint32_t)__double2loint(d1), (uint32_t)__double2hiint(d1));
+    }
+    __device__ __forceinline__ static void zero(char* src) { st_relaxed_v2u64(src, 0ull, 0ull); }
+};
+
+template <typename T>
+__device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
+    using A = Acc128<T>;
+    constexpr uint64_t kAccBytes = (uint64_t)kVecBytes * A::kRatio;
+    const int N = p.nranks, r = s.rank;
+    const unsigned lane = threadIdx.x & 31u;
+    const uint64_t pos0 = (uint64_t)s.sub * p.per_cta;   // per_cta is a multiple of 32
+    const uint64_t pos1 = pos0 + p.per_cta;
+    char* const mine = window(p, r);
+    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+    const uint32_t target = (uint32_t)(N - 1);
+
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint32_t ep = (uint32_t)e;
+        const uint64_t par = e & 1ull;
+        const Split sp = split_step(p, k);
+        const uint64_t end = min(pos1, sp.part);
+        w.step = (int)k;
+        if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
+
+        // ReduceScatter: atomic adds into each owner's accumulators.  The loop
+        // bound is warp-uniform (v - lane is the group start).
+        if (!s.drop) {
+            for (uint64_t v = pos0 + threadIdx.x; v - lane < end; v += blockDim.x) {
+                for (int q = 0; q < N; ++q) {
+                    if (q == r || v >= sp.valid(q)) continue;
+                    const uint4 x = load_input<T>(p.send[r], sp.vec(q, v), p.count);
+                    A::red(window(p, q) + p.region_off + par * p.parity_bytes + v * kAccBytes, x);
+                }
+            }
+            __syncwarp();
+            fence_acq_rel_gpu();  // release: this warp's adds before its counter increments
+            for (uint64_t g0 = pos0 + (threadIdx.x - lane); g0 < end; g0 += blockDim.x) {
+                const uint64_t g = g0 / kGroupVecs;
+                for (int q = (int)lane; q < N; q += 32) {
+                    if (q == r || g0 >= sp.valid(q)) continue;
+                    red_add_u32(window(p, q) + p.aux_off + par * p.aux_parity_bytes + g * 4, 1u);
+                }
+            }
+        }
+        // Owner: wait for each group's counter, consume, re-zero, AllGather push.
+        const uint64_t my_valid = sp.valid(r);
+        for (uint64_t g0 = pos0 + (threadIdx.x - lane); g0 < end && g0 < my_valid; g0 += blockDim.x) {
+            const uint64_t g = g0 / kGroupVecs;
+            char* const cnt = mine + p.aux_off + par * p.aux_parity_bytes + g * 4;
+            int give_up = 0;
+            if (lane == 0) {
+                while (ld_relaxed_u32(cnt) != target) {
+                    if (waiter_expired(w)) { give_up = 1; break; }
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, give_up, 0)) return false;
+            fence_acq_rel_gpu();  // acquire: counter before the lines
+            const uint64_t v = g0 + lane;
+            if (v < my_valid) {
+                char* const acc = mine + p.region_off + par * p.parity_bytes + v * kAccBytes;
+                const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
+                const uint4 red = A::finish(acc, own);
+                A::zero(acc);
+                if (!s.drop) {
+                    const uint64_t off = p.aux2_off + par * p.aux2_parity_bytes + (uint64_t)r * p.aux2_slot_bytes +
+                                         v * 2 * kVecBytes;
+                    for (int q = 0; q < N; ++q) {
+                        if (q == r) continue;
+                        ll_store(window(p, q) + off, red, ep);
+                    }
+                }
+                store_output<T>(p.recv[r], sp.vec(r, v), p.count, red);
+            }
+            __syncwarp();
+            if (lane == 0) st_relaxed_u32(cnt, 0u);
+        }
+        // AllGather receive (LL polls), per lane; the warp leaves together.
+        int failed = 0;
+        for (uint64_t v = pos0 + threadIdx.x; v - lane < end; v += blockDim.x) {
+            if (failed || v >= end) continue;
+            const char* const slot0 = mine + p.aux2_off + par * p.aux2_parity_bytes + v * 2 * kVecBytes;
+            for (int q0 = 0; q0 < N && !failed; q0 += kBatch) {
+                uint4 val[kBatch];
+                bool ok[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    ok[j] = true;
+                    if (q < N && q != r && v < sp.valid(q))
+                        ok[j] = ll_load(slot0 + (uint64_t)q * p.aux2_slot_bytes, ep, val[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    while (!ok[j] && !failed) {
+                        if (waiter_expired(w)) { failed = 1; break; }
+                        ok[j] = ll_load(slot0 + (uint64_t)q * p.aux2_slot_bytes, ep, val[j]);
+                    }
+                }
+                if (failed) break;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q < N && q != r && v < sp.valid(q))
+                        store_output<T>(p.recv[r], sp.vec(q, v), p.count, val[j]);
+                }
+            }
+        }
+        if (__any_sync(0xFFFFFFFFu, failed)) return false;
+    }
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) ll128_kernel(const __grid_constant__ Params p) {
+    const CtaState s = cta_prologue(p);
+    if (!s.skip) (void)ll128_body<T>(p, s);
+    cta_epilogue(p, s);
+}
+
+// ---------------------------------------------------------- initialiser ----
+// Fills every window region with its idle pattern (sentinel regions all-ones,
+// LL flags / accumulators / counters zero) and resets the control block.
+struct FillJob {
+    uint64_t off;    // offset inside a window
+    uint64_t bytes;  // multiple of 16
+    uint32_t value;  // 32-bit fill pattern
+};
+struct InitParams {
+    char* win0;
+    Ctrl* ctrl;
+    uint64_t stride;
+    int nranks;
+    int njobs;
+    FillJob job[6];
+};
+
+__global__ void init_kernel(const __grid_constant__ InitParams ip) {
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) {
+            ip.ctrl->status = 0u;
+            ip.ctrl->err_rank = -1;
+            ip.ctrl->err_step = -1;
+            ip.ctrl->drop_rank = -1;
+        }
+        for (int i = threadIdx.x; i < kEpochSlots; i += blockDim.x) ip.ctrl->epoch[i] = 1ull;
+    }
+    for (int r = 0; r < ip.nranks; ++r) {
+        for (int j = 0; j < ip.njobs; ++j) {
+            const FillJob& f = ip.job[j];
+            const uint4 v = make_uint4(f.value, f.value, f.value, f.value);
+            uint4* dst = (uint4*)(ip.win0 + (uint64_t)r * ip.stride + f.off);
+            for (uint64_t i = tid; i < f.bytes / 16; i += nthreads) dst[i] = v;
+        }
+    }
+}
+
+// --------------------------------------------------------- host launch ----
+template <typename T>
+static const void* kernel_for(rra_algo_t algo) {
+    switch (algo) {
+        case RRA_ONESHOT_LL: return (const void*)oneshot_kernel<T, true>;
+        case RRA_ONESHOT_SENTINEL: return (const void*)oneshot_kernel<T, false>;
+        case RRA_TWOSHOT_DBUF: return (const void*)twoshot_kernel<T>;
+        case RRA_LL128_ATOMIC: return (const void*)ll128_kernel<T>;
+    }
+    return nullptr;
+}
+
+static const void* kernel_for(rra_dtype_t dtype, rra_algo_t algo) {
+    switch (dtype) {
+        case RRA_FP32: return kernel_for<float>(algo);
+        case RRA_BF16: return kernel_for<__nv_bfloat16>(algo);
+        case RRA_FP64: return kernel_for<double>(algo);
+    }
+    return nullptr;
+}
+
+cudaError_t occupancy(rra_dtype_t dtype, rra_algo_t algo, int threads, int* blocks_per_sm) {
+    const void* k = kernel_for(dtype, algo);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, threads, 0);
+}
+
+cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, rra_algo_t algo, int threads,
+                             cudaStream_t stream) {
+    const void* k = kernel_for(dtype, algo);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.nranks * p.ctas_per_rank));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {(void*)&p};
+    return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
+                        cudaStream_t stream) {
+    (void)total;
+    InitParams ip = {};
+    ip.ctrl = (Ctrl*)base;
+    ip.win0 = base + lay.ctrl_bytes;
+    ip.stride = lay.window_stride;
+    ip.nranks = nranks;
+    uint64_t off = 0;
+    int j = 0;
+    // Region order inside a window: LL, sentinel one-shot, two-shot (RS+AG),
+    // LL128 (accumulators + counters + LL AllGather).  Must match the planner.
+    ip.job[j++] = FillJob{off, lay.ll_bytes, 0u};           off += lay.ll_bytes;
+    ip.job[j++] = FillJob{off, lay.os_bytes, 0xFFFFFFFFu};  off += lay.os_bytes;
+    ip.job[j++] = FillJob{off, lay.ts_bytes, 0xFFFFFFFFu};  off += lay.ts_bytes;
+    ip.job[j++] = FillJob{off, lay.la_bytes, 0u};           off += lay.la_bytes;
+    ip.njobs = j;
+    init_kernel<<<1024, 256, 0, stream>>>(ip);
+    return cudaGetLastError();
+}
+
+}  // namespace rra

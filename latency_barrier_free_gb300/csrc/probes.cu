@@ -1,0 +1,183 @@
+// probes.cu -- single-GPU latency-floor probes (include/rra_probe.h).
+//
+// "Every Microsecond Matters", Sec. VI: L_SoL = 2 * L_L2_RTT + L_remote_store.
+// L_L2_RTT is measured here as the per-hop time of a dependent pointer chase
+// through an L2-resident buffer (the review of the paper points out that a
+// fence's latency is not a load-to-use time); L_remote_store as half the
+// round trip of a fence-free store/poll ping-pong between two SMs.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <numeric>
+#include <random>
+#include <vector>
+
+#include "rra.h"
+#include "rra_probe.h"
+
+namespace {
+
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint64_t ld_cg_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+// out[0] = elapsed ns of the timed pass, out[1] = final index (keeps the chain live)
+__global__ void chase_kernel(const uint64_t* next, uint64_t nwords, uint64_t hops, uint64_t* out) {
+    uint64_t i = 0;
+    for (uint64_t h = 0; h < nwords; ++h) i = ld_cg_u64(next + i);  // warm pass: whole cycle into L2
+    const uint64_t t0 = gtimer();
+    for (uint64_t h = 0; h < hops; ++h) i = ld_cg_u64(next + i);
+    const uint64_t t1 = gtimer();
+    out[0] = t1 - t0;
+    out[1] = i;
+}
+
+// flags[0]: a -> b, flags[32]: b -> a (separate 128-byte lines).
+// res[0] = round trips ns total, res[1] = smid a, res[2] = smid b, res[3] = error
+__global__ void pingpong_kernel(uint32_t* flags, int cta_a, int cta_b, int warm, int iters, uint64_t* res) {
+    if (threadIdx.x != 0) return;
+    const int me = (int)blockIdx.x;
+    if (me != cta_a && me != cta_b) return;
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const uint64_t deadline = gtimer() + 1000000000ull;  // 1 s
+    uint32_t* to_b = flags;
+    uint32_t* to_a = flags + 32;
+    const int total = warm + iters;
+    if (me == cta_a) {
+        res[1] = smid;
+        uint64_t t0 = 0;
+        for (int i = 1; i <= total; ++i) {
+            if (i == warm + 1) t0 = gtimer();
+            st_relaxed(to_b, (uint32_t)i);
+            uint32_t spins = 0;
+            while (ld_relaxed(to_a) != (uint32_t)i) {
+                if ((++spins & 255u) == 0u && gtimer() > deadline) { res[3] = 1; return; }
+            }
+        }
+        res[0] = gtimer() - t0;
+    } else {
+        res[2] = smid;
+        for (int i = 1; i <= total; ++i) {
+            uint32_t spins = 0;
+            while (ld_relaxed(to_b) != (uint32_t)i) {
+                if ((++spins & 255u) == 0u && gtimer() > deadline) { res[3] = 1; return; }
+            }
+            st_relaxed(to_a, (uint32_t)i);
+        }
+    }
+}
+
+__global__ void empty_kernel() {}
+
+}  // namespace
+
+extern "C" {
+
+rra_status_t rra_probe_sm_count(int* sms) {
+    if (sms == nullptr) return RRA_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RRA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return RRA_ERR_CUDA;
+    return RRA_OK;
+}
+
+rra_status_t rra_probe_l2_chase(size_t buf_bytes, uint64_t hops, uint64_t seed, double* ns_per_hop) {
+    if (ns_per_hop == nullptr || buf_bytes < (64u << 10) || hops == 0 || buf_bytes > (1ull << 31))
+        return RRA_ERR_INVALID_ARG;
+    const uint64_t n = buf_bytes / 8;
+    // One random cycle through all words: Sattolo's algorithm.
+    std::vector<uint64_t> perm(n);
+    std::iota(perm.begin(), perm.end(), 0ull);
+    std::mt19937_64 g(seed);
+    for (uint64_t i = n - 1; i > 0; --i) {
+        std::uniform_int_distribution<uint64_t> d(0, i - 1);
+        std::swap(perm[i], perm[d(g)]);
+    }
+    std::vector<uint64_t> next(n);
+    for (uint64_t i = 0; i < n; ++i) next[perm[i]] = perm[(i + 1) % n];
+    uint64_t* dnext = nullptr;
+    uint64_t* dout = nullptr;
+    if (cudaMalloc((void**)&dnext, n * 8) != cudaSuccess) { cudaGetLastError(); return RRA_ERR_OOM; }
+    if (cudaMalloc((void**)&dout, 16) != cudaSuccess) { cudaGetLastError(); cudaFree(dnext); return RRA_ERR_OOM; }
+    rra_status_t st = RRA_OK;
+    uint64_t out[2] = {0, 0};
+    if (cudaMemcpy(dnext, next.data(), n * 8, cudaMemcpyHostToDevice) != cudaSuccess) st = RRA_ERR_CUDA;
+    if (st == RRA_OK) {
+        chase_kernel<<<1, 1>>>(dnext, n, hops, dout);
+        if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+            cudaMemcpy(out, dout, 16, cudaMemcpyDeviceToHost) != cudaSuccess)
+            st = RRA_ERR_CUDA;
+    }
+    cudaFree(dnext);
+    cudaFree(dout);
+    if (st == RRA_OK) *ns_per_hop = (double)out[0] / (double)hops;
+    return st;
+}
+
+rra_status_t rra_probe_pingpong(int cta_a, int cta_b, int iters, double* ns_round_trip, int* sm_a, int* sm_b) {
+    if (ns_round_trip == nullptr || iters <= 0 || iters > (1 << 24) || cta_a == cta_b || cta_a < 0 || cta_b < 0)
+        return RRA_ERR_INVALID_ARG;
+    int dev = 0, sms = 0, smem_max = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cta_a >= sms || cta_b >= sms || !coop) return RRA_ERR_INVALID_ARG;
+    // One CTA per SM: each CTA asks for more than half of the SM's shared memory.
+    const int smem = smem_max;
+    if (cudaFuncSetAttribute(pingpong_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    uint32_t* flags = nullptr;
+    uint64_t* res = nullptr;
+    if (cudaMalloc((void**)&flags, 256) != cudaSuccess) { cudaGetLastError(); return RRA_ERR_OOM; }
+    if (cudaMalloc((void**)&res, 32) != cudaSuccess) { cudaGetLastError(); cudaFree(flags); return RRA_ERR_OOM; }
+    rra_status_t st = RRA_OK;
+    uint64_t h[4] = {0, 0, 0, 0};
+    if (cudaMemset(flags, 0, 256) != cudaSuccess || cudaMemset(res, 0, 32) != cudaSuccess) st = RRA_ERR_CUDA;
+    if (st == RRA_OK) {
+        int warm = std::max(1, iters / 8);
+        void* args[] = {(void*)&flags, (void*)&cta_a, (void*)&cta_b, (void*)&warm, (void*)&iters, (void*)&res};
+        if (cudaLaunchCooperativeKernel((const void*)pingpong_kernel, dim3(sms), dim3(32), args, (size_t)smem, 0) !=
+                cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(h, res, 32, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            st = RRA_ERR_CUDA;
+        }
+    }
+    cudaFree(flags);
+    cudaFree(res);
+    if (st != RRA_OK) return st;
+    if (h[3] != 0) return RRA_ERR_TIMEOUT;
+    *ns_round_trip = (double)h[0] / (double)iters;
+    if (sm_a) *sm_a = (int)h[1];
+    if (sm_b) *sm_b = (int)h[2];
+    return RRA_OK;
+}
+
+rra_status_t rra_probe_empty_kernel(rra_stream_t stream) {
+    empty_kernel<<<1, 32, 0, (cudaStream_t)stream>>>();
+    return cudaGetLastError() == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+}
+
+}  // extern "C"

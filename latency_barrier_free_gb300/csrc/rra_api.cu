@@ -1,0 +1,533 @@
+// rra_api.cu -- host side of the C ABI declared in include/rra.h.
+//
+// The communicator owns one device allocation: a control block followed by N
+// windows at a fixed stride ("symmetric memory", "Every Microsecond Matters"
+// Sec. II-B, restated for virtual ranks on one GPU).  Window regions, in
+// order: one-shot LL slots, one-shot sentinel slots, two-shot RS + AG slots,
+// LL128-atomic accumulators + counters + LL AllGather slots.  Scratch caps
+// default to the paper's sizes (Sec. VII, Fig. 12): 4 MiB per window for
+// one-shot, 64 MiB for two-shot and LL128-atomic; messages larger than a
+// step's capacity run as a chunk loop (Sec. IV, double buffering).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "rra.h"
+#include "rra_internal.h"
+
+using rra::Ctrl;
+using rra::Params;
+
+namespace {
+
+constexpr size_t kDefaultScratchOneshot = 4ull << 20;   // Fig. 12: one-shot
+constexpr size_t kDefaultScratchTwoshot = 64ull << 20;  // Fig. 12: two-shot, LL128
+constexpr size_t kWindowAlign = 64ull << 10;
+
+size_t floor16(size_t x) { return x & ~(size_t)15; }
+size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
+size_t align_up(size_t x, size_t a) { return ceil_div(x, a) * a; }
+
+size_t elem_size(rra_dtype_t d) {
+    switch (d) {
+        case RRA_FP32: return 4;
+        case RRA_BF16: return 2;
+        case RRA_FP64: return 8;
+    }
+    return 0;
+}
+
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_LL128_ATOMIC; }
+bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
+
+int64_t env_i64(const char* name, int64_t dflt) {
+    const char* s = getenv(name);
+    if (s == nullptr || *s == '\0') return dflt;
+    char* end = nullptr;
+    long long v = strtoll(s, &end, 10);
+    if (end == s) return dflt;
+    return (int64_t)v;
+}
+
+// LL128-atomic region of one window for a partition of `part` payload bytes.
+struct LaSizes {
+    size_t acc_parity;   // accumulator bytes per parity (bf16 needs 2x: binary32 accumulators)
+    size_t cnt_parity;   // counter bytes per parity
+    size_t ag_slot;      // LL AllGather slot bytes (2x payload)
+    size_t total;
+};
+LaSizes la_sizes(size_t part, int n) {
+    LaSizes s;
+    s.acc_parity = 2 * part;
+    const size_t groups = ceil_div(part / rra::kVecBytes, rra::kGroupVecs);
+    s.cnt_parity = align_up(groups * 4, 256);
+    s.ag_slot = 2 * part;
+    s.total = 2 * s.acc_parity + 2 * s.cnt_parity + 2 * (size_t)n * s.ag_slot;
+    return s;
+}
+
+}  // namespace
+
+struct rra_comm {
+    int device = -1;
+    int nranks = 0;
+    size_t max_bytes = 0;
+    size_t cap_oneshot = 0, cap_twoshot = 0;
+    rra_layout_t lay = {};
+    char* base = nullptr;
+    Ctrl* ctrl = nullptr;
+    char* win0 = nullptr;
+    int sm_count = 0;
+    int threads = 512;
+    int64_t ctas_per_rank = 0;
+    int64_t timeout_ms = 1000;
+    int64_t ts_chunk = 0, la_chunk = 0, os_chunk = 0;
+    int blocks_per_sm[3][4];  // by dtype, algo; -1 = not queried (for `threads`)
+    bool poisoned = false;
+    uint64_t* timing = nullptr;
+    // rra_allreduce_host staging (allocated on first use)
+    char* stage = nullptr;
+    size_t stage_slot = 0;
+    uint32_t* host_status = nullptr;
+    std::mutex mu;
+};
+
+extern "C" {
+
+const char* rra_version(void) { return "0.1.0"; }
+
+const char* rra_status_string(rra_status_t s) {
+    switch (s) {
+        case RRA_OK: return "ok";
+        case RRA_ERR_INVALID_ARG: return "invalid argument";
+        case RRA_ERR_CUDA: return "CUDA runtime error";
+        case RRA_ERR_OOM: return "out of device memory";
+        case RRA_ERR_NOT_CORESIDENT: return "ranks cannot all be co-resident on the GPU";
+        case RRA_ERR_TIMEOUT: return "a device-side wait timed out";
+        case RRA_ERR_POISONED: return "communicator poisoned by an earlier device error; reset it";
+        case RRA_ERR_EPOCH: return "epoch counter near wrap; reset the communicator";
+    }
+    return "unknown status";
+}
+
+rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_oneshot,
+                             size_t scratch_twoshot, rra_layout_t* out) {
+    if (out == nullptr || nranks < 2 || nranks > RRA_MAX_RANKS || max_bytes == 0)
+        return RRA_ERR_INVALID_ARG;
+    if (max_bytes > (1ull << 40)) return RRA_ERR_INVALID_ARG;
+    const size_t cap_os = scratch_oneshot ? scratch_oneshot : kDefaultScratchOneshot;
+    const size_t cap_ts = scratch_twoshot ? scratch_twoshot : kDefaultScratchTwoshot;
+    const size_t n = (size_t)nranks;
+    const size_t nvec = ceil_div(max_bytes, rra::kVecBytes);
+    const size_t payload = nvec * rra::kVecBytes;
+    const size_t part_need = ceil_div(nvec, n) * rra::kVecBytes;
+
+    rra_layout_t L = {};
+    L.nranks = nranks;
+    L.max_bytes = max_bytes;
+    // One-shot: 2 parities x N source slots; LL doubles every payload byte
+    // (Fig. 8: 2 x sizeof(T) per element in LL mode).
+    L.ll_chunk = std::min(payload, floor16(cap_os / (2 * n * 2)));
+    L.os_chunk = std::min(payload, floor16(cap_os / (2 * n)));
+    // Two-shot: RS and AG regions, each 2 parities x N slots of one partition.
+    L.ts_part = std::min(part_need, floor16(cap_ts / (4 * n)));
+    // LL128-atomic: shrink the partition until the region fits the cap.
+    size_t la_part = std::min(part_need, floor16(cap_ts / (4 * (n + 1))));
+    while (la_part >= (size_t)rra::kVecBytes && la_sizes(la_part, nranks).total > cap_ts)
+        la_part -= rra::kVecBytes;
+    L.la_part = la_part;
+    if (L.ll_chunk < 16 || L.os_chunk < 16 || L.ts_part < 16 || L.la_part < 16)
+        return RRA_ERR_INVALID_ARG;
+    L.ll_bytes = align_up(2 * n * 2 * L.ll_chunk, rra::kRegionAlign);
+    L.os_bytes = align_up(2 * n * L.os_chunk, rra::kRegionAlign);
+    L.ts_bytes = align_up(2 * (2 * n * L.ts_part), rra::kRegionAlign);
+    L.la_bytes = align_up(la_sizes(L.la_part, nranks).total, rra::kRegionAlign);
+    L.window_stride = align_up(L.ll_bytes + L.os_bytes + L.ts_bytes + L.la_bytes, kWindowAlign);
+    L.ctrl_bytes = align_up(sizeof(Ctrl), rra::kRegionAlign);
+    L.total_bytes = L.ctrl_bytes + n * L.window_stride;
+    *out = L;
+    return RRA_OK;
+}
+
+static rra_status_t query_blocks(rra_comm* c, rra_dtype_t d, rra_algo_t a, int* out) {
+    int& b = c->blocks_per_sm[d][a];
+    if (b < 0) {
+        int v = 0;
+        if (rra::occupancy(d, a, c->threads, &v) != cudaSuccess) return RRA_ERR_CUDA;
+        b = v;
+    }
+    *out = b;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out) {
+    if (out == nullptr) return RRA_ERR_INVALID_ARG;
+    const size_t cap_os = (size_t)std::max<int64_t>(0, env_i64("RRA_SCRATCH_ONESHOT", 0));
+    const size_t cap_ts = (size_t)std::max<int64_t>(0, env_i64("RRA_SCRATCH_TWOSHOT", 0));
+    rra_layout_t lay;
+    rra_status_t st = rra_plan_layout(nranks, max_bytes, cap_os, cap_ts, &lay);
+    if (st != RRA_OK) return st;
+
+    rra_comm* c = new (std::nothrow) rra_comm();
+    if (c == nullptr) return RRA_ERR_OOM;
+    c->nranks = nranks;
+    c->max_bytes = max_bytes;
+    c->cap_oneshot = cap_os;
+    c->cap_twoshot = cap_ts;
+    c->lay = lay;
+    for (auto& row : c->blocks_per_sm)
+        for (int& b : row) b = -1;
+    c->timeout_ms = env_i64("RRA_POLL_TIMEOUT_MS", 1000);
+    c->ctas_per_rank = env_i64("RRA_CTAS_PER_RANK", 0);
+    const int64_t thr = env_i64("RRA_THREADS", 512);
+    if (thr == 128 || thr == 256 || thr == 512) c->threads = (int)thr;
+    if (c->timeout_ms <= 0) c->timeout_ms = 1000;
+    if (c->ctas_per_rank < 0) c->ctas_per_rank = 0;
+
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+        delete c;
+        return RRA_ERR_CUDA;
+    }
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device) != cudaSuccess || !coop) {
+        delete c;
+        return RRA_ERR_CUDA;
+    }
+    // Every algorithm must fit at least one CTA per rank at once.
+    for (int d = 0; d < 3; ++d) {
+        for (int a = 0; a < 4; ++a) {
+            int b = 0;
+            if (query_blocks(c, (rra_dtype_t)d, (rra_algo_t)a, &b) != RRA_OK) {
+                delete c;
+                return RRA_ERR_CUDA;
+            }
+            if ((int64_t)b * c->sm_count < nranks) {
+                delete c;
+                return RRA_ERR_NOT_CORESIDENT;
+            }
+        }
+    }
+    if (cudaMalloc((void**)&c->base, lay.total_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return RRA_ERR_OOM;
+    }
+    c->ctrl = (Ctrl*)c->base;
+    c->win0 = c->base + lay.ctrl_bytes;
+    if (rra::launch_init(c->base, lay.total_bytes, lay, nranks, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(c->base);
+        delete c;
+        return RRA_ERR_CUDA;
+    }
+    *out = c;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_destroy(rra_comm_t c) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    rra_status_t st = RRA_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) st = RRA_ERR_CUDA;
+    if (c->base) cudaFree(c->base);
+    if (c->stage) cudaFree(c->stage);
+    if (c->host_status) cudaFreeHost(c->host_status);
+    delete c;
+    return st;
+}
+
+rra_status_t rra_comm_layout(rra_comm_t c, rra_layout_t* out) {
+    if (c == nullptr || out == nullptr) return RRA_ERR_INVALID_ARG;
+    *out = c->lay;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(c->mu);
+    switch (attr) {
+        case RRA_ATTR_CTAS_PER_RANK:
+            if (v < 0 || v > rra::kEpochSlots) return RRA_ERR_INVALID_ARG;
+            c->ctas_per_rank = v;
+            return RRA_OK;
+        case RRA_ATTR_POLL_TIMEOUT_MS:
+            if (v <= 0 || v > 3600000) return RRA_ERR_INVALID_ARG;
+            c->timeout_ms = v;
+            return RRA_OK;
+        case RRA_ATTR_THREADS:
+            if (v != 128 && v != 256 && v != 512) return RRA_ERR_INVALID_ARG;
+            if (c->threads != (int)v) {
+                c->threads = (int)v;
+                for (auto& row : c->blocks_per_sm)
+                    for (int& b : row) b = -1;
+            }
+            return RRA_OK;
+        case RRA_ATTR_TWOSHOT_CHUNK:
+            if (v < 0 || v % 16) return RRA_ERR_INVALID_ARG;
+            c->ts_chunk = v;
+            return RRA_OK;
+        case RRA_ATTR_LL128_CHUNK:
+            if (v < 0 || v % 16) return RRA_ERR_INVALID_ARG;
+            c->la_chunk = v;
+            return RRA_OK;
+        case RRA_ATTR_ONESHOT_CHUNK:
+            if (v < 0 || v % 16) return RRA_ERR_INVALID_ARG;
+            c->os_chunk = v;
+            return RRA_OK;
+    }
+    return RRA_ERR_INVALID_ARG;
+}
+
+rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
+    if (c == nullptr || v == nullptr) return RRA_ERR_INVALID_ARG;
+    switch (attr) {
+        case RRA_ATTR_CTAS_PER_RANK: *v = c->ctas_per_rank; return RRA_OK;
+        case RRA_ATTR_POLL_TIMEOUT_MS: *v = c->timeout_ms; return RRA_OK;
+        case RRA_ATTR_THREADS: *v = c->threads; return RRA_OK;
+        case RRA_ATTR_TWOSHOT_CHUNK: *v = c->ts_chunk; return RRA_OK;
+        case RRA_ATTR_LL128_CHUNK: *v = c->la_chunk; return RRA_OK;
+        case RRA_ATTR_ONESHOT_CHUNK: *v = c->os_chunk; return RRA_OK;
+    }
+    return RRA_ERR_INVALID_ARG;
+}
+
+rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, int* ctas) {
+    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a)) return RRA_ERR_INVALID_ARG;
+    int b = 0;
+    rra_status_t st = query_blocks(c, d, a, &b);
+    if (st != RRA_OK) return st;
+    *ctas = std::min(b * c->sm_count, rra::kEpochSlots);
+    return RRA_OK;
+}
+
+// Fills everything in Params except the pointer tables.
+static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                              Params* p) {
+    const size_t es = elem_size(dtype);
+    const size_t ve = rra::kVecBytes / es;
+    const size_t n = (size_t)c->nranks;
+    const rra_layout_t& L = c->lay;
+    int max_ctas = 0;
+    rra_status_t st = rra_comm_max_coresident(c, dtype, algo, &max_ctas);
+    if (st != RRA_OK) return st;
+    const int64_t cmax = std::max<int64_t>(1, max_ctas / c->nranks);
+    const size_t T = (size_t)c->threads;
+
+    memset(p, 0, sizeof(*p));
+    p->win0 = c->win0;
+    p->ctrl = c->ctrl;
+    p->timing = c->timing;
+    p->stride = L.window_stride;
+    p->count = count;
+    p->nvec = ceil_div(count, ve);
+    p->timeout_ns = (uint64_t)c->timeout_ms * 1000000ull;
+    p->nranks = c->nranks;
+    p->epoch_slots = rra::kEpochSlots;
+
+    const size_t off_ll = 0;
+    const size_t off_os = off_ll + L.ll_bytes;
+    const size_t off_ts = off_os + L.os_bytes;
+    const size_t off_la = off_ts + L.ts_bytes;
+    size_t work = 0;  // positions per step that the CTAs of one rank split
+    int64_t ctas;
+    switch (algo) {
+        case RRA_ONESHOT_LL:
+        case RRA_ONESHOT_SENTINEL: {
+            const bool ll = algo == RRA_ONESHOT_LL;
+            size_t cap = (ll ? L.ll_chunk : L.os_chunk) / rra::kVecBytes;
+            if (c->os_chunk > 0) cap = std::min(cap, std::max<size_t>(1, (size_t)c->os_chunk / rra::kVecBytes));
+            const size_t chunk = std::min<size_t>(p->nvec, cap);
+            p->chunk_vecs = chunk;
+            p->nsteps = (uint32_t)ceil_div(p->nvec, chunk);
+            p->region_off = ll ? off_ll : off_os;
+            p->slot_bytes = ll ? 2 * L.ll_chunk : L.os_chunk;
+            p->parity_bytes = n * p->slot_bytes;
+            work = chunk;
+            break;
+        }
+        case RRA_TWOSHOT_DBUF: {
+            size_t cap = L.ts_part / rra::kVecBytes;
+            if (c->ts_chunk > 0)
+                cap = std::min(cap, std::max<size_t>(1, (size_t)c->ts_chunk / rra::kVecBytes / n));
+            const size_t part = std::min(ceil_div(p->nvec, n), cap);
+            p->chunk_vecs = part;
+            p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
+            p->region_off = off_ts;
+            p->slot_bytes = L.ts_part;
+            p->parity_bytes = n * L.ts_part;
+            p->aux_off = off_ts + 2 * p->parity_bytes;
+            work = part;
+            break;
+        }
+        case RRA_LL128_ATOMIC: {
+            size_t cap = L.la_part / rra::kVecBytes;
+            if (c->la_chunk > 0)
+                cap = std::min(cap, std::max<size_t>(1, (size_t)c->la_chunk / rra::kVecBytes / n));
+            const size_t part = std::min(ceil_div(p->nvec, n), cap);
+            const LaSizes s = la_sizes(L.la_part, c->nranks);
+            p->chunk_vecs = part;
+            p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
+            p->region_off = off_la;
+            p->parity_bytes = s.acc_parity;
+            p->aux_off = off_la + 2 * s.acc_parity;
+            p->aux_parity_bytes = s.cnt_parity;
+            p->aux2_off = p->aux_off + 2 * s.cnt_parity;
+            p->aux2_slot_bytes = s.ag_slot;
+            p->aux2_parity_bytes = n * s.ag_slot;
+            work = part;
+            break;
+        }
+        default:
+            return RRA_ERR_INVALID_ARG;
+    }
+    if (c->ctas_per_rank > 0) ctas = std::min<int64_t>(c->ctas_per_rank, cmax);
+    else ctas = std::min<int64_t>((int64_t)ceil_div(work, T), cmax);
+    ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)work));
+    size_t per = ceil_div(work, (size_t)ctas);
+    if (algo == RRA_LL128_ATOMIC) per = align_up(per, rra::kGroupVecs);
+    ctas = (int64_t)ceil_div(work, per);
+    p->ctas_per_rank = (int32_t)ctas;
+    p->per_cta = per;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                                int* grid_ctas, int* steps) {
+    if (c == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0) return RRA_ERR_INVALID_ARG;
+    if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
+    Params p;
+    rra_status_t st = plan_call(c, count, dtype, algo, &p);
+    if (st != RRA_OK) return st;
+    if (grid_ctas) *grid_ctas = p.nranks * p.ctas_per_rank;
+    if (steps) *steps = (int)p.nsteps;
+    return RRA_OK;
+}
+
+rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                           rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
+    if (c == nullptr || send == nullptr || recv == nullptr) return RRA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_algo(algo)) return RRA_ERR_INVALID_ARG;
+    if (c->poisoned) return RRA_ERR_POISONED;
+    if (count == 0) return RRA_OK;
+    const size_t es = elem_size(dtype);
+    if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
+    Params p;
+    {
+        std::lock_guard<std::mutex> g(c->mu);
+        rra_status_t st = plan_call(c, count, dtype, algo, &p);
+        if (st != RRA_OK) return st;
+    }
+    for (int r = 0; r < c->nranks; ++r) {
+        if (send[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
+        if (((uintptr_t)send[r] | (uintptr_t)recv[r]) & 15u) return RRA_ERR_INVALID_ARG;
+        p.send[r] = send[r];
+        p.recv[r] = recv[r];
+    }
+    cudaError_t e = rra::launch_allreduce(p, dtype, algo, c->threads, (cudaStream_t)stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        return RRA_ERR_NOT_CORESIDENT;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RRA_ERR_CUDA;
+    }
+    return RRA_OK;
+}
+
+rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                                rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
+    if (c == nullptr || send == nullptr || recv == nullptr) return RRA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_algo(algo)) return RRA_ERR_INVALID_ARG;
+    if (c->poisoned) return RRA_ERR_POISONED;
+    if (count == 0) return RRA_OK;
+    const size_t es = elem_size(dtype);
+    if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
+    for (int r = 0; r < c->nranks; ++r)
+        if (send[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
+    if (c->stage == nullptr) {
+        c->stage_slot = align_up(c->max_bytes, 256);
+        if (cudaMalloc((void**)&c->stage, 2 * (size_t)c->nranks * c->stage_slot) != cudaSuccess) {
+            cudaGetLastError();
+            c->stage = nullptr;
+            return RRA_ERR_OOM;
+        }
+        if (cudaHostAlloc((void**)&c->host_status, sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(c->stage);
+            c->stage = nullptr;
+            return RRA_ERR_OOM;
+        }
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = count * es;
+    const void* dsend[RRA_MAX_RANKS];
+    void* drecv[RRA_MAX_RANKS];
+    for (int r = 0; r < c->nranks; ++r) {
+        dsend[r] = c->stage + (size_t)r * c->stage_slot;
+        drecv[r] = c->stage + (size_t)(c->nranks + r) * c->stage_slot;
+        if (cudaMemcpyAsync((void*)dsend[r], send[r], bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return RRA_ERR_CUDA;
+    }
+    rra_status_t st = rra_allreduce(c, dsend, drecv, count, dtype, algo, stream);
+    if (st != RRA_OK) return st;
+    for (int r = 0; r < c->nranks; ++r) {
+        if (cudaMemcpyAsync(recv[r], drecv[r], bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return RRA_ERR_CUDA;
+    }
+    if (cudaMemcpyAsync(c->host_status, &c->ctrl->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RRA_ERR_CUDA;
+    if (*c->host_status != 0u) {
+        c->poisoned = true;
+        return (rra_status_t)*c->host_status;
+    }
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_status(rra_comm_t c, int* rank, int* step) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
+    uint32_t hdr[4];
+    if (cudaMemcpy(hdr, c->ctrl, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return RRA_ERR_CUDA;
+    if (rank) *rank = hdr[0] ? (int)(int32_t)hdr[1] : -1;
+    if (step) *step = hdr[0] ? (int)(int32_t)hdr[2] : -1;
+    if (hdr[0] != 0u) {
+        c->poisoned = true;
+        return (rra_status_t)hdr[0];
+    }
+    return c->poisoned ? RRA_ERR_POISONED : RRA_OK;
+}
+
+rra_status_t rra_comm_reset(rra_comm_t c) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
+    if (rra::launch_init(c->base, c->lay.total_bytes, c->lay, c->nranks, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return RRA_ERR_CUDA;
+    c->poisoned = false;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_set_timing(rra_comm_t c, uint64_t* dev_buf) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(c->mu);
+    c->timing = dev_buf;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_inject_drop(rra_comm_t c, int rank) {
+    if (c == nullptr || rank < -1 || rank >= c->nranks) return RRA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
+    int32_t v = rank;
+    if (cudaMemcpy(&c->ctrl->drop_rank, &v, sizeof(v), cudaMemcpyHostToDevice) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    return RRA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// rra_internal.h -- definitions shared by the host library and the kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+#include "rra.h"
+
+namespace rra {
+
+constexpr int kMaxRanks = RRA_MAX_RANKS;
+constexpr int kVecBytes = 16;          // every transfer unit is one 16-byte vector
+constexpr int kEpochSlots = 4096;      // largest grid a communicator may launch
+constexpr int kGroupVecs = 32;         // LL128-atomic: vectors per completion counter (one warp)
+constexpr size_t kRegionAlign = 4096;
+
+// Control block at the start of the allocation (before window 0).
+struct Ctrl {
+    uint32_t status;     // rra_status_t of the first device-side error; 0 = none
+    int32_t err_rank;    // virtual rank that recorded it
+    int32_t err_step;    // chunk step of the call in which it was recorded
+    int32_t drop_rank;   // injected fault: rank whose stores to peers are skipped; -1 = none
+    uint32_t reserved[60];
+    // Every CTA slot holds the same value: the epoch of the next step.  CTA b
+    // of a call with G CTAs reads slot b at entry and writes epoch + steps to
+    // every slot b' = b (mod G); each slot has exactly one reader/writer per
+    // call, and all slots stay equal whatever grid a later call uses.
+    uint64_t epoch[kEpochSlots];
+};
+
+// Kernel parameters, passed by value (one launch = one call).
+struct Params {
+    const void* send[kMaxRanks];
+    void* recv[kMaxRanks];
+    char* win0;            // window 0 (window r = win0 + r * stride)
+    Ctrl* ctrl;
+    uint64_t* timing;      // optional: (start, end) %globaltimer per CTA
+    uint64_t stride;       // bytes between windows
+    uint64_t count;        // elements per rank
+    uint64_t nvec;         // 16-byte vectors per rank = ceil(count / elems per vector)
+    uint64_t timeout_ns;   // limit of every wait
+    uint64_t region_off;   // offset of the algorithm's region inside a window
+    uint64_t slot_bytes;   // bytes of one (parity, source) slot
+    uint64_t parity_bytes; // bytes of one parity (all sources)
+    uint64_t aux_off;      // two-shot: AllGather region; LL128: counters
+    uint64_t aux2_off;     // LL128: LL-encoded AllGather slots
+    uint64_t aux_parity_bytes;   // LL128: bytes of one parity of counters
+    uint64_t aux2_slot_bytes;    // LL128: bytes of one AllGather slot
+    uint64_t aux2_parity_bytes;  // LL128: bytes of one AllGather parity
+    uint64_t chunk_vecs;   // one-shot: vectors per rank per full step;
+                           // two-shot/LL128: vectors per partition per full step
+    uint64_t per_cta;      // vectors per CTA per step (the same in every step)
+    uint32_t nsteps;
+    int32_t nranks;
+    int32_t ctas_per_rank;
+    int32_t epoch_slots;   // number of epoch slots to keep equal
+};
+
+// Host-side launch entry points (kernels.cu).
+cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, rra_algo_t algo,
+                             int threads, cudaStream_t stream);
+cudaError_t occupancy(rra_dtype_t dtype, rra_algo_t algo, int threads, int* blocks_per_sm);
+cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
+                        cudaStream_t stream);
+
+}  // namespace rra

@@ -1,0 +1,273 @@
+"""Python binding of the rra C ABI (include/rra.h, include/rra_probe.h).
+
+Argument marshalling only: every step of the AllReduce runs in librra.so's
+CUDA kernels.  If librra.so cannot be loaded, every call raises; there is no
+fallback.  Torch is used for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librra.so")
+
+OK = 0
+STATUS_NAMES = {
+    0: "RRA_OK", 1: "RRA_ERR_INVALID_ARG", 2: "RRA_ERR_CUDA", 3: "RRA_ERR_OOM",
+    4: "RRA_ERR_NOT_CORESIDENT", 5: "RRA_ERR_TIMEOUT", 6: "RRA_ERR_POISONED", 7: "RRA_ERR_EPOCH",
+}
+ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_CORESIDENT, ERR_TIMEOUT, ERR_POISONED, ERR_EPOCH = range(1, 8)
+
+DTYPES = {"fp32": 0, "bf16": 1, "fp64": 2}
+ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomic": 3}
+ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,
+         "ll128_chunk": 4, "oneshot_chunk": 5}
+MAX_RANKS = 64
+
+# Exported symbols, in declaration order of the public headers.
+SYMBOLS = [
+    "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_comm_status", "rra_comm_reset",
+    "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
+    "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_inject_drop",
+    "rra_status_string", "rra_version",
+    "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_sm_count",
+]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) if n != "nranks" else (n, ctypes.c_int) for n in (
+        "nranks", "max_bytes", "ll_chunk", "ll_bytes", "os_chunk", "os_bytes", "ts_part", "ts_bytes",
+        "la_part", "la_bytes", "window_stride", "ctrl_bytes", "total_bytes")]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class RraError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        name = STATUS_NAMES.get(self.status, str(status))
+        super().__init__("%s%s: %s" % (what + ": " if what else "", name, status_string(self.status)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load librra.so (once).  Raises if it is missing: build it first with
+    latency_barrier_free_gb300.build_ext.build()."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError("librra.so not found at %s; run latency_barrier_free_gb300.build_ext.build()" % path)
+        lib = ctypes.CDLL(path)
+        vp, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        ip = ctypes.POINTER(ctypes.c_int)
+        sig = {
+            "rra_comm_create": ([i32, sz, pp], i32),
+            "rra_allreduce": ([vp, pp, pp, sz, i32, i32, vp], i32),
+            "rra_allreduce_host": ([vp, pp, pp, sz, i32, i32, vp], i32),
+            "rra_comm_status": ([vp, ip, ip], i32),
+            "rra_comm_reset": ([vp], i32),
+            "rra_comm_destroy": ([vp], i32),
+            "rra_comm_set_attr": ([vp, i32, i64], i32),
+            "rra_comm_get_attr": ([vp, i32, ctypes.POINTER(i64)], i32),
+            "rra_comm_layout": ([vp, ctypes.POINTER(Layout)], i32),
+            "rra_plan_layout": ([i32, sz, sz, sz, ctypes.POINTER(Layout)], i32),
+            "rra_comm_plan_call": ([vp, sz, i32, i32, ip, ip], i32),
+            "rra_comm_max_coresident": ([vp, i32, i32, ip], i32),
+            "rra_comm_set_timing": ([vp, vp], i32),
+            "rra_comm_inject_drop": ([vp, i32], i32),
+            "rra_status_string": ([i32], ctypes.c_char_p),
+            "rra_version": ([], ctypes.c_char_p),
+            "rra_probe_l2_chase": ([sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.POINTER(ctypes.c_double)], i32),
+            "rra_probe_pingpong": ([i32, i32, i32, ctypes.POINTER(ctypes.c_double), ip, ip], i32),
+            "rra_probe_empty_kernel": ([vp], i32),
+            "rra_probe_sm_count": ([ip], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise RraError(status, what)
+
+
+def status_string(status: int) -> str:
+    return load().rra_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return load().rra_version().decode()
+
+
+def plan_layout(nranks: int, max_bytes: int, scratch_oneshot: int = 0, scratch_twoshot: int = 0) -> dict:
+    """Window layout for (nranks, max_bytes); pure host arithmetic (no GPU)."""
+    lay = Layout()
+    _check(load().rra_plan_layout(nranks, max_bytes, scratch_oneshot, scratch_twoshot, ctypes.byref(lay)),
+           "rra_plan_layout")
+    return lay.as_dict()
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_of(t) -> int:
+    import torch
+    m = {torch.float32: 0, torch.bfloat16: 1, torch.float64: 2}
+    if t.dtype not in m:
+        raise TypeError("unsupported dtype %s (float32, bfloat16, float64)" % t.dtype)
+    return m[t.dtype]
+
+
+class Comm:
+    """A communicator of `nranks` virtual ranks on the current CUDA device."""
+
+    def __init__(self, nranks: int, max_bytes: int):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.rra_comm_create(int(nranks), int(max_bytes), ctypes.byref(h)), "rra_comm_create")
+        self._h = h
+        self.nranks = int(nranks)
+        self.max_bytes = int(max_bytes)
+
+    # -- lifetime -----------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            st = self._lib.rra_comm_destroy(self._h)
+            self._h = None
+            _check(st, "rra_comm_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- the operation ------------------------------------------------------
+    def allreduce_ptrs(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None) -> None:
+        sp, ks = _ptr_array(send_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        st = self._lib.rra_allreduce(self._h, sp, rp, int(count), DTYPES[dtype], ALGOS[algo],
+                                     _stream_handle(stream))
+        del ks, kr
+        _check(st, "rra_allreduce")
+
+    def allreduce(self, sends, recvs, algo: str, stream=None) -> None:
+        """recvs[r][:] = sum over ranks of sends[p][:]; tensors on the GPU,
+        one per rank, same dtype and element count, contiguous."""
+        if len(sends) != self.nranks or len(recvs) != self.nranks:
+            raise ValueError("need one send and one recv tensor per rank")
+        dt = _dtype_of(sends[0])
+        n = sends[0].numel()
+        for t in list(sends) + list(recvs):
+            if not t.is_cuda or not t.is_contiguous() or t.numel() != n or _dtype_of(t) != dt:
+                raise ValueError("all tensors must be contiguous CUDA tensors of one dtype and size")
+        dname = {0: "fp32", 1: "bf16", 2: "fp64"}[dt]
+        self.allreduce_ptrs([t.data_ptr() for t in sends], [t.data_ptr() for t in recvs], n, dname, algo, stream)
+
+    def allreduce_host(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None) -> None:
+        """Host buffers in, host buffers out (H2D, kernel, D2H, synchronise)."""
+        sp, ks = _ptr_array(send_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        st = self._lib.rra_allreduce_host(self._h, sp, rp, int(count), DTYPES[dtype], ALGOS[algo],
+                                          _stream_handle(stream))
+        del ks, kr
+        _check(st, "rra_allreduce_host")
+
+    # -- control ------------------------------------------------------------
+    def status(self):
+        """(status code, rank, step); synchronises the device."""
+        rank = ctypes.c_int(-1)
+        step = ctypes.c_int(-1)
+        st = self._lib.rra_comm_status(self._h, ctypes.byref(rank), ctypes.byref(step))
+        return st, rank.value, step.value
+
+    def reset(self):
+        _check(self._lib.rra_comm_reset(self._h), "rra_comm_reset")
+
+    def set_attr(self, name: str, value: int):
+        _check(self._lib.rra_comm_set_attr(self._h, ATTRS[name], int(value)), "rra_comm_set_attr")
+
+    def get_attr(self, name: str) -> int:
+        v = ctypes.c_int64()
+        _check(self._lib.rra_comm_get_attr(self._h, ATTRS[name], ctypes.byref(v)), "rra_comm_get_attr")
+        return v.value
+
+    def layout(self) -> dict:
+        lay = Layout()
+        _check(self._lib.rra_comm_layout(self._h, ctypes.byref(lay)), "rra_comm_layout")
+        return lay.as_dict()
+
+    def plan_call(self, count: int, dtype: str, algo: str):
+        g = ctypes.c_int()
+        s = ctypes.c_int()
+        _check(self._lib.rra_comm_plan_call(self._h, int(count), DTYPES[dtype], ALGOS[algo],
+                                            ctypes.byref(g), ctypes.byref(s)), "rra_comm_plan_call")
+        return g.value, s.value
+
+    def max_coresident(self, dtype: str, algo: str) -> int:
+        v = ctypes.c_int()
+        _check(self._lib.rra_comm_max_coresident(self._h, DTYPES[dtype], ALGOS[algo], ctypes.byref(v)),
+               "rra_comm_max_coresident")
+        return v.value
+
+    def set_timing(self, dev_ptr):
+        _check(self._lib.rra_comm_set_timing(self._h, ctypes.c_void_p(dev_ptr or 0)), "rra_comm_set_timing")
+
+    def inject_drop(self, rank: int):
+        _check(self._lib.rra_comm_inject_drop(self._h, int(rank)), "rra_comm_inject_drop")
+
+
+# ------------------------------------------------------------------ probes --
+def probe_l2_chase(buf_bytes: int = 8 << 20, hops: int = 200000, seed: int = 1) -> float:
+    ns = ctypes.c_double()
+    _check(load().rra_probe_l2_chase(int(buf_bytes), int(hops), int(seed), ctypes.byref(ns)), "rra_probe_l2_chase")
+    return ns.value
+
+
+def probe_pingpong(cta_a: int, cta_b: int, iters: int = 20000):
+    ns = ctypes.c_double()
+    a = ctypes.c_int()
+    b = ctypes.c_int()
+    _check(load().rra_probe_pingpong(int(cta_a), int(cta_b), int(iters), ctypes.byref(ns), ctypes.byref(a),
+                                     ctypes.byref(b)), "rra_probe_pingpong")
+    return ns.value, a.value, b.value
+
+
+def probe_empty_kernel(stream=None):
+    _check(load().rra_probe_empty_kernel(_stream_handle(stream)), "rra_probe_empty_kernel")
+
+
+def probe_sm_count() -> int:
+    v = ctypes.c_int()
+    _check(load().rra_probe_sm_count(ctypes.byref(v)), "rra_probe_sm_count")
+    return v.value

@@ -1,0 +1,161 @@
+"""GPU tests of the runtime around the kernels: CUDA-graph replay with
+device-resident epochs, bounded waits and fault reporting, reset, the
+host-buffer entry point, in-kernel timing and the latency probes."""
+import numpy as np
+import pytest
+
+import oracle
+from latency_barrier_free_gb300 import inputs, rra
+from tests.gpu_util import ALGOS, bits, check_against_oracle, poison_like, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_graph_replay_advances_epochs(algo):
+    """Capture 20 calls in a CUDA graph and replay it 5 times with new inputs
+    copied in between: every replay must see fresh epochs (LL flags) and
+    reset sentinels, so every replay's result is correct."""
+    n, count, calls = 4, 3000, 20
+    with rra.Comm(n, count * 4) as comm:
+        send = torch.zeros(calls, n, count, device="cuda")
+        recv = torch.zeros(calls, n, count, device="cuda")
+
+        def enqueue():
+            for i in range(calls):
+                comm.allreduce_ptrs([send[i, r].data_ptr() for r in range(n)],
+                                    [recv[i, r].data_ptr() for r in range(n)], count, "fp32", algo)
+
+        enqueue()  # warm-up outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                enqueue()
+        torch.cuda.synchronize()
+        for rep in range(5):
+            host = [inputs.normal(inputs.rng(70, rep, i), n, count, "fp32") for i in range(calls)]
+            send.copy_(torch.from_numpy(np.stack([np.stack(h) for h in host])))
+            recv.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert comm.status()[0] == rra.OK
+            got = recv.cpu().numpy()
+            for i in range(calls):
+                check_against_oracle(host[i], list(got[i]), "fp32", algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_timeout_poison_and_reset(algo):
+    """A rank that drops its stores makes its peers' polls run out of time:
+    the device records RRA_ERR_TIMEOUT (no fault, no hang), the communicator
+    is poisoned, and rra_comm_reset restores a working state."""
+    n, count = 4, 5000
+    sends_np = inputs.normal(inputs.rng(71, 0), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("poll_timeout_ms", 20)
+        comm.inject_drop(2)
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        st, rank, step = comm.status()
+        assert st == rra.ERR_TIMEOUT
+        assert 0 <= rank < n and step == 0
+        with pytest.raises(rra.RraError) as e:
+            comm.allreduce(sends, recvs, algo)
+        assert e.value.status == rra.ERR_POISONED
+        comm.reset()
+        assert comm.status()[0] == rra.OK
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+
+
+def test_device_error_makes_later_calls_noops():
+    """Calls enqueued after a device-side failure (before the host looks) do
+    nothing on the device and do not hang."""
+    n, count = 2, 1000
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("poll_timeout_ms", 10)
+        comm.inject_drop(0)
+        x = [torch.ones(count, device="cuda") for _ in range(n)]
+        y = poison_like(x)
+        for _ in range(5):
+            comm.allreduce(x, y, "oneshot_ll")
+        st, _, _ = comm.status()
+        assert st == rra.ERR_TIMEOUT
+        comm.reset()
+        comm.allreduce(x, y, "oneshot_ll")
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        assert torch.equal(y[0], torch.full_like(y[0], 2.0))
+
+
+def test_argument_errors():
+    with rra.Comm(4, 4096) as comm:
+        x = [torch.zeros(1024, device="cuda") for _ in range(4)]
+        ptrs = [t.data_ptr() for t in x]
+        with pytest.raises(rra.RraError) as e:  # larger than max_bytes
+            comm.allreduce_ptrs(ptrs, ptrs, 2048, "fp32", "oneshot_ll")
+        assert e.value.status == rra.ERR_INVALID_ARG
+        with pytest.raises(rra.RraError):       # misaligned pointer
+            comm.allreduce_ptrs([p + 4 for p in ptrs], ptrs, 16, "fp32", "oneshot_ll")
+        with pytest.raises(rra.RraError):       # null pointer
+            comm.allreduce_ptrs([0] * 4, ptrs, 16, "fp32", "oneshot_ll")
+        with pytest.raises(rra.RraError):
+            comm.set_attr("threads", 96)
+    with pytest.raises(rra.RraError):
+        rra.Comm(1, 4096)
+    with pytest.raises(rra.RraError):
+        rra.Comm(65, 4096)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_host_buffer_entry_point(algo):
+    n, count = 8, 10000
+    sends_np = inputs.normal(inputs.rng(72, 0), n, count, "fp32")
+    recvs_np = [np.full(count, np.nan, np.float32) for _ in range(n)]
+    with rra.Comm(n, count * 4) as comm:
+        for _ in range(2):
+            comm.allreduce_host([a.ctypes.data for a in sends_np], [a.ctypes.data for a in recvs_np],
+                                count, "fp32", algo)
+            check_against_oracle(sends_np, recvs_np, "fp32", algo)
+
+
+def test_in_kernel_timing():
+    n, count = 4, 1 << 16
+    with rra.Comm(n, count * 4) as comm:
+        grid, _ = comm.plan_call(count, "fp32", "oneshot_sentinel")
+        buf = torch.zeros(2 * grid, dtype=torch.int64, device="cuda")
+        comm.set_timing(buf.data_ptr())
+        x = [torch.randn(count, device="cuda") for _ in range(n)]
+        y = poison_like(x)
+        comm.allreduce(x, y, "oneshot_sentinel")
+        torch.cuda.synchronize()
+        comm.set_timing(0)
+        t = buf.view(grid, 2).cpu().numpy()
+        assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])
+        assert t[:, 1].max() - t[:, 0].min() < 10_000_000  # < 10 ms
+
+
+def test_probes():
+    ns = rra.probe_l2_chase(4 << 20, 20000, 3)
+    assert 50.0 < ns < 10000.0
+    sms = rra.probe_sm_count()
+    rtt, sa, sb = rra.probe_pingpong(0, sms - 1, 2000)
+    assert sa != sb and 50.0 < rtt < 100000.0
+    rra.probe_empty_kernel()
+    torch.cuda.synchronize()
