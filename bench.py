@@ -1,0 +1,564 @@
+#!/usr/bin/env python3
+"""Benchmark: barrier-free AllReduce over N virtual ranks on one GB300.
+
+Workload (one "step"): N=4 virtual ranks, message sizes 128 B .. 1 MiB per
+rank in powers of two (14 sizes), binary32 and bfloat16 N(0,1) inputs, all
+four algorithms; each (dtype, size, algorithm) runs `--inner` back-to-back
+calls on one stream, timed with CUDA events on that stream.  L2 is flushed
+(a 256 MiB write) between steps; the calls inside a step reuse their
+L2-resident buffers, the regime the small-message latency floor assumes.
+
+value     mean over the 28 (dtype, size) cases of the fastest algorithm's
+          microseconds per call (lower is better)
+e2e       the same metric through rra_allreduce_host: host buffers in and out,
+          host<->device copies inside the timed region
+roofline  the dominant kernel of the step against the measured HBM peak
+floor     measured single-GPU latency floor 2*L2_RTT + L_store->poll and the
+          in-kernel time of the 128-byte calls
+bandwidth twoshot_dbuf at N=8, 64 MiB and 512 MiB binary32 per rank, GB/s of
+          compulsory traffic (2*N*M) against the measured HBM peak
+cpu_baseline  the CPU oracle on a bounded sample of the same sweep
+
+--impl reference times the CPU oracle itself on the same sweep.
+Under torchrun (N>1) every GPU runs its own replica (the virtual ranks of one
+AllReduce never span GPUs); the reported latency is the maximum over GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+NRANKS = 4
+DTYPES = ("fp32", "bf16")
+ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic")
+ELEM = {"fp32": 4, "bf16": 2, "fp64": 8}
+METRIC = "AllReduce us/call at 128B-1MB; GB/s vs HBM roofline; N virtual ranks, 1 GB300"
+WORKLOAD = "N=4 virtual ranks, 128 B-1 MiB per rank (14 sizes), fp32+bf16 N(0,1), 4 algorithms"
+
+
+# ----------------------------------------------------------------- ranks --
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, values, device=None):
+    """Element-wise max of a list of floats over all ranks."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- helpers ----
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "prims.cuh", "rra_internal.h"):
+        h.update(open(os.path.join(ROOT, "latency_barrier_free_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, config):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    except (OSError, ValueError):
+        return None
+    for e in rec.get("entries", []):
+        if e.get("kernel") == kernel and e.get("config") == config and e.get("source_sha") == kernel_source_sha():
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+def to_device(arrs, dtype):
+    """Host numpy arrays (bfloat16 as uint16 bit patterns) -> CUDA tensors."""
+    import torch
+
+    out = []
+    for a in arrs:
+        if dtype == "bf16":
+            out.append(torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).view(torch.bfloat16).cuda())
+        else:
+            out.append(torch.from_numpy(np.ascontiguousarray(a).copy()).cuda())
+    return out
+
+
+def sweep_cases():
+    from latency_barrier_free_gb300 import inputs
+
+    return [(dt, size) for dt in DTYPES for size in inputs.W2_SIZES]
+
+
+# ------------------------------------------------------------ our arm ----
+def run_ours(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+    from latency_barrier_free_gb300 import inputs, measure, rra
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(dev)
+
+    comm = rra.Comm(NRANKS, 1 << 20)
+    cases = sweep_cases()
+    bufs = {}
+    for dt, size in cases:
+        sends = to_device(inputs.workload2(size, dt), dt)
+        recvs = [torch.empty_like(s) for s in sends]
+        bufs[(dt, size)] = ([s.data_ptr() for s in sends], [r.data_ptr() for r in recvs], size // ELEM[dt],
+                            sends, recvs)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    inner = args.inner
+
+    def one_step(events):
+        k = 0
+        for dt, size in cases:
+            sp, rp, count, _, _ = bufs[(dt, size)]
+            for algo in ALGOS:
+                if events is not None:
+                    events[k][0].record(stream)
+                for _ in range(inner):
+                    comm.allreduce_ptrs(sp, rp, count, dt, algo)
+                if events is not None:
+                    events[k][1].record(stream)
+                k += 1
+
+    for w in range(args.warmup):
+        flush.fill_(w & 0xFF)
+        one_step(None)
+    torch.cuda.synchronize()
+    st = comm.status()[0]
+    if st != rra.OK:
+        raise RuntimeError("device status after warm-up: %s" % rra.STATUS_NAMES.get(st))
+
+    ncase = len(cases) * len(ALGOS)
+    per_step_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                        for _ in range(ncase)] for _ in range(args.steps)]
+    step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(dist)
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)          # evict the previous step's lines from L2
+        step_events[s][0].record(stream)
+        one_step(per_step_events[s])
+        step_events[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+    st = comm.status()[0]
+    if st != rra.OK:
+        raise RuntimeError("device status after timed region: %s" % rra.STATUS_NAMES.get(st))
+
+    step_ms = [a.elapsed_time(b) for a, b in step_events]
+    us_call = {}  # (dt, size, algo) -> median over steps of us per call
+    k = 0
+    for dt, size in cases:
+        for algo in ALGOS:
+            vals = [per_step_events[s][k][0].elapsed_time(per_step_events[s][k][1]) * 1000.0 / inner
+                    for s in range(args.steps)]
+            us_call[(dt, size, algo)] = measure.median(vals)
+            k += 1
+    best = {(dt, size): min(ALGOS, key=lambda a: us_call[(dt, size, a)]) for dt, size in cases}
+    best_us = [us_call[(dt, size, best[(dt, size)])] for dt, size in cases]
+    value = float(np.mean(best_us))
+    per_algo_mean = {a: float(np.mean([us_call[(dt, size, a)] for dt, size in cases])) for a in ALGOS}
+
+    # dominant kernel of the step: largest time per step
+    dom = max(us_call, key=lambda key: us_call[key])
+    dom_dt, dom_size, dom_algo = dom
+    peaks = measured_peaks()
+    hbm_peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm_peak else "fallback"
+    hbm_peak = hbm_peak or 6800.0
+    dom_bytes = measure.algorithmic_bytes(NRANKS, dom_size)
+    achieved = dom_bytes / (us_call[dom] * 1e-6) / 1e9
+    kname = {"oneshot_ll": "oneshot_kernel", "oneshot_sentinel": "oneshot_kernel",
+             "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel"}[dom_algo]
+    dom_cfg = "%s N=%d %s %dB" % (dom_algo, NRANKS, dom_dt, dom_size)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": committed_traffic(kname, dom_cfg),
+                "kernel": kname, "config": dom_cfg, "peak_source": peak_src,
+                "note": "at <= 1 MiB the kernels are latency-bound; see floor"}
+
+    floor = latency_floor(comm, rra, measure, torch, stream)
+    bandwidth = bandwidth_end(rra, measure, torch, hbm_peak, args)
+    e2e = end_to_end(comm, rra, cases, best, torch, args)
+    decode = decode_graph(rra, torch) if args.decode else None
+
+    # aggregate over GPU replicas: latency-like numbers take the max
+    agg = max_over_ranks(dist, [value, float(np.mean(step_ms)), e2e["value"]], device=dev)
+    value, ms_step, e2e["value"] = agg
+    launches = args.steps * ncase * inner
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32+bf16",
+        "data": "synthetic (seeded N(0,1), no dataset)",
+        "config": {"workload": WORKLOAD, "nranks": NRANKS, "sizes_bytes": [c[1] for c in cases if c[0] == "fp32"],
+                   "inner_calls": inner, "l2": "flushed (256 MiB write) between steps; calls in a step reuse "
+                   "L2-resident buffers", "parallelism": "replicas" if world > 1 else "single GPU",
+                   "gpu": props.name, "sms": props.multi_processor_count},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "latency_floor": floor,
+        "bandwidth": bandwidth,
+        "e2e": e2e,
+        "clocks": clk,
+        "per_algo_mean_us": {a: round(v, 3) for a, v in per_algo_mean.items()},
+        "per_size_us": {"%s/%d" % (dt, size): {a: round(us_call[(dt, size, a)], 3) for a in ALGOS}
+                        for dt, size in cases},
+        "best_algo": {"%s/%d" % k: v for k, v in best.items()},
+    }
+    if decode is not None:
+        line["decode_graph"] = decode
+    if rank == 0 and args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    comm.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def latency_floor(comm, rra, measure, torch, stream):
+    """Measured floor 2*L2_RTT + L_store->poll next to the in-kernel time of the
+    128-byte calls (N=2 and N=4) and the empty-kernel launch overhead."""
+    l2 = [rra.probe_l2_chase(8 << 20, 100000, seed) for seed in (1, 2, 3)]
+    sms = rra.probe_sm_count()
+    pairs = [(0, j) for j in sorted({1, 2, 3, sms // 4, sms // 2, sms // 2 + 1, 3 * sms // 4, sms - 1}) if j > 0]
+    rtts = []
+    for a, b in pairs:
+        rtt, _, _ = rra.probe_pingpong(a, b, 20000)
+        rtts.append(rtt)
+    l2_ns = measure.median(l2)
+    store_ns = measure.median(rtts) / 2.0
+    floor_ns = measure.sol_floor_ns(l2_ns, store_ns)
+
+    def in_kernel(n, algo, reps=200):
+        with rra.Comm(n, 128) as c:
+            grid, _ = c.plan_call(32, "fp32", algo)
+            buf = torch.zeros(reps, 2 * grid, dtype=torch.int64, device="cuda")
+            xs = [torch.randn(32, device="cuda") for _ in range(n)]
+            ys = [torch.empty_like(x) for x in xs]
+            for i in range(reps):
+                c.set_timing(buf[i].data_ptr())
+                c.allreduce(xs, ys, algo)
+            torch.cuda.synchronize()
+            c.set_timing(0)
+            t = buf.view(reps, grid, 2).cpu().numpy()
+            spans = (t[:, :, 1].max(axis=1) - t[:, :, 0].min(axis=1)) / 1000.0
+            return float(np.median(spans[reps // 10:]))
+
+    kern = {}
+    for n in (2, 4):
+        for algo in ALGOS:
+            kern["N%d/%s" % (n, algo)] = round(in_kernel(n, algo), 3)
+    best_key = min(kern, key=kern.get)
+    # empty-kernel and graph-node overhead, same run
+    reps = 2000
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(100):
+        rra.probe_empty_kernel()
+    e0.record(stream)
+    for _ in range(reps):
+        rra.probe_empty_kernel()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    empty_us = e0.elapsed_time(e1) * 1000.0 / reps
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(160):
+                rra.probe_empty_kernel()
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(20):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    node_us = e0.elapsed_time(e1) * 1000.0 / (20 * 160)
+    return {"l2_rtt_ns": round(l2_ns, 1), "store_poll_ns": round(store_ns, 1),
+            "pingpong_rtt_ns": [round(x, 1) for x in rtts], "floor_us": round(floor_ns / 1000.0, 3),
+            "in_kernel_us_128B": kern, "best_in_kernel": best_key,
+            "best_over_floor": round(kern[best_key] / (floor_ns / 1000.0), 3),
+            "empty_kernel_us": round(empty_us, 3), "graph_node_us": round(node_us, 3),
+            "method": "L2 RTT: dependent ld.global.cg chase, 8 MiB random cycle; store->poll: half the RTT of a "
+                      "fence-free ping-pong between CTA 0 and CTAs on other SMs; in-kernel: %globaltimer first "
+                      "CTA start to last CTA end, median of 180 calls"}
+
+
+def bandwidth_end(rra, measure, torch, hbm_peak, args):
+    """twoshot_dbuf, N=8, binary32, inputs and outputs far larger than L2."""
+    out = {}
+    n = 8
+    sizes = [64 << 20] + ([512 << 20] if args.big else [])
+    for size in sizes:
+        count = size // 4
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(5000 + size // (1 << 20))
+        with rra.Comm(n, size) as c:
+            xs = [torch.rand(count, device="cuda", generator=gen) * 2 - 1 for _ in range(n)]
+            ys = [torch.empty_like(x) for x in xs]
+            for _ in range(2):
+                c.allreduce(xs, ys, "twoshot_dbuf")
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 5
+            e0.record()
+            for _ in range(reps):
+                c.allreduce(xs, ys, "twoshot_dbuf")
+            e1.record()
+            torch.cuda.synchronize()
+            st = c.status()[0]
+            t = e0.elapsed_time(e1) / 1000.0 / reps
+            gbs = measure.hbm_gbs(n, size, t)
+            out["%dMiB" % (size >> 20)] = {"ms": round(t * 1000, 3), "GB/s": round(gbs, 1),
+                                            "frac": round(gbs / hbm_peak, 4),
+                                            "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1),
+                                            "status": rra.STATUS_NAMES.get(st)}
+            del xs, ys
+            torch.cuda.empty_cache()
+    return {"algo": "twoshot_dbuf", "nranks": n, "dtype": "fp32", "bytes": "2*N*M per call", "sizes": out,
+            "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events"}
+
+
+def end_to_end(comm, rra, cases, best, torch, args):
+    """Host buffers in and out through rra_allreduce_host (pinned memory)."""
+    from latency_barrier_free_gb300 import inputs
+
+    reps = max(3, args.inner // 4)
+    per = []
+    h2d = d2h = 0
+    for dt, size in cases:
+        count = size // ELEM[dt]
+        src = inputs.workload2(size, dt)
+        tdt = torch.float32 if dt == "fp32" else torch.bfloat16
+        hs = [torch.from_numpy(s.view(np.int16) if dt == "bf16" else s).view(tdt).pin_memory() for s in src]
+        hr = [torch.empty_like(h).pin_memory() for h in hs]
+        sp = [h.data_ptr() for h in hs]
+        rp = [h.data_ptr() for h in hr]
+        comm.allreduce_host(sp, rp, count, dt, best[(dt, size)])
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            comm.allreduce_host(sp, rp, count, dt, best[(dt, size)])
+        per.append((time.perf_counter() - t0) / reps * 1e6)
+        h2d += NRANKS * size
+        d2h += NRANKS * size
+    return {"value": round(float(np.mean(per)), 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "api": "rra_allreduce_host (pinned host buffers, sync per call)",
+            "per_case_us": [round(x, 2) for x in per]}
+
+
+def decode_graph(rra, torch):
+    """N=8, bfloat16 [batch, 8192], 160 AllReduces per token captured in one
+    CUDA graph; microseconds per AllReduce = replay time / 160."""
+    from latency_barrier_free_gb300 import inputs
+
+    out = {}
+    n, calls = 8, inputs.W3_CALLS_PER_TOKEN
+    for batch in inputs.W3_BATCHES:
+        count = batch * inputs.W3_HIDDEN
+        with rra.Comm(n, count * 2) as c:
+            xs = [torch.randn(count, device="cuda").to(torch.bfloat16) for _ in range(n)]
+            ys = [torch.empty_like(x) for x in xs]
+            for algo in ("oneshot_ll", "twoshot_dbuf"):
+                c.allreduce(xs, ys, algo)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        for _ in range(calls):
+                            c.allreduce(xs, ys, algo)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 10
+                e0.record()
+                for _ in range(reps):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                out["B%d/%s" % (batch, algo)] = round(e0.elapsed_time(e1) * 1000.0 / (reps * calls), 3)
+                assert c.status()[0] == rra.OK
+    return {"us_per_allreduce": out, "calls_per_graph": calls}
+
+
+# ------------------------------------------------------- CPU baseline ----
+def cpu_sweep(seconds_budget: float, threads: int):
+    """Times the oracle over the sweep cases; returns (mean us/call, reps)."""
+    import oracle
+    from latency_barrier_free_gb300 import inputs
+
+    cases = sweep_cases()
+    data = {c: inputs.workload2(c[1], c[0]) for c in cases}
+    outs = {c: [np.empty_like(a) for a in data[c]] for c in cases}
+    for c in cases:  # warm-up
+        oracle.allreduce_mt(data[c], c[0], threads, recvs=outs[c])
+    per = {c: [] for c in cases}
+    t_start = time.perf_counter()
+    reps = 0
+    while True:
+        for c in cases:
+            t0 = time.perf_counter()
+            oracle.allreduce_mt(data[c], c[0], threads, recvs=outs[c])
+            per[c].append((time.perf_counter() - t0) * 1e6)
+        reps += 1
+        if time.perf_counter() - t_start > seconds_budget and reps >= 3:
+            break
+    us = [float(np.median(per[c])) for c in cases]
+    return float(np.mean(us)), reps
+
+
+def cpu_baseline(seconds_budget: float):
+    threads = os.cpu_count() or 1
+    v, reps = cpu_sweep(seconds_budget, threads)
+    return {"value": round(v, 3), "unit": "us/call", "cores": threads, "kind": "oracle",
+            "sample": "the 28-case sweep (N=4, 14 sizes x fp32/bf16), %d repetitions, median per case, "
+                      "element range split over %d host threads" % (reps, threads)}
+
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    vals = []
+    for _ in range(args.warmup):
+        cpu_sweep(0.0, threads)
+    for _ in range(args.steps):
+        v, _ = cpu_sweep(0.0, threads)
+        vals.append(v)
+    el = time.perf_counter() - t0
+    value = float(np.median(vals))
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "us/call", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / max(1, args.steps + args.warmup) * 1000, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32+bf16",
+        "data": "synthetic (seeded N(0,1), no dataset)", "impl": "reference",
+        "config": {"workload": WORKLOAD, "nranks": NRANKS, "what": "the CPU oracle (no reference code exists)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "us/call", "cores": threads, "kind": "oracle",
+                         "sample": "one pass over the 28-case sweep per step"},
+        "e2e": {"value": round(value, 3), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--inner", type=int, default=16, help="back-to-back calls per (dtype, size, algo)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-big", dest="big", action="store_false", help="skip the 512 MiB bandwidth case")
+    ap.add_argument("--no-decode", dest="decode", action="store_false", help="skip the decode graph case")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()
