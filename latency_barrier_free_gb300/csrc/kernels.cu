@@ -43,10 +43,10 @@ __device__ __forceinline__ char* window(const Params& p, int r) {
 // Input vector `vec` of a rank's buffer; elements at or beyond `count` read
 // as zero (never the sentinel).
 template <typename T>
-__device__ __forceinline__ uint4 load_input(const void* base, uint64_t vec, uint64_t count) {
+__device__ __forceinline__ uint4 load_input(const void* base, uint32_t vec, uint64_t count) {
     constexpr int VE = VecMath<T>::kElems;
-    const uint64_t e0 = vec * VE;
-    if (e0 + VE <= count) return ld_input_v4((const char*)base + vec * kVecBytes);
+    const uint64_t e0 = (uint64_t)vec * VE;
+    if (e0 + VE <= count) return ld_input_v4((const char*)base + (uint64_t)vec * kVecBytes);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     const int n = (int)(count - e0);
     if (sizeof(T) == 2) {
@@ -64,11 +64,11 @@ __device__ __forceinline__ uint4 load_input(const void* base, uint64_t vec, uint
 
 // Output vector `vec`; only elements below `count` are written.
 template <typename T>
-__device__ __forceinline__ void store_output(void* base, uint64_t vec, uint64_t count, uint4 v) {
+__device__ __forceinline__ void store_output(void* base, uint32_t vec, uint64_t count, uint4 v) {
     constexpr int VE = VecMath<T>::kElems;
-    const uint64_t e0 = vec * VE;
+    const uint64_t e0 = (uint64_t)vec * VE;
     if (e0 + VE <= count) {
-        st_output_v4((char*)base + vec * kVecBytes, v);
+        st_output_v4((char*)base + (uint64_t)vec * kVecBytes, v);
         return;
     }
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -94,51 +94,44 @@ struct CtaState {
     bool drop;       // injected fault: do not store to peers
 };
 
+// Every thread reads the control words itself (one broadcast line per warp),
+// so the first input loads overlap this round trip instead of waiting behind
+// a block barrier.  The barrier sits in the epilogue instead: no thread may
+// overwrite epoch slot b before every thread of the CTA has read it.
 __device__ __forceinline__ CtaState cta_prologue(const Params& p) {
-    __shared__ uint64_t s_epoch;
-    __shared__ int s_flags;
     CtaState s;
     s.t_start = globaltimer_ns();
     s.rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
     s.sub = (int)(blockIdx.x % (unsigned)p.ctas_per_rank);
-    if (threadIdx.x == 0) {
-        if (p.timing != nullptr) p.timing[2 * blockIdx.x] = s.t_start;
-        const uint64_t e = *(volatile const uint64_t*)&p.ctrl->epoch[blockIdx.x];
-        int flags = 0;
-        if (ld_relaxed_u32(&p.ctrl->status) != 0u) flags |= 1;
-        // 32-bit LL flags must not wrap inside the live window of epochs.
-        if ((e & 0xFFFFFFFFull) + (uint64_t)p.nsteps + 2ull > 0xFFFFFFFFull) {
-            record_error(p.ctrl, RRA_ERR_EPOCH, s.rank, 0);
-            flags |= 1;
-        }
-        if (*(volatile const int32_t*)&p.ctrl->drop_rank == s.rank) flags |= 2;
-        s_epoch = e;
-        s_flags = flags;
+    if (threadIdx.x == 0 && p.timing != nullptr) p.timing[2 * blockIdx.x] = s.t_start;
+    s.epoch = ld_relaxed_u64(&p.ctrl->epoch[blockIdx.x]);
+    const uint32_t status = ld_relaxed_u32(&p.ctrl->status);
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    s.skip = status != 0u;
+    // 32-bit LL flags must not wrap inside the live window of epochs.
+    if ((s.epoch & 0xFFFFFFFFull) + (uint64_t)p.nsteps + 2ull > 0xFFFFFFFFull) {
+        if (threadIdx.x == 0) record_error(p.ctrl, RRA_ERR_EPOCH, s.rank, 0);
+        s.skip = true;
     }
-    __syncthreads();
-    s.epoch = s_epoch;
-    s.skip = (s_flags & 1) != 0;
-    s.drop = (s_flags & 2) != 0;
+    s.drop = drop == s.rank;
     return s;
 }
 
 __device__ __forceinline__ void cta_epilogue(const Params& p, const CtaState& s) {
+    __syncthreads();  // every thread has read its epoch slot
     if (!s.skip) {
         // Advance every epoch slot this CTA owns: slots b, b + G, b + 2G, ...
         const uint64_t next = s.epoch + p.nsteps;
         const unsigned G = gridDim.x;
         for (unsigned slot = blockIdx.x + threadIdx.x * G; slot < (unsigned)p.epoch_slots;
              slot += blockDim.x * G) {
-            *(volatile uint64_t*)&p.ctrl->epoch[slot] = next;
+            st_relaxed_u64(&p.ctrl->epoch[slot], next);
         }
     }
-    if (p.timing != nullptr) {
-        __syncthreads();
-        if (threadIdx.x == 0) p.timing[2 * blockIdx.x + 1] = globaltimer_ns();
-    }
+    if (p.timing != nullptr && threadIdx.x == 0) p.timing[2 * blockIdx.x + 1] = globaltimer_ns();
 }
 
-constexpr int kBatch = 8;  // sources polled with loads in flight at once
+constexpr int kBatch = 4;  // sources polled with loads in flight at once
 
 // Poll one scratch vector once.  LL: both LL lines carry `ep` in all four
 // flags.  Sentinel: no atomic unit still holds the sentinel.
@@ -149,6 +142,30 @@ __device__ __forceinline__ bool poll_once(const char* slot_pos, uint32_t ep, uin
     return sentinel_arrived<VecMath<T>::kUnitBytes>(out);
 }
 
+// Poll the slots of sources q0 .. q0+kBatch-1 (skipping `skip` and sources at
+// or beyond n) with all loads in flight, then spin on the ones not yet
+// arrived.  Returns false if the wait gave up.
+template <typename T, bool kLL>
+__device__ __forceinline__ bool poll_batch(const char* slot0, uint64_t slot_stride, int q0, int n, int skip,
+                                           uint32_t ep, Waiter& w, uint4 (&val)[kBatch]) {
+    bool ok[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+        const int q = q0 + j;
+        ok[j] = true;
+        if (q < n && q != skip) ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * slot_stride, ep, val[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+        const int q = q0 + j;
+        while (!ok[j]) {
+            if (waiter_expired(w)) return false;
+            ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * slot_stride, ep, val[j]);
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------- one-shot (push) ----
 // Sec. III-A "One-shot" in push mode + Sec. IV "LL" / "Sentinel"; the
 // bcast() of Fig. 9: each rank stores its chunk into every peer's slot, then
@@ -157,58 +174,47 @@ template <typename T, bool kLL>
 __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s) {
     using M = VecMath<T>;
     constexpr int U = M::kUnitBytes;
-    constexpr uint64_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
+    constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
     const int N = p.nranks, r = s.rank;
-    const uint64_t pos0 = (uint64_t)s.sub * p.per_cta;
-    const uint64_t pos1 = pos0 + p.per_cta;
+    const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
+    const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r) + p.region_off;
     Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
 
+#pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
         const uint64_t e = s.epoch + k;
         const uint32_t ep = (uint32_t)e;
         const uint64_t par_off = (e & 1ull) * p.parity_bytes;
-        const uint64_t base = (uint64_t)k * p.chunk_vecs;
-        const uint64_t nv = min(p.chunk_vecs, p.nvec - base);
-        const uint64_t end = min(pos1, nv);
+        const uint32_t base = k * p.chunk_vecs;
+        const uint32_t end = min(pos1, min(p.chunk_vecs, p.nvec - base));
         w.step = (int)k;
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
         // push: my chunk into slot [parity][r] of every peer
         if (!s.drop) {
-            for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+#pragma unroll 1
+            for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
                 const uint4 x = load_input<T>(p.send[r], base + v, p.count);
-                const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + v * kPosBytes;
-                for (int q = 0; q < N; ++q) {
+                char* dst = p.win0 + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kPosBytes;
+#pragma unroll 1
+                for (int q = 0; q < N; ++q, dst += p.stride) {
                     if (q == r) continue;
-                    char* dst = window(p, q) + off;
                     if (kLL) ll_store(dst, x, ep);
                     else st_scratch<U>(dst, x);
                 }
             }
         }
         // receive: poll the N-1 incoming slots, reduce in rank order
-        for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+#pragma unroll 1
+        for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
             const uint4 own = load_input<T>(p.send[r], base + v, p.count);
-            const char* const slot0 = mine + par_off + v * kPosBytes;
+            char* const slot0 = mine + par_off + (uint64_t)v * kPosBytes;
             typename M::Acc acc;
+#pragma unroll 1
             for (int q0 = 0; q0 < N; q0 += kBatch) {
                 uint4 val[kBatch];
-                bool ok[kBatch];
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    ok[j] = true;
-                    if (q < N && q != r) ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * p.slot_bytes, ep, val[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    while (!ok[j]) {
-                        if (waiter_expired(w)) return false;
-                        ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * p.slot_bytes, ep, val[j]);
-                    }
-                }
+                if (!poll_batch<T, kLL>(slot0, p.slot_bytes, q0, N, r, ep, w, val)) return false;
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int q = q0 + j;
@@ -216,14 +222,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
                     const uint4 x = (q == r) ? own : val[j];
                     if (q == 0) acc = M::load(x);
                     else M::add(acc, x);
-                }
-                if (!kLL) {
-#pragma unroll
-                    for (int j = 0; j < kBatch; ++j) {
-                        const int q = q0 + j;
-                        if (q < N && q != r)
-                            st_scratch<U>((char*)slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                    }
+                    if (!kLL && q != r) st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
                 }
             }
             store_output<T>(p.recv[r], base + v, p.count, M::store(acc));
@@ -248,26 +247,24 @@ __global__ void __launch_bounds__(512) oneshot_kernel(const __grid_constant__ Pa
 // the result into every peer's AG slot [parity][owner] and its own output.
 // AG: every rank polls the N-1 AG slots and writes its output.
 struct Split {
-    uint64_t base;  // first vector of the step
-    uint64_t part;  // vectors per partition in this step
-    uint64_t rem;   // vectors left from `base` to the end of the message
-    __device__ __forceinline__ uint64_t valid(int q) const {  // vectors of partition q
-        const uint64_t lo = (uint64_t)q * part;
-        return rem > lo ? min(part, rem - lo) : 0ull;
+    uint32_t base;  // first vector of the step
+    uint32_t part;  // vectors per partition in this step
+    uint32_t rem;   // vectors left from `base` to the end of the message
+    __device__ __forceinline__ uint32_t valid(int q) const {  // vectors of partition q
+        const uint32_t lo = (uint32_t)q * part;
+        return rem > lo ? min(part, rem - lo) : 0u;
     }
-    __device__ __forceinline__ uint64_t vec(int q, uint64_t v) const {
-        return base + (uint64_t)q * part + v;
-    }
+    __device__ __forceinline__ uint32_t vec(int q, uint32_t v) const { return base + (uint32_t)q * part + v; }
 };
 
 // The last step shrinks its partitions so the remaining vectors spread over
 // all owners; positions stay a prefix of the full-step positions.
 __device__ __forceinline__ Split split_step(const Params& p, uint32_t k) {
     Split sp;
-    const uint64_t full = (uint64_t)p.nranks * p.chunk_vecs;
-    sp.base = (uint64_t)k * full;
+    const uint32_t full = (uint32_t)p.nranks * p.chunk_vecs;
+    sp.base = k * full;
     sp.rem = p.nvec - sp.base;
-    sp.part = sp.rem >= full ? p.chunk_vecs : (sp.rem + p.nranks - 1) / p.nranks;
+    sp.part = sp.rem >= full ? p.chunk_vecs : (sp.rem + (uint32_t)p.nranks - 1u) / (uint32_t)p.nranks;
     return sp;
 }
 
@@ -276,57 +273,43 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
     using M = VecMath<T>;
     constexpr int U = M::kUnitBytes;
     const int N = p.nranks, r = s.rank;
-    const uint64_t pos0 = (uint64_t)s.sub * p.per_cta;
-    const uint64_t pos1 = pos0 + p.per_cta;
+    const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
+    const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r);
     Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
 
+#pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
         const uint64_t e = s.epoch + k;
         const uint64_t par_off = (e & 1ull) * p.parity_bytes;
         const Split sp = split_step(p, k);
-        const uint64_t end = min(pos1, sp.part);
+        const uint32_t end = min(pos1, sp.part);
         w.step = (int)k;
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
         // ReduceScatter push: part q of my input -> owner q's RS slot [r]
         if (!s.drop) {
-            for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
-                const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + v * kVecBytes;
-                for (int q = 0; q < N; ++q) {
+#pragma unroll 1
+            for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+                char* dst = p.win0 + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+#pragma unroll 1
+                for (int q = 0; q < N; ++q, dst += p.stride) {
                     if (q == r || v >= sp.valid(q)) continue;
-                    const uint4 x = load_input<T>(p.send[r], sp.vec(q, v), p.count);
-                    st_scratch<U>(window(p, q) + off, x);
+                    st_scratch<U>(dst, load_input<T>(p.send[r], sp.vec(q, v), p.count));
                 }
             }
         }
         // Owner: reduce my partition in rank order, push it to every AG slot
-        const uint64_t my_valid = sp.valid(r);
-        for (uint64_t v = pos0 + threadIdx.x; v < end && v < my_valid; v += blockDim.x) {
+        const uint32_t my_end = min(end, sp.valid(r));
+#pragma unroll 1
+        for (uint32_t v = pos0 + threadIdx.x; v < my_end; v += blockDim.x) {
             const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
-            const char* const slot0 = mine + p.region_off + par_off + v * kVecBytes;
+            char* const slot0 = mine + p.region_off + par_off + (uint64_t)v * kVecBytes;
             typename M::Acc acc;
+#pragma unroll 1
             for (int q0 = 0; q0 < N; q0 += kBatch) {
                 uint4 val[kBatch];
-                bool ok[kBatch];
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    ok[j] = true;
-                    if (q < N && q != r) {
-                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
-                        ok[j] = sentinel_arrived<U>(val[j]);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    while (!ok[j]) {
-                        if (waiter_expired(w)) return false;
-                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
-                        ok[j] = sentinel_arrived<U>(val[j]);
-                    }
-                }
+                if (!poll_batch<T, false>(slot0, p.slot_bytes, q0, N, r, 0u, w, val)) return false;
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int q = q0 + j;
@@ -334,28 +317,27 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
                     const uint4 x = (q == r) ? own : val[j];
                     if (q == 0) acc = M::load(x);
                     else M::add(acc, x);
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    if (q < N && q != r)
-                        st_scratch<U>((char*)slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    if (q != r) st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
                 }
             }
             const uint4 red = M::store(acc);
             if (!s.drop) {
-                const uint64_t off = p.aux_off + par_off + (uint64_t)r * p.slot_bytes + v * kVecBytes;
-                for (int q = 0; q < N; ++q) {
-                    if (q == r) continue;
-                    st_scratch<U>(window(p, q) + off, red);
+                char* dst = p.win0 + p.aux_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+#pragma unroll 1
+                for (int q = 0; q < N; ++q, dst += p.stride) {
+                    if (q != r) st_scratch<U>(dst, red);
                 }
             }
             store_output<T>(p.recv[r], sp.vec(r, v), p.count, red);
         }
         // AllGather receive: the N-1 reduced partitions of the other owners
-        for (uint64_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
-            const char* const slot0 = mine + p.aux_off + par_off + v * kVecBytes;
+#pragma unroll 1
+        for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+            char* const slot0 = mine + p.aux_off + par_off + (uint64_t)v * kVecBytes;
+#pragma unroll 1
             for (int q0 = 0; q0 < N; q0 += kBatch) {
+                // sources whose partition does not reach position v are skipped
+                // by polling them as if they were the caller itself
                 uint4 val[kBatch];
                 bool ok[kBatch];
 #pragma unroll
@@ -381,7 +363,7 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
                     const int q = q0 + j;
                     if (q < N && q != r && v < sp.valid(q)) {
                         store_output<T>(p.recv[r], sp.vec(q, v), p.count, val[j]);
-                        st_scratch<U>((char*)slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                        st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
                     }
                 }
             }
@@ -409,7 +391,8 @@ __global__ void __launch_bounds__(512) twoshot_kernel(const __grid_constant__ Pa
 // atomics are per element, so a contributor warp first issues all its
 // red.add operations for a group of 32 vectors, synchronises the warp, and
 // every lane issues fence.acq_rel.gpu before the counter increments (release);
-// the owner reads the counter, then fences (acquire) before reading the lines.
+// the owner's lane 0 reads the counter, fences (acquire) and synchronises the
+// warp before the lanes read the lines.
 template <typename T>
 struct Acc128;
 template <>
@@ -476,69 +459,77 @@ struct Acc128<double> {         // binary64 -> binary64 accumulators
 template <typename T>
 __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
     using A = Acc128<T>;
-    constexpr uint64_t kAccBytes = (uint64_t)kVecBytes * A::kRatio;
+    constexpr uint32_t kAccBytes = (uint32_t)kVecBytes * A::kRatio;
     const int N = p.nranks, r = s.rank;
-    const unsigned lane = threadIdx.x & 31u;
-    const uint64_t pos0 = (uint64_t)s.sub * p.per_cta;   // per_cta is a multiple of 32
-    const uint64_t pos1 = pos0 + p.per_cta;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t wbase = threadIdx.x - lane;               // first thread of this warp
+    const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;       // per_cta is a multiple of 32
+    const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r);
     Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
     const uint32_t target = (uint32_t)(N - 1);
 
+#pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
         const uint64_t e = s.epoch + k;
         const uint32_t ep = (uint32_t)e;
         const uint64_t par = e & 1ull;
         const Split sp = split_step(p, k);
-        const uint64_t end = min(pos1, sp.part);
+        const uint32_t end = min(pos1, sp.part);
         w.step = (int)k;
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
-        // ReduceScatter: atomic adds into each owner's accumulators.  The loop
-        // bound is warp-uniform (v - lane is the group start).
+        // ReduceScatter: atomic adds into each owner's accumulators.  Loop
+        // bounds use the warp's first position, so they are warp-uniform.
         if (!s.drop) {
-            for (uint64_t v = pos0 + threadIdx.x; v - lane < end; v += blockDim.x) {
-                for (int q = 0; q < N; ++q) {
+#pragma unroll 1
+            for (uint32_t g0 = pos0 + wbase; g0 < end; g0 += blockDim.x) {
+                const uint32_t v = g0 + lane;
+                char* dst = p.win0 + p.region_off + par * p.parity_bytes + (uint64_t)v * kAccBytes;
+#pragma unroll 1
+                for (int q = 0; q < N; ++q, dst += p.stride) {
                     if (q == r || v >= sp.valid(q)) continue;
-                    const uint4 x = load_input<T>(p.send[r], sp.vec(q, v), p.count);
-                    A::red(window(p, q) + p.region_off + par * p.parity_bytes + v * kAccBytes, x);
+                    A::red(dst, load_input<T>(p.send[r], sp.vec(q, v), p.count));
                 }
             }
             __syncwarp();
             fence_acq_rel_gpu();  // release: this warp's adds before its counter increments
-            for (uint64_t g0 = pos0 + (threadIdx.x - lane); g0 < end; g0 += blockDim.x) {
-                const uint64_t g = g0 / kGroupVecs;
+#pragma unroll 1
+            for (uint32_t g0 = pos0 + wbase; g0 < end; g0 += blockDim.x) {
+                const uint64_t coff = p.aux_off + par * p.aux_parity_bytes + (uint64_t)(g0 / kGroupVecs) * 4;
+#pragma unroll 1
                 for (int q = (int)lane; q < N; q += 32) {
                     if (q == r || g0 >= sp.valid(q)) continue;
-                    red_add_u32(window(p, q) + p.aux_off + par * p.aux_parity_bytes + g * 4, 1u);
+                    red_add_u32(window(p, q) + coff, 1u);
                 }
             }
         }
         // Owner: wait for each group's counter, consume, re-zero, AllGather push.
-        const uint64_t my_valid = sp.valid(r);
-        for (uint64_t g0 = pos0 + (threadIdx.x - lane); g0 < end && g0 < my_valid; g0 += blockDim.x) {
-            const uint64_t g = g0 / kGroupVecs;
-            char* const cnt = mine + p.aux_off + par * p.aux_parity_bytes + g * 4;
+        const uint32_t my_end = min(end, sp.valid(r));
+#pragma unroll 1
+        for (uint32_t g0 = pos0 + wbase; g0 < my_end; g0 += blockDim.x) {
+            char* const cnt = mine + p.aux_off + par * p.aux_parity_bytes + (uint64_t)(g0 / kGroupVecs) * 4;
             int give_up = 0;
             if (lane == 0) {
                 while (ld_relaxed_u32(cnt) != target) {
                     if (waiter_expired(w)) { give_up = 1; break; }
                 }
+                fence_acq_rel_gpu();  // acquire: the counter before the lines
             }
             if (__shfl_sync(0xFFFFFFFFu, give_up, 0)) return false;
-            fence_acq_rel_gpu();  // acquire: counter before the lines
-            const uint64_t v = g0 + lane;
-            if (v < my_valid) {
-                char* const acc = mine + p.region_off + par * p.parity_bytes + v * kAccBytes;
+            __syncwarp();
+            const uint32_t v = g0 + lane;
+            if (v < my_end) {
+                char* const acc = mine + p.region_off + par * p.parity_bytes + (uint64_t)v * kAccBytes;
                 const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
                 const uint4 red = A::finish(acc, own);
                 A::zero(acc);
                 if (!s.drop) {
-                    const uint64_t off = p.aux2_off + par * p.aux2_parity_bytes + (uint64_t)r * p.aux2_slot_bytes +
-                                         v * 2 * kVecBytes;
-                    for (int q = 0; q < N; ++q) {
-                        if (q == r) continue;
-                        ll_store(window(p, q) + off, red, ep);
+                    char* dst = p.win0 + p.aux2_off + par * p.aux2_parity_bytes + (uint64_t)r * p.aux2_slot_bytes +
+                                (uint64_t)v * (2 * kVecBytes);
+#pragma unroll 1
+                    for (int q = 0; q < N; ++q, dst += p.stride) {
+                        if (q != r) ll_store(dst, red, ep);
                     }
                 }
                 store_output<T>(p.recv[r], sp.vec(r, v), p.count, red);
@@ -548,10 +539,13 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
         }
         // AllGather receive (LL polls), per lane; the warp leaves together.
         int failed = 0;
-        for (uint64_t v = pos0 + threadIdx.x; v - lane < end; v += blockDim.x) {
+#pragma unroll 1
+        for (uint32_t g0 = pos0 + wbase; g0 < end; g0 += blockDim.x) {
+            const uint32_t v = g0 + lane;
             if (failed || v >= end) continue;
-            const char* const slot0 = mine + p.aux2_off + par * p.aux2_parity_bytes + v * 2 * kVecBytes;
-            for (int q0 = 0; q0 < N && !failed; q0 += kBatch) {
+            char* const slot0 = mine + p.aux2_off + par * p.aux2_parity_bytes + (uint64_t)v * (2 * kVecBytes);
+#pragma unroll 1
+            for (int q0 = 0; q0 < N; q0 += kBatch) {
                 uint4 val[kBatch];
                 bool ok[kBatch];
 #pragma unroll
@@ -564,10 +558,11 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int q = q0 + j;
-                    while (!ok[j] && !failed) {
+                    while (!ok[j]) {
                         if (waiter_expired(w)) { failed = 1; break; }
                         ok[j] = ll_load(slot0 + (uint64_t)q * p.aux2_slot_bytes, ep, val[j]);
                     }
+                    if (failed) break;
                 }
                 if (failed) break;
 #pragma unroll

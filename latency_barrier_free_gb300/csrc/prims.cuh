@@ -53,6 +53,12 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
     return v;
 }
 
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const void* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_u32(const void* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -73,6 +79,10 @@ __device__ __forceinline__ void st_relaxed_v2u64(void* p, uint64_t a, uint64_t b
 
 __device__ __forceinline__ void st_relaxed_u32(void* p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" : : "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u64(void* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" : : "l"(p), "l"(v) : "memory");
 }
 
 // Output vector: plain store.

@@ -118,7 +118,7 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
                              size_t scratch_twoshot, rra_layout_t* out) {
     if (out == nullptr || nranks < 2 || nranks > RRA_MAX_RANKS || max_bytes == 0)
         return RRA_ERR_INVALID_ARG;
-    if (max_bytes > (1ull << 40)) return RRA_ERR_INVALID_ARG;
+    if (max_bytes > rra::kMaxMessageBytes) return RRA_ERR_INVALID_ARG;
     const size_t cap_os = scratch_oneshot ? scratch_oneshot : kDefaultScratchOneshot;
     const size_t cap_ts = scratch_twoshot ? scratch_twoshot : kDefaultScratchTwoshot;
     const size_t n = (size_t)nranks;
@@ -323,7 +323,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     p->timing = c->timing;
     p->stride = L.window_stride;
     p->count = count;
-    p->nvec = ceil_div(count, ve);
+    p->nvec = (uint32_t)ceil_div(count, ve);
     p->timeout_ns = (uint64_t)c->timeout_ms * 1000000ull;
     p->nranks = c->nranks;
     p->epoch_slots = rra::kEpochSlots;
@@ -341,7 +341,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             size_t cap = (ll ? L.ll_chunk : L.os_chunk) / rra::kVecBytes;
             if (c->os_chunk > 0) cap = std::min(cap, std::max<size_t>(1, (size_t)c->os_chunk / rra::kVecBytes));
             const size_t chunk = std::min<size_t>(p->nvec, cap);
-            p->chunk_vecs = chunk;
+            p->chunk_vecs = (uint32_t)chunk;
             p->nsteps = (uint32_t)ceil_div(p->nvec, chunk);
             p->region_off = ll ? off_ll : off_os;
             p->slot_bytes = ll ? 2 * L.ll_chunk : L.os_chunk;
@@ -354,7 +354,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             if (c->ts_chunk > 0)
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->ts_chunk / rra::kVecBytes / n));
             const size_t part = std::min(ceil_div(p->nvec, n), cap);
-            p->chunk_vecs = part;
+            p->chunk_vecs = (uint32_t)part;
             p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
             p->region_off = off_ts;
             p->slot_bytes = L.ts_part;
@@ -369,7 +369,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->la_chunk / rra::kVecBytes / n));
             const size_t part = std::min(ceil_div(p->nvec, n), cap);
             const LaSizes s = la_sizes(L.la_part, c->nranks);
-            p->chunk_vecs = part;
+            p->chunk_vecs = (uint32_t)part;
             p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
             p->region_off = off_la;
             p->parity_bytes = s.acc_parity;
@@ -391,7 +391,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     if (algo == RRA_LL128_ATOMIC) per = align_up(per, rra::kGroupVecs);
     ctas = (int64_t)ceil_div(work, per);
     p->ctas_per_rank = (int32_t)ctas;
-    p->per_cta = per;
+    p->per_cta = (uint32_t)per;
     return RRA_OK;
 }
 

@@ -15,6 +15,7 @@ constexpr int kVecBytes = 16;          // every transfer unit is one 16-byte vec
 constexpr int kEpochSlots = 4096;      // largest grid a communicator may launch
 constexpr int kGroupVecs = 32;         // LL128-atomic: vectors per completion counter (one warp)
 constexpr size_t kRegionAlign = 4096;
+constexpr uint64_t kMaxMessageBytes = (1ull << 36) - 16;  // 16-byte vector indices fit in 32 bits
 
 // Control block at the start of the allocation (before window 0).
 struct Ctrl {
@@ -39,7 +40,6 @@ struct Params {
     uint64_t* timing;      // optional: (start, end) %globaltimer per CTA
     uint64_t stride;       // bytes between windows
     uint64_t count;        // elements per rank
-    uint64_t nvec;         // 16-byte vectors per rank = ceil(count / elems per vector)
     uint64_t timeout_ns;   // limit of every wait
     uint64_t region_off;   // offset of the algorithm's region inside a window
     uint64_t slot_bytes;   // bytes of one (parity, source) slot
@@ -49,9 +49,10 @@ struct Params {
     uint64_t aux_parity_bytes;   // LL128: bytes of one parity of counters
     uint64_t aux2_slot_bytes;    // LL128: bytes of one AllGather slot
     uint64_t aux2_parity_bytes;  // LL128: bytes of one AllGather parity
-    uint64_t chunk_vecs;   // one-shot: vectors per rank per full step;
+    uint32_t nvec;         // 16-byte vectors per rank = ceil(count / elems per vector)
+    uint32_t chunk_vecs;   // one-shot: vectors per rank per full step;
                            // two-shot/LL128: vectors per partition per full step
-    uint64_t per_cta;      // vectors per CTA per step (the same in every step)
+    uint32_t per_cta;      // vectors per CTA per step (the same in every step)
     uint32_t nsteps;
     int32_t nranks;
     int32_t ctas_per_rank;
