@@ -231,10 +231,122 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
     return true;
 }
 
+// Wide variant for many ranks: the threads of a CTA split the (source,
+// position) items of both the push and the poll, so a position's N-1 sources
+// are polled by different threads at once (one round trip instead of N/4).
+// Polled vectors are staged raw in shared memory; one thread per position
+// then adds the N values in rank order, so the result is the same bit pattern
+// as the narrow variant.  Positions are processed in rounds of `R` so the
+// stage fits.  A thread that gives up raises a shared flag; the whole CTA
+// leaves at the next block barrier.
+constexpr int kStageVecs = 3072;  // 48 KiB of shared memory
+
+template <typename T, bool kLL>
+__device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaState& s, uint4* stage, int* fail) {
+    using M = VecMath<T>;
+    constexpr int U = M::kUnitBytes;
+    constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
+    const int N = p.nranks, r = s.rank;
+    const uint32_t T_ = blockDim.x;
+    const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
+    const uint32_t pos1 = pos0 + p.per_cta;
+    const uint32_t R = (uint32_t)(kStageVecs / N);
+    char* const mine = window(p, r) + p.region_off;
+    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+
+#pragma unroll 1
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint32_t ep = (uint32_t)e;
+        const uint64_t par_off = (e & 1ull) * p.parity_bytes;
+        const uint32_t base = k * p.chunk_vecs;
+        const uint32_t end = min(pos1, min(p.chunk_vecs, p.nvec - base));
+        const uint32_t npos = end > pos0 ? end - pos0 : 0u;
+        w.step = (int)k;
+        if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
+
+        // push: item i = (peer q = i / npos, position pos0 + i % npos)
+        if (!s.drop) {
+            const uint32_t items = npos * (uint32_t)N;
+#pragma unroll 1
+            for (uint32_t i = threadIdx.x; i < items; i += T_) {
+                const int q = (int)(i / npos);
+                if (q == r) continue;
+                const uint32_t v = pos0 + i % npos;
+                const uint4 x = load_input<T>(p.send[r], base + v, p.count);
+                char* dst = window(p, q) + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kPosBytes;
+                if (kLL) ll_store(dst, x, ep);
+                else st_scratch<U>(dst, x);
+            }
+        }
+#pragma unroll 1
+        for (uint32_t r0 = pos0; r0 < end; r0 += R) {
+            const uint32_t rn = min(R, end - r0);
+            const uint32_t items = rn * (uint32_t)N;
+            // poll: item i = (source q = i / rn, position r0 + i % rn), kBatch in flight
+#pragma unroll 1
+            for (uint32_t i0 = threadIdx.x; i0 < items; i0 += kBatch * T_) {
+                uint4 val[kBatch];
+                bool ok[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const uint32_t i = i0 + (uint32_t)j * T_;
+                    ok[j] = true;
+                    if (i < items) {
+                        const int q = (int)(i / rn);
+                        const uint32_t v = r0 + i % rn;
+                        if (q == r) val[j] = load_input<T>(p.send[r], base + v, p.count);
+                        else ok[j] = poll_once<T, kLL>(mine + par_off + (uint64_t)q * p.slot_bytes +
+                                                           (uint64_t)v * kPosBytes, ep, val[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const uint32_t i = i0 + (uint32_t)j * T_;
+                    if (i >= items) break;
+                    const int q = (int)(i / rn);
+                    const uint32_t v = r0 + i % rn;
+                    const char* slot = mine + par_off + (uint64_t)q * p.slot_bytes + (uint64_t)v * kPosBytes;
+                    while (!ok[j] && *(volatile int*)fail == 0) {
+                        if (waiter_expired(w)) { *(volatile int*)fail = 1; break; }
+                        ok[j] = poll_once<T, kLL>(slot, ep, val[j]);
+                    }
+                    if (!ok[j]) break;
+                    stage[(uint32_t)q * R + (i % rn)] = val[j];
+                    if (!kLL && q != r) st_scratch<U>((char*)slot, sentinel_vec());
+                }
+            }
+            __syncthreads();
+            if (*(volatile int*)fail) return false;
+            // reduce: one thread per position, sources in rank order
+#pragma unroll 1
+            for (uint32_t vl = threadIdx.x; vl < rn; vl += T_) {
+                typename M::Acc acc = M::load(stage[vl]);
+#pragma unroll 1
+                for (int q = 1; q < N; ++q) M::add(acc, stage[(uint32_t)q * R + vl]);
+                store_output<T>(p.recv[r], base + r0 + vl, p.count, M::store(acc));
+            }
+            __syncthreads();
+        }
+    }
+    return true;
+}
+
 template <typename T, bool kLL>
 __global__ void __launch_bounds__(512) oneshot_kernel(const __grid_constant__ Params p) {
     const CtaState s = cta_prologue(p);
     if (!s.skip) (void)oneshot_body<T, kLL>(p, s);
+    cta_epilogue(p, s);
+}
+
+template <typename T, bool kLL>
+__global__ void __launch_bounds__(512) oneshot_wide_kernel(const __grid_constant__ Params p) {
+    __shared__ uint4 stage[kStageVecs];
+    __shared__ int fail;
+    if (threadIdx.x == 0) fail = 0;
+    __syncthreads();
+    const CtaState s = cta_prologue(p);
+    if (!s.skip) (void)oneshot_wide_body<T, kLL>(p, s, stage, &fail);
     cta_epilogue(p, s);
 }
 
@@ -626,34 +738,35 @@ __global__ void init_kernel(const __grid_constant__ InitParams ip) {
 
 // --------------------------------------------------------- host launch ----
 template <typename T>
-static const void* kernel_for(rra_algo_t algo) {
-    switch (algo) {
-        case RRA_ONESHOT_LL: return (const void*)oneshot_kernel<T, true>;
-        case RRA_ONESHOT_SENTINEL: return (const void*)oneshot_kernel<T, false>;
-        case RRA_TWOSHOT_DBUF: return (const void*)twoshot_kernel<T>;
-        case RRA_LL128_ATOMIC: return (const void*)ll128_kernel<T>;
+static const void* kernel_for(int kind) {
+    switch (kind) {
+        case kKindOneshotLL: return (const void*)oneshot_kernel<T, true>;
+        case kKindOneshotSentinel: return (const void*)oneshot_kernel<T, false>;
+        case kKindTwoshot: return (const void*)twoshot_kernel<T>;
+        case kKindLL128: return (const void*)ll128_kernel<T>;
+        case kKindOneshotLLWide: return (const void*)oneshot_wide_kernel<T, true>;
+        case kKindOneshotSentinelWide: return (const void*)oneshot_wide_kernel<T, false>;
     }
     return nullptr;
 }
 
-static const void* kernel_for(rra_dtype_t dtype, rra_algo_t algo) {
+static const void* kernel_for(rra_dtype_t dtype, int kind) {
     switch (dtype) {
-        case RRA_FP32: return kernel_for<float>(algo);
-        case RRA_BF16: return kernel_for<__nv_bfloat16>(algo);
-        case RRA_FP64: return kernel_for<double>(algo);
+        case RRA_FP32: return kernel_for<float>(kind);
+        case RRA_BF16: return kernel_for<__nv_bfloat16>(kind);
+        case RRA_FP64: return kernel_for<double>(kind);
     }
     return nullptr;
 }
 
-cudaError_t occupancy(rra_dtype_t dtype, rra_algo_t algo, int threads, int* blocks_per_sm) {
-    const void* k = kernel_for(dtype, algo);
+cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm) {
+    const void* k = kernel_for(dtype, kind);
     if (k == nullptr) return cudaErrorInvalidValue;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, threads, 0);
 }
 
-cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, rra_algo_t algo, int threads,
-                             cudaStream_t stream) {
-    const void* k = kernel_for(dtype, algo);
+cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream) {
+    const void* k = kernel_for(dtype, kind);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.nranks * p.ctas_per_rank));

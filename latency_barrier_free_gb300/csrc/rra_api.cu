@@ -86,7 +86,8 @@ struct rra_comm {
     int64_t ctas_per_rank = 0;
     int64_t timeout_ms = 1000;
     int64_t ts_chunk = 0, la_chunk = 0, os_chunk = 0;
-    int blocks_per_sm[3][4];  // by dtype, algo; -1 = not queried (for `threads`)
+    int blocks_per_sm[3][rra::kNumKinds];  // by dtype, kernel kind; -1 = not queried
+    int64_t oneshot_wide = -1;              // -1 auto (N >= 16), 0 never, 1 always
     bool poisoned = false;
     uint64_t* timing = nullptr;
     // rra_allreduce_host staging (allocated on first use)
@@ -153,11 +154,11 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
     return RRA_OK;
 }
 
-static rra_status_t query_blocks(rra_comm* c, rra_dtype_t d, rra_algo_t a, int* out) {
-    int& b = c->blocks_per_sm[d][a];
+static rra_status_t query_blocks(rra_comm* c, rra_dtype_t d, int kind, int* out) {
+    int& b = c->blocks_per_sm[d][kind];
     if (b < 0) {
         int v = 0;
-        if (rra::occupancy(d, a, c->threads, &v) != cudaSuccess) return RRA_ERR_CUDA;
+        if (rra::occupancy(d, kind, c->threads, &v) != cudaSuccess) return RRA_ERR_CUDA;
         b = v;
     }
     *out = b;
@@ -198,11 +199,11 @@ rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out) {
         delete c;
         return RRA_ERR_CUDA;
     }
-    // Every algorithm must fit at least one CTA per rank at once.
+    // Every kernel must fit at least one CTA per rank at once.
     for (int d = 0; d < 3; ++d) {
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < rra::kNumKinds; ++a) {
             int b = 0;
-            if (query_blocks(c, (rra_dtype_t)d, (rra_algo_t)a, &b) != RRA_OK) {
+            if (query_blocks(c, (rra_dtype_t)d, a, &b) != RRA_OK) {
                 delete c;
                 return RRA_ERR_CUDA;
             }
@@ -278,6 +279,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < 0 || v % 16) return RRA_ERR_INVALID_ARG;
             c->os_chunk = v;
             return RRA_OK;
+        case RRA_ATTR_ONESHOT_WIDE:
+            if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->oneshot_wide = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -291,29 +296,44 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_TWOSHOT_CHUNK: *v = c->ts_chunk; return RRA_OK;
         case RRA_ATTR_LL128_CHUNK: *v = c->la_chunk; return RRA_OK;
         case RRA_ATTR_ONESHOT_CHUNK: *v = c->os_chunk; return RRA_OK;
+        case RRA_ATTR_ONESHOT_WIDE: *v = c->oneshot_wide; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
 
-rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, int* ctas) {
-    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a)) return RRA_ERR_INVALID_ARG;
+static int kernel_kind(const rra_comm* c, rra_algo_t algo) {
+    if (algo == RRA_ONESHOT_LL || algo == RRA_ONESHOT_SENTINEL) {
+        const bool wide = c->oneshot_wide == 1 || (c->oneshot_wide < 0 && c->nranks >= 16);
+        if (wide) return algo == RRA_ONESHOT_LL ? rra::kKindOneshotLLWide : rra::kKindOneshotSentinelWide;
+    }
+    return (int)algo;
+}
+
+static rra_status_t max_ctas_kind(rra_comm* c, rra_dtype_t d, int kind, int* ctas) {
     int b = 0;
-    rra_status_t st = query_blocks(c, d, a, &b);
+    rra_status_t st = query_blocks(c, d, kind, &b);
     if (st != RRA_OK) return st;
     *ctas = std::min(b * c->sm_count, rra::kEpochSlots);
     return RRA_OK;
 }
 
+rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, int* ctas) {
+    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a)) return RRA_ERR_INVALID_ARG;
+    return max_ctas_kind(c, d, kernel_kind(c, a), ctas);
+}
+
 // Fills everything in Params except the pointer tables.
 static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo,
-                              Params* p) {
+                              Params* p, int* kind_out) {
     const size_t es = elem_size(dtype);
     const size_t ve = rra::kVecBytes / es;
     const size_t n = (size_t)c->nranks;
     const rra_layout_t& L = c->lay;
+    const int kind = kernel_kind(c, algo);
     int max_ctas = 0;
-    rra_status_t st = rra_comm_max_coresident(c, dtype, algo, &max_ctas);
+    rra_status_t st = max_ctas_kind(c, dtype, kind, &max_ctas);
     if (st != RRA_OK) return st;
+    *kind_out = kind;
     const int64_t cmax = std::max<int64_t>(1, max_ctas / c->nranks);
     const size_t T = (size_t)c->threads;
 
@@ -400,7 +420,8 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     if (c == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0) return RRA_ERR_INVALID_ARG;
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
     Params p;
-    rra_status_t st = plan_call(c, count, dtype, algo, &p);
+    int kind = 0;
+    rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind);
     if (st != RRA_OK) return st;
     if (grid_ctas) *grid_ctas = p.nranks * p.ctas_per_rank;
     if (steps) *steps = (int)p.nsteps;
@@ -416,9 +437,10 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     const size_t es = elem_size(dtype);
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
     Params p;
+    int kind = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = plan_call(c, count, dtype, algo, &p);
+        rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind);
         if (st != RRA_OK) return st;
     }
     for (int r = 0; r < c->nranks; ++r) {
@@ -427,7 +449,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
-    cudaError_t e = rra::launch_allreduce(p, dtype, algo, c->threads, (cudaStream_t)stream);
+    cudaError_t e = rra::launch_allreduce(p, dtype, kind, c->threads, (cudaStream_t)stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
         return RRA_ERR_NOT_CORESIDENT;

@@ -59,10 +59,21 @@ struct Params {
     int32_t epoch_slots;   // number of epoch slots to keep equal
 };
 
+// Kernel kinds: the four algorithms (same values as rra_algo_t) plus the
+// wide one-shot variants that split a position's sources over threads.
+enum KernelKind {
+    kKindOneshotLL = RRA_ONESHOT_LL,
+    kKindOneshotSentinel = RRA_ONESHOT_SENTINEL,
+    kKindTwoshot = RRA_TWOSHOT_DBUF,
+    kKindLL128 = RRA_LL128_ATOMIC,
+    kKindOneshotLLWide = 4,
+    kKindOneshotSentinelWide = 5,
+    kNumKinds = 6
+};
+
 // Host-side launch entry points (kernels.cu).
-cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, rra_algo_t algo,
-                             int threads, cudaStream_t stream);
-cudaError_t occupancy(rra_dtype_t dtype, rra_algo_t algo, int threads, int* blocks_per_sm);
+cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream);
+cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

@@ -212,3 +212,27 @@ def test_inputs_equal_to_rank_index_pattern_fp64_halves():
         for algo in ALGOS:
             got = run(comm, vals, "fp64", algo)
             check_against_oracle(vals, got, "fp64", algo)
+
+
+@pytest.mark.parametrize("algo", ["oneshot_ll", "oneshot_sentinel"])
+@pytest.mark.parametrize("wide", [0, 1])
+@pytest.mark.parametrize("n", [2, 5, 16, 64])
+def test_oneshot_wide_and_narrow_variants(algo, wide, n):
+    """Both one-shot receive variants (thread per position / threads split a
+    position's sources and stage in shared memory) give the oracle's bits,
+    single-step and multi-step, for every dtype."""
+    for dtype, counts in (("fp32", (1, 33, 4097, 70001)), ("bf16", (7, 5000)), ("fp64", (3, 3001))):
+        with rra.Comm(n, 70001 * 4) as comm:
+            comm.set_attr("oneshot_wide", wide)
+            for count in counts:
+                sends_np = inputs.normal(inputs.rng(64, count, n, wide), n, count, dtype)
+                got = run(comm, sends_np, dtype, algo)
+                check_against_oracle(sends_np, got, dtype, algo)
+            comm.set_attr("oneshot_chunk", 1024)
+            comm.set_attr("ctas_per_rank", 2)
+            count = 20000 // ELEM[dtype] * 4 + 5
+            _, steps = comm.plan_call(count, dtype, algo)
+            assert steps >= 3
+            sends_np = inputs.normal(inputs.rng(65, n, wide), n, count, dtype)
+            got = run(comm, sends_np, dtype, algo)
+            check_against_oracle(sends_np, got, dtype, algo)
