@@ -64,7 +64,7 @@ typedef enum {
     RRA_ERR_NOT_CORESIDENT = 4,  /* N ranks cannot all be resident at once */
     RRA_ERR_TIMEOUT = 5,         /* a device-side poll gave up (see status) */
     RRA_ERR_POISONED = 6,        /* an earlier device error; call rra_comm_reset */
-    RRA_ERR_EPOCH = 7            /* epoch counter near wrap; call rra_comm_reset */
+    RRA_ERR_EPOCH = 7            /* reserved (epochs are scrubbed on the device) */
 } rra_status_t;
 
 typedef enum { RRA_FP32 = 0, RRA_BF16 = 1, RRA_FP64 = 2 } rra_dtype_t;
@@ -206,6 +206,17 @@ rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
  * polls run into their time limit and record RRA_ERR_TIMEOUT.  rank = -1
  * clears it; rra_comm_reset also clears it.  Synchronises the device. */
 rra_status_t rra_comm_inject_drop(rra_comm_t comm, int rank);
+
+/* Epoch of the next step (diagnostics and tests).  Each step of a call uses
+ * one epoch; the LL flags carry its low 32 bits.  When a call's epochs would
+ * reach a multiple of 2^31, the call first zeroes every LL flag region of every
+ * window (the whole co-resident grid, followed by one bounded grid barrier)
+ * and restarts at that multiple + 1, so no stale flag can match a live epoch.
+ * rra_comm_set_epoch overwrites the epoch (epoch >= 1; it does not scrub, so
+ * only move it forward to exercise that boundary).  Both synchronise the
+ * device. */
+rra_status_t rra_comm_get_epoch(rra_comm_t comm, uint64_t* epoch);
+rra_status_t rra_comm_set_epoch(rra_comm_t comm, uint64_t epoch);
 
 /* Text for a status code (static storage). */
 const char* rra_status_string(rra_status_t status);

@@ -94,6 +94,44 @@ struct CtaState {
     bool drop;       // injected fault: do not store to peers
 };
 
+// Epoch scrub (once per kScrubPeriod steps).  Every CTA of the co-resident
+// grid zeroes its share of all LL flag regions, then the grid meets at one
+// bounded barrier: the only grid-wide wait in the library, taken once every
+// 2^31 steps and never on the per-call path.
+__device__ __noinline__ bool epoch_scrub(const Params& p, int rank) {
+    __shared__ int s_ok;
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t n1 = p.ll_bytes / 16, n2 = p.llag_bytes / 16;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int q = 0; q < p.nranks; ++q) {
+        char* wq = p.win0 + (uint64_t)q * p.stride;
+        for (uint64_t i = tid; i < n1; i += nthreads) st_relaxed_v4(wq + p.ll_off + i * 16, z);
+        for (uint64_t i = tid; i < n2; i += nthreads) st_relaxed_v4(wq + p.llag_off + i * 16, z);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const uint32_t gen = ld_relaxed_u32(&p.ctrl->scrub_gen);
+        fence_acq_rel_gpu();  // release this CTA's zeroes; the gen read before the arrival
+        const uint32_t arrived = atomicAdd(&p.ctrl->scrub_arrive, 1u) + 1u;
+        if (arrived == gridDim.x) {
+            st_relaxed_u32(&p.ctrl->scrub_arrive, 0u);
+            fence_acq_rel_gpu();
+            st_relaxed_u32(&p.ctrl->scrub_gen, gen + 1u);
+        } else {
+            Waiter w{globaltimer_ns() + p.timeout_ns, p.ctrl, rank, -2, 0u};
+            while (ld_relaxed_u32(&p.ctrl->scrub_gen) == gen) {
+                if (waiter_expired(w)) { ok = 0; break; }
+            }
+        }
+        fence_acq_rel_gpu();  // acquire every CTA's zeroes
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
 // Every thread reads the control words itself (one broadcast line per warp),
 // so the first input loads overlap this round trip instead of waiting behind
 // a block barrier.  The barrier sits in the epilogue instead: no thread may
@@ -108,12 +146,15 @@ __device__ __forceinline__ CtaState cta_prologue(const Params& p) {
     const uint32_t status = ld_relaxed_u32(&p.ctrl->status);
     const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
     s.skip = status != 0u;
-    // 32-bit LL flags must not wrap inside the live window of epochs.
-    if ((s.epoch & 0xFFFFFFFFull) + (uint64_t)p.nsteps + 2ull > 0xFFFFFFFFull) {
-        if (threadIdx.x == 0) record_error(p.ctrl, RRA_ERR_EPOCH, s.rank, 0);
-        s.skip = true;
-    }
     s.drop = drop == s.rank;
+    // The epochs of this call are [epoch, epoch + nsteps); if they would reach
+    // the next multiple of kScrubPeriod, scrub first and restart one past it.
+    // The test depends only on the epoch, which every thread of every CTA
+    // reads equal, so the whole grid takes this branch together.
+    if ((s.epoch & (kScrubPeriod - 1)) + (uint64_t)p.nsteps + 1ull >= kScrubPeriod) {
+        if (epoch_scrub(p, s.rank)) s.epoch = (s.epoch | (kScrubPeriod - 1)) + 2ull;
+        else s.skip = true;
+    }
     return s;
 }
 
@@ -344,8 +385,8 @@ __global__ void __launch_bounds__(512) oneshot_wide_kernel(const __grid_constant
     __shared__ uint4 stage[kStageVecs];
     __shared__ int fail;
     if (threadIdx.x == 0) fail = 0;
-    __syncthreads();
-    const CtaState s = cta_prologue(p);
+    CtaState s = cta_prologue(p);
+    s.skip = __syncthreads_or(s.skip) != 0;  // block barriers follow: skip must be CTA-uniform
     if (!s.skip) (void)oneshot_wide_body<T, kLL>(p, s, stage, &fail);
     cta_epilogue(p, s);
 }
@@ -692,7 +733,8 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
 
 template <typename T>
 __global__ void __launch_bounds__(512) ll128_kernel(const __grid_constant__ Params p) {
-    const CtaState s = cta_prologue(p);
+    CtaState s = cta_prologue(p);
+    s.skip = __any_sync(0xFFFFFFFFu, s.skip) != 0;  // warp syncs follow: skip must be warp-uniform
     if (!s.skip) (void)ll128_body<T>(p, s);
     cta_epilogue(p, s);
 }
@@ -723,6 +765,8 @@ __global__ void init_kernel(const __grid_constant__ InitParams ip) {
             ip.ctrl->err_rank = -1;
             ip.ctrl->err_step = -1;
             ip.ctrl->drop_rank = -1;
+            ip.ctrl->scrub_arrive = 0u;
+            ip.ctrl->scrub_gen = 0u;
         }
         for (int i = threadIdx.x; i < kEpochSlots; i += blockDim.x) ip.ctrl->epoch[i] = 1ull;
     }

@@ -110,7 +110,7 @@ const char* rra_status_string(rra_status_t s) {
         case RRA_ERR_NOT_CORESIDENT: return "ranks cannot all be co-resident on the GPU";
         case RRA_ERR_TIMEOUT: return "a device-side wait timed out";
         case RRA_ERR_POISONED: return "communicator poisoned by an earlier device error; reset it";
-        case RRA_ERR_EPOCH: return "epoch counter near wrap; reset the communicator";
+        case RRA_ERR_EPOCH: return "epoch error (reserved)";
     }
     return "unknown status";
 }
@@ -352,6 +352,14 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     const size_t off_os = off_ll + L.ll_bytes;
     const size_t off_ts = off_os + L.os_bytes;
     const size_t off_la = off_ts + L.ts_bytes;
+    {
+        // LL flag regions, zeroed by the epoch scrub whatever the algorithm
+        const LaSizes ls = la_sizes(L.la_part, c->nranks);
+        p->ll_off = off_ll;
+        p->ll_bytes = 2 * n * 2 * L.ll_chunk;
+        p->llag_off = off_la + 2 * ls.acc_parity + 2 * ls.cnt_parity;
+        p->llag_bytes = 2 * n * ls.ag_slot;
+    }
     size_t work = 0;  // positions per step that the CTAs of one rank split
     int64_t ctas;
     switch (algo) {
@@ -541,6 +549,25 @@ rra_status_t rra_comm_set_timing(rra_comm_t c, uint64_t* dev_buf) {
     std::lock_guard<std::mutex> g(c->mu);
     c->timing = dev_buf;
     return RRA_OK;
+}
+
+rra_status_t rra_comm_get_epoch(rra_comm_t c, uint64_t* epoch) {
+    if (c == nullptr || epoch == nullptr) return RRA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
+    if (cudaMemcpy(epoch, &c->ctrl->epoch[0], sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_set_epoch(rra_comm_t c, uint64_t epoch) {
+    if (c == nullptr || epoch == 0) return RRA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
+    uint64_t* h = (uint64_t*)malloc(sizeof(uint64_t) * rra::kEpochSlots);
+    if (h == nullptr) return RRA_ERR_OOM;
+    for (int i = 0; i < rra::kEpochSlots; ++i) h[i] = epoch;
+    const cudaError_t e = cudaMemcpy(c->ctrl->epoch, h, sizeof(uint64_t) * rra::kEpochSlots, cudaMemcpyHostToDevice);
+    free(h);
+    return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
 }
 
 rra_status_t rra_comm_inject_drop(rra_comm_t c, int rank) {

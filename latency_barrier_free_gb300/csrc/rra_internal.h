@@ -16,6 +16,10 @@ constexpr int kEpochSlots = 4096;      // largest grid a communicator may launch
 constexpr int kGroupVecs = 32;         // LL128-atomic: vectors per completion counter (one warp)
 constexpr size_t kRegionAlign = 4096;
 constexpr uint64_t kMaxMessageBytes = (1ull << 36) - 16;  // 16-byte vector indices fit in 32 bits
+// LL flags are the low 32 bits of the epoch.  When a call's epochs would cross
+// a multiple of kScrubPeriod, all LL flag regions are zeroed and the epoch
+// restarts one past that multiple, so every live flag value is unique.
+constexpr uint64_t kScrubPeriod = 1ull << 31;
 
 // Control block at the start of the allocation (before window 0).
 struct Ctrl {
@@ -23,7 +27,9 @@ struct Ctrl {
     int32_t err_rank;    // virtual rank that recorded it
     int32_t err_step;    // chunk step of the call in which it was recorded
     int32_t drop_rank;   // injected fault: rank whose stores to peers are skipped; -1 = none
-    uint32_t reserved[60];
+    uint32_t scrub_arrive;  // LL flag scrub: CTAs arrived at the grid barrier
+    uint32_t scrub_gen;     // LL flag scrub: completed scrubs (barrier generation)
+    uint32_t reserved[58];
     // Every CTA slot holds the same value: the epoch of the next step.  CTA b
     // of a call with G CTAs reads slot b at entry and writes epoch + steps to
     // every slot b' = b (mod G); each slot has exactly one reader/writer per
@@ -49,6 +55,8 @@ struct Params {
     uint64_t aux_parity_bytes;   // LL128: bytes of one parity of counters
     uint64_t aux2_slot_bytes;    // LL128: bytes of one AllGather slot
     uint64_t aux2_parity_bytes;  // LL128: bytes of one AllGather parity
+    uint64_t ll_off, ll_bytes;        // LL flag regions of a window (one-shot LL slots,
+    uint64_t llag_off, llag_bytes;    // LL128 AllGather slots), zeroed by the epoch scrub
     uint32_t nvec;         // 16-byte vectors per rank = ceil(count / elems per vector)
     uint32_t chunk_vecs;   // one-shot: vectors per rank per full step;
                            // two-shot/LL128: vectors per partition per full step

@@ -31,7 +31,7 @@ SYMBOLS = [
     "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_comm_status", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
     "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_inject_drop",
-    "rra_status_string", "rra_version",
+    "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string", "rra_version",
     "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_sm_count",
 ]
 
@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH):
             "rra_comm_max_coresident": ([vp, i32, i32, ip], i32),
             "rra_comm_set_timing": ([vp, vp], i32),
             "rra_comm_inject_drop": ([vp, i32], i32),
+            "rra_comm_get_epoch": ([vp, ctypes.POINTER(ctypes.c_uint64)], i32),
+            "rra_comm_set_epoch": ([vp, ctypes.c_uint64], i32),
             "rra_status_string": ([i32], ctypes.c_char_p),
             "rra_version": ([], ctypes.c_char_p),
             "rra_probe_l2_chase": ([sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.POINTER(ctypes.c_double)], i32),
@@ -242,6 +244,14 @@ class Comm:
 
     def set_timing(self, dev_ptr):
         _check(self._lib.rra_comm_set_timing(self._h, ctypes.c_void_p(dev_ptr or 0)), "rra_comm_set_timing")
+
+    def epoch(self) -> int:
+        v = ctypes.c_uint64()
+        _check(self._lib.rra_comm_get_epoch(self._h, ctypes.byref(v)), "rra_comm_get_epoch")
+        return v.value
+
+    def set_epoch(self, epoch: int):
+        _check(self._lib.rra_comm_set_epoch(self._h, int(epoch)), "rra_comm_set_epoch")
 
     def inject_drop(self, rank: int):
         _check(self._lib.rra_comm_inject_drop(self._h, int(rank)), "rra_comm_inject_drop")

@@ -159,3 +159,30 @@ def test_probes():
     assert sa != sb and 50.0 < rtt < 100000.0
     rra.probe_empty_kernel()
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("start", [2 ** 31 - 5, 2 ** 32 - 3, 3 * 2 ** 31 - 1])
+def test_epoch_scrub_at_boundary(algo, start):
+    """Calls whose epochs reach a multiple of 2^31 first zero every LL flag
+    region (grid-wide, one bounded barrier) and restart the epoch one past the
+    multiple; results stay exact across the boundary, also where the low 32
+    bits of the epoch wrap."""
+    n, count = 4, 50000
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("oneshot_chunk", 4096)
+        comm.set_attr("twoshot_chunk", 8192)
+        comm.set_attr("ll128_chunk", 8192)
+        _, steps = comm.plan_call(count, "fp32", algo)
+        assert steps >= 5
+        comm.set_epoch(start)
+        for it in range(3):
+            sends_np = inputs.normal(inputs.rng(73, it), n, count, "fp32")
+            sends = to_device(sends_np, "fp32")
+            recvs = poison_like(sends)
+            comm.allreduce(sends, recvs, algo)
+            torch.cuda.synchronize()
+            assert comm.status()[0] == rra.OK
+            check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+        boundary = (start | (2 ** 31 - 1)) + 1
+        assert comm.epoch() == boundary + 1 + 3 * steps
