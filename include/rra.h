@@ -73,7 +73,9 @@ typedef enum {
     RRA_ONESHOT_LL = 0,        /* Sec. IV "LL": data and epoch flag share one atomic word */
     RRA_ONESHOT_SENTINEL = 1,  /* Sec. IV "Sentinel": scratch pre-filled with -NaN, polled */
     RRA_TWOSHOT_DBUF = 2,      /* Sec. III-A two-shot + Sec. IV double buffering, Fig. 4 */
-    RRA_LL128_ATOMIC = 3       /* Fig. 5: atomic adds into the owner's lines, counter == N-1 */
+    RRA_LL128_ATOMIC = 3,      /* Fig. 5: atomic adds into the owner's lines, counter == N-1 */
+    RRA_ONESHOT_BARRIER = 4    /* BASELINE, not barrier-free: plain stores + two flag barriers
+                                  per step (Sec. III-B, the design the paper replaces) */
 } rra_algo_t;
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
@@ -84,8 +86,13 @@ typedef enum {
     RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step, 0 = largest that fits */
     RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step, 0 = largest */
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
-    RRA_ATTR_ONESHOT_WIDE = 6      /* one-shot polls split a position's sources over
+    RRA_ATTR_ONESHOT_WIDE = 6,     /* one-shot polls split a position's sources over
                                       threads: -1 auto (N >= 16, default), 0 off, 1 on */
+    RRA_ATTR_COOPERATIVE = 7       /* 1 (default): cooperative launch, so the driver
+                                      guarantees that all CTAs are resident together;
+                                      0: plain launch of the same occupancy-checked grid
+                                      (progress then relies on no other work holding the
+                                      SMs for longer than the poll time limit) */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -105,6 +112,9 @@ typedef struct {
     size_t window_stride;   /* bytes between consecutive windows */
     size_t ctrl_bytes;      /* control block before window 0 */
     size_t total_bytes;     /* ctrl_bytes + nranks * window_stride */
+    size_t bf_bytes;        /* barrier baseline flags: 64 CTAs x 64 ranks x 4 B */
+    size_t bd_chunk;        /* barrier baseline payload bytes per rank per step */
+    size_t bd_bytes;        /* barrier baseline data: N x bd_chunk (one-shot cap) */
 } rra_layout_t;
 
 /*
@@ -206,6 +216,13 @@ rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
  * polls run into their time limit and record RRA_ERR_TIMEOUT.  rank = -1
  * clears it; rra_comm_reset also clears it.  Synchronises the device. */
 rra_status_t rra_comm_inject_drop(rra_comm_t comm, int rank);
+
+/* Barrier latency on this communicator's N ranks (Fig. 3 analogue, one
+ * GPU): one CTA per rank runs `iters` flag barriers back to back (the barrier
+ * of RRA_ONESHOT_BARRIER); output: mean ns per barrier between the first and
+ * the last.  Synchronises the device.  Errors: RRA_ERR_INVALID_ARG (iters < 2),
+ * RRA_ERR_POISONED, RRA_ERR_CUDA, and device errors as rra_comm_status. */
+rra_status_t rra_comm_barrier_latency(rra_comm_t comm, int iters, double* ns_per_barrier);
 
 /* Epoch of the next step (diagnostics and tests).  Each step of a call uses
  * one epoch; the LL flags carry its low 32 bits.  When a call's epochs would

@@ -391,6 +391,134 @@ __global__ void __launch_bounds__(512) oneshot_wide_kernel(const __grid_constant
     cta_epilogue(p, s);
 }
 
+// ----------------------------------------- barrier baseline (not barrier-free) ----
+// The design the paper replaces ("Every Microsecond Matters", Sec. III-B and
+// Fig. 3): plain stores, then a memory barrier among the peers, then reads,
+// then a second barrier before the buffers may be reused.  The barrier is the
+// pattern the paper measures with ncclLsaBarrierSession: a flag is written to
+// every peer, then each participant waits for every peer's flag.  Here the
+// participants are the CTAs with one sub-index c of all N ranks; thread q of
+// the CTA signals and waits for peer q.  Flags carry a tag that only grows
+// within an epoch scrub period, and arrival is tested as tag-difference >= 0
+// because a fast peer may already have posted the next tag.
+__device__ __forceinline__ bool flag_barrier(const Params& p, const CtaState& s, uint32_t tag, Waiter& w,
+                                             int* fail) {
+    __syncthreads();  // the CTA's data stores happen before the flag stores
+    const int N = p.nranks, r = s.rank, q = (int)threadIdx.x;
+    if (q < N && q != r) {
+        fence_acq_rel_gpu();  // release
+        if (!s.drop)
+            st_relaxed_u32(window(p, q) + p.aux_off + ((uint64_t)s.sub * kMaxRanks + (uint64_t)r) * 4, tag);
+        const char* flag = window(p, r) + p.aux_off + ((uint64_t)s.sub * kMaxRanks + (uint64_t)q) * 4;
+        while ((int32_t)(ld_relaxed_u32(flag) - tag) < 0) {
+            if (*(volatile int*)fail) break;
+            if (waiter_expired(w)) { *(volatile int*)fail = 1; break; }
+        }
+        fence_acq_rel_gpu();  // acquire
+    }
+    __syncthreads();  // every peer's data before the CTA's reads
+    return *(volatile int*)fail == 0;
+}
+
+template <typename T>
+__device__ __forceinline__ bool oneshot_barrier_body(const Params& p, const CtaState& s, int* fail) {
+    using M = VecMath<T>;
+    const int N = p.nranks, r = s.rank;
+    const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
+    const uint32_t pos1 = pos0 + p.per_cta;
+    char* const mine = window(p, r) + p.region_off;
+    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+
+#pragma unroll 1
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint32_t tag = (uint32_t)(2ull * e);
+        const uint32_t base = k * p.chunk_vecs;
+        const uint32_t end = min(pos1, min(p.chunk_vecs, p.nvec - base));
+        w.step = (int)k;
+        if (!s.drop) {
+#pragma unroll 1
+            for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+                const uint4 x = load_input<T>(p.send[r], base + v, p.count);
+                char* dst = p.win0 + p.region_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+#pragma unroll 1
+                for (int q = 0; q < N; ++q, dst += p.stride) {
+                    if (q != r) st_relaxed_v4(dst, x);
+                }
+            }
+        }
+        if (!flag_barrier(p, s, tag, w, fail)) return false;  // data ready everywhere
+#pragma unroll 1
+        for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+            const uint4 own = load_input<T>(p.send[r], base + v, p.count);
+            const char* const slot0 = mine + (uint64_t)v * kVecBytes;
+            typename M::Acc acc;
+#pragma unroll 1
+            for (int q0 = 0; q0 < N; q0 += kBatch) {
+                uint4 val[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q < N && q != r) val[j] = ld_relaxed_v4(slot0 + (uint64_t)q * p.slot_bytes);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int q = q0 + j;
+                    if (q >= N) break;
+                    const uint4 x = (q == r) ? own : val[j];
+                    if (q == 0) acc = M::load(x);
+                    else M::add(acc, x);
+                }
+            }
+            store_output<T>(p.recv[r], base + v, p.count, M::store(acc));
+        }
+        if (!flag_barrier(p, s, tag + 1u, w, fail)) return false;  // buffers free again
+    }
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) oneshot_barrier_kernel(const __grid_constant__ Params p) {
+    __shared__ int fail;
+    if (threadIdx.x == 0) fail = 0;
+    CtaState s = cta_prologue(p);
+    s.skip = __syncthreads_or(s.skip) != 0;
+    if (!s.skip) (void)oneshot_barrier_body<T>(p, s, &fail);
+    cta_epilogue(p, s);
+}
+
+// Barrier latency (Fig. 3 analogue): N ranks x 1 CTA run `nsteps` flag
+// barriers back to back; CTA 0 records %globaltimer after the first and after
+// the last barrier in timing[0..1].
+__global__ void __launch_bounds__(512) barrier_probe_kernel(const __grid_constant__ Params p) {
+    __shared__ int fail;
+    if (threadIdx.x == 0) fail = 0;
+    CtaState s = cta_prologue(p);
+    s.skip = __syncthreads_or(s.skip) != 0;
+    if (!s.skip) {
+        Waiter w{s.t_start + p.timeout_ns, p.ctrl, s.rank, 0, 0u};
+        uint64_t t_first = 0;
+#pragma unroll 1
+        for (uint32_t k = 0; k < p.nsteps; ++k) {
+            w.step = (int)k;
+            if (!flag_barrier(p, s, (uint32_t)(2ull * (s.epoch + k)), w, &fail)) break;
+            if (k == 0) t_first = globaltimer_ns();
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0 && p.timing != nullptr) {
+            p.timing[0] = t_first;
+            p.timing[1] = globaltimer_ns();
+        }
+    }
+    const Params& q = p;
+    if (!s.skip) {  // epoch bookkeeping as for any call; no per-CTA timing here
+        __syncthreads();
+        const uint64_t next = s.epoch + q.nsteps;
+        for (unsigned slot = blockIdx.x + threadIdx.x * gridDim.x; slot < (unsigned)q.epoch_slots;
+             slot += blockDim.x * gridDim.x)
+            st_relaxed_u64(&q.ctrl->epoch[slot], next);
+    }
+}
+
 // ------------------------------------------ two-shot, double buffered ----
 // Sec. III-A "Two-shot" (ReduceScatter then AllGather, both push) with
 // sentinel synchronisation and the bidirectional double buffering of Sec. IV /
@@ -790,6 +918,8 @@ static const void* kernel_for(int kind) {
         case kKindLL128: return (const void*)ll128_kernel<T>;
         case kKindOneshotLLWide: return (const void*)oneshot_wide_kernel<T, true>;
         case kKindOneshotSentinelWide: return (const void*)oneshot_wide_kernel<T, false>;
+        case kKindOneshotBarrier: return (const void*)oneshot_barrier_kernel<T>;
+        case kKindBarrierProbe: return (const void*)barrier_probe_kernel;
     }
     return nullptr;
 }
@@ -809,7 +939,8 @@ cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, threads, 0);
 }
 
-cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream) {
+cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
+                             bool cooperative) {
     const void* k = kernel_for(dtype, kind);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -821,7 +952,7 @@ cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int t
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cooperative ? 1 : 0;
     void* args[] = {(void*)&p};
     return cudaLaunchKernelExC(&cfg, k, args);
 }
@@ -836,12 +967,14 @@ cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int n
     ip.nranks = nranks;
     uint64_t off = 0;
     int j = 0;
-    // Region order inside a window: LL, sentinel one-shot, two-shot (RS+AG),
-    // LL128 (accumulators + counters + LL AllGather).  Must match the planner.
-    ip.job[j++] = FillJob{off, lay.ll_bytes, 0u};           off += lay.ll_bytes;
-    ip.job[j++] = FillJob{off, lay.os_bytes, 0xFFFFFFFFu};  off += lay.os_bytes;
-    ip.job[j++] = FillJob{off, lay.ts_bytes, 0xFFFFFFFFu};  off += lay.ts_bytes;
-    ip.job[j++] = FillJob{off, lay.la_bytes, 0u};           off += lay.la_bytes;
+    // Region order inside a window: LL slots, barrier flags, sentinel one-shot,
+    // two-shot (RS+AG), LL128 (accumulators + counters + LL AllGather),
+    // barrier-baseline data.  Must match the planner.
+    ip.job[j++] = FillJob{off, lay.ll_bytes + lay.bf_bytes, 0u};  off += lay.ll_bytes + lay.bf_bytes;
+    ip.job[j++] = FillJob{off, lay.os_bytes, 0xFFFFFFFFu};        off += lay.os_bytes;
+    ip.job[j++] = FillJob{off, lay.ts_bytes, 0xFFFFFFFFu};        off += lay.ts_bytes;
+    ip.job[j++] = FillJob{off, lay.la_bytes, 0u};                 off += lay.la_bytes;
+    ip.job[j++] = FillJob{off, lay.bd_bytes, 0u};                 off += lay.bd_bytes;
     ip.njobs = j;
     init_kernel<<<1024, 256, 0, stream>>>(ip);
     return cudaGetLastError();

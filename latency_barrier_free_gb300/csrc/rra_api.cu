@@ -41,7 +41,7 @@ size_t elem_size(rra_dtype_t d) {
     return 0;
 }
 
-bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_LL128_ATOMIC; }
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_ONESHOT_BARRIER; }
 bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
 
 int64_t env_i64(const char* name, int64_t dflt) {
@@ -88,6 +88,7 @@ struct rra_comm {
     int64_t ts_chunk = 0, la_chunk = 0, os_chunk = 0;
     int blocks_per_sm[3][rra::kNumKinds];  // by dtype, kernel kind; -1 = not queried
     int64_t oneshot_wide = -1;              // -1 auto (N >= 16), 0 never, 1 always
+    int64_t cooperative = 1;                // cooperative launch (co-residency guaranteed)
     bool poisoned = false;
     uint64_t* timing = nullptr;
     // rra_allreduce_host staging (allocated on first use)
@@ -143,11 +144,17 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
     L.la_part = la_part;
     if (L.ll_chunk < 16 || L.os_chunk < 16 || L.ts_part < 16 || L.la_part < 16)
         return RRA_ERR_INVALID_ARG;
+    // Barrier baseline: one parity (the second barrier frees the buffers).
+    L.bd_chunk = std::min(payload, floor16(cap_os / n));
+    if (L.bd_chunk < 16) return RRA_ERR_INVALID_ARG;
     L.ll_bytes = align_up(2 * n * 2 * L.ll_chunk, rra::kRegionAlign);
+    L.bf_bytes = align_up((size_t)rra::kBarrierCtas * RRA_MAX_RANKS * 4, rra::kRegionAlign);
     L.os_bytes = align_up(2 * n * L.os_chunk, rra::kRegionAlign);
     L.ts_bytes = align_up(2 * (2 * n * L.ts_part), rra::kRegionAlign);
     L.la_bytes = align_up(la_sizes(L.la_part, nranks).total, rra::kRegionAlign);
-    L.window_stride = align_up(L.ll_bytes + L.os_bytes + L.ts_bytes + L.la_bytes, kWindowAlign);
+    L.bd_bytes = align_up(n * L.bd_chunk, rra::kRegionAlign);
+    L.window_stride = align_up(L.ll_bytes + L.bf_bytes + L.os_bytes + L.ts_bytes + L.la_bytes + L.bd_bytes,
+                               kWindowAlign);
     L.ctrl_bytes = align_up(sizeof(Ctrl), rra::kRegionAlign);
     L.total_bytes = L.ctrl_bytes + n * L.window_stride;
     *out = L;
@@ -283,6 +290,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
             c->oneshot_wide = v;
             return RRA_OK;
+        case RRA_ATTR_COOPERATIVE:
+            if (v < 0 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->cooperative = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -297,6 +308,7 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_LL128_CHUNK: *v = c->la_chunk; return RRA_OK;
         case RRA_ATTR_ONESHOT_CHUNK: *v = c->os_chunk; return RRA_OK;
         case RRA_ATTR_ONESHOT_WIDE: *v = c->oneshot_wide; return RRA_OK;
+        case RRA_ATTR_COOPERATIVE: *v = c->cooperative; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -348,15 +360,20 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     p->nranks = c->nranks;
     p->epoch_slots = rra::kEpochSlots;
 
+    // Window regions, in order (must match launch_init):
+    // LL slots | barrier flags | sentinel slots | two-shot | LL128 | barrier data
     const size_t off_ll = 0;
-    const size_t off_os = off_ll + L.ll_bytes;
+    const size_t off_bf = off_ll + L.ll_bytes;
+    const size_t off_os = off_bf + L.bf_bytes;
     const size_t off_ts = off_os + L.os_bytes;
     const size_t off_la = off_ts + L.ts_bytes;
+    const size_t off_bd = off_la + L.la_bytes;
     {
-        // LL flag regions, zeroed by the epoch scrub whatever the algorithm
+        // flag regions zeroed by the epoch scrub whatever the algorithm:
+        // LL slots + barrier flags (contiguous), LL128 AllGather slots
         const LaSizes ls = la_sizes(L.la_part, c->nranks);
         p->ll_off = off_ll;
-        p->ll_bytes = 2 * n * 2 * L.ll_chunk;
+        p->ll_bytes = L.ll_bytes + L.bf_bytes;
         p->llag_off = off_la + 2 * ls.acc_parity + 2 * ls.cnt_parity;
         p->llag_bytes = 2 * n * ls.ag_slot;
     }
@@ -409,11 +426,26 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             work = part;
             break;
         }
+        case RRA_ONESHOT_BARRIER: {
+            size_t cap = L.bd_chunk / rra::kVecBytes;
+            if (c->os_chunk > 0) cap = std::min(cap, std::max<size_t>(1, (size_t)c->os_chunk / rra::kVecBytes));
+            const size_t chunk = std::min<size_t>(p->nvec, cap);
+            p->chunk_vecs = (uint32_t)chunk;
+            p->nsteps = (uint32_t)ceil_div(p->nvec, chunk);
+            p->region_off = off_bd;
+            p->slot_bytes = L.bd_chunk;
+            p->parity_bytes = 0;
+            p->aux_off = off_bf;
+            work = chunk;
+            break;
+        }
         default:
             return RRA_ERR_INVALID_ARG;
     }
-    if (c->ctas_per_rank > 0) ctas = std::min<int64_t>(c->ctas_per_rank, cmax);
-    else ctas = std::min<int64_t>((int64_t)ceil_div(work, T), cmax);
+    int64_t cap_ctas = cmax;
+    if (algo == RRA_ONESHOT_BARRIER) cap_ctas = std::min<int64_t>(cap_ctas, rra::kBarrierCtas);
+    if (c->ctas_per_rank > 0) ctas = std::min<int64_t>(c->ctas_per_rank, cap_ctas);
+    else ctas = std::min<int64_t>((int64_t)ceil_div(work, T), cap_ctas);
     ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)work));
     size_t per = ceil_div(work, (size_t)ctas);
     if (algo == RRA_LL128_ATOMIC) per = align_up(per, rra::kGroupVecs);
@@ -457,7 +489,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
-    cudaError_t e = rra::launch_allreduce(p, dtype, kind, c->threads, (cudaStream_t)stream);
+    cudaError_t e = rra::launch_allreduce(p, dtype, kind, c->threads, (cudaStream_t)stream, c->cooperative != 0);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
         return RRA_ERR_NOT_CORESIDENT;
@@ -548,6 +580,43 @@ rra_status_t rra_comm_set_timing(rra_comm_t c, uint64_t* dev_buf) {
     if (c == nullptr) return RRA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> g(c->mu);
     c->timing = dev_buf;
+    return RRA_OK;
+}
+
+rra_status_t rra_comm_barrier_latency(rra_comm_t c, int iters, double* ns_per_barrier) {
+    if (c == nullptr || ns_per_barrier == nullptr || iters < 2 || iters > (1 << 24)) return RRA_ERR_INVALID_ARG;
+    if (c->poisoned) return RRA_ERR_POISONED;
+    Params p;
+    int kind = 0;
+    rra_status_t st;
+    {
+        std::lock_guard<std::mutex> g(c->mu);
+        st = plan_call(c, 1, RRA_FP32, RRA_ONESHOT_BARRIER, &p, &kind);
+    }
+    if (st != RRA_OK) return st;
+    uint64_t* dt = nullptr;
+    if (cudaMalloc((void**)&dt, 2 * sizeof(uint64_t)) != cudaSuccess) {
+        cudaGetLastError();
+        return RRA_ERR_OOM;
+    }
+    p.ctas_per_rank = 1;
+    p.per_cta = 1;
+    p.nsteps = (uint32_t)iters;
+    p.timing = dt;
+    uint64_t h[2] = {0, 0};
+    st = RRA_OK;
+    if (rra::launch_allreduce(p, RRA_FP32, rra::kKindBarrierProbe, 128, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(h, dt, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        st = RRA_ERR_CUDA;
+    }
+    cudaFree(dt);
+    if (st != RRA_OK) return st;
+    int rank = -1, step = -1;
+    st = rra_comm_status(c, &rank, &step);
+    if (st != RRA_OK) return st;
+    *ns_per_barrier = (double)(h[1] - h[0]) / (double)(iters - 1);
     return RRA_OK;
 }
 

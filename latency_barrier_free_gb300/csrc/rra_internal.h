@@ -74,13 +74,17 @@ enum KernelKind {
     kKindOneshotSentinel = RRA_ONESHOT_SENTINEL,
     kKindTwoshot = RRA_TWOSHOT_DBUF,
     kKindLL128 = RRA_LL128_ATOMIC,
-    kKindOneshotLLWide = 4,
-    kKindOneshotSentinelWide = 5,
-    kNumKinds = 6
+    kKindOneshotBarrier = RRA_ONESHOT_BARRIER,
+    kKindOneshotLLWide = 5,
+    kKindOneshotSentinelWide = 6,
+    kKindBarrierProbe = 7,
+    kNumKinds = 8
 };
+constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 
 // Host-side launch entry points (kernels.cu).
-cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream);
+cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
+                             bool cooperative = true);
 cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);

@@ -21,9 +21,11 @@ STATUS_NAMES = {
 ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_CORESIDENT, ERR_TIMEOUT, ERR_POISONED, ERR_EPOCH = range(1, 8)
 
 DTYPES = {"fp32": 0, "bf16": 1, "fp64": 2}
-ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomic": 3}
+ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomic": 3,
+         "oneshot_barrier": 4}
+BARRIER_FREE = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic")
 ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,
-         "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6}
+         "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6, "cooperative": 7}
 MAX_RANKS = 64
 
 # Exported symbols, in declaration order of the public headers.
@@ -31,7 +33,8 @@ SYMBOLS = [
     "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_comm_status", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
     "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_inject_drop",
-    "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string", "rra_version",
+    "rra_comm_barrier_latency", "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string",
+    "rra_version",
     "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_sm_count",
 ]
 
@@ -39,7 +42,8 @@ SYMBOLS = [
 class Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) if n != "nranks" else (n, ctypes.c_int) for n in (
         "nranks", "max_bytes", "ll_chunk", "ll_bytes", "os_chunk", "os_bytes", "ts_part", "ts_bytes",
-        "la_part", "la_bytes", "window_stride", "ctrl_bytes", "total_bytes")]
+        "la_part", "la_bytes", "window_stride", "ctrl_bytes", "total_bytes", "bf_bytes", "bd_chunk",
+        "bd_bytes")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -84,6 +88,7 @@ def load(path: str = LIB_PATH):
             "rra_comm_max_coresident": ([vp, i32, i32, ip], i32),
             "rra_comm_set_timing": ([vp, vp], i32),
             "rra_comm_inject_drop": ([vp, i32], i32),
+            "rra_comm_barrier_latency": ([vp, i32, ctypes.POINTER(ctypes.c_double)], i32),
             "rra_comm_get_epoch": ([vp, ctypes.POINTER(ctypes.c_uint64)], i32),
             "rra_comm_set_epoch": ([vp, ctypes.c_uint64], i32),
             "rra_status_string": ([i32], ctypes.c_char_p),
@@ -183,6 +188,21 @@ class Comm:
         del ks, kr
         _check(st, "rra_allreduce")
 
+    def prepare(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None):
+        """Build the ctypes arguments of one call once; the returned callable
+        enqueues that call (same buffers) with no per-call marshalling."""
+        sp, ks = _ptr_array(send_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        fn = self._lib.rra_allreduce
+        args = (self._h, sp, rp, ctypes.c_size_t(int(count)), ctypes.c_int(DTYPES[dtype]),
+                ctypes.c_int(ALGOS[algo]), _stream_handle(stream))
+
+        def call(_keep=(ks, kr)):
+            st = fn(*args)
+            if st != OK:
+                raise RraError(st, "rra_allreduce")
+        return call
+
     def allreduce(self, sends, recvs, algo: str, stream=None) -> None:
         """recvs[r][:] = sum over ranks of sends[p][:]; tensors on the GPU,
         one per rank, same dtype and element count, contiguous."""
@@ -244,6 +264,12 @@ class Comm:
 
     def set_timing(self, dev_ptr):
         _check(self._lib.rra_comm_set_timing(self._h, ctypes.c_void_p(dev_ptr or 0)), "rra_comm_set_timing")
+
+    def barrier_latency(self, iters: int = 1000) -> float:
+        """Mean ns per N-way flag barrier (the baseline's barrier)."""
+        v = ctypes.c_double()
+        _check(self._lib.rra_comm_barrier_latency(self._h, int(iters), ctypes.byref(v)), "rra_comm_barrier_latency")
+        return v.value
 
     def epoch(self) -> int:
         v = ctypes.c_uint64()

@@ -236,3 +236,21 @@ def test_oneshot_wide_and_narrow_variants(algo, wide, n):
             sends_np = inputs.normal(inputs.rng(65, n, wide), n, count, dtype)
             got = run(comm, sends_np, dtype, algo)
             check_against_oracle(sends_np, got, dtype, algo)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+def test_barrier_baseline_parity(dtype):
+    """The barrier-based baseline (plain stores + two flag barriers per step)
+    adds in rank order too, so it is bit-exact against the oracle."""
+    for n in (2, 4, 7, 64):
+        with rra.Comm(n, 70000 * ELEM[dtype]) as comm:
+            for count in (1, 33, 4097, 70000):
+                sends_np = inputs.normal(inputs.rng(66, count, n), n, count, dtype)
+                got = run(comm, sends_np, dtype, "oneshot_barrier")
+                check_against_oracle(sends_np, got, dtype, "oneshot_barrier")
+            comm.set_attr("oneshot_chunk", 1024)
+            comm.set_attr("ctas_per_rank", 3)
+            sends_np = inputs.normal(inputs.rng(67, n), n, 9000, dtype)
+            assert comm.plan_call(9000, dtype, "oneshot_barrier")[1] >= 3
+            got = run(comm, sends_np, dtype, "oneshot_barrier")
+            check_against_oracle(sends_np, got, dtype, "oneshot_barrier")

@@ -186,3 +186,42 @@ def test_epoch_scrub_at_boundary(algo, start):
             check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
         boundary = (start | (2 ** 31 - 1)) + 1
         assert comm.epoch() == boundary + 1 + 3 * steps
+
+
+def test_barrier_latency_and_baseline_timeout():
+    """The flag barrier of the baseline is measurable for N = 2..64, and a rank
+    that never signals makes the baseline time out like the others."""
+    for n in (2, 8, 64):
+        with rra.Comm(n, 4096) as comm:
+            ns = comm.barrier_latency(200)
+            assert 50.0 < ns < 1e6
+            x = [torch.ones(1024, device="cuda") for _ in range(n)]
+            y = poison_like(x)
+            comm.allreduce(x, y, "oneshot_barrier")
+            torch.cuda.synchronize()
+            assert comm.status()[0] == rra.OK
+            assert torch.equal(y[n - 1], torch.full_like(y[0], float(n)))
+            comm.set_attr("poll_timeout_ms", 20)
+            comm.inject_drop(1)
+            comm.allreduce(x, y, "oneshot_barrier")
+            assert comm.status()[0] == rra.ERR_TIMEOUT
+            comm.reset()
+            comm.allreduce(x, y, "oneshot_barrier")
+            torch.cuda.synchronize()
+            assert comm.status()[0] == rra.OK
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_plain_launch_matches_cooperative(algo):
+    """With the cooperative attribute off, the same occupancy-checked grid runs
+    as a plain launch and gives the same results."""
+    n, count = 4, 100000
+    sends_np = inputs.normal(inputs.rng(74, 0), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cooperative", 0)
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
