@@ -3,10 +3,12 @@
 
 Workload (one "step"): N=4 virtual ranks, message sizes 128 B .. 1 MiB per
 rank in powers of two (14 sizes), binary32 and bfloat16 N(0,1) inputs, all
-four algorithms; each (dtype, size, algorithm) runs `--inner` back-to-back
-calls on one stream, timed with CUDA events on that stream.  L2 is flushed
-(a 256 MiB write) between steps; the calls inside a step reuse their
-L2-resident buffers, the regime the small-message latency floor assumes.
+four algorithms; each (dtype, size, algorithm) replays a CUDA graph of
+`--inner` back-to-back calls (the decode-style replay path: no host work per
+call), timed with CUDA events on the replay stream.  L2 is flushed (a 256 MiB
+write) between steps; the calls inside a step reuse their L2-resident
+buffers, the regime the small-message latency floor assumes.  The same calls
+launched one by one from Python are reported as stream_launch_us.
 
 value     mean over the 28 (dtype, size) cases of the fastest algorithm's
           microseconds per call (lower is better)
@@ -96,7 +98,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -190,6 +192,8 @@ def run_ours(args, world, rank, local):
 
     comm = rra.Comm(NRANKS, 1 << 20)
     cases = sweep_cases()
+    clocks = ClockSampler(local)
+    clocks.start()
     bufs = {}
     for dt, size in cases:
         sends = to_device(inputs.workload2(size, dt), dt)
@@ -199,15 +203,33 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     inner = args.inner
 
+    # One CUDA graph per (dtype, size, algorithm) holding `inner` back-to-back
+    # calls (decode-style replay: no host work per call).  The calls are
+    # prepared with the capture stream so they are recorded into the graph.
+    cap = torch.cuda.Stream()
+    graphs = {}
+    for dt, size in cases:
+        sp, rp, count, _, _ = bufs[(dt, size)]
+        for algo in ALGOS:
+            f = comm.prepare(sp, rp, count, dt, algo, stream=cap)
+            f()  # plan/occupancy queries happen outside capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    for _ in range(inner):
+                        f()
+            graphs[(dt, size, algo)] = g
+    torch.cuda.synchronize()
+
     def one_step(events):
         k = 0
         for dt, size in cases:
-            sp, rp, count, _, _ = bufs[(dt, size)]
             for algo in ALGOS:
                 if events is not None:
                     events[k][0].record(stream)
-                for _ in range(inner):
-                    comm.allreduce_ptrs(sp, rp, count, dt, algo)
+                graphs[(dt, size, algo)].replay()
                 if events is not None:
                     events[k][1].record(stream)
                 k += 1
@@ -225,8 +247,6 @@ def run_ours(args, world, rank, local):
                         for _ in range(ncase)] for _ in range(args.steps)]
     step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier(dist)
     torch.cuda.synchronize()
     for s in range(args.steps):
@@ -236,7 +256,6 @@ def run_ours(args, world, rank, local):
         step_events[s][1].record(stream)
     torch.cuda.synchronize()
     barrier(dist)
-    clk = clocks.stop()
     st = comm.status()[0]
     if st != rra.OK:
         raise RuntimeError("device status after timed region: %s" % rra.STATUS_NAMES.get(st))
@@ -250,6 +269,7 @@ def run_ours(args, world, rank, local):
                     for s in range(args.steps)]
             us_call[(dt, size, algo)] = measure.median(vals)
             k += 1
+    stream_us = stream_launch_us(comm, bufs, cases, torch, stream)
     best = {(dt, size): min(ALGOS, key=lambda a: us_call[(dt, size, a)]) for dt, size in cases}
     best_us = [us_call[(dt, size, best[(dt, size)])] for dt, size in cases]
     value = float(np.mean(best_us))
@@ -273,6 +293,7 @@ def run_ours(args, world, rank, local):
                 "note": "at <= 1 MiB the kernels are latency-bound; see floor"}
 
     floor = latency_floor(comm, rra, measure, torch, stream)
+    clk = clocks.stop()
     bandwidth = bandwidth_end(rra, measure, torch, hbm_peak, args)
     e2e = end_to_end(comm, rra, cases, best, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
@@ -297,6 +318,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "clocks": clk,
         "per_algo_mean_us": {a: round(v, 3) for a, v in per_algo_mean.items()},
+        "stream_launch_us": stream_us,
         "per_size_us": {"%s/%d" % (dt, size): {a: round(us_call[(dt, size, a)], 3) for a in ALGOS}
                         for dt, size in cases},
         "best_algo": {"%s/%d" % k: v for k, v in best.items()},
@@ -310,6 +332,30 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def stream_launch_us(comm, bufs, cases, torch, stream, reps=400):
+    """The same calls launched one by one from Python on a stream (prepared
+    arguments): host-bound, reported next to the graph figure."""
+    out = {}
+    for dt, size in [c for c in cases if c[1] in (128, 65536, 1 << 20)]:
+        sp, rp, count, _, _ = bufs[(dt, size)]
+        for algo in ALGOS:
+            f = comm.prepare(sp, rp, count, dt, algo)
+            for _ in range(20):
+                f()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            e0.record(stream)
+            for _ in range(reps):
+                f()
+            e1.record(stream)
+            host = (time.perf_counter() - t0) / reps * 1e6
+            torch.cuda.synchronize()
+            out["%s/%d/%s" % (dt, size, algo)] = {"gpu_us": round(e0.elapsed_time(e1) * 1000.0 / reps, 3),
+                                                  "host_us": round(host, 3)}
+    return out
 
 
 def latency_floor(comm, rra, measure, torch, stream):

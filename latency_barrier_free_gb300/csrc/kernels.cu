@@ -120,7 +120,7 @@ __device__ __noinline__ bool epoch_scrub(const Params& p, int rank) {
             fence_acq_rel_gpu();
             st_relaxed_u32(&p.ctrl->scrub_gen, gen + 1u);
         } else {
-            Waiter w{globaltimer_ns() + p.timeout_ns, p.ctrl, rank, -2, 0u};
+            Waiter w = make_waiter(globaltimer_ns(), p.timeout_ns, p.ctrl, rank, -2);
             while (ld_relaxed_u32(&p.ctrl->scrub_gen) == gen) {
                 if (waiter_expired(w)) { ok = 0; break; }
             }
@@ -207,6 +207,42 @@ __device__ __forceinline__ bool poll_batch(const char* slot0, uint64_t slot_stri
     return true;
 }
 
+// One-shot push of this thread's positions v0, v0 + T, ... < end: the input
+// loads of kPushPos positions are issued together, then each vector is stored
+// into slot [parity][r] of every peer (consecutive lanes store consecutive
+// vectors of the same peer window, so the stores coalesce).
+constexpr int kPushPos = 4;
+
+template <typename T, bool kLL>
+__device__ __forceinline__ void push_positions(const Params& p, int r, uint32_t base, uint32_t v0, uint32_t end,
+                                               uint64_t par_off, uint32_t ep) {
+    constexpr int U = VecMath<T>::kUnitBytes;
+    constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
+    const uint32_t T_ = blockDim.x;
+    const int N = p.nranks;
+#pragma unroll 1
+    for (; v0 < end; v0 += kPushPos * T_) {
+        uint4 x[kPushPos];
+#pragma unroll
+        for (int j = 0; j < kPushPos; ++j) {
+            const uint32_t v = v0 + (uint32_t)j * T_;
+            if (v < end) x[j] = load_input<T>(p.send[r], base + v, p.count);
+        }
+#pragma unroll
+        for (int j = 0; j < kPushPos; ++j) {
+            const uint32_t v = v0 + (uint32_t)j * T_;
+            if (v >= end) break;
+            char* dst = p.win0 + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kPosBytes;
+#pragma unroll 1
+            for (int q = 0; q < N; ++q, dst += p.stride) {
+                if (q == r) continue;
+                if (kLL) ll_store(dst, x[j], ep);
+                else st_scratch<U>(dst, x[j]);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------- one-shot (push) ----
 // Sec. III-A "One-shot" in push mode + Sec. IV "LL" / "Sentinel"; the
 // bcast() of Fig. 9: each rank stores its chunk into every peer's slot, then
@@ -220,7 +256,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
     const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
     const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r) + p.region_off;
-    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -233,19 +269,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
         // push: my chunk into slot [parity][r] of every peer
-        if (!s.drop) {
-#pragma unroll 1
-            for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
-                const uint4 x = load_input<T>(p.send[r], base + v, p.count);
-                char* dst = p.win0 + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kPosBytes;
-#pragma unroll 1
-                for (int q = 0; q < N; ++q, dst += p.stride) {
-                    if (q == r) continue;
-                    if (kLL) ll_store(dst, x, ep);
-                    else st_scratch<U>(dst, x);
-                }
-            }
-        }
+        if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep);
         // receive: poll the N-1 incoming slots, reduce in rank order
 #pragma unroll 1
         for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
@@ -280,7 +304,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
 // as the narrow variant.  Positions are processed in rounds of `R` so the
 // stage fits.  A thread that gives up raises a shared flag; the whole CTA
 // leaves at the next block barrier.
-constexpr int kStageVecs = 3072;  // 48 KiB of shared memory
+constexpr int kStageVecs = kWideStageVecs;  // 48 KiB of shared memory
 
 template <typename T, bool kLL>
 __device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaState& s, uint4* stage, int* fail) {
@@ -293,7 +317,7 @@ __device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaStat
     const uint32_t pos1 = pos0 + p.per_cta;
     const uint32_t R = (uint32_t)(kStageVecs / N);
     char* const mine = window(p, r) + p.region_off;
-    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -302,24 +326,11 @@ __device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaStat
         const uint64_t par_off = (e & 1ull) * p.parity_bytes;
         const uint32_t base = k * p.chunk_vecs;
         const uint32_t end = min(pos1, min(p.chunk_vecs, p.nvec - base));
-        const uint32_t npos = end > pos0 ? end - pos0 : 0u;
         w.step = (int)k;
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
-        // push: item i = (peer q = i / npos, position pos0 + i % npos)
-        if (!s.drop) {
-            const uint32_t items = npos * (uint32_t)N;
-#pragma unroll 1
-            for (uint32_t i = threadIdx.x; i < items; i += T_) {
-                const int q = (int)(i / npos);
-                if (q == r) continue;
-                const uint32_t v = pos0 + i % npos;
-                const uint4 x = load_input<T>(p.send[r], base + v, p.count);
-                char* dst = window(p, q) + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kPosBytes;
-                if (kLL) ll_store(dst, x, ep);
-                else st_scratch<U>(dst, x);
-            }
-        }
+        // push: thread per position, as in the narrow variant
+        if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep);
 #pragma unroll 1
         for (uint32_t r0 = pos0; r0 < end; r0 += R) {
             const uint32_t rn = min(R, end - r0);
@@ -427,7 +438,7 @@ __device__ __forceinline__ bool oneshot_barrier_body(const Params& p, const CtaS
     const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
     const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r) + p.region_off;
-    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(512) barrier_probe_kernel(const __grid_constan
     CtaState s = cta_prologue(p);
     s.skip = __syncthreads_or(s.skip) != 0;
     if (!s.skip) {
-        Waiter w{s.t_start + p.timeout_ns, p.ctrl, s.rank, 0, 0u};
+        Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, s.rank, 0);
         uint64_t t_first = 0;
 #pragma unroll 1
         for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -538,6 +549,8 @@ struct Split {
     __device__ __forceinline__ uint32_t vec(int q, uint32_t v) const { return base + (uint32_t)q * part + v; }
 };
 
+constexpr int kLoadParts = 8;  // partitions whose input vectors are loaded together
+
 // The last step shrinks its partitions so the remaining vectors spread over
 // all owners; positions stay a prefix of the full-step positions.
 __device__ __forceinline__ Split split_step(const Params& p, uint32_t k) {
@@ -557,7 +570,7 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
     const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
     const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r);
-    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -568,15 +581,25 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
         w.step = (int)k;
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
-        // ReduceScatter push: part q of my input -> owner q's RS slot [r]
+        // ReduceScatter push: part q of my input -> owner q's RS slot [r];
+        // the inputs of kLoadParts partitions are loaded together
         if (!s.drop) {
 #pragma unroll 1
             for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
-                char* dst = p.win0 + p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+                const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
 #pragma unroll 1
-                for (int q = 0; q < N; ++q, dst += p.stride) {
-                    if (q == r || v >= sp.valid(q)) continue;
-                    st_scratch<U>(dst, load_input<T>(p.send[r], sp.vec(q, v), p.count));
+                for (int q0 = 0; q0 < N; q0 += kLoadParts) {
+                    uint4 x[kLoadParts];
+#pragma unroll
+                    for (int j = 0; j < kLoadParts; ++j) {
+                        const int q = q0 + j;
+                        if (q < N && q != r && v < sp.valid(q)) x[j] = load_input<T>(p.send[r], sp.vec(q, v), p.count);
+                    }
+#pragma unroll
+                    for (int j = 0; j < kLoadParts; ++j) {
+                        const int q = q0 + j;
+                        if (q < N && q != r && v < sp.valid(q)) st_scratch<U>(window(p, q) + off, x[j]);
+                    }
                 }
             }
         }
@@ -747,7 +770,7 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
     const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;       // per_cta is a multiple of 32
     const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r);
-    Waiter w{s.t_start + p.timeout_ns, p.ctrl, r, 0, 0u};
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
     const uint32_t target = (uint32_t)(N - 1);
 
 #pragma unroll 1
@@ -766,11 +789,20 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
 #pragma unroll 1
             for (uint32_t g0 = pos0 + wbase; g0 < end; g0 += blockDim.x) {
                 const uint32_t v = g0 + lane;
-                char* dst = p.win0 + p.region_off + par * p.parity_bytes + (uint64_t)v * kAccBytes;
+                const uint64_t off = p.region_off + par * p.parity_bytes + (uint64_t)v * kAccBytes;
 #pragma unroll 1
-                for (int q = 0; q < N; ++q, dst += p.stride) {
-                    if (q == r || v >= sp.valid(q)) continue;
-                    A::red(dst, load_input<T>(p.send[r], sp.vec(q, v), p.count));
+                for (int q0 = 0; q0 < N; q0 += kLoadParts) {
+                    uint4 x[kLoadParts];
+#pragma unroll
+                    for (int j = 0; j < kLoadParts; ++j) {
+                        const int q = q0 + j;
+                        if (q < N && q != r && v < sp.valid(q)) x[j] = load_input<T>(p.send[r], sp.vec(q, v), p.count);
+                    }
+#pragma unroll
+                    for (int j = 0; j < kLoadParts; ++j) {
+                        const int q = q0 + j;
+                        if (q < N && q != r && v < sp.valid(q)) A::red(window(p, q) + off, x[j]);
+                    }
                 }
             }
             __syncwarp();

@@ -199,17 +199,26 @@ __device__ __forceinline__ uint4 ld_scratch(const void* p) {
 }
 
 // ------------------------------------------------------- bounded waits ----
-// Every spin is bounded: each 64th iteration reads %globaltimer and the
-// status word.  Past the deadline the waiter records RRA_ERR_TIMEOUT (first
-// writer wins) and gives up; if another CTA already recorded an error it
-// gives up too, so all CTAs of a failed call leave promptly.
+// Every spin is bounded: each 64th iteration reads %globaltimer.  Past the
+// deadline the waiter records RRA_ERR_TIMEOUT (first writer wins) and gives
+// up.  Once a wait has lasted kStatusAfterNs it also reads the status word,
+// so that when another CTA has already recorded an error all CTAs of a failed
+// call leave promptly; normal (short) waits never touch that shared line.
+constexpr uint64_t kStatusAfterNs = 20000;
+
 struct Waiter {
-    uint64_t deadline;
+    uint64_t deadline;      // give up after this %globaltimer value
+    uint64_t status_after;  // read the status word only after this value
     Ctrl* ctrl;
     int rank;
     int step;
     uint32_t spins;
 };
+
+__device__ __forceinline__ Waiter make_waiter(uint64_t start_ns, uint64_t timeout_ns, Ctrl* ctrl, int rank,
+                                              int step) {
+    return Waiter{start_ns + timeout_ns, start_ns + kStatusAfterNs, ctrl, rank, step, 0u};
+}
 
 __device__ __noinline__ void record_error(Ctrl* ctrl, uint32_t code, int rank, int step) {
     if (atomicCAS(&ctrl->status, 0u, code) == 0u) {
@@ -221,12 +230,12 @@ __device__ __noinline__ void record_error(Ctrl* ctrl, uint32_t code, int rank, i
 // Returns true if the caller must give up.
 __device__ __forceinline__ bool waiter_expired(Waiter& w) {
     if ((++w.spins & 63u) != 0u) return false;
-    if (ld_relaxed_u32(&w.ctrl->status) != 0u) return true;
-    if (globaltimer_ns() > w.deadline) {
+    const uint64_t now = globaltimer_ns();
+    if (now > w.deadline) {
         record_error(w.ctrl, RRA_ERR_TIMEOUT, w.rank, w.step);
         return true;
     }
-    return false;
+    return now > w.status_after && ld_relaxed_u32(&w.ctrl->status) != 0u;
 }
 
 // ----------------------------------------------------- dtype handling ----

@@ -336,7 +336,7 @@ rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, 
 
 // Fills everything in Params except the pointer tables.
 static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo,
-                              Params* p, int* kind_out) {
+                              Params* p, int* kind_out, int* threads_out) {
     const size_t es = elem_size(dtype);
     const size_t ve = rra::kVecBytes / es;
     const size_t n = (size_t)c->nranks;
@@ -444,14 +444,24 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     }
     int64_t cap_ctas = cmax;
     if (algo == RRA_ONESHOT_BARRIER) cap_ctas = std::min<int64_t>(cap_ctas, rra::kBarrierCtas);
+    const bool wide = kind == rra::kKindOneshotLLWide || kind == rra::kKindOneshotSentinelWide;
+    // positions per CTA to aim for: one per thread, or, for the wide variant,
+    // as many as one shared-memory stage round holds
+    const size_t target = wide ? std::max<size_t>(32, (size_t)rra::kWideStageVecs / n) : T;
     if (c->ctas_per_rank > 0) ctas = std::min<int64_t>(c->ctas_per_rank, cap_ctas);
-    else ctas = std::min<int64_t>((int64_t)ceil_div(work, T), cap_ctas);
+    else ctas = std::min<int64_t>((int64_t)ceil_div(work, target), cap_ctas);
     ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)work));
     size_t per = ceil_div(work, (size_t)ctas);
     if (algo == RRA_LL128_ATOMIC) per = align_up(per, rra::kGroupVecs);
     ctas = (int64_t)ceil_div(work, per);
     p->ctas_per_rank = (int32_t)ctas;
     p->per_cta = (uint32_t)per;
+    // Small CTAs for small per-CTA work (fewer idle warps to launch and
+    // retire); never below 64 threads (the barrier baseline needs one thread
+    // per rank), never above the occupancy-checked size.
+    int threads = (int)T;
+    if (!wide) threads = (int)std::min<size_t>(T, std::max<size_t>(64, align_up(per, 32)));
+    *threads_out = threads;
     return RRA_OK;
 }
 
@@ -460,8 +470,8 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     if (c == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0) return RRA_ERR_INVALID_ARG;
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
     Params p;
-    int kind = 0;
-    rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind);
+    int kind = 0, threads = 0;
+    rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
     if (st != RRA_OK) return st;
     if (grid_ctas) *grid_ctas = p.nranks * p.ctas_per_rank;
     if (steps) *steps = (int)p.nsteps;
@@ -477,10 +487,10 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     const size_t es = elem_size(dtype);
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
     Params p;
-    int kind = 0;
+    int kind = 0, threads = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind);
+        rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
         if (st != RRA_OK) return st;
     }
     for (int r = 0; r < c->nranks; ++r) {
@@ -489,7 +499,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
-    cudaError_t e = rra::launch_allreduce(p, dtype, kind, c->threads, (cudaStream_t)stream, c->cooperative != 0);
+    cudaError_t e = rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
         return RRA_ERR_NOT_CORESIDENT;
@@ -587,11 +597,11 @@ rra_status_t rra_comm_barrier_latency(rra_comm_t c, int iters, double* ns_per_ba
     if (c == nullptr || ns_per_barrier == nullptr || iters < 2 || iters > (1 << 24)) return RRA_ERR_INVALID_ARG;
     if (c->poisoned) return RRA_ERR_POISONED;
     Params p;
-    int kind = 0;
+    int kind = 0, threads = 0;
     rra_status_t st;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        st = plan_call(c, 1, RRA_FP32, RRA_ONESHOT_BARRIER, &p, &kind);
+        st = plan_call(c, 1, RRA_FP32, RRA_ONESHOT_BARRIER, &p, &kind, &threads);
     }
     if (st != RRA_OK) return st;
     uint64_t* dt = nullptr;

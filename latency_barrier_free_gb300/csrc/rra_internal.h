@@ -81,6 +81,7 @@ enum KernelKind {
     kNumKinds = 8
 };
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
+constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors
 
 // Host-side launch entry points (kernels.cu).
 cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
