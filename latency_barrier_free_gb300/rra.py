@@ -36,6 +36,7 @@ SYMBOLS = [
     "rra_comm_barrier_latency", "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string",
     "rra_version",
     "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_sm_count",
+    "rra_allreduce_static",
 ]
 
 
