@@ -88,11 +88,16 @@ typedef enum {
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
     RRA_ATTR_ONESHOT_WIDE = 6,     /* one-shot polls split a position's sources over
                                       threads: -1 auto (N >= 16, default), 0 off, 1 on */
-    RRA_ATTR_COOPERATIVE = 7       /* 1 (default): cooperative launch, so the driver
+    RRA_ATTR_COOPERATIVE = 7,      /* 1 (default): cooperative launch, so the driver
                                       guarantees that all CTAs are resident together;
                                       0: plain launch of the same occupancy-checked grid
                                       (progress then relies on no other work holding the
                                       SMs for longer than the poll time limit) */
+    RRA_ATTR_PDL = 8               /* 1: programmatic dependent launch, so the next
+                                      kernel on the stream is scheduled while this one
+                                      drains; each kernel waits (griddepcontrol.wait)
+                                      for its predecessor before touching memory.
+                                      0 (default): plain stream order */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -210,6 +215,13 @@ rra_status_t rra_comm_max_coresident(rra_comm_t comm, rra_dtype_t dtype, rra_alg
  * %globaltimer start and end (ns) at dev_buf[2*cta] and dev_buf[2*cta+1].
  * NULL switches timing off.  The caller owns the buffer. */
 rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
+
+/* Optional in-kernel trace (diagnostics).  `dev_buf` holds 6 uint64_t per
+ * CTA of the largest grid; while set, thread 0 of every one-shot CTA (narrow
+ * variant) records %globaltimer at: start, control words read, first push
+ * issued, first position polled and reduced, its output stored, end.  Entries
+ * a kernel does not reach stay unchanged.  NULL switches tracing off. */
+rra_status_t rra_comm_set_trace(rra_comm_t comm, uint64_t* dev_buf);
 
 /* Fault injection for tests (host-side injection only; no GPU fault): while
  * set, virtual rank `rank` skips every store to its peers, so the peers'

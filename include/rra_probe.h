@@ -48,6 +48,12 @@ rra_status_t rra_probe_pingpong(int cta_a, int cta_b, int iters,
  * and graph-node overhead next to the AllReduce. */
 rra_status_t rra_probe_empty_kernel(rra_stream_t stream);
 
+/* Launch `ctas` x `threads` empty CTAs on `stream` (cooperative if
+ * `cooperative`), with a 1152-byte parameter block if `big_params` (the size
+ * of the AllReduce kernels' parameters) or none: separates launch and
+ * graph-node cost by grid shape, parameter size and launch kind. */
+rra_status_t rra_probe_launch_shape(int ctas, int threads, int big_params, int cooperative, rra_stream_t stream);
+
 /* Number of SMs of the current device. */
 rra_status_t rra_probe_sm_count(int* sms);
 

@@ -138,6 +138,12 @@ __device__ __noinline__ bool epoch_scrub(const Params& p, int rank) {
 // overwrite epoch slot b before every thread of the CTA has read it.
 __device__ __forceinline__ CtaState cta_prologue(const Params& p) {
     CtaState s;
+    // Programmatic dependent launch: let the next kernel on the stream be
+    // scheduled now (it waits in its own griddepcontrol.wait), and wait until
+    // the previous kernel has completed and its memory is visible before this
+    // one touches global memory.  Both are no-ops without the launch attribute.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     s.t_start = globaltimer_ns();
     s.rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
     s.sub = (int)(blockIdx.x % (unsigned)p.ctas_per_rank);
@@ -169,7 +175,14 @@ __device__ __forceinline__ void cta_epilogue(const Params& p, const CtaState& s)
             st_relaxed_u64(&p.ctrl->epoch[slot], next);
         }
     }
-    if (p.timing != nullptr && threadIdx.x == 0) p.timing[2 * blockIdx.x + 1] = globaltimer_ns();
+    if (threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        if (p.timing != nullptr) p.timing[2 * blockIdx.x + 1] = t_end;
+        if (p.trace != nullptr) {
+            p.trace[(uint64_t)blockIdx.x * kTracePoints] = s.t_start;
+            p.trace[(uint64_t)blockIdx.x * kTracePoints + 5] = t_end;
+        }
+    }
 }
 
 constexpr int kBatch = 4;  // sources polled with loads in flight at once
@@ -257,6 +270,9 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
     const uint32_t pos1 = pos0 + p.per_cta;
     char* const mine = window(p, r) + p.region_off;
     Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
+    uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
+                                                                   : nullptr;
+    if (tr) tr[1] = globaltimer_after(s.epoch);
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -270,6 +286,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
 
         // push: my chunk into slot [parity][r] of every peer
         if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep);
+        if (tr && k == 0) tr[2] = globaltimer_ns();
         // receive: poll the N-1 incoming slots, reduce in rank order
 #pragma unroll 1
         for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
@@ -290,7 +307,10 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
                     if (!kLL && q != r) st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
                 }
             }
-            store_output<T>(p.recv[r], base + v, p.count, M::store(acc));
+            const uint4 out = M::store(acc);
+            if (tr && k == 0 && v == pos0) tr[3] = globaltimer_after(out.x);
+            store_output<T>(p.recv[r], base + v, p.count, out);
+            if (tr && k == 0 && v == pos0) tr[4] = globaltimer_ns();
         }
     }
     return true;
@@ -972,7 +992,7 @@ cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_
 }
 
 cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
-                             bool cooperative) {
+                             bool cooperative, bool pdl) {
     const void* k = kernel_for(dtype, kind);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -980,11 +1000,20 @@ cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int t
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = cooperative ? 1 : 0;
+    cfg.numAttrs = n;
     void* args[] = {(void*)&p};
     return cudaLaunchKernelExC(&cfg, k, args);
 }

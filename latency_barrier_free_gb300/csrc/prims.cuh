@@ -121,6 +121,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// %globaltimer read that waits for `dep` (a value produced by an earlier load):
+// the read is control-dependent on it, so the stamp is taken after that load
+// has returned.  Diagnostics only.
+__device__ __forceinline__ uint64_t globaltimer_after(uint64_t dep) {
+    if (dep == 0x5A5A5A5A5A5A5A5Aull) return 0ull;
+    return globaltimer_ns();
+}
+
 // ---------------------------------------------------------- LL packing ----
 // One 16-byte payload vector (four 32-bit words) travels as two 16-byte LL
 // lines; every 64-bit element carries {payload word (low), epoch (high)}.

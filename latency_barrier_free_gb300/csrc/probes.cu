@@ -89,6 +89,12 @@ __global__ void pingpong_kernel(uint32_t* flags, int cta_a, int cta_b, int warm,
 
 __global__ void empty_kernel() {}
 
+struct BigParams {
+    uint64_t words[144];  // 1152 bytes, the size of the AllReduce parameter block
+};
+// The launch copies the parameter block whether or not the body reads it.
+__global__ void empty_kernel_big(const __grid_constant__ BigParams p) { (void)p; }
+
 }  // namespace
 
 extern "C" {
@@ -178,6 +184,32 @@ rra_status_t rra_probe_pingpong(int cta_a, int cta_b, int iters, double* ns_roun
 rra_status_t rra_probe_empty_kernel(rra_stream_t stream) {
     empty_kernel<<<1, 32, 0, (cudaStream_t)stream>>>();
     return cudaGetLastError() == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+}
+
+rra_status_t rra_probe_launch_shape(int ctas, int threads, int big_params, int cooperative, rra_stream_t stream) {
+    if (ctas < 1 || ctas > 4096 || threads < 32 || threads > 1024) return RRA_ERR_INVALID_ARG;
+    static BigParams bp = {};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cooperative ? 1 : 0;
+    cudaError_t e;
+    if (big_params) {
+        void* args[] = {(void*)&bp};
+        e = cudaLaunchKernelExC(&cfg, (const void*)empty_kernel_big, args);
+    } else {
+        e = cudaLaunchKernelExC(&cfg, (const void*)empty_kernel, nullptr);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RRA_ERR_CUDA;
+    }
+    return RRA_OK;
 }
 
 }  // extern "C"

@@ -89,8 +89,10 @@ struct rra_comm {
     int blocks_per_sm[3][rra::kNumKinds];  // by dtype, kernel kind; -1 = not queried
     int64_t oneshot_wide = -1;              // -1 auto (N >= 16), 0 never, 1 always
     int64_t cooperative = 1;                // cooperative launch (co-residency guaranteed)
+    int64_t pdl = 0;                        // programmatic dependent launch
     bool poisoned = false;
     uint64_t* timing = nullptr;
+    uint64_t* trace = nullptr;
     // rra_allreduce_host staging (allocated on first use)
     char* stage = nullptr;
     size_t stage_slot = 0;
@@ -294,6 +296,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < 0 || v > 1) return RRA_ERR_INVALID_ARG;
             c->cooperative = v;
             return RRA_OK;
+        case RRA_ATTR_PDL:
+            if (v < 0 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->pdl = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -309,6 +315,7 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_ONESHOT_CHUNK: *v = c->os_chunk; return RRA_OK;
         case RRA_ATTR_ONESHOT_WIDE: *v = c->oneshot_wide; return RRA_OK;
         case RRA_ATTR_COOPERATIVE: *v = c->cooperative; return RRA_OK;
+        case RRA_ATTR_PDL: *v = c->pdl; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -353,6 +360,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     p->win0 = c->win0;
     p->ctrl = c->ctrl;
     p->timing = c->timing;
+    p->trace = c->trace;
     p->stride = L.window_stride;
     p->count = count;
     p->nvec = (uint32_t)ceil_div(count, ve);
@@ -499,7 +507,8 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
-    cudaError_t e = rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0);
+    cudaError_t e = rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0,
+                                          c->pdl != 0);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
         return RRA_ERR_NOT_CORESIDENT;
@@ -647,6 +656,13 @@ rra_status_t rra_comm_set_epoch(rra_comm_t c, uint64_t epoch) {
     const cudaError_t e = cudaMemcpy(c->ctrl->epoch, h, sizeof(uint64_t) * rra::kEpochSlots, cudaMemcpyHostToDevice);
     free(h);
     return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+}
+
+rra_status_t rra_comm_set_trace(rra_comm_t c, uint64_t* dev_buf) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(c->mu);
+    c->trace = dev_buf;
+    return RRA_OK;
 }
 
 rra_status_t rra_comm_inject_drop(rra_comm_t c, int rank) {

@@ -44,6 +44,7 @@ struct Params {
     char* win0;            // window 0 (window r = win0 + r * stride)
     Ctrl* ctrl;
     uint64_t* timing;      // optional: (start, end) %globaltimer per CTA
+    uint64_t* trace;       // optional: kTracePoints %globaltimer stamps per CTA (one-shot)
     uint64_t stride;       // bytes between windows
     uint64_t count;        // elements per rank
     uint64_t timeout_ns;   // limit of every wait
@@ -82,10 +83,11 @@ enum KernelKind {
 };
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors
+constexpr int kTracePoints = 6;       // start, control words read, pushed, polled, stored, end
 
 // Host-side launch entry points (kernels.cu).
 cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
-                             bool cooperative = true);
+                             bool cooperative = true, bool pdl = false);
 cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);

@@ -25,17 +25,19 @@ ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomi
          "oneshot_barrier": 4}
 BARRIER_FREE = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic")
 ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,
-         "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6, "cooperative": 7}
+         "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6, "cooperative": 7, "pdl": 8}
 MAX_RANKS = 64
 
 # Exported symbols, in declaration order of the public headers.
 SYMBOLS = [
     "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_comm_status", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
-    "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_inject_drop",
+    "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
+    "rra_comm_inject_drop",
     "rra_comm_barrier_latency", "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string",
     "rra_version",
-    "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_sm_count",
+    "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_launch_shape",
+    "rra_probe_sm_count",
     "rra_allreduce_static",
 ]
 
@@ -88,6 +90,7 @@ def load(path: str = LIB_PATH):
             "rra_comm_plan_call": ([vp, sz, i32, i32, ip, ip], i32),
             "rra_comm_max_coresident": ([vp, i32, i32, ip], i32),
             "rra_comm_set_timing": ([vp, vp], i32),
+            "rra_comm_set_trace": ([vp, vp], i32),
             "rra_comm_inject_drop": ([vp, i32], i32),
             "rra_comm_barrier_latency": ([vp, i32, ctypes.POINTER(ctypes.c_double)], i32),
             "rra_comm_get_epoch": ([vp, ctypes.POINTER(ctypes.c_uint64)], i32),
@@ -98,6 +101,7 @@ def load(path: str = LIB_PATH):
             "rra_probe_pingpong": ([i32, i32, i32, ctypes.POINTER(ctypes.c_double), ip, ip], i32),
             "rra_probe_empty_kernel": ([vp], i32),
             "rra_probe_sm_count": ([ip], i32),
+            "rra_probe_launch_shape": ([i32, i32, i32, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -280,6 +284,9 @@ class Comm:
     def set_epoch(self, epoch: int):
         _check(self._lib.rra_comm_set_epoch(self._h, int(epoch)), "rra_comm_set_epoch")
 
+    def set_trace(self, dev_ptr):
+        _check(self._lib.rra_comm_set_trace(self._h, ctypes.c_void_p(dev_ptr or 0)), "rra_comm_set_trace")
+
     def inject_drop(self, rank: int):
         _check(self._lib.rra_comm_inject_drop(self._h, int(rank)), "rra_comm_inject_drop")
 
@@ -302,6 +309,11 @@ def probe_pingpong(cta_a: int, cta_b: int, iters: int = 20000):
 
 def probe_empty_kernel(stream=None):
     _check(load().rra_probe_empty_kernel(_stream_handle(stream)), "rra_probe_empty_kernel")
+
+
+def probe_launch_shape(ctas: int, threads: int, big_params: bool, cooperative: bool, stream=None):
+    _check(load().rra_probe_launch_shape(int(ctas), int(threads), int(bool(big_params)), int(bool(cooperative)),
+                                         _stream_handle(stream)), "rra_probe_launch_shape")
 
 
 def probe_sm_count() -> int:

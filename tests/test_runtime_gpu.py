@@ -225,3 +225,24 @@ def test_plain_launch_matches_cooperative(algo):
         torch.cuda.synchronize()
         assert comm.status()[0] == rra.OK
         check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS + ("oneshot_barrier",))
+def test_programmatic_dependent_launch(algo):
+    """With programmatic dependent launch each kernel waits for its
+    predecessor before touching memory: back-to-back calls (stream and graph)
+    stay exact."""
+    n, count, calls = 4, 20000, 12
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("pdl", 1)
+        for coop in (1, 0):
+            comm.set_attr("cooperative", coop)
+            host = [inputs.normal(inputs.rng(75, coop, i), n, count, "fp32") for i in range(calls)]
+            send = [to_device(h, "fp32") for h in host]
+            recv = [poison_like(s) for s in send]
+            for i in range(calls):
+                comm.allreduce(send[i], recv[i], algo)
+            torch.cuda.synchronize()
+            assert comm.status()[0] == rra.OK
+            for i in range(calls):
+                check_against_oracle(host[i], to_host(recv[i], "fp32"), "fp32", algo)
