@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 
 NRANKS = 4
 DTYPES = ("fp32", "bf16")
-ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic")
+ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct")
 ELEM = {"fp32": 4, "bf16": 2, "fp64": 8}
 METRIC = "AllReduce us/call at 128B-1MB; GB/s vs HBM roofline; N virtual ranks, 1 GB300"
 WORKLOAD = "N=4 virtual ranks, 128 B-1 MiB per rank (14 sizes), fp32+bf16 N(0,1), 4 algorithms"
@@ -285,7 +285,8 @@ def run_ours(args, world, rank, local):
     dom_bytes = measure.algorithmic_bytes(NRANKS, dom_size)
     achieved = dom_bytes / (us_call[dom] * 1e-6) / 1e9
     kname = {"oneshot_ll": "oneshot_kernel", "oneshot_sentinel": "oneshot_kernel",
-             "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel"}[dom_algo]
+             "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel",
+             "twoshot_direct": "twoshot_kernel"}[dom_algo]
     dom_cfg = "%s N=%d %s %dB" % (dom_algo, NRANKS, dom_dt, dom_size)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": committed_traffic(kname, dom_cfg),
@@ -429,7 +430,8 @@ def latency_floor(comm, rra, measure, torch, stream):
 
 
 def bandwidth_end(rra, measure, torch, hbm_peak, args):
-    """twoshot_dbuf, N=8, binary32, inputs and outputs far larger than L2."""
+    """The two-shot kernels at N=8, binary32, inputs and outputs far larger
+    than L2 (4 GiB of inputs at 512 MiB per rank)."""
     out = {}
     n = 8
     sizes = [64 << 20] + ([512 << 20] if args.big else [])
@@ -440,27 +442,27 @@ def bandwidth_end(rra, measure, torch, hbm_peak, args):
         with rra.Comm(n, size) as c:
             xs = [torch.rand(count, device="cuda", generator=gen) * 2 - 1 for _ in range(n)]
             ys = [torch.empty_like(x) for x in xs]
-            for _ in range(2):
-                c.allreduce(xs, ys, "twoshot_dbuf")
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 5
-            e0.record()
-            for _ in range(reps):
-                c.allreduce(xs, ys, "twoshot_dbuf")
-            e1.record()
-            torch.cuda.synchronize()
-            st = c.status()[0]
-            t = e0.elapsed_time(e1) / 1000.0 / reps
-            gbs = measure.hbm_gbs(n, size, t)
-            out["%dMiB" % (size >> 20)] = {"ms": round(t * 1000, 3), "GB/s": round(gbs, 1),
-                                            "frac": round(gbs / hbm_peak, 4),
-                                            "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1),
-                                            "status": rra.STATUS_NAMES.get(st)}
+            for algo in ("twoshot_dbuf", "twoshot_direct"):
+                for _ in range(2):
+                    c.allreduce(xs, ys, algo)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 5
+                e0.record()
+                for _ in range(reps):
+                    c.allreduce(xs, ys, algo)
+                e1.record()
+                torch.cuda.synchronize()
+                st = c.status()[0]
+                t = e0.elapsed_time(e1) / 1000.0 / reps
+                gbs = measure.hbm_gbs(n, size, t)
+                out["%s/%dMiB" % (algo, size >> 20)] = {
+                    "ms": round(t * 1000, 3), "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+                    "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1), "status": rra.STATUS_NAMES.get(st)}
             del xs, ys
             torch.cuda.empty_cache()
-    return {"algo": "twoshot_dbuf", "nranks": n, "dtype": "fp32", "bytes": "2*N*M per call", "sizes": out,
-            "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events"}
+    return {"nranks": n, "dtype": "fp32", "bytes": "2*N*M per call", "sizes": out,
+            "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events; default chunking"}
 
 
 def end_to_end(comm, rra, cases, best, torch, args):

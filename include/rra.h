@@ -74,15 +74,19 @@ typedef enum {
     RRA_ONESHOT_SENTINEL = 1,  /* Sec. IV "Sentinel": scratch pre-filled with -NaN, polled */
     RRA_TWOSHOT_DBUF = 2,      /* Sec. III-A two-shot + Sec. IV double buffering, Fig. 4 */
     RRA_LL128_ATOMIC = 3,      /* Fig. 5: atomic adds into the owner's lines, counter == N-1 */
-    RRA_ONESHOT_BARRIER = 4    /* BASELINE, not barrier-free: plain stores + two flag barriers
+    RRA_ONESHOT_BARRIER = 4,   /* BASELINE, not barrier-free: plain stores + two flag barriers
                                   per step (Sec. III-B, the design the paper replaces) */
+    RRA_TWOSHOT_DIRECT = 5     /* two-shot whose AllGather stores the reduced partition
+                                  straight into every rank's output (outputs treated as
+                                  registered symmetric buffers, Sec. II-B): RS as
+                                  RRA_TWOSHOT_DBUF, no AG scratch, one hop per step */
 } rra_algo_t;
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
 typedef enum {
     RRA_ATTR_CTAS_PER_RANK = 0,    /* 0 = chosen per call from the message size */
     RRA_ATTR_POLL_TIMEOUT_MS = 1,  /* limit of every device-side wait (default 1000) */
-    RRA_ATTR_THREADS = 2,          /* threads per CTA: 128, 256 or 512 (default 512) */
+    RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256 */
     RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step, 0 = largest that fits */
     RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step, 0 = largest */
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
@@ -93,11 +97,11 @@ typedef enum {
                                       0: plain launch of the same occupancy-checked grid
                                       (progress then relies on no other work holding the
                                       SMs for longer than the poll time limit) */
-    RRA_ATTR_PDL = 8               /* 1: programmatic dependent launch, so the next
-                                      kernel on the stream is scheduled while this one
-                                      drains; each kernel waits (griddepcontrol.wait)
-                                      for its predecessor before touching memory.
-                                      0 (default): plain stream order */
+    RRA_ATTR_PDL = 8               /* 1 (default): programmatic dependent launch, so
+                                      the next kernel on the stream is scheduled while
+                                      this one drains; each kernel waits
+                                      (griddepcontrol.wait) for its predecessor before
+                                      touching memory.  0: plain stream order */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).

@@ -196,19 +196,31 @@ __device__ __forceinline__ bool poll_once(const char* slot_pos, uint32_t ep, uin
     return sentinel_arrived<VecMath<T>::kUnitBytes>(out);
 }
 
-// Poll the slots of sources q0 .. q0+kBatch-1 (skipping `skip` and sources at
-// or beyond n) with all loads in flight, then spin on the ones not yet
-// arrived.  Returns false if the wait gave up.
-template <typename T, bool kLL>
-__device__ __forceinline__ bool poll_batch(const char* slot0, uint64_t slot_stride, int q0, int n, int skip,
-                                           uint32_t ep, Waiter& w, uint4 (&val)[kBatch]) {
-    bool ok[kBatch];
+// Polling the slots of sources q0 .. q0+kBatch-1 of one position (skipping
+// `skip`, sources at or beyond n, and sources whose `limit` is not above the
+// position): `poll_issue` sends all loads at once, `poll_finish` spins on the
+// ones not yet arrived.  Callers issue the batches of two positions before
+// finishing either, so their round trips overlap.  poll_finish returns false
+// if the wait gave up.
+struct NoLimit {
+    __device__ __forceinline__ bool operator()(int) const { return true; }
+};
+
+template <typename T, bool kLL, typename Has = NoLimit>
+__device__ __forceinline__ void poll_issue(const char* slot0, uint64_t slot_stride, int q0, int n, int skip,
+                                           uint32_t ep, uint4 (&val)[kBatch], bool (&ok)[kBatch],
+                                           Has has = Has()) {
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
         const int q = q0 + j;
         ok[j] = true;
-        if (q < n && q != skip) ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * slot_stride, ep, val[j]);
+        if (q < n && q != skip && has(q)) ok[j] = poll_once<T, kLL>(slot0 + (uint64_t)q * slot_stride, ep, val[j]);
     }
+}
+
+template <typename T, bool kLL>
+__device__ __forceinline__ bool poll_finish(const char* slot0, uint64_t slot_stride, int q0, uint32_t ep,
+                                            Waiter& w, uint4 (&val)[kBatch], bool (&ok)[kBatch]) {
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
         const int q = q0 + j;
@@ -218,6 +230,14 @@ __device__ __forceinline__ bool poll_batch(const char* slot0, uint64_t slot_stri
         }
     }
     return true;
+}
+
+template <typename T, bool kLL>
+__device__ __forceinline__ bool poll_batch(const char* slot0, uint64_t slot_stride, int q0, int n, int skip,
+                                           uint32_t ep, Waiter& w, uint4 (&val)[kBatch]) {
+    bool ok[kBatch];
+    poll_issue<T, kLL>(slot0, slot_stride, q0, n, skip, ep, val, ok);
+    return poll_finish<T, kLL>(slot0, slot_stride, q0, ep, w, val, ok);
 }
 
 // One-shot push of this thread's positions v0, v0 + T, ... < end: the input
@@ -287,29 +307,48 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
         // push: my chunk into slot [parity][r] of every peer
         if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep);
         if (tr && k == 0) tr[2] = globaltimer_ns();
-        // receive: poll the N-1 incoming slots, reduce in rank order
+        // receive: poll the N-1 incoming slots of two positions at a time,
+        // reduce each in rank order
 #pragma unroll 1
-        for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+        for (uint32_t v = pos0 + threadIdx.x; v < end; v += 2 * blockDim.x) {
+            const uint32_t v2 = v + blockDim.x;
+            const bool two = v2 < end;
             const uint4 own = load_input<T>(p.send[r], base + v, p.count);
+            const uint4 own2 = two ? load_input<T>(p.send[r], base + v2, p.count) : make_uint4(0, 0, 0, 0);
             char* const slot0 = mine + par_off + (uint64_t)v * kPosBytes;
-            typename M::Acc acc;
+            char* const slot2 = mine + par_off + (uint64_t)v2 * kPosBytes;
+            typename M::Acc acc, acc2;
 #pragma unroll 1
             for (int q0 = 0; q0 < N; q0 += kBatch) {
-                uint4 val[kBatch];
-                if (!poll_batch<T, kLL>(slot0, p.slot_bytes, q0, N, r, ep, w, val)) return false;
+                uint4 val[kBatch], val2[kBatch];
+                bool ok[kBatch], ok2[kBatch];
+                poll_issue<T, kLL>(slot0, p.slot_bytes, q0, N, r, ep, val, ok);
+                poll_issue<T, kLL>(slot2, p.slot_bytes, q0, two ? N : 0, r, ep, val2, ok2);
+                if (!poll_finish<T, kLL>(slot0, p.slot_bytes, q0, ep, w, val, ok)) return false;
+                if (!poll_finish<T, kLL>(slot2, p.slot_bytes, q0, ep, w, val2, ok2)) return false;
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int q = q0 + j;
                     if (q >= N) break;
                     const uint4 x = (q == r) ? own : val[j];
-                    if (q == 0) acc = M::load(x);
-                    else M::add(acc, x);
-                    if (!kLL && q != r) st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    const uint4 x2 = (q == r) ? own2 : val2[j];
+                    if (q == 0) {
+                        acc = M::load(x);
+                        acc2 = M::load(x2);
+                    } else {
+                        M::add(acc, x);
+                        M::add(acc2, x2);
+                    }
+                    if (!kLL && q != r) {
+                        st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                        if (two) st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    }
                 }
             }
             const uint4 out = M::store(acc);
             if (tr && k == 0 && v == pos0) tr[3] = globaltimer_after(out.x);
             store_output<T>(p.recv[r], base + v, p.count, out);
+            if (two) store_output<T>(p.recv[r], base + v2, p.count, M::store(acc2));
             if (tr && k == 0 && v == pos0) tr[4] = globaltimer_ns();
         }
     }
@@ -405,14 +444,14 @@ __device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaStat
 }
 
 template <typename T, bool kLL>
-__global__ void __launch_bounds__(512) oneshot_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(256) oneshot_kernel(const __grid_constant__ Params p) {
     const CtaState s = cta_prologue(p);
     if (!s.skip) (void)oneshot_body<T, kLL>(p, s);
     cta_epilogue(p, s);
 }
 
 template <typename T, bool kLL>
-__global__ void __launch_bounds__(512) oneshot_wide_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(256) oneshot_wide_kernel(const __grid_constant__ Params p) {
     __shared__ uint4 stage[kStageVecs];
     __shared__ int fail;
     if (threadIdx.x == 0) fail = 0;
@@ -509,7 +548,7 @@ __device__ __forceinline__ bool oneshot_barrier_body(const Params& p, const CtaS
 }
 
 template <typename T>
-__global__ void __launch_bounds__(512) oneshot_barrier_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(256) oneshot_barrier_kernel(const __grid_constant__ Params p) {
     __shared__ int fail;
     if (threadIdx.x == 0) fail = 0;
     CtaState s = cta_prologue(p);
@@ -521,7 +560,7 @@ __global__ void __launch_bounds__(512) oneshot_barrier_kernel(const __grid_const
 // Barrier latency (Fig. 3 analogue): N ranks x 1 CTA run `nsteps` flag
 // barriers back to back; CTA 0 records %globaltimer after the first and after
 // the last barrier in timing[0..1].
-__global__ void __launch_bounds__(512) barrier_probe_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(256) barrier_probe_kernel(const __grid_constant__ Params p) {
     __shared__ int fail;
     if (threadIdx.x == 0) fail = 0;
     CtaState s = cta_prologue(p);
@@ -582,7 +621,12 @@ __device__ __forceinline__ Split split_step(const Params& p, uint32_t k) {
     return sp;
 }
 
-template <typename T>
+// kDirect: the owner stores its reduced partition straight into every rank's
+// output (the output buffers play the part of registered symmetric memory,
+// Sec. II-B), so the AllGather needs no scratch, no poll and no reset: one
+// synchronisation hop per step instead of two.  Outputs are complete when the
+// kernel completes; nothing inside the kernel reads them.
+template <typename T, bool kDirect>
 __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s) {
     using M = VecMath<T>;
     constexpr int U = M::kUnitBytes;
@@ -626,68 +670,92 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
         // Owner: reduce my partition in rank order, push it to every AG slot
         const uint32_t my_end = min(end, sp.valid(r));
 #pragma unroll 1
-        for (uint32_t v = pos0 + threadIdx.x; v < my_end; v += blockDim.x) {
+        for (uint32_t v = pos0 + threadIdx.x; v < my_end; v += 2 * blockDim.x) {
+            const uint32_t v2 = v + blockDim.x;
+            const bool two = v2 < my_end;
             const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
+            const uint4 own2 = two ? load_input<T>(p.send[r], sp.vec(r, v2), p.count) : make_uint4(0, 0, 0, 0);
             char* const slot0 = mine + p.region_off + par_off + (uint64_t)v * kVecBytes;
-            typename M::Acc acc;
+            char* const slot2 = mine + p.region_off + par_off + (uint64_t)v2 * kVecBytes;
+            typename M::Acc acc, acc2;
 #pragma unroll 1
             for (int q0 = 0; q0 < N; q0 += kBatch) {
-                uint4 val[kBatch];
-                if (!poll_batch<T, false>(slot0, p.slot_bytes, q0, N, r, 0u, w, val)) return false;
+                uint4 val[kBatch], val2[kBatch];
+                bool ok[kBatch], ok2[kBatch];
+                poll_issue<T, false>(slot0, p.slot_bytes, q0, N, r, 0u, val, ok);
+                poll_issue<T, false>(slot2, p.slot_bytes, q0, two ? N : 0, r, 0u, val2, ok2);
+                if (!poll_finish<T, false>(slot0, p.slot_bytes, q0, 0u, w, val, ok)) return false;
+                if (!poll_finish<T, false>(slot2, p.slot_bytes, q0, 0u, w, val2, ok2)) return false;
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int q = q0 + j;
                     if (q >= N) break;
                     const uint4 x = (q == r) ? own : val[j];
-                    if (q == 0) acc = M::load(x);
-                    else M::add(acc, x);
-                    if (q != r) st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    const uint4 x2 = (q == r) ? own2 : val2[j];
+                    if (q == 0) {
+                        acc = M::load(x);
+                        acc2 = M::load(x2);
+                    } else {
+                        M::add(acc, x);
+                        M::add(acc2, x2);
+                    }
+                    if (q != r) {
+                        st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                        if (two) st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    }
                 }
             }
-            const uint4 red = M::store(acc);
-            if (!s.drop) {
-                char* dst = p.win0 + p.aux_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !two) break;
+                const uint32_t vv = h ? v2 : v;
+                const uint4 red = M::store(h ? acc2 : acc);
+                if (kDirect) {
+                    if (!s.drop) {
 #pragma unroll 1
-                for (int q = 0; q < N; ++q, dst += p.stride) {
-                    if (q != r) st_scratch<U>(dst, red);
+                        for (int q = 0; q < N; ++q) {
+                            if (q != r) store_output<T>(p.recv[q], sp.vec(r, vv), p.count, red);
+                        }
+                    }
+                } else if (!s.drop) {
+                    char* dst = p.win0 + p.aux_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)vv * kVecBytes;
+#pragma unroll 1
+                    for (int q = 0; q < N; ++q, dst += p.stride) {
+                        if (q != r) st_scratch<U>(dst, red);
+                    }
                 }
+                store_output<T>(p.recv[r], sp.vec(r, vv), p.count, red);
             }
-            store_output<T>(p.recv[r], sp.vec(r, v), p.count, red);
         }
-        // AllGather receive: the N-1 reduced partitions of the other owners
+        // AllGather receive: the N-1 reduced partitions of the other owners,
+        // two positions at a time; sources whose partition does not reach a
+        // position are skipped (the direct variant has nothing to receive)
 #pragma unroll 1
-        for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
+        for (uint32_t v = pos0 + threadIdx.x; !kDirect && v < end; v += 2 * blockDim.x) {
+            const uint32_t v2 = v + blockDim.x;
+            const bool two = v2 < end;
             char* const slot0 = mine + p.aux_off + par_off + (uint64_t)v * kVecBytes;
+            char* const slot2 = mine + p.aux_off + par_off + (uint64_t)v2 * kVecBytes;
+            auto has1 = [&](int q) { return v < sp.valid(q); };
+            auto has2 = [&](int q) { return v2 < sp.valid(q); };
 #pragma unroll 1
             for (int q0 = 0; q0 < N; q0 += kBatch) {
-                // sources whose partition does not reach position v are skipped
-                // by polling them as if they were the caller itself
-                uint4 val[kBatch];
-                bool ok[kBatch];
+                uint4 val[kBatch], val2[kBatch];
+                bool ok[kBatch], ok2[kBatch];
+                poll_issue<T, false>(slot0, p.slot_bytes, q0, N, r, 0u, val, ok, has1);
+                poll_issue<T, false>(slot2, p.slot_bytes, q0, two ? N : 0, r, 0u, val2, ok2, has2);
+                if (!poll_finish<T, false>(slot0, p.slot_bytes, q0, 0u, w, val, ok)) return false;
+                if (!poll_finish<T, false>(slot2, p.slot_bytes, q0, 0u, w, val2, ok2)) return false;
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
                     const int q = q0 + j;
-                    ok[j] = true;
-                    if (q < N && q != r && v < sp.valid(q)) {
-                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
-                        ok[j] = sentinel_arrived<U>(val[j]);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    while (!ok[j]) {
-                        if (waiter_expired(w)) return false;
-                        val[j] = ld_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes);
-                        ok[j] = sentinel_arrived<U>(val[j]);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    if (q < N && q != r && v < sp.valid(q)) {
+                    if (q < N && q != r && has1(q)) {
                         store_output<T>(p.recv[r], sp.vec(q, v), p.count, val[j]);
                         st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    }
+                    if (two && q < N && q != r && has2(q)) {
+                        store_output<T>(p.recv[r], sp.vec(q, v2), p.count, val2[j]);
+                        st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
                     }
                 }
             }
@@ -696,10 +764,10 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
     return true;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(512) twoshot_kernel(const __grid_constant__ Params p) {
+template <typename T, bool kDirect>
+__global__ void __launch_bounds__(256) twoshot_kernel(const __grid_constant__ Params p) {
     const CtaState s = cta_prologue(p);
-    if (!s.skip) (void)twoshot_body<T>(p, s);
+    if (!s.skip) (void)twoshot_body<T, kDirect>(p, s);
     cta_epilogue(p, s);
 }
 
@@ -912,7 +980,7 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(512) ll128_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(256) ll128_kernel(const __grid_constant__ Params p) {
     CtaState s = cta_prologue(p);
     s.skip = __any_sync(0xFFFFFFFFu, s.skip) != 0;  // warp syncs follow: skip must be warp-uniform
     if (!s.skip) (void)ll128_body<T>(p, s);
@@ -966,7 +1034,8 @@ static const void* kernel_for(int kind) {
     switch (kind) {
         case kKindOneshotLL: return (const void*)oneshot_kernel<T, true>;
         case kKindOneshotSentinel: return (const void*)oneshot_kernel<T, false>;
-        case kKindTwoshot: return (const void*)twoshot_kernel<T>;
+        case kKindTwoshot: return (const void*)twoshot_kernel<T, false>;
+        case kKindTwoshotDirect: return (const void*)twoshot_kernel<T, true>;
         case kKindLL128: return (const void*)ll128_kernel<T>;
         case kKindOneshotLLWide: return (const void*)oneshot_wide_kernel<T, true>;
         case kKindOneshotSentinelWide: return (const void*)oneshot_wide_kernel<T, false>;

@@ -41,7 +41,7 @@ size_t elem_size(rra_dtype_t d) {
     return 0;
 }
 
-bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_ONESHOT_BARRIER; }
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_TWOSHOT_DIRECT; }
 bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
 
 int64_t env_i64(const char* name, int64_t dflt) {
@@ -82,14 +82,14 @@ struct rra_comm {
     Ctrl* ctrl = nullptr;
     char* win0 = nullptr;
     int sm_count = 0;
-    int threads = 512;
+    int threads = 128;
     int64_t ctas_per_rank = 0;
     int64_t timeout_ms = 1000;
     int64_t ts_chunk = 0, la_chunk = 0, os_chunk = 0;
     int blocks_per_sm[3][rra::kNumKinds];  // by dtype, kernel kind; -1 = not queried
     int64_t oneshot_wide = -1;              // -1 auto (N >= 16), 0 never, 1 always
     int64_t cooperative = 1;                // cooperative launch (co-residency guaranteed)
-    int64_t pdl = 0;                        // programmatic dependent launch
+    int64_t pdl = 1;                        // programmatic dependent launch
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -193,8 +193,8 @@ rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out) {
         for (int& b : row) b = -1;
     c->timeout_ms = env_i64("RRA_POLL_TIMEOUT_MS", 1000);
     c->ctas_per_rank = env_i64("RRA_CTAS_PER_RANK", 0);
-    const int64_t thr = env_i64("RRA_THREADS", 512);
-    if (thr == 128 || thr == 256 || thr == 512) c->threads = (int)thr;
+    const int64_t thr = env_i64("RRA_THREADS", 128);
+    if (thr == 64 || thr == 128 || thr == 256) c->threads = (int)thr;
     if (c->timeout_ms <= 0) c->timeout_ms = 1000;
     if (c->ctas_per_rank < 0) c->ctas_per_rank = 0;
 
@@ -269,7 +269,7 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             c->timeout_ms = v;
             return RRA_OK;
         case RRA_ATTR_THREADS:
-            if (v != 128 && v != 256 && v != 512) return RRA_ERR_INVALID_ARG;
+            if (v != 64 && v != 128 && v != 256) return RRA_ERR_INVALID_ARG;
             if (c->threads != (int)v) {
                 c->threads = (int)v;
                 for (auto& row : c->blocks_per_sm)
@@ -402,7 +402,8 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             work = chunk;
             break;
         }
-        case RRA_TWOSHOT_DBUF: {
+        case RRA_TWOSHOT_DBUF:
+        case RRA_TWOSHOT_DIRECT: {
             size_t cap = L.ts_part / rra::kVecBytes;
             if (c->ts_chunk > 0)
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->ts_chunk / rra::kVecBytes / n));

@@ -76,10 +76,11 @@ enum KernelKind {
     kKindTwoshot = RRA_TWOSHOT_DBUF,
     kKindLL128 = RRA_LL128_ATOMIC,
     kKindOneshotBarrier = RRA_ONESHOT_BARRIER,
-    kKindOneshotLLWide = 5,
-    kKindOneshotSentinelWide = 6,
-    kKindBarrierProbe = 7,
-    kNumKinds = 8
+    kKindTwoshotDirect = RRA_TWOSHOT_DIRECT,
+    kKindOneshotLLWide = 6,
+    kKindOneshotSentinelWide = 7,
+    kKindBarrierProbe = 8,
+    kNumKinds = 9
 };
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors

@@ -21,7 +21,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("algo", ["twoshot_dbuf", "oneshot_ll"])
+@pytest.mark.parametrize("algo", ["twoshot_dbuf", "oneshot_ll", "twoshot_direct", "oneshot_sentinel"])
 @pytest.mark.parametrize("batch", inputs.W3_BATCHES)
 def test_workload3_decode_graph(batch, algo):
     """One token = 160 AllReduces of bf16 [batch, 8192] over N=8, captured in
@@ -94,9 +94,10 @@ def _sampled_check(sends, recvs, dtype, algo, nsample=20000, seed=0):
 @pytest.mark.parametrize("dtype", ["fp32", "fp64"])
 @pytest.mark.parametrize("size", inputs.W5_SIZES)
 def test_workload5_bandwidth_end(size, dtype):
-    """N=8 at 4 MiB / 64 MiB / 512 MiB per rank with twoshot_dbuf (the launch
-    the bench times), uniform(-1,1) inputs from the seeded generator; every
-    rank's output equal, sampled elements bit-exact against the oracle."""
+    """N=8 at 4 MiB / 64 MiB / 512 MiB per rank with the two-shot kernels (the
+    launches the bench times at the bandwidth end), uniform(-1,1) inputs from
+    the seeded generator; every rank's output equal, sampled elements
+    bit-exact against the oracle."""
     n = 8
     elem = 4 if dtype == "fp32" else 8
     count = size // elem
@@ -112,12 +113,15 @@ def test_workload5_bandwidth_end(size, dtype):
         sends.append(t)
     recvs = [torch.empty_like(s) for s in sends]
     with rra.Comm(n, size) as comm:
-        comm.allreduce(sends, recvs, "twoshot_dbuf")
-        torch.cuda.synchronize()
-        assert comm.status()[0] == rra.OK
-        for r in range(1, n):
-            assert torch.equal(recvs[r].view(torch.uint8), recvs[0].view(torch.uint8))
-        _sampled_check(sends, recvs, dtype, "twoshot_dbuf")
+        for algo in ("twoshot_dbuf", "twoshot_direct"):
+            for t in recvs:
+                t.view(torch.uint8).fill_(0x7F)
+            comm.allreduce(sends, recvs, algo)
+            torch.cuda.synchronize()
+            assert comm.status()[0] == rra.OK
+            for r in range(1, n):
+                assert torch.equal(recvs[r].view(torch.uint8), recvs[0].view(torch.uint8))
+            _sampled_check(sends, recvs, dtype, algo)
         for algo in ("oneshot_sentinel", "ll128_atomic"):
             if size > (64 << 20):
                 continue
