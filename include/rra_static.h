@@ -24,7 +24,7 @@ extern "C" {
  * rra_allreduce_static: the one-shot LL AllReduce-sum (same kernel and same
  * result as rra_allreduce with RRA_ONESHOT_LL: ranks added in order, bit for
  * bit), with no communicator and no allocation.  Its scratch is a file-scope
- * device array of about 4.04 MiB (a control block plus 8 windows of LL slots,
+ * device array of about 4 MiB (a control block plus 8 windows of LL slots,
  * 512 KiB each) that every GPU loading this library holds until the process
  * exits.  The call issues no cudaMalloc, cudaFree or other allocating routine.
  *   nranks      2 <= nranks <= RRA_STATIC_MAX_RANKS.

@@ -136,14 +136,18 @@ __device__ __noinline__ bool epoch_scrub(const Params& p, int rank) {
 // so the first input loads overlap this round trip instead of waiting behind
 // a block barrier.  The barrier sits in the epilogue instead: no thread may
 // overwrite epoch slot b before every thread of the CTA has read it.
-__device__ __forceinline__ CtaState cta_prologue(const Params& p) {
-    CtaState s;
-    // Programmatic dependent launch: let the next kernel on the stream be
-    // scheduled now (it waits in its own griddepcontrol.wait), and wait until
-    // the previous kernel has completed and its memory is visible before this
-    // one touches global memory.  Both are no-ops without the launch attribute.
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled now (it waits in its own griddepcontrol.wait), and wait until the
+// previous kernel has completed and its memory is visible before this one
+// touches global memory.  Both are no-ops without the launch attribute.
+// Every kernel calls this first.
+__device__ __forceinline__ void pdl_entry() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ CtaState cta_prologue(const Params& p) {
+    CtaState s;
     s.t_start = globaltimer_ns();
     s.rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
     s.sub = (int)(blockIdx.x % (unsigned)p.ctas_per_rank);
@@ -248,7 +252,7 @@ constexpr int kPushPos = 4;
 
 template <typename T, bool kLL>
 __device__ __forceinline__ void push_positions(const Params& p, int r, uint32_t base, uint32_t v0, uint32_t end,
-                                               uint64_t par_off, uint32_t ep) {
+                                               uint64_t par_off, uint32_t ep, const uint4* pre = nullptr) {
     constexpr int U = VecMath<T>::kUnitBytes;
     constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
     const uint32_t T_ = blockDim.x;
@@ -259,8 +263,9 @@ __device__ __forceinline__ void push_positions(const Params& p, int r, uint32_t 
 #pragma unroll
         for (int j = 0; j < kPushPos; ++j) {
             const uint32_t v = v0 + (uint32_t)j * T_;
-            if (v < end) x[j] = load_input<T>(p.send[r], base + v, p.count);
+            if (v < end) x[j] = (j == 0 && pre != nullptr) ? *pre : load_input<T>(p.send[r], base + v, p.count);
         }
+        pre = nullptr;
 #pragma unroll
         for (int j = 0; j < kPushPos; ++j) {
             const uint32_t v = v0 + (uint32_t)j * T_;
@@ -281,7 +286,7 @@ __device__ __forceinline__ void push_positions(const Params& p, int r, uint32_t 
 // bcast() of Fig. 9: each rank stores its chunk into every peer's slot, then
 // polls its own window for the N-1 incoming slots and reduces.
 template <typename T, bool kLL>
-__device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s) {
+__device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s, const uint4* pre) {
     using M = VecMath<T>;
     constexpr int U = M::kUnitBytes;
     constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
@@ -305,7 +310,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
         // push: my chunk into slot [parity][r] of every peer
-        if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep);
+        if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep, k == 0 ? pre : nullptr);
         if (tr && k == 0) tr[2] = globaltimer_ns();
         // receive: poll the N-1 incoming slots of two positions at a time,
         // reduce each in rank order
@@ -366,7 +371,8 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s)
 constexpr int kStageVecs = kWideStageVecs;  // 48 KiB of shared memory
 
 template <typename T, bool kLL>
-__device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaState& s, uint4* stage, int* fail) {
+__device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaState& s, uint4* stage, int* fail,
+                                                  const uint4* pre) {
     using M = VecMath<T>;
     constexpr int U = M::kUnitBytes;
     constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
@@ -389,7 +395,7 @@ __device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaStat
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
 
         // push: thread per position, as in the narrow variant
-        if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep);
+        if (!s.drop) push_positions<T, kLL>(p, r, base, pos0 + threadIdx.x, end, par_off, ep, k == 0 ? pre : nullptr);
 #pragma unroll 1
         for (uint32_t r0 = pos0; r0 < end; r0 += R) {
             const uint32_t rn = min(R, end - r0);
@@ -443,10 +449,27 @@ __device__ __forceinline__ bool oneshot_wide_body(const Params& p, const CtaStat
     return true;
 }
 
+// The thread's first input vector of step 0, loaded before the control words
+// are read so that the two round trips overlap (only a read of the caller's
+// input, in bounds; unused if the call turns out to be skipped).
+template <typename T>
+__device__ __forceinline__ bool prefetch_first(const Params& p, uint4& pre) {
+    const uint32_t sub = blockIdx.x % (unsigned)p.ctas_per_rank;
+    const int rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
+    const uint32_t v = sub * p.per_cta + threadIdx.x;
+    const uint32_t end = min((sub + 1u) * p.per_cta, min(p.chunk_vecs, p.nvec));
+    if (v >= end) return false;
+    pre = load_input<T>(p.send[rank], v, p.count);
+    return true;
+}
+
 template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_kernel(const __grid_constant__ Params p) {
+    pdl_entry();
+    uint4 pre;
+    const bool has_pre = prefetch_first<T>(p, pre);
     const CtaState s = cta_prologue(p);
-    if (!s.skip) (void)oneshot_body<T, kLL>(p, s);
+    if (!s.skip) (void)oneshot_body<T, kLL>(p, s, has_pre ? &pre : nullptr);
     cta_epilogue(p, s);
 }
 
@@ -454,10 +477,13 @@ template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_wide_kernel(const __grid_constant__ Params p) {
     __shared__ uint4 stage[kStageVecs];
     __shared__ int fail;
+    pdl_entry();
+    uint4 pre;
+    const bool has_pre = prefetch_first<T>(p, pre);
     if (threadIdx.x == 0) fail = 0;
     CtaState s = cta_prologue(p);
     s.skip = __syncthreads_or(s.skip) != 0;  // block barriers follow: skip must be CTA-uniform
-    if (!s.skip) (void)oneshot_wide_body<T, kLL>(p, s, stage, &fail);
+    if (!s.skip) (void)oneshot_wide_body<T, kLL>(p, s, stage, &fail, has_pre ? &pre : nullptr);
     cta_epilogue(p, s);
 }
 
@@ -550,6 +576,7 @@ __device__ __forceinline__ bool oneshot_barrier_body(const Params& p, const CtaS
 template <typename T>
 __global__ void __launch_bounds__(256) oneshot_barrier_kernel(const __grid_constant__ Params p) {
     __shared__ int fail;
+    pdl_entry();
     if (threadIdx.x == 0) fail = 0;
     CtaState s = cta_prologue(p);
     s.skip = __syncthreads_or(s.skip) != 0;
@@ -562,6 +589,7 @@ __global__ void __launch_bounds__(256) oneshot_barrier_kernel(const __grid_const
 // the last barrier in timing[0..1].
 __global__ void __launch_bounds__(256) barrier_probe_kernel(const __grid_constant__ Params p) {
     __shared__ int fail;
+    pdl_entry();
     if (threadIdx.x == 0) fail = 0;
     CtaState s = cta_prologue(p);
     s.skip = __syncthreads_or(s.skip) != 0;
@@ -766,6 +794,7 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
 
 template <typename T, bool kDirect>
 __global__ void __launch_bounds__(256) twoshot_kernel(const __grid_constant__ Params p) {
+    pdl_entry();
     const CtaState s = cta_prologue(p);
     if (!s.skip) (void)twoshot_body<T, kDirect>(p, s);
     cta_epilogue(p, s);
@@ -981,6 +1010,7 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) ll128_kernel(const __grid_constant__ Params p) {
+    pdl_entry();
     CtaState s = cta_prologue(p);
     s.skip = __any_sync(0xFFFFFFFFu, s.skip) != 0;  // warp syncs follow: skip must be warp-uniform
     if (!s.skip) (void)ll128_body<T>(p, s);

@@ -12,7 +12,7 @@ namespace rra {
 
 constexpr int kMaxRanks = RRA_MAX_RANKS;
 constexpr int kVecBytes = 16;          // every transfer unit is one 16-byte vector
-constexpr int kEpochSlots = 4096;      // largest grid a communicator may launch
+constexpr int kEpochSlots = 1024;      // largest grid a communicator may launch
 constexpr int kGroupVecs = 32;         // LL128-atomic: vectors per completion counter (one warp)
 constexpr size_t kRegionAlign = 4096;
 constexpr uint64_t kMaxMessageBytes = (1ull << 36) - 16;  // 16-byte vector indices fit in 32 bits

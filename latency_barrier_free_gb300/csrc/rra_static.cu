@@ -32,7 +32,7 @@ constexpr size_t kSlotBytes = 2 * kMaxBytesStatic;                     // LL dou
 constexpr size_t kParityBytes = (size_t)kMaxRanksStatic * kSlotBytes;  // one slot per source
 constexpr size_t kWindowBytes = 2 * kParityBytes;                      // 512 KiB per window
 constexpr size_t kCtrlBytes = (sizeof(rra::Ctrl) + 4095) / 4096 * 4096;
-constexpr size_t kScratchBytes = kCtrlBytes + (size_t)kMaxRanksStatic * kWindowBytes;  // ~4.04 MiB
+constexpr size_t kScratchBytes = kCtrlBytes + (size_t)kMaxRanksStatic * kWindowBytes;  // ~4.01 MiB
 constexpr int kThreads = 256;
 constexpr int kMaxDevices = 64;
 
