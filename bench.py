@@ -3,15 +3,16 @@
 
 Workload (one "step"): N=4 virtual ranks, message sizes 128 B .. 1 MiB per
 rank in powers of two (14 sizes), binary32 and bfloat16 N(0,1) inputs, all
-four algorithms; each (dtype, size, algorithm) replays a CUDA graph of
+the automatic algorithm choice; each (dtype, size) replays a CUDA graph of
 `--inner` back-to-back calls (the decode-style replay path: no host work per
 call), timed with CUDA events on the replay stream.  L2 is flushed (a 256 MiB
 write) between steps; the calls inside a step reuse their L2-resident
 buffers, the regime the small-message latency floor assumes.  The same calls
 launched one by one from Python are reported as stream_launch_us.
 
-value     mean over the 28 (dtype, size) cases of the fastest algorithm's
-          microseconds per call (lower is better)
+value     mean over the 28 (dtype, size) cases of microseconds per call with
+          the library's automatic choice (RRA_AUTO), lower is better; every
+          algorithm's own figure on every case is reported beside it
 e2e       the same metric through rra_allreduce_host: host buffers in and out,
           host<->device copies inside the timed region
 roofline  the dominant kernel of the step against the measured HBM peak
@@ -203,36 +204,34 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     inner = args.inner
 
-    # One CUDA graph per (dtype, size, algorithm) holding `inner` back-to-back
-    # calls (decode-style replay: no host work per call).  The calls are
-    # prepared with the capture stream so they are recorded into the graph.
+    # One CUDA graph per case holding `inner` back-to-back calls (decode-style
+    # replay: no host work per call).  The calls are prepared with the capture
+    # stream so they are recorded into the graph.
     cap = torch.cuda.Stream()
-    graphs = {}
-    for dt, size in cases:
+
+    def make_graph(dt, size, algo):
         sp, rp, count, _, _ = bufs[(dt, size)]
-        for algo in ALGOS:
-            f = comm.prepare(sp, rp, count, dt, algo, stream=cap)
-            f()  # plan/occupancy queries happen outside capture
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            cap.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(cap):
-                with torch.cuda.graph(g, stream=cap):
-                    for _ in range(inner):
-                        f()
-            graphs[(dt, size, algo)] = g
+        f = comm.prepare(sp, rp, count, dt, algo, stream=cap)
+        f()  # plan/occupancy queries happen outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(inner):
+                    f()
+        return g
+
+    auto_graphs = {(dt, size): make_graph(dt, size, "auto") for dt, size in cases}
     torch.cuda.synchronize()
 
     def one_step(events):
-        k = 0
-        for dt, size in cases:
-            for algo in ALGOS:
-                if events is not None:
-                    events[k][0].record(stream)
-                graphs[(dt, size, algo)].replay()
-                if events is not None:
-                    events[k][1].record(stream)
-                k += 1
+        for k, (dt, size) in enumerate(cases):
+            if events is not None:
+                events[k][0].record(stream)
+            auto_graphs[(dt, size)].replay()
+            if events is not None:
+                events[k][1].record(stream)
 
     for w in range(args.warmup):
         flush.fill_(w & 0xFF)
@@ -242,7 +241,7 @@ def run_ours(args, world, rank, local):
     if st != rra.OK:
         raise RuntimeError("device status after warm-up: %s" % rra.STATUS_NAMES.get(st))
 
-    ncase = len(cases) * len(ALGOS)
+    ncase = len(cases)
     per_step_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                         for _ in range(ncase)] for _ in range(args.steps)]
     step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -261,29 +260,47 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status after timed region: %s" % rra.STATUS_NAMES.get(st))
 
     step_ms = [a.elapsed_time(b) for a, b in step_events]
-    us_call = {}  # (dt, size, algo) -> median over steps of us per call
-    k = 0
+    auto_us = {}
+    for k, (dt, size) in enumerate(cases):
+        vals = [per_step_events[s][k][0].elapsed_time(per_step_events[s][k][1]) * 1000.0 / inner
+                for s in range(args.steps)]
+        auto_us[(dt, size)] = measure.median(vals)
+    value = float(np.mean([auto_us[c] for c in cases]))
+    auto_pick = {c: rra.select_algo(NRANKS, c[1], c[0]) for c in cases}
+
+    # Every algorithm on every case, measured the same way outside the timed
+    # step (context for the automatic choice).
+    us_call = {}
     for dt, size in cases:
         for algo in ALGOS:
-            vals = [per_step_events[s][k][0].elapsed_time(per_step_events[s][k][1]) * 1000.0 / inner
-                    for s in range(args.steps)]
-            us_call[(dt, size, algo)] = measure.median(vals)
-            k += 1
+            g = make_graph(dt, size, algo)
+            ts = []
+            for _ in range(max(3, args.steps)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1000.0 / inner)
+            us_call[(dt, size, algo)] = measure.median(ts)
+            del g
     stream_us = stream_launch_us(comm, bufs, cases, torch, stream)
     best = {(dt, size): min(ALGOS, key=lambda a: us_call[(dt, size, a)]) for dt, size in cases}
-    best_us = [us_call[(dt, size, best[(dt, size)])] for dt, size in cases]
-    value = float(np.mean(best_us))
+    best_us = float(np.mean([us_call[(dt, size, best[(dt, size)])] for dt, size in cases]))
     per_algo_mean = {a: float(np.mean([us_call[(dt, size, a)] for dt, size in cases])) for a in ALGOS}
 
-    # dominant kernel of the step: largest time per step
-    dom = max(us_call, key=lambda key: us_call[key])
-    dom_dt, dom_size, dom_algo = dom
+    # dominant kernel of the timed step: the case with the largest time
+    dom_case = max(cases, key=lambda c: auto_us[c])
+    dom_dt, dom_size = dom_case
+    dom_algo = auto_pick[dom_case]
+    dom = (dom_dt, dom_size, dom_algo)
+    us_call_dom = auto_us[dom_case]
     peaks = measured_peaks()
     hbm_peak = peaks.get("hbm_gbs")
     peak_src = "measured" if hbm_peak else "fallback"
     hbm_peak = hbm_peak or 6800.0
     dom_bytes = measure.algorithmic_bytes(NRANKS, dom_size)
-    achieved = dom_bytes / (us_call[dom] * 1e-6) / 1e9
+    achieved = dom_bytes / (us_call_dom * 1e-6) / 1e9
     kname = {"oneshot_ll": "oneshot_kernel", "oneshot_sentinel": "oneshot_kernel",
              "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel",
              "twoshot_direct": "twoshot_kernel"}[dom_algo]
@@ -296,13 +313,13 @@ def run_ours(args, world, rank, local):
     floor = latency_floor(comm, rra, measure, torch, stream)
     clk = clocks.stop()
     bandwidth = bandwidth_end(rra, measure, torch, hbm_peak, args)
-    e2e = end_to_end(comm, rra, cases, best, torch, args)
+    e2e = end_to_end(comm, rra, cases, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
 
     # aggregate over GPU replicas: latency-like numbers take the max
     agg = max_over_ranks(dist, [value, float(np.mean(step_ms)), e2e["value"]], device=dev)
     value, ms_step, e2e["value"] = agg
-    launches = args.steps * ncase * inner
+    launches = args.steps * ncase * inner  # one kernel per call, all ours
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "us/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
@@ -318,6 +335,9 @@ def run_ours(args, world, rank, local):
         "bandwidth": bandwidth,
         "e2e": e2e,
         "clocks": clk,
+        "auto_us": {"%s/%d" % k: round(v, 3) for k, v in auto_us.items()},
+        "auto_algo": {"%s/%d" % k: v for k, v in auto_pick.items()},
+        "best_of_algos_mean_us": round(best_us, 3),
         "per_algo_mean_us": {a: round(v, 3) for a, v in per_algo_mean.items()},
         "stream_launch_us": stream_us,
         "per_size_us": {"%s/%d" % (dt, size): {a: round(us_call[(dt, size, a)], 3) for a in ALGOS}
@@ -465,7 +485,7 @@ def bandwidth_end(rra, measure, torch, hbm_peak, args):
             "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events; default chunking"}
 
 
-def end_to_end(comm, rra, cases, best, torch, args):
+def end_to_end(comm, rra, cases, torch, args):
     """Host buffers in and out through rra_allreduce_host (pinned memory)."""
     from latency_barrier_free_gb300 import inputs
 
@@ -480,10 +500,10 @@ def end_to_end(comm, rra, cases, best, torch, args):
         hr = [torch.empty_like(h).pin_memory() for h in hs]
         sp = [h.data_ptr() for h in hs]
         rp = [h.data_ptr() for h in hr]
-        comm.allreduce_host(sp, rp, count, dt, best[(dt, size)])
+        comm.allreduce_host(sp, rp, count, dt, "auto")
         t0 = time.perf_counter()
         for _ in range(reps):
-            comm.allreduce_host(sp, rp, count, dt, best[(dt, size)])
+            comm.allreduce_host(sp, rp, count, dt, "auto")
         per.append((time.perf_counter() - t0) / reps * 1e6)
         h2d += NRANKS * size
         d2h += NRANKS * size

@@ -76,10 +76,13 @@ typedef enum {
     RRA_LL128_ATOMIC = 3,      /* Fig. 5: atomic adds into the owner's lines, counter == N-1 */
     RRA_ONESHOT_BARRIER = 4,   /* BASELINE, not barrier-free: plain stores + two flag barriers
                                   per step (Sec. III-B, the design the paper replaces) */
-    RRA_TWOSHOT_DIRECT = 5     /* two-shot whose AllGather stores the reduced partition
+    RRA_TWOSHOT_DIRECT = 5,    /* two-shot whose AllGather stores the reduced partition
                                   straight into every rank's output (outputs treated as
                                   registered symmetric buffers, Sec. II-B): RS as
                                   RRA_TWOSHOT_DBUF, no AG scratch, one hop per step */
+    RRA_AUTO = 6               /* pick by rank count and message size (rra_select_algo);
+                                  may pick a sentinel algorithm, so inputs must not hold
+                                  the all-ones pattern */
 } rra_algo_t;
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
@@ -204,6 +207,14 @@ rra_status_t rra_comm_layout(rra_comm_t comm, rra_layout_t* out);
  * 64 MiB).  Errors: RRA_ERR_INVALID_ARG. */
 rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_oneshot,
                              size_t scratch_twoshot, rra_layout_t* out);
+
+/* The algorithm RRA_AUTO uses for `nranks` ranks and `bytes` per rank (pure
+ * host arithmetic).  The paper selects kernels by message size and rank count
+ * from measurements ("<1 MiB one-shot, 1-2 MiB two-shot at 4 ranks"); these
+ * thresholds are the crossovers measured on GB300 with CUDA-graph replay:
+ * one-shot sentinel while nranks * bytes <= 1.5 MiB (N <= 8), LL128-atomic for
+ * mid sizes at N >= 16, and the direct two-shot above. */
+rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out);
 
 /* Number of CTAs the next call of (count, dtype, algo) would launch, and the
  * number of chunk steps it would take; pure host arithmetic. */

@@ -463,11 +463,35 @@ __device__ __forceinline__ bool prefetch_first(const Params& p, uint4& pre) {
     return true;
 }
 
+// Warm the lines (and address translations) a one-shot thread touches first:
+// its slot in every peer window (both parities: the epoch is not known yet),
+// the slots it will poll in its own window, and its output.  Small N only.
+template <bool kLL>
+__device__ __forceinline__ void prefetch_paths(const Params& p) {
+    constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
+    const uint32_t sub = blockIdx.x % (unsigned)p.ctas_per_rank;
+    const int r = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
+    const uint32_t v = sub * p.per_cta + threadIdx.x;
+    if (p.nranks > 8 || v >= min((sub + 1u) * p.per_cta, min(p.chunk_vecs, p.nvec))) return;
+    const uint64_t pos = (uint64_t)v * kPosBytes;
+    for (int q = 0; q < p.nranks; ++q) {
+        if (q == r) continue;
+        const char* peer = window(p, q) + p.region_off + (uint64_t)r * p.slot_bytes + pos;
+        const char* mine = window(p, r) + p.region_off + (uint64_t)q * p.slot_bytes + pos;
+        prefetch_l2(peer);
+        prefetch_l2(peer + p.parity_bytes);
+        prefetch_l2(mine);
+        prefetch_l2(mine + p.parity_bytes);
+    }
+    prefetch_l2((const char*)p.recv[r] + (uint64_t)v * kVecBytes);
+}
+
 template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_kernel(const __grid_constant__ Params p) {
     pdl_entry();
     uint4 pre;
     const bool has_pre = prefetch_first<T>(p, pre);
+    prefetch_paths<kLL>(p);
     const CtaState s = cta_prologue(p);
     if (!s.skip) (void)oneshot_body<T, kLL>(p, s, has_pre ? &pre : nullptr);
     cta_epilogue(p, s);

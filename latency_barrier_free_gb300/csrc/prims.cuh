@@ -93,6 +93,12 @@ __device__ __forceinline__ void st_output_v4(void* p, uint4 v) {
                  : "memory");
 }
 
+// L2 prefetch of one line: also brings the address translation into the SM,
+// so a later store/poll to that page does not wait for it.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" : : "l"(p));
+}
+
 // --------------------------------------------------------------- fences ----
 __device__ __forceinline__ void fence_acq_rel_gpu() {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");

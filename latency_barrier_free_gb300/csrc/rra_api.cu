@@ -41,7 +41,7 @@ size_t elem_size(rra_dtype_t d) {
     return 0;
 }
 
-bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_TWOSHOT_DIRECT; }
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_AUTO; }
 bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
 
 int64_t env_i64(const char* name, int64_t dflt) {
@@ -116,6 +116,19 @@ const char* rra_status_string(rra_status_t s) {
         case RRA_ERR_EPOCH: return "epoch error (reserved)";
     }
     return "unknown status";
+}
+
+rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out) {
+    if (out == nullptr || nranks < 2 || nranks > RRA_MAX_RANKS || !valid_dtype(dtype)) return RRA_ERR_INVALID_ARG;
+    const size_t total = (size_t)nranks * bytes;
+    if (nranks <= 8) {
+        *out = total <= (3ull << 19) ? RRA_ONESHOT_SENTINEL : RRA_TWOSHOT_DIRECT;
+    } else {
+        if (bytes <= (4u << 10)) *out = RRA_ONESHOT_SENTINEL;
+        else if (bytes <= (128u << 10)) *out = RRA_LL128_ATOMIC;
+        else *out = RRA_TWOSHOT_DIRECT;
+    }
+    return RRA_OK;
 }
 
 rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_oneshot,
@@ -337,7 +350,8 @@ static rra_status_t max_ctas_kind(rra_comm* c, rra_dtype_t d, int kind, int* cta
 }
 
 rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, int* ctas) {
-    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a)) return RRA_ERR_INVALID_ARG;
+    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a) || a == RRA_AUTO)
+        return RRA_ERR_INVALID_ARG;
     return max_ctas_kind(c, d, kernel_kind(c, a), ctas);
 }
 
@@ -478,6 +492,7 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
                                 int* grid_ctas, int* steps) {
     if (c == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0) return RRA_ERR_INVALID_ARG;
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
+    if (algo == RRA_AUTO) rra_select_algo(c->nranks, count * elem_size(dtype), dtype, &algo);
     Params p;
     int kind = 0, threads = 0;
     rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
@@ -495,6 +510,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     if (count == 0) return RRA_OK;
     const size_t es = elem_size(dtype);
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
+    if (algo == RRA_AUTO) rra_select_algo(c->nranks, count * es, dtype, &algo);
     Params p;
     int kind = 0, threads = 0;
     {

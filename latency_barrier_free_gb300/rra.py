@@ -22,7 +22,8 @@ ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_CORESIDENT, ERR_TIMEOUT, ERR_POISONE
 
 DTYPES = {"fp32": 0, "bf16": 1, "fp64": 2}
 ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomic": 3,
-         "oneshot_barrier": 4, "twoshot_direct": 5}
+         "oneshot_barrier": 4, "twoshot_direct": 5, "auto": 6}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 BARRIER_FREE = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct")
 ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,
          "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6, "cooperative": 7, "pdl": 8}
@@ -32,7 +33,7 @@ MAX_RANKS = 64
 SYMBOLS = [
     "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_comm_status", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
-    "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
+    "rra_select_algo", "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
     "rra_comm_inject_drop",
     "rra_comm_barrier_latency", "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string",
     "rra_version",
@@ -87,6 +88,7 @@ def load(path: str = LIB_PATH):
             "rra_comm_get_attr": ([vp, i32, ctypes.POINTER(i64)], i32),
             "rra_comm_layout": ([vp, ctypes.POINTER(Layout)], i32),
             "rra_plan_layout": ([i32, sz, sz, sz, ctypes.POINTER(Layout)], i32),
+            "rra_select_algo": ([i32, sz, i32, ip], i32),
             "rra_comm_plan_call": ([vp, sz, i32, i32, ip, ip], i32),
             "rra_comm_max_coresident": ([vp, i32, i32, ip], i32),
             "rra_comm_set_timing": ([vp, vp], i32),
@@ -130,6 +132,14 @@ def plan_layout(nranks: int, max_bytes: int, scratch_oneshot: int = 0, scratch_t
     _check(load().rra_plan_layout(nranks, max_bytes, scratch_oneshot, scratch_twoshot, ctypes.byref(lay)),
            "rra_plan_layout")
     return lay.as_dict()
+
+
+def select_algo(nranks: int, bytes_per_rank: int, dtype: str = "fp32") -> str:
+    """Name of the algorithm RRA_AUTO uses (pure host arithmetic)."""
+    v = ctypes.c_int()
+    _check(load().rra_select_algo(int(nranks), int(bytes_per_rank), DTYPES[dtype], ctypes.byref(v)),
+           "rra_select_algo")
+    return ALGO_NAMES[v.value]
 
 
 def _ptr_array(ptrs):

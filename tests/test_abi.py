@@ -103,3 +103,22 @@ def test_create_without_gpu_fails_cleanly():
     with pytest.raises(rra.RraError) as e:
         rra.Comm(4, 4096)
     assert e.value.status == rra.ERR_CUDA
+
+
+def test_auto_selection_by_size_and_ranks():
+    # the paper picks one-shot for small and two-shot for larger messages at a
+    # given rank count; the GB300 crossovers differ from its GB200 ones
+    assert rra.select_algo(4, 128) == "oneshot_sentinel"
+    assert rra.select_algo(4, 256 << 10) == "oneshot_sentinel"
+    assert rra.select_algo(4, 1 << 20) == "twoshot_direct"
+    assert rra.select_algo(8, 16 << 10, "bf16") == "oneshot_sentinel"
+    assert rra.select_algo(8, 1 << 20, "bf16") == "twoshot_direct"
+    assert rra.select_algo(64, 1 << 10) == "oneshot_sentinel"
+    assert rra.select_algo(64, 64 << 10) == "ll128_atomic"
+    assert rra.select_algo(64, 1 << 20) == "twoshot_direct"
+    for n in (2, 4, 8, 16, 64):  # once two-shot, always two-shot as the message grows
+        picks = [rra.select_algo(n, 1 << k) for k in range(4, 31)]
+        first = picks.index("twoshot_direct")
+        assert all(p == "twoshot_direct" for p in picks[first:])
+    with pytest.raises(rra.RraError):
+        rra.select_algo(1, 128)

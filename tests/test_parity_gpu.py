@@ -254,3 +254,16 @@ def test_barrier_baseline_parity(dtype):
             assert comm.plan_call(9000, dtype, "oneshot_barrier")[1] >= 3
             got = run(comm, sends_np, dtype, "oneshot_barrier")
             check_against_oracle(sends_np, got, dtype, "oneshot_barrier")
+
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+def test_auto_algorithm(n):
+    """RRA_AUTO runs the algorithm rra_select_algo names, with its results."""
+    max_bytes = 1 << 20
+    with rra.Comm(n, max_bytes) as comm:
+        for size in (128, 4096, 65536, 262144, 393216, 524288, 1 << 20):
+            count = size // 4
+            algo = rra.select_algo(n, size, "fp32")
+            sends_np = inputs.normal(inputs.rng(68, n, size), n, count, "fp32")
+            got = run(comm, sends_np, "fp32", "auto")
+            check_against_oracle(sends_np, got, "fp32", algo)
