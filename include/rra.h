@@ -212,8 +212,9 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
  * host arithmetic).  The paper selects kernels by message size and rank count
  * from measurements ("<1 MiB one-shot, 1-2 MiB two-shot at 4 ranks"); these
  * thresholds are the crossovers measured on GB300 with CUDA-graph replay:
- * one-shot sentinel while nranks * bytes <= 1.5 MiB (N <= 8), LL128-atomic for
- * mid sizes at N >= 16, and the direct two-shot above. */
+ * one-shot sentinel while nranks * bytes <= 1.5 MiB (N <= 8); for N >= 16
+ * one-shot sentinel up to 4 KiB, LL128-atomic up to 16 KiB (64 KiB at N = 64);
+ * the direct two-shot above. */
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out);
 
 /* Number of CTAs the next call of (count, dtype, algo) would launch, and the

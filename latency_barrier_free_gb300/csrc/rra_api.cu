@@ -124,8 +124,9 @@ rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_al
     if (nranks <= 8) {
         *out = total <= (3ull << 19) ? RRA_ONESHOT_SENTINEL : RRA_TWOSHOT_DIRECT;
     } else {
+        const size_t ll128_max = nranks >= 64 ? (64u << 10) : (16u << 10);
         if (bytes <= (4u << 10)) *out = RRA_ONESHOT_SENTINEL;
-        else if (bytes <= (128u << 10)) *out = RRA_LL128_ATOMIC;
+        else if (bytes <= ll128_max) *out = RRA_LL128_ATOMIC;
         else *out = RRA_TWOSHOT_DIRECT;
     }
     return RRA_OK;
