@@ -44,7 +44,7 @@ import numpy as np  # noqa: E402
 
 NRANKS = 4
 DTYPES = ("fp32", "bf16")
-ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct")
+ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct", "oneshot_cluster")
 ELEM = {"fp32": 4, "bf16": 2, "fp64": 8}
 METRIC = "AllReduce us/call at 128B-1MB; GB/s vs HBM roofline; N virtual ranks, 1 GB300"
 WORKLOAD = "N=4 virtual ranks, 128 B-1 MiB per rank (14 sizes), fp32+bf16 N(0,1), 4 algorithms"
@@ -303,7 +303,7 @@ def run_ours(args, world, rank, local):
     achieved = dom_bytes / (us_call_dom * 1e-6) / 1e9
     kname = {"oneshot_ll": "oneshot_kernel", "oneshot_sentinel": "oneshot_kernel",
              "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel",
-             "twoshot_direct": "twoshot_kernel"}[dom_algo]
+             "twoshot_direct": "twoshot_kernel", "oneshot_cluster": "oneshot_cluster_kernel"}[dom_algo]
     dom_cfg = "%s N=%d %s %dB" % (dom_algo, NRANKS, dom_dt, dom_size)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": committed_traffic(kname, dom_cfg),

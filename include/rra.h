@@ -80,9 +80,13 @@ typedef enum {
                                   straight into every rank's output (outputs treated as
                                   registered symmetric buffers, Sec. II-B): RS as
                                   RRA_TWOSHOT_DBUF, no AG scratch, one hop per step */
-    RRA_AUTO = 6               /* pick by rank count and message size (rra_select_algo);
+    RRA_AUTO = 6,              /* pick by rank count and message size (rra_select_algo);
                                   may pick a sentinel algorithm, so inputs must not hold
                                   the all-ones pattern */
+    RRA_ONESHOT_CLUSTER = 7    /* one-shot push through distributed shared memory: one
+                                  thread-block cluster of N CTAs per slice, st.async into
+                                  peers' shared memory completes their mbarrier (arrival
+                                  of the bytes is the signal); N <= 16, any size */
 } rra_algo_t;
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librra.so")
 
-SOURCES = ["kernels.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
+SOURCES = ["kernels.cu", "cluster.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
 HEADERS = ["prims.cuh", "rra_internal.h"]
 PUBLIC_HEADERS = ["rra.h", "rra_probe.h", "rra_static.h"]
 

@@ -40,51 +40,6 @@ __device__ __forceinline__ char* window(const Params& p, int r) {
     return p.win0 + (uint64_t)r * p.stride;
 }
 
-// Input vector `vec` of a rank's buffer; elements at or beyond `count` read
-// as zero (never the sentinel).
-template <typename T>
-__device__ __forceinline__ uint4 load_input(const void* base, uint32_t vec, uint64_t count) {
-    constexpr int VE = VecMath<T>::kElems;
-    const uint64_t e0 = (uint64_t)vec * VE;
-    if (e0 + VE <= count) return ld_input_v4((const char*)base + (uint64_t)vec * kVecBytes);
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    const int n = (int)(count - e0);
-    if (sizeof(T) == 2) {
-        const uint16_t* s = (const uint16_t*)base + e0;
-        for (int i = 0; i < n; ++i) w[i >> 1] |= (uint32_t)s[i] << (16 * (i & 1));
-    } else if (sizeof(T) == 4) {
-        const uint32_t* s = (const uint32_t*)base + e0;
-        for (int i = 0; i < n; ++i) w[i] = s[i];
-    } else {
-        const uint32_t* s = (const uint32_t*)base + 2 * e0;
-        for (int i = 0; i < 2 * n; ++i) w[i] = s[i];
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Output vector `vec`; only elements below `count` are written.
-template <typename T>
-__device__ __forceinline__ void store_output(void* base, uint32_t vec, uint64_t count, uint4 v) {
-    constexpr int VE = VecMath<T>::kElems;
-    const uint64_t e0 = (uint64_t)vec * VE;
-    if (e0 + VE <= count) {
-        st_output_v4((char*)base + (uint64_t)vec * kVecBytes, v);
-        return;
-    }
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    const int n = (int)(count - e0);
-    if (sizeof(T) == 2) {
-        uint16_t* d = (uint16_t*)base + e0;
-        for (int i = 0; i < n; ++i) d[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
-    } else if (sizeof(T) == 4) {
-        uint32_t* d = (uint32_t*)base + e0;
-        for (int i = 0; i < n; ++i) d[i] = w[i];
-    } else {
-        uint32_t* d = (uint32_t*)base + 2 * e0;
-        for (int i = 0; i < 2 * n; ++i) d[i] = w[i];
-    }
-}
-
 // Per-CTA prologue/epilogue shared by all kernels.
 struct CtaState {
     uint64_t epoch;  // epoch of step 0 of this call

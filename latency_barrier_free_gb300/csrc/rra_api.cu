@@ -41,7 +41,7 @@ size_t elem_size(rra_dtype_t d) {
     return 0;
 }
 
-bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_AUTO; }
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_ONESHOT_CLUSTER; }
 bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
 
 int64_t env_i64(const char* name, int64_t dflt) {
@@ -334,6 +334,31 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
     return RRA_ERR_INVALID_ARG;
 }
 
+// Plan of a cluster one-shot call: one position per thread, slices of at most
+// kClusterStageBytes / (N * 16) vectors, one cluster of N CTAs per slice.
+static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, Params* p, int* threads) {
+    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    const size_t ve = rra::kVecBytes / elem_size(dtype);
+    memset(p, 0, sizeof(*p));
+    p->win0 = c->win0;
+    p->ctrl = c->ctrl;
+    p->timing = c->timing;
+    p->stride = c->lay.window_stride;
+    p->count = count;
+    p->nvec = (uint32_t)ceil_div(count, ve);
+    p->timeout_ns = (uint64_t)c->timeout_ms * 1000000ull;
+    p->nranks = c->nranks;
+    p->nsteps = 1;
+    p->chunk_vecs = p->nvec;
+    const size_t pmax = rra::kClusterStageBytes / ((size_t)c->nranks * rra::kVecBytes);
+    const size_t per = std::min<size_t>(std::min<size_t>(pmax, (size_t)c->threads), p->nvec);
+    p->per_cta = (uint32_t)per;
+    p->ctas_per_rank = (int32_t)ceil_div(p->nvec, per);  // slices = clusters
+    p->epoch_slots = rra::kEpochSlots;
+    *threads = (int)std::min<size_t>((size_t)c->threads, std::max<size_t>(32, align_up(per, 32)));
+    return RRA_OK;
+}
+
 static int kernel_kind(const rra_comm* c, rra_algo_t algo) {
     if (algo == RRA_ONESHOT_LL || algo == RRA_ONESHOT_SENTINEL) {
         const bool wide = c->oneshot_wide == 1 || (c->oneshot_wide < 0 && c->nranks >= 16);
@@ -351,7 +376,8 @@ static rra_status_t max_ctas_kind(rra_comm* c, rra_dtype_t d, int kind, int* cta
 }
 
 rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, int* ctas) {
-    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a) || a == RRA_AUTO)
+    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a) || a == RRA_AUTO ||
+        a == RRA_ONESHOT_CLUSTER)
         return RRA_ERR_INVALID_ARG;
     return max_ctas_kind(c, d, kernel_kind(c, a), ctas);
 }
@@ -496,7 +522,8 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     if (algo == RRA_AUTO) rra_select_algo(c->nranks, count * elem_size(dtype), dtype, &algo);
     Params p;
     int kind = 0, threads = 0;
-    rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
+    rra_status_t st = algo == RRA_ONESHOT_CLUSTER ? plan_cluster(c, count, dtype, &p, &threads)
+                                                  : plan_call(c, count, dtype, algo, &p, &kind, &threads);
     if (st != RRA_OK) return st;
     if (grid_ctas) *grid_ctas = p.nranks * p.ctas_per_rank;
     if (steps) *steps = (int)p.nsteps;
@@ -516,7 +543,8 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     int kind = 0, threads = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
+        rra_status_t st = algo == RRA_ONESHOT_CLUSTER ? plan_cluster(c, count, dtype, &p, &threads)
+                                                      : plan_call(c, count, dtype, algo, &p, &kind, &threads);
         if (st != RRA_OK) return st;
     }
     for (int r = 0; r < c->nranks; ++r) {
@@ -525,8 +553,10 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
-    cudaError_t e = rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0,
-                                          c->pdl != 0);
+    cudaError_t e = algo == RRA_ONESHOT_CLUSTER
+                        ? rra::launch_cluster(p, dtype, threads, (cudaStream_t)stream, c->pdl != 0)
+                        : rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0,
+                                                c->pdl != 0);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
         return RRA_ERR_NOT_CORESIDENT;

@@ -85,11 +85,16 @@ enum KernelKind {
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors
 constexpr int kTracePoints = 6;       // start, control words read, pushed, polled, stored, end
+constexpr size_t kClusterStageBytes = 96u << 10;  // cluster one-shot: shared-memory stage per CTA
+constexpr int kClusterMaxRanks = 16;              // cluster one-shot: ranks per cluster (one CTA each)
 
 // Host-side launch entry points (kernels.cu).
 cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
                              bool cooperative = true, bool pdl = false);
 cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm);
+// One-shot through distributed shared memory (cluster.cu): one cluster of
+// nranks CTAs per slice of per_cta vectors; p.ctas_per_rank = slices.
+cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int threads, cudaStream_t stream, bool pdl);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

@@ -267,3 +267,26 @@ def test_auto_algorithm(n):
             sends_np = inputs.normal(inputs.rng(68, n, size), n, count, "fp32")
             got = run(comm, sends_np, "fp32", "auto")
             check_against_oracle(sends_np, got, "fp32", algo)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+def test_oneshot_cluster(n, dtype):
+    """One-shot through distributed shared memory (one cluster of N CTAs per
+    slice): bit-exact, for ragged sizes, many slices, and in place."""
+    with rra.Comm(n, 300000 * ELEM[dtype]) as comm:
+        for count in (1, 7, 33, 4097, 70001, 300000):
+            sends_np = inputs.normal(inputs.rng(69, count, n), n, count, dtype)
+            got = run(comm, sends_np, dtype, "oneshot_cluster")
+            check_against_oracle(sends_np, got, dtype, "oneshot_cluster")
+        sends_np = inputs.normal(inputs.rng(69, 1, n), n, 5000, dtype)
+        got = run(comm, sends_np, dtype, "oneshot_cluster", in_place=True)
+        check_against_oracle(sends_np, got, dtype, "oneshot_cluster")
+
+
+def test_oneshot_cluster_rejects_too_many_ranks():
+    with rra.Comm(17, 4096) as comm:
+        x = [torch.zeros(16, device="cuda") for _ in range(17)]
+        with pytest.raises(rra.RraError) as e:
+            comm.allreduce(x, x, "oneshot_cluster")
+        assert e.value.status == rra.ERR_INVALID_ARG

@@ -21,7 +21,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + ("oneshot_cluster",))
 def test_graph_replay_advances_epochs(algo):
     """Capture 20 calls in a CUDA graph and replay it 5 times with new inputs
     copied in between: every replay must see fresh epochs (LL flags) and
@@ -57,7 +57,7 @@ def test_graph_replay_advances_epochs(algo):
                 check_against_oracle(host[i], list(got[i]), "fp32", algo)
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + ("oneshot_cluster",))
 def test_timeout_poison_and_reset(algo):
     """A rank that drops its stores makes its peers' polls run out of time:
     the device records RRA_ERR_TIMEOUT (no fault, no hang), the communicator
