@@ -94,8 +94,10 @@ typedef enum {
     RRA_ATTR_CTAS_PER_RANK = 0,    /* 0 = chosen per call from the message size */
     RRA_ATTR_POLL_TIMEOUT_MS = 1,  /* limit of every device-side wait (default 1000) */
     RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256 */
-    RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step, 0 = largest that fits */
-    RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step, 0 = largest */
+    RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step; 0 (default) = the step
+                                      whose live scratch over all windows is ~32 MiB (stays
+                                      in L2), within the per-window scratch cap */
+    RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step; 0 = as above */
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
     RRA_ATTR_ONESHOT_WIDE = 6,     /* one-shot polls split a position's sources over
                                       threads: -1 auto (N >= 16, default), 0 off, 1 on */

@@ -27,6 +27,11 @@ namespace {
 constexpr size_t kDefaultScratchOneshot = 4ull << 20;   // Fig. 12: one-shot
 constexpr size_t kDefaultScratchTwoshot = 64ull << 20;  // Fig. 12: two-shot, LL128
 constexpr size_t kWindowAlign = 64ull << 10;
+// Default two-shot / LL128 step size: keep the scratch live in one step (all
+// windows, both parities) near this size, so it stays in L2 while the
+// inputs and outputs stream through HBM (measured on GB300: a 64 MiB cap's
+// 16 MiB steps spilled scratch to DRAM, 2.3x the compulsory traffic).
+constexpr size_t kLiveScratch = 32ull << 20;
 
 size_t floor16(size_t x) { return x & ~(size_t)15; }
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
@@ -448,6 +453,8 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             size_t cap = L.ts_part / rra::kVecBytes;
             if (c->ts_chunk > 0)
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->ts_chunk / rra::kVecBytes / n));
+            else  // live RS (+AG) scratch: N windows x 2 parities x N slots x part
+                cap = std::min(cap, std::max<size_t>(64, kLiveScratch / (2 * n * n) / rra::kVecBytes));
             const size_t part = std::min(ceil_div(p->nvec, n), cap);
             p->chunk_vecs = (uint32_t)part;
             p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
@@ -462,6 +469,8 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             size_t cap = L.la_part / rra::kVecBytes;
             if (c->la_chunk > 0)
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->la_chunk / rra::kVecBytes / n));
+            else  // live accumulators + LL AllGather slots: about 4 N^2 x part
+                cap = std::min(cap, std::max<size_t>(64, kLiveScratch / (4 * n * n) / rra::kVecBytes));
             const size_t part = std::min(ceil_div(p->nvec, n), cap);
             const LaSizes s = la_sizes(L.la_part, c->nranks);
             p->chunk_vecs = (uint32_t)part;
