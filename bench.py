@@ -18,8 +18,8 @@ e2e       the same metric through rra_allreduce_host: host buffers in and out,
 roofline  the dominant kernel of the step against the measured HBM peak
 floor     measured single-GPU latency floor 2*L2_RTT + L_store->poll and the
           in-kernel time of the 128-byte calls
-bandwidth twoshot_dbuf at N=8, 64 MiB and 512 MiB binary32 per rank, GB/s of
-          compulsory traffic (2*N*M) against the measured HBM peak
+bandwidth the two-shot kernels at N=8, 64 MiB and 512 MiB binary32 per rank,
+          GB/s of compulsory traffic (2*N*M) against the measured HBM peak
 cpu_baseline  the CPU oracle on a bounded sample of the same sweep
 
 --impl reference times the CPU oracle itself on the same sweep.
@@ -44,10 +44,11 @@ import numpy as np  # noqa: E402
 
 NRANKS = 4
 DTYPES = ("fp32", "bf16")
-ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct", "oneshot_cluster")
+ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct", "oneshot_cluster",
+         "twoshot_cluster")
 ELEM = {"fp32": 4, "bf16": 2, "fp64": 8}
 METRIC = "AllReduce us/call at 128B-1MB; GB/s vs HBM roofline; N virtual ranks, 1 GB300"
-WORKLOAD = "N=4 virtual ranks, 128 B-1 MiB per rank (14 sizes), fp32+bf16 N(0,1), 4 algorithms"
+WORKLOAD = "N=4 virtual ranks, 128 B-1 MiB per rank (14 sizes), fp32+bf16 N(0,1), automatic algorithm choice"
 
 
 # ----------------------------------------------------------------- ranks --
@@ -303,7 +304,8 @@ def run_ours(args, world, rank, local):
     achieved = dom_bytes / (us_call_dom * 1e-6) / 1e9
     kname = {"oneshot_ll": "oneshot_kernel", "oneshot_sentinel": "oneshot_kernel",
              "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel",
-             "twoshot_direct": "twoshot_kernel", "oneshot_cluster": "oneshot_cluster_kernel"}[dom_algo]
+             "twoshot_direct": "twoshot_kernel", "oneshot_cluster": "cluster_kernel",
+             "twoshot_cluster": "cluster_kernel"}[dom_algo]
     dom_cfg = "%s N=%d %s %dB" % (dom_algo, NRANKS, dom_dt, dom_size)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": committed_traffic(kname, dom_cfg),
@@ -462,7 +464,7 @@ def bandwidth_end(rra, measure, torch, hbm_peak, args):
         with rra.Comm(n, size) as c:
             xs = [torch.rand(count, device="cuda", generator=gen) * 2 - 1 for _ in range(n)]
             ys = [torch.empty_like(x) for x in xs]
-            for algo in ("twoshot_dbuf", "twoshot_direct"):
+            for algo in ("twoshot_dbuf", "twoshot_direct", "twoshot_cluster"):
                 for _ in range(2):
                     c.allreduce(xs, ys, algo)
                 torch.cuda.synchronize()
@@ -524,7 +526,7 @@ def decode_graph(rra, torch):
         with rra.Comm(n, count * 2) as c:
             xs = [torch.randn(count, device="cuda").to(torch.bfloat16) for _ in range(n)]
             ys = [torch.empty_like(x) for x in xs]
-            for algo in ("oneshot_ll", "twoshot_dbuf"):
+            for algo in ("oneshot_ll", "twoshot_dbuf", "oneshot_cluster", "twoshot_cluster"):
                 c.allreduce(xs, ys, algo)
                 torch.cuda.synchronize()
                 g = torch.cuda.CUDAGraph()

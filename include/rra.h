@@ -81,12 +81,20 @@ typedef enum {
                                   registered symmetric buffers, Sec. II-B): RS as
                                   RRA_TWOSHOT_DBUF, no AG scratch, one hop per step */
     RRA_AUTO = 6,              /* pick by rank count and message size (rra_select_algo);
-                                  may pick a sentinel algorithm, so inputs must not hold
-                                  the all-ones pattern */
-    RRA_ONESHOT_CLUSTER = 7    /* one-shot push through distributed shared memory: one
-                                  thread-block cluster of N CTAs per slice, st.async into
-                                  peers' shared memory completes their mbarrier (arrival
-                                  of the bytes is the signal); N <= 16, any size */
+                                  may pick a sentinel algorithm (N > 16, or when clusters
+                                  cannot be scheduled), so inputs must not hold the
+                                  all-ones pattern */
+    RRA_ONESHOT_CLUSTER = 7,   /* one-shot push through distributed shared memory: one
+                                  thread-block cluster of N CTAs per slice (CTA r = rank r),
+                                  st.async into peers' shared memory completes their
+                                  mbarrier (arrival of the bytes is the signal); no state
+                                  between calls; N <= 16, any size */
+    RRA_TWOSHOT_CLUSTER = 8    /* two-shot through distributed shared memory: rank r pushes
+                                  partition q of its slice to CTA q only (ReduceScatter),
+                                  CTA q adds the N contributions in rank order and stores
+                                  the result into every rank's output (AllGather as direct
+                                  stores, as RRA_TWOSHOT_DIRECT); HBM carries only the
+                                  inputs read once and the outputs written once; N <= 16 */
 } rra_algo_t;
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
@@ -106,11 +114,17 @@ typedef enum {
                                       0: plain launch of the same occupancy-checked grid
                                       (progress then relies on no other work holding the
                                       SMs for longer than the poll time limit) */
-    RRA_ATTR_PDL = 8               /* 1 (default): programmatic dependent launch, so
+    RRA_ATTR_PDL = 8,              /* 1 (default): programmatic dependent launch, so
                                       the next kernel on the stream is scheduled while
                                       this one drains; each kernel waits
                                       (griddepcontrol.wait) for its predecessor before
                                       touching memory.  0: plain stream order */
+    RRA_ATTR_CLUSTER_SLICE = 9     /* cluster kernels: bytes per rank per slice (one cluster
+                                      per slice), a multiple of 16, at most 98304; clamped to
+                                      the 96 KiB shared-memory stage (N x slice for the
+                                      one-shot, slice for the two-shot, rounded up to N
+                                      vectors).  0 (default): one 16-byte vector per thread
+                                      for small messages, else about two CTAs per SM */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -166,7 +180,11 @@ rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out);
  * `stream` completes.  RRA_ONESHOT_SENTINEL and RRA_TWOSHOT_DBUF require
  * that no input element has the all-ones bit pattern (the sentinel, a
  * negative NaN, Sec. IV "Sentinel"); such an input makes the call time out.
- * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_POISONED, RRA_ERR_CUDA.
+ * The cluster algorithms take nranks <= 16 (RRA_ERR_INVALID_ARG above that)
+ * and return RRA_ERR_NOT_CORESIDENT if the device cannot schedule a cluster
+ * of nranks CTAs with a 96 KiB stage each.
+ * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_POISONED, RRA_ERR_CUDA,
+ * RRA_ERR_NOT_CORESIDENT.
  */
 rra_status_t rra_allreduce(rra_comm_t comm, const void* const send[], void* const recv[],
                            size_t count, rra_dtype_t dtype, rra_algo_t algo,
@@ -215,12 +233,18 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
                              size_t scratch_twoshot, rra_layout_t* out);
 
 /* The algorithm RRA_AUTO uses for `nranks` ranks and `bytes` per rank (pure
- * host arithmetic).  The paper selects kernels by message size and rank count
- * from measurements ("<1 MiB one-shot, 1-2 MiB two-shot at 4 ranks"); these
- * thresholds are the crossovers measured on GB300 with CUDA-graph replay:
- * one-shot sentinel while nranks * bytes <= 1.5 MiB (N <= 8); for N >= 16
- * one-shot sentinel up to 4 KiB, LL128-atomic up to 16 KiB (64 KiB at N = 64);
- * the direct two-shot above. */
+ * host arithmetic).  The paper picks its kernel from measured crossovers in
+ * message size and rank count (one-shot for small messages, two-shot once
+ * they reach about a mebibyte at four ranks); these thresholds are the
+ * crossovers measured on GB300 with CUDA-graph replay:
+ *   nranks <= 16: the cluster one-shot while nranks^2 * bytes <= 1 MiB (its
+ *                 shared-memory traffic is N (N-1) M), the cluster two-shot
+ *                 above;
+ *   nranks >= 17: one-shot sentinel up to 4 KiB, LL128-atomic up to 16 KiB
+ *                 (64 KiB at N = 64), the direct two-shot above.
+ * If the device cannot schedule a cluster of nranks CTAs, RRA_AUTO uses the
+ * choice without cluster kernels: one-shot sentinel while
+ * nranks * bytes <= 1.5 MiB (N <= 8), else as for nranks >= 17. */
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out);
 
 /* Number of CTAs the next call of (count, dtype, algo) would launch, and the
@@ -239,10 +263,13 @@ rra_status_t rra_comm_max_coresident(rra_comm_t comm, rra_dtype_t dtype, rra_alg
 rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
 
 /* Optional in-kernel trace (diagnostics).  `dev_buf` holds 6 uint64_t per
- * CTA of the largest grid; while set, thread 0 of every one-shot CTA (narrow
- * variant) records %globaltimer at: start, control words read, first push
- * issued, first position polled and reduced, its output stored, end.  Entries
- * a kernel does not reach stay unchanged.  NULL switches tracing off. */
+ * CTA of the largest grid; while set, thread 0 of every CTA records
+ * %globaltimer at six points.  One-shot kernels (narrow variant): start,
+ * control words read, first push issued, first position polled and reduced,
+ * its output stored, end.  Cluster kernels: start, first input in registers,
+ * first cluster barrier passed, pushes issued, all contributions arrived,
+ * end.  Entries a kernel does not reach stay unchanged.  NULL switches
+ * tracing off. */
 rra_status_t rra_comm_set_trace(rra_comm_t comm, uint64_t* dev_buf);
 
 /* Fault injection for tests (host-side injection only; no GPU fault): while

@@ -1,15 +1,28 @@
-// cluster.cu -- one-shot push AllReduce through distributed shared memory.
+// cluster.cu -- push AllReduce through distributed shared memory.
 //
-// "Every Microsecond Matters", Sec. III-A (one-shot, push) and Sec. IV (data
-// arrival as the only synchronisation), restated for what one GB300 offers
-// below L2: the CTAs of a thread-block cluster sit on one GPC and can store
-// into each other's shared memory.  A cluster holds one CTA per virtual rank
-// for one slice of the message; CTA r's shared memory is rank r's window for
-// that slice.  Each CTA pushes its input slice into slot [r] of every peer
-// with st.async, which also completes the receiver's mbarrier transaction
-// count; the receiver waits on its own mbarrier -- the arrival of the bytes
-// is the signal -- and adds the N slots in rank order (bit-identical to the
-// other one-shot kernels).
+// "Every Microsecond Matters", Sec. III-A (one-shot and two-shot, push) and
+// Sec. IV (data arrival as the only synchronisation), restated for what one
+// GB300 offers below L2: the CTAs of a thread-block cluster sit on one GPC,
+// are scheduled together by the hardware, and can store into each other's
+// shared memory.  A cluster holds one CTA per virtual rank for one slice of
+// the message; CTA r's shared memory is rank r's window for that slice.  A
+// CTA reads only its own rank's input and writes only into peers' windows
+// (and, for the two-shot, into every rank's output).  A push is an st.async,
+// which also completes the receiver's mbarrier transaction count: the
+// receiver waits on its own mbarrier -- the arrival of the bytes is the
+// signal -- and adds the N contributions in rank order (bit-identical to the
+// other fixed-order kernels).
+//
+//   one-shot: rank r pushes its whole slice into slot [r] of every peer; each
+//             CTA reduces the slice and stores it into its own rank's output.
+//   two-shot: the slice is cut into N partitions; rank r pushes partition q
+//             into slot [r] of CTA q only (the ReduceScatter), CTA q reduces
+//             partition q and stores it into every rank's output (the
+//             AllGather, as direct stores into the outputs, which are treated
+//             as registered symmetric buffers, Sec. II-B).  N times less
+//             shared-memory traffic and stage than the one-shot, the same
+//             single synchronisation hop, and HBM sees only the compulsory
+//             N*M bytes read and N*M written.
 //
 // Shared memory and mbarriers live only as long as a launch, so no epoch or
 // flag state persists between calls and nothing needs resetting.  The price
@@ -75,24 +88,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 }  // namespace
 
-template <typename T>
-__global__ void __launch_bounds__(256) oneshot_cluster_kernel(const __grid_constant__ Params p) {
+// One slice per cluster, CTA r of the cluster = rank r.  Stage layout: N
+// slots of Q vectors, slot [q] = rank q's contribution; Q = S (one-shot) or
+// S / N (two-shot), S = p.per_cta vectors per slice.
+template <typename T, bool kTwoShot>
+__global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Params p) {
     using M = VecMath<T>;
-    extern __shared__ __align__(16) uint4 stage[];  // [nranks][per_cta] payload vectors
+    extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
-    const int N = p.nranks;
-    const int r = (int)cluster_ctarank();
-    const uint32_t slice = cluster_id();
-    const uint32_t P = p.per_cta;
-    const uint32_t pos0 = slice * P;
-    const uint32_t npos = min(P, p.nvec - pos0);
-    // first input vector and the injected-fault word, both in flight at once
-    uint4 first = make_uint4(0, 0, 0, 0);
-    if (threadIdx.x < npos) first = load_input<T>(p.send[r], pos0 + threadIdx.x, p.count);
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = kTwoShot ? S / N : S;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const void* src = p.send[r];
+    // positions this CTA reduces: the whole slice, or partition r of it
+    const uint32_t mine = kTwoShot ? (npos > r * Q ? min(Q, npos - r * Q) : 0u) : npos;
+
+    // first batch of inputs and the injected-fault word, in flight together
+    // with the barrier set-up below
+    uint4 x[kClusterBatch];
+#pragma unroll
+    for (int j = 0; j < kClusterBatch; ++j) {
+        const uint32_t v = threadIdx.x + (uint32_t)j * nt;
+        x[j] = make_uint4(0, 0, 0, 0);
+        if (v < npos) x[j] = load_input<T>(src, base + v, p.count);
+    }
     const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
+                                                                   : nullptr;
+    if (tr) {
+        tr[0] = t_start;
+        tr[1] = globaltimer_after((uint64_t)x[0].x + (uint64_t)(uint32_t)drop);
+    }
 
     const uint32_t my_bar = smem_u32(&bar);
     if (threadIdx.x == 0) {
@@ -100,31 +133,55 @@ __global__ void __launch_bounds__(256) oneshot_cluster_kernel(const __grid_const
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     cluster_sync();  // every peer's barrier exists before anyone stores into it
+    if (tr) tr[2] = globaltimer_ns();
     if (threadIdx.x == 0) {
         uint64_t state;
-        const uint32_t bytes = (uint32_t)(N - 1) * npos * (uint32_t)kVecBytes;
+        const uint32_t bytes = (N - 1) * mine * (uint32_t)kVecBytes;
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
                      : "=l"(state)
                      : "r"(my_bar), "r"(bytes)
                      : "memory");
     }
-    // push: my slice into slot [r] of every peer (and of my own stage)
-    const uint32_t slot_r = smem_u32(stage + (uint32_t)r * P);
+    // push: vector v of my slice goes to slot [r] of its destination(s)
+    const uint32_t slot_r = smem_u32(stage + r * Q);
+    const uint32_t step = nt * (uint32_t)kClusterBatch;
 #pragma unroll 1
-    for (uint32_t v = threadIdx.x; v < npos; v += blockDim.x) {
-        const uint4 x = (v == threadIdx.x) ? first : load_input<T>(p.send[r], pos0 + v, p.count);
-        stage[(uint32_t)r * P + v] = x;
-        if (drop == r) continue;
+    for (uint32_t b0 = 0; b0 < npos; b0 += step) {
+        if (b0 != 0) {
+#pragma unroll
+            for (int j = 0; j < kClusterBatch; ++j) {
+                const uint32_t v = b0 + threadIdx.x + (uint32_t)j * nt;
+                if (v < npos) x[j] = load_input<T>(src, base + v, p.count);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = b0 + threadIdx.x + (uint32_t)j * nt;
+            if (v >= npos) continue;
+            if (kTwoShot) {
+                const uint32_t q = v / Q;
+                const uint32_t u = v - q * Q;
+                if (q == r) {
+                    stage[r * Q + u] = x[j];
+                } else if (drop != (int32_t)r) {
+                    st_async_v4(map_to_rank(slot_r + u * (uint32_t)kVecBytes, q), x[j], map_to_rank(my_bar, q));
+                }
+            } else {
+                stage[r * Q + v] = x[j];
+                if (drop == (int32_t)r) continue;
 #pragma unroll 1
-        for (int q = 0; q < N; ++q) {
-            if (q == r) continue;
-            st_async_v4(map_to_rank(slot_r + v * kVecBytes, (uint32_t)q), x, map_to_rank(my_bar, (uint32_t)q));
+                for (uint32_t k = 1; k < N; ++k) {
+                    const uint32_t q = r + k < N ? r + k : r + k - N;
+                    st_async_v4(map_to_rank(slot_r + v * (uint32_t)kVecBytes, q), x[j], map_to_rank(my_bar, q));
+                }
+            }
         }
     }
-    // wait for the N-1 incoming slices (bounded)
+    if (tr) tr[3] = globaltimer_ns();
+    // wait for the N-1 incoming contributions (bounded)
     int ok = 1;
     {
-        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, r, 0);
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
         while (!mbar_try_wait(my_bar, 0u)) {
             if (waiter_expired(w)) {
                 ok = 0;
@@ -132,28 +189,41 @@ __global__ void __launch_bounds__(256) oneshot_cluster_kernel(const __grid_const
             }
         }
     }
+    if (tr && ok) tr[4] = globaltimer_ns();
+    __syncthreads();  // my own slot was written by other threads of this CTA
     if (ok) {
-        // reduce in rank order; each thread reads its own stage[r] writes and
-        // the peers' slots, which the mbarrier completion made visible
+        // reduce in rank order; the mbarrier completion made the peers' slots visible
 #pragma unroll 1
-        for (uint32_t v = threadIdx.x; v < npos; v += blockDim.x) {
-            typename M::Acc acc = M::load(stage[v]);
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            typename M::Acc acc = M::load(stage[u]);
 #pragma unroll 1
-            for (int q = 1; q < N; ++q) M::add(acc, stage[(uint32_t)q * P + v]);
-            store_output<T>(p.recv[r], pos0 + v, p.count, M::store(acc));
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * Q + u]);
+            const uint4 out = M::store(acc);
+            if (kTwoShot) {
+                const uint32_t pos = base + r * Q + u;
+#pragma unroll 1
+                for (uint32_t k = 0; k < N; ++k) {
+                    const uint32_t d = r + k < N ? r + k : r + k - N;
+                    store_output<T>(p.recv[d], pos, p.count, out);
+                }
+            } else {
+                store_output<T>(p.recv[r], base + u, p.count, out);
+            }
         }
     }
     __syncthreads();
     cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
     if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
         p.timing[2 * blockIdx.x] = t_start;
-        p.timing[2 * blockIdx.x + 1] = globaltimer_ns();
+        p.timing[2 * blockIdx.x + 1] = t_end;
     }
+    if (tr) tr[5] = globaltimer_ns();
 }
 
-template <typename T>
+template <typename T, bool kTwoShot>
 static cudaError_t launch_cluster_t(const Params& p, int threads, size_t smem, cudaStream_t stream, bool pdl) {
-    const void* k = (const void*)oneshot_cluster_kernel<T>;
+    const void* k = (const void*)cluster_kernel<T, kTwoShot>;
     static bool configured[3] = {false, false, false};
     const int idx = sizeof(T) == 4 ? 0 : sizeof(T) == 2 ? 1 : 2;
     if (!configured[idx]) {
@@ -186,15 +256,65 @@ static cudaError_t launch_cluster_t(const Params& p, int threads, size_t smem, c
     return cudaLaunchKernelExC(&cfg, k, args);
 }
 
-cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int threads, cudaStream_t stream, bool pdl) {
-    const size_t smem = (size_t)p.nranks * p.per_cta * kVecBytes;
-    if (smem > kClusterStageBytes || p.nranks > kClusterMaxRanks) return cudaErrorInvalidValue;
+template <bool kTwoShot>
+static cudaError_t launch_cluster_kind(const Params& p, rra_dtype_t dtype, int threads, size_t smem,
+                                       cudaStream_t stream, bool pdl) {
     switch (dtype) {
-        case RRA_FP32: return launch_cluster_t<float>(p, threads, smem, stream, pdl);
-        case RRA_BF16: return launch_cluster_t<__nv_bfloat16>(p, threads, smem, stream, pdl);
-        case RRA_FP64: return launch_cluster_t<double>(p, threads, smem, stream, pdl);
+        case RRA_FP32: return launch_cluster_t<float, kTwoShot>(p, threads, smem, stream, pdl);
+        case RRA_BF16: return launch_cluster_t<__nv_bfloat16, kTwoShot>(p, threads, smem, stream, pdl);
+        case RRA_FP64: return launch_cluster_t<double, kTwoShot>(p, threads, smem, stream, pdl);
     }
     return cudaErrorInvalidValue;
+}
+
+size_t cluster_stage_bytes(const Params& p, bool two_shot) {
+    const size_t q = two_shot ? p.per_cta / (uint32_t)p.nranks : p.per_cta;
+    return (size_t)p.nranks * q * kVecBytes;
+}
+
+cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, bool two_shot, int threads, cudaStream_t stream,
+                           bool pdl) {
+    const size_t smem = cluster_stage_bytes(p, two_shot);
+    if (smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks) return cudaErrorInvalidValue;
+    if (two_shot && p.per_cta % (uint32_t)p.nranks != 0) return cudaErrorInvalidValue;
+    return two_shot ? launch_cluster_kind<true>(p, dtype, threads, smem, stream, pdl)
+                    : launch_cluster_kind<false>(p, dtype, threads, smem, stream, pdl);
+}
+
+// Clusters of `nranks` CTAs with the largest stage that can be resident at
+// once (0 = this cluster shape cannot run on the device).
+int cluster_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads) {
+    const void* k = nullptr;
+    switch (dtype) {
+        case RRA_FP32: k = two_shot ? (const void*)cluster_kernel<float, true> : (const void*)cluster_kernel<float, false>; break;
+        case RRA_BF16:
+            k = two_shot ? (const void*)cluster_kernel<__nv_bfloat16, true> : (const void*)cluster_kernel<__nv_bfloat16, false>;
+            break;
+        case RRA_FP64: k = two_shot ? (const void*)cluster_kernel<double, true> : (const void*)cluster_kernel<double, false>; break;
+    }
+    if (k == nullptr) return 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nranks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = kClusterStageBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)nranks;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace rra

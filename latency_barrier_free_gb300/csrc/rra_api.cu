@@ -46,7 +46,8 @@ size_t elem_size(rra_dtype_t d) {
     return 0;
 }
 
-bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_ONESHOT_CLUSTER; }
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_TWOSHOT_CLUSTER; }
+bool is_cluster(int a) { return a == RRA_ONESHOT_CLUSTER || a == RRA_TWOSHOT_CLUSTER; }
 bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
 
 int64_t env_i64(const char* name, int64_t dflt) {
@@ -95,6 +96,8 @@ struct rra_comm {
     int64_t oneshot_wide = -1;              // -1 auto (N >= 16), 0 never, 1 always
     int64_t cooperative = 1;                // cooperative launch (co-residency guaranteed)
     int64_t pdl = 1;                        // programmatic dependent launch
+    int64_t cluster_slice = 0;              // cluster kernels: bytes per rank per slice, 0 = auto
+    int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -123,16 +126,26 @@ const char* rra_status_string(rra_status_t s) {
     return "unknown status";
 }
 
+// Choice without the cluster kernels (also the fallback when the device
+// cannot schedule a cluster of N CTAs).
+static rra_algo_t select_global(int nranks, size_t bytes) {
+    const size_t total = (size_t)nranks * bytes;
+    if (nranks <= 8) return total <= (3ull << 19) ? RRA_ONESHOT_SENTINEL : RRA_TWOSHOT_DIRECT;
+    const size_t ll128_max = nranks >= 64 ? (64u << 10) : (16u << 10);
+    if (bytes <= (4u << 10)) return RRA_ONESHOT_SENTINEL;
+    if (bytes <= ll128_max) return RRA_LL128_ATOMIC;
+    return RRA_TWOSHOT_DIRECT;
+}
+
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out) {
     if (out == nullptr || nranks < 2 || nranks > RRA_MAX_RANKS || !valid_dtype(dtype)) return RRA_ERR_INVALID_ARG;
-    const size_t total = (size_t)nranks * bytes;
-    if (nranks <= 8) {
-        *out = total <= (3ull << 19) ? RRA_ONESHOT_SENTINEL : RRA_TWOSHOT_DIRECT;
+    if (nranks <= rra::kClusterMaxRanks) {
+        // one-shot while its shared-memory traffic N (N-1) M stays small:
+        // N^2 M <= 1 MiB (GB300 sweep, N = 2..16); two-shot above
+        const size_t n2m = (size_t)nranks * (size_t)nranks * bytes;
+        *out = n2m <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
     } else {
-        const size_t ll128_max = nranks >= 64 ? (64u << 10) : (16u << 10);
-        if (bytes <= (4u << 10)) *out = RRA_ONESHOT_SENTINEL;
-        else if (bytes <= ll128_max) *out = RRA_LL128_ATOMIC;
-        else *out = RRA_TWOSHOT_DIRECT;
+        *out = select_global(nranks, bytes);
     }
     return RRA_OK;
 }
@@ -319,6 +332,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < 0 || v > 1) return RRA_ERR_INVALID_ARG;
             c->pdl = v;
             return RRA_OK;
+        case RRA_ATTR_CLUSTER_SLICE:
+            if (v < 0 || v % 16 || v > (int64_t)rra::kClusterStageBytes) return RRA_ERR_INVALID_ARG;
+            c->cluster_slice = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -335,19 +352,31 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_ONESHOT_WIDE: *v = c->oneshot_wide; return RRA_OK;
         case RRA_ATTR_COOPERATIVE: *v = c->cooperative; return RRA_OK;
         case RRA_ATTR_PDL: *v = c->pdl; return RRA_OK;
+        case RRA_ATTR_CLUSTER_SLICE: *v = c->cluster_slice; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
 
-// Plan of a cluster one-shot call: one position per thread, slices of at most
-// kClusterStageBytes / (N * 16) vectors, one cluster of N CTAs per slice.
-static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, Params* p, int* threads) {
+// Plan of a cluster call: one cluster of N CTAs per slice of S vectors, CTA
+// r of a cluster = rank r.  S: one position per thread while the message is
+// small; past that, about two CTAs per SM in one wave, up to one batch of
+// kClusterBatch loads per thread (GB300 sweep: 16 KiB slices of 128 threads
+// were fastest from 4 MiB up at N = 2..16); at most the 96 KiB stage (N x S
+// vectors for the one-shot, S for the two-shot, whose S is a multiple of N).
+static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo, Params* p,
+                                 int* threads) {
+    const bool two = algo == RRA_TWOSHOT_CLUSTER;
+    const size_t n = (size_t)c->nranks;
     if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    int& fits = c->cluster_fits[two ? 1 : 0][(int)dtype];
+    if (fits < 0) fits = rra::cluster_max_active(dtype, two, c->nranks, 256) > 0 ? 1 : 0;
+    if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
     const size_t ve = rra::kVecBytes / elem_size(dtype);
     memset(p, 0, sizeof(*p));
     p->win0 = c->win0;
     p->ctrl = c->ctrl;
     p->timing = c->timing;
+    p->trace = c->trace;
     p->stride = c->lay.window_stride;
     p->count = count;
     p->nvec = (uint32_t)ceil_div(count, ve);
@@ -355,12 +384,24 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, P
     p->nranks = c->nranks;
     p->nsteps = 1;
     p->chunk_vecs = p->nvec;
-    const size_t pmax = rra::kClusterStageBytes / ((size_t)c->nranks * rra::kVecBytes);
-    const size_t per = std::min<size_t>(std::min<size_t>(pmax, (size_t)c->threads), p->nvec);
-    p->per_cta = (uint32_t)per;
-    p->ctas_per_rank = (int32_t)ceil_div(p->nvec, per);  // slices = clusters
+    const size_t stage_vecs = rra::kClusterStageBytes / rra::kVecBytes;
+    const size_t smax = two ? stage_vecs / n * n : stage_vecs / n;
+    size_t S;
+    if (c->cluster_slice > 0) {
+        S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else {
+        // one vector per thread for small messages; then spread over about
+        // two CTAs per SM, but at most one batch of loads per thread
+        const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / n);
+        S = std::max<size_t>(std::min<size_t>(p->nvec, (size_t)c->threads), ceil_div(p->nvec, target));
+        S = std::min<size_t>(S, (size_t)c->threads * rra::kClusterBatch);
+    }
+    if (two) S = align_up(S, n);
+    S = std::max<size_t>(two ? n : 1, std::min(S, smax));
+    p->per_cta = (uint32_t)S;
+    p->ctas_per_rank = (int32_t)ceil_div(p->nvec, S);  // slices = clusters
     p->epoch_slots = rra::kEpochSlots;
-    *threads = (int)std::min<size_t>((size_t)c->threads, std::max<size_t>(32, align_up(per, 32)));
+    *threads = (int)std::min<size_t>((size_t)c->threads, std::max<size_t>(32, align_up(S, 32)));
     return RRA_OK;
 }
 
@@ -381,8 +422,7 @@ static rra_status_t max_ctas_kind(rra_comm* c, rra_dtype_t d, int kind, int* cta
 }
 
 rra_status_t rra_comm_max_coresident(rra_comm_t c, rra_dtype_t d, rra_algo_t a, int* ctas) {
-    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a) || a == RRA_AUTO ||
-        a == RRA_ONESHOT_CLUSTER)
+    if (c == nullptr || ctas == nullptr || !valid_dtype(d) || !valid_algo(a) || a == RRA_AUTO || is_cluster(a))
         return RRA_ERR_INVALID_ARG;
     return max_ctas_kind(c, d, kernel_kind(c, a), ctas);
 }
@@ -528,11 +568,16 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
                                 int* grid_ctas, int* steps) {
     if (c == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0) return RRA_ERR_INVALID_ARG;
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
-    if (algo == RRA_AUTO) rra_select_algo(c->nranks, count * elem_size(dtype), dtype, &algo);
+    const bool autoselect = algo == RRA_AUTO;
+    if (autoselect) rra_select_algo(c->nranks, count * elem_size(dtype), dtype, &algo);
     Params p;
     int kind = 0, threads = 0;
-    rra_status_t st = algo == RRA_ONESHOT_CLUSTER ? plan_cluster(c, count, dtype, &p, &threads)
-                                                  : plan_call(c, count, dtype, algo, &p, &kind, &threads);
+    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads)
+                                       : plan_call(c, count, dtype, algo, &p, &kind, &threads);
+    if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
+        algo = select_global(c->nranks, count * elem_size(dtype));
+        st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
+    }
     if (st != RRA_OK) return st;
     if (grid_ctas) *grid_ctas = p.nranks * p.ctas_per_rank;
     if (steps) *steps = (int)p.nsteps;
@@ -547,13 +592,18 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     if (count == 0) return RRA_OK;
     const size_t es = elem_size(dtype);
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
-    if (algo == RRA_AUTO) rra_select_algo(c->nranks, count * es, dtype, &algo);
+    const bool autoselect = algo == RRA_AUTO;
+    if (autoselect) rra_select_algo(c->nranks, count * es, dtype, &algo);
     Params p;
     int kind = 0, threads = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = algo == RRA_ONESHOT_CLUSTER ? plan_cluster(c, count, dtype, &p, &threads)
-                                                      : plan_call(c, count, dtype, algo, &p, &kind, &threads);
+        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads)
+                                           : plan_call(c, count, dtype, algo, &p, &kind, &threads);
+        if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
+            algo = select_global(c->nranks, count * es);
+            st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
+        }
         if (st != RRA_OK) return st;
     }
     for (int r = 0; r < c->nranks; ++r) {
@@ -562,8 +612,9 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
-    cudaError_t e = algo == RRA_ONESHOT_CLUSTER
-                        ? rra::launch_cluster(p, dtype, threads, (cudaStream_t)stream, c->pdl != 0)
+    cudaError_t e = is_cluster(algo)
+                        ? rra::launch_cluster(p, dtype, algo == RRA_TWOSHOT_CLUSTER, threads, (cudaStream_t)stream,
+                                              c->pdl != 0)
                         : rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0,
                                                 c->pdl != 0);
     if (e == cudaErrorCooperativeLaunchTooLarge) {

@@ -85,16 +85,21 @@ enum KernelKind {
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors
 constexpr int kTracePoints = 6;       // start, control words read, pushed, polled, stored, end
-constexpr size_t kClusterStageBytes = 96u << 10;  // cluster one-shot: shared-memory stage per CTA
-constexpr int kClusterMaxRanks = 16;              // cluster one-shot: ranks per cluster (one CTA each)
+constexpr size_t kClusterStageBytes = 96u << 10;  // cluster kernels: shared-memory stage per CTA
+constexpr int kClusterMaxRanks = 16;              // cluster kernels: ranks per cluster (one CTA each)
+constexpr int kClusterBatch = 8;                  // cluster kernels: input vectors a thread keeps in flight
 
 // Host-side launch entry points (kernels.cu).
 cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int threads, cudaStream_t stream,
                              bool cooperative = true, bool pdl = false);
 cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm);
-// One-shot through distributed shared memory (cluster.cu): one cluster of
-// nranks CTAs per slice of per_cta vectors; p.ctas_per_rank = slices.
-cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int threads, cudaStream_t stream, bool pdl);
+// One-shot / two-shot through distributed shared memory (cluster.cu): one
+// cluster of N CTAs per slice of p.per_cta vectors (a multiple of N for the
+// two-shot), p.ctas_per_rank slices.
+size_t cluster_stage_bytes(const Params& p, bool two_shot);
+cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, bool two_shot, int threads, cudaStream_t stream,
+                           bool pdl);
+int cluster_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

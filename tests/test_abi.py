@@ -108,19 +108,24 @@ def test_create_without_gpu_fails_cleanly():
 def test_auto_selection_by_size_and_ranks():
     # the paper picks one-shot for small and two-shot for larger messages at a
     # given rank count; the GB300 crossovers differ from its GB200 ones
-    assert rra.select_algo(4, 128) == "oneshot_sentinel"
-    assert rra.select_algo(4, 256 << 10) == "oneshot_sentinel"
-    assert rra.select_algo(4, 1 << 20) == "twoshot_direct"
-    assert rra.select_algo(8, 16 << 10, "bf16") == "oneshot_sentinel"
-    assert rra.select_algo(8, 1 << 20, "bf16") == "twoshot_direct"
+    assert rra.select_algo(4, 128) == "oneshot_cluster"
+    assert rra.select_algo(4, 64 << 10) == "oneshot_cluster"  # N^2 M = 1 MiB
+    assert rra.select_algo(4, (64 << 10) + 16) == "twoshot_cluster"
+    assert rra.select_algo(4, 1 << 20) == "twoshot_cluster"
+    assert rra.select_algo(2, 256 << 10, "bf16") == "oneshot_cluster"
+    assert rra.select_algo(8, 16 << 10, "bf16") == "oneshot_cluster"
+    assert rra.select_algo(8, 1 << 20, "bf16") == "twoshot_cluster"
+    assert rra.select_algo(16, 4 << 10) == "oneshot_cluster"
+    assert rra.select_algo(16, 64 << 10) == "twoshot_cluster"
+    assert rra.select_algo(17, 1 << 10) == "oneshot_sentinel"
     assert rra.select_algo(64, 1 << 10) == "oneshot_sentinel"
     assert rra.select_algo(64, 64 << 10) == "ll128_atomic"
-    assert rra.select_algo(16, 64 << 10) == "twoshot_direct"
     assert rra.select_algo(32, 16 << 10) == "ll128_atomic"
     assert rra.select_algo(64, 1 << 20) == "twoshot_direct"
-    for n in (2, 4, 8, 16, 64):  # once two-shot, always two-shot as the message grows
+    twoshot = ("twoshot_cluster", "twoshot_direct")
+    for n in (2, 4, 8, 16, 17, 64):  # once two-shot, always two-shot as the message grows
         picks = [rra.select_algo(n, 1 << k) for k in range(4, 31)]
-        first = picks.index("twoshot_direct")
-        assert all(p == "twoshot_direct" for p in picks[first:])
+        first = min(i for i, p in enumerate(picks) if p in twoshot)
+        assert all(p in twoshot for p in picks[first:])
     with pytest.raises(rra.RraError):
         rra.select_algo(1, 128)

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 from latency_barrier_free_gb300 import inputs, rra
-from tests.gpu_util import ALGOS, ELEM, FIXED_ORDER, bits, check_against_oracle, poison_like, to_device, to_host
+from tests.gpu_util import ALGOS, CLUSTER, ELEM, FIXED_ORDER, bits, check_against_oracle, poison_like, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -36,7 +36,7 @@ def run(comm, sends_np, dtype, algo, in_place=False):
 
 
 # ---------------------------------------------------------------- workload 1
-@pytest.mark.parametrize("algo", ["oneshot_ll", "oneshot_sentinel"])
+@pytest.mark.parametrize("algo", ["oneshot_ll", "oneshot_sentinel", "oneshot_cluster", "twoshot_cluster"])
 def test_workload1_1000_back_to_back(algo):
     """N=2, 32 binary32 integers in [-8, 8], a fresh draw for each of 1000
     back-to-back calls (distinct buffers, one stream): every result exact."""
@@ -57,7 +57,7 @@ def test_workload1_1000_back_to_back(algo):
             assert np.array_equal(got[i, r], exact[i].astype(np.float32)), (i, r)
 
 
-@pytest.mark.parametrize("algo", ["oneshot_ll", "oneshot_sentinel"])
+@pytest.mark.parametrize("algo", ["oneshot_ll", "oneshot_sentinel", "twoshot_cluster"])
 def test_workload1_same_buffers(algo):
     """1000 calls reusing one send/recv pair, new inputs copied in between."""
     with rra.Comm(2, 128) as comm:
@@ -77,7 +77,7 @@ def test_workload1_same_buffers(algo):
 
 # ---------------------------------------------------------------- workload 2
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_workload2_size_sweep(algo, dtype):
     """N=4, 128 B .. 1 MiB per rank, N(0,1) inputs."""
     with rra.Comm(4, 1 << 20) as comm:
@@ -110,7 +110,7 @@ def test_workload4_rank_sweep(algo):
 
 # ------------------------------------------------------------- edge cases
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_ragged_counts_and_odd_ranks(algo, dtype):
     """Counts that are not a multiple of a 16-byte vector, odd N."""
     for n in (2, 3, 5):
@@ -121,7 +121,7 @@ def test_ragged_counts_and_odd_ranks(algo, dtype):
                 check_against_oracle(sends_np, got, dtype, algo)
 
 
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_count_zero_is_noop(algo):
     with rra.Comm(4, 1024) as comm:
         x = [torch.ones(4, device="cuda") for _ in range(4)]
@@ -132,7 +132,7 @@ def test_count_zero_is_noop(algo):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_in_place(algo, dtype):
     with rra.Comm(4, 1 << 16) as comm:
         for count in (7, 1000, (1 << 16) // ELEM[dtype]):
@@ -142,7 +142,7 @@ def test_in_place(algo, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_closed_form_every_dtype(algo, dtype):
     """Rank r filled with r + 1 sums to N(N+1)/2 (exact for these N)."""
     for n in (2, 4, 8):
@@ -178,14 +178,14 @@ def test_many_steps_credit_chain(algo, ctas, threads):
 
 
 def test_mixed_algorithms_interleaved():
-    """Alternate all algorithms and dtypes on one communicator, 60 calls
+    """Alternate all algorithms and dtypes on one communicator, 70 calls
     enqueued back to back, all checked at the end."""
     n = 4
     rng_sizes = np.random.Generator(np.random.PCG64(5))
     with rra.Comm(n, 1 << 18) as comm:
         pending = []
-        for i in range(60):
-            algo = ALGOS[i % len(ALGOS)]
+        for i in range(70):
+            algo = (ALGOS + CLUSTER)[i % len(ALGOS + CLUSTER)]
             dtype = ("fp32", "bf16", "fp64")[i % 3]
             count = int(rng_sizes.integers(1, (1 << 18) // ELEM[dtype]))
             sends_np = inputs.normal(inputs.rng(63, i), n, count, dtype)
@@ -269,24 +269,58 @@ def test_auto_algorithm(n):
             check_against_oracle(sends_np, got, "fp32", algo)
 
 
+@pytest.mark.parametrize("algo", CLUSTER)
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
 @pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
-def test_oneshot_cluster(n, dtype):
-    """One-shot through distributed shared memory (one cluster of N CTAs per
-    slice): bit-exact, for ragged sizes, many slices, and in place."""
+def test_cluster_kernels(n, dtype, algo):
+    """One-shot and two-shot through distributed shared memory (one cluster
+    of N CTAs per slice): bit-exact, for ragged sizes (two-shot partitions
+    that are partly or wholly empty), many slices, and in place."""
     with rra.Comm(n, 300000 * ELEM[dtype]) as comm:
         for count in (1, 7, 33, 4097, 70001, 300000):
             sends_np = inputs.normal(inputs.rng(69, count, n), n, count, dtype)
-            got = run(comm, sends_np, dtype, "oneshot_cluster")
-            check_against_oracle(sends_np, got, dtype, "oneshot_cluster")
+            got = run(comm, sends_np, dtype, algo)
+            check_against_oracle(sends_np, got, dtype, algo)
         sends_np = inputs.normal(inputs.rng(69, 1, n), n, 5000, dtype)
-        got = run(comm, sends_np, dtype, "oneshot_cluster", in_place=True)
-        check_against_oracle(sends_np, got, dtype, "oneshot_cluster")
+        got = run(comm, sends_np, dtype, algo, in_place=True)
+        check_against_oracle(sends_np, got, dtype, algo)
 
 
-def test_oneshot_cluster_rejects_too_many_ranks():
+@pytest.mark.parametrize("algo", CLUSTER)
+@pytest.mark.parametrize("threads", [64, 128, 256])
+def test_cluster_slice_sizes(algo, threads):
+    """Slices from one vector per rank to the full 96 KiB stage, so that a
+    thread pushes up to several batches of inputs; ragged last slice."""
+    dtype = "fp32"
+    for n in (2, 4, 16):
+        count = 200000 + 5
+        with rra.Comm(n, count * 4) as comm:
+            comm.set_attr("threads", threads)
+            for slice_bytes in (16, 16 * n, 4096, 48 << 10, 96 << 10):
+                comm.set_attr("cluster_slice", slice_bytes)
+                grid, _ = comm.plan_call(count, dtype, algo)
+                assert grid % n == 0
+                sends_np = inputs.normal(inputs.rng(72, n, slice_bytes, threads), n, count, dtype)
+                got = run(comm, sends_np, dtype, algo)
+                check_against_oracle(sends_np, got, dtype, algo)
+
+
+@pytest.mark.parametrize("algo", CLUSTER)
+def test_cluster_rank_sweep(algo):
+    """N in {2, 4, 8, 16} at 16 KiB and 1 MiB per rank (workload 4's sweep,
+    up to the cluster limit)."""
+    for n in (2, 4, 8, 16):
+        with rra.Comm(n, 1 << 20) as comm:
+            for size in (16 << 10, 1 << 20):
+                sends_np = inputs.workload4(size, n)
+                got = run(comm, sends_np, "fp32", algo)
+                check_against_oracle(sends_np, got, "fp32", algo)
+
+
+@pytest.mark.parametrize("algo", CLUSTER)
+def test_cluster_rejects_too_many_ranks(algo):
     with rra.Comm(17, 4096) as comm:
         x = [torch.zeros(16, device="cuda") for _ in range(17)]
         with pytest.raises(rra.RraError) as e:
-            comm.allreduce(x, x, "oneshot_cluster")
+            comm.allreduce(x, x, algo)
         assert e.value.status == rra.ERR_INVALID_ARG

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from latency_barrier_free_gb300 import inputs, rra
-from tests.gpu_util import ALGOS, bits, check_against_oracle, poison_like, to_device, to_host
+from tests.gpu_util import ALGOS, CLUSTER, bits, check_against_oracle, poison_like, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -21,7 +21,7 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("algo", ALGOS + ("oneshot_cluster",))
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_graph_replay_advances_epochs(algo):
     """Capture 20 calls in a CUDA graph and replay it 5 times with new inputs
     copied in between: every replay must see fresh epochs (LL flags) and
@@ -57,7 +57,7 @@ def test_graph_replay_advances_epochs(algo):
                 check_against_oracle(host[i], list(got[i]), "fp32", algo)
 
 
-@pytest.mark.parametrize("algo", ALGOS + ("oneshot_cluster",))
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
 def test_timeout_poison_and_reset(algo):
     """A rank that drops its stores makes its peers' polls run out of time:
     the device records RRA_ERR_TIMEOUT (no fault, no hang), the communicator
