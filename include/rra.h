@@ -99,7 +99,8 @@ typedef enum {
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
 typedef enum {
-    RRA_ATTR_CTAS_PER_RANK = 0,    /* 0 = chosen per call from the message size */
+    RRA_ATTR_CTAS_PER_RANK = 0,    /* 0 = chosen per call from the message size; for the
+                                      persistent cluster two-shot, a cap on its clusters */
     RRA_ATTR_POLL_TIMEOUT_MS = 1,  /* limit of every device-side wait (default 1000) */
     RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256 */
     RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step; 0 (default) = the step
@@ -119,12 +120,22 @@ typedef enum {
                                       this one drains; each kernel waits
                                       (griddepcontrol.wait) for its predecessor before
                                       touching memory.  0: plain stream order */
-    RRA_ATTR_CLUSTER_SLICE = 9     /* cluster kernels: bytes per rank per slice (one cluster
+    RRA_ATTR_CLUSTER_SLICE = 9,    /* cluster kernels: bytes per rank per slice (one cluster
                                       per slice), a multiple of 16, at most 98304; clamped to
                                       the 96 KiB shared-memory stage (N x slice for the
                                       one-shot, slice for the two-shot, rounded up to N
                                       vectors).  0 (default): one 16-byte vector per thread
-                                      for small messages, else about two CTAs per SM */
+                                      for small messages, else about two CTAs per SM, at
+                                      most 8 vectors per thread */
+    RRA_ATTR_CLUSTER_PIPE = 10     /* cluster two-shot on the persistent, double-buffered
+                                      kernel (as many clusters as fit at once, each looping
+                                      over slices; a receiver's arrival on the sender's
+                                      "empty" mbarrier is the credit for the next push):
+                                      0 (default) never, -1 when the slices do not fit in
+                                      one wave, 1 whenever the slice allows (at most 8
+                                      vectors per thread and a 2 x slice stage <= 96 KiB).
+                                      Off by default: on GB300 it was up to 2.3x slower
+                                      than one cluster per slice at 4-64 MiB per rank */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -266,9 +277,9 @@ rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
  * CTA of the largest grid; while set, thread 0 of every CTA records
  * %globaltimer at six points.  One-shot kernels (narrow variant): start,
  * control words read, first push issued, first position polled and reduced,
- * its output stored, end.  Cluster kernels: start, first input in registers,
- * first cluster barrier passed, pushes issued, all contributions arrived,
- * end.  Entries a kernel does not reach stay unchanged.  NULL switches
+ * its output stored, end.  Cluster kernels (not the persistent two-shot):
+ * start, first input in registers, first cluster barrier passed, pushes
+ * issued, all contributions arrived, end.  Entries a kernel does not reach stay unchanged.  NULL switches
  * tracing off. */
 rra_status_t rra_comm_set_trace(rra_comm_t comm, uint64_t* dev_buf);
 

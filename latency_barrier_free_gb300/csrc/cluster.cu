@@ -62,9 +62,21 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void cluster_sync() {
+__device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    cluster_arrive();
+    cluster_wait();
 }
 
 __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
@@ -78,12 +90,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
         : "r"(bar), "r"(parity)
         : "memory");
     return done != 0;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" : : "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;" : "=l"(state) : "r"(bar), "r"(bytes) : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" : : "r"(cluster_bar) : "memory");
+}
+
+// Bounded wait of all threads on one phase of a local mbarrier.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, Waiter& w) {
+    while (!mbar_try_wait(bar, parity))
+        if (waiter_expired(w)) return false;
+    return true;
 }
 
 }  // namespace
@@ -97,8 +130,6 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint64_t t_start = globaltimer_ns();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -110,8 +141,22 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     // positions this CTA reduces: the whole slice, or partition r of it
     const uint32_t mine = kTwoShot ? (npos > r * Q ? min(Q, npos - r * Q) : 0u) : npos;
 
+    // The barrier lives in this launch's shared memory, so it is set up
+    // before waiting for the previous kernel; its phase completes when the
+    // N-1 contributions' bytes have arrived.  The cluster barrier that makes
+    // it visible to the peers is split: arrive now, wait just before the
+    // first push, so its latency overlaps the input loads.
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, (N - 1) * mine * (uint32_t)kVecBytes);
+    }
+    cluster_arrive();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+
     // first batch of inputs and the injected-fault word, in flight together
-    // with the barrier set-up below
     uint4 x[kClusterBatch];
 #pragma unroll
     for (int j = 0; j < kClusterBatch; ++j) {
@@ -126,22 +171,9 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
         tr[0] = t_start;
         tr[1] = globaltimer_after((uint64_t)x[0].x + (uint64_t)(uint32_t)drop);
     }
-
-    const uint32_t my_bar = smem_u32(&bar);
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" : : "r"(my_bar), "r"(1u) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    cluster_sync();  // every peer's barrier exists before anyone stores into it
+    cluster_wait();  // every peer's barrier exists before anyone stores into it
     if (tr) tr[2] = globaltimer_ns();
-    if (threadIdx.x == 0) {
-        uint64_t state;
-        const uint32_t bytes = (N - 1) * mine * (uint32_t)kVecBytes;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
-                     : "=l"(state)
-                     : "r"(my_bar), "r"(bytes)
-                     : "memory");
-    }
+
     // push: vector v of my slice goes to slot [r] of its destination(s)
     const uint32_t slot_r = smem_u32(stage + r * Q);
     const uint32_t step = nt * (uint32_t)kClusterBatch;
@@ -167,16 +199,23 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
                     st_async_v4(map_to_rank(slot_r + u * (uint32_t)kVecBytes, q), x[j], map_to_rank(my_bar, q));
                 }
             } else {
-                stage[r * Q + v] = x[j];
-                if (drop == (int32_t)r) continue;
+                if (drop != (int32_t)r) {
 #pragma unroll 1
-                for (uint32_t k = 1; k < N; ++k) {
-                    const uint32_t q = r + k < N ? r + k : r + k - N;
-                    st_async_v4(map_to_rank(slot_r + v * (uint32_t)kVecBytes, q), x[j], map_to_rank(my_bar, q));
+                    for (uint32_t k = 1; k < N; ++k) {
+                        const uint32_t q = r + k < N ? r + k : r + k - N;
+                        st_async_v4(map_to_rank(slot_r + v * (uint32_t)kVecBytes, q), x[j], map_to_rank(my_bar, q));
+                    }
                 }
+                stage[r * Q + v] = x[j];
             }
         }
     }
+    // Second cluster barrier, split and relaxed: arriving says "my pushes are
+    // issued".  It orders no data (a release here would stall until the
+    // pushes are acknowledged).  A CTA leaves only after its own mbarrier has
+    // seen every incoming byte, or, if its wait ran out, after every peer
+    // has issued its pushes (at least a poll time limit ago).
+    cluster_arrive_relaxed();
     if (tr) tr[3] = globaltimer_ns();
     // wait for the N-1 incoming contributions (bounded)
     int ok = 1;
@@ -190,7 +229,7 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
         }
     }
     if (tr && ok) tr[4] = globaltimer_ns();
-    __syncthreads();  // my own slot was written by other threads of this CTA
+    if (kTwoShot) __syncthreads();  // my own slot was written by other threads of this CTA
     if (ok) {
         // reduce in rank order; the mbarrier completion made the peers' slots visible
 #pragma unroll 1
@@ -211,8 +250,7 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
             }
         }
     }
-    __syncthreads();
-    cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
+    cluster_wait();  // every peer has issued its pushes into this CTA's shared memory
     if (p.timing != nullptr && threadIdx.x == 0) {
         const uint64_t t_end = globaltimer_ns();
         p.timing[2 * blockIdx.x] = t_start;
@@ -221,18 +259,193 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     if (tr) tr[5] = globaltimer_ns();
 }
 
-template <typename T, bool kTwoShot>
-static cudaError_t launch_cluster_t(const Params& p, int threads, size_t smem, cudaStream_t stream, bool pdl) {
-    const void* k = (const void*)cluster_kernel<T, kTwoShot>;
-    static bool configured[3] = {false, false, false};
-    const int idx = sizeof(T) == 4 ? 0 : sizeof(T) == 2 ? 1 : 2;
-    if (!configured[idx]) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        configured[idx] = true;
+// Persistent, double-buffered two-shot (the pages' "a receive is the credit
+// for the next send", Sec. IV, restated with mbarriers).  Cluster c handles
+// slices c, c + G, c + 2G, ... (G clusters in the grid, p.nsteps slices in
+// all); slice k of a cluster uses stage buffer b = k & 1.  Per buffer, each
+// CTA has a "full" mbarrier (completed by the N-1 incoming partitions'
+// bytes) and an "empty" mbarrier (N-1 arrivals: one from every receiver of
+// this CTA's pushes, made once that receiver has consumed the buffer).  A
+// sender pushes slice k >= 2 into buffer b only after its own empty[b] has
+// seen every receiver finish slice k - 2.  Each thread loads the next
+// slice's inputs before it waits on the current one, so HBM reads overlap
+// the exchange, the reduction and the stores.
+template <typename T>
+__global__ void __launch_bounds__(256) cluster_pipe_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];  // [2][N][Q] payload vectors
+    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(8) uint64_t empty[2];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = S / N;
+    const uint32_t G = (uint32_t)p.ctas_per_rank;  // clusters in the grid
+    const uint32_t nslices = p.nsteps;
+    const uint32_t nt = blockDim.x;
+    const void* src = p.send[r];
+
+    uint32_t s = cluster_id();
+    uint4 x[kClusterBatch];
+    {
+        const uint32_t base = s * S;
+        const uint32_t npos = min(S, p.nvec - base);
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = threadIdx.x + (uint32_t)j * nt;
+            x[j] = make_uint4(0, 0, 0, 0);
+            if (v < npos) x[j] = load_input<T>(src, base + v, p.count);
+        }
     }
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const uint32_t full0 = smem_u32(&full[0]);    // full[b] at full0 + 8 b
+    const uint32_t empty0 = smem_u32(&empty[0]);  // empty[b] at empty0 + 8 b
+    if (threadIdx.x == 0) {
+        mbar_init(full0, 1u);
+        mbar_init(full0 + 8u, 1u);
+        mbar_init(empty0, N - 1);
+        mbar_init(empty0 + 8u, N - 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    cluster_sync();  // every peer's barriers exist before anyone uses them
+
+    Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+#pragma unroll 1
+    for (uint32_t k = 0; s < nslices; s += G, ++k) {
+        const uint32_t b = k & 1u;
+        const uint32_t base = s * S;
+        const uint32_t npos = min(S, p.nvec - base);
+        const uint32_t mine = npos > r * Q ? min(Q, npos - r * Q) : 0u;
+        uint4* const buf = stage + b * N * Q;
+        const uint32_t full_b = full0 + 8u * b;
+        const uint32_t empty_b = empty0 + 8u * b;
+        w.step = (int)k;
+        if (threadIdx.x == 0) mbar_expect_tx(full_b, (N - 1) * mine * (uint32_t)kVecBytes);
+        // credit: every receiver has consumed this buffer's previous slice
+        if (k >= 2) {
+            const bool ok = mbar_wait_bounded(empty_b, ((k - 2) >> 1) & 1u, w);
+            if (!__syncthreads_and(ok)) break;
+        }
+        // push: partition q of my slice into slot [r] of CTA q's buffer b
+        const uint32_t slot_r = smem_u32(buf + r * Q);
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = threadIdx.x + (uint32_t)j * nt;
+            if (v >= npos) continue;
+            const uint32_t q = v / Q;
+            const uint32_t u = v - q * Q;
+            if (q == r) {
+                buf[r * Q + u] = x[j];
+            } else if (drop != (int32_t)r) {
+                st_async_v4(map_to_rank(slot_r + u * (uint32_t)kVecBytes, q), x[j], map_to_rank(full_b, q));
+            }
+        }
+        // next slice's inputs, in flight during the wait, reduction and stores
+        const uint32_t s_next = s + G;
+        if (s_next < nslices) {
+            const uint32_t nbase = s_next * S;
+            const uint32_t nnpos = min(S, p.nvec - nbase);
+#pragma unroll
+            for (int j = 0; j < kClusterBatch; ++j) {
+                const uint32_t v = threadIdx.x + (uint32_t)j * nt;
+                if (v < nnpos) x[j] = load_input<T>(src, nbase + v, p.count);
+            }
+        }
+        {
+            const bool ok = mbar_wait_bounded(full_b, (k >> 1) & 1u, w);
+            if (!__syncthreads_and(ok)) break;  // also makes my own slot visible
+        }
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            typename M::Acc acc = M::load(buf[u]);
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, buf[q * Q + u]);
+            const uint4 out = M::store(acc);
+            const uint32_t pos = base + r * Q + u;
+#pragma unroll 1
+            for (uint32_t d0 = 0; d0 < N; ++d0) {
+                const uint32_t d = r + d0 < N ? r + d0 : r + d0 - N;
+                store_output<T>(p.recv[d], pos, p.count, out);
+            }
+        }
+        __syncthreads();  // every read of buffer b is done
+        if (threadIdx.x == 0 && s + 2 * G < nslices) {
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) {
+                const uint32_t peer = r + q < N ? r + q : r + q - N;
+                mbar_arrive_remote(map_to_rank(empty_b, peer));
+            }
+        }
+    }
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
+template <typename T>
+static const void* cluster_kernel_for(int mode) {
+    switch (mode) {
+        case kClusterOneshot: return (const void*)cluster_kernel<T, false>;
+        case kClusterTwoshot: return (const void*)cluster_kernel<T, true>;
+        case kClusterTwoshotPipe: return (const void*)cluster_pipe_kernel<T>;
+    }
+    return nullptr;
+}
+
+static const void* cluster_kernel_ptr(rra_dtype_t dtype, int mode) {
+    switch (dtype) {
+        case RRA_FP32: return cluster_kernel_for<float>(mode);
+        case RRA_BF16: return cluster_kernel_for<__nv_bfloat16>(mode);
+        case RRA_FP64: return cluster_kernel_for<double>(mode);
+    }
+    return nullptr;
+}
+
+// Opt the kernel in to the full stage and to clusters of up to 16 CTAs
+// (once per kernel; the attributes are process-wide).
+static cudaError_t configure(const void* k) {
+    static const void* done[16] = {};
+    for (const void* d : done)
+        if (d == k) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    for (const void*& d : done)
+        if (d == nullptr) {
+            d = k;
+            break;
+        }
+    return cudaSuccess;
+}
+
+size_t cluster_stage_bytes(const Params& p, int mode) {
+    const size_t n = (size_t)p.nranks;
+    switch (mode) {
+        case kClusterOneshot: return n * p.per_cta * kVecBytes;
+        case kClusterTwoshot: return (size_t)p.per_cta / n * n * kVecBytes;
+        case kClusterTwoshotPipe: return 2 * ((size_t)p.per_cta / n * n) * kVecBytes;
+    }
+    return 0;
+}
+
+cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl) {
+    const size_t smem = cluster_stage_bytes(p, mode);
+    if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks)
+        return cudaErrorInvalidValue;
+    if (mode != kClusterOneshot && p.per_cta % (uint32_t)p.nranks != 0) return cudaErrorInvalidValue;
+    if (mode == kClusterTwoshotPipe && p.per_cta > (uint32_t)threads * kClusterBatch) return cudaErrorInvalidValue;
+    const void* k = cluster_kernel_ptr(dtype, mode);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = configure(k);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.nranks * p.ctas_per_rank));
     cfg.blockDim = dim3((unsigned)threads);
@@ -256,52 +469,19 @@ static cudaError_t launch_cluster_t(const Params& p, int threads, size_t smem, c
     return cudaLaunchKernelExC(&cfg, k, args);
 }
 
-template <bool kTwoShot>
-static cudaError_t launch_cluster_kind(const Params& p, rra_dtype_t dtype, int threads, size_t smem,
-                                       cudaStream_t stream, bool pdl) {
-    switch (dtype) {
-        case RRA_FP32: return launch_cluster_t<float, kTwoShot>(p, threads, smem, stream, pdl);
-        case RRA_BF16: return launch_cluster_t<__nv_bfloat16, kTwoShot>(p, threads, smem, stream, pdl);
-        case RRA_FP64: return launch_cluster_t<double, kTwoShot>(p, threads, smem, stream, pdl);
-    }
-    return cudaErrorInvalidValue;
-}
-
-size_t cluster_stage_bytes(const Params& p, bool two_shot) {
-    const size_t q = two_shot ? p.per_cta / (uint32_t)p.nranks : p.per_cta;
-    return (size_t)p.nranks * q * kVecBytes;
-}
-
-cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, bool two_shot, int threads, cudaStream_t stream,
-                           bool pdl) {
-    const size_t smem = cluster_stage_bytes(p, two_shot);
-    if (smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks) return cudaErrorInvalidValue;
-    if (two_shot && p.per_cta % (uint32_t)p.nranks != 0) return cudaErrorInvalidValue;
-    return two_shot ? launch_cluster_kind<true>(p, dtype, threads, smem, stream, pdl)
-                    : launch_cluster_kind<false>(p, dtype, threads, smem, stream, pdl);
-}
-
-// Clusters of `nranks` CTAs with the largest stage that can be resident at
-// once (0 = this cluster shape cannot run on the device).
-int cluster_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads) {
-    const void* k = nullptr;
-    switch (dtype) {
-        case RRA_FP32: k = two_shot ? (const void*)cluster_kernel<float, true> : (const void*)cluster_kernel<float, false>; break;
-        case RRA_BF16:
-            k = two_shot ? (const void*)cluster_kernel<__nv_bfloat16, true> : (const void*)cluster_kernel<__nv_bfloat16, false>;
-            break;
-        case RRA_FP64: k = two_shot ? (const void*)cluster_kernel<double, true> : (const void*)cluster_kernel<double, false>; break;
-    }
-    if (k == nullptr) return 0;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+// Clusters of `nranks` CTAs of this kernel, `threads` threads and `smem`
+// bytes of stage each, that can be resident at once (0 = this cluster shape
+// cannot run on the device).
+int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem) {
+    const void* k = cluster_kernel_ptr(dtype, mode);
+    if (k == nullptr || configure(k) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)nranks);
     cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = kClusterStageBytes;
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = (unsigned)nranks;

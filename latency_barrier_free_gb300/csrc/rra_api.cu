@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "rra.h"
@@ -97,7 +98,9 @@ struct rra_comm {
     int64_t cooperative = 1;                // cooperative launch (co-residency guaranteed)
     int64_t pdl = 1;                        // programmatic dependent launch
     int64_t cluster_slice = 0;              // cluster kernels: bytes per rank per slice, 0 = auto
+    int64_t cluster_pipe = 0;               // persistent cluster two-shot: -1 auto, 0 never (default), 1 always
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
+    std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -336,6 +339,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < 0 || v % 16 || v > (int64_t)rra::kClusterStageBytes) return RRA_ERR_INVALID_ARG;
             c->cluster_slice = v;
             return RRA_OK;
+        case RRA_ATTR_CLUSTER_PIPE:
+            if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->cluster_pipe = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -353,6 +360,7 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_COOPERATIVE: *v = c->cooperative; return RRA_OK;
         case RRA_ATTR_PDL: *v = c->pdl; return RRA_OK;
         case RRA_ATTR_CLUSTER_SLICE: *v = c->cluster_slice; return RRA_OK;
+        case RRA_ATTR_CLUSTER_PIPE: *v = c->cluster_pipe; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -363,13 +371,21 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
 // kClusterBatch loads per thread (GB300 sweep: 16 KiB slices of 128 threads
 // were fastest from 4 MiB up at N = 2..16); at most the 96 KiB stage (N x S
 // vectors for the one-shot, S for the two-shot, whose S is a multiple of N).
+//
+// Two-shot slices that do not fit in one wave of clusters run on the
+// persistent, double-buffered kernel instead: as many clusters as can be
+// resident, each looping over its share of the slices.
 static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo, Params* p,
-                                 int* threads) {
+                                 int* threads, int* mode) {
     const bool two = algo == RRA_TWOSHOT_CLUSTER;
     const size_t n = (size_t)c->nranks;
     if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
     int& fits = c->cluster_fits[two ? 1 : 0][(int)dtype];
-    if (fits < 0) fits = rra::cluster_max_active(dtype, two, c->nranks, 256) > 0 ? 1 : 0;
+    if (fits < 0)
+        fits = rra::cluster_max_active(dtype, two ? rra::kClusterTwoshot : rra::kClusterOneshot, c->nranks, 256,
+                                       rra::kClusterStageBytes) > 0
+                   ? 1
+                   : 0;
     if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
     const size_t ve = rra::kVecBytes / elem_size(dtype);
     memset(p, 0, sizeof(*p));
@@ -399,9 +415,29 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     if (two) S = align_up(S, n);
     S = std::max<size_t>(two ? n : 1, std::min(S, smax));
     p->per_cta = (uint32_t)S;
-    p->ctas_per_rank = (int32_t)ceil_div(p->nvec, S);  // slices = clusters
+    const size_t nslices = ceil_div(p->nvec, S);
+    p->ctas_per_rank = (int32_t)nslices;  // one cluster per slice
     p->epoch_slots = rra::kEpochSlots;
     *threads = (int)std::min<size_t>((size_t)c->threads, std::max<size_t>(32, align_up(S, 32)));
+    *mode = two ? rra::kClusterTwoshot : rra::kClusterOneshot;
+    if (two && c->cluster_pipe != 0 && S <= (size_t)*threads * rra::kClusterBatch &&
+        2 * S * rra::kVecBytes <= rra::kClusterStageBytes) {
+        const size_t smem = 2 * S * rra::kVecBytes;
+        const uint64_t key = ((uint64_t)dtype << 40) | ((uint64_t)*threads << 24) | (uint64_t)smem;
+        auto it = c->cluster_waves.find(key);
+        if (it == c->cluster_waves.end())
+            it = c->cluster_waves
+                     .emplace(key, rra::cluster_max_active(dtype, rra::kClusterTwoshotPipe, c->nranks, *threads, smem))
+                     .first;
+        const size_t wave = (size_t)it->second;
+        if (wave > 0 && (nslices > wave || c->cluster_pipe == 1)) {
+            // RRA_ATTR_CTAS_PER_RANK, when set, caps the number of clusters
+            const size_t g = c->ctas_per_rank > 0 ? std::min(wave, (size_t)c->ctas_per_rank) : wave;
+            *mode = rra::kClusterTwoshotPipe;
+            p->ctas_per_rank = (int32_t)std::min(nslices, g);
+            p->nsteps = (uint32_t)nslices;
+        }
+    }
     return RRA_OK;
 }
 
@@ -572,7 +608,7 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     if (autoselect) rra_select_algo(c->nranks, count * elem_size(dtype), dtype, &algo);
     Params p;
     int kind = 0, threads = 0;
-    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads)
+    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
                                        : plan_call(c, count, dtype, algo, &p, &kind, &threads);
     if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
         algo = select_global(c->nranks, count * elem_size(dtype));
@@ -598,7 +634,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     int kind = 0, threads = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads)
+        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
                                            : plan_call(c, count, dtype, algo, &p, &kind, &threads);
         if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
             algo = select_global(c->nranks, count * es);
@@ -613,8 +649,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
         p.recv[r] = recv[r];
     }
     cudaError_t e = is_cluster(algo)
-                        ? rra::launch_cluster(p, dtype, algo == RRA_TWOSHOT_CLUSTER, threads, (cudaStream_t)stream,
-                                              c->pdl != 0)
+                        ? rra::launch_cluster(p, dtype, kind, threads, (cudaStream_t)stream, c->pdl != 0)
                         : rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0,
                                                 c->pdl != 0);
     if (e == cudaErrorCooperativeLaunchTooLarge) {

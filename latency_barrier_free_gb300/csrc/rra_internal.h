@@ -95,11 +95,13 @@ cudaError_t launch_allreduce(const Params& p, rra_dtype_t dtype, int kind, int t
 cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_sm);
 // One-shot / two-shot through distributed shared memory (cluster.cu): one
 // cluster of N CTAs per slice of p.per_cta vectors (a multiple of N for the
-// two-shot), p.ctas_per_rank slices.
-size_t cluster_stage_bytes(const Params& p, bool two_shot);
-cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, bool two_shot, int threads, cudaStream_t stream,
-                           bool pdl);
-int cluster_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads);
+// two-shot).  kClusterOneshot / kClusterTwoshot: p.ctas_per_rank slices, one
+// cluster each.  kClusterTwoshotPipe: p.ctas_per_rank persistent clusters
+// over p.nsteps slices of at most threads * kClusterBatch vectors.
+enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2 };
+size_t cluster_stage_bytes(const Params& p, int mode);
+cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl);
+int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

@@ -297,12 +297,38 @@ def test_cluster_slice_sizes(algo, threads):
         with rra.Comm(n, count * 4) as comm:
             comm.set_attr("threads", threads)
             for slice_bytes in (16, 16 * n, 4096, 48 << 10, 96 << 10):
-                comm.set_attr("cluster_slice", slice_bytes)
-                grid, _ = comm.plan_call(count, dtype, algo)
-                assert grid % n == 0
-                sends_np = inputs.normal(inputs.rng(72, n, slice_bytes, threads), n, count, dtype)
-                got = run(comm, sends_np, dtype, algo)
-                check_against_oracle(sends_np, got, dtype, algo)
+                for pipe in ((0, 1) if algo == "twoshot_cluster" else (0,)):
+                    comm.set_attr("cluster_slice", slice_bytes)
+                    comm.set_attr("cluster_pipe", pipe)
+                    grid, _ = comm.plan_call(count, dtype, algo)
+                    assert grid % n == 0
+                    sends_np = inputs.normal(inputs.rng(72, n, slice_bytes, threads, pipe), n, count, dtype)
+                    got = run(comm, sends_np, dtype, algo)
+                    check_against_oracle(sends_np, got, dtype, algo)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("clusters", [1, 3, 0])
+def test_cluster_twoshot_pipelined(n, dtype, clusters):
+    """The persistent, double-buffered two-shot: one cluster looping over
+    hundreds of slices (every buffer reused ~100 times, each reuse gated by
+    the receivers' credits), three clusters, and as many as fit; ragged
+    message tails and slices; bit-exact."""
+    with rra.Comm(n, 70001 * ELEM[dtype]) as comm:
+        comm.set_attr("cluster_pipe", 1)
+        comm.set_attr("ctas_per_rank", clusters)
+        comm.set_attr("cluster_slice", 16 * n * 4)
+        for count in (70001, 5, 4097):
+            grid, steps = comm.plan_call(count, dtype, "twoshot_cluster")
+            if clusters:
+                assert grid == n * min(clusters, steps)
+            sends_np = inputs.normal(inputs.rng(73, count, n, clusters), n, count, dtype)
+            got = run(comm, sends_np, dtype, "twoshot_cluster")
+            check_against_oracle(sends_np, got, dtype, "twoshot_cluster")
+        sends_np = inputs.normal(inputs.rng(73, 2, n, clusters), n, 70001, dtype)
+        got = run(comm, sends_np, dtype, "twoshot_cluster", in_place=True)
+        check_against_oracle(sends_np, got, dtype, "twoshot_cluster")
 
 
 @pytest.mark.parametrize("algo", CLUSTER)

@@ -84,6 +84,31 @@ def test_timeout_poison_and_reset(algo):
         check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
 
 
+def test_pipelined_cluster_timeout_and_reset():
+    """The persistent cluster two-shot with a rank that drops its pushes:
+    waits on data and on credits run out, RRA_ERR_TIMEOUT is recorded, and
+    after a reset the same plan gives the oracle's result."""
+    n, count = 4, 40000
+    sends_np = inputs.normal(inputs.rng(74, 0), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cluster_pipe", 1)
+        comm.set_attr("ctas_per_rank", 2)
+        comm.set_attr("cluster_slice", 1024)
+        comm.set_attr("poll_timeout_ms", 20)
+        comm.inject_drop(1)
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, "twoshot_cluster")
+        st, rank, step = comm.status()
+        assert st == rra.ERR_TIMEOUT
+        assert 0 <= rank < n and step in (0, 1)  # the first wait to give up: slice 0 or 1
+        comm.reset()
+        comm.allreduce(sends, recvs, "twoshot_cluster")
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "twoshot_cluster")
+
+
 def test_device_error_makes_later_calls_noops():
     """Calls enqueued after a device-side failure (before the host looks) do
     nothing on the device and do not hang."""
