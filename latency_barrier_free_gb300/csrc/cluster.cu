@@ -145,14 +145,16 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     // before waiting for the previous kernel; its phase completes when the
     // N-1 contributions' bytes have arrived.  The cluster barrier that makes
     // it visible to the peers is split: arrive now, wait just before the
-    // first push, so its latency overlaps the input loads.
+    // first push, so its latency overlaps the input loads.  The arrive is
+    // relaxed: fence.mbarrier_init already orders the initialisation before
+    // it, and a release would stall every thread on a memory barrier.
     const uint32_t my_bar = smem_u32(&bar);
     if (threadIdx.x == 0) {
         mbar_init(my_bar, 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         mbar_expect_tx(my_bar, (N - 1) * mine * (uint32_t)kVecBytes);
     }
-    cluster_arrive();
+    cluster_arrive_relaxed();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
 
