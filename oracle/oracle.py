@@ -60,6 +60,13 @@ def _load():
             lib.rra_oracle_reference_sum.restype = ctypes.c_int
             lib.rra_oracle_f32_to_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
             lib.rra_oracle_f32_to_bf16_array.restype = None
+            for name in ("rra_oracle_reduce_scatter", "rra_oracle_all_gather"):
+                getattr(lib, name).argtypes = [ctypes.c_int, vpp, vpp, ctypes.c_size_t, ctypes.c_int]
+                getattr(lib, name).restype = ctypes.c_int
+            for name in ("rra_oracle_broadcast", "rra_oracle_reduce"):
+                getattr(lib, name).argtypes = [ctypes.c_int, ctypes.c_int, vpp, vpp, ctypes.c_size_t,
+                                               ctypes.c_int]
+                getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -132,3 +139,64 @@ def f32_to_bf16(x) -> np.ndarray:
     out = np.empty(x.shape, dtype=np.uint16)
     lib.rra_oracle_f32_to_bf16_array(x.ctypes.data, out.ctypes.data, x.size)
     return out
+
+
+def _run(fn, *args):
+    if fn(*args) != 0:
+        raise RuntimeError("oracle rejected its arguments")
+
+
+def reduce_scatter(sends, dtype: str):
+    """ReduceScatter-sum: sends[p] holds N*count elements; returns N outputs
+    of count elements, output r = rank-order sum of the inputs' block r."""
+    lib = _load()
+    code, np_dt, total = _check_inputs(sends, dtype)
+    n = len(sends)
+    if total % n:
+        raise ValueError("each input must hold N * count elements")
+    count = total // n
+    recvs = [np.empty(count, dtype=np_dt) for _ in sends]
+    sp, keep_s = _ptrs(sends)
+    rp, keep_r = _ptrs(recvs)
+    _run(lib.rra_oracle_reduce_scatter, n, sp, rp, count, code)
+    del keep_s, keep_r
+    return recvs
+
+
+def all_gather(sends, dtype: str):
+    """AllGather: every output is the concatenation of the N inputs in rank order."""
+    lib = _load()
+    code, np_dt, count = _check_inputs(sends, dtype)
+    n = len(sends)
+    recvs = [np.empty(n * count, dtype=np_dt) for _ in sends]
+    sp, keep_s = _ptrs(sends)
+    rp, keep_r = _ptrs(recvs)
+    _run(lib.rra_oracle_all_gather, n, sp, rp, count, code)
+    del keep_s, keep_r
+    return recvs
+
+
+def broadcast(sends, dtype: str, root: int):
+    """Broadcast: every output is a copy of sends[root]."""
+    lib = _load()
+    code, np_dt, count = _check_inputs(sends, dtype)
+    recvs = [np.empty(count, dtype=np_dt) for _ in sends]
+    sp, keep_s = _ptrs(sends)
+    rp, keep_r = _ptrs(recvs)
+    _run(lib.rra_oracle_broadcast, len(sends), int(root), sp, rp, count, code)
+    del keep_s, keep_r
+    return recvs
+
+
+def reduce(sends, dtype: str, root: int, recvs=None):
+    """Reduce-sum to `root`: recvs[root] = rank-order sum; other outputs are
+    left as passed (fresh zero arrays when recvs is None)."""
+    lib = _load()
+    code, np_dt, count = _check_inputs(sends, dtype)
+    if recvs is None:
+        recvs = [np.zeros(count, dtype=np_dt) for _ in sends]
+    sp, keep_s = _ptrs(sends)
+    rp, keep_r = _ptrs(recvs)
+    _run(lib.rra_oracle_reduce, len(sends), int(root), sp, rp, count, code)
+    del keep_s, keep_r
+    return recvs

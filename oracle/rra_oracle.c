@@ -197,3 +197,77 @@ int rra_oracle_reference_sum(int nranks, const void* const* send, size_t count,
     }
     return 0;
 }
+
+/* ---- the other collectives ------------------------------------------------
+ * "Every Microsecond Matters", Sec. III-A (opening): AllReduce is commonly
+ * built as ReduceScatter followed by AllGather, or Reduce followed by
+ * Broadcast; the review of the paper (summary) adds that the same
+ * barrier-free primitives serve these four collectives.  Their plain
+ * definitions, with the sum taken exactly as in sum_range (rank order, the
+ * same running type and bfloat16 rounding):
+ *
+ *   ReduceScatter  send[p] holds N*count elements, recv[r] count:
+ *                  recv[r][i] = sum_p send[p][r*count + i]
+ *   AllGather      send[p] holds count elements, recv[r] N*count:
+ *                  recv[r][p*count + i] = send[p][i]
+ *   Broadcast      recv[r][i] = send[root][i]            (every r)
+ *   Reduce         recv[root][i] = sum_p send[p][i]      (other outputs untouched)
+ *
+ * All return 0 on success, -1 on a bad argument.  Outputs must not overlap
+ * inputs here (the oracle is not the place to test aliasing). */
+static size_t elem_bytes(int dtype) {
+    return dtype == ORACLE_FP32 ? 4u : dtype == ORACLE_BF16 ? 2u : 8u;
+}
+
+/* Rank-order sum of element i of the N arrays src[p] + off, written to dst. */
+static void sum_one(int nranks, const void* const* src, size_t off, size_t i, void* dst, int dtype) {
+    if (dtype == ORACLE_FP32) {
+        float acc = ((const float*)src[0])[off + i];
+        for (int p = 1; p < nranks; ++p) acc = acc + ((const float*)src[p])[off + i];
+        ((float*)dst)[i] = acc;
+    } else if (dtype == ORACLE_BF16) {
+        float acc = bf16_to_f32(((const uint16_t*)src[0])[off + i]);
+        for (int p = 1; p < nranks; ++p) acc = acc + bf16_to_f32(((const uint16_t*)src[p])[off + i]);
+        ((uint16_t*)dst)[i] = rra_oracle_f32_to_bf16(acc);
+    } else {
+        double acc = ((const double*)src[0])[off + i];
+        for (int p = 1; p < nranks; ++p) acc = acc + ((const double*)src[p])[off + i];
+        ((double*)dst)[i] = acc;
+    }
+}
+
+int rra_oracle_reduce_scatter(int nranks, const void* const* send, void* const* recv,
+                              size_t count, int dtype) {
+    if (nranks < 1 || send == NULL || recv == NULL) return -1;
+    if (dtype < ORACLE_FP32 || dtype > ORACLE_FP64) return -1;
+    for (int r = 0; r < nranks; ++r)
+        for (size_t i = 0; i < count; ++i) sum_one(nranks, send, (size_t)r * count, i, recv[r], dtype);
+    return 0;
+}
+
+int rra_oracle_all_gather(int nranks, const void* const* send, void* const* recv,
+                          size_t count, int dtype) {
+    if (nranks < 1 || send == NULL || recv == NULL) return -1;
+    if (dtype < ORACLE_FP32 || dtype > ORACLE_FP64) return -1;
+    const size_t eb = elem_bytes(dtype);
+    for (int r = 0; r < nranks; ++r)
+        for (int p = 0; p < nranks; ++p)
+            memcpy((char*)recv[r] + (size_t)p * count * eb, send[p], count * eb);
+    return 0;
+}
+
+int rra_oracle_broadcast(int nranks, int root, const void* const* send, void* const* recv,
+                         size_t count, int dtype) {
+    if (nranks < 1 || root < 0 || root >= nranks || send == NULL || recv == NULL) return -1;
+    if (dtype < ORACLE_FP32 || dtype > ORACLE_FP64) return -1;
+    for (int r = 0; r < nranks; ++r) memcpy(recv[r], send[root], count * elem_bytes(dtype));
+    return 0;
+}
+
+int rra_oracle_reduce(int nranks, int root, const void* const* send, void* const* recv,
+                      size_t count, int dtype) {
+    if (nranks < 1 || root < 0 || root >= nranks || send == NULL || recv == NULL) return -1;
+    if (dtype < ORACLE_FP32 || dtype > ORACLE_FP64) return -1;
+    for (size_t i = 0; i < count; ++i) sum_one(nranks, send, 0, i, recv[root], dtype);
+    return 0;
+}

@@ -230,3 +230,99 @@ def test_empty_and_ragged():
     assert [o.size for o in oracle.allreduce([np.zeros(0, np.float32)] * 3, "fp32")] == [0, 0, 0]
     with pytest.raises(ValueError):
         oracle.allreduce([np.zeros(3, np.float32), np.zeros(4, np.float32)], "fp32")
+
+
+# ------------------------------------------------ the other collectives ----
+# Definitions (paper text, Sec. III-A opening; review summary): ReduceScatter
+# leaves block r of the rank-order sum in rank r; AllGather concatenates the
+# inputs in rank order; Broadcast copies the root's input; Reduce leaves the
+# sum in the root only.
+def _blocked(n, count, dtype):
+    """send[p][r*count + i] = 32 r + 4 p + (i mod 4): integers up to 255, exact
+    in bfloat16 too, so every binary32 sum below is exact, and a swapped
+    block/rank index changes the result (N <= 8)."""
+    np_dt = oracle.DTYPES[dtype][1]
+    i = np.arange(count)
+    out = []
+    for p in range(n):
+        v = np.concatenate([32.0 * r + 4.0 * p + (i % 4) for r in range(n)])
+        out.append(oracle.f32_to_bf16(v) if dtype == "bf16" else v.astype(np_dt))
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [1, 2, 3, 8])
+def test_reduce_scatter_closed_form(n, dtype):
+    count = 11
+    outs = oracle.reduce_scatter(_blocked(n, count, dtype), dtype)
+    i = np.arange(count)
+    for r in range(n):
+        expect = n * 32.0 * r + 4.0 * n * (n - 1) / 2 + n * (i % 4)
+        got = _as_f32(outs[r]) if dtype == "bf16" else outs[r]
+        if dtype == "bf16":  # one rounding of the exact integer to 8 significant bits
+            expect = np.array([_int_round_to_sig_bits(int(e), 8) for e in expect], dtype=np.float64)
+        assert np.array_equal(got.astype(np.float64), expect), r
+
+
+def test_reduce_scatter_rank_order():
+    # block 1 of three ranks holds 2^24, 1, 1: adding in rank order gives 2^24
+    # (each +1 is a tie that rounds to even), the reverse order 2^24 + 2.
+    big = np.float32(2.0 ** 24)
+    sends = [np.array([0, big], np.float32), np.array([0, 1], np.float32), np.array([0, 1], np.float32)]
+    sends = [np.concatenate([s, s, s])[:6] for s in sends]  # N*count = 6, count = 2
+    outs = oracle.reduce_scatter(sends, "fp32")
+    assert outs[0][1] == big  # rank order; the reverse order would give 2^24 + 2
+    rev = oracle.reduce_scatter(sends[::-1], "fp32")
+    assert rev[0][1] == big + 2
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [1, 2, 5])
+def test_all_gather_layout(n, dtype):
+    count = 9
+    np_dt = oracle.DTYPES[dtype][1]
+    sends = [(100 * p + np.arange(count)).astype(np_dt) for p in range(n)]
+    outs = oracle.all_gather(sends, dtype)
+    k = np.arange(n * count)
+    for r in range(n):
+        assert np.array_equal(outs[r], (100 * (k // count) + k % count).astype(np_dt))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+def test_broadcast_copies_root_only(dtype):
+    n, count = 4, 13
+    np_dt = oracle.DTYPES[dtype][1]
+    sends = [(1000 * p + np.arange(count)).astype(np_dt) for p in range(n)]
+    for root in range(n):
+        outs = oracle.broadcast(sends, dtype, root)
+        for r in range(n):
+            assert np.array_equal(outs[r], (1000 * root + np.arange(count)).astype(np_dt))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp64"])
+def test_reduce_to_root_leaves_others(dtype):
+    n, count = 6, 17
+    np_dt = oracle.DTYPES[dtype][1]
+    sends = inputs.rank_plus_one(n, count, dtype)
+    for root in (0, 3, 5):
+        recvs = [np.full(count, -7, dtype=np_dt) for _ in range(n)]
+        oracle.reduce(sends, dtype, root, recvs)
+        for r in range(n):
+            expect = n * (n + 1) // 2 if r == root else -7
+            assert np.all(recvs[r] == expect)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+def test_allgather_of_reducescatter_is_allreduce(dtype):
+    # Element by element both sides are the same rank-order sum, so the
+    # identity holds bit for bit; an index slip in either function breaks it.
+    # The AllReduce side is pinned by the tests above.
+    n, count = 5, 23
+    g = inputs.rng(90, 0)
+    sends = inputs.normal(g, n, n * count, dtype)
+    ag = oracle.all_gather(oracle.reduce_scatter(sends, dtype), dtype)
+    ar = oracle.allreduce(sends, dtype)
+    for r in range(n):
+        assert np.array_equal(ag[r].view(np.uint8), ar[r].view(np.uint8))
+    red = oracle.reduce(sends, dtype, 2)
+    assert np.array_equal(red[2].view(np.uint8), ar[0].view(np.uint8))
