@@ -141,7 +141,7 @@ def measured_peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("kernels.cu", "cluster.cu", "prims.cuh", "rra_internal.h"):
+    for f in ("kernels.cu", "cluster.cu", "coll.cu", "prims.cuh", "cluster_prims.cuh", "rra_internal.h"):
         h.update(open(os.path.join(ROOT, "latency_barrier_free_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

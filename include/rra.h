@@ -216,6 +216,54 @@ rra_status_t rra_allreduce_host(rra_comm_t comm, const void* const send[], void*
                                 size_t count, rra_dtype_t dtype, rra_algo_t algo,
                                 rra_stream_t stream);
 
+/*
+ * The other collectives.  The paper text (Sec. III-A, opening) notes that
+ * AllReduce is commonly built from ReduceScatter + AllGather or from
+ * Reduce + Broadcast; its review (summary) adds that the same barrier-free
+ * primitives serve these four.  Here all four run one thread-block cluster
+ * of nranks CTAs per slice, CTA r acting for rank r, and exchange data
+ * through distributed shared memory: a push is an st.async into a peer's
+ * shared memory that completes the peer's mbarrier, and the only wait is a
+ * bounded wait on one's own mbarrier (data arrival is the signal).  Nothing
+ * persists between calls.
+ *
+ * Common rules: nranks <= 16 (RRA_ERR_INVALID_ARG above that; the cluster
+ * limit).  send/recv are host arrays of nranks device pointers, each 16-byte
+ * aligned where it is used.  count == 0 returns RRA_OK without a launch.
+ * Sums add the ranks in order 0..nranks-1 with a binary32 running value for
+ * binary32 and bfloat16 (rounded to nearest-even once) and binary64 for
+ * binary64, exactly like the fixed-order AllReduce kernels.  Errors: as
+ * rra_allreduce (RRA_ERR_NOT_CORESIDENT if the device cannot schedule a
+ * cluster of nranks CTAs with a 96 KiB stage each).
+ *
+ * rra_reduce_scatter: send[r] holds nranks * count elements (block q =
+ *   elements [q * count, (q + 1) * count)); recv[r] receives count elements,
+ *   the sum over ranks of block r.  nranks * count * element size must not
+ *   exceed max_bytes.  recv[r] may be send[r] + r * count (in place, when
+ *   that address is 16-byte aligned); buffers must not overlap otherwise.
+ */
+rra_status_t rra_reduce_scatter(rra_comm_t comm, const void* const send[], void* const recv[],
+                                size_t count, rra_dtype_t dtype, rra_stream_t stream);
+
+/* rra_all_gather: send[r] holds count elements; recv[r] receives
+ * nranks * count elements, block p being a copy of send[p].
+ * nranks * count * element size must not exceed max_bytes.  send[r] may be
+ * recv[r] + r * count (in place, when 16-byte aligned). */
+rra_status_t rra_all_gather(rra_comm_t comm, const void* const send[], void* const recv[],
+                            size_t count, rra_dtype_t dtype, rra_stream_t stream);
+
+/* rra_broadcast: every recv[r] (count elements) receives a copy of
+ * send[root].  Only send[root] is read; the other send entries may be NULL.
+ * recv[root] may equal send[root].  0 <= root < nranks. */
+rra_status_t rra_broadcast(rra_comm_t comm, int root, const void* const send[], void* const recv[],
+                           size_t count, rra_dtype_t dtype, rra_stream_t stream);
+
+/* rra_reduce: recv[root] receives the sum over ranks of send[r] (count
+ * elements each).  Only recv[root] is written; the other recv entries may
+ * be NULL.  recv[root] may equal send[root].  0 <= root < nranks. */
+rra_status_t rra_reduce(rra_comm_t comm, int root, const void* const send[], void* const recv[],
+                        size_t count, rra_dtype_t dtype, rra_stream_t stream);
+
 /* Synchronise the device and return the device status word: RRA_OK, or the
  * first device-side error (e.g. RRA_ERR_TIMEOUT).  A device error poisons the
  * communicator until rra_comm_reset().  If `rank`/`step` are non-NULL they

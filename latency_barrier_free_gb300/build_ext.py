@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librra.so")
 
-SOURCES = ["kernels.cu", "cluster.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
-HEADERS = ["prims.cuh", "rra_internal.h"]
+SOURCES = ["kernels.cu", "cluster.cu", "coll.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
+HEADERS = ["prims.cuh", "cluster_prims.cuh", "rra_internal.h"]
 PUBLIC_HEADERS = ["rra.h", "rra_probe.h", "rra_static.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,323 @@
+// coll.cu -- ReduceScatter, AllGather, Broadcast and Reduce through
+// distributed shared memory.
+//
+// "Every Microsecond Matters", Sec. III-A (opening): AllReduce is commonly
+// built from ReduceScatter + AllGather or Reduce + Broadcast; the paper's
+// review (summary) notes that the same barrier-free primitives serve these
+// collectives.  Here they use the primitives of the cluster AllReduce
+// (cluster.cu): one thread-block cluster of N CTAs per slice, CTA r = rank r,
+// a push is an st.async into a peer's shared memory that completes the
+// peer's mbarrier, and the only wait is a bounded wait on one's own mbarrier
+// (data arrival is the signal, Sec. IV).  A CTA reads only its own rank's
+// input and writes only its own rank's output.
+//
+// Layout (v = 16-byte vector, S = slice of p.per_cta vectors, nv = p.nvec
+// vectors per block of `count` elements):
+//   ReduceScatter  send[r] = N blocks of count; CTA r pushes block q's slice
+//                  to CTA q's slot [r]; CTA q adds the N slots in rank order
+//                  into recv[q].
+//   AllGather      CTA r pushes its slice to slot [r] of every peer; CTA r
+//                  writes slot p into block p of recv[r], for every p.
+//   Broadcast      the root CTA pushes its slice to slot [0] of every peer
+//                  and writes its own output from registers.
+//   Reduce         every CTA but the root's pushes its slice to the root's
+//                  slot [r]; the root adds in rank order into recv[root].
+// Blocks start at element q * count, which is not 16-byte aligned when count
+// is not a multiple of the elements per vector; such vectors are moved
+// element by element.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "cluster_prims.cuh"
+#include "prims.cuh"
+#include "rra_internal.h"
+
+namespace rra {
+namespace {
+
+template <typename T>
+struct Bits;
+template <>
+struct Bits<__nv_bfloat16> { using U = uint16_t; };
+template <>
+struct Bits<float> { using U = uint32_t; };
+template <>
+struct Bits<double> { using U = uint64_t; };
+
+// Vector u of a block of `count` elements that starts at element `elem0` of
+// `base`; elements past the block's end read as zero.
+template <typename T>
+__device__ __forceinline__ uint4 load_block(const void* base, uint64_t elem0, uint32_t u, uint64_t count) {
+    constexpr int VE = VecMath<T>::kElems;
+    using U = typename Bits<T>::U;
+    const uint64_t e = (uint64_t)u * VE;
+    const uint64_t first = elem0 + e;
+    if (e + VE <= count && first % VE == 0) return ld_input_v4((const T*)base + first);
+    union {
+        uint4 v;
+        U x[VE];
+    } w;
+    w.v = make_uint4(0u, 0u, 0u, 0u);
+    const int n = (int)min((uint64_t)VE, count - e);
+    const U* s = (const U*)base + first;
+    for (int i = 0; i < n; ++i) w.x[i] = s[i];
+    return w.v;
+}
+
+// Store vector u of such a block; only elements inside the block are written.
+template <typename T>
+__device__ __forceinline__ void store_block(void* base, uint64_t elem0, uint32_t u, uint64_t count, uint4 v) {
+    constexpr int VE = VecMath<T>::kElems;
+    using U = typename Bits<T>::U;
+    const uint64_t e = (uint64_t)u * VE;
+    const uint64_t first = elem0 + e;
+    if (e + VE <= count && first % VE == 0) {
+        st_output_v4((T*)base + first, v);
+        return;
+    }
+    union {
+        uint4 v;
+        U x[VE];
+    } w;
+    w.v = v;
+    const int n = (int)min((uint64_t)VE, count - e);
+    U* d = (U*)base + first;
+    for (int i = 0; i < n; ++i) d[i] = w.x[i];
+}
+
+}  // namespace
+
+template <typename T, int kOp>
+__global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];  // [slots][S]
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint32_t root = (uint32_t)p.root;
+    const uint64_t count = p.count;
+    const bool is_root = r == root;
+
+    // bytes this CTA receives, and input vectors it reads
+    uint32_t incoming = 0, items = 0;
+    switch (kOp) {
+        case kCollReduceScatter: incoming = (N - 1) * npos; items = N * npos; break;
+        case kCollAllGather: incoming = (N - 1) * npos; items = npos; break;
+        case kCollBroadcast: incoming = is_root ? 0u : npos; items = is_root ? npos : 0u; break;
+        case kCollReduce: incoming = is_root ? (N - 1) * npos : 0u; items = npos; break;
+    }
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, incoming * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const void* src = p.send[r];
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const bool pushes = drop != (int32_t)r;
+
+    // input item v: block q = v / npos (ReduceScatter; else 0), vector u
+    uint4 x[kClusterBatch];
+    auto load_batch = [&](uint32_t b0) {
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = b0 + threadIdx.x + (uint32_t)j * nt;
+            if (v >= items) continue;
+            const uint32_t q = kOp == kCollReduceScatter ? v / npos : 0u;
+            const uint32_t u = v - q * npos;
+            x[j] = load_block<T>(src, (uint64_t)q * count, base + u, count);
+        }
+    };
+    load_batch(0);
+    cluster_wait();  // every peer's barrier exists before anyone stores into it
+
+    const uint32_t step = nt * (uint32_t)kClusterBatch;
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < items; b0 += step) {
+        if (b0 != 0) load_batch(b0);
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = b0 + threadIdx.x + (uint32_t)j * nt;
+            if (v >= items) continue;
+            if (kOp == kCollReduceScatter) {
+                const uint32_t q = v / npos;
+                const uint32_t u = v - q * npos;
+                if (q == r) stage[r * S + u] = x[j];
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(stage + r * S + u), q), x[j], map_to_rank(my_bar, q));
+            } else if (kOp == kCollAllGather) {
+                stage[r * S + v] = x[j];
+                if (pushes) {
+#pragma unroll 1
+                    for (uint32_t k = 1; k < N; ++k) {
+                        const uint32_t q = r + k < N ? r + k : r + k - N;
+                        st_async_v4(map_to_rank(smem_u32(stage + r * S + v), q), x[j], map_to_rank(my_bar, q));
+                    }
+                }
+            } else if (kOp == kCollBroadcast) {  // root only
+                if (pushes) {
+#pragma unroll 1
+                    for (uint32_t k = 1; k < N; ++k) {
+                        const uint32_t q = r + k < N ? r + k : r + k - N;
+                        st_async_v4(map_to_rank(smem_u32(stage + v), q), x[j], map_to_rank(my_bar, q));
+                    }
+                }
+                store_block<T>(p.recv[r], 0, base + v, count, x[j]);
+            } else {  // Reduce
+                if (is_root) stage[r * S + v] = x[j];
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(stage + r * S + v), root), x[j], map_to_rank(my_bar, root));
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
+
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    __syncthreads();  // own slot written by other threads of this CTA
+    if (ok) {
+        if (kOp == kCollReduceScatter || (kOp == kCollReduce && is_root)) {
+#pragma unroll 1
+            for (uint32_t u = threadIdx.x; u < npos; u += nt) {
+                typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+                for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * S + u]);
+                store_block<T>(p.recv[r], 0, base + u, count, M::store(acc));
+            }
+        } else if (kOp == kCollAllGather) {
+#pragma unroll 1
+            for (uint32_t v = threadIdx.x; v < N * npos; v += nt) {
+                const uint32_t q = v / npos;
+                const uint32_t u = v - q * npos;
+                store_block<T>(p.recv[r], (uint64_t)q * count, base + u, count, stage[q * S + u]);
+            }
+        } else if (kOp == kCollBroadcast && !is_root) {
+#pragma unroll 1
+            for (uint32_t u = threadIdx.x; u < npos; u += nt) store_block<T>(p.recv[r], 0, base + u, count, stage[u]);
+        }
+    }
+    cluster_wait();  // every peer has issued its pushes into this CTA's shared memory
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
+template <typename T>
+static const void* coll_kernel_for(int op) {
+    switch (op) {
+        case kCollReduceScatter: return (const void*)coll_kernel<T, kCollReduceScatter>;
+        case kCollAllGather: return (const void*)coll_kernel<T, kCollAllGather>;
+        case kCollBroadcast: return (const void*)coll_kernel<T, kCollBroadcast>;
+        case kCollReduce: return (const void*)coll_kernel<T, kCollReduce>;
+    }
+    return nullptr;
+}
+
+static const void* coll_kernel_ptr(rra_dtype_t dtype, int op) {
+    switch (dtype) {
+        case RRA_FP32: return coll_kernel_for<float>(op);
+        case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op);
+        case RRA_FP64: return coll_kernel_for<double>(op);
+    }
+    return nullptr;
+}
+
+// Opt a kernel in to the full stage and to clusters of up to 16 CTAs (once
+// per kernel; the attributes are process-wide).
+static cudaError_t configure_coll(const void* k) {
+    static const void* done[12] = {};
+    for (const void* d : done)
+        if (d == k) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    for (const void*& d : done)
+        if (d == nullptr) {
+            d = k;
+            break;
+        }
+    return cudaSuccess;
+}
+
+size_t coll_stage_bytes(const Params& p, int op) {
+    const size_t slots = op == kCollBroadcast ? 1 : (size_t)p.nranks;
+    return slots * p.per_cta * kVecBytes;
+}
+
+cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl) {
+    const size_t smem = coll_stage_bytes(p, op);
+    if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks ||
+        p.root < 0 || p.root >= p.nranks)
+        return cudaErrorInvalidValue;
+    const void* k = coll_kernel_ptr(dtype, op);
+    if (k == nullptr) return cudaErrorInvalidValue;
+    cudaError_t e = configure_coll(k);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.nranks * p.ctas_per_rank));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)p.nranks;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    void* args[] = {(void*)&p};
+    return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem) {
+    const void* k = coll_kernel_ptr(dtype, op);
+    if (k == nullptr || configure_coll(k) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nranks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)nranks;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace rra

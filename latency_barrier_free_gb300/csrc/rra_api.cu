@@ -101,6 +101,7 @@ struct rra_comm {
     int64_t cluster_pipe = 0;               // persistent cluster two-shot: -1 auto, 0 never (default), 1 always
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
+    int coll_fits[4][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -441,6 +442,51 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     return RRA_OK;
 }
 
+// Plan of a ReduceScatter / AllGather / Broadcast / Reduce call: one cluster
+// of N CTAs per slice of S vectors of a block of `count` elements; S as for
+// the cluster AllReduce (one vector per thread while small, then about two
+// CTAs per SM), with at most one batch of kClusterBatch input vectors per
+// thread and the 96 KiB stage (N slots of S vectors; one slot for Broadcast).
+static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int op, int root, Params* p,
+                              int* threads) {
+    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    int& fits = c->coll_fits[op][(int)dtype];
+    if (fits < 0) fits = rra::coll_max_active(dtype, op, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
+    if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
+    const size_t n = (size_t)c->nranks;
+    const size_t ve = rra::kVecBytes / elem_size(dtype);
+    memset(p, 0, sizeof(*p));
+    p->win0 = c->win0;
+    p->ctrl = c->ctrl;
+    p->timing = c->timing;
+    p->stride = c->lay.window_stride;
+    p->count = count;
+    p->nvec = (uint32_t)ceil_div(count, ve);
+    p->timeout_ns = (uint64_t)c->timeout_ms * 1000000ull;
+    p->nranks = c->nranks;
+    p->nsteps = 1;
+    p->chunk_vecs = p->nvec;
+    p->epoch_slots = rra::kEpochSlots;
+    p->root = root;
+    const size_t slots = op == rra::kCollBroadcast ? 1 : n;
+    const size_t per_pos = op == rra::kCollReduceScatter ? n : 1;  // input vectors per slice position
+    const size_t smax = rra::kClusterStageBytes / rra::kVecBytes / slots;
+    const size_t t = (size_t)c->threads;
+    size_t S;
+    if (c->cluster_slice > 0) {
+        S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else {
+        const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / n);
+        S = std::max<size_t>(std::min<size_t>(p->nvec, std::max<size_t>(1, t / per_pos)), ceil_div(p->nvec, target));
+        S = std::min<size_t>(S, std::max<size_t>(1, t * rra::kClusterBatch / per_pos));
+    }
+    S = std::max<size_t>(1, std::min(S, smax));
+    p->per_cta = (uint32_t)S;
+    p->ctas_per_rank = (int32_t)ceil_div(p->nvec, S);
+    *threads = (int)std::min<size_t>(t, std::max<size_t>(32, align_up(S * per_pos, 32)));
+    return RRA_OK;
+}
+
 static int kernel_kind(const rra_comm* c, rra_algo_t algo) {
     if (algo == RRA_ONESHOT_LL || algo == RRA_ONESHOT_SENTINEL) {
         const bool wide = c->oneshot_wide == 1 || (c->oneshot_wide < 0 && c->nranks >= 16);
@@ -712,6 +758,64 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
         return (rra_status_t)*c->host_status;
     }
     return RRA_OK;
+}
+
+// Shared front end of the four collectives.  ReduceScatter's inputs and
+// AllGather's outputs hold nranks blocks of `count` elements; those must fit
+// max_bytes.  Broadcast reads only send[root]; Reduce writes only recv[root].
+static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const send[], void* const recv[],
+                             size_t count, rra_dtype_t dtype, rra_stream_t stream) {
+    if (c == nullptr || send == nullptr || recv == nullptr || !valid_dtype(dtype)) return RRA_ERR_INVALID_ARG;
+    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    if ((op == rra::kCollBroadcast || op == rra::kCollReduce) && (root < 0 || root >= c->nranks))
+        return RRA_ERR_INVALID_ARG;
+    if (c->poisoned) return RRA_ERR_POISONED;
+    if (count == 0) return RRA_OK;
+    const size_t es = elem_size(dtype);
+    const size_t blocks = (op == rra::kCollReduceScatter || op == rra::kCollAllGather) ? (size_t)c->nranks : 1;
+    if (count > c->max_bytes / es / blocks) return RRA_ERR_INVALID_ARG;
+    Params p;
+    int threads = 0;
+    {
+        std::lock_guard<std::mutex> g(c->mu);
+        rra_status_t st = plan_coll(c, count, dtype, op, root < 0 ? 0 : root, &p, &threads);
+        if (st != RRA_OK) return st;
+    }
+    for (int r = 0; r < c->nranks; ++r) {
+        const bool need_send = op != rra::kCollBroadcast || r == root;
+        const bool need_recv = op != rra::kCollReduce || r == root;
+        if ((need_send && send[r] == nullptr) || (need_recv && recv[r] == nullptr)) return RRA_ERR_INVALID_ARG;
+        if (((uintptr_t)(need_send ? send[r] : nullptr) | (uintptr_t)(need_recv ? recv[r] : nullptr)) & 15u)
+            return RRA_ERR_INVALID_ARG;
+        p.send[r] = need_send ? send[r] : nullptr;
+        p.recv[r] = need_recv ? recv[r] : nullptr;
+    }
+    cudaError_t e = rra::launch_coll(p, dtype, op, threads, (cudaStream_t)stream, c->pdl != 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RRA_ERR_CUDA;
+    }
+    return RRA_OK;
+}
+
+rra_status_t rra_reduce_scatter(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                                rra_dtype_t dtype, rra_stream_t stream) {
+    return run_coll(c, rra::kCollReduceScatter, -1, send, recv, count, dtype, stream);
+}
+
+rra_status_t rra_all_gather(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                            rra_dtype_t dtype, rra_stream_t stream) {
+    return run_coll(c, rra::kCollAllGather, -1, send, recv, count, dtype, stream);
+}
+
+rra_status_t rra_broadcast(rra_comm_t c, int root, const void* const send[], void* const recv[], size_t count,
+                           rra_dtype_t dtype, rra_stream_t stream) {
+    return run_coll(c, rra::kCollBroadcast, root, send, recv, count, dtype, stream);
+}
+
+rra_status_t rra_reduce(rra_comm_t c, int root, const void* const send[], void* const recv[], size_t count,
+                        rra_dtype_t dtype, rra_stream_t stream) {
+    return run_coll(c, rra::kCollReduce, root, send, recv, count, dtype, stream);
 }
 
 rra_status_t rra_comm_status(rra_comm_t c, int* rank, int* step) {

@@ -66,6 +66,7 @@ struct Params {
     int32_t nranks;
     int32_t ctas_per_rank;
     int32_t epoch_slots;   // number of epoch slots to keep equal
+    int32_t root;          // Broadcast / Reduce: the root rank
 };
 
 // Kernel kinds: the four algorithms (same values as rra_algo_t) plus the
@@ -102,6 +103,13 @@ enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2 };
 size_t cluster_stage_bytes(const Params& p, int mode);
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl);
 int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem);
+// ReduceScatter, AllGather, Broadcast, Reduce through distributed shared
+// memory (coll.cu): one cluster of N CTAs per slice of p.per_cta vectors of
+// a block of p.count elements (p.nvec vectors), p.ctas_per_rank slices.
+enum { kCollReduceScatter = 0, kCollAllGather = 1, kCollBroadcast = 2, kCollReduce = 3 };
+size_t coll_stage_bytes(const Params& p, int op);
+cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl);
+int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

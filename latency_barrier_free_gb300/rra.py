@@ -42,7 +42,11 @@ SYMBOLS = [
     "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_launch_shape",
     "rra_probe_sm_count",
     "rra_allreduce_static",
+    "rra_reduce_scatter", "rra_all_gather", "rra_broadcast", "rra_reduce",
 ]
+
+# The collectives besides AllReduce (all through distributed shared memory, N <= 16).
+COLLECTIVES = ("reduce_scatter", "all_gather", "broadcast", "reduce")
 
 
 class Layout(ctypes.Structure):
@@ -106,6 +110,10 @@ def load(path: str = LIB_PATH):
             "rra_probe_empty_kernel": ([vp], i32),
             "rra_probe_sm_count": ([ip], i32),
             "rra_probe_launch_shape": ([i32, i32, i32, i32, vp], i32),
+            "rra_reduce_scatter": ([vp, pp, pp, sz, i32, vp], i32),
+            "rra_all_gather": ([vp, pp, pp, sz, i32, vp], i32),
+            "rra_broadcast": ([vp, i32, pp, pp, sz, i32, vp], i32),
+            "rra_reduce": ([vp, i32, pp, pp, sz, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -232,6 +240,69 @@ class Comm:
                 raise ValueError("all tensors must be contiguous CUDA tensors of one dtype and size")
         dname = {0: "fp32", 1: "bf16", 2: "fp64"}[dt]
         self.allreduce_ptrs([t.data_ptr() for t in sends], [t.data_ptr() for t in recvs], n, dname, algo, stream)
+
+    # -- the other collectives ----------------------------------------------
+    def _coll_args(self, op, send_ptrs, recv_ptrs, count, dtype, root, stream):
+        if op not in COLLECTIVES:
+            raise ValueError("collective must be one of %s" % (COLLECTIVES,))
+        sp, ks = _ptr_array(send_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        fn = getattr(self._lib, "rra_" + op)
+        tail = (ctypes.c_size_t(int(count)), ctypes.c_int(DTYPES[dtype]), _stream_handle(stream))
+        if op in ("broadcast", "reduce"):
+            args = (self._h, ctypes.c_int(int(root)), sp, rp) + tail
+        else:
+            args = (self._h, sp, rp) + tail
+        return fn, args, (ks, kr)
+
+    def collective_ptrs(self, op: str, send_ptrs, recv_ptrs, count: int, dtype: str, root: int = 0,
+                        stream=None) -> None:
+        """One ReduceScatter / AllGather / Broadcast / Reduce on raw device
+        pointers (None where the collective ignores an entry)."""
+        fn, args, keep = self._coll_args(op, send_ptrs, recv_ptrs, count, dtype, root, stream)
+        st = fn(*args)
+        del keep
+        _check(st, "rra_" + op)
+
+    def prepare_collective(self, op: str, send_ptrs, recv_ptrs, count: int, dtype: str, root: int = 0,
+                           stream=None):
+        """As prepare(), for one of the other collectives."""
+        fn, args, keep = self._coll_args(op, send_ptrs, recv_ptrs, count, dtype, root, stream)
+
+        def call(_keep=keep):
+            st = fn(*args)
+            if st != OK:
+                raise RraError(st, "rra_" + op)
+        return call
+
+    def _tensor_call(self, op, sends, recvs, count, root, stream):
+        if len(sends) != self.nranks or len(recvs) != self.nranks:
+            raise ValueError("need one send and one recv entry per rank (None where unused)")
+        ts = [t for t in list(sends) + list(recvs) if t is not None]
+        dt = _dtype_of(ts[0])
+        for t in ts:
+            if not t.is_cuda or not t.is_contiguous() or _dtype_of(t) != dt:
+                raise ValueError("all tensors must be contiguous CUDA tensors of one dtype")
+        dname = {0: "fp32", 1: "bf16", 2: "fp64"}[dt]
+        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        self.collective_ptrs(op, [ptr(t) for t in sends], [ptr(t) for t in recvs], count, dname, root, stream)
+
+    def reduce_scatter(self, sends, recvs, stream=None) -> None:
+        """recvs[r] = sum over ranks of block r of sends[p]; each send holds
+        N * recvs[r].numel() elements."""
+        self._tensor_call("reduce_scatter", sends, recvs, recvs[0].numel(), 0, stream)
+
+    def all_gather(self, sends, recvs, stream=None) -> None:
+        """recvs[r] = concatenation of sends[0..N-1]."""
+        self._tensor_call("all_gather", sends, recvs, sends[0].numel(), 0, stream)
+
+    def broadcast(self, sends, recvs, root: int, stream=None) -> None:
+        """Every recvs[r] = sends[root] (other sends may be None)."""
+        self._tensor_call("broadcast", sends, recvs, recvs[0].numel(), root, stream)
+
+    def reduce(self, sends, recvs, root: int, stream=None) -> None:
+        """recvs[root] = sum over ranks of sends[p] (other recvs may be None)."""
+        self._tensor_call("reduce", sends, recvs, sends[0].numel(), root, stream)
 
     def allreduce_host(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None) -> None:
         """Host buffers in, host buffers out (H2D, kernel, D2H, synchronise)."""
