@@ -20,6 +20,8 @@ floor     measured single-GPU latency floor 2*L2_RTT + L_store->poll and the
           in-kernel time of the 128-byte calls
 bandwidth the two-shot kernels at N=8, 64 MiB and 512 MiB binary32 per rank,
           GB/s of compulsory traffic (2*N*M) against the measured HBM peak
+collectives ReduceScatter, AllGather, Broadcast, Reduce: N=4 latency (graph
+          replay) and N=8 bandwidth of compulsory bytes against the HBM peak
 cpu_baseline  the CPU oracle on a bounded sample of the same sweep
 
 --impl reference times the CPU oracle itself on the same sweep.
@@ -315,6 +317,7 @@ def run_ours(args, world, rank, local):
     floor = latency_floor(comm, rra, measure, torch, stream)
     clk = clocks.stop()
     bandwidth = bandwidth_end(rra, measure, torch, hbm_peak, args)
+    colls = collectives_table(rra, measure, torch, hbm_peak) if args.collectives else None
     e2e = end_to_end(comm, rra, cases, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
 
@@ -348,6 +351,8 @@ def run_ours(args, world, rank, local):
     }
     if decode is not None:
         line["decode_graph"] = decode
+    if colls is not None:
+        line["collectives"] = colls
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     comm.close()
@@ -487,6 +492,86 @@ def bandwidth_end(rra, measure, torch, hbm_peak, args):
             "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events; default chunking"}
 
 
+def collective_bytes(op, n, m):
+    """Compulsory HBM bytes of one call: every input read once, every output
+    written once (m = bytes of one block of `count` elements)."""
+    return {"reduce_scatter": n * n * m + n * m, "all_gather": n * m + n * n * m,
+            "broadcast": m + n * m, "reduce": n * m + m}[op]
+
+
+def collectives_table(rra, measure, torch, hbm_peak):
+    """ReduceScatter, AllGather, Broadcast (root 0) and Reduce (root 0):
+    N=4 latency (CUDA-graph replay of 16 calls, L2-resident buffers) at 128 B,
+    64 KiB and 1 MiB per block, and N=8 bandwidth (inputs and outputs far
+    beyond L2) at 16 MiB blocks (ReduceScatter, AllGather) / 64 MiB
+    (Broadcast, Reduce), binary32."""
+    lat = {}
+    n = 4
+    cap = torch.cuda.Stream()
+    for m in (128, 65536, 1 << 20):
+        count = m // 4
+        with rra.Comm(n, n * m) as c:
+            big = [torch.randn(n * count, device="cuda") for _ in range(n)]
+            small = [torch.randn(count, device="cuda") for _ in range(n)]
+            io = {"reduce_scatter": (big, small), "all_gather": (small, big),
+                  "broadcast": (small, [torch.empty_like(t) for t in small]),
+                  "reduce": (small, [torch.empty_like(t) for t in small])}
+            for op in rra.COLLECTIVES:
+                sends, recvs = io[op]
+                f = c.prepare_collective(op, [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs],
+                                         count, "fp32", 0, stream=cap)
+                f()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                cap.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.graph(g, stream=cap):
+                    for _ in range(16):
+                        f()
+                g.replay()
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(20):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    g.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1000.0 / 16)
+                lat["%s/%dB" % (op, m)] = round(measure.median(ts), 3)
+                del g
+            assert c.status()[0] == rra.OK
+    bw = {}
+    n = 8
+    for op in rra.COLLECTIVES:
+        m = (16 << 20) if op in ("reduce_scatter", "all_gather") else (64 << 20)
+        count = m // 4
+        blocks_in = n if op == "reduce_scatter" else 1
+        blocks_out = n if op == "all_gather" else 1
+        with rra.Comm(n, n * m) as c:
+            sends = [torch.rand(blocks_in * count, device="cuda") for _ in range(n)]
+            recvs = [torch.empty(blocks_out * count, device="cuda") for _ in range(n)]
+            sp, rp = [t.data_ptr() for t in sends], [t.data_ptr() for t in recvs]
+            for _ in range(2):
+                c.collective_ptrs(op, sp, rp, count, "fp32", 0)
+            torch.cuda.synchronize()
+            reps = 5
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                c.collective_ptrs(op, sp, rp, count, "fp32", 0)
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1000.0 / reps
+            gbs = collective_bytes(op, n, m) / t / 1e9
+            bw["%s/%dMiB" % (op, m >> 20)] = {"ms": round(t * 1000, 3), "GB/s": round(gbs, 1),
+                                              "frac": round(gbs / hbm_peak, 4),
+                                              "status": rra.STATUS_NAMES.get(c.status()[0])}
+            del sends, recvs
+        torch.cuda.empty_cache()
+    return {"latency_us_N4_fp32": lat, "bandwidth_N8_fp32": bw,
+            "bytes": "compulsory: every input read once, every output written once"}
+
+
 def end_to_end(comm, rra, cases, torch, args):
     """Host buffers in and out through rra_allreduce_host (pinned memory)."""
     from latency_barrier_free_gb300 import inputs
@@ -620,6 +705,8 @@ def main():
     ap.add_argument("--no-big", dest="big", action="store_false", help="skip the 512 MiB bandwidth case")
     ap.add_argument("--no-decode", dest="decode", action="store_false", help="skip the decode graph case")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-collectives", dest="collectives", action="store_false",
+                    help="skip the ReduceScatter/AllGather/Broadcast/Reduce table")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
