@@ -8,7 +8,7 @@ The operation follows "Every Microsecond Matters: Achieving Near Speed-of-Light
 Latency in GPU Collectives", Sec. III-A: an AllReduce-sum leaves in every rank's
 output the element-wise sum of all ranks' inputs.  The same section names the
 building blocks ReduceScatter, AllGather, Reduce and Broadcast, which are here
-too.  See ``rra_oracle.c`` for the exact evaluation order and precision.
+too, and the AllReduce with a residual-add epilogue.  See ``rra_oracle.c`` for the exact evaluation order and precision.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, exact integer sums, an order-sensitive binary32 case,
@@ -21,6 +21,7 @@ from .oracle import (  # noqa: F401
     all_gather,
     allreduce,
     allreduce_mt,
+    allreduce_residual,
     broadcast,
     build,
     f32_to_bf16,

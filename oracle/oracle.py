@@ -63,6 +63,9 @@ def _load():
             for name in ("rra_oracle_reduce_scatter", "rra_oracle_all_gather"):
                 getattr(lib, name).argtypes = [ctypes.c_int, vpp, vpp, ctypes.c_size_t, ctypes.c_int]
                 getattr(lib, name).restype = ctypes.c_int
+            lib.rra_oracle_allreduce_residual.argtypes = [ctypes.c_int, vpp, vpp, vpp, ctypes.c_size_t,
+                                                          ctypes.c_int]
+            lib.rra_oracle_allreduce_residual.restype = ctypes.c_int
             for name in ("rra_oracle_broadcast", "rra_oracle_reduce"):
                 getattr(lib, name).argtypes = [ctypes.c_int, ctypes.c_int, vpp, vpp, ctypes.c_size_t,
                                                ctypes.c_int]
@@ -199,4 +202,21 @@ def reduce(sends, dtype: str, root: int, recvs=None):
     rp, keep_r = _ptrs(recvs)
     _run(lib.rra_oracle_reduce, len(sends), int(root), sp, rp, count, code)
     del keep_s, keep_r
+    return recvs
+
+
+def allreduce_residual(sends, residuals, dtype: str):
+    """AllReduce-sum with each rank's residual added to the running value
+    before the one rounding: recv[r] = round(sum_p x_p + res[r])."""
+    lib = _load()
+    code, np_dt, count = _check_inputs(sends, dtype)
+    _check_inputs(residuals, dtype)
+    if len(residuals) != len(sends) or residuals[0].size != count:
+        raise ValueError("one residual of the inputs' size per rank")
+    recvs = [np.empty(count, dtype=np_dt) for _ in sends]
+    sp, keep_s = _ptrs(sends)
+    qp, keep_q = _ptrs(residuals)
+    rp, keep_r = _ptrs(recvs)
+    _run(lib.rra_oracle_allreduce_residual, len(sends), sp, qp, rp, count, code)
+    del keep_s, keep_q, keep_r
     return recvs

@@ -271,3 +271,41 @@ int rra_oracle_reduce(int nranks, int root, const void* const* send, void* const
     for (size_t i = 0; i < count; ++i) sum_one(nranks, send, 0, i, recv[root], dtype);
     return 0;
 }
+
+/* ---- AllReduce with a residual-add epilogue -------------------------------
+ * "Every Microsecond Matters" (Abstract; Sec. I, contributions) builds a
+ * low-latency device-side API so that custom collective kernels can be
+ * written on it.  The custom kernel built here is the AllReduce together
+ * with the residual add that follows it in a tensor-parallel transformer
+ * layer (the pages' LLM-inference setting): each rank adds its own residual
+ * stream to the AllReduce result.  Plain definition used here:
+ *
+ *   recv[r][i] = round_T( (x_0[i] + x_1[i] + ... + x_{N-1}[i]) + res[r][i] )
+ *
+ * the rank-order sum in the running type (binary32 for binary32/bfloat16,
+ * binary64 for binary64), then the widened residual added to the running
+ * value, then one rounding to bfloat16.  Returns 0, or -1 on a bad argument. */
+int rra_oracle_allreduce_residual(int nranks, const void* const* send, const void* const* res,
+                                  void* const* recv, size_t count, int dtype) {
+    if (nranks < 1 || send == NULL || res == NULL || recv == NULL) return -1;
+    if (dtype < ORACLE_FP32 || dtype > ORACLE_FP64) return -1;
+    for (size_t i = 0; i < count; ++i) {
+        for (int r = 0; r < nranks; ++r) {
+            if (dtype == ORACLE_FP32) {
+                float acc = ((const float*)send[0])[i];
+                for (int p = 1; p < nranks; ++p) acc = acc + ((const float*)send[p])[i];
+                ((float*)recv[r])[i] = acc + ((const float*)res[r])[i];
+            } else if (dtype == ORACLE_BF16) {
+                float acc = bf16_to_f32(((const uint16_t*)send[0])[i]);
+                for (int p = 1; p < nranks; ++p) acc = acc + bf16_to_f32(((const uint16_t*)send[p])[i]);
+                acc = acc + bf16_to_f32(((const uint16_t*)res[r])[i]);
+                ((uint16_t*)recv[r])[i] = rra_oracle_f32_to_bf16(acc);
+            } else {
+                double acc = ((const double*)send[0])[i];
+                for (int p = 1; p < nranks; ++p) acc = acc + ((const double*)send[p])[i];
+                ((double*)recv[r])[i] = acc + ((const double*)res[r])[i];
+            }
+        }
+    }
+    return 0;
+}

@@ -326,3 +326,53 @@ def test_allgather_of_reducescatter_is_allreduce(dtype):
         assert np.array_equal(ag[r].view(np.uint8), ar[r].view(np.uint8))
     red = oracle.reduce(sends, dtype, 2)
     assert np.array_equal(red[2].view(np.uint8), ar[0].view(np.uint8))
+
+
+# ------------------------------------------- AllReduce + residual add ----
+# recv[r] = round(sum_p x_p + res[r]): the residual joins the running value
+# after the rank-order sum, and bfloat16 is rounded once at the end.
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+def test_residual_closed_form(dtype):
+    n, count = 6, 19
+    sends = inputs.rank_plus_one(n, count, dtype)
+    np_dt = oracle.DTYPES[dtype][1]
+    res = []
+    for r in range(n):
+        v = np.full(count, 2.0 * r, dtype=np.float64)
+        res.append(oracle.f32_to_bf16(v) if dtype == "bf16" else v.astype(np_dt))
+    outs = oracle.allreduce_residual(sends, res, dtype)
+    for r in range(n):
+        got = _as_f32(outs[r]) if dtype == "bf16" else outs[r]
+        assert np.all(got == n * (n + 1) // 2 + 2 * r), r  # integers below 256: exact
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+def test_residual_zero_is_allreduce(dtype):
+    n, count = 5, 31
+    sends = inputs.normal(inputs.rng(91, 0), n, count, dtype)
+    zeros = [np.zeros(count, dtype=oracle.DTYPES[dtype][1]) for _ in range(n)]
+    outs = oracle.allreduce_residual(sends, zeros, dtype)
+    ar = oracle.allreduce(sends, dtype)
+    for a, b in zip(outs, ar):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_residual_added_after_the_sum():
+    # x = (2^24, 1), res = 1: the sum rounds 2^24 + 1 to 2^24 (tie to even),
+    # then + 1 rounds again to 2^24; adding the residual first would give
+    # 2^24 + 2.
+    big = np.float32(2.0 ** 24)
+    sends = [np.array([big], np.float32), np.array([1], np.float32)]
+    res = [np.array([1], np.float32)] * 2
+    outs = oracle.allreduce_residual(sends, res, "fp32")
+    assert outs[0][0] == big and outs[1][0] == big
+
+
+def test_residual_bf16_rounds_once():
+    # 256 + 1 + residual 1 = 258 exactly in binary32, one rounding -> 258.
+    # Rounding the AllReduce to bfloat16 first (257 -> 256, ties to even)
+    # and adding the residual after (257 -> 256) would give 256.
+    sends = [oracle.f32_to_bf16(np.array([256.0])), oracle.f32_to_bf16(np.array([1.0]))]
+    res = [oracle.f32_to_bf16(np.array([1.0]))] * 2
+    outs = oracle.allreduce_residual(sends, res, "bf16")
+    assert _as_f32(outs[0])[0] == 258.0 and _as_f32(outs[1])[0] == 258.0
