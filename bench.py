@@ -143,7 +143,7 @@ def measured_peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("kernels.cu", "cluster.cu", "coll.cu", "prims.cuh", "cluster_prims.cuh", "rra_internal.h"):
+    for f in ("kernels.cu", "cluster.cu", "coll.cu", "fused.cu", "prims.cuh", "cluster_prims.cuh", "rra_internal.h"):
         h.update(open(os.path.join(ROOT, "latency_barrier_free_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -632,7 +632,45 @@ def decode_graph(rra, torch):
                 torch.cuda.synchronize()
                 out["B%d/%s" % (batch, algo)] = round(e0.elapsed_time(e1) * 1000.0 / (reps * calls), 3)
                 assert c.status()[0] == rra.OK
-    return {"us_per_allreduce": out, "calls_per_graph": calls}
+            # the layer's AllReduce followed by its residual add: fused into one
+            # kernel, against the automatic AllReduce plus a separate add kernel
+            # ranks' rows of one [N, count] tensor each, so the unfused add is one kernel
+            y_all = torch.empty(n, count, dtype=torch.bfloat16, device="cuda")
+            res_all = torch.randn(n, count, device="cuda").to(torch.bfloat16)
+            z_all = torch.empty_like(y_all)
+            sp = [t.data_ptr() for t in xs]
+            qp = [res_all[r].data_ptr() for r in range(n)]
+            yp = [y_all[r].data_ptr() for r in range(n)]
+            for name in ("fused_residual", "auto+add"):
+                def step():
+                    if name == "fused_residual":
+                        c.allreduce_residual_ptrs(sp, qp, yp, count, "bf16")
+                    else:
+                        c.allreduce_ptrs(sp, yp, count, "bf16", "auto")
+                        torch.add(y_all, res_all, out=z_all)
+                step()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        for _ in range(calls):
+                            step()
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 10
+                e0.record()
+                for _ in range(reps):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                out["B%d/%s" % (batch, name)] = round(e0.elapsed_time(e1) * 1000.0 / (reps * calls), 3)
+                assert c.status()[0] == rra.OK
+    return {"us_per_allreduce": out, "calls_per_graph": calls,
+            "note": "fused_residual = rra_allreduce_residual; auto+add = rra_allreduce(auto) then one torch add "
+                    "kernel over all ranks' rows (the unfused layer epilogue)"}
 
 
 # ------------------------------------------------------- CPU baseline ----

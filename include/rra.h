@@ -264,6 +264,32 @@ rra_status_t rra_broadcast(rra_comm_t comm, int root, const void* const send[], 
 rra_status_t rra_reduce(rra_comm_t comm, int root, const void* const send[], void* const recv[],
                         size_t count, rra_dtype_t dtype, rra_stream_t stream);
 
+/*
+ * rra_allreduce_residual: AllReduce with the residual add of a
+ * tensor-parallel layer fused into it.
+ *     recv[r][i] = round( (send[0][i] + ... + send[N-1][i]) + residual[r][i] )
+ * The ranks are added in order 0..N-1 with a binary32 running value for
+ * binary32 and bfloat16 (binary64 for binary64), the residual is added to
+ * the running value, and bfloat16 is rounded once, at the end.  The paper
+ * (Abstract; Sec. I, contributions; Fig. 6-9) builds a device-side API for
+ * custom collective kernels; this kernel is written on this library's
+ * restatement of it, include/rra_device.cuh.
+ *   send, residual, recv: host arrays of nranks device pointers, 16-byte
+ *   aligned, count elements each; recv[r] may equal send[r] or residual[r].
+ * nranks <= 16 (RRA_ERR_INVALID_ARG above that).  Shape: one thread-block
+ * cluster of nranks CTAs per slice; each rank pushes its slice to every
+ * peer's shared memory while nranks^2 * count * element size <= 1 MiB, and
+ * to one partition owner each above that, the owner then writing every
+ * rank's output with that rank's residual (outputs and residuals are then
+ * treated as registered symmetric buffers, as by RRA_TWOSHOT_DIRECT).
+ * RRA_ATTR_CLUSTER_SLICE and RRA_ATTR_THREADS apply; RRA_ATTR_CTAS_PER_RANK,
+ * when set, caps the clusters, each then looping over several slices.
+ * Errors: as rra_allreduce.
+ */
+rra_status_t rra_allreduce_residual(rra_comm_t comm, const void* const send[], const void* const residual[],
+                                    void* const recv[], size_t count, rra_dtype_t dtype,
+                                    rra_stream_t stream);
+
 /* Synchronise the device and return the device status word: RRA_OK, or the
  * first device-side error (e.g. RRA_ERR_TIMEOUT).  A device error poisons the
  * communicator until rra_comm_reset().  If `rank`/`step` are non-NULL they

@@ -18,9 +18,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librra.so")
 
-SOURCES = ["kernels.cu", "cluster.cu", "coll.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
+SOURCES = ["kernels.cu", "cluster.cu", "coll.cu", "fused.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
 HEADERS = ["prims.cuh", "cluster_prims.cuh", "rra_internal.h"]
-PUBLIC_HEADERS = ["rra.h", "rra_probe.h", "rra_static.h"]
+PUBLIC_HEADERS = ["rra.h", "rra_probe.h", "rra_static.h", "rra_device.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

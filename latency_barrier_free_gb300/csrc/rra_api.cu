@@ -102,6 +102,7 @@ struct rra_comm {
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
     int coll_fits[4][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
+    int residual_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -816,6 +817,85 @@ rra_status_t rra_broadcast(rra_comm_t c, int root, const void* const send[], voi
 rra_status_t rra_reduce(rra_comm_t c, int root, const void* const send[], void* const recv[], size_t count,
                         rra_dtype_t dtype, rra_stream_t stream) {
     return run_coll(c, rra::kCollReduce, root, send, recv, count, dtype, stream);
+}
+
+// AllReduce + residual add (fused.cu): the one-shot shape while N^2 M <= 1 MiB
+// (as RRA_AUTO's cluster choice), the two-shot shape above.  Slices as for
+// the cluster AllReduce, within a stage of two sub-buffers; one cluster per
+// slice unless RRA_ATTR_CTAS_PER_RANK caps the clusters (then each loops
+// over several slices, one epoch each).
+static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, rra::FusedParams* f,
+                                  int* threads, bool* two_shot) {
+    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    const size_t n = (size_t)c->nranks;
+    const size_t es = elem_size(dtype);
+    const bool two = n * n * count * es > (1ull << 20);
+    int& fits = c->residual_fits[two ? 1 : 0][(int)dtype];
+    if (fits < 0) fits = rra::residual_max_active(dtype, two, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
+    if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
+    memset(f, 0, sizeof(*f));
+    rra::Params* p = &f->base;
+    p->win0 = c->win0;
+    p->ctrl = c->ctrl;
+    p->timing = c->timing;
+    p->stride = c->lay.window_stride;
+    p->count = count;
+    p->nvec = (uint32_t)ceil_div(count, rra::kVecBytes / es);
+    p->timeout_ns = (uint64_t)c->timeout_ms * 1000000ull;
+    p->nranks = c->nranks;
+    p->chunk_vecs = p->nvec;
+    p->epoch_slots = rra::kEpochSlots;
+    const size_t half = rra::kClusterStageBytes / 2 / rra::kVecBytes;  // vectors per sub-buffer
+    const size_t smax = two ? half / n * n : half / n;
+    const size_t t = (size_t)c->threads;
+    size_t S;
+    if (c->cluster_slice > 0) {
+        S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else {
+        const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / n);
+        S = std::max<size_t>(std::min<size_t>(p->nvec, t), ceil_div(p->nvec, target));
+        S = std::min<size_t>(S, t * rra::kClusterBatch);
+    }
+    if (two) S = align_up(S, n);
+    S = std::max<size_t>(two ? n : 1, std::min(S, smax));
+    const size_t nslices = ceil_div(p->nvec, S);
+    p->per_cta = (uint32_t)S;
+    p->nsteps = (uint32_t)nslices;
+    p->ctas_per_rank = (int32_t)(c->ctas_per_rank > 0 ? std::min(nslices, (size_t)c->ctas_per_rank) : nslices);
+    *threads = (int)std::min<size_t>(t, std::max<size_t>(32, align_up(S, 32)));
+    *two_shot = two;
+    return RRA_OK;
+}
+
+rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], const void* const residual[],
+                                    void* const recv[], size_t count, rra_dtype_t dtype, rra_stream_t stream) {
+    if (c == nullptr || send == nullptr || residual == nullptr || recv == nullptr || !valid_dtype(dtype))
+        return RRA_ERR_INVALID_ARG;
+    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    if (c->poisoned) return RRA_ERR_POISONED;
+    if (count == 0) return RRA_OK;
+    if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
+    rra::FusedParams f;
+    int threads = 0;
+    bool two = false;
+    {
+        std::lock_guard<std::mutex> g(c->mu);
+        rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two);
+        if (st != RRA_OK) return st;
+    }
+    for (int r = 0; r < c->nranks; ++r) {
+        if (send[r] == nullptr || residual[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
+        if (((uintptr_t)send[r] | (uintptr_t)residual[r] | (uintptr_t)recv[r]) & 15u) return RRA_ERR_INVALID_ARG;
+        f.base.send[r] = send[r];
+        f.base.recv[r] = recv[r];
+        f.resid[r] = residual[r];
+    }
+    cudaError_t e = rra::launch_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RRA_ERR_CUDA;
+    }
+    return RRA_OK;
 }
 
 rra_status_t rra_comm_status(rra_comm_t c, int* rank, int* step) {

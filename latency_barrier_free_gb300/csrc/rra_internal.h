@@ -110,6 +110,17 @@ enum { kCollReduceScatter = 0, kCollAllGather = 1, kCollBroadcast = 2, kCollRedu
 size_t coll_stage_bytes(const Params& p, int op);
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl);
 int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem);
+// AllReduce + residual add on the public device API (fused.cu): the cluster
+// AllReduce's launch shape; cluster c handles slices c, c + G, ... of
+// p.nsteps slices (G = p.ctas_per_rank), one epoch each.
+struct FusedParams {
+    Params base;
+    const void* resid[kClusterMaxRanks];  // rank r's residual stream (count elements)
+};
+size_t residual_stage_bytes(const Params& p, bool two_shot);
+cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
+                            cudaStream_t stream, bool pdl);
+int residual_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads, size_t smem);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

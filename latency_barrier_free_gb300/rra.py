@@ -43,6 +43,7 @@ SYMBOLS = [
     "rra_probe_sm_count",
     "rra_allreduce_static",
     "rra_reduce_scatter", "rra_all_gather", "rra_broadcast", "rra_reduce",
+    "rra_allreduce_residual",
 ]
 
 # The collectives besides AllReduce (all through distributed shared memory, N <= 16).
@@ -114,6 +115,7 @@ def load(path: str = LIB_PATH):
             "rra_all_gather": ([vp, pp, pp, sz, i32, vp], i32),
             "rra_broadcast": ([vp, i32, pp, pp, sz, i32, vp], i32),
             "rra_reduce": ([vp, i32, pp, pp, sz, i32, vp], i32),
+            "rra_allreduce_residual": ([vp, pp, pp, pp, sz, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -240,6 +242,43 @@ class Comm:
                 raise ValueError("all tensors must be contiguous CUDA tensors of one dtype and size")
         dname = {0: "fp32", 1: "bf16", 2: "fp64"}[dt]
         self.allreduce_ptrs([t.data_ptr() for t in sends], [t.data_ptr() for t in recvs], n, dname, algo, stream)
+
+    # -- AllReduce + residual add ------------------------------------------
+    def allreduce_residual_ptrs(self, send_ptrs, resid_ptrs, recv_ptrs, count: int, dtype: str,
+                                stream=None) -> None:
+        sp, ks = _ptr_array(send_ptrs)
+        qp, kq = _ptr_array(resid_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        st = self._lib.rra_allreduce_residual(self._h, sp, qp, rp, int(count), DTYPES[dtype], _stream_handle(stream))
+        del ks, kq, kr
+        _check(st, "rra_allreduce_residual")
+
+    def prepare_residual(self, send_ptrs, resid_ptrs, recv_ptrs, count: int, dtype: str, stream=None):
+        """As prepare(), for rra_allreduce_residual."""
+        sp, ks = _ptr_array(send_ptrs)
+        qp, kq = _ptr_array(resid_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        fn = self._lib.rra_allreduce_residual
+        args = (self._h, sp, qp, rp, ctypes.c_size_t(int(count)), ctypes.c_int(DTYPES[dtype]), _stream_handle(stream))
+
+        def call(_keep=(ks, kq, kr)):
+            st = fn(*args)
+            if st != OK:
+                raise RraError(st, "rra_allreduce_residual")
+        return call
+
+    def allreduce_residual(self, sends, residuals, recvs, stream=None) -> None:
+        """recvs[r] = sum over ranks of sends[p] + residuals[r] (one rounding)."""
+        ts = list(sends) + list(residuals) + list(recvs)
+        if len(sends) != self.nranks or len(residuals) != self.nranks or len(recvs) != self.nranks:
+            raise ValueError("need one send, residual and recv tensor per rank")
+        dt, n = _dtype_of(ts[0]), ts[0].numel()
+        for t in ts:
+            if not t.is_cuda or not t.is_contiguous() or t.numel() != n or _dtype_of(t) != dt:
+                raise ValueError("all tensors must be contiguous CUDA tensors of one dtype and size")
+        self.allreduce_residual_ptrs([t.data_ptr() for t in sends], [t.data_ptr() for t in residuals],
+                                     [t.data_ptr() for t in recvs], n, {0: "fp32", 1: "bf16", 2: "fp64"}[dt],
+                                     stream)
 
     # -- the other collectives ----------------------------------------------
     def _coll_args(self, op, send_ptrs, recv_ptrs, count, dtype, root, stream):
