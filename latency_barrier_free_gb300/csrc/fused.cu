@@ -72,11 +72,37 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
             if (v < npos) x[j] = load_input<T>(src, base + v, p.count);
         }
     };
-    // the first epoch's first inputs are in flight while the cluster barrier
-    // that guards the peers' windows completes
+    // Residual vectors of this thread's first outputs of an epoch: one-shot,
+    // its first kClusterBatch positions; two-shot, its first position for
+    // the first kClusterBatch ranks.  Loaded early, consumed after the wait.
+    uint4 rp[kClusterBatch];
+    auto prefetch_residual = [&](uint32_t base, uint32_t mine) {
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            if (kTwoShot) {
+                const uint32_t d = r + j < N ? r + j : r + j - N;
+                if (threadIdx.x < mine && (uint32_t)j < N)
+                    rp[j] = load_input<T>(f.resid[d], base + r * Q + threadIdx.x, p.count);
+            } else {
+                const uint32_t u = threadIdx.x + (uint32_t)j * nt;
+                if (u < mine) rp[j] = load_input<T>(f.resid[r], base + u, p.count);
+            }
+        }
+    };
+    // the first epoch's first inputs and residuals are in flight while the
+    // cluster barrier that guards the peers' windows completes
     load_batch(cid * S, npos_of(cid), 0);
-    const bool pushes = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank) != (int32_t)r;
+    prefetch_residual(cid * S, mine_of(cid, r));
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const bool pushes = drop != (int32_t)r;
+    uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
+                                                                   : nullptr;
+    if (tr) {
+        tr[0] = t_start;
+        tr[1] = globaltimer_after((uint64_t)x[0].x + (uint64_t)(uint32_t)drop);
+    }
     t.ready();
+    if (tr) tr[2] = globaltimer_ns();
 
     uint32_t k = 0;
     bool arrived = false;  // t.sent() done (CTA-uniform)
@@ -105,29 +131,17 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
                 }
             }
         }
+        if (tr && k == 0) tr[3] = globaltimer_ns();
         if (s + G >= nslices) {  // that was this CTA's last send: start the exit barrier now
             t.sent();
             arrived = true;
         }
-        // residual vectors of this thread's first outputs, in flight during
-        // the wait: one-shot, the thread's first kClusterBatch positions;
-        // two-shot, its first position for the first kClusterBatch ranks
-        uint4 rp[kClusterBatch];
-#pragma unroll
-        for (int j = 0; j < kClusterBatch; ++j) {
-            if (kTwoShot) {
-                const uint32_t d = r + j < N ? r + j : r + j - N;
-                if (threadIdx.x < mine && (uint32_t)j < N)
-                    rp[j] = load_input<T>(f.resid[d], base + r * Q + threadIdx.x, p.count);
-            } else {
-                const uint32_t u = threadIdx.x + (uint32_t)j * nt;
-                if (u < mine) rp[j] = load_input<T>(f.resid[r], base + u, p.count);
-            }
-        }
+        if (k > 0) prefetch_residual(base, mine);
         if (!t.wait(deadline)) {
             if (threadIdx.x == 0) record_error(p.ctrl, RRA_ERR_TIMEOUT, (int)r, (int)k);
             break;
         }
+        if (tr && k == 0) tr[4] = globaltimer_ns();
         // reduce in rank order, add the residual to the running value, round once
         auto sum_at = [&](uint32_t u) {
             typename M::Acc acc = M::load(t.recv(0, u));
@@ -176,6 +190,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
         p.timing[2 * blockIdx.x] = t_start;
         p.timing[2 * blockIdx.x + 1] = t_end;
     }
+    if (tr) tr[5] = globaltimer_ns();
 }
 
 template <typename T>

@@ -838,6 +838,7 @@ static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, 
     p->win0 = c->win0;
     p->ctrl = c->ctrl;
     p->timing = c->timing;
+    p->trace = c->trace;
     p->stride = c->lay.window_stride;
     p->count = count;
     p->nvec = (uint32_t)ceil_div(count, rra::kVecBytes / es);
