@@ -127,7 +127,7 @@ typedef enum {
                                       vectors).  0 (default): one 16-byte vector per thread
                                       for small messages, else about two CTAs per SM, at
                                       most 8 vectors per thread */
-    RRA_ATTR_CLUSTER_PIPE = 10     /* cluster two-shot on the persistent, double-buffered
+    RRA_ATTR_CLUSTER_PIPE = 10,    /* cluster two-shot on the persistent, double-buffered
                                       kernel (as many clusters as fit at once, each looping
                                       over slices; a receiver's arrival on the sender's
                                       "empty" mbarrier is the credit for the next push):
@@ -136,6 +136,10 @@ typedef enum {
                                       vectors per thread and a 2 x slice stage <= 96 KiB).
                                       Off by default: on GB300 it was up to 2.3x slower
                                       than one cluster per slice at 4-64 MiB per rank */
+    RRA_ATTR_HOST_ZERO_COPY = 11   /* rra_allreduce_host: 1 (default) when every buffer is
+                                      pinned host memory the device can address, the
+                                      kernel reads and writes it in place (no staging);
+                                      0: always stage through device buffers */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -166,7 +170,9 @@ typedef struct {
  *   max_bytes  largest message (count * element size) a call may pass, > 0.
  *   out        receives the communicator; unchanged on error.
  * Uses the current CUDA device.  Allocates once (cudaMalloc of
- * layout.total_bytes); fills sentinel regions with all-one bytes, LL flags,
+ * layout.total_bytes, and one pinned, device-mapped host word into which
+ * device code mirrors the first error, so that rra_allreduce_host can read
+ * it without a copy); fills sentinel regions with all-one bytes, LL flags,
  * accumulators and counters with zero, sets the epoch to 1 and synchronises.
  * Environment overrides read here: RRA_POLL_TIMEOUT_MS, RRA_CTAS_PER_RANK,
  * RRA_THREADS, RRA_SCRATCH_ONESHOT, RRA_SCRATCH_TWOSHOT (bytes).
@@ -203,11 +209,15 @@ rra_status_t rra_allreduce(rra_comm_t comm, const void* const send[], void* cons
 
 /*
  * rra_allreduce_host: the same operation on HOST buffers, end to end.
- * send[r]/recv[r] are host pointers (pinned memory gives the fastest copies).
- * The call copies every send[r] to device staging buffers owned by the
- * communicator (allocated on the first call: 2 * nranks * max_bytes), runs
- * rra_allreduce on `stream`, copies every recv[r] back and synchronises
- * `stream` before returning.  One cudaMemcpyAsync per rank and direction.
+ * send[r]/recv[r] are host pointers, 16-byte aligned.  If every one of them
+ * is pinned host memory that the device can address (cudaHostAlloc'd or
+ * registered; on GB300 the GPU reaches it over the coherent NVLink-C2C link
+ * to the Grace CPU) and RRA_ATTR_HOST_ZERO_COPY is 1 (default), the kernel
+ * reads the inputs and writes the outputs in host memory directly.
+ * Otherwise the call copies every send[r] to device staging buffers owned
+ * by the communicator (allocated on first use: 2 * nranks * max_bytes), runs
+ * rra_allreduce, and copies every recv[r] back (one cudaMemcpyAsync per rank
+ * and direction).  Either way it synchronises `stream` before returning.
  * Errors: as rra_allreduce, plus RRA_ERR_OOM for the staging buffers, plus
  * any device-side error of this call (the status word is read after the
  * synchronisation).

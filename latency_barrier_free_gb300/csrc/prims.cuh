@@ -238,6 +238,8 @@ static __device__ __noinline__ void record_error(Ctrl* ctrl, uint32_t code, int 
     if (atomicCAS(&ctrl->status, 0u, code) == 0u) {
         ctrl->err_rank = rank;
         ctrl->err_step = step;
+        uint32_t* const mirror = ctrl->host_status;
+        if (mirror != nullptr) *(volatile uint32_t*)mirror = code;  // visible to the host once the stream completes
     }
 }
 

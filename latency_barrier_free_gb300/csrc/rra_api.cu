@@ -99,6 +99,7 @@ struct rra_comm {
     int64_t pdl = 1;                        // programmatic dependent launch
     int64_t cluster_slice = 0;              // cluster kernels: bytes per rank per slice, 0 = auto
     int64_t cluster_pipe = 0;               // persistent cluster two-shot: -1 auto, 0 never (default), 1 always
+    int64_t host_zero_copy = 1;             // rra_allreduce_host: run on mapped pinned buffers directly
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
     int coll_fits[4][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
@@ -109,7 +110,8 @@ struct rra_comm {
     // rra_allreduce_host staging (allocated on first use)
     char* stage = nullptr;
     size_t stage_slot = 0;
-    uint32_t* host_status = nullptr;
+    uint32_t* host_status = nullptr;       // pinned host word (device-mapped when host_mirror)
+    bool host_mirror = false;              // device code mirrors the status word into host_status
     std::mutex mu;
 };
 
@@ -266,12 +268,26 @@ rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out) {
     }
     c->ctrl = (Ctrl*)c->base;
     c->win0 = c->base + lay.ctrl_bytes;
+    // A pinned, device-mapped host word that device code writes together with
+    // the status word on the first error: the host entry reads it after
+    // synchronising instead of copying the status word back.
+    uint32_t* mirror_dev = nullptr;
+    if (cudaHostAlloc((void**)&c->host_status, sizeof(uint32_t), cudaHostAllocMapped) == cudaSuccess) {
+        *c->host_status = 0u;
+        if (cudaHostGetDevicePointer((void**)&mirror_dev, c->host_status, 0) != cudaSuccess) mirror_dev = nullptr;
+    } else {
+        c->host_status = nullptr;
+    }
+    cudaGetLastError();
     if (rra::launch_init(c->base, lay.total_bytes, lay, nranks, 0) != cudaSuccess ||
+        cudaMemcpy(&c->ctrl->host_status, &mirror_dev, sizeof(mirror_dev), cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(c->base);
+        if (c->host_status) cudaFreeHost(c->host_status);
         delete c;
         return RRA_ERR_CUDA;
     }
+    c->host_mirror = mirror_dev != nullptr;
     *out = c;
     return RRA_OK;
 }
@@ -345,6 +361,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
             c->cluster_pipe = v;
             return RRA_OK;
+        case RRA_ATTR_HOST_ZERO_COPY:
+            if (v < 0 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->host_zero_copy = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -363,6 +383,7 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_PDL: *v = c->pdl; return RRA_OK;
         case RRA_ATTR_CLUSTER_SLICE: *v = c->cluster_slice; return RRA_OK;
         case RRA_ATTR_CLUSTER_PIPE: *v = c->cluster_pipe; return RRA_OK;
+        case RRA_ATTR_HOST_ZERO_COPY: *v = c->host_zero_copy; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -720,6 +741,49 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
     for (int r = 0; r < c->nranks; ++r)
         if (send[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
+    if (c->host_status == nullptr) return RRA_ERR_OOM;  // its allocation failed at creation
+    cudaStream_t s = (cudaStream_t)stream;
+    // After the stream completes: the status of this call's kernels, from the
+    // device-written mirror, or by copying the status word back.
+    auto finish = [&]() -> rra_status_t {
+        if (!c->host_mirror &&
+            cudaMemcpyAsync(c->host_status, &c->ctrl->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
+                cudaSuccess)
+            return RRA_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return RRA_ERR_CUDA;
+        const uint32_t v = *(volatile uint32_t*)c->host_status;
+        if (v != 0u) {
+            c->poisoned = true;
+            return (rra_status_t)v;
+        }
+        return RRA_OK;
+    };
+    // Zero copy: when every buffer is pinned host memory that the device can
+    // address (on GB300, reached over the coherent NVLink-C2C link to the
+    // Grace CPU), the kernel reads the inputs and writes the outputs in host
+    // memory itself; no staging buffers and no copies.
+    if (c->host_zero_copy) {
+        const void* msend[RRA_MAX_RANKS];
+        void* mrecv[RRA_MAX_RANKS];
+        bool mapped = true;
+        for (int r = 0; r < c->nranks && mapped; ++r) {
+            cudaPointerAttributes a{}, b{};
+            if (cudaPointerGetAttributes(&a, send[r]) != cudaSuccess ||
+                cudaPointerGetAttributes(&b, recv[r]) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+                b.type != cudaMemoryTypeHost || a.devicePointer == nullptr || b.devicePointer == nullptr) {
+                cudaGetLastError();
+                mapped = false;
+                break;
+            }
+            msend[r] = a.devicePointer;
+            mrecv[r] = b.devicePointer;
+        }
+        if (mapped) {
+            rra_status_t st = rra_allreduce(c, msend, mrecv, count, dtype, algo, stream);
+            if (st != RRA_OK) return st;
+            return finish();
+        }
+    }
     if (c->stage == nullptr) {
         c->stage_slot = align_up(c->max_bytes, 256);
         if (cudaMalloc((void**)&c->stage, 2 * (size_t)c->nranks * c->stage_slot) != cudaSuccess) {
@@ -727,14 +791,7 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
             c->stage = nullptr;
             return RRA_ERR_OOM;
         }
-        if (cudaHostAlloc((void**)&c->host_status, sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess) {
-            cudaGetLastError();
-            cudaFree(c->stage);
-            c->stage = nullptr;
-            return RRA_ERR_OOM;
-        }
     }
-    cudaStream_t s = (cudaStream_t)stream;
     const size_t bytes = count * es;
     const void* dsend[RRA_MAX_RANKS];
     void* drecv[RRA_MAX_RANKS];
@@ -750,15 +807,7 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
         if (cudaMemcpyAsync(recv[r], drecv[r], bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
             return RRA_ERR_CUDA;
     }
-    if (cudaMemcpyAsync(c->host_status, &c->ctrl->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
-        cudaSuccess)
-        return RRA_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return RRA_ERR_CUDA;
-    if (*c->host_status != 0u) {
-        c->poisoned = true;
-        return (rra_status_t)*c->host_status;
-    }
-    return RRA_OK;
+    return finish();
 }
 
 // Shared front end of the four collectives.  ReduceScatter's inputs and
@@ -919,6 +968,7 @@ rra_status_t rra_comm_reset(rra_comm_t c) {
     if (rra::launch_init(c->base, c->lay.total_bytes, c->lay, c->nranks, 0) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
         return RRA_ERR_CUDA;
+    if (c->host_status) *(volatile uint32_t*)c->host_status = 0u;
     c->poisoned = false;
     return RRA_OK;
 }

@@ -29,7 +29,9 @@ struct Ctrl {
     int32_t drop_rank;   // injected fault: rank whose stores to peers are skipped; -1 = none
     uint32_t scrub_arrive;  // LL flag scrub: CTAs arrived at the grid barrier
     uint32_t scrub_gen;     // LL flag scrub: completed scrubs (barrier generation)
-    uint32_t reserved[58];
+    uint32_t* host_status;  // device address of a pinned host word that mirrors `status`
+                            // (written with it on the first error), or null
+    uint32_t reserved[56];
     // Every CTA slot holds the same value: the epoch of the next step.  CTA b
     // of a call with G CTAs reads slot b at entry and writes epoch + steps to
     // every slot b' = b (mod G); each slot has exactly one reader/writer per

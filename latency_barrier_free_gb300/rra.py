@@ -28,7 +28,7 @@ ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 BARRIER_FREE = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct")
 ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,
          "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6, "cooperative": 7, "pdl": 8,
-         "cluster_slice": 9, "cluster_pipe": 10}
+         "cluster_slice": 9, "cluster_pipe": 10, "host_zero_copy": 11}
 MAX_RANKS = 64
 
 # Exported symbols, in declaration order of the public headers.
@@ -342,6 +342,20 @@ class Comm:
     def reduce(self, sends, recvs, root: int, stream=None) -> None:
         """recvs[root] = sum over ranks of sends[p] (other recvs may be None)."""
         self._tensor_call("reduce", sends, recvs, sends[0].numel(), root, stream)
+
+    def prepare_host(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None):
+        """As prepare(), for rra_allreduce_host (host buffers; synchronises)."""
+        sp, ks = _ptr_array(send_ptrs)
+        rp, kr = _ptr_array(recv_ptrs)
+        fn = self._lib.rra_allreduce_host
+        args = (self._h, sp, rp, ctypes.c_size_t(int(count)), ctypes.c_int(DTYPES[dtype]),
+                ctypes.c_int(ALGOS[algo]), _stream_handle(stream))
+
+        def call(_keep=(ks, kr)):
+            st = fn(*args)
+            if st != OK:
+                raise RraError(st, "rra_allreduce_host")
+        return call
 
     def allreduce_host(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None) -> None:
         """Host buffers in, host buffers out (H2D, kernel, D2H, synchronise)."""

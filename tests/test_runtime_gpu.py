@@ -160,6 +160,25 @@ def test_host_buffer_entry_point(algo):
             check_against_oracle(sends_np, recvs_np, "fp32", algo)
 
 
+@pytest.mark.parametrize("zero_copy", [1, 0])
+@pytest.mark.parametrize("algo", ALGOS + CLUSTER)
+def test_host_entry_pinned_buffers(algo, zero_copy):
+    """Pinned host buffers: with zero copy the kernel reads and writes host
+    memory directly; without it the call stages through device buffers.
+    Both give the oracle's result, twice in a row."""
+    n, count = 4, 70001
+    sends_np = inputs.normal(inputs.rng(73, 0), n, count, "fp32")
+    hs = [torch.from_numpy(a).pin_memory() for a in sends_np]
+    hr = [torch.full((count,), float("nan")).pin_memory() for _ in range(n)]
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("host_zero_copy", zero_copy)
+        for _ in range(2):
+            comm.allreduce_host([t.data_ptr() for t in hs], [t.data_ptr() for t in hr], count, "fp32", algo)
+            check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", algo)
+            for t in hr:
+                t.fill_(float("nan"))
+
+
 def test_in_kernel_timing():
     n, count = 4, 1 << 16
     with rra.Comm(n, count * 4) as comm:
