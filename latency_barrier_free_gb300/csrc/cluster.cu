@@ -181,8 +181,9 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     if (tr) tr[5] = globaltimer_ns();
 }
 
-// Persistent, double-buffered two-shot (the pages' "a receive is the credit
-// for the next send", Sec. IV, restated with mbarriers).  Cluster c handles
+// Persistent, double-buffered two-shot (the pages' double buffering, Sec. IV,
+// in which receiving from a peer is what permits the next send to it,
+// restated with mbarriers).  Cluster c handles
 // slices c, c + G, c + 2G, ... (G clusters in the grid, p.nsteps slices in
 // all); slice k of a cluster uses stage buffer b = k & 1.  Per buffer, each
 // CTA has a "full" mbarrier (completed by the N-1 incoming partitions'
