@@ -20,6 +20,8 @@ floor     measured single-GPU latency floor 2*L2_RTT + L_store->poll and the
           in-kernel time of the 128-byte calls
 bandwidth the two-shot kernels at N=8, 64 MiB and 512 MiB binary32 per rank,
           GB/s of compulsory traffic (2*N*M) against the measured HBM peak
+barrier_baseline  flag-barrier latency vs N, and the one-shot and two-shot
+          barrier baselines beside their barrier-free counterparts (N=4)
 collectives ReduceScatter, AllGather, Broadcast, Reduce: N=4 latency (graph
           replay) and N=8 bandwidth of compulsory bytes against the HBM peak
 cpu_baseline  the CPU oracle on a bounded sample of the same sweep
@@ -318,6 +320,7 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     bandwidth = bandwidth_end(rra, measure, torch, hbm_peak, args)
     colls = collectives_table(rra, measure, torch, hbm_peak) if args.collectives else None
+    barriers = barrier_table(rra, measure, torch) if args.barriers else None
     e2e = end_to_end(comm, rra, cases, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
 
@@ -353,6 +356,8 @@ def run_ours(args, world, rank, local):
         line["decode_graph"] = decode
     if colls is not None:
         line["collectives"] = colls
+    if barriers is not None:
+        line["barrier_baseline"] = barriers
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     comm.close()
@@ -490,6 +495,52 @@ def bandwidth_end(rra, measure, torch, hbm_peak, args):
             torch.cuda.empty_cache()
     return {"nranks": n, "dtype": "fp32", "bytes": "2*N*M per call", "sizes": out,
             "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events; default chunking"}
+
+
+def barrier_table(rra, measure, torch):
+    """The design the paper replaces, measured beside the barrier-free one:
+    the flag barrier's latency against N (one CTA per rank, back to back),
+    and at N=4 binary32 the barrier baselines against their barrier-free
+    counterparts (CUDA-graph replay of 16 calls, µs per call)."""
+    lat = {}
+    for n in (2, 4, 8, 16, 64):
+        with rra.Comm(n, 4096) as c:
+            lat["N%d" % n] = round(c.barrier_latency(2000) / 1000.0, 3)
+    pairs = (("oneshot_barrier", "oneshot_sentinel"), ("twoshot_barrier", "twoshot_dbuf"))
+    cap = torch.cuda.Stream()
+    us = {}
+    n = 4
+    for m in (128, 65536, 1 << 20):
+        count = m // 4
+        with rra.Comm(n, m) as c:
+            xs = [torch.randn(count, device="cuda") for _ in range(n)]
+            ys = [torch.empty_like(x) for x in xs]
+            for pair in pairs:
+                for algo in pair:
+                    f = c.prepare([t.data_ptr() for t in xs], [t.data_ptr() for t in ys], count, "fp32", algo,
+                                  stream=cap)
+                    f()
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    cap.wait_stream(torch.cuda.current_stream())
+                    with torch.cuda.graph(g, stream=cap):
+                        for _ in range(16):
+                            f()
+                    g.replay()
+                    torch.cuda.synchronize()
+                    ts = []
+                    for _ in range(20):
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        g.replay()
+                        e1.record()
+                        torch.cuda.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1000.0 / 16)
+                    us["%s/%dB" % (algo, m)] = round(measure.median(ts), 3)
+                    del g
+            assert c.status()[0] == rra.OK
+    return {"barrier_us_vs_N": lat, "N4_fp32_us_per_call": us,
+            "pairs": ["%s vs %s" % p for p in pairs]}
 
 
 def collective_bytes(op, n, m):
@@ -746,6 +797,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-collectives", dest="collectives", action="store_false",
                     help="skip the ReduceScatter/AllGather/Broadcast/Reduce table")
+    ap.add_argument("--no-barriers", dest="barriers", action="store_false",
+                    help="skip the barrier-baseline table")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always

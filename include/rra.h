@@ -89,12 +89,16 @@ typedef enum {
                                   st.async into peers' shared memory completes their
                                   mbarrier (arrival of the bytes is the signal); no state
                                   between calls; N <= 16, any size */
-    RRA_TWOSHOT_CLUSTER = 8    /* two-shot through distributed shared memory: rank r pushes
+    RRA_TWOSHOT_CLUSTER = 8,   /* two-shot through distributed shared memory: rank r pushes
                                   partition q of its slice to CTA q only (ReduceScatter),
                                   CTA q adds the N contributions in rank order and stores
                                   the result into every rank's output (AllGather as direct
                                   stores, as RRA_TWOSHOT_DIRECT); HBM carries only the
                                   inputs read once and the outputs written once; N <= 16 */
+    RRA_TWOSHOT_BARRIER = 9    /* BASELINE, not barrier-free: two-shot with plain stores and
+                                  two flag barriers per step (ReduceScatter, barrier, reduce
+                                  + AllGather stores, barrier, gather; Sec. III-B's design
+                                  applied to Sec. III-A's two-shot); rank-order sums */
 } rra_algo_t;
 
 /* Communicator attributes (rra_comm_set_attr / rra_comm_get_attr). */
@@ -161,7 +165,8 @@ typedef struct {
     size_t total_bytes;     /* ctrl_bytes + nranks * window_stride */
     size_t bf_bytes;        /* barrier baseline flags: 64 CTAs x 64 ranks x 4 B */
     size_t bd_chunk;        /* barrier baseline payload bytes per rank per step */
-    size_t bd_bytes;        /* barrier baseline data: N x bd_chunk (one-shot cap) */
+    size_t bd_bytes;        /* barrier baselines' data: 2 x N x bd_chunk (one-shot cap);
+                               the two-shot baseline's AllGather slots are the second half */
 } rra_layout_t;
 
 /*

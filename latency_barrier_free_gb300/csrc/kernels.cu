@@ -563,6 +563,97 @@ __global__ void __launch_bounds__(256) oneshot_barrier_kernel(const __grid_const
     cta_epilogue(p, s);
 }
 
+// Two-shot with barriers (the design the paper replaces, Sec. III-B, here for
+// the two-shot of Sec. III-A): per step, plain stores of partition q of the
+// chunk into window q's ReduceScatter slot [r]; an N-way flag barrier; the
+// owner reduces its partition in rank order and stores the result into its
+// own output and into every window's AllGather slot [r]; a second barrier;
+// every rank copies the gathered partitions into its output.  CTA c of every
+// rank handles the same positions u of every partition, so the per-CTA flag
+// barriers order every exchange.  Reuse: a step's ReduceScatter slots are
+// consumed before its second barrier, its AllGather slots before the next
+// step's first barrier, after which alone they are written again.
+template <typename T>
+__device__ __forceinline__ bool twoshot_barrier_body(const Params& p, const CtaState& s, int* fail) {
+    using M = VecMath<T>;
+    const int N = p.nranks, r = s.rank;
+    char* const rs_mine = window(p, r) + p.region_off;
+    char* const ag_mine = window(p, r) + p.aux2_off;
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
+
+#pragma unroll 1
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint32_t tag = (uint32_t)(2ull * e);
+        const uint32_t base = k * p.chunk_vecs;
+        const uint32_t rem = min(p.chunk_vecs, p.nvec - base);  // vectors of this step
+        const uint32_t pk = (rem + (uint32_t)N - 1) / (uint32_t)N;  // partition of this step
+        const uint32_t u0 = (uint32_t)s.sub * p.per_cta;
+        const uint32_t u1 = min(u0 + p.per_cta, pk);
+        w.step = (int)k;
+        // ReduceScatter: plain stores into the owners' windows
+        if (!s.drop) {
+#pragma unroll 1
+            for (uint32_t u = u0 + threadIdx.x; u < u1; u += blockDim.x) {
+#pragma unroll 1
+                for (int q = 0; q < N; ++q) {
+                    const uint32_t v = (uint32_t)q * pk + u;
+                    if (q == r || v >= rem) continue;
+                    st_relaxed_v4(window(p, q) + p.region_off + (uint64_t)r * p.slot_bytes + (uint64_t)u * kVecBytes,
+                                  load_input<T>(p.send[r], base + v, p.count));
+                }
+            }
+        }
+        if (!flag_barrier(p, s, tag, w, fail)) return false;  // partitions delivered
+        // reduce my partition in rank order; AllGather: plain stores to every window
+#pragma unroll 1
+        for (uint32_t u = u0 + threadIdx.x; u < u1; u += blockDim.x) {
+            const uint32_t pos = (uint32_t)r * pk + u;
+            if (pos >= rem) continue;
+            typename M::Acc acc;
+#pragma unroll 1
+            for (int q = 0; q < N; ++q) {
+                const uint4 x = q == r ? load_input<T>(p.send[r], base + pos, p.count)
+                                       : ld_relaxed_v4(rs_mine + (uint64_t)q * p.slot_bytes + (uint64_t)u * kVecBytes);
+                if (q == 0) acc = M::load(x);
+                else M::add(acc, x);
+            }
+            const uint4 out = M::store(acc);
+            store_output<T>(p.recv[r], base + pos, p.count, out);
+            if (!s.drop) {
+#pragma unroll 1
+                for (int d = 0; d < N; ++d)
+                    if (d != r)
+                        st_relaxed_v4(window(p, d) + p.aux2_off + (uint64_t)r * p.slot_bytes + (uint64_t)u * kVecBytes,
+                                      out);
+            }
+        }
+        if (!flag_barrier(p, s, tag + 1u, w, fail)) return false;  // reduced partitions delivered
+#pragma unroll 1
+        for (uint32_t u = u0 + threadIdx.x; u < u1; u += blockDim.x) {
+#pragma unroll 1
+            for (int q = 0; q < N; ++q) {
+                const uint32_t pos = (uint32_t)q * pk + u;
+                if (q == r || pos >= rem) continue;
+                store_output<T>(p.recv[r], base + pos, p.count,
+                                ld_relaxed_v4(ag_mine + (uint64_t)q * p.slot_bytes + (uint64_t)u * kVecBytes));
+            }
+        }
+    }
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) twoshot_barrier_kernel(const __grid_constant__ Params p) {
+    __shared__ int fail;
+    pdl_entry();
+    if (threadIdx.x == 0) fail = 0;
+    CtaState s = cta_prologue(p);
+    s.skip = __syncthreads_or(s.skip) != 0;
+    if (!s.skip) (void)twoshot_barrier_body<T>(p, s, &fail);
+    cta_epilogue(p, s);
+}
+
 // Barrier latency (Fig. 3 analogue): N ranks x 1 CTA run `nsteps` flag
 // barriers back to back; CTA 0 records %globaltimer after the first and after
 // the last barrier in timing[0..1].
@@ -1049,6 +1140,7 @@ static const void* kernel_for(int kind) {
         case kKindOneshotLLWide: return (const void*)oneshot_wide_kernel<T, true>;
         case kKindOneshotSentinelWide: return (const void*)oneshot_wide_kernel<T, false>;
         case kKindOneshotBarrier: return (const void*)oneshot_barrier_kernel<T>;
+        case kKindTwoshotBarrier: return (const void*)twoshot_barrier_kernel<T>;
         case kKindBarrierProbe: return (const void*)barrier_probe_kernel;
     }
     return nullptr;

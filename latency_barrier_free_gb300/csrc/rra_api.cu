@@ -47,7 +47,7 @@ size_t elem_size(rra_dtype_t d) {
     return 0;
 }
 
-bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_TWOSHOT_CLUSTER; }
+bool valid_algo(int a) { return a >= RRA_ONESHOT_LL && a <= RRA_TWOSHOT_BARRIER; }
 bool is_cluster(int a) { return a == RRA_ONESHOT_CLUSTER || a == RRA_TWOSHOT_CLUSTER; }
 bool valid_dtype(int d) { return d >= RRA_FP32 && d <= RRA_FP64; }
 
@@ -193,7 +193,7 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
     L.os_bytes = align_up(2 * n * L.os_chunk, rra::kRegionAlign);
     L.ts_bytes = align_up(2 * (2 * n * L.ts_part), rra::kRegionAlign);
     L.la_bytes = align_up(la_sizes(L.la_part, nranks).total, rra::kRegionAlign);
-    L.bd_bytes = align_up(n * L.bd_chunk, rra::kRegionAlign);
+    L.bd_bytes = align_up(2 * n * L.bd_chunk, rra::kRegionAlign);  // slots; the two-shot baseline's AllGather
     L.window_stride = align_up(L.ll_bytes + L.bf_bytes + L.os_bytes + L.ts_bytes + L.la_bytes + L.bd_bytes,
                                kWindowAlign);
     L.ctrl_bytes = align_up(sizeof(Ctrl), rra::kRegionAlign);
@@ -642,11 +642,27 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             work = chunk;
             break;
         }
+        case RRA_TWOSHOT_BARRIER: {
+            // partitions of at most one slot (bd_chunk); a step covers N of them
+            size_t part = L.bd_chunk / rra::kVecBytes;
+            if (c->ts_chunk > 0) part = std::min(part, std::max<size_t>(1, (size_t)c->ts_chunk / rra::kVecBytes / n));
+            part = std::min(part, ceil_div(p->nvec, n));
+            p->chunk_vecs = (uint32_t)(n * part);
+            p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
+            p->region_off = off_bd;                      // ReduceScatter slots [q]
+            p->aux2_off = off_bd + n * L.bd_chunk;       // AllGather slots [q]
+            p->slot_bytes = L.bd_chunk;
+            p->parity_bytes = 0;
+            p->aux_off = off_bf;
+            work = part;
+            break;
+        }
         default:
             return RRA_ERR_INVALID_ARG;
     }
     int64_t cap_ctas = cmax;
-    if (algo == RRA_ONESHOT_BARRIER) cap_ctas = std::min<int64_t>(cap_ctas, rra::kBarrierCtas);
+    if (algo == RRA_ONESHOT_BARRIER || algo == RRA_TWOSHOT_BARRIER)
+        cap_ctas = std::min<int64_t>(cap_ctas, rra::kBarrierCtas);
     const bool wide = kind == rra::kKindOneshotLLWide || kind == rra::kKindOneshotSentinelWide;
     // positions per CTA to aim for: one per thread, or, for the wide variant,
     // as many as one shared-memory stage round holds

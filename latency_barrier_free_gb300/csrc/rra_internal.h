@@ -83,7 +83,8 @@ enum KernelKind {
     kKindOneshotLLWide = 6,
     kKindOneshotSentinelWide = 7,
     kKindBarrierProbe = 8,
-    kNumKinds = 9
+    kKindTwoshotBarrier = RRA_TWOSHOT_BARRIER,
+    kNumKinds = 10
 };
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors

@@ -23,7 +23,7 @@ ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_CORESIDENT, ERR_TIMEOUT, ERR_POISONE
 DTYPES = {"fp32": 0, "bf16": 1, "fp64": 2}
 ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomic": 3,
          "oneshot_barrier": 4, "twoshot_direct": 5, "auto": 6, "oneshot_cluster": 7,
-         "twoshot_cluster": 8}
+         "twoshot_cluster": 8, "twoshot_barrier": 9}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 BARRIER_FREE = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct")
 ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,

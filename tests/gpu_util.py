@@ -9,7 +9,7 @@ import oracle
 TORCH_DT = {"fp32": "float32", "bf16": "bfloat16", "fp64": "float64"}
 ELEM = {"fp32": 4, "bf16": 2, "fp64": 8}
 FIXED_ORDER = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "oneshot_barrier", "twoshot_direct",
-               "oneshot_cluster", "twoshot_cluster")
+               "oneshot_cluster", "twoshot_cluster", "twoshot_barrier")
 ALGOS = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "twoshot_direct")
 CLUSTER = ("oneshot_cluster", "twoshot_cluster")  # N <= 16
 

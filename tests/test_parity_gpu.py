@@ -238,22 +238,27 @@ def test_oneshot_wide_and_narrow_variants(algo, wide, n):
             check_against_oracle(sends_np, got, dtype, algo)
 
 
+@pytest.mark.parametrize("algo", ["oneshot_barrier", "twoshot_barrier"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-def test_barrier_baseline_parity(dtype):
-    """The barrier-based baseline (plain stores + two flag barriers per step)
-    adds in rank order too, so it is bit-exact against the oracle."""
+def test_barrier_baseline_parity(dtype, algo):
+    """The barrier-based baselines (plain stores + two flag barriers per step)
+    add in rank order too, so they are bit-exact against the oracle; several
+    steps, several CTAs per rank, ragged partitions, in place."""
     for n in (2, 4, 7, 64):
         with rra.Comm(n, 70000 * ELEM[dtype]) as comm:
             for count in (1, 33, 4097, 70000):
                 sends_np = inputs.normal(inputs.rng(66, count, n), n, count, dtype)
-                got = run(comm, sends_np, dtype, "oneshot_barrier")
-                check_against_oracle(sends_np, got, dtype, "oneshot_barrier")
+                got = run(comm, sends_np, dtype, algo)
+                check_against_oracle(sends_np, got, dtype, algo)
             comm.set_attr("oneshot_chunk", 1024)
+            comm.set_attr("twoshot_chunk", 16 * 8 * n)  # partitions of 8 vectors
             comm.set_attr("ctas_per_rank", 3)
             sends_np = inputs.normal(inputs.rng(67, n), n, 9000, dtype)
-            assert comm.plan_call(9000, dtype, "oneshot_barrier")[1] >= 3
-            got = run(comm, sends_np, dtype, "oneshot_barrier")
-            check_against_oracle(sends_np, got, dtype, "oneshot_barrier")
+            assert comm.plan_call(9000, dtype, algo)[1] >= 3
+            got = run(comm, sends_np, dtype, algo)
+            check_against_oracle(sends_np, got, dtype, algo)
+            got = run(comm, sends_np, dtype, algo, in_place=True)
+            check_against_oracle(sends_np, got, dtype, algo)
 
 
 @pytest.mark.parametrize("n", [4, 8, 16])

@@ -233,26 +233,28 @@ def test_epoch_scrub_at_boundary(algo, start):
 
 
 def test_barrier_latency_and_baseline_timeout():
-    """The flag barrier of the baseline is measurable for N = 2..64, and a rank
-    that never signals makes the baseline time out like the others."""
+    """The flag barrier of the baselines is measurable for N = 2..64, and a
+    rank that never signals makes both baselines time out like the others."""
     for n in (2, 8, 64):
         with rra.Comm(n, 4096) as comm:
             ns = comm.barrier_latency(200)
             assert 50.0 < ns < 1e6
             x = [torch.ones(1024, device="cuda") for _ in range(n)]
             y = poison_like(x)
-            comm.allreduce(x, y, "oneshot_barrier")
-            torch.cuda.synchronize()
-            assert comm.status()[0] == rra.OK
-            assert torch.equal(y[n - 1], torch.full_like(y[0], float(n)))
-            comm.set_attr("poll_timeout_ms", 20)
-            comm.inject_drop(1)
-            comm.allreduce(x, y, "oneshot_barrier")
-            assert comm.status()[0] == rra.ERR_TIMEOUT
-            comm.reset()
-            comm.allreduce(x, y, "oneshot_barrier")
-            torch.cuda.synchronize()
-            assert comm.status()[0] == rra.OK
+            for algo in ("oneshot_barrier", "twoshot_barrier"):
+                comm.allreduce(x, y, algo)
+                torch.cuda.synchronize()
+                assert comm.status()[0] == rra.OK
+                assert torch.equal(y[n - 1], torch.full_like(y[0], float(n)))
+                comm.set_attr("poll_timeout_ms", 20)
+                comm.inject_drop(1)
+                comm.allreduce(x, y, algo)
+                assert comm.status()[0] == rra.ERR_TIMEOUT
+                comm.reset()
+                comm.set_attr("poll_timeout_ms", 1000)
+                comm.allreduce(x, y, algo)
+                torch.cuda.synchronize()
+                assert comm.status()[0] == rra.OK
 
 
 @pytest.mark.parametrize("algo", ALGOS)
@@ -271,7 +273,7 @@ def test_plain_launch_matches_cooperative(algo):
         check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
 
 
-@pytest.mark.parametrize("algo", ALGOS + ("oneshot_barrier",))
+@pytest.mark.parametrize("algo", ALGOS + ("oneshot_barrier", "twoshot_barrier"))
 def test_programmatic_dependent_launch(algo):
     """With programmatic dependent launch each kernel waits for its
     predecessor before touching memory: back-to-back calls (stream and graph)
