@@ -321,6 +321,7 @@ def run_ours(args, world, rank, local):
     bandwidth = bandwidth_end(rra, measure, torch, hbm_peak, args)
     colls = collectives_table(rra, measure, torch, hbm_peak) if args.collectives else None
     barriers = barrier_table(rra, measure, torch) if args.barriers else None
+    sweep = scratch_sweep(rra, measure, torch) if args.scratch_sweep else None
     e2e = end_to_end(comm, rra, cases, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
 
@@ -358,6 +359,8 @@ def run_ours(args, world, rank, local):
         line["collectives"] = colls
     if barriers is not None:
         line["barrier_baseline"] = barriers
+    if sweep is not None:
+        line["scratch_sweep"] = sweep
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     comm.close()
@@ -541,6 +544,52 @@ def barrier_table(rra, measure, torch):
             assert c.status()[0] == rra.OK
     return {"barrier_us_vs_N": lat, "N4_fp32_us_per_call": us,
             "pairs": ["%s vs %s" % p for p in pairs]}
+
+
+# live scratch per window as a function of the per-rank step (chunk) bytes
+SCRATCH_OF_CHUNK = {
+    "oneshot_sentinel": ("oneshot_chunk", lambda n, ch: 2 * n * ch),      # 2 parities x N slots
+    "oneshot_ll": ("oneshot_chunk", lambda n, ch: 4 * n * ch),            # LL doubles every byte
+    "twoshot_dbuf": ("twoshot_chunk", lambda n, ch: 4 * ch),              # RS + AG, 2 parities, N parts
+    "twoshot_direct": ("twoshot_chunk", lambda n, ch: 2 * ch),            # RS only
+    "ll128_atomic": ("ll128_chunk", lambda n, ch: 4 * ch + 4 * ch // n),  # LL AllGather + accumulators
+}
+
+
+def scratch_sweep(rra, measure, torch):
+    """Fig. 12 restated: AllReduce latency against the scratch each window
+    keeps live, set through the per-step chunk, N=8 binary32, 1 MiB and
+    16 MiB per rank (stream-ordered calls, CUDA events, 2 warm-up + 10)."""
+    n = 8
+    out = {}
+    for size in (1 << 20, 16 << 20):
+        count = size // 4
+        with rra.Comm(n, size) as c:
+            xs = [torch.randn(count, device="cuda") for _ in range(n)]
+            ys = [torch.empty_like(x) for x in xs]
+            for algo, (attr, scratch) in SCRATCH_OF_CHUNK.items():
+                if algo.startswith("oneshot") and size > (1 << 20):
+                    continue
+                for kib in (16, 64, 256, 1024, 4096, 16384, 65536):
+                    chunk = kib << 10
+                    if chunk > size:
+                        continue
+                    c.set_attr(attr, chunk)
+                    for _ in range(2):
+                        c.allreduce(xs, ys, algo)
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(10):
+                        c.allreduce(xs, ys, algo)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    out["%s/%dMiB/chunk%dKiB" % (algo, size >> 20, kib)] = {
+                        "us": round(e0.elapsed_time(e1) * 100.0, 2),
+                        "scratch_KiB": scratch(n, chunk) >> 10}
+                c.set_attr(attr, 0)
+            assert c.status()[0] == rra.OK
+    return out
 
 
 def collective_bytes(op, n, m):
@@ -799,6 +848,8 @@ def main():
                     help="skip the ReduceScatter/AllGather/Broadcast/Reduce table")
     ap.add_argument("--no-barriers", dest="barriers", action="store_false",
                     help="skip the barrier-baseline table")
+    ap.add_argument("--scratch-sweep", action="store_true",
+                    help="add the latency-vs-scratch sweep of the global-memory kernels (Fig. 12; about a minute)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
