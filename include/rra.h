@@ -140,10 +140,15 @@ typedef enum {
                                       vectors per thread and a 2 x slice stage <= 96 KiB).
                                       Off by default: on GB300 it was up to 2.3x slower
                                       than one cluster per slice at 4-64 MiB per rank */
-    RRA_ATTR_HOST_ZERO_COPY = 11   /* rra_allreduce_host: 1 (default) when every buffer is
+    RRA_ATTR_HOST_ZERO_COPY = 11,  /* rra_allreduce_host: 1 (default) when every buffer is
                                       pinned host memory the device can address, the
                                       kernel reads and writes it in place (no staging);
                                       0: always stage through device buffers */
+    RRA_ATTR_COLL_SPLIT = 12       /* rra_broadcast / rra_reduce in two hops (the root
+                                      scatters its slice and every CTA forwards its part /
+                                      ReduceScatter, then every owner sends to the root):
+                                      -1 (default) when nranks >= 3 and the message is at
+                                      least 256 KiB, 0 never, 1 always */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     // every peer has issued its pushes into it.  After a completed wait every
     // incoming byte has landed and no peer will touch this memory again, so
     // the thread leaves without waiting (exited threads count as arrived).
-    if (!ok) cluster_wait();
+    if (!__all_sync(0xffffffffu, ok)) cluster_wait();  // warp-uniform, as .aligned requires
     if (p.timing != nullptr && threadIdx.x == 0) {
         const uint64_t t_end = globaltimer_ns();
         p.timing[2 * blockIdx.x] = t_start;

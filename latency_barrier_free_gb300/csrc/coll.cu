@@ -220,6 +220,154 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
     }
 }
 
+// Broadcast and Reduce in two hops, for large slices: the root's CTA would
+// otherwise send (Broadcast) or receive (Reduce) (N-1) S vectors alone.  The
+// slice is cut into N parts of Q = S / N vectors (part q = CTA q's).
+//   Broadcast: the root pushes part q to CTA q (region A); every CTA then
+//     pushes its part to every CTA but the root (region B slot [r]); each
+//     writes its output from its part and region B.  The root writes its
+//     output from its input.
+//   Reduce: ReduceScatter (rank r pushes part q to CTA q's region A slot
+//     [r]); CTA q adds part q in rank order and pushes it to the root's
+//     region B slot [q]; the root writes its output.  Same rank-order sums.
+// Region A, then region B, in shared memory; one mbarrier per region.
+template <typename T, int kOp>
+__global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    constexpr bool kBcast = kOp == kCollBroadcastSplit;
+    extern __shared__ __align__(16) uint4 stage[];
+    __shared__ __align__(8) uint64_t bars[2];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = S / N;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint32_t root = (uint32_t)p.root;
+    const uint64_t count = p.count;
+    const bool is_root = r == root;
+    auto len_of = [&](uint32_t q) { return npos > q * Q ? min(Q, npos - q * Q) : 0u; };
+    const uint32_t mine = len_of(r);
+    uint4* const regA = stage;
+    uint4* const regB = stage + (kBcast ? Q : N * Q);
+    const uint32_t barA = smem_u32(&bars[0]);
+    const uint32_t barB = smem_u32(&bars[1]);
+    if (threadIdx.x == 0) {
+        mbar_init(barA, 1u);
+        mbar_init(barB, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (kBcast) {
+            mbar_expect_tx(barA, (is_root ? 0u : mine) * (uint32_t)kVecBytes);
+            mbar_expect_tx(barB, (is_root ? 0u : npos - mine) * (uint32_t)kVecBytes);
+        } else {
+            mbar_expect_tx(barA, (N - 1) * mine * (uint32_t)kVecBytes);
+            mbar_expect_tx(barB, (is_root ? npos - mine : 0u) * (uint32_t)kVecBytes);
+        }
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const void* src = p.send[r];
+    const bool pushes = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank) != (int32_t)r;
+    const uint32_t items = kBcast ? (is_root ? npos : 0u) : npos;
+    uint4 x[kClusterBatch];
+    auto load_batch = [&](uint32_t b0) {
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = b0 + threadIdx.x + (uint32_t)j * nt;
+            if (v < items) x[j] = load_input<T>(src, base + v, count);
+        }
+    };
+    load_batch(0);
+    cluster_wait();  // every peer's barriers exist
+
+    // hop 1: part q of the slice to CTA q
+    const uint32_t step = nt * (uint32_t)kClusterBatch;
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < items; b0 += step) {
+        if (b0 != 0) load_batch(b0);
+#pragma unroll
+        for (int j = 0; j < kClusterBatch; ++j) {
+            const uint32_t v = b0 + threadIdx.x + (uint32_t)j * nt;
+            if (v >= items) continue;
+            const uint32_t q = v / Q;
+            const uint32_t u = v - q * Q;
+            if (kBcast) {
+                store_output<T>(p.recv[r], base + v, count, x[j]);  // the root's own output
+                if (q == r) regB[r * Q + u] = x[j];
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(regA + u), q), x[j], map_to_rank(barA, q));
+            } else {
+                if (q == r) regA[r * Q + u] = x[j];
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(regA + r * Q + u), q), x[j], map_to_rank(barA, q));
+            }
+        }
+    }
+    int ok = 1;
+    Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+    while (!mbar_try_wait(barA, 0u))
+        if (waiter_expired(w)) {
+            ok = 0;
+            break;
+        }
+    ok = __syncthreads_and(ok);  // also: this CTA's own part, written by other threads
+    // hop 2
+    if (ok) {
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            if (kBcast) {
+                const uint4 y = is_root ? regB[r * Q + u] : regA[u];
+                if (!is_root) store_output<T>(p.recv[r], base + r * Q + u, count, y);
+                if (pushes) {
+#pragma unroll 1
+                    for (uint32_t k = 1; k < N; ++k) {
+                        const uint32_t q = r + k < N ? r + k : r + k - N;
+                        if (q != root)
+                            st_async_v4(map_to_rank(smem_u32(regB + r * Q + u), q), y, map_to_rank(barB, q));
+                    }
+                }
+            } else {
+                typename M::Acc acc = M::load(regA[u]);
+#pragma unroll 1
+                for (uint32_t q = 1; q < N; ++q) M::add(acc, regA[q * Q + u]);
+                const uint4 out = M::store(acc);
+                if (is_root) store_output<T>(p.recv[r], base + r * Q + u, count, out);
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(regB + r * Q + u), root), out, map_to_rank(barB, root));
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my pushes are issued"
+    if (ok) {
+        w.step = 1;
+        while (!mbar_try_wait(barB, 0u))
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+    }
+    ok = __syncthreads_and(ok);
+    // the other parts into this CTA's output (Broadcast: every CTA but the
+    // root's; Reduce: the root's)
+    if (ok && (kBcast ? !is_root : is_root)) {
+#pragma unroll 1
+        for (uint32_t v = threadIdx.x; v < npos; v += nt) {
+            const uint32_t q = v / Q;
+            if (q == r) continue;
+            store_output<T>(p.recv[r], base + v, count, regB[v]);
+        }
+    }
+    if (!ok) cluster_wait();  // a CTA whose wait ran out keeps its memory until every peer has pushed
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 template <typename T>
 static const void* coll_kernel_for(int op) {
     switch (op) {
@@ -227,6 +375,8 @@ static const void* coll_kernel_for(int op) {
         case kCollAllGather: return (const void*)coll_kernel<T, kCollAllGather>;
         case kCollBroadcast: return (const void*)coll_kernel<T, kCollBroadcast>;
         case kCollReduce: return (const void*)coll_kernel<T, kCollReduce>;
+        case kCollBroadcastSplit: return (const void*)coll_split_kernel<T, kCollBroadcastSplit>;
+        case kCollReduceSplit: return (const void*)coll_split_kernel<T, kCollReduceSplit>;
     }
     return nullptr;
 }
@@ -243,7 +393,7 @@ static const void* coll_kernel_ptr(rra_dtype_t dtype, int op) {
 // Opt a kernel in to the full stage and to clusters of up to 16 CTAs (once
 // per kernel; the attributes are process-wide).
 static cudaError_t configure_coll(const void* k) {
-    static const void* done[12] = {};
+    static const void* done[18] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
@@ -259,14 +409,22 @@ static cudaError_t configure_coll(const void* k) {
 }
 
 size_t coll_stage_bytes(const Params& p, int op) {
-    const size_t slots = op == kCollBroadcast ? 1 : (size_t)p.nranks;
-    return slots * p.per_cta * kVecBytes;
+    const size_t n = (size_t)p.nranks;
+    const size_t q = p.per_cta / n;  // split forms: vectors per part
+    switch (op) {
+        case kCollBroadcast: return (size_t)p.per_cta * kVecBytes;
+        case kCollBroadcastSplit: return (q + n * q) * kVecBytes;
+        case kCollReduceSplit: return 2 * n * q * kVecBytes;
+        default: return n * p.per_cta * kVecBytes;
+    }
 }
 
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl) {
     const size_t smem = coll_stage_bytes(p, op);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks ||
         p.root < 0 || p.root >= p.nranks)
+        return cudaErrorInvalidValue;
+    if ((op == kCollBroadcastSplit || op == kCollReduceSplit) && p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
     const void* k = coll_kernel_ptr(dtype, op);
     if (k == nullptr) return cudaErrorInvalidValue;

@@ -102,7 +102,9 @@ struct rra_comm {
     int64_t host_zero_copy = 1;             // rra_allreduce_host: run on mapped pinned buffers directly
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
-    int coll_fits[4][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
+    int coll_fits[6][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1},
+                           {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
+    int64_t coll_split = -1;                // Broadcast/Reduce in two hops: -1 auto, 0 never, 1 always
     int residual_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]
     bool poisoned = false;
     uint64_t* timing = nullptr;
@@ -365,6 +367,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < 0 || v > 1) return RRA_ERR_INVALID_ARG;
             c->host_zero_copy = v;
             return RRA_OK;
+        case RRA_ATTR_COLL_SPLIT:
+            if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->coll_split = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -384,6 +390,7 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_CLUSTER_SLICE: *v = c->cluster_slice; return RRA_OK;
         case RRA_ATTR_CLUSTER_PIPE: *v = c->cluster_pipe; return RRA_OK;
         case RRA_ATTR_HOST_ZERO_COPY: *v = c->host_zero_copy; return RRA_OK;
+        case RRA_ATTR_COLL_SPLIT: *v = c->coll_split; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -490,9 +497,16 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     p->chunk_vecs = p->nvec;
     p->epoch_slots = rra::kEpochSlots;
     p->root = root;
-    const size_t slots = op == rra::kCollBroadcast ? 1 : n;
+    const bool split = op == rra::kCollBroadcastSplit || op == rra::kCollReduceSplit;
     const size_t per_pos = op == rra::kCollReduceScatter ? n : 1;  // input vectors per slice position
-    const size_t smax = rra::kClusterStageBytes / rra::kVecBytes / slots;
+    const size_t stage_vecs = rra::kClusterStageBytes / rra::kVecBytes;
+    size_t smax;
+    switch (op) {
+        case rra::kCollBroadcast: smax = stage_vecs; break;
+        case rra::kCollBroadcastSplit: smax = stage_vecs * n / (n + 1) / n * n; break;  // (S/N + S) vectors
+        case rra::kCollReduceSplit: smax = stage_vecs / 2 / n * n; break;              // 2 S vectors
+        default: smax = stage_vecs / n; break;
+    }
     const size_t t = (size_t)c->threads;
     size_t S;
     if (c->cluster_slice > 0) {
@@ -502,7 +516,8 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
         S = std::max<size_t>(std::min<size_t>(p->nvec, std::max<size_t>(1, t / per_pos)), ceil_div(p->nvec, target));
         S = std::min<size_t>(S, std::max<size_t>(1, t * rra::kClusterBatch / per_pos));
     }
-    S = std::max<size_t>(1, std::min(S, smax));
+    if (split) S = align_up(S, n);  // N parts per slice
+    S = std::max<size_t>(split ? n : 1, std::min(S, smax));
     p->per_cta = (uint32_t)S;
     p->ctas_per_rank = (int32_t)ceil_div(p->nvec, S);
     *threads = (int)std::min<size_t>(t, std::max<size_t>(32, align_up(S * per_pos, 32)));
@@ -840,6 +855,12 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
     const size_t es = elem_size(dtype);
     const size_t blocks = (op == rra::kCollReduceScatter || op == rra::kCollAllGather) ? (size_t)c->nranks : 1;
     if (count > c->max_bytes / es / blocks) return RRA_ERR_INVALID_ARG;
+    // Broadcast / Reduce: two hops for large messages (the root's CTA no
+    // longer carries all of a slice's traffic), one hop for small ones
+    if (op == rra::kCollBroadcast || op == rra::kCollReduce) {
+        const bool split = c->coll_split == 1 || (c->coll_split < 0 && c->nranks >= 3 && count * es >= (256u << 10));
+        if (split) op = op == rra::kCollBroadcast ? rra::kCollBroadcastSplit : rra::kCollReduceSplit;
+    }
     Params p;
     int threads = 0;
     {
@@ -847,9 +868,11 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
         rra_status_t st = plan_coll(c, count, dtype, op, root < 0 ? 0 : root, &p, &threads);
         if (st != RRA_OK) return st;
     }
+    const bool bcast = op == rra::kCollBroadcast || op == rra::kCollBroadcastSplit;
+    const bool reduce = op == rra::kCollReduce || op == rra::kCollReduceSplit;
     for (int r = 0; r < c->nranks; ++r) {
-        const bool need_send = op != rra::kCollBroadcast || r == root;
-        const bool need_recv = op != rra::kCollReduce || r == root;
+        const bool need_send = !bcast || r == root;  // Broadcast reads only the root's input
+        const bool need_recv = !reduce || r == root;  // Reduce writes only the root's output
         if ((need_send && send[r] == nullptr) || (need_recv && recv[r] == nullptr)) return RRA_ERR_INVALID_ARG;
         if (((uintptr_t)(need_send ? send[r] : nullptr) | (uintptr_t)(need_recv ? recv[r] : nullptr)) & 15u)
             return RRA_ERR_INVALID_ARG;

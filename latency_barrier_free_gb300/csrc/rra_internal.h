@@ -109,7 +109,14 @@ int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, siz
 // ReduceScatter, AllGather, Broadcast, Reduce through distributed shared
 // memory (coll.cu): one cluster of N CTAs per slice of p.per_cta vectors of
 // a block of p.count elements (p.nvec vectors), p.ctas_per_rank slices.
-enum { kCollReduceScatter = 0, kCollAllGather = 1, kCollBroadcast = 2, kCollReduce = 3 };
+enum {
+    kCollReduceScatter = 0,
+    kCollAllGather = 1,
+    kCollBroadcast = 2,
+    kCollReduce = 3,
+    kCollBroadcastSplit = 4,  // two hops: scatter from the root, then every CTA pushes its part
+    kCollReduceSplit = 5      // two hops: ReduceScatter, then every owner pushes to the root
+};
 size_t coll_stage_bytes(const Params& p, int op);
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl);
 int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem);

@@ -109,6 +109,30 @@ def test_reduce(n, dtype):
                 _same_bits(got[root], expect, (count, root, "null"))
 
 
+@pytest.mark.parametrize("split", [1, -1])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+def test_two_hop_broadcast_and_reduce(n, dtype, split):
+    """Broadcast and Reduce in two hops (forced, and chosen automatically for
+    a message of at least 256 KiB): the same bits as the oracle; ragged
+    parts; Broadcast with NULL non-root inputs, Reduce with NULL non-root
+    outputs."""
+    big = (300 << 10) // ELEM[dtype]
+    counts = (1, 5, 33, 4097, 20001, big) if split == 1 else (big,)
+    with rra.Comm(n, big * ELEM[dtype]) as comm:
+        comm.set_attr("coll_split", split)
+        for count in counts:
+            for root in sorted({0, n - 1}):
+                sends_np = inputs.normal(inputs.rng(89, count, n, root), n, count, dtype)
+                got = _run(comm, "broadcast", sends_np, count, dtype, root,
+                           send_mask=[r == root for r in range(n)])
+                expect = oracle.broadcast(sends_np, dtype, root)
+                for r in range(n):
+                    _same_bits(got[r], expect[r], ("bc", count, root, r))
+                got = _run(comm, "reduce", sends_np, count, dtype, root, recv_mask=[r == root for r in range(n)])
+                _same_bits(got[root], oracle.reduce(sends_np, dtype, root)[root], ("rd", count, root))
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_reduce_scatter_then_all_gather_is_allreduce(dtype):
     """AllGather(ReduceScatter(x)) equals the fixed-order AllReduce bit for
@@ -223,14 +247,17 @@ def test_graph_replay():
             _same_bits(rd_out[1].cpu().numpy(), oracle.reduce(b, dtype, 1)[1], ("rd", rep))
 
 
+@pytest.mark.parametrize("split", [0, 1])
 @pytest.mark.parametrize("op", rra.COLLECTIVES)
-def test_dropped_rank_times_out_and_reset(op):
+def test_dropped_rank_times_out_and_reset(op, split):
     """A rank that skips its pushes makes its receivers' bounded waits run
-    out: RRA_ERR_TIMEOUT, no hang; after a reset the call is correct."""
+    out: RRA_ERR_TIMEOUT, no hang; after a reset the call is correct (one-
+    and two-hop Broadcast / Reduce)."""
     n, count, dtype = 4, 3000, "fp32"
     root = 0
-    drop = 2 if op != "broadcast" else root  # a Broadcast's only sender is the root
+    drop = 2 if op != "broadcast" else root  # a Broadcast's only first-hop sender is the root
     with rra.Comm(n, n * count * 4) as comm:
+        comm.set_attr("coll_split", split)
         comm.set_attr("poll_timeout_ms", 20)
         comm.inject_drop(drop)
         m = n * count if op == "reduce_scatter" else count
