@@ -106,7 +106,9 @@ typedef enum {
     RRA_ATTR_CTAS_PER_RANK = 0,    /* 0 = chosen per call from the message size; for the
                                       persistent cluster two-shot, a cap on its clusters */
     RRA_ATTR_POLL_TIMEOUT_MS = 1,  /* limit of every device-side wait (default 1000) */
-    RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256 */
+    RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256; while
+                                      it is not set, the cluster two-shot may use 256 for
+                                      messages up to ~1-2 MiB per rank */
     RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step; 0 (default) = the step
                                       whose live scratch over all windows is ~32 MiB (stays
                                       in L2), within the per-window scratch cap */

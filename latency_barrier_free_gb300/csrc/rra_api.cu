@@ -90,6 +90,7 @@ struct rra_comm {
     char* win0 = nullptr;
     int sm_count = 0;
     int threads = 128;
+    bool threads_set = false;              // THREADS given by the user (attribute or environment)
     int64_t ctas_per_rank = 0;
     int64_t timeout_ms = 1000;
     int64_t ts_chunk = 0, la_chunk = 0, os_chunk = 0;
@@ -236,6 +237,7 @@ rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out) {
     c->ctas_per_rank = env_i64("RRA_CTAS_PER_RANK", 0);
     const int64_t thr = env_i64("RRA_THREADS", 128);
     if (thr == 64 || thr == 128 || thr == 256) c->threads = (int)thr;
+    c->threads_set = getenv("RRA_THREADS") != nullptr;
     if (c->timeout_ms <= 0) c->timeout_ms = 1000;
     if (c->ctas_per_rank < 0) c->ctas_per_rank = 0;
 
@@ -327,6 +329,7 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v != 64 && v != 128 && v != 256) return RRA_ERR_INVALID_ARG;
             if (c->threads != (int)v) {
                 c->threads = (int)v;
+                c->threads_set = true;
                 for (auto& row : c->blocks_per_sm)
                     for (int& b : row) b = -1;
             }
@@ -433,14 +436,22 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     const size_t stage_vecs = rra::kClusterStageBytes / rra::kVecBytes;
     const size_t smax = two ? stage_vecs / n * n : stage_vecs / n;
     size_t S;
+    size_t T = (size_t)c->threads;
+    const size_t s_mid = ceil_div((size_t)p->nvec * n, 512);  // ~512 CTAs in all
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else if (two && s_mid <= 1024) {
+        // two-shot up to ~1-2 MiB per rank (latency-bound): about 512 CTAs of
+        // 256 threads, 2-4 vectors per thread (GB300 sweep at N = 4, 8:
+        // 1 MiB in 3.5 / 5.5 us against 4.7 / 8.1 with the rule below)
+        if (!c->threads_set) T = 256;
+        S = std::max<size_t>(std::min<size_t>(p->nvec, T), s_mid);
     } else {
         // one vector per thread for small messages; then spread over about
         // two CTAs per SM, but at most one batch of loads per thread
         const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / n);
-        S = std::max<size_t>(std::min<size_t>(p->nvec, (size_t)c->threads), ceil_div(p->nvec, target));
-        S = std::min<size_t>(S, (size_t)c->threads * rra::kClusterBatch);
+        S = std::max<size_t>(std::min<size_t>(p->nvec, T), ceil_div(p->nvec, target));
+        S = std::min<size_t>(S, T * rra::kClusterBatch);
     }
     if (two) S = align_up(S, n);
     S = std::max<size_t>(two ? n : 1, std::min(S, smax));
@@ -448,7 +459,7 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     const size_t nslices = ceil_div(p->nvec, S);
     p->ctas_per_rank = (int32_t)nslices;  // one cluster per slice
     p->epoch_slots = rra::kEpochSlots;
-    *threads = (int)std::min<size_t>((size_t)c->threads, std::max<size_t>(32, align_up(S, 32)));
+    *threads = (int)std::min<size_t>(T, std::max<size_t>(32, align_up(S, 32)));
     *mode = two ? rra::kClusterTwoshot : rra::kClusterOneshot;
     if (two && c->cluster_pipe != 0 && S <= (size_t)*threads * rra::kClusterBatch &&
         2 * S * rra::kVecBytes <= rra::kClusterStageBytes) {
