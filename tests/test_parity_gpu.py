@@ -261,7 +261,7 @@ def test_barrier_baseline_parity(dtype, algo):
             check_against_oracle(sends_np, got, dtype, algo)
 
 
-@pytest.mark.parametrize("n", [4, 8, 16])
+@pytest.mark.parametrize("n", [2, 4, 8, 16, 64])
 def test_auto_algorithm(n):
     """RRA_AUTO runs the algorithm rra_select_algo names, with its results."""
     max_bytes = 1 << 20

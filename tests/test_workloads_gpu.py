@@ -21,7 +21,8 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("algo", ["twoshot_dbuf", "oneshot_ll", "twoshot_direct", "oneshot_sentinel"])
+@pytest.mark.parametrize("algo", ["twoshot_dbuf", "oneshot_ll", "twoshot_direct", "oneshot_sentinel",
+                                  "oneshot_cluster", "twoshot_cluster", "auto"])
 @pytest.mark.parametrize("batch", inputs.W3_BATCHES)
 def test_workload3_decode_graph(batch, algo):
     """One token = 160 AllReduces of bf16 [batch, 8192] over N=8, captured in
@@ -95,7 +96,8 @@ def _sampled_check(sends, recvs, dtype, algo, nsample=20000, seed=0):
 @pytest.mark.parametrize("size", inputs.W5_SIZES)
 def test_workload5_bandwidth_end(size, dtype):
     """N=8 at 4 MiB / 64 MiB / 512 MiB per rank with the two-shot kernels (the
-    launches the bench times at the bandwidth end), uniform(-1,1) inputs from
+    cluster two-shot is the one the bench times at the bandwidth end, and the
+    automatic choice), uniform(-1,1) inputs from
     the seeded generator; every rank's output equal, sampled elements
     bit-exact against the oracle."""
     n = 8
@@ -113,7 +115,7 @@ def test_workload5_bandwidth_end(size, dtype):
         sends.append(t)
     recvs = [torch.empty_like(s) for s in sends]
     with rra.Comm(n, size) as comm:
-        for algo in ("twoshot_dbuf", "twoshot_direct"):
+        for algo in ("twoshot_dbuf", "twoshot_direct", "twoshot_cluster", "auto"):
             for t in recvs:
                 t.view(torch.uint8).fill_(0x7F)
             comm.allreduce(sends, recvs, algo)
@@ -121,7 +123,7 @@ def test_workload5_bandwidth_end(size, dtype):
             assert comm.status()[0] == rra.OK
             for r in range(1, n):
                 assert torch.equal(recvs[r].view(torch.uint8), recvs[0].view(torch.uint8))
-            _sampled_check(sends, recvs, dtype, algo)
+            _sampled_check(sends, recvs, dtype, rra.select_algo(n, size, dtype) if algo == "auto" else algo)
         for algo in ("oneshot_sentinel", "ll128_atomic"):
             if size > (64 << 20):
                 continue
