@@ -93,10 +93,12 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir=None):
+        import tempfile
+
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), "clocks_rank%d.csv" % gpu_index)
 
     def start(self):
         try:
@@ -198,7 +200,7 @@ def run_ours(args, world, rank, local):
 
     comm = rra.Comm(NRANKS, 1 << 20)
     cases = sweep_cases()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clock_log_dir)
     clocks.start()
     bufs = {}
     for dt, size in cases:
@@ -848,6 +850,8 @@ def main():
                     help="skip the ReduceScatter/AllGather/Broadcast/Reduce table")
     ap.add_argument("--no-barriers", dest="barriers", action="store_false",
                     help="skip the barrier-baseline table")
+    ap.add_argument("--clock-log-dir", default=None,
+                    help="directory for the raw nvidia-smi clock samples (default: the system temp directory)")
     ap.add_argument("--scratch-sweep", action="store_true",
                     help="add the latency-vs-scratch sweep of the global-memory kernels (Fig. 12; about a minute)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
