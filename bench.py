@@ -18,8 +18,11 @@ e2e       the same metric through rra_allreduce_host: host buffers in and out,
 roofline  the dominant kernel of the step against the measured HBM peak
 floor     measured single-GPU latency floor 2*L2_RTT + L_store->poll and the
           in-kernel time of the 128-byte calls
-bandwidth the two-shot kernels at N=8, 64 MiB and 512 MiB binary32 per rank,
-          GB/s of compulsory traffic (2*N*M) against the measured HBM peak
+bandwidth the two-shot kernels at N=8, 4 / 64 / 512 MiB per rank, binary32 and
+          binary64, GB/s of compulsory traffic (2*N*M) against the measured HBM
+          peak, L2 evicted between calls
+configs   N=2 128 B over 1000 back-to-back calls; N=64 1 KiB-256 KiB and an N
+          sweep at 16 KiB
 barrier_baseline  flag-barrier latency vs N, and the one-shot and two-shot
           barrier baselines beside their barrier-free counterparts (N=4)
 collectives ReduceScatter, AllGather, Broadcast, Reduce: N=4 latency (graph
@@ -324,6 +327,7 @@ def run_ours(args, world, rank, local):
     colls = collectives_table(rra, measure, torch, hbm_peak) if args.collectives else None
     barriers = barrier_table(rra, measure, torch) if args.barriers else None
     sweep = scratch_sweep(rra, measure, torch) if args.scratch_sweep else None
+    configs = configs_table(rra, measure, torch) if args.configs else None
     e2e = end_to_end(comm, rra, cases, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
 
@@ -363,6 +367,8 @@ def run_ours(args, world, rank, local):
         line["barrier_baseline"] = barriers
     if sweep is not None:
         line["scratch_sweep"] = sweep
+    if configs is not None:
+        line["configs"] = configs
     if rank == 0 and args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     comm.close()
@@ -467,39 +473,125 @@ def latency_floor(comm, rra, measure, torch, stream):
 
 
 def bandwidth_end(rra, measure, torch, hbm_peak, args):
-    """The two-shot kernels at N=8, binary32, inputs and outputs far larger
-    than L2 (4 GiB of inputs at 512 MiB per rank)."""
+    """Workload 5: N=8, binary32 and binary64 uniform(-1, 1), 4 / 64 / 512 MiB
+    per rank, the two-shot kernels.  Enough buffer sets are rotated that
+    each call's working set was evicted from L2 (more than 2x its 129 MB)."""
     out = {}
     n = 8
-    sizes = [64 << 20] + ([512 << 20] if args.big else [])
-    for size in sizes:
-        count = size // 4
-        gen = torch.Generator(device="cuda")
-        gen.manual_seed(5000 + size // (1 << 20))
-        with rra.Comm(n, size) as c:
-            xs = [torch.rand(count, device="cuda", generator=gen) * 2 - 1 for _ in range(n)]
-            ys = [torch.empty_like(x) for x in xs]
-            for algo in ("twoshot_dbuf", "twoshot_direct", "twoshot_cluster"):
-                for _ in range(2):
-                    c.allreduce(xs, ys, algo)
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                reps = 5
-                e0.record()
-                for _ in range(reps):
-                    c.allreduce(xs, ys, algo)
-                e1.record()
-                torch.cuda.synchronize()
-                st = c.status()[0]
-                t = e0.elapsed_time(e1) / 1000.0 / reps
-                gbs = measure.hbm_gbs(n, size, t)
-                out["%s/%dMiB" % (algo, size >> 20)] = {
-                    "ms": round(t * 1000, 3), "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
-                    "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1), "status": rra.STATUS_NAMES.get(st)}
-            del xs, ys
+    sizes = [4 << 20, 64 << 20] + ([512 << 20] if args.big else [])
+    for dtype in ("fp32", "fp64"):
+        es = 4 if dtype == "fp32" else 8
+        tdt = torch.float32 if dtype == "fp32" else torch.float64
+        algos = ("twoshot_dbuf", "twoshot_direct", "twoshot_cluster") if dtype == "fp32" else (
+            "twoshot_dbuf", "twoshot_cluster")
+        for size in sizes:
+            count = size // es
+            nsets = max(1, -(-(300 << 20) // (2 * n * size)))
+            gen = torch.Generator(device="cuda")
+            gen.manual_seed(5000 + size // (1 << 20) + es)
+            with rra.Comm(n, size) as c:
+                sets = []
+                for _ in range(nsets):
+                    xs = [(torch.rand(count, device="cuda", generator=gen) * 2 - 1).to(tdt) for _ in range(n)]
+                    sets.append((xs, [torch.empty_like(x) for x in xs]))
+                for algo in algos:
+                    for k in range(2):
+                        c.allreduce(*sets[k % nsets], algo)
+                    torch.cuda.synchronize()
+                    reps = max(5, nsets)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for k in range(reps):
+                        c.allreduce(*sets[k % nsets], algo)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    st = c.status()[0]
+                    t = e0.elapsed_time(e1) / 1000.0 / reps
+                    gbs = measure.hbm_gbs(n, size, t)
+                    out["%s/%s/%dMiB" % (algo, dtype, size >> 20)] = {
+                        "ms": round(t * 1000, 3), "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+                        "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1), "status": rra.STATUS_NAMES.get(st)}
+                del sets
             torch.cuda.empty_cache()
-    return {"nranks": n, "dtype": "fp32", "bytes": "2*N*M per call", "sizes": out,
-            "note": "inputs > L2; 5 calls after 2 warm-up, CUDA events; default chunking"}
+    return {"nranks": n, "bytes": "2*N*M per call", "sizes": out,
+            "note": "L2 evicted between calls (rotating buffer sets, >2x L2); CUDA events; default chunking"}
+
+
+def _graph_us(torch, measure, fn, calls=16, reps=20):
+    """Median microseconds per call of `fn` replayed `calls` times in a CUDA graph."""
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1000.0 / calls)
+    return round(measure.median(ts), 3)
+
+
+def configs_table(rra, measure, torch):
+    """The other configurations' own figures.  Config 1: N=2, 32 binary32
+    integers, 1000 back-to-back calls on distinct buffers in one graph.
+    Config 4: N=64, binary32, 1 KiB..256 KiB, and an N sweep at 16 KiB, with
+    each algorithm's scratch bytes per window (µs per call, graph replay)."""
+    from latency_barrier_free_gb300 import inputs
+
+    out = {}
+    calls = 1000
+    host = np.stack([np.stack(inputs.workload1(i)) for i in range(calls)])
+    send = torch.from_numpy(host).cuda()
+    recv = torch.empty_like(send)
+    c1 = {}
+    with rra.Comm(2, 128) as c:
+        for algo in ("oneshot_ll", "oneshot_sentinel", "oneshot_cluster", "auto"):
+            def step(algo=algo):
+                for i in range(calls):
+                    c.allreduce_ptrs([send[i, 0].data_ptr(), send[i, 1].data_ptr()],
+                                     [recv[i, 0].data_ptr(), recv[i, 1].data_ptr()], 32, "fp32", algo)
+            c1[algo] = round(_graph_us(torch, measure, step, calls=1, reps=5) / calls, 3)
+        assert c.status()[0] == rra.OK
+    exact = host.astype(np.int64).sum(axis=1).astype(np.float32)
+    out["config1_N2_128B_us_per_call"] = c1
+    out["config1_exact"] = bool(np.array_equal(recv.cpu().numpy()[:, 0], exact))
+    algos = ("oneshot_sentinel", "ll128_atomic", "auto")
+    c4 = {}
+    with rra.Comm(64, 256 << 10) as c:
+        lay = c.layout()
+        for size in inputs.W4_SIZES:
+            count = size // 4
+            xs = [torch.randn(count, device="cuda") for _ in range(64)]
+            ys = [torch.empty_like(x) for x in xs]
+            sp, yp = [t.data_ptr() for t in xs], [t.data_ptr() for t in ys]
+            for algo in algos:
+                c4["%s/%dB" % (algo, size)] = _graph_us(torch, measure, lambda: c.allreduce_ptrs(sp, yp, count, "fp32", algo))
+        assert c.status()[0] == rra.OK
+    out["config4_N64_us_per_call"] = c4
+    out["config4_scratch_bytes_per_window"] = {"oneshot_sentinel": lay["os_bytes"], "ll128_atomic": lay["la_bytes"],
+                                               "max_bytes": 256 << 10}
+    sweep = {}
+    for n in inputs.W4_NSWEEP:
+        count = (16 << 10) // 4
+        with rra.Comm(n, 16 << 10) as c:
+            xs = [torch.randn(count, device="cuda") for _ in range(n)]
+            ys = [torch.empty_like(x) for x in xs]
+            sp, yp = [t.data_ptr() for t in xs], [t.data_ptr() for t in ys]
+            for algo in algos + (("oneshot_cluster", "twoshot_cluster") if n <= 16 else ()):
+                sweep["N%d/%s" % (n, algo)] = _graph_us(torch, measure, lambda: c.allreduce_ptrs(sp, yp, count, "fp32", algo))
+            assert c.status()[0] == rra.OK
+    out["nsweep_16KiB_us_per_call"] = sweep
+    return out
 
 
 def barrier_table(rra, measure, torch):
@@ -850,6 +942,8 @@ def main():
                     help="skip the ReduceScatter/AllGather/Broadcast/Reduce table")
     ap.add_argument("--no-barriers", dest="barriers", action="store_false",
                     help="skip the barrier-baseline table")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the N=2 (1000 calls) and N=64 tables")
     ap.add_argument("--clock-log-dir", default=None,
                     help="directory for the raw nvidia-smi clock samples (default: the system temp directory)")
     ap.add_argument("--scratch-sweep", action="store_true",

@@ -81,20 +81,23 @@ typedef enum {
                                   registered symmetric buffers, Sec. II-B): RS as
                                   RRA_TWOSHOT_DBUF, no AG scratch, one hop per step */
     RRA_AUTO = 6,              /* pick by rank count and message size (rra_select_algo);
-                                  may pick a sentinel algorithm (N > 16, or when clusters
-                                  cannot be scheduled), so inputs must not hold the
-                                  all-ones pattern */
+                                  may pick a sentinel algorithm when clusters cannot be
+                                  scheduled, so inputs must not hold the all-ones
+                                  pattern */
     RRA_ONESHOT_CLUSTER = 7,   /* one-shot push through distributed shared memory: one
                                   thread-block cluster of N CTAs per slice (CTA r = rank r),
                                   st.async into peers' shared memory completes their
                                   mbarrier (arrival of the bytes is the signal); no state
-                                  between calls; N <= 16, any size */
+                                  between calls.  For N > 16 the clusters have 16 CTAs and
+                                  CTA j hosts ranks j, j+16, ... (pushes go to the 15 other
+                                  CTAs; still the rank-order sum of all N) */
     RRA_TWOSHOT_CLUSTER = 8,   /* two-shot through distributed shared memory: rank r pushes
                                   partition q of its slice to CTA q only (ReduceScatter),
                                   CTA q adds the N contributions in rank order and stores
                                   the result into every rank's output (AllGather as direct
                                   stores, as RRA_TWOSHOT_DIRECT); HBM carries only the
-                                  inputs read once and the outputs written once; N <= 16 */
+                                  inputs read once and the outputs written once.  N > 16:
+                                  16-CTA clusters, CTA q reduces part q over all N ranks */
     RRA_TWOSHOT_BARRIER = 9    /* BASELINE, not barrier-free: two-shot with plain stores and
                                   two flag barriers per step (ReduceScatter, barrier, reduce
                                   + AllGather stores, barrier, gather; Sec. III-B's design
@@ -209,9 +212,8 @@ rra_status_t rra_comm_create(int nranks, size_t max_bytes, rra_comm_t* out);
  * `stream` completes.  RRA_ONESHOT_SENTINEL and RRA_TWOSHOT_DBUF require
  * that no input element has the all-ones bit pattern (the sentinel, a
  * negative NaN, Sec. IV "Sentinel"); such an input makes the call time out.
- * The cluster algorithms take nranks <= 16 (RRA_ERR_INVALID_ARG above that)
- * and return RRA_ERR_NOT_CORESIDENT if the device cannot schedule a cluster
- * of nranks CTAs with a 96 KiB stage each.
+ * The cluster algorithms return RRA_ERR_NOT_CORESIDENT if the device cannot
+ * schedule a cluster of min(nranks, 16) CTAs with a 96 KiB stage each.
  * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_POISONED, RRA_ERR_CUDA,
  * RRA_ERR_NOT_CORESIDENT.
  */
@@ -343,15 +345,13 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
  * host arithmetic).  The paper picks its kernel from measured crossovers in
  * message size and rank count (one-shot for small messages, two-shot once
  * they reach about a mebibyte at four ranks); these thresholds are the
- * crossovers measured on GB300 with CUDA-graph replay:
- *   nranks <= 16: the cluster one-shot while nranks^2 * bytes <= 1 MiB (its
- *                 shared-memory traffic is N (N-1) M), the cluster two-shot
- *                 above;
- *   nranks >= 17: one-shot sentinel up to 4 KiB, LL128-atomic up to 16 KiB
- *                 (64 KiB at N = 64), the direct two-shot above.
- * If the device cannot schedule a cluster of nranks CTAs, RRA_AUTO uses the
- * choice without cluster kernels: one-shot sentinel while
- * nranks * bytes <= 1.5 MiB (N <= 8), else as for nranks >= 17. */
+ * crossovers measured on GB300 with CUDA-graph replay: the cluster one-shot
+ * while min(nranks, 16) * nranks * bytes <= 1 MiB (its shared-memory
+ * traffic), the cluster two-shot above, for every nranks up to 64.
+ * If the device cannot schedule the cluster shape, RRA_AUTO uses the choice
+ * without cluster kernels: one-shot sentinel while nranks * bytes <= 1.5 MiB
+ * (N <= 8); for N > 8 one-shot sentinel up to 4 KiB, LL128-atomic up to
+ * 16 KiB (64 KiB at N = 64), the direct two-shot above. */
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out);
 
 /* Number of CTAs the next call of (count, dtype, algo) would launch, and the

@@ -185,6 +185,122 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     if (tr) tr[5] = globaltimer_ns();
 }
 
+// More ranks than CTAs in a cluster (N > 16): CTA j of a cluster of G = 16
+// CTAs hosts ranks j, j + G, j + 2G, ... (< N), reading each hosted rank's
+// input and writing each hosted rank's output.  A window holds a slot per
+// rank; a push goes to the G - 1 other CTAs (every rank they host sees the
+// same window), and the reduction still adds all N slots in rank order.
+//   one-shot: each CTA receives every other rank's slice and reduces it;
+//   two-shot: the slice is cut into G parts, CTA q reduces part q over all N
+//             ranks and stores it into every rank's output (direct).
+template <typename T, bool kTwoShot>
+__global__ void __launch_bounds__(256) cluster_multi_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t G = (uint32_t)kClusterMaxRanks;
+    const uint32_t j = cluster_ctarank();
+    const uint32_t hosted = (N - j + G - 1) / G;  // ranks j, j + G, ...
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = kTwoShot ? S / G : S;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint32_t mine = kTwoShot ? (npos > j * Q ? min(Q, npos - j * Q) : 0u) : npos;
+
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, (N - hosted) * mine * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    // item it = (hosted rank m, vector v)
+    const uint32_t items = hosted * npos;
+    uint4 x[kClusterBatch];
+    auto load_batch = [&](uint32_t b0) {
+#pragma unroll
+        for (int k = 0; k < kClusterBatch; ++k) {
+            const uint32_t it = b0 + threadIdx.x + (uint32_t)k * nt;
+            if (it >= items) continue;
+            const uint32_t m = it / npos;
+            x[k] = load_input<T>(p.send[j + m * G], base + (it - m * npos), p.count);
+        }
+    };
+    load_batch(0);
+    cluster_wait();  // every peer's barrier exists before anyone stores into it
+
+    const uint32_t step = nt * (uint32_t)kClusterBatch;
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < items; b0 += step) {
+        if (b0 != 0) load_batch(b0);
+#pragma unroll
+        for (int k = 0; k < kClusterBatch; ++k) {
+            const uint32_t it = b0 + threadIdx.x + (uint32_t)k * nt;
+            if (it >= items) continue;
+            const uint32_t m = it / npos;
+            const uint32_t v = it - m * npos;
+            const uint32_t rank = j + m * G;
+            const bool pushes = drop != (int32_t)rank;
+            if (kTwoShot) {
+                const uint32_t q = v / Q;
+                const uint32_t u = v - q * Q;
+                if (q == j) stage[rank * Q + u] = x[k];
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(stage + rank * Q + u), q), x[k], map_to_rank(my_bar, q));
+            } else {
+                if (pushes) {
+#pragma unroll 1
+                    for (uint32_t c = 1; c < G; ++c) {
+                        const uint32_t q = j + c < G ? j + c : j + c - G;
+                        st_async_v4(map_to_rank(smem_u32(stage + rank * Q + v), q), x[k], map_to_rank(my_bar, q));
+                    }
+                }
+                stage[rank * Q + v] = x[k];
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)j, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    __syncthreads();  // the hosted ranks' slots were written by other threads
+    if (ok) {
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * Q + u]);
+            const uint4 out = M::store(acc);
+            if (kTwoShot) {
+#pragma unroll 1
+                for (uint32_t d = 0; d < N; ++d) store_output<T>(p.recv[d], base + j * Q + u, p.count, out);
+            } else {
+#pragma unroll 1
+                for (uint32_t m = 0; m < hosted; ++m) store_output<T>(p.recv[j + m * G], base + u, p.count, out);
+            }
+        }
+    }
+    if (!__all_sync(0xffffffffu, ok)) cluster_wait();  // a thread whose wait ran out keeps the memory alive
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 // Persistent, double-buffered two-shot (the pages' double buffering, Sec. IV,
 // in which receiving from a peer is what permits the next send to it,
 // restated with mbarriers).  Cluster c handles
@@ -322,6 +438,8 @@ static const void* cluster_kernel_for(int mode) {
         case kClusterOneshot: return (const void*)cluster_kernel<T, false>;
         case kClusterTwoshot: return (const void*)cluster_kernel<T, true>;
         case kClusterTwoshotPipe: return (const void*)cluster_pipe_kernel<T>;
+        case kClusterOneshotMulti: return (const void*)cluster_multi_kernel<T, false>;
+        case kClusterTwoshotMulti: return (const void*)cluster_multi_kernel<T, true>;
     }
     return nullptr;
 }
@@ -338,7 +456,7 @@ static const void* cluster_kernel_ptr(rra_dtype_t dtype, int mode) {
 // Opt the kernel in to the full stage and to clusters of up to 16 CTAs
 // (once per kernel; the attributes are process-wide).
 static cudaError_t configure(const void* k) {
-    static const void* done[16] = {};
+    static const void* done[24] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
@@ -359,29 +477,42 @@ size_t cluster_stage_bytes(const Params& p, int mode) {
         case kClusterOneshot: return n * p.per_cta * kVecBytes;
         case kClusterTwoshot: return (size_t)p.per_cta / n * n * kVecBytes;
         case kClusterTwoshotPipe: return 2 * ((size_t)p.per_cta / n * n) * kVecBytes;
+        case kClusterOneshotMulti: return n * p.per_cta * kVecBytes;
+        case kClusterTwoshotMulti: return n * ((size_t)p.per_cta / kClusterMaxRanks) * kVecBytes;
     }
     return 0;
 }
 
+// CTAs per cluster: one per rank, or 16 hosting several ranks each.
+static unsigned cluster_ctas(int mode, int nranks) {
+    return (mode == kClusterOneshotMulti || mode == kClusterTwoshotMulti) ? (unsigned)kClusterMaxRanks
+                                                                          : (unsigned)nranks;
+}
+
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl) {
     const size_t smem = cluster_stage_bytes(p, mode);
-    if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks)
+    const bool multi = mode == kClusterOneshotMulti || mode == kClusterTwoshotMulti;
+    if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > (multi ? kMaxRanks : kClusterMaxRanks))
         return cudaErrorInvalidValue;
-    if (mode != kClusterOneshot && p.per_cta % (uint32_t)p.nranks != 0) return cudaErrorInvalidValue;
+    if (multi && p.nranks <= kClusterMaxRanks) return cudaErrorInvalidValue;
+    if ((mode == kClusterTwoshot || mode == kClusterTwoshotPipe) && p.per_cta % (uint32_t)p.nranks != 0)
+        return cudaErrorInvalidValue;
+    if (mode == kClusterTwoshotMulti && p.per_cta % (uint32_t)kClusterMaxRanks != 0) return cudaErrorInvalidValue;
     if (mode == kClusterTwoshotPipe && p.per_cta > (uint32_t)threads * kClusterBatch) return cudaErrorInvalidValue;
     const void* k = cluster_kernel_ptr(dtype, mode);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = configure(k);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.nranks * p.ctas_per_rank));
+    const unsigned cdim = cluster_ctas(mode, p.nranks);
+    cfg.gridDim = dim3(cdim * (unsigned)p.ctas_per_rank);
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)p.nranks;
+    attr[n].val.clusterDim.x = cdim;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -406,12 +537,13 @@ int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, siz
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)nranks);
+    const unsigned cdim = cluster_ctas(mode, nranks);
+    cfg.gridDim = dim3(cdim);
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)nranks;
+    attr.val.clusterDim.x = cdim;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;

@@ -102,6 +102,7 @@ struct rra_comm {
     int64_t cluster_pipe = 0;               // persistent cluster two-shot: -1 auto, 0 never (default), 1 always
     int64_t host_zero_copy = 1;             // rra_allreduce_host: run on mapped pinned buffers directly
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
+    int cluster_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
     int coll_fits[6][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1},
                            {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
@@ -149,14 +150,11 @@ static rra_algo_t select_global(int nranks, size_t bytes) {
 
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out) {
     if (out == nullptr || nranks < 2 || nranks > RRA_MAX_RANKS || !valid_dtype(dtype)) return RRA_ERR_INVALID_ARG;
-    if (nranks <= rra::kClusterMaxRanks) {
-        // one-shot while its shared-memory traffic N (N-1) M stays small:
-        // N^2 M <= 1 MiB (GB300 sweep, N = 2..16); two-shot above
-        const size_t n2m = (size_t)nranks * (size_t)nranks * bytes;
-        *out = n2m <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
-    } else {
-        *out = select_global(nranks, bytes);
-    }
+    // Cluster kernels at every N (16-CTA clusters hosting several ranks each
+    // above 16): the one-shot while its shared-memory traffic stays small,
+    // min(N, 16) N M <= 1 MiB (GB300 sweeps, N = 2..64), the two-shot above.
+    const size_t g = (size_t)std::min(nranks, rra::kClusterMaxRanks);
+    *out = g * (size_t)nranks * bytes <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
     return RRA_OK;
 }
 
@@ -398,6 +396,55 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
     return RRA_ERR_INVALID_ARG;
 }
 
+// More ranks than a cluster holds (N > 16): clusters of 16 CTAs, CTA j
+// hosting ranks j, j + 16, ...; one cluster per slice of S vectors.  A
+// window holds N slots: N x S vectors (one-shot) or N x S/16 (two-shot, S a
+// multiple of 16) within the 96 KiB stage.  S: the whole message while it
+// fits one slice (one-shot) or, for the two-shot, about two CTAs per SM.
+static rra_status_t plan_cluster_multi(rra_comm* c, size_t count, rra_dtype_t dtype, bool two, Params* p,
+                                       int* threads, int* mode) {
+    const size_t n = (size_t)c->nranks;
+    const size_t g = (size_t)rra::kClusterMaxRanks;
+    const int kmode = two ? rra::kClusterTwoshotMulti : rra::kClusterOneshotMulti;
+    int& fits = c->cluster_multi_fits[two ? 1 : 0][(int)dtype];
+    if (fits < 0) fits = rra::cluster_max_active(dtype, kmode, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
+    if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
+    const size_t ve = rra::kVecBytes / elem_size(dtype);
+    memset(p, 0, sizeof(*p));
+    p->win0 = c->win0;
+    p->ctrl = c->ctrl;
+    p->timing = c->timing;
+    p->trace = c->trace;
+    p->stride = c->lay.window_stride;
+    p->count = count;
+    p->nvec = (uint32_t)ceil_div(count, ve);
+    p->timeout_ns = (uint64_t)c->timeout_ms * 1000000ull;
+    p->nranks = c->nranks;
+    p->nsteps = 1;
+    p->chunk_vecs = p->nvec;
+    p->epoch_slots = rra::kEpochSlots;
+    const size_t stage_vecs = rra::kClusterStageBytes / rra::kVecBytes;
+    const size_t smax = two ? (stage_vecs / n) * g : stage_vecs / n;  // N x S (one-shot), N x S/16 (two-shot)
+    size_t S;
+    if (c->cluster_slice > 0) {
+        S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else if (two) {
+        const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / g);
+        S = std::max<size_t>(g, ceil_div(p->nvec, target));
+    } else {
+        S = p->nvec;
+    }
+    if (two) S = align_up(S, g);
+    S = std::max<size_t>(two ? g : 1, std::min(S, smax));
+    p->per_cta = (uint32_t)S;
+    p->ctas_per_rank = (int32_t)ceil_div(p->nvec, S);  // clusters (slices)
+    const size_t hosted = ceil_div(n, g);
+    const size_t cap = c->threads_set ? (size_t)c->threads : 256;
+    *threads = (int)std::min<size_t>(cap, std::max<size_t>(32, align_up(S * hosted, 32)));
+    *mode = kmode;
+    return RRA_OK;
+}
+
 // Plan of a cluster call: one cluster of N CTAs per slice of S vectors, CTA
 // r of a cluster = rank r.  S: one position per thread while the message is
 // small; past that, about two CTAs per SM in one wave, up to one batch of
@@ -412,7 +459,7 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
                                  int* threads, int* mode) {
     const bool two = algo == RRA_TWOSHOT_CLUSTER;
     const size_t n = (size_t)c->nranks;
-    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
+    if (c->nranks > rra::kClusterMaxRanks) return plan_cluster_multi(c, count, dtype, two, p, threads, mode);
     int& fits = c->cluster_fits[two ? 1 : 0][(int)dtype];
     if (fits < 0)
         fits = rra::cluster_max_active(dtype, two ? rra::kClusterTwoshot : rra::kClusterOneshot, c->nranks, 256,
@@ -725,7 +772,8 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
         st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
     }
     if (st != RRA_OK) return st;
-    if (grid_ctas) *grid_ctas = p.nranks * p.ctas_per_rank;
+    const bool multi = is_cluster(algo) && (kind == rra::kClusterOneshotMulti || kind == rra::kClusterTwoshotMulti);
+    if (grid_ctas) *grid_ctas = (multi ? rra::kClusterMaxRanks : p.nranks) * p.ctas_per_rank;
     if (steps) *steps = (int)p.nsteps;
     return RRA_OK;
 }

@@ -102,7 +102,10 @@ cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_
 // two-shot).  kClusterOneshot / kClusterTwoshot: p.ctas_per_rank slices, one
 // cluster each.  kClusterTwoshotPipe: p.ctas_per_rank persistent clusters
 // over p.nsteps slices of at most threads * kClusterBatch vectors.
-enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2 };
+// kClusterOneshotMulti / kClusterTwoshotMulti: N > 16, clusters of 16 CTAs,
+// CTA j hosting ranks j, j + 16, ...; the two-shot's slice is a multiple of 16.
+enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2, kClusterOneshotMulti = 3,
+       kClusterTwoshotMulti = 4 };
 size_t cluster_stage_bytes(const Params& p, int mode);
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl);
 int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem);

@@ -117,11 +117,14 @@ def test_auto_selection_by_size_and_ranks():
     assert rra.select_algo(8, 1 << 20, "bf16") == "twoshot_cluster"
     assert rra.select_algo(16, 4 << 10) == "oneshot_cluster"
     assert rra.select_algo(16, 64 << 10) == "twoshot_cluster"
-    assert rra.select_algo(17, 1 << 10) == "oneshot_sentinel"
-    assert rra.select_algo(64, 1 << 10) == "oneshot_sentinel"
-    assert rra.select_algo(64, 64 << 10) == "ll128_atomic"
-    assert rra.select_algo(32, 16 << 10) == "ll128_atomic"
-    assert rra.select_algo(64, 1 << 20) == "twoshot_direct"
+    # above 16 ranks: 16-CTA clusters hosting several ranks each; min(N, 16) N M <= 1 MiB
+    assert rra.select_algo(17, 1 << 10) == "oneshot_cluster"
+    assert rra.select_algo(64, 1 << 10) == "oneshot_cluster"
+    assert rra.select_algo(64, (1 << 10) + 16) == "twoshot_cluster"
+    assert rra.select_algo(32, 2 << 10) == "oneshot_cluster"
+    assert rra.select_algo(64, 64 << 10) == "twoshot_cluster"
+    assert rra.select_algo(32, 16 << 10) == "twoshot_cluster"
+    assert rra.select_algo(64, 1 << 20) == "twoshot_cluster"
     twoshot = ("twoshot_cluster", "twoshot_direct")
     for n in (2, 4, 8, 16, 17, 64):  # once two-shot, always two-shot as the message grows
         picks = [rra.select_algo(n, 1 << k) for k in range(4, 31)]

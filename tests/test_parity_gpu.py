@@ -276,7 +276,7 @@ def test_auto_algorithm(n):
 
 @pytest.mark.parametrize("algo", CLUSTER)
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 17, 32, 64])
 def test_cluster_kernels(n, dtype, algo):
     """One-shot and two-shot through distributed shared memory (one cluster
     of N CTAs per slice): bit-exact, for ragged sizes (two-shot partitions
@@ -349,9 +349,15 @@ def test_cluster_rank_sweep(algo):
 
 
 @pytest.mark.parametrize("algo", CLUSTER)
-def test_cluster_rejects_too_many_ranks(algo):
-    with rra.Comm(17, 4096) as comm:
-        x = [torch.zeros(16, device="cuda") for _ in range(17)]
-        with pytest.raises(rra.RraError) as e:
-            comm.allreduce(x, x, algo)
-        assert e.value.status == rra.ERR_INVALID_ARG
+@pytest.mark.parametrize("n", [20, 33, 48])
+def test_cluster_more_ranks_than_ctas(n, algo):
+    """N > 16: clusters of 16 CTAs, CTA j hosting ranks j, j + 16, ...
+    (uneven: some CTAs host one more rank); slices from one vector to the
+    stage limit; bit-exact."""
+    count = 50000 + 3
+    with rra.Comm(n, count * 4) as comm:
+        for slice_bytes in (0, 16 * 16, 4096):
+            comm.set_attr("cluster_slice", slice_bytes)
+            sends_np = inputs.normal(inputs.rng(76, n, slice_bytes), n, count, "fp32")
+            got = run(comm, sends_np, "fp32", algo)
+            check_against_oracle(sends_np, got, "fp32", algo)

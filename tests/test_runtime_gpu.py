@@ -84,6 +84,26 @@ def test_timeout_poison_and_reset(algo):
         check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
 
 
+@pytest.mark.parametrize("algo", CLUSTER)
+def test_cluster_many_ranks_timeout_and_reset(algo):
+    """N=32 (16-CTA clusters hosting two ranks each) with a dropped rank:
+    RRA_ERR_TIMEOUT, no hang; correct after a reset."""
+    n, count = 32, 4000
+    sends_np = inputs.normal(inputs.rng(77, 0), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("poll_timeout_ms", 20)
+        comm.inject_drop(21)
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        assert comm.status()[0] == rra.ERR_TIMEOUT
+        comm.reset()
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+
+
 def test_pipelined_cluster_timeout_and_reset():
     """The persistent cluster two-shot with a rank that drops its pushes:
     waits on data and on credits run out, RRA_ERR_TIMEOUT is recorded, and
