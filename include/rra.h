@@ -117,8 +117,9 @@ typedef enum {
                                       in L2), within the per-window scratch cap */
     RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step; 0 = as above */
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
-    RRA_ATTR_ONESHOT_WIDE = 6,     /* one-shot polls split a position's sources over
-                                      threads: -1 auto (N >= 16, default), 0 off, 1 on */
+    RRA_ATTR_ONESHOT_WIDE = 6,     /* the one-shot's polls and the LL128-atomic kernel's adds
+                                      and polls split a position's sources over threads:
+                                      -1 auto (N >= 16, default), 0 off, 1 on */
     RRA_ATTR_COOPERATIVE = 7,      /* 1 (default): cooperative launch, so the driver
                                       guarantees that all CTAs are resident together;
                                       0: plain launch of the same occupancy-checked grid

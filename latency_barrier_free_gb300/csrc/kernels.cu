@@ -1078,6 +1078,160 @@ __device__ __forceinline__ bool ll128_body(const Params& p, const CtaState& s) {
     return true;
 }
 
+// Wide variant for many ranks: the threads of a CTA split the (owner q,
+// position v) items of the ReduceScatter's atomic adds and of the AllGather's
+// polls, so a small partition no longer leaves one thread walking the N-1
+// owners in order.  The counter of a group (32 positions, inside one CTA) is
+// incremented once per contributing rank after a CTA-wide release: every
+// thread fences its adds, the CTA meets, then one thread per (owner, group)
+// increments.  Same owner phase and results as ll128_body.
+template <typename T>
+__device__ __forceinline__ bool ll128_wide_body(const Params& p, const CtaState& s) {
+    using A = Acc128<T>;
+    constexpr uint32_t kAccBytes = (uint32_t)kVecBytes * A::kRatio;
+    const int N = p.nranks, r = s.rank;
+    const uint32_t nt = blockDim.x;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t wbase = threadIdx.x - lane;
+    const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;  // per_cta is a multiple of 32
+    const uint32_t pos1 = pos0 + p.per_cta;
+    char* const mine = window(p, r);
+    Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
+    const uint32_t target = (uint32_t)(N - 1);
+
+#pragma unroll 1
+    for (uint32_t k = 0; k < p.nsteps; ++k) {
+        const uint64_t e = s.epoch + k;
+        const uint32_t ep = (uint32_t)e;
+        const uint64_t par = e & 1ull;
+        const Split sp = split_step(p, k);
+        const uint32_t end = min(pos1, sp.part);
+        const uint32_t np = end > pos0 ? end - pos0 : 0u;  // this CTA's positions in this step
+        const uint32_t items = (uint32_t)N * np;           // (owner q, position) pairs
+        w.step = (int)k;
+        if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
+
+        // ReduceScatter: atomic adds, one item per thread and batch
+        if (!s.drop) {
+#pragma unroll 1
+            for (uint32_t b0 = 0; b0 < items; b0 += nt * (uint32_t)kLoadParts) {
+                uint4 x[kLoadParts];
+#pragma unroll
+                for (int j = 0; j < kLoadParts; ++j) {
+                    const uint32_t it = b0 + threadIdx.x + (uint32_t)j * nt;
+                    if (it >= items) continue;
+                    const int q = (int)(it / np);
+                    const uint32_t v = pos0 + (it - (uint32_t)q * np);
+                    if (q != r && v < sp.valid(q)) x[j] = load_input<T>(p.send[r], sp.vec(q, v), p.count);
+                }
+#pragma unroll
+                for (int j = 0; j < kLoadParts; ++j) {
+                    const uint32_t it = b0 + threadIdx.x + (uint32_t)j * nt;
+                    if (it >= items) continue;
+                    const int q = (int)(it / np);
+                    const uint32_t v = pos0 + (it - (uint32_t)q * np);
+                    if (q != r && v < sp.valid(q))
+                        A::red(window(p, q) + p.region_off + par * p.parity_bytes + (uint64_t)v * kAccBytes, x[j]);
+                }
+            }
+            fence_acq_rel_gpu();  // release: this thread's adds before any counter increment
+            __syncthreads();
+            const uint32_t g_first = pos0 / kGroupVecs;
+            const uint32_t ng = np == 0 ? 0u : (end - 1) / kGroupVecs - g_first + 1;
+#pragma unroll 1
+            for (uint32_t it = threadIdx.x; it < (uint32_t)N * ng; it += nt) {
+                const int q = (int)(it / ng);
+                const uint32_t g = g_first + (it - (uint32_t)q * ng);
+                if (q == r || g * kGroupVecs >= sp.valid(q)) continue;
+                red_add_u32(window(p, q) + p.aux_off + par * p.aux_parity_bytes + (uint64_t)g * 4, 1u);
+            }
+        }
+        // Owner: per group (a warp), wait for the counter, consume, re-zero,
+        // AllGather push.  A warp that gives up stops; the CTA decides below.
+        int failed = 0;
+        const uint32_t my_end = min(end, sp.valid(r));
+#pragma unroll 1
+        for (uint32_t g0 = pos0 + wbase; g0 < my_end; g0 += nt) {
+            char* const cnt = mine + p.aux_off + par * p.aux_parity_bytes + (uint64_t)(g0 / kGroupVecs) * 4;
+            int give_up = 0;
+            if (lane == 0) {
+                while (ld_relaxed_u32(cnt) != target) {
+                    if (waiter_expired(w)) { give_up = 1; break; }
+                }
+                fence_acq_rel_gpu();  // acquire: the counter before the lines
+            }
+            if (__shfl_sync(0xFFFFFFFFu, give_up, 0)) {
+                failed = 1;
+                break;
+            }
+            __syncwarp();
+            const uint32_t v = g0 + lane;
+            if (v < my_end) {
+                char* const acc = mine + p.region_off + par * p.parity_bytes + (uint64_t)v * kAccBytes;
+                const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
+                const uint4 red = A::finish(acc, own);
+                A::zero(acc);
+                if (!s.drop) {
+                    char* dst = p.win0 + p.aux2_off + par * p.aux2_parity_bytes + (uint64_t)r * p.aux2_slot_bytes +
+                                (uint64_t)v * (2 * kVecBytes);
+#pragma unroll 1
+                    for (int q = 0; q < N; ++q, dst += p.stride) {
+                        if (q != r) ll_store(dst, red, ep);
+                    }
+                }
+                store_output<T>(p.recv[r], sp.vec(r, v), p.count, red);
+            }
+            __syncwarp();
+            if (lane == 0) st_relaxed_u32(cnt, 0u);
+        }
+        if (__syncthreads_or(failed)) return false;
+        // AllGather receive: (owner q, position v) items spread over the CTA
+#pragma unroll 1
+        for (uint32_t b0 = 0; b0 < items && !failed; b0 += nt * (uint32_t)kBatch) {
+            uint4 val[kBatch];
+            bool ok[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const uint32_t it = b0 + threadIdx.x + (uint32_t)j * nt;
+                ok[j] = true;
+                if (it >= items) continue;
+                const int q = (int)(it / np);
+                const uint32_t v = pos0 + (it - (uint32_t)q * np);
+                if (q != r && v < sp.valid(q))
+                    ok[j] = ll_load(mine + p.aux2_off + par * p.aux2_parity_bytes + (uint64_t)q * p.aux2_slot_bytes +
+                                        (uint64_t)v * (2 * kVecBytes),
+                                    ep, val[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const uint32_t it = b0 + threadIdx.x + (uint32_t)j * nt;
+                if (it >= items) continue;
+                const int q = (int)(it / np);
+                const uint32_t v = pos0 + (it - (uint32_t)q * np);
+                if (q == r || v >= sp.valid(q)) continue;
+                const char* const slot = mine + p.aux2_off + par * p.aux2_parity_bytes +
+                                         (uint64_t)q * p.aux2_slot_bytes + (uint64_t)v * (2 * kVecBytes);
+                while (!ok[j] && !failed) {
+                    if (waiter_expired(w)) failed = 1;
+                    else ok[j] = ll_load(slot, ep, val[j]);
+                }
+                if (ok[j]) store_output<T>(p.recv[r], sp.vec(q, v), p.count, val[j]);
+            }
+        }
+        if (__syncthreads_or(failed)) return false;
+    }
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) ll128_wide_kernel(const __grid_constant__ Params p) {
+    pdl_entry();
+    CtaState s = cta_prologue(p);
+    s.skip = __syncthreads_or(s.skip) != 0;  // CTA-wide syncs follow: skip must be CTA-uniform
+    if (!s.skip) (void)ll128_wide_body<T>(p, s);
+    cta_epilogue(p, s);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) ll128_kernel(const __grid_constant__ Params p) {
     pdl_entry();
@@ -1137,6 +1291,7 @@ static const void* kernel_for(int kind) {
         case kKindTwoshot: return (const void*)twoshot_kernel<T, false>;
         case kKindTwoshotDirect: return (const void*)twoshot_kernel<T, true>;
         case kKindLL128: return (const void*)ll128_kernel<T>;
+        case kKindLL128Wide: return (const void*)ll128_wide_kernel<T>;
         case kKindOneshotLLWide: return (const void*)oneshot_wide_kernel<T, true>;
         case kKindOneshotSentinelWide: return (const void*)oneshot_wide_kernel<T, false>;
         case kKindOneshotBarrier: return (const void*)oneshot_barrier_kernel<T>;

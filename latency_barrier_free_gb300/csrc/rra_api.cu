@@ -583,10 +583,10 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
 }
 
 static int kernel_kind(const rra_comm* c, rra_algo_t algo) {
-    if (algo == RRA_ONESHOT_LL || algo == RRA_ONESHOT_SENTINEL) {
-        const bool wide = c->oneshot_wide == 1 || (c->oneshot_wide < 0 && c->nranks >= 16);
-        if (wide) return algo == RRA_ONESHOT_LL ? rra::kKindOneshotLLWide : rra::kKindOneshotSentinelWide;
-    }
+    const bool wide = c->oneshot_wide == 1 || (c->oneshot_wide < 0 && c->nranks >= 16);
+    if (wide && (algo == RRA_ONESHOT_LL || algo == RRA_ONESHOT_SENTINEL))
+        return algo == RRA_ONESHOT_LL ? rra::kKindOneshotLLWide : rra::kKindOneshotSentinelWide;
+    if (wide && algo == RRA_LL128_ATOMIC) return rra::kKindLL128Wide;
     return (int)algo;
 }
 
@@ -737,9 +737,12 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     if (algo == RRA_ONESHOT_BARRIER || algo == RRA_TWOSHOT_BARRIER)
         cap_ctas = std::min<int64_t>(cap_ctas, rra::kBarrierCtas);
     const bool wide = kind == rra::kKindOneshotLLWide || kind == rra::kKindOneshotSentinelWide;
-    // positions per CTA to aim for: one per thread, or, for the wide variant,
-    // as many as one shared-memory stage round holds
-    const size_t target = wide ? std::max<size_t>(32, (size_t)rra::kWideStageVecs / n) : T;
+    const bool wide_la = kind == rra::kKindLL128Wide;
+    // positions per CTA to aim for: one per thread; for the wide one-shot, as
+    // many as one shared-memory stage round holds; for the wide LL128-atomic,
+    // about 8 (owner, position) items per thread
+    const size_t target = wide ? std::max<size_t>(32, (size_t)rra::kWideStageVecs / n)
+                               : wide_la ? std::max<size_t>(32, 8 * T / n) : T;
     if (c->ctas_per_rank > 0) ctas = std::min<int64_t>(c->ctas_per_rank, cap_ctas);
     else ctas = std::min<int64_t>((int64_t)ceil_div(work, target), cap_ctas);
     ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)work));
@@ -752,7 +755,8 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     // retire); never below 64 threads (the barrier baseline needs one thread
     // per rank), never above the occupancy-checked size.
     int threads = (int)T;
-    if (!wide) threads = (int)std::min<size_t>(T, std::max<size_t>(64, align_up(per, 32)));
+    if (wide_la) threads = (int)std::min<size_t>(T, std::max<size_t>(64, align_up(n * std::min(per, work), 32)));
+    else if (!wide) threads = (int)std::min<size_t>(T, std::max<size_t>(64, align_up(per, 32)));
     *threads_out = threads;
     return RRA_OK;
 }

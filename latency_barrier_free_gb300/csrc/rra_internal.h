@@ -71,8 +71,9 @@ struct Params {
     int32_t root;          // Broadcast / Reduce: the root rank
 };
 
-// Kernel kinds: the four algorithms (same values as rra_algo_t) plus the
-// wide one-shot variants that split a position's sources over threads.
+// Kernel kinds: the algorithms (same values as rra_algo_t) plus the wide
+// one-shot and LL128-atomic variants that split a position's sources over
+// threads.
 enum KernelKind {
     kKindOneshotLL = RRA_ONESHOT_LL,
     kKindOneshotSentinel = RRA_ONESHOT_SENTINEL,
@@ -84,7 +85,8 @@ enum KernelKind {
     kKindOneshotSentinelWide = 7,
     kKindBarrierProbe = 8,
     kKindTwoshotBarrier = RRA_TWOSHOT_BARRIER,
-    kNumKinds = 10
+    kKindLL128Wide = 10,
+    kNumKinds = 11
 };
 constexpr int kBarrierCtas = 64;  // CTAs per rank of the barrier baseline (flag slots per window)
 constexpr int kWideStageVecs = 3072;  // wide one-shot: shared-memory stage, in 16-byte vectors

@@ -238,6 +238,30 @@ def test_oneshot_wide_and_narrow_variants(algo, wide, n):
             check_against_oracle(sends_np, got, dtype, algo)
 
 
+@pytest.mark.parametrize("wide", [0, 1])
+@pytest.mark.parametrize("n", [2, 5, 16, 64])
+def test_ll128_wide_and_narrow_variants(wide, n):
+    """Both LL128-atomic variants (a thread walks a position's owners / the
+    CTA's threads split the (owner, position) items of the atomic adds and
+    of the AllGather polls) stay within the atomic-order bound, single-step
+    and multi-step, for every dtype; ragged partitions and tails."""
+    for dtype, counts in (("fp32", (1, 33, 4097, 70001)), ("bf16", (7, 5000)), ("fp64", (3, 3001))):
+        with rra.Comm(n, 70001 * 4) as comm:
+            comm.set_attr("oneshot_wide", wide)
+            for count in counts:
+                sends_np = inputs.normal(inputs.rng(66, count, n, wide), n, count, dtype)
+                got = run(comm, sends_np, dtype, "ll128_atomic")
+                check_against_oracle(sends_np, got, dtype, "ll128_atomic")
+            comm.set_attr("ll128_chunk", 16 * 40 * n)  # 40 positions per owner and step
+            comm.set_attr("ctas_per_rank", 2)
+            count = 16 * 40 * n * 3 // ELEM[dtype] + 5
+            _, steps = comm.plan_call(count, dtype, "ll128_atomic")
+            assert steps >= 3
+            sends_np = inputs.normal(inputs.rng(67, n, wide), n, count, dtype)
+            got = run(comm, sends_np, dtype, "ll128_atomic")
+            check_against_oracle(sends_np, got, dtype, "ll128_atomic")
+
+
 @pytest.mark.parametrize("algo", ["oneshot_barrier", "twoshot_barrier"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
 def test_barrier_baseline_parity(dtype, algo):
