@@ -695,14 +695,13 @@ def collective_bytes(op, n, m):
 
 def collectives_table(rra, measure, torch, hbm_peak):
     """ReduceScatter, AllGather, Broadcast (root 0) and Reduce (root 0):
-    N=4 latency (CUDA-graph replay of 16 calls, L2-resident buffers) at 128 B,
-    64 KiB and 1 MiB per block, and N=8 bandwidth (inputs and outputs far
-    beyond L2) at 16 MiB blocks (ReduceScatter, AllGather) / 64 MiB
-    (Broadcast, Reduce), binary32."""
-    lat = {}
-    n = 4
+    latency (CUDA-graph replay of 16 calls, L2-resident buffers) at N=4 with
+    128 B, 64 KiB and 1 MiB per block and at N=64 with 1 KiB and 16 KiB, and
+    N=8 bandwidth (inputs and outputs far beyond L2) at 16 MiB blocks
+    (ReduceScatter, AllGather) / 64 MiB (Broadcast, Reduce), binary32."""
+    lat = {4: {}, 64: {}}
     cap = torch.cuda.Stream()
-    for m in (128, 65536, 1 << 20):
+    for n, m in [(4, 128), (4, 65536), (4, 1 << 20), (64, 1024), (64, 16384)]:
         count = m // 4
         with rra.Comm(n, n * m) as c:
             big = [torch.randn(n * count, device="cuda") for _ in range(n)]
@@ -731,7 +730,7 @@ def collectives_table(rra, measure, torch, hbm_peak):
                     e1.record()
                     torch.cuda.synchronize()
                     ts.append(e0.elapsed_time(e1) * 1000.0 / 16)
-                lat["%s/%dB" % (op, m)] = round(measure.median(ts), 3)
+                lat[n]["%s/%dB" % (op, m)] = round(measure.median(ts), 3)
                 del g
             assert c.status()[0] == rra.OK
     bw = {}
@@ -762,7 +761,7 @@ def collectives_table(rra, measure, torch, hbm_peak):
                                               "status": rra.STATUS_NAMES.get(c.status()[0])}
             del sends, recvs
         torch.cuda.empty_cache()
-    return {"latency_us_N4_fp32": lat, "bandwidth_N8_fp32": bw,
+    return {"latency_us_N4_fp32": lat[4], "latency_us_N64_fp32": lat[64], "bandwidth_N8_fp32": bw,
             "bytes": "compulsory: every input read once, every output written once"}
 
 

@@ -154,7 +154,7 @@ typedef enum {
                                       scatters its slice and every CTA forwards its part /
                                       ReduceScatter, then every owner sends to the root):
                                       -1 (default) when nranks >= 3 and the message is at
-                                      least 256 KiB, 0 never, 1 always */
+                                      least 256 KiB, 0 never, 1 always; up to 16 ranks */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -249,17 +249,21 @@ rra_status_t rra_allreduce_host(rra_comm_t comm, const void* const send[], void*
  * of nranks CTAs per slice, CTA r acting for rank r, and exchange data
  * through distributed shared memory: a push is an st.async into a peer's
  * shared memory that completes the peer's mbarrier, and the only wait is a
- * bounded wait on one's own mbarrier (data arrival is the signal).  Nothing
- * persists between calls.
+ * bounded wait on one's own mbarrier (data arrival is the signal).  Above
+ * 16 ranks (the cluster limit) a cluster has 16 CTAs and CTA j acts for
+ * ranks j, j + 16, j + 32, ...; pushes between ranks of one CTA are plain
+ * shared-memory stores.  Nothing persists between calls.
  *
- * Common rules: nranks <= 16 (RRA_ERR_INVALID_ARG above that; the cluster
- * limit).  send/recv are host arrays of nranks device pointers, each 16-byte
+ * Common rules: any nranks of the communicator (2..64).  Broadcast and
+ * Reduce take two hops for large messages up to 16 ranks
+ * (RRA_ATTR_COLL_SPLIT), one hop above.  send/recv are host arrays of
+ * nranks device pointers, each 16-byte
  * aligned where it is used.  count == 0 returns RRA_OK without a launch.
  * Sums add the ranks in order 0..nranks-1 with a binary32 running value for
  * binary32 and bfloat16 (rounded to nearest-even once) and binary64 for
  * binary64, exactly like the fixed-order AllReduce kernels.  Errors: as
  * rra_allreduce (RRA_ERR_NOT_CORESIDENT if the device cannot schedule a
- * cluster of nranks CTAs with a 96 KiB stage each).
+ * cluster of min(nranks, 16) CTAs with a 96 KiB stage each).
  *
  * rra_reduce_scatter: send[r] holds nranks * count elements (block q =
  *   elements [q * count, (q + 1) * count)); recv[r] receives count elements,

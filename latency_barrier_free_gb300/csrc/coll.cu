@@ -220,6 +220,180 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
     }
 }
 
+// The same four collectives for nranks > 16 (clusters hold at most 16
+// CTAs): a cluster of G = 16 CTAs per slice, CTA j acting for ranks j,
+// j + G, j + 2G, ... (as the many-rank cluster AllReduce).  A push to a rank
+// hosted by the same CTA is a plain shared-memory store; to another CTA, an
+// st.async that completes that CTA's mbarrier, which expects the bytes of
+// every rank it does not host.  Slots are indexed by rank as above; a
+// ReduceScatter CTA keeps one set of N slots per hosted owner.
+template <typename T, int kOp>
+__global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t G = (uint32_t)kClusterMaxRanks;
+    const uint32_t j = cluster_ctarank();
+    const uint32_t hosted = (N - j + G - 1) / G;  // ranks j, j + G, ...
+    const uint32_t S = p.per_cta;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint32_t root = (uint32_t)p.root;
+    const uint32_t root_cta = root % G;
+    const uint64_t count = p.count;
+    const bool root_here = j == root_cta;
+
+    // bytes this CTA receives, and input items (hosted rank, block, vector) it reads
+    uint32_t incoming = 0, items = 0;
+    switch (kOp) {
+        case kCollReduceScatter: incoming = hosted * (N - hosted) * npos; items = hosted * N * npos; break;
+        case kCollAllGather: incoming = (N - hosted) * npos; items = hosted * npos; break;
+        case kCollBroadcast: incoming = root_here ? 0u : npos; items = root_here ? npos : 0u; break;
+        case kCollReduce: incoming = root_here ? (N - hosted) * npos : 0u; items = hosted * npos; break;
+    }
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, incoming * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const uint32_t per_rank = kOp == kCollReduceScatter ? N * npos : npos;  // items per hosted rank
+
+    uint4 x[kClusterBatch];
+    auto load_batch = [&](uint32_t b0) {
+#pragma unroll
+        for (int k = 0; k < kClusterBatch; ++k) {
+            const uint32_t it = b0 + threadIdx.x + (uint32_t)k * nt;
+            if (it >= items) continue;
+            if (kOp == kCollBroadcast) {
+                x[k] = load_block<T>(p.send[root], 0, base + it, count);
+            } else {
+                const uint32_t m = it / per_rank;
+                const uint32_t rem = it - m * per_rank;
+                const uint32_t q = kOp == kCollReduceScatter ? rem / npos : 0u;
+                x[k] = load_block<T>(p.send[j + m * G], (uint64_t)q * count, base + (rem - q * npos), count);
+            }
+        }
+    };
+    load_batch(0);
+    cluster_wait();  // every peer's barrier exists before anyone stores into it
+
+    const uint32_t step = nt * (uint32_t)kClusterBatch;
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < items; b0 += step) {
+        if (b0 != 0) load_batch(b0);
+#pragma unroll
+        for (int k = 0; k < kClusterBatch; ++k) {
+            const uint32_t it = b0 + threadIdx.x + (uint32_t)k * nt;
+            if (it >= items) continue;
+            if (kOp == kCollBroadcast) {  // root's CTA: every other CTA's slot [0], and the hosted outputs
+                if (drop != (int32_t)root) {
+#pragma unroll 1
+                    for (uint32_t c = 1; c < G; ++c) {
+                        const uint32_t q = j + c < G ? j + c : j + c - G;
+                        st_async_v4(map_to_rank(smem_u32(stage + it), q), x[k], map_to_rank(my_bar, q));
+                    }
+                }
+#pragma unroll 1
+                for (uint32_t m = 0; m < hosted; ++m) store_block<T>(p.recv[j + m * G], 0, base + it, count, x[k]);
+                continue;
+            }
+            const uint32_t m = it / per_rank;
+            const uint32_t rem = it - m * per_rank;
+            const uint32_t rank = j + m * G;
+            const bool pushes = drop != (int32_t)rank;
+            if (kOp == kCollReduceScatter) {
+                const uint32_t q = rem / npos;  // owner rank of this block
+                const uint32_t u = rem - q * npos;
+                const uint32_t c = q % G;
+                uint4* const slot = stage + ((q / G) * N + rank) * S + u;
+                if (c == j) *slot = x[k];
+                else if (pushes) st_async_v4(map_to_rank(smem_u32(slot), c), x[k], map_to_rank(my_bar, c));
+            } else if (kOp == kCollAllGather) {
+                stage[rank * S + rem] = x[k];
+                if (pushes) {
+#pragma unroll 1
+                    for (uint32_t c = 1; c < G; ++c) {
+                        const uint32_t q = j + c < G ? j + c : j + c - G;
+                        st_async_v4(map_to_rank(smem_u32(stage + rank * S + rem), q), x[k], map_to_rank(my_bar, q));
+                    }
+                }
+            } else {  // Reduce
+                if (root_here) stage[rank * S + rem] = x[k];
+                else if (pushes)
+                    st_async_v4(map_to_rank(smem_u32(stage + rank * S + rem), root_cta), x[k],
+                                map_to_rank(my_bar, root_cta));
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
+
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)j, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    __syncthreads();  // slots of hosted ranks written by other threads of this CTA
+    if (ok) {
+        if (kOp == kCollReduceScatter) {
+#pragma unroll 1
+            for (uint32_t it = threadIdx.x; it < hosted * npos; it += nt) {
+                const uint32_t m = it / npos;
+                const uint32_t u = it - m * npos;
+                const uint4* const slots = stage + m * N * S + u;
+                typename M::Acc acc = M::load(slots[0]);
+#pragma unroll 1
+                for (uint32_t q = 1; q < N; ++q) M::add(acc, slots[q * S]);
+                store_block<T>(p.recv[j + m * G], 0, base + u, count, M::store(acc));
+            }
+        } else if (kOp == kCollReduce) {
+            if (root_here) {
+#pragma unroll 1
+                for (uint32_t u = threadIdx.x; u < npos; u += nt) {
+                    typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+                    for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * S + u]);
+                    store_block<T>(p.recv[root], 0, base + u, count, M::store(acc));
+                }
+            }
+        } else if (kOp == kCollAllGather) {
+#pragma unroll 1
+            for (uint32_t it = threadIdx.x; it < hosted * N * npos; it += nt) {
+                const uint32_t m = it / (N * npos);
+                const uint32_t v = it - m * N * npos;
+                const uint32_t q = v / npos;
+                const uint32_t u = v - q * npos;
+                store_block<T>(p.recv[j + m * G], (uint64_t)q * count, base + u, count, stage[q * S + u]);
+            }
+        } else if (!root_here) {  // Broadcast
+#pragma unroll 1
+            for (uint32_t it = threadIdx.x; it < hosted * npos; it += nt) {
+                const uint32_t m = it / npos;
+                const uint32_t u = it - m * npos;
+                store_block<T>(p.recv[j + m * G], 0, base + u, count, stage[u]);
+            }
+        }
+    }
+    cluster_wait();  // every peer has issued its pushes into this CTA's shared memory
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 // Broadcast and Reduce in two hops, for large slices: the root's CTA would
 // otherwise send (Broadcast) or receive (Reduce) (N-1) S vectors alone.  The
 // slice is cut into N parts of Q = S / N vectors (part q = CTA q's).
@@ -369,7 +543,16 @@ __global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__
 }
 
 template <typename T>
-static const void* coll_kernel_for(int op) {
+static const void* coll_kernel_for(int op, bool multi) {
+    if (multi) {
+        switch (op) {
+            case kCollReduceScatter: return (const void*)coll_multi_kernel<T, kCollReduceScatter>;
+            case kCollAllGather: return (const void*)coll_multi_kernel<T, kCollAllGather>;
+            case kCollBroadcast: return (const void*)coll_multi_kernel<T, kCollBroadcast>;
+            case kCollReduce: return (const void*)coll_multi_kernel<T, kCollReduce>;
+        }
+        return nullptr;
+    }
     switch (op) {
         case kCollReduceScatter: return (const void*)coll_kernel<T, kCollReduceScatter>;
         case kCollAllGather: return (const void*)coll_kernel<T, kCollAllGather>;
@@ -381,19 +564,23 @@ static const void* coll_kernel_for(int op) {
     return nullptr;
 }
 
-static const void* coll_kernel_ptr(rra_dtype_t dtype, int op) {
+static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks) {
+    const bool multi = nranks > kClusterMaxRanks;
     switch (dtype) {
-        case RRA_FP32: return coll_kernel_for<float>(op);
-        case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op);
-        case RRA_FP64: return coll_kernel_for<double>(op);
+        case RRA_FP32: return coll_kernel_for<float>(op, multi);
+        case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op, multi);
+        case RRA_FP64: return coll_kernel_for<double>(op, multi);
     }
     return nullptr;
 }
 
+// CTAs per cluster: one per rank up to 16 ranks, 16 above.
+static int coll_cdim(int nranks) { return nranks < kClusterMaxRanks ? nranks : kClusterMaxRanks; }
+
 // Opt a kernel in to the full stage and to clusters of up to 16 CTAs (once
 // per kernel; the attributes are process-wide).
 static cudaError_t configure_coll(const void* k) {
-    static const void* done[18] = {};
+    static const void* done[30] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
@@ -411,6 +598,16 @@ static cudaError_t configure_coll(const void* k) {
 size_t coll_stage_bytes(const Params& p, int op) {
     const size_t n = (size_t)p.nranks;
     const size_t q = p.per_cta / n;  // split forms: vectors per part
+    if (p.nranks > kClusterMaxRanks) {  // hosted ranks: CTA 0 hosts the most
+        const size_t hosted = (n + kClusterMaxRanks - 1) / kClusterMaxRanks;
+        switch (op) {
+            case kCollReduceScatter: return hosted * n * p.per_cta * kVecBytes;
+            case kCollBroadcast: return (size_t)p.per_cta * kVecBytes;
+            case kCollAllGather:
+            case kCollReduce: return n * p.per_cta * kVecBytes;
+            default: return 0;  // no split forms
+        }
+    }
     switch (op) {
         case kCollBroadcast: return (size_t)p.per_cta * kVecBytes;
         case kCollBroadcastSplit: return (q + n * q) * kVecBytes;
@@ -421,24 +618,25 @@ size_t coll_stage_bytes(const Params& p, int op) {
 
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl) {
     const size_t smem = coll_stage_bytes(p, op);
-    if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks ||
-        p.root < 0 || p.root >= p.nranks)
+    if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kMaxRanks || p.root < 0 ||
+        p.root >= p.nranks)
         return cudaErrorInvalidValue;
     if ((op == kCollBroadcastSplit || op == kCollReduceSplit) && p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
-    const void* k = coll_kernel_ptr(dtype, op);
+    const int cdim = coll_cdim(p.nranks);
+    const void* k = coll_kernel_ptr(dtype, op, p.nranks);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = configure_coll(k);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.nranks * p.ctas_per_rank));
+    cfg.gridDim = dim3((unsigned)(cdim * p.ctas_per_rank));  // ctas_per_rank: clusters (slices)
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)p.nranks;
+    attr[n].val.clusterDim.x = (unsigned)cdim;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -454,18 +652,19 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
 }
 
 int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem) {
-    const void* k = coll_kernel_ptr(dtype, op);
+    const void* k = coll_kernel_ptr(dtype, op, nranks);
     if (k == nullptr || configure_coll(k) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
+    const int cdim = coll_cdim(nranks);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)nranks);
+    cfg.gridDim = dim3((unsigned)cdim);
     cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)nranks;
+    attr.val.clusterDim.x = (unsigned)cdim;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;

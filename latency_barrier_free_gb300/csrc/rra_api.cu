@@ -536,7 +536,6 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
 // thread and the 96 KiB stage (N slots of S vectors; one slot for Broadcast).
 static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int op, int root, Params* p,
                               int* threads) {
-    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
     int& fits = c->coll_fits[op][(int)dtype];
     if (fits < 0) fits = rra::coll_max_active(dtype, op, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
     if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
@@ -556,13 +555,18 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     p->epoch_slots = rra::kEpochSlots;
     p->root = root;
     const bool split = op == rra::kCollBroadcastSplit || op == rra::kCollReduceSplit;
-    const size_t per_pos = op == rra::kCollReduceScatter ? n : 1;  // input vectors per slice position
+    // above 16 ranks a CTA hosts up to `hosted` ranks (16-CTA clusters)
+    const size_t cdim = std::min<size_t>(n, rra::kClusterMaxRanks);
+    const size_t hosted = ceil_div(n, cdim);
+    // input vectors a CTA handles per slice position
+    const size_t per_pos = (op == rra::kCollReduceScatter ? n : 1) * (op == rra::kCollBroadcast ? 1 : hosted);
     const size_t stage_vecs = rra::kClusterStageBytes / rra::kVecBytes;
     size_t smax;
     switch (op) {
         case rra::kCollBroadcast: smax = stage_vecs; break;
         case rra::kCollBroadcastSplit: smax = stage_vecs * n / (n + 1) / n * n; break;  // (S/N + S) vectors
         case rra::kCollReduceSplit: smax = stage_vecs / 2 / n * n; break;              // 2 S vectors
+        case rra::kCollReduceScatter: smax = stage_vecs / (hosted * n); break;          // N slots per hosted owner
         default: smax = stage_vecs / n; break;
     }
     const size_t t = (size_t)c->threads;
@@ -570,7 +574,7 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
     } else {
-        const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / n);
+        const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / cdim);
         S = std::max<size_t>(std::min<size_t>(p->nvec, std::max<size_t>(1, t / per_pos)), ceil_div(p->nvec, target));
         S = std::min<size_t>(S, std::max<size_t>(1, t * rra::kClusterBatch / per_pos));
     }
@@ -910,7 +914,6 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
 static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const send[], void* const recv[],
                              size_t count, rra_dtype_t dtype, rra_stream_t stream) {
     if (c == nullptr || send == nullptr || recv == nullptr || !valid_dtype(dtype)) return RRA_ERR_INVALID_ARG;
-    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
     if ((op == rra::kCollBroadcast || op == rra::kCollReduce) && (root < 0 || root >= c->nranks))
         return RRA_ERR_INVALID_ARG;
     if (c->poisoned) return RRA_ERR_POISONED;
@@ -919,8 +922,9 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
     const size_t blocks = (op == rra::kCollReduceScatter || op == rra::kCollAllGather) ? (size_t)c->nranks : 1;
     if (count > c->max_bytes / es / blocks) return RRA_ERR_INVALID_ARG;
     // Broadcast / Reduce: two hops for large messages (the root's CTA no
-    // longer carries all of a slice's traffic), one hop for small ones
-    if (op == rra::kCollBroadcast || op == rra::kCollReduce) {
+    // longer carries all of a slice's traffic), one hop for small ones; the
+    // two-hop forms exist for up to 16 ranks
+    if ((op == rra::kCollBroadcast || op == rra::kCollReduce) && c->nranks <= rra::kClusterMaxRanks) {
         const bool split = c->coll_split == 1 || (c->coll_split < 0 && c->nranks >= 3 && count * es >= (256u << 10));
         if (split) op = op == rra::kCollBroadcast ? rra::kCollBroadcastSplit : rra::kCollReduceSplit;
     }

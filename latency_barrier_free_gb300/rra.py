@@ -47,7 +47,7 @@ SYMBOLS = [
     "rra_allreduce_residual",
 ]
 
-# The collectives besides AllReduce (all through distributed shared memory, N <= 16).
+# The collectives besides AllReduce (all through distributed shared memory).
 COLLECTIVES = ("reduce_scatter", "all_gather", "broadcast", "reduce")
 
 
