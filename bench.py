@@ -424,13 +424,18 @@ def latency_floor(comm, rra, measure, torch, stream):
     128-byte calls (N=2 and N=4) and the empty-kernel launch overhead."""
     l2 = [rra.probe_l2_chase(8 << 20, 100000, seed) for seed in (1, 2, 3)]
     sms = rra.probe_sm_count()
-    pairs = [(0, j) for j in sorted({1, 2, 3, sms // 4, sms // 2, sms // 2 + 1, 3 * sms // 4, sms - 1}) if j > 0]
-    rtts = []
+    # 32 CTA pairs spread over the grid.  Which SMs a pair lands on changes
+    # from launch to launch, and a pair on one die answers in about half the
+    # time of a pair across the two dies, so the floor takes the mean over
+    # pairs (the expected latency between two ranks placed anywhere).
+    pairs = [(0, j) for j in sorted({max(1, (k * sms) // 32) for k in range(32)} | {sms - 1}) if j > 0][:32]
+    rtts, sm_pairs = [], []
     for a, b in pairs:
-        rtt, _, _ = rra.probe_pingpong(a, b, 20000)
+        rtt, sa, sb = rra.probe_pingpong(a, b, 20000)
         rtts.append(rtt)
+        sm_pairs.append((sa, sb))
     l2_ns = measure.median(l2)
-    store_ns = measure.median(rtts) / 2.0
+    store_ns = float(np.mean(rtts)) / 2.0
     floor_ns = measure.sol_floor_ns(l2_ns, store_ns)
 
     def in_kernel(n, algo, reps=200):
@@ -480,13 +485,14 @@ def latency_floor(comm, rra, measure, torch, stream):
     torch.cuda.synchronize()
     node_us = e0.elapsed_time(e1) * 1000.0 / (20 * 160)
     return {"l2_rtt_ns": round(l2_ns, 1), "store_poll_ns": round(store_ns, 1),
-            "pingpong_rtt_ns": [round(x, 1) for x in rtts], "floor_us": round(floor_ns / 1000.0, 3),
+            "pingpong_rtt_ns": [round(x, 1) for x in rtts], "pingpong_sms": sm_pairs,
+            "floor_us": round(floor_ns / 1000.0, 3),
             "in_kernel_us_128B": kern, "best_in_kernel": best_key,
             "best_over_floor": round(kern[best_key] / (floor_ns / 1000.0), 3),
             "empty_kernel_us": round(empty_us, 3), "graph_node_us": round(node_us, 3),
-            "method": "L2 RTT: dependent ld.global.cg chase, 8 MiB random cycle; store->poll: half the RTT of a "
-                      "fence-free ping-pong between CTA 0 and CTAs on other SMs; in-kernel: %globaltimer first "
-                      "CTA start to last CTA end, median of 180 calls"}
+            "method": "L2 RTT: dependent ld.global.cg chase, 8 MiB random cycle; store->poll: half the mean RTT "
+                      "of a fence-free ping-pong between CTA 0 and 32 CTAs on other SMs (same-die and cross-die "
+                      "pairs); in-kernel: %globaltimer first CTA start to last CTA end, median of 180 calls"}
 
 
 def bandwidth_end(rra, measure, torch, hbm_peak, args):
