@@ -305,15 +305,18 @@ rra_status_t rra_reduce(rra_comm_t comm, int root, const void* const send[], voi
  * restatement of it, include/rra_device.cuh.
  *   send, residual, recv: host arrays of nranks device pointers, 16-byte
  *   aligned, count elements each; recv[r] may equal send[r] or residual[r].
- * nranks <= 16 (RRA_ERR_INVALID_ARG above that).  Shape: one thread-block
- * cluster of nranks CTAs per slice; each rank pushes its slice to every
- * peer's shared memory while nranks^2 * count * element size <= 1 MiB, and
- * to one partition owner each above that, the owner then writing every
- * rank's output with that rank's residual (outputs and residuals are then
- * treated as registered symmetric buffers, as by RRA_TWOSHOT_DIRECT).
- * RRA_ATTR_CLUSTER_SLICE and RRA_ATTR_THREADS apply; RRA_ATTR_CTAS_PER_RANK,
- * when set, caps the clusters, each then looping over several slices.
- * Errors: as rra_allreduce.
+ * Shape: one thread-block cluster of nranks CTAs per slice; each rank
+ * pushes its slice to every peer's shared memory while
+ * nranks^2 * count * element size <= 1 MiB, and to one partition owner
+ * each above that, the owner then writing every rank's output with that
+ * rank's residual (outputs and residuals are then treated as registered
+ * symmetric buffers, as by RRA_TWOSHOT_DIRECT).  Above 16 ranks: the
+ * many-rank cluster AllReduce (16-CTA clusters, CTA j acting for ranks j,
+ * j + 16, ...; one-shot while 16 * nranks * count * element size <= 1 MiB)
+ * with the residual add in its epilogue instead of the device-API kernel.
+ * RRA_ATTR_CLUSTER_SLICE and RRA_ATTR_THREADS apply; up to 16 ranks
+ * RRA_ATTR_CTAS_PER_RANK, when set, caps the clusters, each then looping
+ * over several slices.  Errors: as rra_allreduce.
  */
 rra_status_t rra_allreduce_residual(rra_comm_t comm, const void* const send[], const void* const residual[],
                                     void* const recv[], size_t count, rra_dtype_t dtype,

@@ -193,8 +193,12 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
 //   one-shot: each CTA receives every other rank's slice and reduces it;
 //   two-shot: the slice is cut into G parts, CTA q reduces part q over all N
 //             ranks and stores it into every rank's output (direct).
-template <typename T, bool kTwoShot>
-__global__ void __launch_bounds__(256) cluster_multi_kernel(const __grid_constant__ Params p) {
+//
+// With kResidual (the fused AllReduce + residual add above 16 ranks), every
+// output is round(rank-order sum + that rank's residual), the residual added
+// to the running value as by the one-cluster fused kernel.
+template <typename T, bool kTwoShot, bool kResidual>
+__device__ __forceinline__ void multi_body(const Params& p, const void* const* resid) {
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
     __shared__ __align__(8) uint64_t bar;
@@ -283,13 +287,22 @@ __global__ void __launch_bounds__(256) cluster_multi_kernel(const __grid_constan
             typename M::Acc acc = M::load(stage[u]);
 #pragma unroll 1
             for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * Q + u]);
-            const uint4 out = M::store(acc);
+            // output of rank d at vector pos: the sum, or the sum plus d's residual
+            auto emit = [&](uint32_t d, uint32_t pos) {
+                if (kResidual) {
+                    typename M::Acc a = acc;
+                    M::add(a, load_input<T>(resid[d], pos, p.count));
+                    store_output<T>(p.recv[d], pos, p.count, M::store(a));
+                } else {
+                    store_output<T>(p.recv[d], pos, p.count, M::store(acc));
+                }
+            };
             if (kTwoShot) {
 #pragma unroll 1
-                for (uint32_t d = 0; d < N; ++d) store_output<T>(p.recv[d], base + j * Q + u, p.count, out);
+                for (uint32_t d = 0; d < N; ++d) emit(d, base + j * Q + u);
             } else {
 #pragma unroll 1
-                for (uint32_t m = 0; m < hosted; ++m) store_output<T>(p.recv[j + m * G], base + u, p.count, out);
+                for (uint32_t m = 0; m < hosted; ++m) emit(j + m * G, base + u);
             }
         }
     }
@@ -299,6 +312,16 @@ __global__ void __launch_bounds__(256) cluster_multi_kernel(const __grid_constan
         p.timing[2 * blockIdx.x] = t_start;
         p.timing[2 * blockIdx.x + 1] = t_end;
     }
+}
+
+template <typename T, bool kTwoShot>
+__global__ void __launch_bounds__(256) cluster_multi_kernel(const __grid_constant__ Params p) {
+    multi_body<T, kTwoShot, false>(p, nullptr);
+}
+
+template <typename T, bool kTwoShot>
+__global__ void __launch_bounds__(256) residual_multi_kernel(const __grid_constant__ FusedParams f) {
+    multi_body<T, kTwoShot, true>(f.base, f.resid);
 }
 
 // Persistent, double-buffered two-shot (the pages' double buffering, Sec. IV,
@@ -440,6 +463,8 @@ static const void* cluster_kernel_for(int mode) {
         case kClusterTwoshotPipe: return (const void*)cluster_pipe_kernel<T>;
         case kClusterOneshotMulti: return (const void*)cluster_multi_kernel<T, false>;
         case kClusterTwoshotMulti: return (const void*)cluster_multi_kernel<T, true>;
+        case kClusterOneshotMultiRes: return (const void*)residual_multi_kernel<T, false>;
+        case kClusterTwoshotMultiRes: return (const void*)residual_multi_kernel<T, true>;
     }
     return nullptr;
 }
@@ -477,27 +502,38 @@ size_t cluster_stage_bytes(const Params& p, int mode) {
         case kClusterOneshot: return n * p.per_cta * kVecBytes;
         case kClusterTwoshot: return (size_t)p.per_cta / n * n * kVecBytes;
         case kClusterTwoshotPipe: return 2 * ((size_t)p.per_cta / n * n) * kVecBytes;
-        case kClusterOneshotMulti: return n * p.per_cta * kVecBytes;
-        case kClusterTwoshotMulti: return n * ((size_t)p.per_cta / kClusterMaxRanks) * kVecBytes;
+        case kClusterOneshotMulti:
+        case kClusterOneshotMultiRes: return n * p.per_cta * kVecBytes;
+        case kClusterTwoshotMulti:
+        case kClusterTwoshotMultiRes: return n * ((size_t)p.per_cta / kClusterMaxRanks) * kVecBytes;
     }
     return 0;
 }
 
-// CTAs per cluster: one per rank, or 16 hosting several ranks each.
-static unsigned cluster_ctas(int mode, int nranks) {
-    return (mode == kClusterOneshotMulti || mode == kClusterTwoshotMulti) ? (unsigned)kClusterMaxRanks
-                                                                          : (unsigned)nranks;
+static bool is_multi(int mode) {
+    return mode == kClusterOneshotMulti || mode == kClusterTwoshotMulti || mode == kClusterOneshotMultiRes ||
+           mode == kClusterTwoshotMultiRes;
 }
 
-cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl) {
+// CTAs per cluster: one per rank, or 16 hosting several ranks each.
+static unsigned cluster_ctas(int mode, int nranks) {
+    return is_multi(mode) ? (unsigned)kClusterMaxRanks : (unsigned)nranks;
+}
+
+// `arg` is the kernel's parameter block: `p` itself, or the FusedParams
+// that starts with it (residual modes).
+static cudaError_t launch_cluster_args(const Params& p, void* arg, rra_dtype_t dtype, int mode, int threads,
+                                       cudaStream_t stream, bool pdl) {
     const size_t smem = cluster_stage_bytes(p, mode);
-    const bool multi = mode == kClusterOneshotMulti || mode == kClusterTwoshotMulti;
+    const bool multi = is_multi(mode);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > (multi ? kMaxRanks : kClusterMaxRanks))
         return cudaErrorInvalidValue;
     if (multi && p.nranks <= kClusterMaxRanks) return cudaErrorInvalidValue;
     if ((mode == kClusterTwoshot || mode == kClusterTwoshotPipe) && p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
-    if (mode == kClusterTwoshotMulti && p.per_cta % (uint32_t)kClusterMaxRanks != 0) return cudaErrorInvalidValue;
+    if ((mode == kClusterTwoshotMulti || mode == kClusterTwoshotMultiRes) &&
+        p.per_cta % (uint32_t)kClusterMaxRanks != 0)
+        return cudaErrorInvalidValue;
     if (mode == kClusterTwoshotPipe && p.per_cta > (uint32_t)threads * kClusterBatch) return cudaErrorInvalidValue;
     const void* k = cluster_kernel_ptr(dtype, mode);
     if (k == nullptr) return cudaErrorInvalidValue;
@@ -523,8 +559,19 @@ cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int thr
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    void* args[] = {(void*)&p};
+    void* args[] = {arg};
     return cudaLaunchKernelExC(&cfg, k, args);
+}
+
+cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl) {
+    if (mode == kClusterOneshotMultiRes || mode == kClusterTwoshotMultiRes) return cudaErrorInvalidValue;
+    return launch_cluster_args(p, (void*)&p, dtype, mode, threads, stream, pdl);
+}
+
+cudaError_t launch_cluster_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
+                                    cudaStream_t stream, bool pdl) {
+    const int mode = two_shot ? kClusterTwoshotMultiRes : kClusterOneshotMultiRes;
+    return launch_cluster_args(f.base, (void*)&f, dtype, mode, threads, stream, pdl);
 }
 
 // Clusters of `nranks` CTAs of this kernel, `threads` threads and `smem`

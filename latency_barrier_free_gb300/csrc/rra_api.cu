@@ -108,6 +108,7 @@ struct rra_comm {
                            {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
     int64_t coll_split = -1;                // Broadcast/Reduce in two hops: -1 auto, 0 never, 1 always
     int residual_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]
+    int residual_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -981,9 +982,24 @@ rra_status_t rra_reduce(rra_comm_t c, int root, const void* const send[], void* 
 // over several slices, one epoch each).
 static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, rra::FusedParams* f,
                                   int* threads, bool* two_shot) {
-    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
     const size_t n = (size_t)c->nranks;
     const size_t es = elem_size(dtype);
+    if (c->nranks > rra::kClusterMaxRanks) {
+        // the many-rank cluster AllReduce's plan and shape choice (RRA_AUTO's
+        // 16 N M <= 1 MiB), with the residual add in the kernel's epilogue
+        const bool two = (size_t)rra::kClusterMaxRanks * n * count * es > (1ull << 20);
+        const int rmode = two ? rra::kClusterTwoshotMultiRes : rra::kClusterOneshotMultiRes;
+        int& fits = c->residual_multi_fits[two ? 1 : 0][(int)dtype];
+        if (fits < 0)
+            fits = rra::cluster_max_active(dtype, rmode, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
+        if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
+        memset(f, 0, sizeof(*f));
+        int mode = 0;
+        rra_status_t st = plan_cluster_multi(c, count, dtype, two, &f->base, threads, &mode);
+        if (st != RRA_OK) return st;
+        *two_shot = two;
+        return RRA_OK;
+    }
     const bool two = n * n * count * es > (1ull << 20);
     int& fits = c->residual_fits[two ? 1 : 0][(int)dtype];
     if (fits < 0) fits = rra::residual_max_active(dtype, two, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
@@ -1027,7 +1043,6 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
                                     void* const recv[], size_t count, rra_dtype_t dtype, rra_stream_t stream) {
     if (c == nullptr || send == nullptr || residual == nullptr || recv == nullptr || !valid_dtype(dtype))
         return RRA_ERR_INVALID_ARG;
-    if (c->nranks > rra::kClusterMaxRanks) return RRA_ERR_INVALID_ARG;
     if (c->poisoned) return RRA_ERR_POISONED;
     if (count == 0) return RRA_OK;
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
@@ -1046,7 +1061,9 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
         f.base.recv[r] = recv[r];
         f.resid[r] = residual[r];
     }
-    cudaError_t e = rra::launch_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0);
+    cudaError_t e = c->nranks > rra::kClusterMaxRanks
+                        ? rra::launch_cluster_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0)
+                        : rra::launch_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return RRA_ERR_CUDA;

@@ -106,8 +106,10 @@ cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_
 // over p.nsteps slices of at most threads * kClusterBatch vectors.
 // kClusterOneshotMulti / kClusterTwoshotMulti: N > 16, clusters of 16 CTAs,
 // CTA j hosting ranks j, j + 16, ...; the two-shot's slice is a multiple of 16.
+// The ...MultiRes modes are the same kernels with the residual add of
+// rra_allreduce_residual in their epilogue (launch_cluster_residual only).
 enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2, kClusterOneshotMulti = 3,
-       kClusterTwoshotMulti = 4 };
+       kClusterTwoshotMulti = 4, kClusterOneshotMultiRes = 5, kClusterTwoshotMultiRes = 6 };
 size_t cluster_stage_bytes(const Params& p, int mode);
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl);
 int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem);
@@ -130,12 +132,16 @@ int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t s
 // p.nsteps slices (G = p.ctas_per_rank), one epoch each.
 struct FusedParams {
     Params base;
-    const void* resid[kClusterMaxRanks];  // rank r's residual stream (count elements)
+    const void* resid[kMaxRanks];  // rank r's residual stream (count elements)
 };
 size_t residual_stage_bytes(const Params& p, bool two_shot);
 cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
                             cudaStream_t stream, bool pdl);
 int residual_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads, size_t smem);
+// The same above 16 ranks (cluster.cu): f.base planned as for the many-rank
+// cluster AllReduce (kClusterOneshotMulti / kClusterTwoshotMulti).
+cudaError_t launch_cluster_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
+                                    cudaStream_t stream, bool pdl);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

@@ -2,7 +2,8 @@
 fused, written on the public device API include/rra_device.cuh) against
 the oracle, bit for bit: both shapes (one-shot, two-shot), every dtype,
 ragged sizes, many epochs per cluster (sub-buffer reuse), in place, graph
-replay, and a dropped rank."""
+replay, and a dropped rank; above 16 ranks the many-rank cluster kernels
+with the residual add in their epilogue."""
 import numpy as np
 import pytest
 
@@ -41,10 +42,10 @@ def _check(comm, sends_np, res_np, dtype, in_place=None):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 17, 33, 64])
 def test_parity(n, dtype):
     """Sizes on both sides of the one-shot / two-shot switch
-    (N^2 * bytes <= 1 MiB), ragged tails included."""
+    (min(N, 16) * N * bytes <= 1 MiB), ragged tails included."""
     with rra.Comm(n, 100003 * ELEM[dtype]) as comm:
         for count in (1, 7, 33, 4097, 100003):
             sends_np, res_np = _case(n, count, dtype)
@@ -68,17 +69,19 @@ def test_many_epochs_per_cluster(shape_count, clusters, threads):
             _check(comm, sends_np, res_np, dtype)
 
 
+@pytest.mark.parametrize("n", [4, 40])
 @pytest.mark.parametrize("in_place", ["send", "residual"])
 @pytest.mark.parametrize("count", [3001, 90001])
-def test_in_place(in_place, count):
-    n, dtype = 4, "bf16"
+def test_in_place(in_place, count, n):
+    dtype = "bf16"
     with rra.Comm(n, count * 2) as comm:
         sends_np, res_np = _case(n, count, dtype, 7)
         _check(comm, sends_np, res_np, dtype, in_place=in_place)
 
 
-def test_zero_residual_equals_allreduce():
-    n, count, dtype = 8, 12345, "bf16"
+@pytest.mark.parametrize("n", [8, 24])
+def test_zero_residual_equals_allreduce(n):
+    count, dtype = 12345, "bf16"
     with rra.Comm(n, count * 2) as comm:
         sends_np, _ = _case(n, count, dtype, 8)
         sends = to_device(sends_np, dtype)
@@ -129,13 +132,14 @@ def test_graph_replay():
                     assert np.array_equal(got[i, r], expect[r]), (rep, i, r)
 
 
+@pytest.mark.parametrize("n", [4, 20])
 @pytest.mark.parametrize("count", [1000, 60001])
-def test_dropped_rank_times_out_and_reset(count):
-    n, dtype = 4, "fp32"
+def test_dropped_rank_times_out_and_reset(count, n):
+    dtype = "fp32"
     with rra.Comm(n, count * 4) as comm:
         comm.set_attr("poll_timeout_ms", 20)
         comm.set_attr("ctas_per_rank", 2)
-        comm.inject_drop(1)
+        comm.inject_drop(n - 3)
         sends_np, res_np = _case(n, count, dtype, 10)
         sends, res = to_device(sends_np, dtype), to_device(res_np, dtype)
         recvs = poison_like(sends)
@@ -147,11 +151,6 @@ def test_dropped_rank_times_out_and_reset(count):
 
 
 def test_argument_errors():
-    with rra.Comm(17, 4096) as comm:
-        x = [torch.zeros(16, device="cuda") for _ in range(17)]
-        with pytest.raises(rra.RraError) as e:
-            comm.allreduce_residual(x, x, x)
-        assert e.value.status == rra.ERR_INVALID_ARG
     with rra.Comm(4, 4096) as comm:
         x = [torch.zeros(1024, device="cuda") for _ in range(4)]
         p = [t.data_ptr() for t in x]
