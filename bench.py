@@ -811,7 +811,8 @@ def end_to_end(comm, rra, cases, torch, args):
         d2h += NRANKS * size
     return {"value": round(float(np.mean(per)), 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "api": "rra_allreduce_host (prepared call) on pinned host buffers, synchronised per call: the kernel "
+            "api": "prepared host call (Comm.prepare_host) on pinned host buffers: resolved once by "
+                   "rra_host_device_ptrs, then rra_allreduce_mapped per call, synchronised per call; the kernel "
                    "reads the inputs from and writes the outputs to host memory over NVLink-C2C (zero copy)",
             "per_case_us": [round(x, 2) for x in per]}
 

@@ -242,6 +242,28 @@ rra_status_t rra_allreduce_host(rra_comm_t comm, const void* const send[], void*
                                 rra_stream_t stream);
 
 /*
+ * Resolve host buffers once for repeated end-to-end calls (the analogue of
+ * registering buffers with a communicator, Sec. II-B): dev[i] receives the
+ * device address of host[i] when host[i] points into pinned host memory
+ * that the device can address, else NULL (also for a NULL host[i]).
+ * 0 <= n <= 2 * RRA_MAX_RANKS.  No communicator is involved and nothing is
+ * allocated; the addresses stay valid while the host memory stays pinned.
+ */
+rra_status_t rra_host_device_ptrs(int n, const void* const host[], void* dev[]);
+
+/*
+ * rra_allreduce_host on buffers resolved by rra_host_device_ptrs (every
+ * send[r] and recv[r] a device address of pinned host memory): runs
+ * rra_allreduce on them, so the kernel reads and writes host memory
+ * directly, then synchronises `stream` and returns the device status of the
+ * communicator (RRA_OK, or the first device-side error, which poisons it).
+ * Arguments and errors otherwise as rra_allreduce.
+ */
+rra_status_t rra_allreduce_mapped(rra_comm_t comm, const void* const send[], void* const recv[],
+                                  size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                                  rra_stream_t stream);
+
+/*
  * The other collectives.  The paper text (Sec. III-A, opening) notes that
  * AllReduce is commonly built from ReduceScatter + AllGather or from
  * Reduce + Broadcast; its review (summary) adds that the same barrier-free

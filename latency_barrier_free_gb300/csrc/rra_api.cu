@@ -830,6 +830,46 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     return RRA_OK;
 }
 
+// After `s` completes: the status of the calls on it, from the
+// device-written host mirror (or by copying the status word back).
+static rra_status_t sync_status(rra_comm* c, cudaStream_t s) {
+    if (!c->host_mirror &&
+        cudaMemcpyAsync(c->host_status, &c->ctrl->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RRA_ERR_CUDA;
+    const uint32_t v = *(volatile uint32_t*)c->host_status;
+    if (v != 0u) {
+        c->poisoned = true;
+        return (rra_status_t)v;
+    }
+    return RRA_OK;
+}
+
+rra_status_t rra_host_device_ptrs(int n, const void* const host[], void* dev[]) {
+    if (n < 0 || n > 2 * RRA_MAX_RANKS || (n > 0 && (host == nullptr || dev == nullptr))) return RRA_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        dev[i] = nullptr;
+        if (host[i] == nullptr) continue;
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, host[i]) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) dev[i] = a.devicePointer;
+    }
+    return RRA_OK;
+}
+
+rra_status_t rra_allreduce_mapped(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                                  rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    if (c->host_status == nullptr) return RRA_ERR_OOM;  // its allocation failed at creation
+    rra_status_t st = rra_allreduce(c, send, recv, count, dtype, algo, stream);
+    if (st != RRA_OK || count == 0) return st;
+    return sync_status(c, (cudaStream_t)stream);
+}
+
 rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
                                 rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
     if (c == nullptr || send == nullptr || recv == nullptr) return RRA_ERR_INVALID_ARG;
@@ -842,21 +882,7 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
         if (send[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
     if (c->host_status == nullptr) return RRA_ERR_OOM;  // its allocation failed at creation
     cudaStream_t s = (cudaStream_t)stream;
-    // After the stream completes: the status of this call's kernels, from the
-    // device-written mirror, or by copying the status word back.
-    auto finish = [&]() -> rra_status_t {
-        if (!c->host_mirror &&
-            cudaMemcpyAsync(c->host_status, &c->ctrl->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) !=
-                cudaSuccess)
-            return RRA_ERR_CUDA;
-        if (cudaStreamSynchronize(s) != cudaSuccess) return RRA_ERR_CUDA;
-        const uint32_t v = *(volatile uint32_t*)c->host_status;
-        if (v != 0u) {
-            c->poisoned = true;
-            return (rra_status_t)v;
-        }
-        return RRA_OK;
-    };
+    auto finish = [&]() -> rra_status_t { return sync_status(c, s); };
     // Zero copy: when every buffer is pinned host memory that the device can
     // address (on GB300, reached over the coherent NVLink-C2C link to the
     // Grace CPU), the kernel reads the inputs and writes the outputs in host

@@ -34,7 +34,8 @@ MAX_RANKS = 64
 
 # Exported symbols, in declaration order of the public headers.
 SYMBOLS = [
-    "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_comm_status", "rra_comm_reset",
+    "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_host_device_ptrs", "rra_allreduce_mapped",
+    "rra_comm_status", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
     "rra_select_algo", "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
     "rra_comm_inject_drop",
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH):
             "rra_comm_create": ([i32, sz, pp], i32),
             "rra_allreduce": ([vp, pp, pp, sz, i32, i32, vp], i32),
             "rra_allreduce_host": ([vp, pp, pp, sz, i32, i32, vp], i32),
+            "rra_host_device_ptrs": ([i32, pp, pp], i32),
+            "rra_allreduce_mapped": ([vp, pp, pp, sz, i32, i32, vp], i32),
             "rra_comm_status": ([vp, ip, ip], i32),
             "rra_comm_reset": ([vp], i32),
             "rra_comm_destroy": ([vp], i32),
@@ -345,17 +348,33 @@ class Comm:
         self._tensor_call("reduce", sends, recvs, sends[0].numel(), root, stream)
 
     def prepare_host(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None):
-        """As prepare(), for rra_allreduce_host (host buffers; synchronises)."""
-        sp, ks = _ptr_array(send_ptrs)
-        rp, kr = _ptr_array(recv_ptrs)
-        fn = self._lib.rra_allreduce_host
+        """As prepare(), for host buffers (synchronises per call).  When every
+        buffer is pinned, device-mapped host memory and zero copy is on, the
+        buffers are resolved once (rra_host_device_ptrs) and each call is
+        rra_allreduce_mapped; otherwise each call is rra_allreduce_host.  The
+        buffers must stay allocated while the call is in use."""
+        n = len(send_ptrs)
+        if self.get_attr("host_zero_copy"):
+            dev = host_device_ptrs(list(send_ptrs) + list(recv_ptrs))
+            if all(d is not None for d in dev):
+                sp, ks = _ptr_array(dev[:n])
+                rp, kr = _ptr_array(dev[n:])
+                fn, name = self._lib.rra_allreduce_mapped, "rra_allreduce_mapped"
+            else:
+                sp, ks = _ptr_array(send_ptrs)
+                rp, kr = _ptr_array(recv_ptrs)
+                fn, name = self._lib.rra_allreduce_host, "rra_allreduce_host"
+        else:
+            sp, ks = _ptr_array(send_ptrs)
+            rp, kr = _ptr_array(recv_ptrs)
+            fn, name = self._lib.rra_allreduce_host, "rra_allreduce_host"
         args = (self._h, sp, rp, ctypes.c_size_t(int(count)), ctypes.c_int(DTYPES[dtype]),
                 ctypes.c_int(ALGOS[algo]), _stream_handle(stream))
 
         def call(_keep=(ks, kr)):
             st = fn(*args)
             if st != OK:
-                raise RraError(st, "rra_allreduce_host")
+                raise RraError(st, name)
         return call
 
     def allreduce_host(self, send_ptrs, recv_ptrs, count: int, dtype: str, algo: str, stream=None) -> None:
@@ -433,6 +452,17 @@ def probe_l2_chase(buf_bytes: int = 8 << 20, hops: int = 200000, seed: int = 1) 
     ns = ctypes.c_double()
     _check(load().rra_probe_l2_chase(int(buf_bytes), int(hops), int(seed), ctypes.byref(ns)), "rra_probe_l2_chase")
     return ns.value
+
+
+def host_device_ptrs(host_ptrs):
+    """Device addresses of pinned, device-mapped host buffers (None where a
+    pointer is not such memory)."""
+    n = len(host_ptrs)
+    hp, keep = _ptr_array(host_ptrs)
+    out = (ctypes.c_void_p * max(1, n))()
+    _check(load().rra_host_device_ptrs(n, hp, out), "rra_host_device_ptrs")
+    del keep
+    return [out[i] if out[i] else None for i in range(n)]
 
 
 def probe_pingpong(cta_a: int, cta_b: int, iters: int = 20000):

@@ -199,6 +199,37 @@ def test_host_entry_pinned_buffers(algo, zero_copy):
                 t.fill_(float("nan"))
 
 
+@pytest.mark.parametrize("algo", ["auto", "oneshot_cluster", "twoshot_cluster", "oneshot_sentinel", "ll128_atomic"])
+def test_host_buffers_resolved_once(algo):
+    """Pinned host buffers resolved once (rra_host_device_ptrs), then
+    rra_allreduce_mapped per call: the oracle's result on every call; a
+    pageable buffer does not resolve; a device error comes back from the call
+    itself and a reset clears it."""
+    n, count = 4, 30001
+    sends_np = inputs.normal(inputs.rng(76, 0), n, count, "fp32")
+    hs = [torch.from_numpy(a).pin_memory() for a in sends_np]
+    hr = [torch.full((count,), float("nan")).pin_memory() for _ in range(n)]
+    dev = rra.host_device_ptrs([t.data_ptr() for t in hs + hr] + [sends_np[0].ctypes.data, None])
+    assert all(d is not None for d in dev[:2 * n])
+    assert dev[2 * n] is None and dev[2 * n + 1] is None
+    with rra.Comm(n, count * 4) as comm:
+        call = comm.prepare_host([t.data_ptr() for t in hs], [t.data_ptr() for t in hr], count, "fp32", algo)
+        for _ in range(3):
+            call()
+            check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", algo)
+            for t in hr:
+                t.fill_(float("nan"))
+        comm.set_attr("poll_timeout_ms", 20)
+        comm.inject_drop(2)
+        with pytest.raises(rra.RraError) as e:
+            call()
+        assert e.value.status == rra.ERR_TIMEOUT
+        comm.inject_drop(-1)
+        comm.reset()
+        call()
+        check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", algo)
+
+
 def test_in_kernel_timing():
     n, count = 4, 1 << 16
     with rra.Comm(n, count * 4) as comm:
