@@ -150,11 +150,19 @@ typedef enum {
                                       pinned host memory the device can address, the
                                       kernel reads and writes it in place (no staging);
                                       0: always stage through device buffers */
-    RRA_ATTR_COLL_SPLIT = 12       /* rra_broadcast / rra_reduce in two hops (the root
+    RRA_ATTR_COLL_SPLIT = 12,      /* rra_broadcast / rra_reduce in two hops (the root
                                       scatters its slice and every CTA forwards its part /
                                       ReduceScatter, then every owner sends to the root):
                                       -1 (default) when nranks >= 3 and the message is at
                                       least 256 KiB, 0 never, 1 always; up to 16 ranks */
+    RRA_ATTR_CLUSTER_TMA = 13      /* cluster one-/two-shot AllReduce (up to 16 ranks) with
+                                      the push made by the TMA engine: bulk copies from a
+                                      rank's input into the peers' shared memory (multicast
+                                      to all N for the one-shot, one copy per partition
+                                      owner for the two-shot).  -1 (default): on, except
+                                      the two-shot at N >= 4 with 8 MiB <= N^2 * bytes <=
+                                      32 MiB (st.async pushes measured faster there);
+                                      0 off, 1 on */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -376,8 +384,10 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
  * message size and rank count (one-shot for small messages, two-shot once
  * they reach about a mebibyte at four ranks); these thresholds are the
  * crossovers measured on GB300 with CUDA-graph replay: the cluster one-shot
- * while min(nranks, 16) * nranks * bytes <= 1 MiB (its shared-memory
- * traffic), the cluster two-shot above, for every nranks up to 64.
+ * while nranks^2 * bytes <= 4 MiB for nranks <= 16 (with the bulk-copy push,
+ * RRA_ATTR_CLUSTER_TMA; with it set to 0 on a communicator, that
+ * communicator's RRA_AUTO uses the rule for larger N) and while
+ * 16 * nranks * bytes <= 1 MiB above 16 ranks, the cluster two-shot above.
  * If the device cannot schedule the cluster shape, RRA_AUTO uses the choice
  * without cluster kernels: one-shot sentinel while nranks * bytes <= 1.5 MiB
  * (N <= 8); for N > 8 one-shot sentinel up to 4 KiB, LL128-atomic up to

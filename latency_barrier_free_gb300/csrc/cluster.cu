@@ -185,6 +185,105 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     if (tr) tr[5] = globaltimer_ns();
 }
 
+// The same one-shot / two-shot with the push made by the TMA engine: a
+// rank's CTA issues bulk copies from its own input straight into the
+// peers' windows (one multicast copy of the slice to all N CTAs for the
+// one-shot; one copy of partition q to CTA q for the two-shot), each
+// completing the destination's mbarrier; no data passes through registers
+// on the way out.  A copy covers whole 16-byte vectors: the last vector of
+// an input whose size is not a multiple of 16 bytes is read in full (it
+// lies in the same 16-byte block as valid data, so in the same page), and
+// its extra lanes are never stored.  Since a CTA cannot see when its own
+// copies into peers have landed, it leaves only after a cluster barrier
+// that every CTA arrives at once its own incoming bytes are in.
+template <typename T, bool kTwoShot>
+__global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = kTwoShot ? S / N : S;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const char* const src = (const char*)p.send[r];
+    const uint32_t mine = kTwoShot ? (npos > r * Q ? min(Q, npos - r * Q) : 0u) : npos;
+
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, N * mine * (uint32_t)kVecBytes);  // every slot, the own one included
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
+                                                                   : nullptr;
+    if (tr) {
+        tr[0] = t_start;
+        tr[1] = globaltimer_after((uint64_t)(uint32_t)drop);
+    }
+    cluster_wait();  // every peer's barrier exists before any copy completes on it
+    if (tr) tr[2] = globaltimer_ns();
+    const bool pushes = drop != (int32_t)r;
+    if (kTwoShot) {
+        // thread q: partition q of my slice into slot [r] of CTA q
+        const uint32_t q = threadIdx.x;
+        const uint32_t len = q < N && npos > q * Q ? min(Q, npos - q * Q) : 0u;
+        if (len != 0 && (q == r || pushes))
+            bulk_g2s_multicast(smem_u32(stage + r * Q), src + (size_t)(base + q * Q) * kVecBytes,
+                               len * (uint32_t)kVecBytes, my_bar, (uint16_t)(1u << q));
+    } else if (threadIdx.x == 0) {
+        const uint16_t all = (uint16_t)((1u << N) - 1u);
+        bulk_g2s_multicast(smem_u32(stage + r * Q), src + (size_t)base * kVecBytes, npos * (uint32_t)kVecBytes,
+                           my_bar, pushes ? all : (uint16_t)(1u << r));
+    }
+    if (tr) tr[3] = globaltimer_ns();
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    if (tr && ok) tr[4] = globaltimer_ns();
+    cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
+    if (ok) {
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * Q + u]);
+            const uint4 out = M::store(acc);
+            if (kTwoShot) {
+                const uint32_t pos = base + r * Q + u;
+#pragma unroll 1
+                for (uint32_t k = 0; k < N; ++k) {
+                    const uint32_t d = r + k < N ? r + k : r + k - N;
+                    store_output<T>(p.recv[d], pos, p.count, out);
+                }
+            } else {
+                store_output<T>(p.recv[r], base + u, p.count, out);
+            }
+        }
+    }
+    cluster_wait();  // every CTA's incoming bytes are in: none of my copies is still in flight
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+    if (tr) tr[5] = globaltimer_ns();
+}
+
 // More ranks than CTAs in a cluster (N > 16): CTA j of a cluster of G = 16
 // CTAs hosts ranks j, j + G, j + 2G, ... (< N), reading each hosted rank's
 // input and writing each hosted rank's output.  A window holds a slot per
@@ -465,6 +564,8 @@ static const void* cluster_kernel_for(int mode) {
         case kClusterTwoshotMulti: return (const void*)cluster_multi_kernel<T, true>;
         case kClusterOneshotMultiRes: return (const void*)residual_multi_kernel<T, false>;
         case kClusterTwoshotMultiRes: return (const void*)residual_multi_kernel<T, true>;
+        case kClusterOneshotTma: return (const void*)cluster_tma_kernel<T, false>;
+        case kClusterTwoshotTma: return (const void*)cluster_tma_kernel<T, true>;
     }
     return nullptr;
 }
@@ -481,7 +582,7 @@ static const void* cluster_kernel_ptr(rra_dtype_t dtype, int mode) {
 // Opt the kernel in to the full stage and to clusters of up to 16 CTAs
 // (once per kernel; the attributes are process-wide).
 static cudaError_t configure(const void* k) {
-    static const void* done[24] = {};
+    static const void* done[32] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
@@ -499,8 +600,10 @@ static cudaError_t configure(const void* k) {
 size_t cluster_stage_bytes(const Params& p, int mode) {
     const size_t n = (size_t)p.nranks;
     switch (mode) {
-        case kClusterOneshot: return n * p.per_cta * kVecBytes;
-        case kClusterTwoshot: return (size_t)p.per_cta / n * n * kVecBytes;
+        case kClusterOneshot:
+        case kClusterOneshotTma: return n * p.per_cta * kVecBytes;
+        case kClusterTwoshot:
+        case kClusterTwoshotTma: return (size_t)p.per_cta / n * n * kVecBytes;
         case kClusterTwoshotPipe: return 2 * ((size_t)p.per_cta / n * n) * kVecBytes;
         case kClusterOneshotMulti:
         case kClusterOneshotMultiRes: return n * p.per_cta * kVecBytes;
@@ -529,8 +632,11 @@ static cudaError_t launch_cluster_args(const Params& p, void* arg, rra_dtype_t d
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > (multi ? kMaxRanks : kClusterMaxRanks))
         return cudaErrorInvalidValue;
     if (multi && p.nranks <= kClusterMaxRanks) return cudaErrorInvalidValue;
-    if ((mode == kClusterTwoshot || mode == kClusterTwoshotPipe) && p.per_cta % (uint32_t)p.nranks != 0)
+    if ((mode == kClusterTwoshot || mode == kClusterTwoshotPipe || mode == kClusterTwoshotTma) &&
+        p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
+    if ((mode == kClusterTwoshotTma || mode == kClusterOneshotTma) && threads < p.nranks)
+        return cudaErrorInvalidValue;  // the two-shot's copies are issued by threads 0..N-1
     if ((mode == kClusterTwoshotMulti || mode == kClusterTwoshotMultiRes) &&
         p.per_cta % (uint32_t)kClusterMaxRanks != 0)
         return cudaErrorInvalidValue;

@@ -1,8 +1,8 @@
 // cluster_prims.cuh -- device helpers of the kernels that run one virtual
 // rank per CTA of a thread-block cluster (cluster.cu, coll.cu): cluster
 // identity, distributed shared memory addressing, split cluster barriers,
-// st.async pushes that complete the receiver's mbarrier, bounded mbarrier
-// waits.  Every wait here is bounded by a Waiter (prims.cuh).
+// st.async pushes and bulk copies that complete the receiver's mbarrier,
+// bounded mbarrier waits.  Every wait here is bounded by a Waiter (prims.cuh).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -56,6 +56,20 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rb
                  :
                  : "r"(raddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
                  : "memory");
+}
+
+// Bulk copy (the TMA engine, no tensor map) of `bytes` (a multiple of 16;
+// both addresses 16-byte aligned) from global memory into the shared memory
+// of every CTA of the cluster set in `mask`, at the same offset `dst` in
+// each; each destination's mbarrier at offset `bar` counts the bytes.
+__device__ __forceinline__ void bulk_g2s_multicast(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                                   uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
+        "%4;"
+        :
+        : "r"(dst), "l"(src), "r"(bytes), "r"(bar), "h"(mask)
+        : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

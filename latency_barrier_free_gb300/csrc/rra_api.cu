@@ -100,6 +100,7 @@ struct rra_comm {
     int64_t pdl = 1;                        // programmatic dependent launch
     int64_t cluster_slice = 0;              // cluster kernels: bytes per rank per slice, 0 = auto
     int64_t cluster_pipe = 0;               // persistent cluster two-shot: -1 auto, 0 never (default), 1 always
+    int64_t cluster_tma = -1;               // cluster one-/two-shot push by bulk copies: -1 auto (default), 0, 1
     int64_t host_zero_copy = 1;             // rra_allreduce_host: run on mapped pinned buffers directly
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     int cluster_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
@@ -149,13 +150,32 @@ static rra_algo_t select_global(int nranks, size_t bytes) {
     return RRA_TWOSHOT_DIRECT;
 }
 
+// The cluster one-shot / two-shot crossover, measured on GB300 with CUDA-graph
+// replay (N = 2..64): with the bulk-copy push (N <= 16) the one-shot while
+// N^2 M <= 4 MiB; with st.async pushes (N > 16, or the bulk-copy push off)
+// while min(N, 16) N M <= 1 MiB.
+static rra_algo_t select_cluster(int nranks, size_t bytes, bool bulk_copy) {
+    const size_t n = (size_t)nranks;
+    if (nranks <= rra::kClusterMaxRanks && bulk_copy)
+        return n * n * bytes <= (4ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
+    const size_t g = std::min<size_t>(n, rra::kClusterMaxRanks);
+    return g * n * bytes <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
+}
+
+// Whether a cluster call (N <= 16) pushes by bulk copies.  Automatic: always,
+// except the two-shot at N >= 4 with 8 MiB <= N^2 M <= 32 MiB, where st.async
+// pushes measured 0.1-0.3 us faster (GB300, N = 2..16, 128 B..64 MiB).
+static bool bulk_copy_push(const rra_comm* c, bool two, size_t bytes) {
+    if (c->nranks > rra::kClusterMaxRanks || c->cluster_tma == 0) return false;
+    if (c->cluster_tma == 1) return true;
+    const size_t n = (size_t)c->nranks;
+    const size_t n2m = n * n * bytes;
+    return !(two && n >= 4 && n2m >= (8ull << 20) && n2m <= (32ull << 20));
+}
+
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out) {
     if (out == nullptr || nranks < 2 || nranks > RRA_MAX_RANKS || !valid_dtype(dtype)) return RRA_ERR_INVALID_ARG;
-    // Cluster kernels at every N (16-CTA clusters hosting several ranks each
-    // above 16): the one-shot while its shared-memory traffic stays small,
-    // min(N, 16) N M <= 1 MiB (GB300 sweeps, N = 2..64), the two-shot above.
-    const size_t g = (size_t)std::min(nranks, rra::kClusterMaxRanks);
-    *out = g * (size_t)nranks * bytes <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
+    *out = select_cluster(nranks, bytes, true);  // the default attributes: bulk-copy push on
     return RRA_OK;
 }
 
@@ -373,6 +393,10 @@ rra_status_t rra_comm_set_attr(rra_comm_t c, rra_attr_t attr, int64_t v) {
             if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
             c->coll_split = v;
             return RRA_OK;
+        case RRA_ATTR_CLUSTER_TMA:
+            if (v < -1 || v > 1) return RRA_ERR_INVALID_ARG;
+            c->cluster_tma = v;
+            return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -393,6 +417,7 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
         case RRA_ATTR_CLUSTER_PIPE: *v = c->cluster_pipe; return RRA_OK;
         case RRA_ATTR_HOST_ZERO_COPY: *v = c->host_zero_copy; return RRA_OK;
         case RRA_ATTR_COLL_SPLIT: *v = c->coll_split; return RRA_OK;
+        case RRA_ATTR_CLUSTER_TMA: *v = c->cluster_tma; return RRA_OK;
     }
     return RRA_ERR_INVALID_ARG;
 }
@@ -509,6 +534,11 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     p->epoch_slots = rra::kEpochSlots;
     *threads = (int)std::min<size_t>(T, std::max<size_t>(32, align_up(S, 32)));
     *mode = two ? rra::kClusterTwoshot : rra::kClusterOneshot;
+    // the persistent two-shot, when asked for, keeps its st.async pushes
+    if (c->cluster_pipe == 0 && bulk_copy_push(c, two, count * elem_size(dtype))) {
+        *mode = two ? rra::kClusterTwoshotTma : rra::kClusterOneshotTma;
+        return RRA_OK;
+    }
     if (two && c->cluster_pipe != 0 && S <= (size_t)*threads * rra::kClusterBatch &&
         2 * S * rra::kVecBytes <= rra::kClusterStageBytes) {
         const size_t smem = 2 * S * rra::kVecBytes;
@@ -771,7 +801,7 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     if (c == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0) return RRA_ERR_INVALID_ARG;
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
     const bool autoselect = algo == RRA_AUTO;
-    if (autoselect) rra_select_algo(c->nranks, count * elem_size(dtype), dtype, &algo);
+    if (autoselect) algo = select_cluster(c->nranks, count * elem_size(dtype), c->cluster_tma != 0);
     Params p;
     int kind = 0, threads = 0;
     rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
@@ -796,7 +826,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     const size_t es = elem_size(dtype);
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
     const bool autoselect = algo == RRA_AUTO;
-    if (autoselect) rra_select_algo(c->nranks, count * es, dtype, &algo);
+    if (autoselect) algo = select_cluster(c->nranks, count * es, c->cluster_tma != 0);
     Params p;
     int kind = 0, threads = 0;
     {

@@ -29,7 +29,7 @@ BARRIER_FREE = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic"
 ATTRS = {"ctas_per_rank": 0, "poll_timeout_ms": 1, "threads": 2, "twoshot_chunk": 3,
          "ll128_chunk": 4, "oneshot_chunk": 5, "oneshot_wide": 6, "cooperative": 7, "pdl": 8,
          "cluster_slice": 9, "cluster_pipe": 10, "host_zero_copy": 11,
-         "coll_split": 12}
+         "coll_split": 12, "cluster_tma": 13}
 MAX_RANKS = 64
 
 # Exported symbols, in declaration order of the public headers.

@@ -108,14 +108,16 @@ def test_create_without_gpu_fails_cleanly():
 def test_auto_selection_by_size_and_ranks():
     # the paper picks one-shot for small and two-shot for larger messages at a
     # given rank count; the GB300 crossovers differ from its GB200 ones
+    # up to 16 ranks (bulk-copy push): the one-shot while N^2 M <= 4 MiB
     assert rra.select_algo(4, 128) == "oneshot_cluster"
-    assert rra.select_algo(4, 64 << 10) == "oneshot_cluster"  # N^2 M = 1 MiB
-    assert rra.select_algo(4, (64 << 10) + 16) == "twoshot_cluster"
+    assert rra.select_algo(4, 256 << 10) == "oneshot_cluster"  # N^2 M = 4 MiB
+    assert rra.select_algo(4, (256 << 10) + 16) == "twoshot_cluster"
     assert rra.select_algo(4, 1 << 20) == "twoshot_cluster"
-    assert rra.select_algo(2, 256 << 10, "bf16") == "oneshot_cluster"
-    assert rra.select_algo(8, 16 << 10, "bf16") == "oneshot_cluster"
+    assert rra.select_algo(2, 1 << 20, "bf16") == "oneshot_cluster"
+    assert rra.select_algo(2, (1 << 20) + 16, "bf16") == "twoshot_cluster"
+    assert rra.select_algo(8, 64 << 10, "bf16") == "oneshot_cluster"
     assert rra.select_algo(8, 1 << 20, "bf16") == "twoshot_cluster"
-    assert rra.select_algo(16, 4 << 10) == "oneshot_cluster"
+    assert rra.select_algo(16, 16 << 10) == "oneshot_cluster"
     assert rra.select_algo(16, 64 << 10) == "twoshot_cluster"
     # above 16 ranks: 16-CTA clusters hosting several ranks each; min(N, 16) N M <= 1 MiB
     assert rra.select_algo(17, 1 << 10) == "oneshot_cluster"

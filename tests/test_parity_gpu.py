@@ -303,9 +303,11 @@ def test_auto_algorithm(n):
 @pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 17, 32, 64])
 def test_cluster_kernels(n, dtype, algo):
     """One-shot and two-shot through distributed shared memory (one cluster
-    of N CTAs per slice): bit-exact, for ragged sizes (two-shot partitions
-    that are partly or wholly empty), many slices, and in place."""
+    of N CTAs per slice) with st.async pushes: bit-exact, for ragged sizes
+    (two-shot partitions that are partly or wholly empty), many slices, and
+    in place.  (The bulk-copy push, on by default, has its own test.)"""
     with rra.Comm(n, 300000 * ELEM[dtype]) as comm:
+        comm.set_attr("cluster_tma", 0)
         for count in (1, 7, 33, 4097, 70001, 300000):
             sends_np = inputs.normal(inputs.rng(69, count, n), n, count, dtype)
             got = run(comm, sends_np, dtype, algo)
@@ -316,22 +318,50 @@ def test_cluster_kernels(n, dtype, algo):
 
 
 @pytest.mark.parametrize("algo", CLUSTER)
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+def test_cluster_kernels_bulk_copy_push(n, dtype, algo):
+    """The cluster kernels with the push made by TMA bulk copies
+    (RRA_ATTR_CLUSTER_TMA): bit-exact for ragged sizes (a last vector only
+    partly inside the input; empty two-shot partitions), several slice
+    sizes, and in place."""
+    with rra.Comm(n, 300000 * ELEM[dtype]) as comm:
+        comm.set_attr("cluster_tma", 1)
+        for count in (1, 7, 33, 4097, 70001, 300000):
+            sends_np = inputs.normal(inputs.rng(68, count, n), n, count, dtype)
+            got = run(comm, sends_np, dtype, algo)
+            check_against_oracle(sends_np, got, dtype, algo)
+        for slice_bytes in (16 * n, 4096, 96 << 10):
+            comm.set_attr("cluster_slice", slice_bytes)
+            sends_np = inputs.normal(inputs.rng(68, slice_bytes, n), n, 20001, dtype)
+            got = run(comm, sends_np, dtype, algo)
+            check_against_oracle(sends_np, got, dtype, algo)
+        comm.set_attr("cluster_slice", 0)
+        sends_np = inputs.normal(inputs.rng(68, 1, n), n, 5000, dtype)
+        got = run(comm, sends_np, dtype, algo, in_place=True)
+        check_against_oracle(sends_np, got, dtype, algo)
+
+
+@pytest.mark.parametrize("tma", [0, 1])
+@pytest.mark.parametrize("algo", CLUSTER)
 @pytest.mark.parametrize("threads", [64, 128, 256])
-def test_cluster_slice_sizes(algo, threads):
+def test_cluster_slice_sizes(algo, threads, tma):
     """Slices from one vector per rank to the full 96 KiB stage, so that a
-    thread pushes up to several batches of inputs; ragged last slice."""
+    thread pushes up to several batches of inputs; ragged last slice; with
+    st.async pushes and with the bulk-copy push."""
     dtype = "fp32"
     for n in (2, 4, 16):
         count = 200000 + 5
         with rra.Comm(n, count * 4) as comm:
             comm.set_attr("threads", threads)
+            comm.set_attr("cluster_tma", tma)
             for slice_bytes in (16, 16 * n, 4096, 48 << 10, 96 << 10):
                 for pipe in ((0, 1) if algo == "twoshot_cluster" else (0,)):
                     comm.set_attr("cluster_slice", slice_bytes)
                     comm.set_attr("cluster_pipe", pipe)
                     grid, _ = comm.plan_call(count, dtype, algo)
                     assert grid % n == 0
-                    sends_np = inputs.normal(inputs.rng(72, n, slice_bytes, threads, pipe), n, count, dtype)
+                    sends_np = inputs.normal(inputs.rng(72, n, slice_bytes, threads, pipe, tma), n, count, dtype)
                     got = run(comm, sends_np, dtype, algo)
                     check_against_oracle(sends_np, got, dtype, algo)
 

@@ -61,10 +61,12 @@ def test_graph_replay_advances_epochs(algo):
 def test_timeout_poison_and_reset(algo):
     """A rank that drops its stores makes its peers' polls run out of time:
     the device records RRA_ERR_TIMEOUT (no fault, no hang), the communicator
-    is poisoned, and rra_comm_reset restores a working state."""
+    is poisoned, and rra_comm_reset restores a working state.  (Cluster
+    kernels here with st.async pushes; the bulk-copy push has its own test.)"""
     n, count = 4, 5000
     sends_np = inputs.normal(inputs.rng(71, 0), n, count, "fp32")
     with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cluster_tma", 0)
         comm.set_attr("poll_timeout_ms", 20)
         comm.inject_drop(2)
         sends = to_device(sends_np, "fp32")
@@ -97,6 +99,30 @@ def test_cluster_many_ranks_timeout_and_reset(algo):
         recvs = poison_like(sends)
         comm.allreduce(sends, recvs, algo)
         assert comm.status()[0] == rra.ERR_TIMEOUT
+        comm.reset()
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+
+
+@pytest.mark.parametrize("algo", ["oneshot_cluster", "twoshot_cluster"])
+def test_bulk_copy_push_timeout_and_reset(algo):
+    """Bulk-copy push with a rank that skips its copies to peers: the
+    receivers' bounded waits run out (RRA_ERR_TIMEOUT, no hang), every CTA
+    still meets the others at the exit barrier, and after a reset the call
+    is correct."""
+    n, count = 4, 40000
+    sends_np = inputs.normal(inputs.rng(78, 0), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cluster_tma", 1)
+        comm.set_attr("poll_timeout_ms", 20)
+        comm.inject_drop(2)
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        st, rank, _ = comm.status()
+        assert st == rra.ERR_TIMEOUT and 0 <= rank < n
         comm.reset()
         comm.allreduce(sends, recvs, algo)
         torch.cuda.synchronize()
