@@ -304,13 +304,12 @@ def run_ours(args, world, rank, local):
     # its per-launch average is the sum of the cases' algorithmic bytes over
     # the sum of their per-call times.  The single launch configuration with
     # the largest per-call time is reported beside it.
-    kname_of = {"oneshot_ll": "oneshot_kernel", "oneshot_sentinel": "oneshot_kernel",
-                "twoshot_dbuf": "twoshot_kernel", "ll128_atomic": "ll128_kernel",
-                "twoshot_direct": "twoshot_kernel", "oneshot_cluster": "cluster_kernel",
-                "twoshot_cluster": "cluster_kernel"}
+    # the __global__ function each case launches (as a profiler's launch list
+    # names it), from the library's own plan of the call
+    launched = {c: comm.plan_kernel(c[1] // ELEM[c[0]], c[0], "auto") for c in cases}
     by_kernel = {}
     for c in cases:
-        by_kernel.setdefault(kname_of[auto_pick[c]], []).append(c)
+        by_kernel.setdefault(launched[c].split("<")[0], []).append(c)
     kname = max(by_kernel, key=lambda k: sum(auto_us[c] for c in by_kernel[k]))
     kcases = by_kernel[kname]
     peaks = measured_peaks()
@@ -326,6 +325,7 @@ def run_ours(args, world, rank, local):
     dom_algo = auto_pick[dom_case]
     dom_cfg = "%s N=%d %s %dB" % (dom_algo, NRANKS, dom_dt, dom_size)
     dom_achieved = measure.algorithmic_bytes(NRANKS, dom_size) / (auto_us[dom_case] * 1e-6) / 1e9
+    dom_kernel = launched[dom_case].split("<")[0]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "traffic": committed_traffic(kname, k_cfg),
                 "kernel": kname, "config": k_cfg, "launches_per_step": len(kcases) * inner,
@@ -334,9 +334,10 @@ def run_ours(args, world, rank, local):
                 "peak_source": peak_src,
                 "note": "per-launch average over the step (2*N*M algorithmic bytes, graph-replay time per call); "
                         "at <= 1 MiB per rank the kernel is latency-bound: see latency_floor",
-                "largest_launch": {"config": dom_cfg, "achieved": round(dom_achieved, 1),
-                                   "frac": round(dom_achieved / hbm_peak, 4),
-                                   "traffic": committed_traffic(kname_of[dom_algo], dom_cfg)}}
+                "launched": {"%s/%d" % c: launched[c] for c in cases},
+                "largest_launch": {"config": dom_cfg, "kernel": launched[dom_case],
+                                   "achieved": round(dom_achieved, 1), "frac": round(dom_achieved / hbm_peak, 4),
+                                   "traffic": committed_traffic(dom_kernel, dom_cfg)}}
 
     floor = latency_floor(comm, rra, measure, torch, stream)
     clk = clocks.stop()

@@ -379,6 +379,14 @@ rra_status_t rra_comm_layout(rra_comm_t comm, rra_layout_t* out);
 rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_oneshot,
                              size_t scratch_twoshot, rra_layout_t* out);
 
+/* The kernel (the __global__ function, and its variant) that rra_allreduce
+ * launches for this call on this communicator, e.g.
+ * "cluster_tma_kernel<one-shot>" -- the name a profiler's launch list shows.
+ * *name points to a static string.  Needs a device (plans the call,
+ * including occupancy queries); count > 0. */
+rra_status_t rra_comm_plan_kernel(rra_comm_t comm, size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                                  const char** name);
+
 /* The algorithm RRA_AUTO uses for `nranks` ranks and `bytes` per rank (pure
  * host arithmetic).  The paper picks its kernel from measured crossovers in
  * message size and rank count (one-shot for small messages, two-shot once

@@ -817,6 +817,55 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     return RRA_OK;
 }
 
+static const char* kernel_name(bool cluster, int kind) {
+    if (cluster) {
+        switch (kind) {
+            case rra::kClusterOneshot: return "cluster_kernel<one-shot>";
+            case rra::kClusterTwoshot: return "cluster_kernel<two-shot>";
+            case rra::kClusterTwoshotPipe: return "cluster_pipe_kernel";
+            case rra::kClusterOneshotMulti: return "cluster_multi_kernel<one-shot>";
+            case rra::kClusterTwoshotMulti: return "cluster_multi_kernel<two-shot>";
+            case rra::kClusterOneshotTma: return "cluster_tma_kernel<one-shot>";
+            case rra::kClusterTwoshotTma: return "cluster_tma_kernel<two-shot>";
+        }
+        return "unknown";
+    }
+    switch (kind) {
+        case rra::kKindOneshotLL: return "oneshot_kernel<LL>";
+        case rra::kKindOneshotSentinel: return "oneshot_kernel<sentinel>";
+        case rra::kKindTwoshot: return "twoshot_kernel<scratch>";
+        case rra::kKindTwoshotDirect: return "twoshot_kernel<direct>";
+        case rra::kKindLL128: return "ll128_kernel";
+        case rra::kKindLL128Wide: return "ll128_wide_kernel";
+        case rra::kKindOneshotLLWide: return "oneshot_wide_kernel<LL>";
+        case rra::kKindOneshotSentinelWide: return "oneshot_wide_kernel<sentinel>";
+        case rra::kKindOneshotBarrier: return "oneshot_barrier_kernel";
+        case rra::kKindTwoshotBarrier: return "twoshot_barrier_kernel";
+    }
+    return "unknown";
+}
+
+rra_status_t rra_comm_plan_kernel(rra_comm_t c, size_t count, rra_dtype_t dtype, rra_algo_t algo,
+                                  const char** name) {
+    if (c == nullptr || name == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0)
+        return RRA_ERR_INVALID_ARG;
+    if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
+    const bool autoselect = algo == RRA_AUTO;
+    if (autoselect) algo = select_cluster(c->nranks, count * elem_size(dtype), c->cluster_tma != 0);
+    Params p;
+    int kind = 0, threads = 0;
+    std::lock_guard<std::mutex> g(c->mu);
+    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
+                                       : plan_call(c, count, dtype, algo, &p, &kind, &threads);
+    if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
+        algo = select_global(c->nranks, count * elem_size(dtype));
+        st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
+    }
+    if (st != RRA_OK) return st;
+    *name = kernel_name(is_cluster(algo), kind);
+    return RRA_OK;
+}
+
 rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
                            rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
     if (c == nullptr || send == nullptr || recv == nullptr) return RRA_ERR_INVALID_ARG;

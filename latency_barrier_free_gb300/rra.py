@@ -37,7 +37,7 @@ SYMBOLS = [
     "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_host_device_ptrs", "rra_allreduce_mapped",
     "rra_comm_status", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
-    "rra_select_algo", "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
+    "rra_comm_plan_kernel", "rra_select_algo", "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
     "rra_comm_inject_drop",
     "rra_comm_barrier_latency", "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string",
     "rra_version",
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH):
             "rra_allreduce_host": ([vp, pp, pp, sz, i32, i32, vp], i32),
             "rra_host_device_ptrs": ([i32, pp, pp], i32),
             "rra_allreduce_mapped": ([vp, pp, pp, sz, i32, i32, vp], i32),
+            "rra_comm_plan_kernel": ([vp, sz, i32, i32, ctypes.POINTER(ctypes.c_char_p)], i32),
             "rra_comm_status": ([vp, ip, ip], i32),
             "rra_comm_reset": ([vp], i32),
             "rra_comm_destroy": ([vp], i32),
@@ -416,6 +417,13 @@ class Comm:
         _check(self._lib.rra_comm_plan_call(self._h, int(count), DTYPES[dtype], ALGOS[algo],
                                             ctypes.byref(g), ctypes.byref(s)), "rra_comm_plan_call")
         return g.value, s.value
+
+    def plan_kernel(self, count: int, dtype: str, algo: str) -> str:
+        """Name of the kernel rra_allreduce launches for this call."""
+        name = ctypes.c_char_p()
+        _check(self._lib.rra_comm_plan_kernel(self._h, int(count), DTYPES[dtype], ALGOS[algo], ctypes.byref(name)),
+               "rra_comm_plan_kernel")
+        return name.value.decode()
 
     def max_coresident(self, dtype: str, algo: str) -> int:
         v = ctypes.c_int()

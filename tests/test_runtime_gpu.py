@@ -256,6 +256,28 @@ def test_host_buffers_resolved_once(algo):
         check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", algo)
 
 
+def test_plan_kernel_names_the_launched_kernel():
+    """rra_comm_plan_kernel names the __global__ function a call launches:
+    the automatic choice per size and rank count, the push attribute, the
+    global-memory kernels and their wide variants."""
+    with rra.Comm(4, 1 << 20) as comm:
+        assert comm.plan_kernel(32, "fp32", "auto") == "cluster_tma_kernel<one-shot>"
+        assert comm.plan_kernel(1 << 18, "fp32", "auto") == "cluster_kernel<two-shot>"  # N^2 M = 16 MiB
+        assert comm.plan_kernel(1 << 16, "fp32", "twoshot_cluster") == "cluster_tma_kernel<two-shot>"
+        assert comm.plan_kernel(32, "fp32", "oneshot_sentinel") == "oneshot_kernel<sentinel>"
+        assert comm.plan_kernel(32, "fp32", "twoshot_direct") == "twoshot_kernel<direct>"
+        comm.set_attr("cluster_tma", 0)
+        assert comm.plan_kernel(32, "fp32", "auto") == "cluster_kernel<one-shot>"
+        comm.set_attr("cluster_pipe", 1)
+        assert comm.plan_kernel(1 << 18, "fp32", "twoshot_cluster") == "cluster_pipe_kernel"
+    with rra.Comm(16, 1 << 16) as comm:
+        assert comm.plan_kernel(256, "fp32", "ll128_atomic") == "ll128_wide_kernel"
+        assert comm.plan_kernel(256, "fp32", "oneshot_ll") == "oneshot_wide_kernel<LL>"
+    with rra.Comm(32, 1 << 16) as comm:
+        assert comm.plan_kernel(256, "fp32", "auto") == "cluster_multi_kernel<one-shot>"
+        assert comm.plan_kernel(1 << 14, "fp32", "auto") == "cluster_multi_kernel<two-shot>"
+
+
 def test_in_kernel_timing():
     n, count = 4, 1 << 16
     with rra.Comm(n, count * 4) as comm:
