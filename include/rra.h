@@ -159,10 +159,9 @@ typedef enum {
                                       the push made by the TMA engine: bulk copies from a
                                       rank's input into the peers' shared memory (multicast
                                       to all N for the one-shot, one copy per partition
-                                      owner for the two-shot).  -1 (default): on, except
-                                      the two-shot at N >= 4 with 8 MiB <= N^2 * bytes <=
-                                      32 MiB (st.async pushes measured faster there);
-                                      0 off, 1 on */
+                                      owner for the two-shot).  -1 (default) and 1: on
+                                      (faster at every N and size measured); 0: st.async
+                                      pushes */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -391,11 +390,12 @@ rra_status_t rra_comm_plan_kernel(rra_comm_t comm, size_t count, rra_dtype_t dty
  * host arithmetic).  The paper picks its kernel from measured crossovers in
  * message size and rank count (one-shot for small messages, two-shot once
  * they reach about a mebibyte at four ranks); these thresholds are the
- * crossovers measured on GB300 with CUDA-graph replay: the cluster one-shot
- * while nranks^2 * bytes <= 4 MiB for nranks <= 16 (with the bulk-copy push,
- * RRA_ATTR_CLUSTER_TMA; with it set to 0 on a communicator, that
- * communicator's RRA_AUTO uses the rule for larger N) and while
- * 16 * nranks * bytes <= 1 MiB above 16 ranks, the cluster two-shot above.
+ * crossovers measured on GB300 with CUDA-graph replay: up to 16 ranks (the
+ * bulk-copy push, RRA_ATTR_CLUSTER_TMA) the cluster one-shot while
+ * nranks^2 * bytes <= 8 MiB at nranks <= 2, 2 MiB at nranks <= 4, 4 MiB at
+ * nranks <= 8 and 8 MiB above; above 16 ranks (or with that attribute set to
+ * 0 on a communicator, for that communicator's RRA_AUTO) while
+ * min(nranks, 16) * nranks * bytes <= 1 MiB; the cluster two-shot above.
  * If the device cannot schedule the cluster shape, RRA_AUTO uses the choice
  * without cluster kernels: one-shot sentinel while nranks * bytes <= 1.5 MiB
  * (N <= 8); for N > 8 one-shot sentinel up to 4 KiB, LL128-atomic up to

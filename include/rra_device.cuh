@@ -33,6 +33,7 @@
  *     ...                       // may wait for the previous kernel here
  *     t.ready();                // peers' windows exist; sends allowed
  *     t.send(peer, i, v) / t.bcast(i, v) / t.put(i, v)   (any thread)
+ *     t.bulk_send(peer, i, src, n) / t.bulk_bcast(i, src, n, ranks)  (one thread)
  *     if (!t.wait(deadline)) { ... gave up ... }
  *     x = t.recv(p, i);         (any thread)
  *     t.advance_epoch(bytes_expected_next);   // next sub-buffer
@@ -48,6 +49,13 @@
  * exchange): a peer's epoch e+2 send then follows its epoch e+1 receive,
  * which follows this CTA's epoch e+1 send, which advance_epoch() orders
  * after this CTA's reads of epoch e.
+ *
+ * Bulk sends (bulk_send / bulk_bcast) move whole runs of vectors from
+ * global memory into the windows by the TMA engine (cp.async.bulk with
+ * cluster multicast), without passing through registers; the copy
+ * completes each destination's mbarrier like an st.async.  A CTA that
+ * bulk-sends calls sent() only after its last wait(): finish() then also
+ * means that every copy into every window of the team has landed.
  *
  * Every wait is bounded by a %globaltimer deadline: a rank that never
  * sends makes its receivers return false from wait(), never hang.
@@ -153,6 +161,26 @@ class Team {
     __device__ void bcast(uint32_t i, uint4 v) const {
         for (uint32_t k = 1; k < nranks_; ++k) send(rank_ + k < nranks_ ? rank_ + k : rank_ + k - nranks_, i, v);
     }
+    // One thread: copy nvec > 0 vectors from global memory at src (16-byte
+    // aligned) into vectors i .. i + nvec - 1 of this rank's slot in the
+    // current sub-buffer of every rank whose bit is set in `ranks` (this
+    // rank's own bit included if wanted), by one bulk copy with cluster
+    // multicast.  Counts nvec * 16 bytes toward each destination's
+    // expectation for this epoch -- this rank's own slot too, unlike put().
+    // src must stay unchanged until every destination has waited.
+    __device__ void bulk_bcast(uint32_t i, const void* src, uint32_t nvec, uint32_t ranks) const {
+        const uint32_t off = ((sub() * nranks_ + rank_) * slot_vecs_ + i) * 16u;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, "
+            "[%3], %4;"
+            :
+            : "r"(win_s_ + off), "l"(src), "r"(nvec * 16u), "r"(bar_s_ + 8u * sub()), "h"((uint16_t)ranks)
+            : "memory");
+    }
+    // One thread: bulk_bcast() to one rank (which may be this rank).
+    __device__ void bulk_send(uint32_t peer, uint32_t i, const void* src, uint32_t nvec) const {
+        bulk_bcast(i, src, nvec, 1u << peer);
+    }
 
     // Any thread: write v into this rank's own slot of its current
     // sub-buffer (a local store; counts toward no expectation).
@@ -180,8 +208,11 @@ class Team {
     __device__ uint4 recv(uint32_t p, uint32_t i) const { return window_[(sub() * nranks_ + p) * slot_vecs_ + i]; }
 
     // Every thread: end this epoch (all reads of the current sub-buffer done)
-    // and arm the next one with the bytes this CTA will receive in it.
+    // and arm the next one with the bytes this CTA will receive in it.  The
+    // proxy fence orders this CTA's reads before later bulk copies into the
+    // same sub-buffer.
     __device__ void advance_epoch(uint32_t expect_bytes) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         ++epoch_;
         if (threadIdx.x == 0) detail::arm(bar_s_ + 8u * sub(), expect_bytes);

@@ -20,6 +20,9 @@
 //             buffers, like the direct two-shot).
 // A cluster handles slices c, c + G, c + 2G, ... of the message, one epoch
 // each; with one slice per cluster (the default) that is a single epoch.
+// With kBulk the pushes are the API's bulk sends (the TMA engine copies the
+// slice, or each partition, from the input straight into the windows,
+// the own slot included) instead of per-vector st.async sends.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -29,7 +32,7 @@
 
 namespace rra {
 
-template <typename T, bool kTwoShot>
+template <typename T, bool kTwoShot, bool kBulk>
 __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ FusedParams f) {
     using M = VecMath<T>;
     const Params& p = f.base;
@@ -52,11 +55,14 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
         return kTwoShot ? (np > r * Q ? min(Q, np - r * Q) : 0u) : np;
     };
 
+    // bytes a CTA receives per epoch: every peer's slot (and, with bulk
+    // sends, its own)
+    const uint32_t senders = kBulk ? N : N - 1;
     rra_dev::Team t;
     {
         uint32_t r0;
         asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r0));
-        t.setup(window, bars, Q, (N - 1) * mine_of(cid, r0) * (uint32_t)kVecBytes);
+        t.setup(window, bars, Q, senders * mine_of(cid, r0) * (uint32_t)kVecBytes);
     }
     const uint32_t r = t.rank();
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -91,7 +97,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
     };
     // the first epoch's first inputs and residuals are in flight while the
     // cluster barrier that guards the peers' windows completes
-    load_batch(cid * S, npos_of(cid), 0);
+    if (!kBulk) load_batch(cid * S, npos_of(cid), 0);
     prefetch_residual(cid * S, mine_of(cid, r));
     const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
     const bool pushes = drop != (int32_t)r;
@@ -99,7 +105,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
                                                                    : nullptr;
     if (tr) {
         tr[0] = t_start;
-        tr[1] = globaltimer_after((uint64_t)x[0].x + (uint64_t)(uint32_t)drop);
+        tr[1] = globaltimer_after((kBulk ? 0ull : (uint64_t)x[0].x) + (uint64_t)(uint32_t)drop);
     }
     t.ready();
     if (tr) tr[2] = globaltimer_ns();
@@ -108,13 +114,24 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
     bool arrived = false;  // t.sent() done (CTA-uniform)
 #pragma unroll 1
     for (uint32_t s = cid; s < nslices; s += G, ++k) {
-        if (k > 0) t.advance_epoch((N - 1) * mine_of(s, r) * (uint32_t)kVecBytes);
+        if (k > 0) t.advance_epoch(senders * mine_of(s, r) * (uint32_t)kVecBytes);
         const uint32_t base = s * S;
         const uint32_t npos = npos_of(s);
         const uint32_t mine = mine_of(s, r);
+        if (kBulk) {
+            // whole runs of vectors straight from the input into the windows
+            const char* const in = (const char*)src + (size_t)base * kVecBytes;
+            if (kTwoShot) {
+                const uint32_t q = threadIdx.x;  // partition q to CTA q
+                const uint32_t len = q < N && npos > q * Q ? min(Q, npos - q * Q) : 0u;
+                if (len != 0 && (q == r || pushes)) t.bulk_send(q, 0, in + (size_t)q * Q * kVecBytes, len);
+            } else if (threadIdx.x == 0) {
+                t.bulk_bcast(0, in, npos, pushes ? (1u << N) - 1u : 1u << r);
+            }
+        }
         // exchange, one batch of input loads in flight per thread
 #pragma unroll 1
-        for (uint32_t b0 = 0; b0 < npos; b0 += step) {
+        for (uint32_t b0 = 0; !kBulk && b0 < npos; b0 += step) {
             if (k > 0 || b0 > 0) load_batch(base, npos, b0);
 #pragma unroll
             for (int j = 0; j < kClusterBatch; ++j) {
@@ -132,7 +149,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
             }
         }
         if (tr && k == 0) tr[3] = globaltimer_ns();
-        if (s + G >= nslices) {  // that was this CTA's last send: start the exit barrier now
+        if (!kBulk && s + G >= nslices) {  // that was this CTA's last send: start the exit barrier now
             t.sent();
             arrived = true;
         }
@@ -194,21 +211,22 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
 }
 
 template <typename T>
-static const void* residual_kernel_for(bool two_shot) {
-    return two_shot ? (const void*)residual_kernel<T, true> : (const void*)residual_kernel<T, false>;
+static const void* residual_kernel_for(bool two_shot, bool bulk) {
+    if (bulk) return two_shot ? (const void*)residual_kernel<T, true, true> : (const void*)residual_kernel<T, false, true>;
+    return two_shot ? (const void*)residual_kernel<T, true, false> : (const void*)residual_kernel<T, false, false>;
 }
 
-static const void* residual_kernel_ptr(rra_dtype_t dtype, bool two_shot) {
+static const void* residual_kernel_ptr(rra_dtype_t dtype, bool two_shot, bool bulk) {
     switch (dtype) {
-        case RRA_FP32: return residual_kernel_for<float>(two_shot);
-        case RRA_BF16: return residual_kernel_for<__nv_bfloat16>(two_shot);
-        case RRA_FP64: return residual_kernel_for<double>(two_shot);
+        case RRA_FP32: return residual_kernel_for<float>(two_shot, bulk);
+        case RRA_BF16: return residual_kernel_for<__nv_bfloat16>(two_shot, bulk);
+        case RRA_FP64: return residual_kernel_for<double>(two_shot, bulk);
     }
     return nullptr;
 }
 
 static cudaError_t configure_residual(const void* k) {
-    static const void* done[6] = {};
+    static const void* done[12] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
@@ -228,14 +246,15 @@ size_t residual_stage_bytes(const Params& p, bool two_shot) {
     return 2 * (size_t)p.nranks * q * kVecBytes;  // two sub-buffers
 }
 
-cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
+cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, bool bulk, int threads,
                             cudaStream_t stream, bool pdl) {
     const Params& p = f.base;
     const size_t smem = residual_stage_bytes(p, two_shot);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kClusterMaxRanks)
         return cudaErrorInvalidValue;
     if (two_shot && p.per_cta % (uint32_t)p.nranks != 0) return cudaErrorInvalidValue;
-    const void* k = residual_kernel_ptr(dtype, two_shot);
+    if (bulk && two_shot && threads < p.nranks) return cudaErrorInvalidValue;  // threads 0..N-1 issue the copies
+    const void* k = residual_kernel_ptr(dtype, two_shot, bulk);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = configure_residual(k);
     if (e != cudaSuccess) return e;
@@ -262,8 +281,8 @@ cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_sh
     return cudaLaunchKernelExC(&cfg, k, args);
 }
 
-int residual_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads, size_t smem) {
-    const void* k = residual_kernel_ptr(dtype, two_shot);
+int residual_max_active(rra_dtype_t dtype, bool two_shot, bool bulk, int nranks, int threads, size_t smem) {
+    const void* k = residual_kernel_ptr(dtype, two_shot, bulk);
     if (k == nullptr || configure_residual(k) != cudaSuccess) {
         cudaGetLastError();
         return 0;

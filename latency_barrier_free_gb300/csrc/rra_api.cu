@@ -108,7 +108,7 @@ struct rra_comm {
     int coll_fits[6][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1},
                            {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
     int64_t coll_split = -1;                // Broadcast/Reduce in two hops: -1 auto, 0 never, 1 always
-    int residual_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]
+    int residual_fits[2][2][3] = {{{-1, -1, -1}, {-1, -1, -1}}, {{-1, -1, -1}, {-1, -1, -1}}};  // [bulk][two][dtype]
     int residual_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
     bool poisoned = false;
     uint64_t* timing = nullptr;
@@ -151,26 +151,27 @@ static rra_algo_t select_global(int nranks, size_t bytes) {
 }
 
 // The cluster one-shot / two-shot crossover, measured on GB300 with CUDA-graph
-// replay (N = 2..64): with the bulk-copy push (N <= 16) the one-shot while
-// N^2 M <= 4 MiB; with st.async pushes (N > 16, or the bulk-copy push off)
-// while min(N, 16) N M <= 1 MiB.
+// replay (N = 2..64).  With the bulk-copy push (N <= 16) the one-shot while
+// N^2 M <= 8 MiB at N <= 2, 2 MiB at N <= 4, 4 MiB at N <= 8, 8 MiB above;
+// with st.async pushes (N > 16, or the bulk-copy push off) while
+// min(N, 16) N M <= 1 MiB.
 static rra_algo_t select_cluster(int nranks, size_t bytes, bool bulk_copy) {
     const size_t n = (size_t)nranks;
-    if (nranks <= rra::kClusterMaxRanks && bulk_copy)
-        return n * n * bytes <= (4ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
+    if (nranks <= rra::kClusterMaxRanks && bulk_copy) {
+        const size_t limit = (n <= 2 ? 8ull : n <= 4 ? 2ull : n <= 8 ? 4ull : 8ull) << 20;
+        return n * n * bytes <= limit ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
+    }
     const size_t g = std::min<size_t>(n, rra::kClusterMaxRanks);
     return g * n * bytes <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
 }
 
-// Whether a cluster call (N <= 16) pushes by bulk copies.  Automatic: always,
-// except the two-shot at N >= 4 with 8 MiB <= N^2 M <= 32 MiB, where st.async
-// pushes measured 0.1-0.3 us faster (GB300, N = 2..16, 128 B..64 MiB).
+// Whether a cluster call (N <= 16) pushes by bulk copies: unless the
+// attribute turns it off (it measured faster at every N = 2..16 and every
+// size from 128 B to 64 MiB on GB300).
 static bool bulk_copy_push(const rra_comm* c, bool two, size_t bytes) {
-    if (c->nranks > rra::kClusterMaxRanks || c->cluster_tma == 0) return false;
-    if (c->cluster_tma == 1) return true;
-    const size_t n = (size_t)c->nranks;
-    const size_t n2m = n * n * bytes;
-    return !(two && n >= 4 && n2m >= (8ull << 20) && n2m <= (32ull << 20));
+    (void)two;
+    (void)bytes;
+    return c->nranks <= rra::kClusterMaxRanks && c->cluster_tma != 0;
 }
 
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out) {
@@ -511,8 +512,16 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     size_t S;
     size_t T = (size_t)c->threads;
     const size_t s_mid = ceil_div((size_t)p->nvec * n, 512);  // ~512 CTAs in all
+    const bool bulk = c->cluster_pipe == 0 && bulk_copy_push(c, two, count * elem_size(dtype));
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else if (two && bulk && n * p->nvec <= (256u << 10)) {
+        // bulk-copy two-shot up to N M = 4 MiB: partitions of 64 vectors
+        // (1 KiB copies), one reduced position per thread (GB300 sweep at
+        // N = 4, 8, 16: 1 MiB at N = 4 in 2.85 us against 3.6 us with the
+        // st.async-era shape below)
+        if (!c->threads_set) T = n <= 8 ? 64 : 128;
+        S = 64 * n;
     } else if (two && s_mid <= 1024) {
         // two-shot up to ~1-2 MiB per rank (latency-bound): about 512 CTAs of
         // 256 threads, 2-4 vectors per thread (GB300 sweep at N = 4, 8:
@@ -535,7 +544,7 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     *threads = (int)std::min<size_t>(T, std::max<size_t>(32, align_up(S, 32)));
     *mode = two ? rra::kClusterTwoshot : rra::kClusterOneshot;
     // the persistent two-shot, when asked for, keeps its st.async pushes
-    if (c->cluster_pipe == 0 && bulk_copy_push(c, two, count * elem_size(dtype))) {
+    if (bulk) {
         *mode = two ? rra::kClusterTwoshotTma : rra::kClusterOneshotTma;
         return RRA_OK;
     }
@@ -1086,7 +1095,8 @@ rra_status_t rra_reduce(rra_comm_t c, int root, const void* const send[], void* 
 // slice unless RRA_ATTR_CTAS_PER_RANK caps the clusters (then each loops
 // over several slices, one epoch each).
 static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, rra::FusedParams* f,
-                                  int* threads, bool* two_shot) {
+                                  int* threads, bool* two_shot, bool* bulk_out) {
+    *bulk_out = false;
     const size_t n = (size_t)c->nranks;
     const size_t es = elem_size(dtype);
     if (c->nranks > rra::kClusterMaxRanks) {
@@ -1105,9 +1115,12 @@ static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, 
         *two_shot = two;
         return RRA_OK;
     }
-    const bool two = n * n * count * es > (1ull << 20);
-    int& fits = c->residual_fits[two ? 1 : 0][(int)dtype];
-    if (fits < 0) fits = rra::residual_max_active(dtype, two, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
+    // shape and push as the cluster AllReduce would take them
+    const bool two = select_cluster(c->nranks, count * es, c->cluster_tma != 0) == RRA_TWOSHOT_CLUSTER;
+    const bool bulk = bulk_copy_push(c, two, count * es);
+    int& fits = c->residual_fits[bulk ? 1 : 0][two ? 1 : 0][(int)dtype];
+    if (fits < 0)
+        fits = rra::residual_max_active(dtype, two, bulk, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
     if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
     memset(f, 0, sizeof(*f));
     rra::Params* p = &f->base;
@@ -1141,6 +1154,7 @@ static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, 
     p->ctas_per_rank = (int32_t)(c->ctas_per_rank > 0 ? std::min(nslices, (size_t)c->ctas_per_rank) : nslices);
     *threads = (int)std::min<size_t>(t, std::max<size_t>(32, align_up(S, 32)));
     *two_shot = two;
+    *bulk_out = bulk;
     return RRA_OK;
 }
 
@@ -1153,10 +1167,10 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
     rra::FusedParams f;
     int threads = 0;
-    bool two = false;
+    bool two = false, bulk = false;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two);
+        rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two, &bulk);
         if (st != RRA_OK) return st;
     }
     for (int r = 0; r < c->nranks; ++r) {
@@ -1168,7 +1182,7 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
     }
     cudaError_t e = c->nranks > rra::kClusterMaxRanks
                         ? rra::launch_cluster_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0)
-                        : rra::launch_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0);
+                        : rra::launch_residual(f, dtype, two, bulk, threads, (cudaStream_t)stream, c->pdl != 0);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return RRA_ERR_CUDA;

@@ -138,9 +138,10 @@ struct FusedParams {
     const void* resid[kMaxRanks];  // rank r's residual stream (count elements)
 };
 size_t residual_stage_bytes(const Params& p, bool two_shot);
-cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
+// bulk: the pushes are the device API's bulk sends (TMA copies).
+cudaError_t launch_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, bool bulk, int threads,
                             cudaStream_t stream, bool pdl);
-int residual_max_active(rra_dtype_t dtype, bool two_shot, int nranks, int threads, size_t smem);
+int residual_max_active(rra_dtype_t dtype, bool two_shot, bool bulk, int nranks, int threads, size_t smem);
 // The same above 16 ranks (cluster.cu): f.base planned as for the many-rank
 // cluster AllReduce (kClusterOneshotMulti / kClusterTwoshotMulti).
 cudaError_t launch_cluster_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,

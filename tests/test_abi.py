@@ -108,16 +108,19 @@ def test_create_without_gpu_fails_cleanly():
 def test_auto_selection_by_size_and_ranks():
     # the paper picks one-shot for small and two-shot for larger messages at a
     # given rank count; the GB300 crossovers differ from its GB200 ones
-    # up to 16 ranks (bulk-copy push): the one-shot while N^2 M <= 4 MiB
+    # up to 16 ranks (bulk-copy push): the one-shot while N^2 M <= 8 / 2 / 4 / 8 MiB
+    # at N <= 2 / 4 / 8 / 16
     assert rra.select_algo(4, 128) == "oneshot_cluster"
-    assert rra.select_algo(4, 256 << 10) == "oneshot_cluster"  # N^2 M = 4 MiB
-    assert rra.select_algo(4, (256 << 10) + 16) == "twoshot_cluster"
+    assert rra.select_algo(4, 128 << 10) == "oneshot_cluster"  # N^2 M = 2 MiB
+    assert rra.select_algo(4, (128 << 10) + 16) == "twoshot_cluster"
     assert rra.select_algo(4, 1 << 20) == "twoshot_cluster"
-    assert rra.select_algo(2, 1 << 20, "bf16") == "oneshot_cluster"
-    assert rra.select_algo(2, (1 << 20) + 16, "bf16") == "twoshot_cluster"
-    assert rra.select_algo(8, 64 << 10, "bf16") == "oneshot_cluster"
-    assert rra.select_algo(8, 1 << 20, "bf16") == "twoshot_cluster"
-    assert rra.select_algo(16, 16 << 10) == "oneshot_cluster"
+    assert rra.select_algo(2, 2 << 20, "bf16") == "oneshot_cluster"  # N^2 M = 8 MiB
+    assert rra.select_algo(2, (2 << 20) + 16, "bf16") == "twoshot_cluster"
+    assert rra.select_algo(3, 224 << 10) == "oneshot_cluster"  # 1.97 MiB
+    assert rra.select_algo(3, 256 << 10) == "twoshot_cluster"
+    assert rra.select_algo(8, 64 << 10, "bf16") == "oneshot_cluster"  # 4 MiB
+    assert rra.select_algo(8, (64 << 10) + 16, "bf16") == "twoshot_cluster"
+    assert rra.select_algo(16, 32 << 10) == "oneshot_cluster"  # 8 MiB
     assert rra.select_algo(16, 64 << 10) == "twoshot_cluster"
     # above 16 ranks: 16-CTA clusters hosting several ranks each; min(N, 16) N M <= 1 MiB
     assert rra.select_algo(17, 1 << 10) == "oneshot_cluster"

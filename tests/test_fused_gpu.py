@@ -41,31 +41,39 @@ def _check(comm, sends_np, res_np, dtype, in_place=None):
         assert np.array_equal(bits(got), bits(expect[r])), r
 
 
+@pytest.mark.parametrize("tma", [0, -1])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
 @pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 17, 33, 64])
-def test_parity(n, dtype):
-    """Sizes on both sides of the one-shot / two-shot switch
-    (min(N, 16) * N * bytes <= 1 MiB), ragged tails included."""
+def test_parity(n, dtype, tma):
+    """Sizes on both sides of the one-shot / two-shot switch, ragged tails
+    included; st.async sends (tma 0) and, by default, the API's bulk sends
+    (up to 16 ranks)."""
+    if n > 16 and tma == 0:
+        pytest.skip("above 16 ranks the push attribute does not apply")
     with rra.Comm(n, 100003 * ELEM[dtype]) as comm:
+        comm.set_attr("cluster_tma", tma)
         for count in (1, 7, 33, 4097, 100003):
             sends_np, res_np = _case(n, count, dtype)
             _check(comm, sends_np, res_np, dtype)
 
 
-@pytest.mark.parametrize("shape_count", [1000, 60001])  # one-shot, two-shot at N=4
+@pytest.mark.parametrize("tma", [0, 1])
+@pytest.mark.parametrize("shape_count", [1000, 300001])  # one-shot, two-shot at N=4
 @pytest.mark.parametrize("clusters", [1, 3])
 @pytest.mark.parametrize("threads", [64, 256])
-def test_many_epochs_per_cluster(shape_count, clusters, threads):
+def test_many_epochs_per_cluster(shape_count, clusters, threads, tma):
     """Few clusters looping over many small slices: every sub-buffer of the
     device API's window is reused many times, each reuse relying on the
-    receive-before-resend order; ragged last slice."""
+    receive-before-resend order; ragged last slice; st.async sends and bulk
+    sends."""
     n, dtype = 4, "fp32"
     with rra.Comm(n, shape_count * 4) as comm:
+        comm.set_attr("cluster_tma", tma)
         comm.set_attr("ctas_per_rank", clusters)
         comm.set_attr("threads", threads)
         comm.set_attr("cluster_slice", 16 * n * 3)  # 12 vectors per slice
         for it in range(2):
-            sends_np, res_np = _case(n, shape_count, dtype, clusters, threads, it)
+            sends_np, res_np = _case(n, shape_count, dtype, clusters, threads, it, tma)
             _check(comm, sends_np, res_np, dtype)
 
 
@@ -132,11 +140,12 @@ def test_graph_replay():
                     assert np.array_equal(got[i, r], expect[r]), (rep, i, r)
 
 
-@pytest.mark.parametrize("n", [4, 20])
-@pytest.mark.parametrize("count", [1000, 60001])
-def test_dropped_rank_times_out_and_reset(count, n):
+@pytest.mark.parametrize("n,tma", [(4, 0), (4, 1), (20, -1)])
+@pytest.mark.parametrize("count", [1000, 300001])
+def test_dropped_rank_times_out_and_reset(count, n, tma):
     dtype = "fp32"
     with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cluster_tma", tma)
         comm.set_attr("poll_timeout_ms", 20)
         comm.set_attr("ctas_per_rank", 2)
         comm.inject_drop(n - 3)

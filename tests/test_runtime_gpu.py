@@ -262,7 +262,7 @@ def test_plan_kernel_names_the_launched_kernel():
     global-memory kernels and their wide variants."""
     with rra.Comm(4, 1 << 20) as comm:
         assert comm.plan_kernel(32, "fp32", "auto") == "cluster_tma_kernel<one-shot>"
-        assert comm.plan_kernel(1 << 18, "fp32", "auto") == "cluster_kernel<two-shot>"  # N^2 M = 16 MiB
+        assert comm.plan_kernel(1 << 18, "fp32", "auto") == "cluster_tma_kernel<two-shot>"  # N^2 M = 16 MiB
         assert comm.plan_kernel(1 << 16, "fp32", "twoshot_cluster") == "cluster_tma_kernel<two-shot>"
         assert comm.plan_kernel(32, "fp32", "oneshot_sentinel") == "oneshot_kernel<sentinel>"
         assert comm.plan_kernel(32, "fp32", "twoshot_direct") == "twoshot_kernel<direct>"
