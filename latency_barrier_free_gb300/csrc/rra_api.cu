@@ -482,8 +482,10 @@ static rra_status_t plan_cluster_multi(rra_comm* c, size_t count, rra_dtype_t dt
 // Two-shot slices that do not fit in one wave of clusters run on the
 // persistent, double-buffered kernel instead: as many clusters as can be
 // resident, each looping over its share of the slices.
+// host: the buffers are pinned host memory (read and written over
+// NVLink-C2C), where larger copies measured faster.
 static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo, Params* p,
-                                 int* threads, int* mode) {
+                                 int* threads, int* mode, bool host = false) {
     const bool two = algo == RRA_TWOSHOT_CLUSTER;
     const size_t n = (size_t)c->nranks;
     if (c->nranks > rra::kClusterMaxRanks) return plan_cluster_multi(c, count, dtype, two, p, threads, mode);
@@ -515,7 +517,7 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     const bool bulk = c->cluster_pipe == 0 && bulk_copy_push(c, two, count * elem_size(dtype));
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
-    } else if (two && bulk && n * p->nvec <= (256u << 10)) {
+    } else if (two && bulk && !host && n * p->nvec <= (256u << 10)) {
         // bulk-copy two-shot up to N M = 4 MiB: partitions of 64 vectors
         // (1 KiB copies), one reduced position per thread (GB300 sweep at
         // N = 4, 8, 16: 1 MiB at N = 4 in 2.85 us against 3.6 us with the
@@ -875,8 +877,16 @@ rra_status_t rra_comm_plan_kernel(rra_comm_t c, size_t count, rra_dtype_t dtype,
     return RRA_OK;
 }
 
+static rra_status_t run_allreduce(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                                  rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream, bool host);
+
 rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
                            rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
+    return run_allreduce(c, send, recv, count, dtype, algo, stream, false);
+}
+
+static rra_status_t run_allreduce(rra_comm_t c, const void* const send[], void* const recv[], size_t count,
+                                  rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream, bool host) {
     if (c == nullptr || send == nullptr || recv == nullptr) return RRA_ERR_INVALID_ARG;
     if (!valid_dtype(dtype) || !valid_algo(algo)) return RRA_ERR_INVALID_ARG;
     if (c->poisoned) return RRA_ERR_POISONED;
@@ -889,7 +899,7 @@ rra_status_t rra_allreduce(rra_comm_t c, const void* const send[], void* const r
     int kind = 0, threads = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
+        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind, host)
                                            : plan_call(c, count, dtype, algo, &p, &kind, &threads);
         if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
             algo = select_global(c->nranks, count * es);
@@ -953,7 +963,7 @@ rra_status_t rra_allreduce_mapped(rra_comm_t c, const void* const send[], void* 
                                   rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
     if (c == nullptr) return RRA_ERR_INVALID_ARG;
     if (c->host_status == nullptr) return RRA_ERR_OOM;  // its allocation failed at creation
-    rra_status_t st = rra_allreduce(c, send, recv, count, dtype, algo, stream);
+    rra_status_t st = run_allreduce(c, send, recv, count, dtype, algo, stream, true);
     if (st != RRA_OK || count == 0) return st;
     return sync_status(c, (cudaStream_t)stream);
 }
@@ -992,7 +1002,7 @@ rra_status_t rra_allreduce_host(rra_comm_t c, const void* const send[], void* co
             mrecv[r] = b.devicePointer;
         }
         if (mapped) {
-            rra_status_t st = rra_allreduce(c, msend, mrecv, count, dtype, algo, stream);
+            rra_status_t st = run_allreduce(c, msend, mrecv, count, dtype, algo, stream, true);
             if (st != RRA_OK) return st;
             return finish();
         }
