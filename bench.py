@@ -148,10 +148,29 @@ def measured_peaks():
         return {}
 
 
+KERNEL_SOURCES = ("latency_barrier_free_gb300/csrc/kernels.cu", "latency_barrier_free_gb300/csrc/cluster.cu",
+                  "latency_barrier_free_gb300/csrc/coll.cu", "latency_barrier_free_gb300/csrc/fused.cu",
+                  "latency_barrier_free_gb300/csrc/prims.cuh", "latency_barrier_free_gb300/csrc/cluster_prims.cuh",
+                  "latency_barrier_free_gb300/csrc/rra_internal.h", "include/rra_device.cuh")
+
+
+def strip_comments(text):
+    """C/C++ source without its comments and blank lines (the kernel sources
+    hold no comment markers inside string literals)."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha():
+    """Hash of the device code's sources, comments and blank lines left out:
+    the source a profile's DRAM traffic belongs to."""
     h = hashlib.sha256()
-    for f in ("kernels.cu", "cluster.cu", "coll.cu", "fused.cu", "prims.cuh", "cluster_prims.cuh", "rra_internal.h"):
-        h.update(open(os.path.join(ROOT, "latency_barrier_free_gb300", "csrc", f), "rb").read())
+    for f in KERNEL_SOURCES:
+        h.update(f.encode() + b"\0")
+        h.update(strip_comments(open(os.path.join(ROOT, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

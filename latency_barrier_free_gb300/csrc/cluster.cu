@@ -7,11 +7,13 @@
 // shared memory.  A cluster holds one CTA per virtual rank for one slice of
 // the message; CTA r's shared memory is rank r's window for that slice.  A
 // CTA reads only its own rank's input and writes only into peers' windows
-// (and, for the two-shot, into every rank's output).  A push is an st.async,
-// which also completes the receiver's mbarrier transaction count: the
-// receiver waits on its own mbarrier -- the arrival of the bytes is the
-// signal -- and adds the N contributions in rank order (bit-identical to the
-// other fixed-order kernels).
+// (and, for the two-shot, into every rank's output).  A push is an st.async
+// (cluster_kernel), or a TMA bulk copy straight from the rank's input
+// (cluster_tma_kernel, multicast to all N CTAs for the one-shot); either
+// completes the receiver's mbarrier transaction count: the receiver waits on
+// its own mbarrier -- the arrival of the bytes is the signal -- and adds the
+// N contributions in rank order (bit-identical to the other fixed-order
+// kernels).
 //
 //   one-shot: rank r pushes its whole slice into slot [r] of every peer; each
 //             CTA reduces the slice and stores it into its own rank's output.
