@@ -86,3 +86,18 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "us/call" and d["higher_is_better"] is False
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["warmup"] >= 3
+
+
+def test_source_hash_ignores_comments_not_code():
+    """The hash that ties a committed DRAM-traffic figure to the device code:
+    a comment or blank-line edit keeps it, any code edit changes it."""
+    src = "int a; // note\n/* block\n comment */\n\n__device__ int f() { return 1; }\n"
+    same = "int a;\n// another note\n__device__ int f() { return 1; }   \n"
+    other = "int a;\n__device__ int f() { return 2; }\n"
+    assert bench.strip_comments(src) == bench.strip_comments(same)
+    assert bench.strip_comments(src) != bench.strip_comments(other)
+    assert bench.strip_comments('asm volatile("mov.u32 %0, 1;");') == 'asm volatile("mov.u32 %0, 1;");'
+    h = bench.kernel_source_sha()
+    assert len(h) == 16 and h == bench.kernel_source_sha()
+    entries = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))["entries"]
+    assert entries and all(len(e["source_sha"]) == 16 for e in entries)
