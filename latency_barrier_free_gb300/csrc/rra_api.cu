@@ -473,15 +473,19 @@ static rra_status_t plan_cluster_multi(rra_comm* c, size_t count, rra_dtype_t dt
 }
 
 // Plan of a cluster call: one cluster of N CTAs per slice of S vectors, CTA
-// r of a cluster = rank r.  S: one position per thread while the message is
-// small; past that, about two CTAs per SM in one wave, up to one batch of
-// kClusterBatch loads per thread (GB300 sweep: 16 KiB slices of 128 threads
-// were fastest from 4 MiB up at N = 2..16); at most the 96 KiB stage (N x S
-// vectors for the one-shot, S for the two-shot, whose S is a multiple of N).
+// r of a cluster = rank r, the push made by bulk copies (cluster_tma_kernel)
+// unless RRA_ATTR_CLUSTER_TMA is 0 or the persistent two-shot is asked for.
+// S: for the bulk-copy two-shot up to N M = 4 MiB on device buffers,
+// partitions of 64 vectors; otherwise one position per thread while the
+// message is small, then about two CTAs per SM in one wave, up to one batch
+// of kClusterBatch loads per thread (GB300 sweep: 16 KiB slices of 128
+// threads were fastest from 4 MiB up at N = 2..16); at most the 96 KiB stage
+// (N x S vectors for the one-shot, S for the two-shot, whose S is a multiple
+// of N).
 //
-// Two-shot slices that do not fit in one wave of clusters run on the
-// persistent, double-buffered kernel instead: as many clusters as can be
-// resident, each looping over its share of the slices.
+// With RRA_ATTR_CLUSTER_PIPE (off by default) the two-shot runs on the
+// persistent, double-buffered kernel: as many clusters as can be resident,
+// each looping over its share of the slices.
 // host: the buffers are pinned host memory (read and written over
 // NVLink-C2C), where larger copies measured faster.
 static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo, Params* p,
@@ -1099,11 +1103,11 @@ rra_status_t rra_reduce(rra_comm_t c, int root, const void* const send[], void* 
     return run_coll(c, rra::kCollReduce, root, send, recv, count, dtype, stream);
 }
 
-// AllReduce + residual add (fused.cu): the one-shot shape while N^2 M <= 1 MiB
-// (as RRA_AUTO's cluster choice), the two-shot shape above.  Slices as for
-// the cluster AllReduce, within a stage of two sub-buffers; one cluster per
-// slice unless RRA_ATTR_CTAS_PER_RANK caps the clusters (then each loops
-// over several slices, one epoch each).
+// AllReduce + residual add (fused.cu): the shape (one- or two-shot) and the
+// push (bulk copies or st.async) that RRA_AUTO's cluster AllReduce would
+// take.  Slices as for the cluster AllReduce, within a stage of two
+// sub-buffers; one cluster per slice unless RRA_ATTR_CTAS_PER_RANK caps the
+// clusters (then each loops over several slices, one epoch each).
 static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, rra::FusedParams* f,
                                   int* threads, bool* two_shot, bool* bulk_out) {
     *bulk_out = false;
