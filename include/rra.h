@@ -85,10 +85,11 @@ typedef enum {
                                   scheduled, so inputs must not hold the all-ones
                                   pattern */
     RRA_ONESHOT_CLUSTER = 7,   /* one-shot push through distributed shared memory: one
-                                  thread-block cluster of N CTAs per slice (CTA r = rank r),
-                                  st.async into peers' shared memory completes their
-                                  mbarrier (arrival of the bytes is the signal); no state
-                                  between calls.  For N > 16 the clusters have 16 CTAs and
+                                  thread-block cluster of N CTAs per slice (CTA r = rank r);
+                                  the push -- a TMA bulk copy of the slice with cluster
+                                  multicast (default, RRA_ATTR_CLUSTER_TMA), or st.async
+                                  stores -- completes the peers' mbarrier (arrival of the
+                                  bytes is the signal); no state between calls.  For N > 16 the clusters have 16 CTAs and
                                   CTA j hosts ranks j, j+16, ... (pushes go to the 15 other
                                   CTAs; still the rank-order sum of all N) */
     RRA_TWOSHOT_CLUSTER = 8,   /* two-shot through distributed shared memory: rank r pushes
@@ -335,11 +336,12 @@ rra_status_t rra_reduce(rra_comm_t comm, int root, const void* const send[], voi
  *   send, residual, recv: host arrays of nranks device pointers, 16-byte
  *   aligned, count elements each; recv[r] may equal send[r] or residual[r].
  * Shape: one thread-block cluster of nranks CTAs per slice; each rank
- * pushes its slice to every peer's shared memory while
- * nranks^2 * count * element size <= 1 MiB, and to one partition owner
- * each above that, the owner then writing every rank's output with that
- * rank's residual (outputs and residuals are then treated as registered
- * symmetric buffers, as by RRA_TWOSHOT_DIRECT).  Above 16 ranks: the
+ * pushes its slice to every peer's shared memory (one-shot) or each
+ * partition to its owner (two-shot), the owner then writing every rank's
+ * output with that rank's residual (outputs and residuals are then treated
+ * as registered symmetric buffers, as by RRA_TWOSHOT_DIRECT).  The shape is
+ * the one RRA_AUTO's cluster AllReduce takes (rra_select_algo); the pushes
+ * are the device API's bulk sends unless RRA_ATTR_CLUSTER_TMA is 0.  Above 16 ranks: the
  * many-rank cluster AllReduce (16-CTA clusters, CTA j acting for ranks j,
  * j + 16, ...; one-shot while 16 * nranks * count * element size <= 1 MiB)
  * with the residual add in its epilogue instead of the device-API kernel.
