@@ -168,9 +168,7 @@ static rra_algo_t select_cluster(int nranks, size_t bytes, bool bulk_copy) {
 // Whether a cluster call (N <= 16) pushes by bulk copies: unless the
 // attribute turns it off (it measured faster at every N = 2..16 and every
 // size from 128 B to 64 MiB on GB300).
-static bool bulk_copy_push(const rra_comm* c, bool two, size_t bytes) {
-    (void)two;
-    (void)bytes;
+static bool bulk_copy_push(const rra_comm* c) {
     return c->nranks <= rra::kClusterMaxRanks && c->cluster_tma != 0;
 }
 
@@ -518,7 +516,7 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     size_t S;
     size_t T = (size_t)c->threads;
     const size_t s_mid = ceil_div((size_t)p->nvec * n, 512);  // ~512 CTAs in all
-    const bool bulk = c->cluster_pipe == 0 && bulk_copy_push(c, two, count * elem_size(dtype));
+    const bool bulk = c->cluster_pipe == 0 && bulk_copy_push(c);
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
     } else if (two && bulk && !host && n * p->nvec <= (256u << 10)) {
@@ -1131,7 +1129,7 @@ static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, 
     }
     // shape and push as the cluster AllReduce would take them
     const bool two = select_cluster(c->nranks, count * es, c->cluster_tma != 0) == RRA_TWOSHOT_CLUSTER;
-    const bool bulk = bulk_copy_push(c, two, count * es);
+    const bool bulk = bulk_copy_push(c);
     int& fits = c->residual_fits[bulk ? 1 : 0][two ? 1 : 0][(int)dtype];
     if (fits < 0)
         fits = rra::residual_max_active(dtype, two, bulk, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
