@@ -148,10 +148,11 @@ def measured_peaks():
         return {}
 
 
-KERNEL_SOURCES = ("latency_barrier_free_gb300/csrc/kernels.cu", "latency_barrier_free_gb300/csrc/cluster.cu",
-                  "latency_barrier_free_gb300/csrc/coll.cu", "latency_barrier_free_gb300/csrc/fused.cu",
-                  "latency_barrier_free_gb300/csrc/prims.cuh", "latency_barrier_free_gb300/csrc/cluster_prims.cuh",
-                  "latency_barrier_free_gb300/csrc/rra_internal.h", "include/rra_device.cuh")
+# The translation unit of the profiled kernels (cluster_kernel,
+# cluster_tma_kernel): cluster.cu and every header it includes.
+KERNEL_SOURCES = ("latency_barrier_free_gb300/csrc/cluster.cu", "latency_barrier_free_gb300/csrc/cluster_prims.cuh",
+                  "latency_barrier_free_gb300/csrc/prims.cuh", "latency_barrier_free_gb300/csrc/rra_internal.h",
+                  "include/rra.h")
 
 
 def strip_comments(text):
@@ -165,8 +166,8 @@ def strip_comments(text):
 
 
 def kernel_source_sha():
-    """Hash of the device code's sources, comments and blank lines left out:
-    the source a profile's DRAM traffic belongs to."""
+    """Hash of the profiled kernels' sources, comments and blank lines left
+    out: the source a profile's DRAM traffic belongs to."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         h.update(f.encode() + b"\0")
