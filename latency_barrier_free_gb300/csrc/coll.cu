@@ -220,6 +220,79 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
     }
 }
 
+// AllGather and Broadcast up to 16 ranks with the push made by the TMA
+// engine: one multicast bulk copy per slice from the sender's input into
+// slot [r] of every CTA's window (AllGather) or into slot [0] (Broadcast,
+// from the root; the root's own window included), completing each CTA's
+// mbarrier.  Every CTA then writes its output from its window.  Whole
+// 16-byte vectors are copied: the last vector of an input whose size is not
+// a multiple of 16 bytes is read in full (it lies in the same 16-byte block,
+// so the same page, as valid data) and its extra lanes are never stored.  A
+// CTA leaves after a cluster barrier that every CTA reaches once its own
+// bytes are in, so no copy it issued is still in flight.
+template <typename T, int kOp>
+__global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(16) uint4 stage[];  // AllGather [N][S], Broadcast [S]
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint32_t root = (uint32_t)p.root;
+    const uint64_t count = p.count;
+    const uint32_t incoming = kOp == kCollAllGather ? N * npos : npos;  // vectors, the own copy included
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, incoming * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    cluster_wait();  // every peer's barrier exists before any copy completes on it
+    if (threadIdx.x == 0 && (kOp == kCollAllGather || r == root)) {
+        const uint16_t mask = drop != (int32_t)r ? (uint16_t)((1u << N) - 1u) : (uint16_t)(1u << r);
+        bulk_g2s_multicast(smem_u32(stage + (kOp == kCollAllGather ? r * S : 0u)),
+                           (const char*)p.send[r] + (size_t)base * kVecBytes, npos * (uint32_t)kVecBytes, my_bar,
+                           mask);
+    }
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
+    if (ok) {
+        if (kOp == kCollAllGather) {
+#pragma unroll 1
+            for (uint32_t v = threadIdx.x; v < N * npos; v += nt) {
+                const uint32_t q = v / npos;
+                const uint32_t u = v - q * npos;
+                store_block<T>(p.recv[r], (uint64_t)q * count, base + u, count, stage[q * S + u]);
+            }
+        } else {
+#pragma unroll 1
+            for (uint32_t u = threadIdx.x; u < npos; u += nt) store_block<T>(p.recv[r], 0, base + u, count, stage[u]);
+        }
+    }
+    cluster_wait();  // every CTA's bytes are in: none of my copies is still in flight
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 // The same four collectives for nranks > 16 (clusters hold at most 16
 // CTAs): a cluster of G = 16 CTAs per slice, CTA j acting for ranks j,
 // j + G, j + 2G, ... (as the many-rank cluster AllReduce).  A push to a rank
@@ -564,8 +637,27 @@ static const void* coll_kernel_for(int op, bool multi) {
     return nullptr;
 }
 
+// AllGather and Broadcast up to 16 ranks: the bulk-copy kernel.
+static bool coll_bulk(int op, int nranks) {
+    return (op == kCollAllGather || op == kCollBroadcast) && nranks <= kClusterMaxRanks;
+}
+
+template <typename T>
+static const void* coll_bulk_for(int op) {
+    return op == kCollAllGather ? (const void*)coll_bulk_kernel<T, kCollAllGather>
+                                : (const void*)coll_bulk_kernel<T, kCollBroadcast>;
+}
+
 static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks) {
     const bool multi = nranks > kClusterMaxRanks;
+    if (coll_bulk(op, nranks)) {
+        switch (dtype) {
+            case RRA_FP32: return coll_bulk_for<float>(op);
+            case RRA_BF16: return coll_bulk_for<__nv_bfloat16>(op);
+            case RRA_FP64: return coll_bulk_for<double>(op);
+        }
+        return nullptr;
+    }
     switch (dtype) {
         case RRA_FP32: return coll_kernel_for<float>(op, multi);
         case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op, multi);
@@ -580,7 +672,7 @@ static int coll_cdim(int nranks) { return nranks < kClusterMaxRanks ? nranks : k
 // Opt a kernel in to the full stage and to clusters of up to 16 CTAs (once
 // per kernel; the attributes are process-wide).
 static cudaError_t configure_coll(const void* k) {
-    static const void* done[30] = {};
+    static const void* done[40] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
