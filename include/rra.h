@@ -278,8 +278,10 @@ rra_status_t rra_allreduce_mapped(rra_comm_t comm, const void* const send[], voi
  * primitives serve these four.  Here all four run one thread-block cluster
  * of nranks CTAs per slice, CTA r acting for rank r, and exchange data
  * through distributed shared memory: a push is an st.async into a peer's
- * shared memory that completes the peer's mbarrier, and the only wait is a
- * bounded wait on one's own mbarrier (data arrival is the signal).  Above
+ * shared memory (AllGather and Broadcast up to 16 ranks: one TMA bulk copy
+ * of the slice with cluster multicast) that completes the peer's mbarrier,
+ * and the only wait is a bounded wait on one's own mbarrier (data arrival
+ * is the signal).  Above
  * 16 ranks (the cluster limit) a cluster has 16 CTAs and CTA j acts for
  * ranks j, j + 16, j + 32, ...; pushes between ranks of one CTA are plain
  * shared-memory stores.  Nothing persists between calls.
