@@ -173,3 +173,35 @@ def test_many_rank_collectives_accounting(op):
         for S, nvec in ((1, 3), (5, 13), (8, 8), (7, 30)):
             for root in sorted({0, N - 1, 16 % N, N // 2}):
                 _coll_multi(op, N, S, nvec, root)
+
+
+def _coll_bulk(op, N, S, nvec, root):
+    """coll_bulk_kernel (AllGather, Broadcast up to 16 ranks): one multicast
+    copy per sender and slice, the sender's own window included."""
+    stage = N * S if op == "ag" else S
+    for base, npos in _slices(nvec, S):
+        writes = [dict() for _ in range(N)]
+        got = [0] * N
+        senders = range(N) if op == "ag" else (root,)
+        for r in senders:
+            assert (base + npos) * 16 <= nvec * 16
+            for c in range(N):
+                for u in range(npos):
+                    slot = (r * S if op == "ag" else 0) + u
+                    assert slot < stage
+                    writes[c][slot] = writes[c].get(slot, 0) + 1
+                got[c] += npos * 16
+        for c in range(N):
+            assert got[c] == (N if op == "ag" else 1) * npos * 16  # the armed expectation
+            assert all(v == 1 for v in writes[c].values())
+            for q in (range(N) if op == "ag" else (0,)):
+                for u in range(npos):
+                    assert writes[c].get((q * S if op == "ag" else 0) + u) == 1
+
+
+@pytest.mark.parametrize("op", ["ag", "bc"])
+def test_bulk_copy_collectives_accounting(op):
+    for N in (2, 3, 4, 8, 16):
+        for S, nvec in ((1, 3), (5, 13), (64, 100), (7, 30)):
+            for root in sorted({0, N - 1, N // 2}):
+                _coll_bulk(op, N, S, nvec, root)
