@@ -8,7 +8,9 @@ kernel's pushes write and how many bytes each CTA's mbarrier expects:
   cluster_multi_kernel N > 16: 16-CTA clusters, CTA j acting for ranks
                        j, j + 16, ...; st.async pushes to the other CTAs,
                        plain stores for ranks of the same CTA;
-  coll_multi_kernel    the four other collectives above 16 ranks.
+  coll_multi_kernel    the four other collectives above 16 ranks;
+  coll_bulk_kernel     AllGather and Broadcast up to 16 ranks by multicast
+                       bulk copies.
 The checks: every write lands inside the launch's stage and is made
 exactly once; the bytes a CTA receives from other CTAs (or, for bulk
 copies, from every copy that targets it) equal what it arms its mbarrier
