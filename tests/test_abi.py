@@ -137,3 +137,53 @@ def test_auto_selection_by_size_and_ranks():
         assert all(p in twoshot for p in picks[first:])
     with pytest.raises(rra.RraError):
         rra.select_algo(1, 128)
+
+
+def _declarations():
+    """name -> list of parameter declarations, from include/*.h."""
+    out = {}
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^\s*(?:const\s+)?\w+\**\s+\**(rra_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M):
+            params = [p.strip() for p in m.group(2).split(",")]
+            out[m.group(1)] = [] if params == ["void"] or params == [""] else params
+    return out
+
+
+def _kind(param):
+    """Coarse C kind of one parameter declaration."""
+    if "*" in param or "[" in param or param.split()[0] in ("rra_comm_t", "rra_stream_t"):
+        return "pointer"
+    base = param.replace("const ", "").split()[0]
+    # size_t and uint64_t are the same 64-bit unsigned type on the 64-bit targets (as in ctypes)
+    return {"size_t": "u64", "int": "int", "double": "double", "int64_t": "int64", "uint64_t": "u64",
+            "rra_dtype_t": "int", "rra_algo_t": "int", "rra_attr_t": "int", "rra_status_t": "int"}.get(base, base)
+
+
+def _ctype_kind(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "pointer"
+    return {ctypes.c_size_t: "u64", ctypes.c_uint64: "u64", ctypes.c_int: "int", ctypes.c_double: "double",
+            ctypes.c_int64: "int64"}.get(t, repr(t))
+
+
+def test_binding_prototypes_match_the_headers():
+    """Every function the ctypes binding gives a prototype takes as many
+    arguments, of the same coarse kinds, as its declaration in include/*.h."""
+    decls = _declarations()
+    lib = rra.load()
+    checked = 0
+    for name in rra.SYMBOLS:
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert name in decls, name
+        want = [_kind(p) for p in decls[name]]
+        got = [_ctype_kind(t) for t in fn.argtypes]
+        assert got == want, (name, got, want)
+        checked += 1
+    assert checked >= 30
