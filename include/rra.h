@@ -38,6 +38,20 @@
  * fault the GPU, later calls on the same communicator become no-ops on the
  * device, rra_comm_status() reports them, and the communicator stays
  * poisoned (RRA_ERR_POISONED) until rra_comm_reset().
+ *
+ * Bulk-copy pushes stay on one GPU.  Some cluster kernels push by TMA bulk
+ * copies with cluster multicast (cp.async.bulk ... .multicast::cluster) that
+ * read straight from the callers' input buffers: the cluster one-/two-shot
+ * AllReduce and the fused residual AllReduce up to 16 ranks, and AllGather and
+ * Broadcast up to 16 ranks.  A call uses them only when (a) every buffer such
+ * a copy reads is device memory of the current GPU -- checked with
+ * cudaPointerGetAttributes at both ends of the range read, the result of a
+ * passing check remembered for the last 8 sets of input pointers of the
+ * communicator -- and (b) the process holds no active context on any other
+ * GPU.  Host buffers (rra_allreduce_host, rra_allreduce_mapped), another
+ * GPU's memory, managed memory, and processes that also drive other GPUs
+ * always get the st.async push (the same results).  rra_comm_last_kernel
+ * names the kernel a call launched.
  */
 #ifndef RRA_H
 #define RRA_H
@@ -63,8 +77,7 @@ typedef enum {
     RRA_ERR_OOM = 3,             /* device allocation failed */
     RRA_ERR_NOT_CORESIDENT = 4,  /* N ranks cannot all be resident at once */
     RRA_ERR_TIMEOUT = 5,         /* a device-side poll gave up (see status) */
-    RRA_ERR_POISONED = 6,        /* an earlier device error; call rra_comm_reset */
-    RRA_ERR_EPOCH = 7            /* reserved (epochs are scrubbed on the device) */
+    RRA_ERR_POISONED = 6         /* an earlier device error; call rra_comm_reset */
 } rra_status_t;
 
 typedef enum { RRA_FP32 = 0, RRA_BF16 = 1, RRA_FP64 = 2 } rra_dtype_t;
@@ -87,8 +100,9 @@ typedef enum {
     RRA_ONESHOT_CLUSTER = 7,   /* one-shot push through distributed shared memory: one
                                   thread-block cluster of N CTAs per slice (CTA r = rank r);
                                   the push -- a TMA bulk copy of the slice with cluster
-                                  multicast (default, RRA_ATTR_CLUSTER_TMA), or st.async
-                                  stores -- completes the peers' mbarrier (arrival of the
+                                  multicast (default, RRA_ATTR_CLUSTER_TMA, only on inputs
+                                  in this GPU's device memory: see "Bulk-copy pushes" above),
+                                  or st.async stores -- completes the peers' mbarrier (arrival of the
                                   bytes is the signal); no state between calls.  For N > 16 the clusters have 16 CTAs and
                                   CTA j hosts ranks j, j+16, ... (pushes go to the 15 other
                                   CTAs; still the rank-order sum of all N) */
@@ -113,10 +127,14 @@ typedef enum {
     RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256; while
                                       it is not set, the cluster two-shot may use 256 for
                                       messages up to ~1-2 MiB per rank */
-    RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step; 0 (default) = the step
+    RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step (RRA_TWOSHOT_DBUF,
+                                      RRA_TWOSHOT_DIRECT); 0 (default) = one 16-byte position
+                                      per thread of the largest co-resident grid, at most the
+                                      step whose live ReduceScatter scratch over all windows
+                                      is ~32 MiB, within the per-window scratch cap */
+    RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step; 0 = the step
                                       whose live scratch over all windows is ~32 MiB (stays
                                       in L2), within the per-window scratch cap */
-    RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step; 0 = as above */
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
     RRA_ATTR_ONESHOT_WIDE = 6,     /* the one-shot's polls and the LL128-atomic kernel's adds
                                       and polls split a position's sources over threads:
@@ -160,9 +178,11 @@ typedef enum {
                                       the push made by the TMA engine: bulk copies from a
                                       rank's input into the peers' shared memory (multicast
                                       to all N for the one-shot, one copy per partition
-                                      owner for the two-shot).  -1 (default) and 1: on
-                                      (faster at every N and size measured); 0: st.async
-                                      pushes */
+                                      owner for the two-shot); also the fused residual
+                                      AllReduce, AllGather and Broadcast.  -1 (default) and
+                                      1: on (faster at every N and size measured) for calls
+                                      whose inputs pass the check of "Bulk-copy pushes"
+                                      above; 0: st.async pushes always */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
@@ -356,10 +376,24 @@ rra_status_t rra_allreduce_residual(rra_comm_t comm, const void* const send[], c
                                     rra_stream_t stream);
 
 /* Synchronise the device and return the device status word: RRA_OK, or the
- * first device-side error (e.g. RRA_ERR_TIMEOUT).  A device error poisons the
- * communicator until rra_comm_reset().  If `rank`/`step` are non-NULL they
- * receive the virtual rank and step that recorded the error (-1 if none). */
-rra_status_t rra_comm_status(rra_comm_t comm, int* rank, int* step);
+ * first device-side error (e.g. RRA_ERR_TIMEOUT); RRA_ERR_POISONED if an
+ * earlier call of this function saw one and no rra_comm_reset followed.  A
+ * device error poisons the communicator until rra_comm_reset(). */
+rra_status_t rra_comm_status(rra_comm_t comm);
+
+/* Where the first device-side error was recorded: synchronises the device
+ * and stores the virtual rank and the chunk step of the call that recorded it
+ * (-1 and -1 when the status word is clear).  Returns RRA_OK (also when an
+ * error is recorded: read it with rra_comm_status), RRA_ERR_INVALID_ARG for
+ * NULL arguments, RRA_ERR_CUDA. */
+rra_status_t rra_comm_error_site(rra_comm_t comm, int* rank, int* step);
+
+/* The kernel (as rra_comm_plan_kernel names it, e.g.
+ * "cluster_tma_kernel<one-shot>" or "coll_bulk_kernel<all_gather>") that the
+ * last call enqueued on this communicator launched: AllReduce, host and
+ * mapped AllReduce, the four collectives, the fused residual AllReduce.
+ * "none" before the first call.  *name points to a static string. */
+rra_status_t rra_comm_last_kernel(rra_comm_t comm, const char** name);
 
 /* Synchronise the device, re-initialise every window (sentinels, flags,
  * accumulators, counters), the epoch and the status word, and clear the
@@ -383,8 +417,9 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
                              size_t scratch_twoshot, rra_layout_t* out);
 
 /* The kernel (the __global__ function, and its variant) that rra_allreduce
- * launches for this call on this communicator, e.g.
- * "cluster_tma_kernel<one-shot>" -- the name a profiler's launch list shows.
+ * launches for this call on this communicator when its buffers are device
+ * memory of this GPU, e.g. "cluster_tma_kernel<one-shot>" -- the name a
+ * profiler's launch list shows.
  * *name points to a static string.  Needs a device (plans the call,
  * including occupancy queries); count > 0. */
 rra_status_t rra_comm_plan_kernel(rra_comm_t comm, size_t count, rra_dtype_t dtype, rra_algo_t algo,
@@ -431,9 +466,10 @@ rra_status_t rra_comm_set_timing(rra_comm_t comm, uint64_t* dev_buf);
  * tracing off. */
 rra_status_t rra_comm_set_trace(rra_comm_t comm, uint64_t* dev_buf);
 
-/* Fault injection for tests (host-side injection only; no GPU fault): while
- * set, virtual rank `rank` skips every store to its peers, so the peers'
- * polls run into their time limit and record RRA_ERR_TIMEOUT.  rank = -1
+/* Fault injection for tests (host-side injection only; no GPU fault): in every
+ * call enqueued (or captured) while it is set, virtual rank `rank` skips every
+ * store to its peers, so the peers' polls run into their time limit and record
+ * RRA_ERR_TIMEOUT.  The rank travels in the kernel parameters.  rank = -1
  * clears it; rra_comm_reset also clears it.  Synchronises the device. */
 rra_status_t rra_comm_inject_drop(rra_comm_t comm, int rank);
 

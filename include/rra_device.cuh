@@ -56,6 +56,13 @@
  * completes each destination's mbarrier like an st.async.  A CTA that
  * bulk-sends calls sent() only after its last wait(): finish() then also
  * means that every copy into every window of the team has landed.
+ * Source rule: a bulk send's source range must lie entirely in device
+ * memory of the GPU the kernel runs on -- not host memory (pinned, mapped
+ * or managed), not another GPU's memory reached through peer access -- and
+ * bulk sends belong only in kernels of a process that drives this one GPU
+ * alone.  The caller checks this on the host before choosing a kernel with
+ * bulk sends (librra does so with cudaPointerGetAttributes, and otherwise
+ * launches its st.async variant); send() and bcast() have no such rule.
  *
  * Every wait is bounded by a %globaltimer deadline: a rank that never
  * sends makes its receivers return false from wait(), never hang.
@@ -167,7 +174,9 @@ class Team {
     // rank's own bit included if wanted), by one bulk copy with cluster
     // multicast.  Counts nvec * 16 bytes toward each destination's
     // expectation for this epoch -- this rank's own slot too, unlike put().
-    // src must stay unchanged until every destination has waited.
+    // src must stay unchanged until every destination has waited, and
+    // [src, src + 16 nvec) must be device memory of this GPU (the source
+    // rule above).
     __device__ void bulk_bcast(uint32_t i, const void* src, uint32_t nvec, uint32_t ranks) const {
         const uint32_t off = ((sub() * nranks_ + rank_) * slot_vecs_ + i) * 16u;
         asm volatile(

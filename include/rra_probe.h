@@ -44,6 +44,21 @@ rra_status_t rra_probe_l2_chase(size_t buf_bytes, uint64_t hops, uint64_t seed,
 rra_status_t rra_probe_pingpong(int cta_a, int cta_b, int iters,
                                 double* ns_round_trip, int* sm_a, int* sm_b);
 
+/* The same floor for the cluster kernels, whose ranks exchange data through
+ * distributed shared memory.  Two CTAs of one thread-block cluster play
+ * ping-pong with TMA bulk copies: each turn copies 128 bytes from an
+ * L2-resident device buffer into the other CTA's shared memory, and the
+ * copy's arrival completes that CTA's mbarrier, on which it waits.  Outputs:
+ * mean ns per round trip over `iters` turns after `iters`/8 warm-up turns;
+ * mean ns per cluster barrier (relaxed arrive, acquire wait) over `iters`
+ * back-to-back barriers; the two SM ids.  Half the round trip (the input
+ * read and the push in one) plus one cluster barrier (the one such a kernel
+ * passes before its first push) is the floor of one push through shared
+ * memory.  Errors: RRA_ERR_INVALID_ARG, RRA_ERR_OOM, RRA_ERR_TIMEOUT (a wait
+ * passed 1 s), RRA_ERR_CUDA. */
+rra_status_t rra_probe_dsmem_pingpong(int iters, double* ns_round_trip, double* ns_cluster_barrier,
+                                      int* sm_a, int* sm_b);
+
 /* Launch one empty kernel (1 CTA, 32 threads) on `stream`, to measure launch
  * and graph-node overhead next to the AllReduce. */
 rra_status_t rra_probe_empty_kernel(rra_stream_t stream);

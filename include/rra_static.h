@@ -3,10 +3,12 @@
  *
  * The paper has no counterpart to this entry point; it exists for callers of
  * this library that cannot allocate device memory when they need an
- * AllReduce: code running while another component captures a CUDA graph (where
- * cudaMalloc is refused), plug-ins whose host framework owns the GPU allocator
- * and forbids direct cudaMalloc/cudaFree, and latency-critical paths that must
- * not pay for an allocation.
+ * AllReduce: plug-ins and extensions whose host framework owns the GPU
+ * allocator and forbids direct cudaMalloc/cudaFree (they are handed their
+ * input and output buffers and nothing else), processes that reserve their
+ * whole device-memory budget up front and may not grow it, and
+ * latency-critical paths that must not pay for an allocation or for the
+ * device-wide synchronisation that freeing memory can imply.
  */
 #ifndef RRA_STATIC_H
 #define RRA_STATIC_H
@@ -38,15 +40,19 @@ extern "C" {
  *               RRA_ERR_TIMEOUT if a wait ran out).  NULL skips the copy.
  *   stream      CUDA stream.
  * Set-up: the first call on a device (with that device current) looks up the
- * array's device address with cudaGetSymbolAddress, initialises it with one
- * kernel and synchronises the device; make that first call before any stream
- * capture starts.  Later calls only enqueue work on `stream`.
+ * array's device address with cudaGetSymbolAddress and queries occupancy; make
+ * that first call before any stream capture starts.  The array needs no
+ * initialisation: all-zero, its state when the module loads, is the idle state.
+ * Every call looks the address up again on the host, and redoes the set-up if
+ * it moved (after cudaDeviceReset the module is loaded anew).
  * Sharing: every call on a device uses the same array, which keeps the last
- * call's contents.  Each call clears the status word before its kernel; LL
- * flags need no clearing because every call uses new epochs.  Calls whose work
- * overlaps on the GPU (different streams, or several host threads without
- * ordering) race on the array and give wrong results: order them on one
- * stream.
+ * call's contents.  A call enqueues two kernels on `stream`: a one-CTA kernel
+ * that, only if the previous call recorded an error, returns the whole array
+ * to the idle state (so one failed call does not spoil the next), then the
+ * AllReduce.  LL flags need no clearing after a successful call because every
+ * call uses new epochs.  Calls whose work overlaps on the GPU (different
+ * streams, or several host threads without ordering) race on the array and
+ * give wrong results: order them on one stream.
  * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_CUDA, RRA_ERR_NOT_CORESIDENT.
  */
 rra_status_t rra_allreduce_static(int nranks, const void* const send[], void* const recv[], size_t count,

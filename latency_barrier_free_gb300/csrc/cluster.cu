@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
         x[j] = make_uint4(0, 0, 0, 0);
         if (v < npos) x[j] = load_input<T>(src, base + v, p.count);
     }
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
                                                                    : nullptr;
     if (tr) {
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant_
     cluster_arrive_relaxed();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
                                                                    : nullptr;
     if (tr) {
@@ -324,7 +324,7 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
     cluster_arrive_relaxed();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     // item it = (hosted rank m, vector v)
     const uint32_t items = hosted * npos;
     uint4 x[kClusterBatch];
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(256) cluster_pipe_kernel(const __grid_constant
             if (v < npos) x[j] = load_input<T>(src, base + v, p.count);
         }
     }
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     const uint32_t full0 = smem_u32(&full[0]);    // full[b] at full0 + 8 b
     const uint32_t empty0 = smem_u32(&empty[0]);  // empty[b] at empty0 + 8 b
     if (threadIdx.x == 0) {

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
     const void* src = p.send[r];
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     const bool pushes = drop != (int32_t)r;
 
     // input item v: block q = v / npos (ReduceScatter; else 0), vector u
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ 
     cluster_arrive_relaxed();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     cluster_wait();  // every peer's barrier exists before any copy completes on it
     if (threadIdx.x == 0 && (kOp == kCollAllGather || r == root)) {
         const uint16_t mask = drop != (int32_t)r ? (uint16_t)((1u << N) - 1u) : (uint16_t)(1u << r);
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
     cluster_arrive_relaxed();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     const uint32_t per_rank = kOp == kCollReduceScatter ? N * npos : npos;  // items per hosted rank
 
     uint4 x[kClusterBatch];
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
     const void* src = p.send[r];
-    const bool pushes = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank) != (int32_t)r;
+    const bool pushes = p.drop_rank != (int32_t)r;
     const uint32_t items = kBcast ? (is_root ? npos : 0u) : npos;
     uint4 x[kClusterBatch];
     auto load_batch = [&](uint32_t b0) {
@@ -637,9 +637,22 @@ static const void* coll_kernel_for(int op, bool multi) {
     return nullptr;
 }
 
-// AllGather and Broadcast up to 16 ranks: the bulk-copy kernel.
-static bool coll_bulk(int op, int nranks) {
+// AllGather and Broadcast up to 16 ranks have a bulk-copy kernel.
+bool coll_has_bulk(int op, int nranks) {
     return (op == kCollAllGather || op == kCollBroadcast) && nranks <= kClusterMaxRanks;
+}
+
+const char* coll_kernel_name(int op, int nranks, bool bulk) {
+    static const char* const kBulk[] = {"", "coll_bulk_kernel<all_gather>", "coll_bulk_kernel<broadcast>"};
+    static const char* const kPlain[] = {"coll_kernel<reduce_scatter>", "coll_kernel<all_gather>",
+                                         "coll_kernel<broadcast>", "coll_kernel<reduce>"};
+    static const char* const kMulti[] = {"coll_multi_kernel<reduce_scatter>", "coll_multi_kernel<all_gather>",
+                                         "coll_multi_kernel<broadcast>", "coll_multi_kernel<reduce>"};
+    if (op < 0 || op > kCollReduceSplit) return "unknown";
+    if (op == kCollBroadcastSplit) return "coll_split_kernel<broadcast>";
+    if (op == kCollReduceSplit) return "coll_split_kernel<reduce>";
+    if (bulk && coll_has_bulk(op, nranks)) return kBulk[op];
+    return nranks > kClusterMaxRanks ? kMulti[op] : kPlain[op];
 }
 
 template <typename T>
@@ -648,9 +661,9 @@ static const void* coll_bulk_for(int op) {
                                 : (const void*)coll_bulk_kernel<T, kCollBroadcast>;
 }
 
-static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks) {
+static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks, bool bulk) {
     const bool multi = nranks > kClusterMaxRanks;
-    if (coll_bulk(op, nranks)) {
+    if (bulk && coll_has_bulk(op, nranks)) {
         switch (dtype) {
             case RRA_FP32: return coll_bulk_for<float>(op);
             case RRA_BF16: return coll_bulk_for<__nv_bfloat16>(op);
@@ -708,7 +721,8 @@ size_t coll_stage_bytes(const Params& p, int op) {
     }
 }
 
-cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl) {
+cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl,
+                        bool bulk) {
     const size_t smem = coll_stage_bytes(p, op);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kMaxRanks || p.root < 0 ||
         p.root >= p.nranks)
@@ -716,7 +730,7 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
     if ((op == kCollBroadcastSplit || op == kCollReduceSplit) && p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
     const int cdim = coll_cdim(p.nranks);
-    const void* k = coll_kernel_ptr(dtype, op, p.nranks);
+    const void* k = coll_kernel_ptr(dtype, op, p.nranks, bulk);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = configure_coll(k);
     if (e != cudaSuccess) return e;
@@ -743,8 +757,8 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
     return cudaLaunchKernelExC(&cfg, k, args);
 }
 
-int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem) {
-    const void* k = coll_kernel_ptr(dtype, op, nranks);
+int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem, bool bulk) {
+    const void* k = coll_kernel_ptr(dtype, op, nranks, bulk);
     if (k == nullptr || configure_coll(k) != cudaSuccess) {
         cudaGetLastError();
         return 0;

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
     // cluster barrier that guards the peers' windows completes
     if (!kBulk) load_batch(cid * S, npos_of(cid), 0);
     prefetch_residual(cid * S, mine_of(cid, r));
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
+    const int32_t drop = p.drop_rank;
     const bool pushes = drop != (int32_t)r;
     uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
                                                                    : nullptr;

@@ -42,11 +42,12 @@ __device__ __forceinline__ char* window(const Params& p, int r) {
 
 // Per-CTA prologue/epilogue shared by all kernels.
 struct CtaState {
-    uint64_t epoch;  // epoch of step 0 of this call
+    uint64_t epoch;  // epoch of step 0 of this call (0 when the call needs none)
     uint64_t t_start;
     int rank, sub;
     bool skip;       // earlier device error, or epoch wrap: do nothing
     bool drop;       // injected fault: do not store to peers
+    bool advance;    // the call uses epochs: advance them at exit
 };
 
 // Epoch scrub (once per kScrubPeriod steps).  Every CTA of the co-resident
@@ -59,7 +60,8 @@ __device__ __noinline__ bool epoch_scrub(const Params& p, int rank) {
     const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t n1 = p.ll_bytes / 16, n2 = p.llag_bytes / 16;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    for (int q = 0; q < p.nranks; ++q) {
+    const int nwin = p.scrub_ranks > 0 ? p.scrub_ranks : p.nranks;
+    for (int q = 0; q < nwin; ++q) {
         char* wq = p.win0 + (uint64_t)q * p.stride;
         for (uint64_t i = tid; i < n1; i += nthreads) st_relaxed_v4(wq + p.ll_off + i * 16, z);
         for (uint64_t i = tid; i < n2; i += nthreads) st_relaxed_v4(wq + p.llag_off + i * 16, z);
@@ -101,22 +103,39 @@ __device__ __forceinline__ void pdl_entry() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-__device__ __forceinline__ CtaState cta_prologue(const Params& p) {
+// The parameter fields the AllReduce kernels use, read once before the kernel
+// waits for its predecessor (griddepcontrol.wait): a first read of a
+// parameter line misses the constant cache (about 0.1 us each on GB300), and
+// these misses are then paid while the previous kernel drains instead of one
+// after another on the critical path.  Touches no global memory.
+__device__ __forceinline__ void warm_params(const Params& p) {
+    const unsigned r = blockIdx.x / (unsigned)p.ctas_per_rank;
+    asm volatile("" : : "l"(p.win0), "l"(p.ctrl), "l"(p.timing), "l"(p.trace), "l"(p.stride), "l"(p.count),
+                 "l"(p.timeout_ns), "l"(p.region_off), "l"(p.slot_bytes), "l"(p.parity_bytes), "l"(p.aux_off));
+    asm volatile("" : : "r"(p.nvec), "r"(p.chunk_vecs), "r"(p.per_cta), "r"(p.nsteps), "r"(p.nranks),
+                 "r"(p.epoch_slots), "r"(p.drop_rank), "l"(p.send[r]), "l"(p.recv[r]));
+}
+
+// need_epoch: the call uses epochs (LL flags, or the parity of a multi-step
+// call's double buffering).  A single-step call on sentinel slots needs none:
+// at a call boundary every sentinel slot is idle, so it uses parity 0, reads
+// no epoch and leaves the epoch unchanged.
+__device__ __forceinline__ CtaState cta_prologue(const Params& p, bool need_epoch = true) {
     CtaState s;
     s.t_start = globaltimer_ns();
     s.rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
     s.sub = (int)(blockIdx.x % (unsigned)p.ctas_per_rank);
     if (threadIdx.x == 0 && p.timing != nullptr) p.timing[2 * blockIdx.x] = s.t_start;
-    s.epoch = ld_relaxed_u64(&p.ctrl->epoch[blockIdx.x]);
+    s.advance = need_epoch;
+    s.epoch = need_epoch ? ld_relaxed_u64(&p.ctrl->epoch_m1[blockIdx.x]) + 1ull : 0ull;
     const uint32_t status = ld_relaxed_u32(&p.ctrl->status);
-    const int32_t drop = (int32_t)ld_relaxed_u32(&p.ctrl->drop_rank);
     s.skip = status != 0u;
-    s.drop = drop == s.rank;
+    s.drop = p.drop_rank == s.rank;
     // The epochs of this call are [epoch, epoch + nsteps); if they would reach
     // the next multiple of kScrubPeriod, scrub first and restart one past it.
     // The test depends only on the epoch, which every thread of every CTA
     // reads equal, so the whole grid takes this branch together.
-    if ((s.epoch & (kScrubPeriod - 1)) + (uint64_t)p.nsteps + 1ull >= kScrubPeriod) {
+    if (need_epoch && (s.epoch & (kScrubPeriod - 1)) + (uint64_t)p.nsteps + 1ull >= kScrubPeriod) {
         if (epoch_scrub(p, s.rank)) s.epoch = (s.epoch | (kScrubPeriod - 1)) + 2ull;
         else s.skip = true;
     }
@@ -125,13 +144,15 @@ __device__ __forceinline__ CtaState cta_prologue(const Params& p) {
 
 __device__ __forceinline__ void cta_epilogue(const Params& p, const CtaState& s) {
     __syncthreads();  // every thread has read its epoch slot
-    if (!s.skip) {
+    if (!s.skip && s.advance) {
         // Advance every epoch slot this CTA owns: slots b, b + G, b + 2G, ...
-        const uint64_t next = s.epoch + p.nsteps;
+        // Plain stores: the slots are read only by later kernels, after the
+        // kernel boundary (or griddepcontrol.wait) has made them visible.
+        const uint64_t next_m1 = s.epoch + p.nsteps - 1ull;
         const unsigned G = gridDim.x;
         for (unsigned slot = blockIdx.x + threadIdx.x * G; slot < (unsigned)p.epoch_slots;
              slot += blockDim.x * G) {
-            st_relaxed_u64(&p.ctrl->epoch[slot], next);
+            st_weak_u64(&p.ctrl->epoch_m1[slot], next_m1);
         }
     }
     if (threadIdx.x == 0) {
@@ -252,7 +273,7 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s,
     Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
     uint64_t* const tr = (p.trace != nullptr && threadIdx.x == 0) ? p.trace + (uint64_t)blockIdx.x * kTracePoints
                                                                    : nullptr;
-    if (tr) tr[1] = globaltimer_after(s.epoch);
+    if (tr) tr[1] = globaltimer_after(s.epoch + (uint64_t)s.skip);  // epoch and status words arrived
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -299,10 +320,6 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s,
                         M::add(acc, x);
                         M::add(acc2, x2);
                     }
-                    if (!kLL && q != r) {
-                        st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                        if (two) st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                    }
                 }
             }
             const uint4 out = M::store(acc);
@@ -310,6 +327,16 @@ __device__ __forceinline__ bool oneshot_body(const Params& p, const CtaState& s,
             store_output<T>(p.recv[r], base + v, p.count, out);
             if (two) store_output<T>(p.recv[r], base + v2, p.count, M::store(acc2));
             if (tr && k == 0 && v == pos0) tr[4] = globaltimer_ns();
+            // sentinel: the consumed slots back to the sentinel (after the
+            // output, which is what the caller waits for)
+            if (!kLL) {
+#pragma unroll 1
+                for (int q = 0; q < N; ++q) {
+                    if (q == r) continue;
+                    st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                    if (two) st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
+                }
+            }
         }
     }
     return true;
@@ -418,36 +445,14 @@ __device__ __forceinline__ bool prefetch_first(const Params& p, uint4& pre) {
     return true;
 }
 
-// Warm the lines (and address translations) a one-shot thread touches first:
-// its slot in every peer window (both parities: the epoch is not known yet),
-// the slots it will poll in its own window, and its output.  Small N only.
-template <bool kLL>
-__device__ __forceinline__ void prefetch_paths(const Params& p) {
-    constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
-    const uint32_t sub = blockIdx.x % (unsigned)p.ctas_per_rank;
-    const int r = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
-    const uint32_t v = sub * p.per_cta + threadIdx.x;
-    if (p.nranks > 8 || v >= min((sub + 1u) * p.per_cta, min(p.chunk_vecs, p.nvec))) return;
-    const uint64_t pos = (uint64_t)v * kPosBytes;
-    for (int q = 0; q < p.nranks; ++q) {
-        if (q == r) continue;
-        const char* peer = window(p, q) + p.region_off + (uint64_t)r * p.slot_bytes + pos;
-        const char* mine = window(p, r) + p.region_off + (uint64_t)q * p.slot_bytes + pos;
-        prefetch_l2(peer);
-        prefetch_l2(peer + p.parity_bytes);
-        prefetch_l2(mine);
-        prefetch_l2(mine + p.parity_bytes);
-    }
-    prefetch_l2((const char*)p.recv[r] + (uint64_t)v * kVecBytes);
-}
-
 template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_kernel(const __grid_constant__ Params p) {
-    pdl_entry();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    warm_params(p);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     uint4 pre;
     const bool has_pre = prefetch_first<T>(p, pre);
-    prefetch_paths<kLL>(p);
-    const CtaState s = cta_prologue(p);
+    const CtaState s = cta_prologue(p, kLL || p.nsteps > 1);
     if (!s.skip) (void)oneshot_body<T, kLL>(p, s, has_pre ? &pre : nullptr);
     cta_epilogue(p, s);
 }
@@ -456,11 +461,13 @@ template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_wide_kernel(const __grid_constant__ Params p) {
     __shared__ uint4 stage[kStageVecs];
     __shared__ int fail;
-    pdl_entry();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    warm_params(p);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     uint4 pre;
     const bool has_pre = prefetch_first<T>(p, pre);
     if (threadIdx.x == 0) fail = 0;
-    CtaState s = cta_prologue(p);
+    CtaState s = cta_prologue(p, kLL || p.nsteps > 1);
     s.skip = __syncthreads_or(s.skip) != 0;  // block barriers follow: skip must be CTA-uniform
     if (!s.skip) (void)oneshot_wide_body<T, kLL>(p, s, stage, &fail, has_pre ? &pre : nullptr);
     cta_epilogue(p, s);
@@ -680,10 +687,10 @@ __global__ void __launch_bounds__(256) barrier_probe_kernel(const __grid_constan
     const Params& q = p;
     if (!s.skip) {  // epoch bookkeeping as for any call; no per-CTA timing here
         __syncthreads();
-        const uint64_t next = s.epoch + q.nsteps;
+        const uint64_t next_m1 = s.epoch + q.nsteps - 1ull;
         for (unsigned slot = blockIdx.x + threadIdx.x * gridDim.x; slot < (unsigned)q.epoch_slots;
              slot += blockDim.x * gridDim.x)
-            st_relaxed_u64(&q.ctrl->epoch[slot], next);
+            st_relaxed_u64(&q.ctrl->epoch_m1[slot], next_m1);
     }
 }
 
@@ -724,15 +731,162 @@ __device__ __forceinline__ Split split_step(const Params& p, uint32_t k) {
 // Sec. II-B), so the AllGather needs no scratch, no poll and no reset: one
 // synchronisation hop per step instead of two.  Outputs are complete when the
 // kernel completes; nothing inside the kernel reads them.
+//
+// Shape (for bandwidth): a thread handles one position of the partitions at a
+// time; the push issues the input loads of up to kLoadParts partitions, the
+// receive phases the polls of up to kPollParts sources, before waiting for
+// any of them.  The planner gives each thread about one position per step and
+// as many co-resident CTAs as the occupancy allows, so a step keeps the whole
+// GPU's loads in flight; the kernel is built for 4 CTAs of 128 threads per SM
+// (at most 128 registers per thread: it needs about that many without
+// spilling).
+constexpr int kPollParts = 4;  // sources polled with loads in flight at once (two-shot)
+
+// L2 policies of the two-shot: its scratch is written and read back within a
+// step (keep it in L2), its inputs and outputs stream through once.
+struct TwoshotHints {
+    uint64_t keep, stream;
+};
+
+// ReduceScatter push of position v of this step: part q of my input ->
+// owner q's RS slot [r], the inputs of kLoadParts partitions loaded together.
+template <typename T>
+__device__ __forceinline__ void twoshot_push(const Params& p, const Split sp, int r, uint32_t v, uint64_t par_off,
+                                             TwoshotHints h) {
+    constexpr int U = VecMath<T>::kUnitBytes;
+    const int N = p.nranks;
+    const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+#pragma unroll 1
+    for (int q0 = 0; q0 < N; q0 += kLoadParts) {
+        uint4 x[kLoadParts];
+#pragma unroll
+        for (int j = 0; j < kLoadParts; ++j) {
+            const int q = q0 + j;
+            if (q < N && q != r && v < sp.valid(q)) x[j] = load_input_hint<T>(p.send[r], sp.vec(q, v), p.count, h.stream);
+        }
+#pragma unroll
+        for (int j = 0; j < kLoadParts; ++j) {
+            const int q = q0 + j;
+            if (q < N && q != r && v < sp.valid(q)) st_scratch_hint<U>(window(p, q) + off, x[j], h.keep);
+        }
+    }
+}
+
+// One poll of a two-shot scratch vector (sentinel).
+template <typename T>
+__device__ __forceinline__ bool twoshot_poll(const char* slot, uint64_t pol, uint4& out) {
+    constexpr int U = VecMath<T>::kUnitBytes;
+    out = ld_scratch_hint<U>(slot, pol);
+    return sentinel_arrived<U>(out);
+}
+
+// Owner of position v: poll the N-1 RS slots (kPollParts sources in flight),
+// add in rank order, push the sum to every peer's AG slot [r] (kDirect: into
+// every peer's output), store my own output, then reset the consumed slots
+// (plain stores: the next writer of a slot is ordered after this thread by
+// the credit chain -- the fence of a later step, or the kernel boundary).
 template <typename T, bool kDirect>
-__device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s) {
+__device__ __forceinline__ bool twoshot_own(const Params& p, const Split sp, int r, bool drop, uint32_t v,
+                                            uint64_t par_off, Waiter& w, TwoshotHints h) {
     using M = VecMath<T>;
     constexpr int U = M::kUnitBytes;
-    const int N = p.nranks, r = s.rank;
+    const int N = p.nranks;
+    const uint4 own = load_input_hint<T>(p.send[r], sp.vec(r, v), p.count, h.stream);
+    char* const slot0 = window(p, r) + p.region_off + par_off + (uint64_t)v * kVecBytes;
+    typename M::Acc acc;
+#pragma unroll 1
+    for (int q0 = 0; q0 < N; q0 += kPollParts) {
+        uint4 val[kPollParts];
+        bool ok[kPollParts];
+#pragma unroll
+        for (int j = 0; j < kPollParts; ++j) {
+            const int q = q0 + j;
+            ok[j] = true;
+            if (q < N && q != r) ok[j] = twoshot_poll<T>(slot0 + (uint64_t)q * p.slot_bytes, h.keep, val[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kPollParts; ++j) {
+            const int q = q0 + j;
+            while (!ok[j]) {
+                if (waiter_expired(w)) return false;
+                ok[j] = twoshot_poll<T>(slot0 + (uint64_t)q * p.slot_bytes, h.keep, val[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPollParts; ++j) {
+            const int q = q0 + j;
+            if (q >= N) break;
+            const uint4 x = (q == r) ? own : val[j];
+            if (q == 0) acc = M::load(x);
+            else M::add(acc, x);
+        }
+    }
+    const uint4 red = M::store(acc);
+    if (!drop) {
+        if (kDirect) {
+#pragma unroll 1
+            for (int q = 0; q < N; ++q)
+                if (q != r) store_output_hint<T>(p.recv[q], sp.vec(r, v), p.count, red, h.stream);
+        } else {
+            char* dst = p.win0 + p.aux_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
+#pragma unroll 1
+            for (int q = 0; q < N; ++q, dst += p.stride)
+                if (q != r) st_scratch_hint<U>(dst, red, h.keep);
+        }
+    }
+    store_output_hint<T>(p.recv[r], sp.vec(r, v), p.count, red, h.stream);
+#pragma unroll 1
+    for (int q = 0; q < N; ++q)
+        if (q != r) st_weak_v4_hint(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec(), h.keep);
+    return true;
+}
+
+// AllGather receive of position v: the N-1 reduced partitions of the other
+// owners (sources whose partition does not reach v are skipped), polled
+// kPollParts at a time, stored into my output, the slots reset (plain stores,
+// as in twoshot_own).
+template <typename T>
+__device__ __forceinline__ bool twoshot_gather(const Params& p, const Split sp, int r, uint32_t v, uint64_t par_off,
+                                               Waiter& w, TwoshotHints h) {
+    const int N = p.nranks;
+    char* const slot0 = window(p, r) + p.aux_off + par_off + (uint64_t)v * kVecBytes;
+#pragma unroll 1
+    for (int q0 = 0; q0 < N; q0 += kPollParts) {
+        uint4 val[kPollParts];
+        bool ok[kPollParts];
+#pragma unroll
+        for (int j = 0; j < kPollParts; ++j) {
+            const int q = q0 + j;
+            ok[j] = true;
+            if (q < N && q != r && v < sp.valid(q)) ok[j] = twoshot_poll<T>(slot0 + (uint64_t)q * p.slot_bytes, h.keep, val[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kPollParts; ++j) {
+            const int q = q0 + j;
+            while (!ok[j]) {
+                if (waiter_expired(w)) return false;
+                ok[j] = twoshot_poll<T>(slot0 + (uint64_t)q * p.slot_bytes, h.keep, val[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPollParts; ++j) {
+            const int q = q0 + j;
+            if (q < N && q != r && v < sp.valid(q)) {
+                store_output_hint<T>(p.recv[r], sp.vec(q, v), p.count, val[j], h.stream);
+                st_weak_v4_hint(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec(), h.keep);
+            }
+        }
+    }
+    return true;
+}
+
+template <typename T, bool kDirect>
+__device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s) {
+    const int r = s.rank;
     const uint32_t pos0 = (uint32_t)s.sub * p.per_cta;
     const uint32_t pos1 = pos0 + p.per_cta;
-    char* const mine = window(p, r);
     Waiter w = make_waiter(s.t_start, p.timeout_ns, p.ctrl, r, 0);
+    const TwoshotHints h{l2_keep_policy(), l2_stream_policy()};
 
 #pragma unroll 1
     for (uint32_t k = 0; k < p.nsteps; ++k) {
@@ -742,130 +896,27 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
         const uint32_t end = min(pos1, sp.part);
         w.step = (int)k;
         if (k > 0 && p.nsteps > 2) fence_acq_rel_gpu();
-
-        // ReduceScatter push: part q of my input -> owner q's RS slot [r];
-        // the inputs of kLoadParts partitions are loaded together
         if (!s.drop) {
 #pragma unroll 1
-            for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) {
-                const uint64_t off = p.region_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)v * kVecBytes;
-#pragma unroll 1
-                for (int q0 = 0; q0 < N; q0 += kLoadParts) {
-                    uint4 x[kLoadParts];
-#pragma unroll
-                    for (int j = 0; j < kLoadParts; ++j) {
-                        const int q = q0 + j;
-                        if (q < N && q != r && v < sp.valid(q)) x[j] = load_input<T>(p.send[r], sp.vec(q, v), p.count);
-                    }
-#pragma unroll
-                    for (int j = 0; j < kLoadParts; ++j) {
-                        const int q = q0 + j;
-                        if (q < N && q != r && v < sp.valid(q)) st_scratch<U>(window(p, q) + off, x[j]);
-                    }
-                }
-            }
+            for (uint32_t v = pos0 + threadIdx.x; v < end; v += blockDim.x) twoshot_push<T>(p, sp, r, v, par_off, h);
         }
-        // Owner: reduce my partition in rank order, push it to every AG slot
         const uint32_t my_end = min(end, sp.valid(r));
 #pragma unroll 1
-        for (uint32_t v = pos0 + threadIdx.x; v < my_end; v += 2 * blockDim.x) {
-            const uint32_t v2 = v + blockDim.x;
-            const bool two = v2 < my_end;
-            const uint4 own = load_input<T>(p.send[r], sp.vec(r, v), p.count);
-            const uint4 own2 = two ? load_input<T>(p.send[r], sp.vec(r, v2), p.count) : make_uint4(0, 0, 0, 0);
-            char* const slot0 = mine + p.region_off + par_off + (uint64_t)v * kVecBytes;
-            char* const slot2 = mine + p.region_off + par_off + (uint64_t)v2 * kVecBytes;
-            typename M::Acc acc, acc2;
+        for (uint32_t v = pos0 + threadIdx.x; v < my_end; v += blockDim.x)
+            if (!twoshot_own<T, kDirect>(p, sp, r, s.drop, v, par_off, w, h)) return false;
 #pragma unroll 1
-            for (int q0 = 0; q0 < N; q0 += kBatch) {
-                uint4 val[kBatch], val2[kBatch];
-                bool ok[kBatch], ok2[kBatch];
-                poll_issue<T, false>(slot0, p.slot_bytes, q0, N, r, 0u, val, ok);
-                poll_issue<T, false>(slot2, p.slot_bytes, q0, two ? N : 0, r, 0u, val2, ok2);
-                if (!poll_finish<T, false>(slot0, p.slot_bytes, q0, 0u, w, val, ok)) return false;
-                if (!poll_finish<T, false>(slot2, p.slot_bytes, q0, 0u, w, val2, ok2)) return false;
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    if (q >= N) break;
-                    const uint4 x = (q == r) ? own : val[j];
-                    const uint4 x2 = (q == r) ? own2 : val2[j];
-                    if (q == 0) {
-                        acc = M::load(x);
-                        acc2 = M::load(x2);
-                    } else {
-                        M::add(acc, x);
-                        M::add(acc2, x2);
-                    }
-                    if (q != r) {
-                        st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                        if (two) st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                    }
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (h == 1 && !two) break;
-                const uint32_t vv = h ? v2 : v;
-                const uint4 red = M::store(h ? acc2 : acc);
-                if (kDirect) {
-                    if (!s.drop) {
-#pragma unroll 1
-                        for (int q = 0; q < N; ++q) {
-                            if (q != r) store_output<T>(p.recv[q], sp.vec(r, vv), p.count, red);
-                        }
-                    }
-                } else if (!s.drop) {
-                    char* dst = p.win0 + p.aux_off + par_off + (uint64_t)r * p.slot_bytes + (uint64_t)vv * kVecBytes;
-#pragma unroll 1
-                    for (int q = 0; q < N; ++q, dst += p.stride) {
-                        if (q != r) st_scratch<U>(dst, red);
-                    }
-                }
-                store_output<T>(p.recv[r], sp.vec(r, vv), p.count, red);
-            }
-        }
-        // AllGather receive: the N-1 reduced partitions of the other owners,
-        // two positions at a time; sources whose partition does not reach a
-        // position are skipped (the direct variant has nothing to receive)
-#pragma unroll 1
-        for (uint32_t v = pos0 + threadIdx.x; !kDirect && v < end; v += 2 * blockDim.x) {
-            const uint32_t v2 = v + blockDim.x;
-            const bool two = v2 < end;
-            char* const slot0 = mine + p.aux_off + par_off + (uint64_t)v * kVecBytes;
-            char* const slot2 = mine + p.aux_off + par_off + (uint64_t)v2 * kVecBytes;
-            auto has1 = [&](int q) { return v < sp.valid(q); };
-            auto has2 = [&](int q) { return v2 < sp.valid(q); };
-#pragma unroll 1
-            for (int q0 = 0; q0 < N; q0 += kBatch) {
-                uint4 val[kBatch], val2[kBatch];
-                bool ok[kBatch], ok2[kBatch];
-                poll_issue<T, false>(slot0, p.slot_bytes, q0, N, r, 0u, val, ok, has1);
-                poll_issue<T, false>(slot2, p.slot_bytes, q0, two ? N : 0, r, 0u, val2, ok2, has2);
-                if (!poll_finish<T, false>(slot0, p.slot_bytes, q0, 0u, w, val, ok)) return false;
-                if (!poll_finish<T, false>(slot2, p.slot_bytes, q0, 0u, w, val2, ok2)) return false;
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const int q = q0 + j;
-                    if (q < N && q != r && has1(q)) {
-                        store_output<T>(p.recv[r], sp.vec(q, v), p.count, val[j]);
-                        st_scratch<U>(slot0 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                    }
-                    if (two && q < N && q != r && has2(q)) {
-                        store_output<T>(p.recv[r], sp.vec(q, v2), p.count, val2[j]);
-                        st_scratch<U>(slot2 + (uint64_t)q * p.slot_bytes, sentinel_vec());
-                    }
-                }
-            }
-        }
+        for (uint32_t v = pos0 + threadIdx.x; !kDirect && v < end; v += blockDim.x)
+            if (!twoshot_gather<T>(p, sp, r, v, par_off, w, h)) return false;
     }
     return true;
 }
 
 template <typename T, bool kDirect>
-__global__ void __launch_bounds__(256) twoshot_kernel(const __grid_constant__ Params p) {
-    pdl_entry();
-    const CtaState s = cta_prologue(p);
+__global__ void __launch_bounds__(128, 4) twoshot_kernel(const __grid_constant__ Params p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    warm_params(p);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const CtaState s = cta_prologue(p, p.nsteps > 1);
     if (!s.skip) (void)twoshot_body<T, kDirect>(p, s);
     cta_epilogue(p, s);
 }
@@ -1225,7 +1276,9 @@ __device__ __forceinline__ bool ll128_wide_body(const Params& p, const CtaState&
 
 template <typename T>
 __global__ void __launch_bounds__(256) ll128_wide_kernel(const __grid_constant__ Params p) {
-    pdl_entry();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    warm_params(p);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     CtaState s = cta_prologue(p);
     s.skip = __syncthreads_or(s.skip) != 0;  // CTA-wide syncs follow: skip must be CTA-uniform
     if (!s.skip) (void)ll128_wide_body<T>(p, s);
@@ -1234,7 +1287,9 @@ __global__ void __launch_bounds__(256) ll128_wide_kernel(const __grid_constant__
 
 template <typename T>
 __global__ void __launch_bounds__(256) ll128_kernel(const __grid_constant__ Params p) {
-    pdl_entry();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    warm_params(p);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     CtaState s = cta_prologue(p);
     s.skip = __any_sync(0xFFFFFFFFu, s.skip) != 0;  // warp syncs follow: skip must be warp-uniform
     if (!s.skip) (void)ll128_body<T>(p, s);
@@ -1266,11 +1321,10 @@ __global__ void init_kernel(const __grid_constant__ InitParams ip) {
             ip.ctrl->status = 0u;
             ip.ctrl->err_rank = -1;
             ip.ctrl->err_step = -1;
-            ip.ctrl->drop_rank = -1;
             ip.ctrl->scrub_arrive = 0u;
             ip.ctrl->scrub_gen = 0u;
         }
-        for (int i = threadIdx.x; i < kEpochSlots; i += blockDim.x) ip.ctrl->epoch[i] = 1ull;
+        for (int i = threadIdx.x; i < kEpochSlots; i += blockDim.x) ip.ctrl->epoch_m1[i] = 0ull;  // epoch 1
     }
     for (int r = 0; r < ip.nranks; ++r) {
         for (int j = 0; j < ip.njobs; ++j) {

@@ -85,6 +85,10 @@ __device__ __forceinline__ void st_relaxed_u64(void* p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" : : "l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_weak_u64(void* p, uint64_t v) {
+    asm volatile("st.global.u64 [%0], %1;" : : "l"(p), "l"(v) : "memory");
+}
+
 // Output vector: plain store.
 __device__ __forceinline__ void st_output_v4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
@@ -120,6 +124,70 @@ __device__ __forceinline__ void red_add_u32(void* p, uint32_t a) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" : : "l"(p), "r"(a) : "memory");
 }
 
+// ------------------------------------------------- L2 residency hints ----
+// Cache policies for the bandwidth kernels: scratch that is written and read
+// back within a step stays in L2 (evict_last) while the inputs and outputs
+// that stream through once are the first to go (evict_first).
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_stream_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ld_input_v4_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_relaxed_v4_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void ld_relaxed_v2u64_hint(const void* p, uint64_t pol, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.L2::cache_hint.v2.u64 {%0,%1}, [%2], %3;"
+                 : "=l"(a), "=l"(b)
+                 : "l"(p), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v4_hint(void* p, uint4 v, uint64_t pol) {
+    asm volatile("st.relaxed.gpu.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v2u64_hint(void* p, uint64_t a, uint64_t b, uint64_t pol) {
+    asm volatile("st.relaxed.gpu.global.L2::cache_hint.v2.u64 [%0], {%1,%2}, %3;"
+                 :
+                 : "l"(p), "l"(a), "l"(b), "l"(pol)
+                 : "memory");
+}
+
+// Plain (weak) vector store with a policy: outputs, and sentinel resets whose
+// next reader is ordered after them by the credit chain (a fence or the
+// kernel boundary), never a concurrent poll.
+__device__ __forceinline__ void st_weak_v4_hint(void* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :
+                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- timer ----
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -128,11 +196,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // %globaltimer read that waits for `dep` (a value produced by an earlier load):
-// the read is control-dependent on it, so the stamp is taken after that load
-// has returned.  Diagnostics only.
+// a predicate is computed from `dep` inside the same asm block and guards the
+// timer read, so the stamp cannot be taken before that load has returned
+// (a C++ branch on `dep` may be turned into a select that reads the timer
+// first).  Diagnostics only.
 __device__ __forceinline__ uint64_t globaltimer_after(uint64_t dep) {
-    if (dep == 0x5A5A5A5A5A5A5A5Aull) return 0ull;
-    return globaltimer_ns();
+    uint64_t t;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.eq.u64 p, %1, 0x5A5A5A5A5A5A5A5A;\n\t"
+        "@p mov.u64 %0, 0;\n\t"
+        "@!p mov.u64 %0, %%globaltimer;\n\t}"
+        : "=l"(t)
+        : "l"(dep));
+    return t;
 }
 
 // ---------------------------------------------------------- LL packing ----
@@ -209,6 +286,27 @@ __device__ __forceinline__ uint4 ld_scratch(const void* p) {
         return make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
     } else {
         return ld_relaxed_v4(p);
+    }
+}
+
+// The same with an L2 policy (the bandwidth kernels).
+template <int kUnitBytes>
+__device__ __forceinline__ void st_scratch_hint(void* p, uint4 v, uint64_t pol) {
+    if (kUnitBytes == 8) {
+        st_relaxed_v2u64_hint(p, (uint64_t)v.x | ((uint64_t)v.y << 32), (uint64_t)v.z | ((uint64_t)v.w << 32), pol);
+    } else {
+        st_relaxed_v4_hint(p, v, pol);
+    }
+}
+
+template <int kUnitBytes>
+__device__ __forceinline__ uint4 ld_scratch_hint(const void* p, uint64_t pol) {
+    if (kUnitBytes == 8) {
+        uint64_t a, b;
+        ld_relaxed_v2u64_hint(p, pol, a, b);
+        return make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
+    } else {
+        return ld_relaxed_v4_hint(p, pol);
     }
 }
 
@@ -362,6 +460,15 @@ __device__ __forceinline__ uint4 load_input(const void* base, uint32_t vec, uint
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// load_input with an L2 policy for the full vectors (the ragged tail is read
+// as by load_input).
+template <typename T>
+__device__ __forceinline__ uint4 load_input_hint(const void* base, uint32_t vec, uint64_t count, uint64_t pol) {
+    constexpr int VE = VecMath<T>::kElems;
+    if ((uint64_t)vec * VE + VE <= count) return ld_input_v4_hint((const char*)base + (uint64_t)vec * kVecBytes, pol);
+    return load_input<T>(base, vec, count);
+}
+
 // Output vector `vec`; only elements below `count` are written.
 template <typename T>
 __device__ __forceinline__ void store_output(void* base, uint32_t vec, uint64_t count, uint4 v) {
@@ -385,4 +492,16 @@ __device__ __forceinline__ void store_output(void* base, uint32_t vec, uint64_t 
     }
 }
 
+// store_output with an L2 policy for full vectors.
+template <typename T>
+__device__ __forceinline__ void store_output_hint(void* base, uint32_t vec, uint64_t count, uint4 v, uint64_t pol) {
+    constexpr int VE = VecMath<T>::kElems;
+    if ((uint64_t)vec * VE + VE <= count) {
+        st_weak_v4_hint((char*)base + (uint64_t)vec * kVecBytes, v, pol);
+        return;
+    }
+    store_output<T>(base, vec, count, v);
+}
+
 }  // namespace rra
+

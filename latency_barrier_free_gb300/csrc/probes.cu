@@ -5,6 +5,11 @@
 // through an L2-resident buffer (the review of the paper points out that a
 // fence's latency is not a load-to-use time); L_remote_store as half the
 // round trip of a fence-free store/poll ping-pong between two SMs.
+// The same model for the transport of the cluster kernels: a bulk copy from
+// an L2-resident input straight into a peer CTA's shared memory, whose
+// arrival completes the peer's mbarrier (half the round trip of a bulk-copy
+// ping-pong inside one cluster), plus the one cluster barrier such a kernel
+// must pass before its first push.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,6 +18,7 @@
 #include <random>
 #include <vector>
 
+#include "cluster_prims.cuh"
 #include "rra.h"
 #include "rra_probe.h"
 
@@ -85,6 +91,69 @@ __global__ void pingpong_kernel(uint32_t* flags, int cta_a, int cta_b, int warm,
             st_relaxed(to_a, (uint32_t)i);
         }
     }
+}
+
+// Bulk-copy ping-pong between the two CTAs of a cluster.  CTA 0 copies 128
+// bytes from `src` (global memory, L2-resident after the first round) into
+// CTA 1's shared memory with one bulk copy that completes CTA 1's mbarrier;
+// CTA 1's wait returns and it answers the same way into CTA 0; CTA 0's wait
+// returns.  Then both run `iters` cluster barriers (relaxed arrive + acquire
+// wait, as the cluster kernels use them).  Every wait is bounded (1 s).
+// res[0] = ns of `iters` round trips after `warm`, res[1] = ns of `iters`
+// cluster barriers (CTA 0), res[2] = error flag, res[3], res[4] = SM ids.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32)
+    dsmem_pingpong_kernel(const uint4* src, int warm, int iters, uint64_t* res) {
+    __shared__ __align__(128) uint4 buf[8];
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t me = rra::cluster_ctarank();
+    const uint32_t peer = me ^ 1u;
+    const uint32_t bar_s = rra::smem_u32(&bar);
+    const uint32_t buf_s = rra::smem_u32(buf);
+    if (threadIdx.x == 0) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        res[3 + me] = smid;
+        rra::mbar_init(bar_s, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        rra::mbar_expect_tx(bar_s, 128u);  // the arrival of phase 0
+    }
+    __syncwarp();
+    rra::cluster_sync();  // both mbarriers exist
+    const uint64_t deadline = gtimer() + 1000000000ull;
+    int ok = 1;
+    uint32_t parity = 0;
+    uint64_t t0 = 0;
+    auto wait_own = [&]() {
+        uint32_t spins = 0;
+        while (!rra::mbar_try_wait(bar_s, parity)) {
+            if ((++spins & 63u) == 0u && gtimer() > deadline) return false;
+        }
+        return true;
+    };
+    for (int i = 0; i < warm + iters && ok; ++i) {
+        if (me == 0 && i == warm) t0 = gtimer();
+        if (me == 0) {
+            if (threadIdx.x == 0) rra::bulk_g2s_multicast(buf_s, src, 128u, bar_s, (uint16_t)(1u << peer));
+            ok = __all_sync(0xffffffffu, wait_own());  // warp-uniform: the cluster barriers below are .aligned
+            if (ok && threadIdx.x == 0) rra::mbar_expect_tx(bar_s, 128u);  // the arrival of the next phase
+        } else {
+            ok = __all_sync(0xffffffffu, wait_own());
+            if (ok && threadIdx.x == 0) {
+                rra::mbar_expect_tx(bar_s, 128u);
+                rra::bulk_g2s_multicast(buf_s, src, 128u, bar_s, (uint16_t)(1u << peer));
+            }
+        }
+        parity ^= 1u;
+    }
+    if (me == 0 && threadIdx.x == 0) res[0] = ok ? gtimer() - t0 : 0ull;
+    if (!ok && threadIdx.x == 0) res[2] = 1ull;
+    const uint64_t t1 = gtimer();
+    for (int i = 0; i < iters; ++i) {
+        rra::cluster_arrive_relaxed();
+        rra::cluster_wait();
+    }
+    if (me == 0 && threadIdx.x == 0) res[1] = gtimer() - t1;
+    rra::cluster_sync();  // no CTA leaves while a copy into the other may be in flight
 }
 
 __global__ void empty_kernel() {}
@@ -178,6 +247,37 @@ rra_status_t rra_probe_pingpong(int cta_a, int cta_b, int iters, double* ns_roun
     *ns_round_trip = (double)h[0] / (double)iters;
     if (sm_a) *sm_a = (int)h[1];
     if (sm_b) *sm_b = (int)h[2];
+    return RRA_OK;
+}
+
+rra_status_t rra_probe_dsmem_pingpong(int iters, double* ns_round_trip, double* ns_cluster_barrier, int* sm_a,
+                                      int* sm_b) {
+    if (ns_round_trip == nullptr || ns_cluster_barrier == nullptr || iters <= 0 || iters > (1 << 22))
+        return RRA_ERR_INVALID_ARG;
+    uint4* src = nullptr;
+    uint64_t* res = nullptr;
+    if (cudaMalloc((void**)&src, 128) != cudaSuccess) { cudaGetLastError(); return RRA_ERR_OOM; }
+    if (cudaMalloc((void**)&res, 64) != cudaSuccess) { cudaGetLastError(); cudaFree(src); return RRA_ERR_OOM; }
+    rra_status_t st = RRA_OK;
+    uint64_t h[8] = {};
+    if (cudaMemset(src, 0, 128) != cudaSuccess || cudaMemset(res, 0, 64) != cudaSuccess) st = RRA_ERR_CUDA;
+    if (st == RRA_OK) {
+        const int warm = std::max(1, iters / 8);
+        dsmem_pingpong_kernel<<<2, 32>>>(src, warm, iters, res);
+        if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+            cudaMemcpy(h, res, 64, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            st = RRA_ERR_CUDA;
+        }
+    }
+    cudaFree(src);
+    cudaFree(res);
+    if (st != RRA_OK) return st;
+    if (h[2] != 0) return RRA_ERR_TIMEOUT;
+    *ns_round_trip = (double)h[0] / (double)iters;
+    *ns_cluster_barrier = (double)h[1] / (double)iters;
+    if (sm_a) *sm_a = (int)h[3];
+    if (sm_b) *sm_b = (int)h[4];
     return RRA_OK;
 }
 

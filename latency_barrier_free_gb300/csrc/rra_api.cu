@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <array>
 #include <map>
 #include <mutex>
 
@@ -105,11 +106,23 @@ struct rra_comm {
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
     int cluster_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
-    int coll_fits[6][3] = {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1},
-                           {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}};  // [op][dtype]
+    int coll_fits[2][6][3] = {{{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}},
+                              {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}}};
+                              // [bulk-copy kernel][op][dtype]
     int64_t coll_split = -1;                // Broadcast/Reduce in two hops: -1 auto, 0 never, 1 always
     int residual_fits[2][2][3] = {{{-1, -1, -1}, {-1, -1, -1}}, {{-1, -1, -1}, {-1, -1, -1}}};  // [bulk][two][dtype]
     int residual_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
+    // source sets that passed the bulk-copy check (bulk_sources_local), newest
+    // overwriting the oldest
+    struct LocalSources {
+        int n = 0;
+        size_t bytes = 0;
+        const void* ptr[rra::kClusterMaxRanks] = {};
+    };
+    std::array<LocalSources, 8> local_sources;
+    int local_next = 0;
+    const char* last_kernel = "none";       // the kernel the last enqueued call launched
+    int32_t drop_rank = -1;                 // injected fault (rra_comm_inject_drop), -1 = none
     bool poisoned = false;
     uint64_t* timing = nullptr;
     uint64_t* trace = nullptr;
@@ -120,6 +133,101 @@ struct rra_comm {
     bool host_mirror = false;              // device code mirrors the status word into host_status
     std::mutex mu;
 };
+
+// ----------------------------------------------------------------------------
+// Where the bulk-copy push may run.  Its copies (cp.async.bulk ...
+// .multicast::cluster, issued by cluster_tma_kernel, coll_bulk_kernel and the
+// device API's bulk sends) read straight from the caller's buffers.  They are
+// issued only when every buffer they read is device memory of the
+// communicator's own GPU -- checked at both ends of the range a copy reads --
+// and the process holds no context on another GPU.  Any other call (host
+// memory, another GPU's memory, managed memory, or a process that also
+// drives other GPUs) pushes with st.async stores instead: the same results.
+
+namespace {
+
+// cuDevicePrimaryCtxGetState / cuDeviceGet, looked up once through the
+// runtime (no link against the driver library).
+typedef int (*PfnPrimaryCtxGetState)(int dev, unsigned int* flags, int* active);
+typedef int (*PfnDeviceGet)(int* dev, int ordinal);
+
+// True when the process holds an active primary context on a GPU other
+// than `dev`, or when that cannot be determined.
+bool other_gpu_in_use(int dev) {
+    static std::once_flag once;
+    static int ndev = -1;
+    static PfnPrimaryCtxGetState ctx_state = nullptr;
+    static PfnDeviceGet device_get = nullptr;
+    std::call_once(once, [] {
+        int n = 0;
+        if (cudaGetDeviceCount(&n) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        ndev = n;
+        if (n <= 1) return;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuDevicePrimaryCtxGetState", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            ctx_state = (PfnPrimaryCtxGetState)f;
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuDeviceGet", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            device_get = (PfnDeviceGet)f;
+        cudaGetLastError();
+    });
+    if (ndev < 0) return true;
+    if (ndev <= 1) return false;
+    if (ctx_state == nullptr || device_get == nullptr) return true;
+    for (int d = 0; d < ndev; ++d) {
+        if (d == dev) continue;
+        int h = 0, active = 0;
+        unsigned int flags = 0;
+        if (device_get(&h, d) != 0 || ctx_state(h, &flags, &active) != 0) return true;
+        if (active) return true;
+    }
+    return false;
+}
+
+// True when address `p` lies in device memory of GPU `dev`.
+bool on_device(int dev, const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+}  // namespace
+
+// True when bulk copies may read `bytes` (rounded up to whole 16-byte
+// vectors: a copy reads the last vector in full) from each of src[0..n-1].
+// Source sets that passed are remembered (the last 8), so repeated calls on
+// the same buffers query nothing.  Called with c->mu held.
+static bool bulk_sources_local(rra_comm* c, const void* const src[], int n, size_t bytes) {
+    if (n < 1 || n > rra::kClusterMaxRanks || bytes == 0) return false;
+    if (other_gpu_in_use(c->device)) return false;
+    for (const auto& e : c->local_sources) {
+        if (e.n != n || bytes > e.bytes) continue;
+        bool same = true;
+        for (int r = 0; r < n && same; ++r) same = e.ptr[r] == src[r];
+        if (same) return true;
+    }
+    const size_t span = (bytes + rra::kVecBytes - 1) / rra::kVecBytes * rra::kVecBytes;
+    for (int r = 0; r < n; ++r) {
+        if (src[r] == nullptr) return false;
+        if (!on_device(c->device, src[r]) || !on_device(c->device, (const char*)src[r] + (span - 1))) return false;
+    }
+    auto& e = c->local_sources[(size_t)c->local_next];
+    c->local_next = (c->local_next + 1) % (int)c->local_sources.size();
+    e.n = n;
+    e.bytes = bytes;
+    for (int r = 0; r < n; ++r) e.ptr[r] = src[r];
+    return true;
+}
 
 extern "C" {
 
@@ -134,7 +242,6 @@ const char* rra_status_string(rra_status_t s) {
         case RRA_ERR_NOT_CORESIDENT: return "ranks cannot all be co-resident on the GPU";
         case RRA_ERR_TIMEOUT: return "a device-side wait timed out";
         case RRA_ERR_POISONED: return "communicator poisoned by an earlier device error; reset it";
-        case RRA_ERR_EPOCH: return "epoch error (reserved)";
     }
     return "unknown status";
 }
@@ -223,11 +330,18 @@ rra_status_t rra_plan_layout(int nranks, size_t max_bytes, size_t scratch_onesho
     return RRA_OK;
 }
 
+// Largest CTA a kernel kind is built for: the two-shot kernels are built for
+// 4 CTAs of 128 threads per SM, the others for up to 256 threads.
+static int kind_max_threads(int kind) {
+    return kind == rra::kKindTwoshot || kind == rra::kKindTwoshotDirect ? 128 : 256;
+}
+
 static rra_status_t query_blocks(rra_comm* c, rra_dtype_t d, int kind, int* out) {
     int& b = c->blocks_per_sm[d][kind];
     if (b < 0) {
         int v = 0;
-        if (rra::occupancy(d, kind, c->threads, &v) != cudaSuccess) return RRA_ERR_CUDA;
+        if (rra::occupancy(d, kind, std::min(c->threads, kind_max_threads(kind)), &v) != cudaSuccess)
+            return RRA_ERR_CUDA;
         b = v;
     }
     *out = b;
@@ -485,9 +599,11 @@ static rra_status_t plan_cluster_multi(rra_comm* c, size_t count, rra_dtype_t dt
 // persistent, double-buffered kernel: as many clusters as can be resident,
 // each looping over its share of the slices.
 // host: the buffers are pinned host memory (read and written over
-// NVLink-C2C), where larger copies measured faster.
+// NVLink-C2C), where larger copies measured faster.  local: every input is
+// device memory of this GPU (bulk_sources_local); only then may the push be
+// made by bulk copies.
 static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, rra_algo_t algo, Params* p,
-                                 int* threads, int* mode, bool host = false) {
+                                 int* threads, int* mode, bool host, bool local) {
     const bool two = algo == RRA_TWOSHOT_CLUSTER;
     const size_t n = (size_t)c->nranks;
     if (c->nranks > rra::kClusterMaxRanks) return plan_cluster_multi(c, count, dtype, two, p, threads, mode);
@@ -516,7 +632,7 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
     size_t S;
     size_t T = (size_t)c->threads;
     const size_t s_mid = ceil_div((size_t)p->nvec * n, 512);  // ~512 CTAs in all
-    const bool bulk = c->cluster_pipe == 0 && bulk_copy_push(c);
+    const bool bulk = c->cluster_pipe == 0 && bulk_copy_push(c) && local && !host;
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
     } else if (two && bulk && !host && n * p->nvec <= (256u << 10)) {
@@ -578,10 +694,10 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
 // the cluster AllReduce (one vector per thread while small, then about two
 // CTAs per SM), with at most one batch of kClusterBatch input vectors per
 // thread and the 96 KiB stage (N slots of S vectors; one slot for Broadcast).
-static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int op, int root, Params* p,
+static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int op, int root, bool bulk, Params* p,
                               int* threads) {
-    int& fits = c->coll_fits[op][(int)dtype];
-    if (fits < 0) fits = rra::coll_max_active(dtype, op, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
+    int& fits = c->coll_fits[bulk ? 1 : 0][op][(int)dtype];
+    if (fits < 0) fits = rra::coll_max_active(dtype, op, c->nranks, 256, rra::kClusterStageBytes, bulk) > 0 ? 1 : 0;
     if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
     const size_t n = (size_t)c->nranks;
     const size_t ve = rra::kVecBytes / elem_size(dtype);
@@ -665,7 +781,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
     if (st != RRA_OK) return st;
     *kind_out = kind;
     const int64_t cmax = std::max<int64_t>(1, max_ctas / c->nranks);
-    const size_t T = (size_t)c->threads;
+    const size_t T = (size_t)std::min(c->threads, kind_max_threads(kind));
 
     memset(p, 0, sizeof(*p));
     p->win0 = c->win0;
@@ -716,10 +832,16 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
         case RRA_TWOSHOT_DBUF:
         case RRA_TWOSHOT_DIRECT: {
             size_t cap = L.ts_part / rra::kVecBytes;
-            if (c->ts_chunk > 0)
+            if (c->ts_chunk > 0) {
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->ts_chunk / rra::kVecBytes / n));
-            else  // live RS (+AG) scratch: N windows x 2 parities x N slots x part
+            } else {
+                // live RS (+AG) scratch: N windows x 2 parities x N slots x part
                 cap = std::min(cap, std::max<size_t>(64, kLiveScratch / (2 * n * n) / rra::kVecBytes));
+                // one position per thread per step on the largest co-resident
+                // grid (GB300 sweep at N = 8, 16-64 MiB per rank: 2.1x the
+                // bandwidth of 1.7 positions per thread in 2 MiB steps)
+                cap = std::min(cap, (size_t)cmax * T);
+            }
             const size_t part = std::min(ceil_div(p->nvec, n), cap);
             p->chunk_vecs = (uint32_t)part;
             p->nsteps = (uint32_t)ceil_div(p->nvec, n * part);
@@ -817,7 +939,7 @@ rra_status_t rra_comm_plan_call(rra_comm_t c, size_t count, rra_dtype_t dtype, r
     if (autoselect) algo = select_cluster(c->nranks, count * elem_size(dtype), c->cluster_tma != 0);
     Params p;
     int kind = 0, threads = 0;
-    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
+    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind, false, true)
                                        : plan_call(c, count, dtype, algo, &p, &kind, &threads);
     if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
         algo = select_global(c->nranks, count * elem_size(dtype));
@@ -858,6 +980,7 @@ static const char* kernel_name(bool cluster, int kind) {
     return "unknown";
 }
 
+// The plan of a call on device buffers of this GPU (bulk-copy push allowed).
 rra_status_t rra_comm_plan_kernel(rra_comm_t c, size_t count, rra_dtype_t dtype, rra_algo_t algo,
                                   const char** name) {
     if (c == nullptr || name == nullptr || !valid_dtype(dtype) || !valid_algo(algo) || count == 0)
@@ -868,7 +991,7 @@ rra_status_t rra_comm_plan_kernel(rra_comm_t c, size_t count, rra_dtype_t dtype,
     Params p;
     int kind = 0, threads = 0;
     std::lock_guard<std::mutex> g(c->mu);
-    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind)
+    rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind, false, true)
                                        : plan_call(c, count, dtype, algo, &p, &kind, &threads);
     if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
         algo = select_global(c->nranks, count * elem_size(dtype));
@@ -896,18 +1019,21 @@ static rra_status_t run_allreduce(rra_comm_t c, const void* const send[], void* 
     const size_t es = elem_size(dtype);
     if (count > c->max_bytes / es) return RRA_ERR_INVALID_ARG;
     const bool autoselect = algo == RRA_AUTO;
-    if (autoselect) algo = select_cluster(c->nranks, count * es, c->cluster_tma != 0);
     Params p;
     int kind = 0, threads = 0;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind, host)
+        // bulk copies only from this GPU's own device memory (never host buffers)
+        const bool local = !host && bulk_copy_push(c) && bulk_sources_local(c, send, c->nranks, count * es);
+        if (autoselect) algo = select_cluster(c->nranks, count * es, local);
+        rra_status_t st = is_cluster(algo) ? plan_cluster(c, count, dtype, algo, &p, &threads, &kind, host, local)
                                            : plan_call(c, count, dtype, algo, &p, &kind, &threads);
         if (st == RRA_ERR_NOT_CORESIDENT && autoselect && is_cluster(algo)) {
             algo = select_global(c->nranks, count * es);
             st = plan_call(c, count, dtype, algo, &p, &kind, &threads);
         }
         if (st != RRA_OK) return st;
+        c->last_kernel = kernel_name(is_cluster(algo), kind);
     }
     for (int r = 0; r < c->nranks; ++r) {
         if (send[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
@@ -915,6 +1041,7 @@ static rra_status_t run_allreduce(rra_comm_t c, const void* const send[], void* 
         p.send[r] = send[r];
         p.recv[r] = recv[r];
     }
+    p.drop_rank = c->drop_rank;
     cudaError_t e = is_cluster(algo)
                         ? rra::launch_cluster(p, dtype, kind, threads, (cudaStream_t)stream, c->pdl != 0)
                         : rra::launch_allreduce(p, dtype, kind, threads, (cudaStream_t)stream, c->cooperative != 0,
@@ -1057,10 +1184,19 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
     }
     Params p;
     int threads = 0;
+    bool bulk = false;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = plan_coll(c, count, dtype, op, root < 0 ? 0 : root, &p, &threads);
+        // AllGather and Broadcast (up to 16 ranks) push by bulk copies from
+        // the senders' inputs, when those are device memory of this GPU
+        if (rra::coll_has_bulk(op, c->nranks) && c->cluster_tma != 0) {
+            const int nsrc = op == rra::kCollBroadcast ? 1 : c->nranks;
+            const void* const* src = op == rra::kCollBroadcast ? send + root : send;
+            bulk = bulk_sources_local(c, src, nsrc, count * es);
+        }
+        rra_status_t st = plan_coll(c, count, dtype, op, root < 0 ? 0 : root, bulk, &p, &threads);
         if (st != RRA_OK) return st;
+        c->last_kernel = rra::coll_kernel_name(op, c->nranks, bulk);
     }
     const bool bcast = op == rra::kCollBroadcast || op == rra::kCollBroadcastSplit;
     const bool reduce = op == rra::kCollReduce || op == rra::kCollReduceSplit;
@@ -1073,7 +1209,8 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
         p.send[r] = need_send ? send[r] : nullptr;
         p.recv[r] = need_recv ? recv[r] : nullptr;
     }
-    cudaError_t e = rra::launch_coll(p, dtype, op, threads, (cudaStream_t)stream, c->pdl != 0);
+    p.drop_rank = c->drop_rank;
+    cudaError_t e = rra::launch_coll(p, dtype, op, threads, (cudaStream_t)stream, c->pdl != 0, bulk);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return RRA_ERR_CUDA;
@@ -1106,8 +1243,9 @@ rra_status_t rra_reduce(rra_comm_t c, int root, const void* const send[], void* 
 // take.  Slices as for the cluster AllReduce, within a stage of two
 // sub-buffers; one cluster per slice unless RRA_ATTR_CTAS_PER_RANK caps the
 // clusters (then each loops over several slices, one epoch each).
+// local: every send[r] is device memory of this GPU (bulk_sources_local).
 static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, rra::FusedParams* f,
-                                  int* threads, bool* two_shot, bool* bulk_out) {
+                                  int* threads, bool* two_shot, bool* bulk_out, bool local) {
     *bulk_out = false;
     const size_t n = (size_t)c->nranks;
     const size_t es = elem_size(dtype);
@@ -1128,8 +1266,8 @@ static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, 
         return RRA_OK;
     }
     // shape and push as the cluster AllReduce would take them
-    const bool two = select_cluster(c->nranks, count * es, c->cluster_tma != 0) == RRA_TWOSHOT_CLUSTER;
-    const bool bulk = bulk_copy_push(c);
+    const bool bulk = bulk_copy_push(c) && local;
+    const bool two = select_cluster(c->nranks, count * es, bulk) == RRA_TWOSHOT_CLUSTER;
     int& fits = c->residual_fits[bulk ? 1 : 0][two ? 1 : 0][(int)dtype];
     if (fits < 0)
         fits = rra::residual_max_active(dtype, two, bulk, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
@@ -1182,8 +1320,13 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
     bool two = false, bulk = false;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two, &bulk);
+        const bool local = bulk_copy_push(c) && bulk_sources_local(c, send, c->nranks, count * elem_size(dtype));
+        rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two, &bulk, local);
         if (st != RRA_OK) return st;
+        c->last_kernel = c->nranks > rra::kClusterMaxRanks
+                             ? (two ? "residual_multi_kernel<two-shot>" : "residual_multi_kernel<one-shot>")
+                             : bulk ? (two ? "residual_kernel<two-shot, bulk>" : "residual_kernel<one-shot, bulk>")
+                                    : (two ? "residual_kernel<two-shot>" : "residual_kernel<one-shot>");
     }
     for (int r = 0; r < c->nranks; ++r) {
         if (send[r] == nullptr || residual[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
@@ -1192,6 +1335,7 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
         f.base.recv[r] = recv[r];
         f.resid[r] = residual[r];
     }
+    f.base.drop_rank = c->drop_rank;
     cudaError_t e = c->nranks > rra::kClusterMaxRanks
                         ? rra::launch_cluster_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0)
                         : rra::launch_residual(f, dtype, two, bulk, threads, (cudaStream_t)stream, c->pdl != 0);
@@ -1202,10 +1346,10 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
     return RRA_OK;
 }
 
-rra_status_t rra_comm_status(rra_comm_t c, int* rank, int* step) {
-    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+// Synchronises, reads the status word and where it was recorded.
+static rra_status_t read_status(rra_comm* c, int* rank, int* step) {
     if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
-    uint32_t hdr[4];
+    uint32_t hdr[3];
     if (cudaMemcpy(hdr, c->ctrl, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return RRA_ERR_CUDA;
     if (rank) *rank = hdr[0] ? (int)(int32_t)hdr[1] : -1;
     if (step) *step = hdr[0] ? (int)(int32_t)hdr[2] : -1;
@@ -1216,6 +1360,24 @@ rra_status_t rra_comm_status(rra_comm_t c, int* rank, int* step) {
     return c->poisoned ? RRA_ERR_POISONED : RRA_OK;
 }
 
+rra_status_t rra_comm_status(rra_comm_t c) {
+    if (c == nullptr) return RRA_ERR_INVALID_ARG;
+    return read_status(c, nullptr, nullptr);
+}
+
+rra_status_t rra_comm_error_site(rra_comm_t c, int* rank, int* step) {
+    if (c == nullptr || rank == nullptr || step == nullptr) return RRA_ERR_INVALID_ARG;
+    const rra_status_t st = read_status(c, rank, step);
+    return st == RRA_ERR_CUDA || st == RRA_ERR_INVALID_ARG ? st : RRA_OK;
+}
+
+rra_status_t rra_comm_last_kernel(rra_comm_t c, const char** name) {
+    if (c == nullptr || name == nullptr) return RRA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(c->mu);
+    *name = c->last_kernel;
+    return RRA_OK;
+}
+
 rra_status_t rra_comm_reset(rra_comm_t c) {
     if (c == nullptr) return RRA_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
@@ -1224,6 +1386,7 @@ rra_status_t rra_comm_reset(rra_comm_t c) {
         return RRA_ERR_CUDA;
     if (c->host_status) *(volatile uint32_t*)c->host_status = 0u;
     c->poisoned = false;
+    c->drop_rank = -1;
     return RRA_OK;
 }
 
@@ -1254,6 +1417,7 @@ rra_status_t rra_comm_barrier_latency(rra_comm_t c, int iters, double* ns_per_ba
     p.per_cta = 1;
     p.nsteps = (uint32_t)iters;
     p.timing = dt;
+    p.drop_rank = c->drop_rank;
     uint64_t h[2] = {0, 0};
     st = RRA_OK;
     if (rra::launch_allreduce(p, RRA_FP32, rra::kKindBarrierProbe, 128, 0) != cudaSuccess ||
@@ -1264,8 +1428,7 @@ rra_status_t rra_comm_barrier_latency(rra_comm_t c, int iters, double* ns_per_ba
     }
     cudaFree(dt);
     if (st != RRA_OK) return st;
-    int rank = -1, step = -1;
-    st = rra_comm_status(c, &rank, &step);
+    st = read_status(c, nullptr, nullptr);
     if (st != RRA_OK) return st;
     *ns_per_barrier = (double)(h[1] - h[0]) / (double)(iters - 1);
     return RRA_OK;
@@ -1274,8 +1437,10 @@ rra_status_t rra_comm_barrier_latency(rra_comm_t c, int iters, double* ns_per_ba
 rra_status_t rra_comm_get_epoch(rra_comm_t c, uint64_t* epoch) {
     if (c == nullptr || epoch == nullptr) return RRA_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
-    if (cudaMemcpy(epoch, &c->ctrl->epoch[0], sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    uint64_t m1 = 0;
+    if (cudaMemcpy(&m1, &c->ctrl->epoch_m1[0], sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
         return RRA_ERR_CUDA;
+    *epoch = m1 + 1;
     return RRA_OK;
 }
 
@@ -1284,8 +1449,9 @@ rra_status_t rra_comm_set_epoch(rra_comm_t c, uint64_t epoch) {
     if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
     uint64_t* h = (uint64_t*)malloc(sizeof(uint64_t) * rra::kEpochSlots);
     if (h == nullptr) return RRA_ERR_OOM;
-    for (int i = 0; i < rra::kEpochSlots; ++i) h[i] = epoch;
-    const cudaError_t e = cudaMemcpy(c->ctrl->epoch, h, sizeof(uint64_t) * rra::kEpochSlots, cudaMemcpyHostToDevice);
+    for (int i = 0; i < rra::kEpochSlots; ++i) h[i] = epoch - 1;
+    const cudaError_t e =
+        cudaMemcpy(c->ctrl->epoch_m1, h, sizeof(uint64_t) * rra::kEpochSlots, cudaMemcpyHostToDevice);
     free(h);
     return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
 }
@@ -1300,9 +1466,8 @@ rra_status_t rra_comm_set_trace(rra_comm_t c, uint64_t* dev_buf) {
 rra_status_t rra_comm_inject_drop(rra_comm_t c, int rank) {
     if (c == nullptr || rank < -1 || rank >= c->nranks) return RRA_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return RRA_ERR_CUDA;
-    int32_t v = rank;
-    if (cudaMemcpy(&c->ctrl->drop_rank, &v, sizeof(v), cudaMemcpyHostToDevice) != cudaSuccess)
-        return RRA_ERR_CUDA;
+    std::lock_guard<std::mutex> g(c->mu);
+    c->drop_rank = rank;
     return RRA_OK;
 }
 

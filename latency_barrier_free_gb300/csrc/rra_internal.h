@@ -21,22 +21,24 @@ constexpr uint64_t kMaxMessageBytes = (1ull << 36) - 16;  // 16-byte vector indi
 // restarts one past that multiple, so every live flag value is unique.
 constexpr uint64_t kScrubPeriod = 1ull << 31;
 
-// Control block at the start of the allocation (before window 0).
+// Control block at the start of the allocation (before window 0).  All-zero
+// bytes (with all-zero windows: LL flags 0, counters 0) are the idle state:
+// status 0, epoch 1.
 struct Ctrl {
     uint32_t status;     // rra_status_t of the first device-side error; 0 = none
     int32_t err_rank;    // virtual rank that recorded it
     int32_t err_step;    // chunk step of the call in which it was recorded
-    int32_t drop_rank;   // injected fault: rank whose stores to peers are skipped; -1 = none
     uint32_t scrub_arrive;  // LL flag scrub: CTAs arrived at the grid barrier
     uint32_t scrub_gen;     // LL flag scrub: completed scrubs (barrier generation)
     uint32_t* host_status;  // device address of a pinned host word that mirrors `status`
                             // (written with it on the first error), or null
     uint32_t reserved[56];
-    // Every CTA slot holds the same value: the epoch of the next step.  CTA b
-    // of a call with G CTAs reads slot b at entry and writes epoch + steps to
-    // every slot b' = b (mod G); each slot has exactly one reader/writer per
-    // call, and all slots stay equal whatever grid a later call uses.
-    uint64_t epoch[kEpochSlots];
+    // Every CTA slot holds the same value: the epoch of the next step, minus
+    // one (so that zero is epoch 1).  CTA b of a call with G CTAs reads slot b
+    // at entry and writes epoch + steps - 1 to every slot b' = b (mod G); each
+    // slot has exactly one reader/writer per call, and all slots stay equal
+    // whatever grid a later call uses.
+    uint64_t epoch_m1[kEpochSlots];
 };
 
 // Kernel parameters, passed by value (one launch = one call).
@@ -69,6 +71,8 @@ struct Params {
     int32_t ctas_per_rank;
     int32_t epoch_slots;   // number of epoch slots to keep equal
     int32_t root;          // Broadcast / Reduce: the root rank
+    int32_t drop_rank;     // injected fault: rank whose stores to peers are skipped; -1 = none
+    int32_t scrub_ranks;   // windows the epoch scrub zeroes (0: nranks)
 };
 
 // Kernel kinds: the algorithms (same values as rra_algo_t) plus the wide
@@ -128,8 +132,14 @@ enum {
     kCollReduceSplit = 5      // two hops: ReduceScatter, then every owner pushes to the root
 };
 size_t coll_stage_bytes(const Params& p, int op);
-cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl);
-int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem);
+// bulk: AllGather / Broadcast up to 16 ranks on the bulk-copy kernel (the
+// caller has checked that every input it reads is device memory of this GPU);
+// otherwise the st.async kernels.
+bool coll_has_bulk(int op, int nranks);
+const char* coll_kernel_name(int op, int nranks, bool bulk);
+cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl,
+                        bool bulk);
+int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem, bool bulk);
 // AllReduce + residual add on the public device API (fused.cu): the cluster
 // AllReduce's launch shape; cluster c handles slices c, c + G, ... of
 // p.nsteps slices (G = p.ctas_per_rank), one epoch each.

@@ -3,11 +3,11 @@
 // Who needs it.  Some callers cannot call cudaMalloc at the moment they need
 // an AllReduce, and cannot hold a communicator whose creation allocated for
 // them either:
-//  * code that runs while some other component is capturing a CUDA graph on
-//    the device in the global capture mode, where cudaMalloc is refused;
 //  * plug-ins and extensions whose host framework owns the GPU allocator and
 //    forbids direct cudaMalloc / cudaFree (all device memory must come from
 //    the framework, and the plug-in is only handed input and output buffers);
+//  * processes that reserve their whole device-memory budget up front and
+//    may not grow it afterwards;
 //  * latency-critical paths that must not pay for an allocation, or for the
 //    device-wide synchronisation that freeing memory can imply.
 // For them, rra_allreduce_static runs the one-shot LL AllReduce on scratch
@@ -37,7 +37,9 @@ constexpr int kThreads = 256;
 constexpr int kMaxDevices = 64;
 
 // The scratch: control block (status word, epochs) followed by 8 windows of
-// LL slots.  Zero at load; set-up writes the idle state (epoch 1).
+// LL slots.  It is zero when the module loads, and all-zero is the idle
+// state (status 0, epoch 1, LL flags 0), so no initialisation is needed --
+// also not after cudaDeviceReset, when the module is loaded again.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 struct DeviceState {
@@ -47,39 +49,46 @@ struct DeviceState {
     int blocks_per_sm[3];  // co-resident CTAs per SM of the LL one-shot kernel, per dtype
 };
 
+// Runs before every call's AllReduce, on its stream.  After a call that
+// failed (a wait ran out: the status word is set), some CTAs may have left
+// their epoch slots behind and LL flags of that epoch in the windows, so the
+// whole array goes back to the idle state; otherwise it does nothing.  One
+// CTA, so the status word is read and cleared by the same block.
+__global__ void __launch_bounds__(1024) static_recover_kernel() {
+    rra::Ctrl* ctrl = (rra::Ctrl*)g_scratch;
+    __shared__ uint32_t failed;
+    if (threadIdx.x == 0) failed = *(volatile uint32_t*)&ctrl->status;
+    __syncthreads();
+    if (failed == 0u) return;
+    uint4* words = (uint4*)g_scratch;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (size_t i = threadIdx.x; i < kScratchBytes / sizeof(uint4); i += blockDim.x) words[i] = z;
+}
+
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 size_t elem_size(rra_dtype_t d) { return d == RRA_FP32 ? 4 : d == RRA_BF16 ? 2 : d == RRA_FP64 ? 8 : 0; }
 
 // Once per device, with that device current: look up the array's device
-// address, query occupancy, and write the idle state (epoch 1, LL flags 0,
-// status 0, no injected fault).  Synchronises the device, so the first call
-// on a device must not happen while a stream is being captured.
+// address (cudaGetSymbolAddress) and query occupancy.  The address is looked
+// up again on every call (host-side only, nothing is enqueued); if it moved
+// -- the device was reset and the module loaded again -- the set-up is
+// redone.  Set-up enqueues no work and does not synchronise.
 rra_status_t setup(int dev, DeviceState** out) {
     std::lock_guard<std::mutex> g(g_mu);
     DeviceState& d = g_dev[dev];
-    if (!d.ready) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) {
-            cudaGetLastError();
-            return RRA_ERR_CUDA;
-        }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return RRA_ERR_CUDA;
+    }
+    if (!d.ready || d.base != (char*)ptr) {
+        d.ready = false;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return RRA_ERR_CUDA;
         for (int t = 0; t < 3; ++t) {
             if (rra::occupancy((rra_dtype_t)t, rra::kKindOneshotLL, kThreads, &d.blocks_per_sm[t]) != cudaSuccess)
                 return RRA_ERR_CUDA;
-        }
-        rra_layout_t lay = {};
-        lay.nranks = kMaxRanksStatic;
-        lay.ll_bytes = kWindowBytes;
-        lay.window_stride = kWindowBytes;
-        lay.ctrl_bytes = kCtrlBytes;
-        lay.total_bytes = kScratchBytes;
-        if (rra::launch_init((char*)ptr, kScratchBytes, lay, kMaxRanksStatic, 0) != cudaSuccess ||
-            cudaDeviceSynchronize() != cudaSuccess) {
-            cudaGetLastError();
-            return RRA_ERR_CUDA;
         }
         d.base = (char*)ptr;
         d.ready = true;
@@ -138,12 +147,16 @@ extern "C" rra_status_t rra_allreduce_static(int nranks, const void* const send[
     p.nsteps = 1;
     p.nranks = nranks;
     p.epoch_slots = rra::kEpochSlots;
+    p.drop_rank = -1;
+    p.scrub_ranks = kMaxRanksStatic;  // calls with any rank count share the 8 windows
 
     cudaStream_t s = (cudaStream_t)stream;
-    // The array keeps the previous call's contents.  The status word must start
-    // at zero (a failed earlier call would otherwise turn this one into a
-    // no-op); LL flags need no clearing (each call uses new epochs).
-    if (cudaMemsetAsync(&p.ctrl->status, 0, sizeof(uint32_t), s) != cudaSuccess) return RRA_ERR_CUDA;
+    // The array keeps the previous call's contents.  After a successful call
+    // that is the idle state of the next epoch (LL flags need no clearing:
+    // each call uses new epochs); after a failed one, the recovery kernel
+    // returns the whole array to the idle state first.
+    static_recover_kernel<<<1, 1024, 0, s>>>();
+    if (cudaGetLastError() != cudaSuccess) return RRA_ERR_CUDA;
     const cudaError_t e = rra::launch_allreduce(p, dtype, rra::kKindOneshotLL, kThreads, s, true);
     if (e != cudaSuccess) {
         cudaGetLastError();

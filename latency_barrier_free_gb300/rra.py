@@ -16,9 +16,9 @@ LIB_PATH = os.path.join(HERE, "librra.so")
 OK = 0
 STATUS_NAMES = {
     0: "RRA_OK", 1: "RRA_ERR_INVALID_ARG", 2: "RRA_ERR_CUDA", 3: "RRA_ERR_OOM",
-    4: "RRA_ERR_NOT_CORESIDENT", 5: "RRA_ERR_TIMEOUT", 6: "RRA_ERR_POISONED", 7: "RRA_ERR_EPOCH",
+    4: "RRA_ERR_NOT_CORESIDENT", 5: "RRA_ERR_TIMEOUT", 6: "RRA_ERR_POISONED",
 }
-ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_CORESIDENT, ERR_TIMEOUT, ERR_POISONED, ERR_EPOCH = range(1, 8)
+ERR_INVALID_ARG, ERR_CUDA, ERR_OOM, ERR_NOT_CORESIDENT, ERR_TIMEOUT, ERR_POISONED = range(1, 7)
 
 DTYPES = {"fp32": 0, "bf16": 1, "fp64": 2}
 ALGOS = {"oneshot_ll": 0, "oneshot_sentinel": 1, "twoshot_dbuf": 2, "ll128_atomic": 3,
@@ -35,13 +35,14 @@ MAX_RANKS = 64
 # Exported symbols, in declaration order of the public headers.
 SYMBOLS = [
     "rra_comm_create", "rra_allreduce", "rra_allreduce_host", "rra_host_device_ptrs", "rra_allreduce_mapped",
-    "rra_comm_status", "rra_comm_reset",
+    "rra_comm_status", "rra_comm_error_site", "rra_comm_last_kernel", "rra_comm_reset",
     "rra_comm_destroy", "rra_comm_set_attr", "rra_comm_get_attr", "rra_comm_layout", "rra_plan_layout",
     "rra_comm_plan_kernel", "rra_select_algo", "rra_comm_plan_call", "rra_comm_max_coresident", "rra_comm_set_timing", "rra_comm_set_trace",
     "rra_comm_inject_drop",
     "rra_comm_barrier_latency", "rra_comm_get_epoch", "rra_comm_set_epoch", "rra_status_string",
     "rra_version",
-    "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_empty_kernel", "rra_probe_launch_shape",
+    "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_dsmem_pingpong", "rra_probe_empty_kernel",
+    "rra_probe_launch_shape",
     "rra_probe_sm_count",
     "rra_allreduce_static",
     "rra_reduce_scatter", "rra_all_gather", "rra_broadcast", "rra_reduce",
@@ -93,7 +94,9 @@ def load(path: str = LIB_PATH):
             "rra_host_device_ptrs": ([i32, pp, pp], i32),
             "rra_allreduce_mapped": ([vp, pp, pp, sz, i32, i32, vp], i32),
             "rra_comm_plan_kernel": ([vp, sz, i32, i32, ctypes.POINTER(ctypes.c_char_p)], i32),
-            "rra_comm_status": ([vp, ip, ip], i32),
+            "rra_comm_status": ([vp], i32),
+            "rra_comm_error_site": ([vp, ip, ip], i32),
+            "rra_comm_last_kernel": ([vp, ctypes.POINTER(ctypes.c_char_p)], i32),
             "rra_comm_reset": ([vp], i32),
             "rra_comm_destroy": ([vp], i32),
             "rra_comm_set_attr": ([vp, i32, i64], i32),
@@ -113,6 +116,8 @@ def load(path: str = LIB_PATH):
             "rra_version": ([], ctypes.c_char_p),
             "rra_probe_l2_chase": ([sz, ctypes.c_uint64, ctypes.c_uint64, ctypes.POINTER(ctypes.c_double)], i32),
             "rra_probe_pingpong": ([i32, i32, i32, ctypes.POINTER(ctypes.c_double), ip, ip], i32),
+            "rra_probe_dsmem_pingpong": ([i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                          ip, ip], i32),
             "rra_probe_empty_kernel": ([vp], i32),
             "rra_probe_sm_count": ([ip], i32),
             "rra_probe_launch_shape": ([i32, i32, i32, i32, vp], i32),
@@ -389,11 +394,20 @@ class Comm:
 
     # -- control ------------------------------------------------------------
     def status(self):
-        """(status code, rank, step); synchronises the device."""
+        """(status code, rank, step) -- rra_comm_status, then rra_comm_error_site
+        for where the error was recorded; synchronises the device."""
+        st = self._lib.rra_comm_status(self._h)
         rank = ctypes.c_int(-1)
         step = ctypes.c_int(-1)
-        st = self._lib.rra_comm_status(self._h, ctypes.byref(rank), ctypes.byref(step))
+        _check(self._lib.rra_comm_error_site(self._h, ctypes.byref(rank), ctypes.byref(step)),
+               "rra_comm_error_site")
         return st, rank.value, step.value
+
+    def last_kernel(self) -> str:
+        """Name of the kernel the last call on this communicator launched."""
+        name = ctypes.c_char_p()
+        _check(self._lib.rra_comm_last_kernel(self._h, ctypes.byref(name)), "rra_comm_last_kernel")
+        return name.value.decode()
 
     def reset(self):
         _check(self._lib.rra_comm_reset(self._h), "rra_comm_reset")
@@ -495,3 +509,15 @@ def probe_sm_count() -> int:
     v = ctypes.c_int()
     _check(load().rra_probe_sm_count(ctypes.byref(v)), "rra_probe_sm_count")
     return v.value
+
+
+def probe_dsmem_pingpong(iters: int = 20000):
+    """(ns per bulk-copy round trip inside a 2-CTA cluster, ns per cluster
+    barrier, SM id of CTA 0, SM id of CTA 1)."""
+    rt = ctypes.c_double()
+    cb = ctypes.c_double()
+    a = ctypes.c_int()
+    b = ctypes.c_int()
+    _check(load().rra_probe_dsmem_pingpong(int(iters), ctypes.byref(rt), ctypes.byref(cb), ctypes.byref(a),
+                                           ctypes.byref(b)), "rra_probe_dsmem_pingpong")
+    return rt.value, cb.value, a.value, b.value

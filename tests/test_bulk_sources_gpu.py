@@ -1,0 +1,155 @@
+"""GPU tests of where the bulk-copy push (TMA bulk copies with cluster
+multicast, read straight from the callers' inputs) may run: only on inputs in
+device memory of this GPU.  Host buffers -- the host entry points, and
+device-mapped pinned host memory passed to the device entry points -- get the
+st.async kernels, with the same results.  rra_comm_last_kernel names the
+kernel each call launched."""
+import numpy as np
+import pytest
+
+import oracle
+from latency_barrier_free_gb300 import inputs, rra
+from tests.gpu_util import bits, check_against_oracle, poison_like, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def _pinned(arrs):
+    return [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in arrs]
+
+
+@pytest.mark.parametrize("algo,count", [("oneshot_cluster", 32), ("twoshot_cluster", 70000), ("auto", 32),
+                                        ("auto", 300000)])
+def test_device_buffers_take_the_bulk_copy_push(algo, count):
+    n = 4
+    sends_np = inputs.normal(inputs.rng(90, count), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        assert comm.last_kernel() == "none"
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        assert comm.last_kernel().startswith("cluster_tma_kernel<")
+        assert comm.last_kernel() == comm.plan_kernel(count, "fp32", algo)
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
+
+
+@pytest.mark.parametrize("algo,count", [("oneshot_cluster", 32), ("twoshot_cluster", 70000), ("auto", 1000)])
+def test_host_entry_never_takes_the_bulk_copy_push(algo, count):
+    """rra_allreduce_host and rra_allreduce_mapped with the bulk-copy push
+    switched on explicitly: the kernel reads host memory, so the push is
+    st.async (cluster_kernel), and the sums are exact."""
+    n = 4
+    sends_np = inputs.normal(inputs.rng(91, count), n, count, "fp32")
+    hs = _pinned(sends_np)
+    hr = [torch.full((count,), float("nan")).pin_memory() for _ in range(n)]
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cluster_tma", 1)
+        comm.allreduce_host([t.data_ptr() for t in hs], [t.data_ptr() for t in hr], count, "fp32", algo)
+        assert comm.last_kernel().startswith("cluster_kernel<"), comm.last_kernel()
+        check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", "oneshot_cluster")
+        for t in hr:
+            t.fill_(float("nan"))
+        call = comm.prepare_host([t.data_ptr() for t in hs], [t.data_ptr() for t in hr], count, "fp32", algo)
+        call()
+        assert comm.last_kernel().startswith("cluster_kernel<"), comm.last_kernel()
+        check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", "oneshot_cluster")
+
+
+def test_mapped_host_pointers_on_the_device_entry_get_st_async():
+    """Device addresses of pinned host memory handed to rra_allreduce itself
+    (not through the host entry) still fail the device-memory check."""
+    n, count = 4, 4096
+    sends_np = inputs.normal(inputs.rng(92, 0), n, count, "fp32")
+    hs = _pinned(sends_np)
+    dev_send = rra.host_device_ptrs([t.data_ptr() for t in hs])
+    assert all(d is not None for d in dev_send)
+    recvs = [torch.full((count,), float("nan"), device="cuda") for _ in range(n)]
+    with rra.Comm(n, count * 4) as comm:
+        comm.allreduce_ptrs(dev_send, [t.data_ptr() for t in recvs], count, "fp32", "oneshot_cluster")
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        assert comm.last_kernel() == "cluster_kernel<one-shot>"
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
+        # one rank's input on the device, the others in host memory: still st.async
+        first = to_device([sends_np[0]], "fp32")[0]  # kept alive: the call reads it
+        mixed = [first.data_ptr()] + dev_send[1:]
+        comm.allreduce_ptrs(mixed, [t.data_ptr() for t in recvs], count, "fp32", "oneshot_cluster")
+        torch.cuda.synchronize()
+        assert comm.last_kernel() == "cluster_kernel<one-shot>"
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
+
+
+def test_bulk_copy_attribute_off():
+    n, count = 4, 32
+    sends_np = inputs.normal(inputs.rng(93, 0), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        comm.set_attr("cluster_tma", 0)
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, "oneshot_cluster")
+        torch.cuda.synchronize()
+        assert comm.last_kernel() == "cluster_kernel<one-shot>"
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
+
+
+def test_collectives_choose_their_push_by_source_memory():
+    """AllGather and Broadcast push by bulk copies from device inputs, by
+    st.async from inputs in host memory; the results are the oracle's."""
+    n, m = 4, 1000
+    small_np = [inputs.normal(inputs.rng(94, r), 1, m, "fp32")[0] for r in range(n)]
+    want_ag = oracle.all_gather(small_np, "fp32")
+    want_bc = oracle.broadcast(small_np, "fp32", 2)
+    hs = _pinned(small_np)
+    dev_host = rra.host_device_ptrs([t.data_ptr() for t in hs])
+    on_device = to_device(small_np, "fp32")  # kept alive: the calls read it
+    with rra.Comm(n, n * m * 4) as comm:
+        for where, src in (("device", [t.data_ptr() for t in on_device]), ("host", dev_host)):
+            out = [torch.full((n * m,), float("nan"), device="cuda") for _ in range(n)]
+            comm.collective_ptrs("all_gather", src, [t.data_ptr() for t in out], m, "fp32", 0)
+            torch.cuda.synchronize()
+            kind = comm.last_kernel()
+            assert kind == ("coll_bulk_kernel<all_gather>" if where == "device" else "coll_kernel<all_gather>"), kind
+            for g, w in zip(out, want_ag):
+                assert np.array_equal(bits(g.cpu().numpy()), bits(w))
+            bc = [torch.full((m,), float("nan"), device="cuda") for _ in range(n)]
+            comm.collective_ptrs("broadcast", src, [t.data_ptr() for t in bc], m, "fp32", 2)
+            torch.cuda.synchronize()
+            kind = comm.last_kernel()
+            assert kind == ("coll_bulk_kernel<broadcast>" if where == "device" else "coll_kernel<broadcast>"), kind
+            for g, w in zip(bc, want_bc):
+                assert np.array_equal(bits(g.cpu().numpy()), bits(w))
+        assert comm.status()[0] == rra.OK
+
+
+def test_fused_residual_chooses_its_push_by_source_memory():
+    n, count = 4, 2000
+    sends_np = inputs.normal(inputs.rng(95, 0), n, count, "fp32")
+    res_np = inputs.normal(inputs.rng(95, 1), n, count, "fp32")
+    want = oracle.allreduce_residual(sends_np, res_np, "fp32")
+    hs = _pinned(sends_np)
+    dev_host = rra.host_device_ptrs([t.data_ptr() for t in hs])
+    res = to_device(res_np, "fp32")
+    on_device = to_device(sends_np, "fp32")  # kept alive: the calls read it
+    with rra.Comm(n, count * 4) as comm:
+        for where, src in (("device", [t.data_ptr() for t in on_device]), ("host", dev_host)):
+            out = [torch.full((count,), float("nan"), device="cuda") for _ in range(n)]
+            comm.allreduce_residual_ptrs(src, [t.data_ptr() for t in res], [t.data_ptr() for t in out], count, "fp32")
+            torch.cuda.synchronize()
+            kind = comm.last_kernel()
+            assert kind.startswith("residual_kernel<")
+            assert kind.endswith(", bulk>") == (where == "device"), kind
+            for g, w in zip(out, want):
+                assert np.array_equal(bits(g.cpu().numpy()), bits(w))
+        assert comm.status()[0] == rra.OK

@@ -1,12 +1,14 @@
 """The entry point that allocates nothing (rra_allreduce_static), called
-through the C ABI and checked against rra_allreduce on the same inputs.
+through the C ABI and checked against the oracle and against rra_allreduce on
+the same inputs.
 
 It exists for callers that cannot allocate device memory when they need an
-AllReduce (inside another component's graph capture, inside plug-ins whose
-framework owns the allocator, on paths that must not pay for an allocation).
-Both entry points run the one-shot LL kernel, which adds the ranks in order,
-so the bar is the one the other GPU tests use for it: identical bits.  Each
-case runs two calls in a row on the shared static scratch.
+AllReduce: plug-ins whose host framework owns the allocator, processes whose
+device-memory budget is fixed up front, paths that must not pay for an
+allocation.  Both entry points run the one-shot LL kernel, which adds the
+ranks in order, so the bar is the one the other GPU tests use for it:
+identical bits.  Each case runs two calls in a row on the shared static
+scratch.
 
 This file is collected last on purpose; it also passes on its own.
 """
@@ -15,6 +17,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from latency_barrier_free_gb300 import inputs, rra
 
 pytestmark = pytest.mark.gpu
@@ -77,9 +80,32 @@ def test_static_entry_matches_allreduce_twice(lib, n, count, dtype):
             assert st == rra.OK
             torch.cuda.synchronize()
             assert int(status.item()) == 0
+            expect = oracle.allreduce(host, dtype)
             for r in range(n):
-                assert np.array_equal(_bits(got[r]), _bits(ref[r])), (call, r)
+                assert np.array_equal(_bits(got[r]), expect[r].view(np.uint8)), (call, r)  # the oracle
+                assert np.array_equal(_bits(got[r]), _bits(ref[r])), (call, r)  # the existing entry point
             del ks, kr
+
+
+def test_static_entry_calls_with_changing_rank_counts(lib):
+    """Calls with different rank counts share the array's eight windows."""
+    stream = torch.cuda.current_stream()
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for k, n in enumerate((8, 2, 5, 8, 3, 8)):
+        count = 1500
+        host = inputs.normal(inputs.rng(81, k, n, count), n, count, "fp32")
+        xs = _dev(host, "fp32")
+        got = [torch.full_like(x, float("nan")) for x in xs]
+        sp, ks = _ptrs(xs)
+        rp, kr = _ptrs(got)
+        assert lib.rra_allreduce_static(n, sp, rp, count, rra.DTYPES["fp32"], ctypes.c_void_p(status.data_ptr()),
+                                        ctypes.c_void_p(stream.cuda_stream)) == rra.OK
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        expect = oracle.allreduce(host, "fp32")
+        for r in range(n):
+            assert np.array_equal(_bits(got[r]), expect[r].view(np.uint8)), (k, n, r)
+        del ks, kr
 
 
 def test_static_entry_rejects_what_does_not_fit(lib):
