@@ -29,9 +29,21 @@ collectives ReduceScatter, AllGather, Broadcast, Reduce: N=4 latency (graph
           replay) and N=8 bandwidth of compulsory bytes against the HBM peak
 cpu_baseline  the CPU oracle on a bounded sample of the same sweep
 
+Output: the last stdout line is one compact JSON object (well under 4 KB):
+the headline, roofline, e2e, cpu_baseline, clocks, the latency floor with
+the 128-byte in-kernel times, and the bandwidth fractions.  Every table in
+full goes to the JSON file --detail-out (default: bench_detail.json in the
+system temp directory), whose path the line names.
+
 --impl reference times the CPU oracle itself on the same sweep.
-Under torchrun (N>1) every GPU runs its own replica (the virtual ranks of one
-AllReduce never span GPUs); the reported latency is the maximum over GPUs.
+--case ALGO NRANKS BYTES DTYPE REPS [attr=value ...] runs one configuration
+REPS times (a load generator for profiling one kernel): it checks the device
+status and that every rank received the same bits, and prints one line.
+
+One GPU only.  The N ranks of an AllReduce are virtual and live on one GPU,
+and the library's bulk-copy push (TMA multicast) is for single-GPU processes,
+so --gpus N > 1 (or a torchrun launch with WORLD_SIZE > 1) does no GPU work:
+rank 0 prints one JSON line with an "unavailable" reason, every rank exits 0.
 """
 from __future__ import annotations
 
@@ -66,28 +78,13 @@ def dist_env():
     return world, rank, local
 
 
-def init_dist(world, backend):
-    import torch.distributed as dist
-
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group(backend=backend)
-    return dist if world > 1 else None
+MULTI_GPU_REASON = ("one GPU only: the N ranks are virtual ranks on one GPU, and the bulk-copy push "
+                    "(TMA multicast) is for single-GPU processes; no multi-GPU run")
 
 
-def barrier(dist):
-    if dist is not None:
-        dist.barrier()
-
-
-def max_over_ranks(dist, values, device=None):
-    """Element-wise max of a list of floats over all ranks."""
-    if dist is None:
-        return list(values)
-    import torch
-
-    t = torch.tensor(list(values), dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return t.cpu().tolist()
+def multi_gpu_line(n_gpus):
+    """The line printed instead of a measurement when more than one GPU is asked for."""
+    return {"metric": METRIC, "n_gpus": n_gpus, "unavailable": MULTI_GPU_REASON}
 
 
 # ---------------------------------------------------------------- clocks --
@@ -208,15 +205,15 @@ def sweep_cases():
 
 
 # ------------------------------------------------------------ our arm ----
-def run_ours(args, world, rank, local):
+def run_ours(args):
     import torch
 
     import __graft_entry__
     from latency_barrier_free_gb300 import inputs, measure, rra
 
     __graft_entry__.build()
+    local = 0
     torch.cuda.set_device(local)
-    dist = init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(dev)
@@ -276,7 +273,6 @@ def run_ours(args, world, rank, local):
                         for _ in range(ncase)] for _ in range(args.steps)]
     step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
-    barrier(dist)
     torch.cuda.synchronize()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)          # evict the previous step's lines from L2
@@ -284,7 +280,6 @@ def run_ours(args, world, rank, local):
         one_step(per_step_events[s])
         step_events[s][1].record(stream)
     torch.cuda.synchronize()
-    barrier(dist)
     st = comm.status()[0]
     if st != rra.OK:
         raise RuntimeError("device status after timed region: %s" % rra.STATUS_NAMES.get(st))
@@ -369,18 +364,16 @@ def run_ours(args, world, rank, local):
     e2e = end_to_end(comm, rra, cases, torch, args)
     decode = decode_graph(rra, torch) if args.decode else None
 
-    # aggregate over GPU replicas: latency-like numbers take the max
-    agg = max_over_ranks(dist, [value, float(np.mean(step_ms)), e2e["value"]], device=dev)
-    value, ms_step, e2e["value"] = agg
+    ms_step = float(np.mean(step_ms))
     launches = args.steps * ncase * inner  # one kernel per call, all ours
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "us/call", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 3), "unit": "us/call", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp32+bf16",
         "data": "synthetic (seeded N(0,1), no dataset)",
         "config": {"workload": WORKLOAD, "nranks": NRANKS, "sizes_bytes": [c[1] for c in cases if c[0] == "fp32"],
                    "inner_calls": inner, "l2": "flushed (256 MiB write) between steps; calls in a step reuse "
-                   "L2-resident buffers", "parallelism": "replicas" if world > 1 else "single GPU",
+                   "L2-resident buffers", "parallelism": "single GPU",
                    "gpu": props.name, "sms": props.multi_processor_count},
         "gpu_launches": launches,
         "roofline": roofline,
@@ -407,13 +400,98 @@ def run_ours(args, world, rank, local):
         line["scratch_sweep"] = sweep
     if configs is not None:
         line["configs"] = configs
-    if rank == 0 and args.cpu_baseline:
+    if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     comm.close()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    import tempfile
+
+    path = args.detail_out or os.path.join(tempfile.gettempdir(), "bench_detail.json")
+    try:
+        with open(path, "w") as f:
+            json.dump(line, f, indent=1)
+    except OSError as e:
+        print("bench: could not write %s: %s" % (path, e), file=sys.stderr)
+        path = None
+    print(json.dumps(summary_line(line, path)), flush=True)
+
+
+# the algorithms whose 128-byte in-kernel time the summary line reports
+NAMED = ("oneshot_ll", "oneshot_sentinel", "twoshot_dbuf", "ll128_atomic", "oneshot_cluster")
+SUMMARY_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "gpu_launches")
+
+
+def summary_line(d, detail_path):
+    """The compact last line (well under 4 KB) from the full result `d`."""
+    out = {k: d[k] for k in SUMMARY_KEYS if k in d}
+    c = d.get("config", {})
+    sizes = c.get("sizes_bytes") or []
+    out["config"] = {"workload": c.get("workload"), "nranks": c.get("nranks"),
+                     "sizes_bytes": "%d-%d" % (min(sizes), max(sizes)) if sizes else None,
+                     "inner_calls": c.get("inner_calls"), "l2": c.get("l2"), "gpu": c.get("gpu"), "sms": c.get("sms")}
+    r = d.get("roofline", {})
+    out["roofline"] = {k: r.get(k) for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "kernel",
+                                             "us_per_launch", "bytes_per_launch", "share_of_step", "peak_source")}
+    if "cpu_baseline" in d:
+        out["cpu_baseline"] = d["cpu_baseline"]
+    e = d.get("e2e", {})
+    out["e2e"] = {k: e.get(k) for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+    out["e2e"]["api"] = "rra_allreduce_mapped on pinned host buffers (zero copy), synchronised per call"
+    ck = d.get("clocks", {})
+    out["clocks"] = {k: ck.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    f = d.get("latency_floor", {})
+    kern = f.get("in_kernel_us_128B", {})
+    floors = {"l2": f.get("floor_us"), "dsmem": f.get("floor_dsmem_us")}
+    lf = {"floor_us": f.get("floor_us"), "floor_dsmem_us": f.get("floor_dsmem_us"), "in_kernel_us_128B": {},
+          "x_floor": {}}
+    for key, us in kern.items():
+        algo = key.split("/", 1)[1]
+        if algo not in NAMED:
+            continue
+        lf["in_kernel_us_128B"][key] = us
+        ref = floors["dsmem"] if algo.endswith("cluster") else floors["l2"]
+        if ref:
+            lf["x_floor"][key] = round(us / ref, 2)
+    out["latency_floor"] = lf
+    bw = d.get("bandwidth", {}).get("sizes", {})
+    out["bandwidth_hbm_frac"] = {k: v.get("frac") for k, v in bw.items() if "MiB" in k}
+    out["detail"] = detail_path
+    return out
+
+
+def run_case(args):
+    """--case ALGO NRANKS BYTES DTYPE REPS [attr=value ...]: one configuration
+    REPS times, for profiling one kernel (seeded uniform(-1, 1) inputs on the
+    device).  Checks the device status and that every rank got the same bits."""
+    import torch
+
+    import __graft_entry__
+    from latency_barrier_free_gb300 import rra
+
+    a = args.case
+    if len(a) < 5:
+        raise SystemExit("--case needs ALGO NRANKS BYTES DTYPE REPS [attr=value ...]")
+    algo, n, size, dtype, reps = a[0], int(a[1]), int(a[2]), a[3], int(a[4])
+    attrs = dict(x.split("=", 1) for x in a[5:])
+    __graft_entry__.build()
+    tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp64": torch.float64}[dtype]
+    count = size // ELEM[dtype]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    xs = [(torch.rand(count, device="cuda", generator=g) * 2 - 1).to(tdt) for _ in range(n)]
+    ys = [torch.empty_like(x) for x in xs]
+    with rra.Comm(n, size) as c:
+        for k, v in attrs.items():
+            c.set_attr(k, int(v))
+        grid, steps = c.plan_call(count, dtype, algo)
+        for _ in range(reps):
+            c.allreduce(xs, ys, algo)
+        torch.cuda.synchronize()
+        st = c.status()[0]
+        same = all(torch.equal(ys[0].view(torch.uint8), y.view(torch.uint8)) for y in ys[1:])
+        print(json.dumps({"case": a, "kernel": c.last_kernel(), "grid": grid, "steps": steps,
+                          "status": rra.STATUS_NAMES.get(st), "ranks_identical": same}), flush=True)
+        return 0 if st == rra.OK and same else 1
 
 
 def stream_launch_us(comm, bufs, cases, torch, stream, reps=400):
@@ -458,6 +536,13 @@ def latency_floor(comm, rra, measure, torch, stream):
     l2_ns = measure.median(l2)
     store_ns = float(np.mean(rtts)) / 2.0
     floor_ns = measure.sol_floor_ns(l2_ns, store_ns)
+    # the floor of the cluster kernels' transport: a bulk copy from an
+    # L2-resident input into a peer CTA's shared memory (half a ping-pong
+    # round trip inside one cluster) plus the one cluster barrier before it
+    ds = [rra.probe_dsmem_pingpong(20000) for _ in range(3)]
+    ds_rtt = measure.median([d[0] for d in ds])
+    ds_bar = measure.median([d[1] for d in ds])
+    dsmem_floor_ns = ds_rtt / 2.0 + ds_bar
 
     def in_kernel(n, algo, reps=200):
         with rra.Comm(n, 128) as c:
@@ -505,15 +590,25 @@ def latency_floor(comm, rra, measure, torch, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     node_us = e0.elapsed_time(e1) * 1000.0 / (20 * 160)
+    def over(key):
+        ref = dsmem_floor_ns if key.endswith("cluster") else floor_ns
+        return round(kern[key] / (ref / 1000.0), 3)
+
     return {"l2_rtt_ns": round(l2_ns, 1), "store_poll_ns": round(store_ns, 1),
             "pingpong_rtt_ns": [round(x, 1) for x in rtts], "pingpong_sms": sm_pairs,
             "floor_us": round(floor_ns / 1000.0, 3),
-            "in_kernel_us_128B": kern, "best_in_kernel": best_key,
-            "best_over_floor": round(kern[best_key] / (floor_ns / 1000.0), 3),
+            "dsmem_bulk_rtt_ns": round(ds_rtt, 1), "cluster_barrier_ns": round(ds_bar, 1),
+            "dsmem_sms": [d[2:] for d in ds], "floor_dsmem_us": round(dsmem_floor_ns / 1000.0, 3),
+            "in_kernel_us_128B": kern, "x_floor": {k: over(k) for k in kern}, "best_in_kernel": best_key,
+            "best_over_floor": over(best_key),
             "empty_kernel_us": round(empty_us, 3), "graph_node_us": round(node_us, 3),
             "method": "L2 RTT: dependent ld.global.cg chase, 8 MiB random cycle; store->poll: half the mean RTT "
                       "of a fence-free ping-pong between CTA 0 and 32 CTAs on other SMs (same-die and cross-die "
-                      "pairs); in-kernel: %globaltimer first CTA start to last CTA end, median of 180 calls"}
+                      "pairs); floor = 2 L2 RTT + store->poll for the global-memory kernels; floor_dsmem = half "
+                      "the RTT of a bulk-copy ping-pong between the 2 CTAs of a cluster (128 B from an "
+                      "L2-resident buffer into the peer's shared memory, completing its mbarrier) + one cluster "
+                      "barrier, for the cluster kernels; in-kernel: %globaltimer first CTA start to last CTA end, "
+                      "median of 180 calls"}
 
 
 def bandwidth_end(rra, measure, torch, hbm_peak, args):
@@ -993,13 +1088,23 @@ def main():
     ap.add_argument("--scratch-sweep", action="store_true",
                     help="add the latency-vs-scratch sweep of the global-memory kernels (Fig. 12; about a minute)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--detail-out", default=None,
+                    help="JSON file for the full result tables (default: bench_detail.json in the temp directory)")
+    ap.add_argument("--case", nargs="+", default=None, metavar="ARG",
+                    help="ALGO NRANKS BYTES DTYPE REPS [attr=value ...]: run one configuration (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
     world, rank, local = dist_env()
+    if args.case is not None:
+        sys.exit(run_case(args))
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+    elif args.gpus > 1 or world > 1:
+        if rank == 0:
+            print(MULTI_GPU_REASON, file=sys.stderr)
+            print(json.dumps(multi_gpu_line(max(args.gpus, world))), flush=True)
     else:
-        run_ours(args, world, rank, local)
+        run_ours(args)
 
 
 if __name__ == "__main__":
