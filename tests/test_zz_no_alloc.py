@@ -108,6 +108,33 @@ def test_static_entry_calls_with_changing_rank_counts(lib):
         del ks, kr
 
 
+def test_static_entry_allocates_no_device_memory(lib):
+    """Free device memory is the same before and after two calls (buffers,
+    the status word and the first call's set-up are all in place first)."""
+    stream = torch.cuda.current_stream()
+    n, count = 4, 2048
+    host = inputs.normal(inputs.rng(82, 0, n, count), n, count, "fp32")
+    xs = _dev(host, "fp32")
+    got = [torch.empty_like(x) for x in xs]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp, ks = _ptrs(xs)
+    rp, kr = _ptrs(got)
+    args = (n, sp, rp, count, rra.DTYPES["fp32"], ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+    assert lib.rra_allreduce_static(*args) == rra.OK
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(2):
+        assert lib.rra_allreduce_static(*args) == rra.OK
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    assert int(status.item()) == 0
+    expect = oracle.allreduce(host, "fp32")
+    for r in range(n):
+        assert np.array_equal(_bits(got[r]), expect[r].view(np.uint8))
+    del ks, kr
+
+
 def test_static_entry_rejects_what_does_not_fit(lib):
     x = [torch.zeros(8192, device="cuda") for _ in range(9)]
     sp, ks = _ptrs(x)
