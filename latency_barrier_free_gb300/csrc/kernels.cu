@@ -125,7 +125,6 @@ __device__ __forceinline__ CtaState cta_prologue(const Params& p, bool need_epoc
     s.t_start = globaltimer_ns();
     s.rank = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
     s.sub = (int)(blockIdx.x % (unsigned)p.ctas_per_rank);
-    if (threadIdx.x == 0 && p.timing != nullptr) p.timing[2 * blockIdx.x] = s.t_start;
     s.advance = need_epoch;
     s.epoch = need_epoch ? ld_relaxed_u64(&p.ctrl->epoch_m1[blockIdx.x]) + 1ull : 0ull;
     const uint32_t status = ld_relaxed_u32(&p.ctrl->status);
@@ -157,7 +156,10 @@ __device__ __forceinline__ void cta_epilogue(const Params& p, const CtaState& s)
     }
     if (threadIdx.x == 0) {
         const uint64_t t_end = globaltimer_ns();
-        if (p.timing != nullptr) p.timing[2 * blockIdx.x + 1] = t_end;
+        if (p.timing != nullptr) {  // both stamps at the end: no store on the timed path
+            p.timing[2 * blockIdx.x] = s.t_start;
+            p.timing[2 * blockIdx.x + 1] = t_end;
+        }
         if (p.trace != nullptr) {
             p.trace[(uint64_t)blockIdx.x * kTracePoints] = s.t_start;
             p.trace[(uint64_t)blockIdx.x * kTracePoints + 5] = t_end;
@@ -445,10 +447,45 @@ __device__ __forceinline__ bool prefetch_first(const Params& p, uint4& pre) {
     return true;
 }
 
+// Address hints for the lines a one-shot thread touches first -- its input
+// vector, its output, its slot in every peer window and the slots it polls in
+// its own window (both parities: the epoch is not known yet), and the
+// control words -- issued before the kernel waits for its predecessor.  A
+// prefetch reads no data into the SM, so it may precede griddepcontrol.wait;
+// it fills L2 and the address translations while the previous kernel drains.
+// Small N only (N <= 8).
+template <bool kLL>
+__device__ __forceinline__ void prefetch_paths(const Params& p) {
+    constexpr uint32_t kPosBytes = kLL ? 2 * kVecBytes : kVecBytes;
+    const uint32_t sub = blockIdx.x % (unsigned)p.ctas_per_rank;
+    const int r = (int)(blockIdx.x / (unsigned)p.ctas_per_rank);
+    const uint32_t v = sub * p.per_cta + threadIdx.x;
+    if (threadIdx.x == 0) {
+        prefetch_l2(&p.ctrl->status);
+        prefetch_l2(&p.ctrl->epoch_m1[blockIdx.x]);
+    }
+    if (p.nranks > 8 || v >= min((sub + 1u) * p.per_cta, min(p.chunk_vecs, p.nvec))) return;
+    const uint64_t pos = (uint64_t)v * kPosBytes;
+    prefetch_l2((const char*)p.send[r] + (uint64_t)v * kVecBytes);
+    prefetch_l2((const char*)p.recv[r] + (uint64_t)v * kVecBytes);
+    for (int q = 0; q < p.nranks; ++q) {
+        if (q == r) continue;
+        const char* peer = window(p, q) + p.region_off + (uint64_t)r * p.slot_bytes + pos;
+        const char* mine = window(p, r) + p.region_off + (uint64_t)q * p.slot_bytes + pos;
+        prefetch_l2(peer);
+        prefetch_l2(mine);
+        if (kLL || p.nsteps > 1) {
+            prefetch_l2(peer + p.parity_bytes);
+            prefetch_l2(mine + p.parity_bytes);
+        }
+    }
+}
+
 template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_kernel(const __grid_constant__ Params p) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     warm_params(p);
+    prefetch_paths<kLL>(p);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     uint4 pre;
     const bool has_pre = prefetch_first<T>(p, pre);
