@@ -126,7 +126,9 @@ typedef enum {
     RRA_ATTR_POLL_TIMEOUT_MS = 1,  /* limit of every device-side wait (default 1000) */
     RRA_ATTR_THREADS = 2,          /* largest threads per CTA: 64, 128 (default) or 256; while
                                       it is not set, the cluster two-shot may use 256 for
-                                      messages up to ~1-2 MiB per rank */
+                                      messages up to ~1-2 MiB per rank.  RRA_TWOSHOT_DBUF and
+                                      RRA_TWOSHOT_DIRECT use at most 128 (their kernels are
+                                      built for 4 CTAs of 128 threads per SM) */
     RRA_ATTR_TWOSHOT_CHUNK = 3,    /* bytes per rank per two-shot step (RRA_TWOSHOT_DBUF,
                                       RRA_TWOSHOT_DIRECT); 0 (default) = one 16-byte position
                                       per thread of the largest co-resident grid, at most the
