@@ -300,6 +300,11 @@ def test_probes():
     sms = rra.probe_sm_count()
     rtt, sa, sb = rra.probe_pingpong(0, sms - 1, 2000)
     assert sa != sb and 50.0 < rtt < 100000.0
+    # bulk-copy ping-pong inside a 2-CTA cluster: SM ids, a round trip and a
+    # cluster barrier in a plausible range
+    brtt, bar, s0, s1 = rra.probe_dsmem_pingpong(2000)
+    assert 0 <= s0 < sms and 0 <= s1 < sms
+    assert 20.0 < brtt < 100000.0 and 1.0 < bar < 100000.0
     rra.probe_empty_kernel()
     torch.cuda.synchronize()
 
