@@ -145,7 +145,11 @@ typedef enum {
                                       guarantees that all CTAs are resident together;
                                       0: plain launch of the same occupancy-checked grid
                                       (progress then relies on no other work holding the
-                                      SMs for longer than the poll time limit) */
+                                      SMs for longer than the poll time limit).  Either
+                                      way, a global-memory one-shot with one CTA per rank
+                                      on 2-16 CTAs launches as one thread-block cluster,
+                                      which keeps its ranks on one GPC and is resident
+                                      together by construction */
     RRA_ATTR_PDL = 8,              /* 1 (default): programmatic dependent launch, so
                                       the next kernel on the stream is scheduled while
                                       this one drains; each kernel waits

@@ -20,6 +20,10 @@
 
 #include "rra.h"
 #include "rra_internal.h"
+#include "placement.h"
+
+static_assert(rra::placement::kMaxRanks == rra::kClusterMaxRanks, "bulk-copy kernels serve up to 16 ranks");
+static_assert(rra::placement::kVecBytes == (size_t)rra::kVecBytes, "one transfer vector");
 
 using rra::Ctrl;
 using rra::Params;
@@ -112,15 +116,7 @@ struct rra_comm {
     int64_t coll_split = -1;                // Broadcast/Reduce in two hops: -1 auto, 0 never, 1 always
     int residual_fits[2][2][3] = {{{-1, -1, -1}, {-1, -1, -1}}, {{-1, -1, -1}, {-1, -1, -1}}};  // [bulk][two][dtype]
     int residual_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
-    // source sets that passed the bulk-copy check (bulk_sources_local), newest
-    // overwriting the oldest
-    struct LocalSources {
-        int n = 0;
-        size_t bytes = 0;
-        const void* ptr[rra::kClusterMaxRanks] = {};
-    };
-    std::array<LocalSources, 8> local_sources;
-    int local_next = 0;
+    rra::placement::SourceCache local_sources;  // source sets that passed the bulk-copy check
     const char* last_kernel = "none";       // the kernel the last enqueued call launched
     int32_t drop_rank = -1;                 // injected fault (rra_comm_inject_drop), -1 = none
     bool poisoned = false;
@@ -203,30 +199,12 @@ bool on_device(int dev, const void* p) {
 
 }  // namespace
 
-// True when bulk copies may read `bytes` (rounded up to whole 16-byte
-// vectors: a copy reads the last vector in full) from each of src[0..n-1].
-// Source sets that passed are remembered (the last 8), so repeated calls on
-// the same buffers query nothing.  Called with c->mu held.
+// True when bulk copies may read `bytes` from each of src[0..n-1] (the rule
+// and its cache: placement.h).  Called with c->mu held.
 static bool bulk_sources_local(rra_comm* c, const void* const src[], int n, size_t bytes) {
-    if (n < 1 || n > rra::kClusterMaxRanks || bytes == 0) return false;
-    if (other_gpu_in_use(c->device)) return false;
-    for (const auto& e : c->local_sources) {
-        if (e.n != n || bytes > e.bytes) continue;
-        bool same = true;
-        for (int r = 0; r < n && same; ++r) same = e.ptr[r] == src[r];
-        if (same) return true;
-    }
-    const size_t span = (bytes + rra::kVecBytes - 1) / rra::kVecBytes * rra::kVecBytes;
-    for (int r = 0; r < n; ++r) {
-        if (src[r] == nullptr) return false;
-        if (!on_device(c->device, src[r]) || !on_device(c->device, (const char*)src[r] + (span - 1))) return false;
-    }
-    auto& e = c->local_sources[(size_t)c->local_next];
-    c->local_next = (c->local_next + 1) % (int)c->local_sources.size();
-    e.n = n;
-    e.bytes = bytes;
-    for (int r = 0; r < n; ++r) e.ptr[r] = src[r];
-    return true;
+    const int dev = c->device;
+    return rra::placement::bulk_sources_local(c->local_sources, other_gpu_in_use(dev), src, n, bytes,
+                                              [dev](const void* p) { return on_device(dev, p); });
 }
 
 extern "C" {
@@ -1385,8 +1363,10 @@ rra_status_t rra_comm_reset(rra_comm_t c) {
         cudaDeviceSynchronize() != cudaSuccess)
         return RRA_ERR_CUDA;
     if (c->host_status) *(volatile uint32_t*)c->host_status = 0u;
+    std::lock_guard<std::mutex> g(c->mu);
     c->poisoned = false;
     c->drop_rank = -1;
+    c->local_sources.clear();
     return RRA_OK;
 }
 
