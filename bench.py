@@ -462,7 +462,10 @@ def summary_line(d, detail_path):
 def run_case(args):
     """--case ALGO NRANKS BYTES DTYPE REPS [attr=value ...]: one configuration
     REPS times, for profiling one kernel (seeded uniform(-1, 1) inputs on the
-    device).  Checks the device status and that every rank got the same bits."""
+    device).  Checks the device status and that every rank got the same bits.
+    ALGO may also name a collective (reduce_scatter, all_gather, broadcast,
+    reduce; root 0), BYTES then being one block; for those the check is the
+    device status, plus identical outputs for AllGather and Broadcast."""
     import torch
 
     import __graft_entry__
@@ -478,6 +481,24 @@ def run_case(args):
     count = size // ELEM[dtype]
     g = torch.Generator(device="cuda")
     g.manual_seed(3)
+    if algo in rra.COLLECTIVES:
+        blocks_in = n if algo == "reduce_scatter" else 1
+        blocks_out = n if algo == "all_gather" else 1
+        xs = [(torch.rand(blocks_in * count, device="cuda", generator=g) * 2 - 1).to(tdt) for _ in range(n)]
+        ys = [torch.empty(blocks_out * count, dtype=tdt, device="cuda") for _ in range(n)]
+        with rra.Comm(n, n * size) as c:
+            for k, v in attrs.items():
+                c.set_attr(k, int(v))
+            sp, rp = [t.data_ptr() for t in xs], [t.data_ptr() for t in ys]
+            for _ in range(reps):
+                c.collective_ptrs(algo, sp, rp, count, dtype, 0)
+            torch.cuda.synchronize()
+            st = c.status()[0]
+            same = algo in ("reduce_scatter", "reduce") or all(
+                torch.equal(ys[0].view(torch.uint8), y.view(torch.uint8)) for y in ys[1:])
+            print(json.dumps({"case": a, "kernel": c.last_kernel(), "status": rra.STATUS_NAMES.get(st),
+                              "ranks_identical": same}), flush=True)
+            return 0 if st == rra.OK and same else 1
     xs = [(torch.rand(count, device="cuda", generator=g) * 2 - 1).to(tdt) for _ in range(n)]
     ys = [torch.empty_like(x) for x in xs]
     with rra.Comm(n, size) as c:
@@ -614,7 +635,11 @@ def latency_floor(comm, rra, measure, torch, stream):
 def bandwidth_end(rra, measure, torch, hbm_peak, args):
     """Workload 5: N=8, binary32 and binary64 uniform(-1, 1), 4 / 64 / 512 MiB
     per rank, the two-shot kernels.  Enough buffer sets are rotated that
-    each call's working set was evicted from L2 (more than 2x its 129 MB)."""
+    each call's working set was evicted from L2 (more than 2x its 129 MB).
+    The calls are timed as a CUDA graph replay of the rotation (device time,
+    launch gaps included); issued one by one from Python, the marshalling of
+    16 tensors per call (about 20 us) would set the pace at 4 MiB per rank,
+    so that figure is kept beside it as `eager_ms`."""
     out = {}
     n = 8
     sizes = [4 << 20, 64 << 20] + ([512 << 20] if args.big else [])
@@ -644,16 +669,36 @@ def bandwidth_end(rra, measure, torch, hbm_peak, args):
                         c.allreduce(*sets[k % nsets], algo)
                     e1.record()
                     torch.cuda.synchronize()
+                    t_eager = e0.elapsed_time(e1) / 1000.0 / reps
+                    cap = torch.cuda.Stream()
+                    cap.wait_stream(torch.cuda.current_stream())
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=cap):
+                        for k in range(reps):
+                            c.allreduce(*sets[k % nsets], algo)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    ts = []
+                    for _ in range(3):
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        g.replay()
+                        e1.record()
+                        torch.cuda.synchronize()
+                        ts.append(e0.elapsed_time(e1) / 1000.0 / reps)
+                    del g
                     st = c.status()[0]
-                    t = e0.elapsed_time(e1) / 1000.0 / reps
+                    t = measure.median(ts)
                     gbs = measure.hbm_gbs(n, size, t)
                     out["%s/%s/%dMiB" % (algo, dtype, size >> 20)] = {
                         "ms": round(t * 1000, 3), "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
-                        "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1), "status": rra.STATUS_NAMES.get(st)}
+                        "busbw_GB/s": round(measure.busbw_gbs(n, size, t), 1), "eager_ms": round(t_eager * 1000, 3),
+                        "status": rra.STATUS_NAMES.get(st)}
                 del sets
             torch.cuda.empty_cache()
     return {"nranks": n, "bytes": "2*N*M per call", "sizes": out,
-            "note": "L2 evicted between calls (rotating buffer sets, >2x L2); CUDA events; default chunking"}
+            "note": "L2 evicted between calls (rotating buffer sets, >2x L2); CUDA events around a CUDA-graph "
+                    "replay of the rotation (eager_ms: the same calls issued one by one from Python); default chunking"}
 
 
 def _graph_us(torch, measure, fn, calls=16, reps=20):
