@@ -72,6 +72,32 @@ __device__ __forceinline__ void bulk_g2s_multicast(uint32_t dst, const void* src
         : "memory");
 }
 
+// Bulk copy (the TMA engine) of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) from this CTA's shared memory `src` to global memory
+// `dst`, in the issuing thread's bulk group.  Data that an earlier bulk copy
+// or st.async wrote into `src` is read once the mbarrier that counted it has
+// completed and fence_proxy_async_smem() has run.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :
+                 : "l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// The issuing thread's bulk copies to global memory, committed and waited
+// for until their writes are done (so shared memory may be released and the
+// outputs are complete when the CTA exits).
+__device__ __forceinline__ void bulk_s2g_commit_wait() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Orders this CTA's earlier shared-memory accesses before later accesses by
+// the async proxy (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(

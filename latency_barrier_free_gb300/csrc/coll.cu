@@ -230,7 +230,12 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
 // so the same page, as valid data) and its extra lanes are never stored.  A
 // CTA leaves after a cluster barrier that every CTA reaches once its own
 // bytes are in, so no copy it issued is still in flight.
-template <typename T, int kOp>
+// kStoreBulk: the window goes to the output by bulk copies too (one per
+// block, issued by thread 0, waited for before the CTA leaves) instead of
+// vector stores by every thread; the host chooses it only when every output
+// is device memory of this GPU and a block is a whole number of 16-byte
+// vectors (so no copy writes past its block).
+template <typename T, int kOp, bool kStoreBulk>
 __global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) uint4 stage[];  // AllGather [N][S], Broadcast [S]
     __shared__ __align__(8) uint64_t bar;
@@ -272,7 +277,18 @@ __global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ 
         }
     }
     cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
-    if (ok) {
+    if (ok && kStoreBulk) {
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            constexpr uint32_t nblk = kOp == kCollAllGather ? kClusterMaxRanks : 1u;
+            const uint64_t block_bytes = count * sizeof(T);
+#pragma unroll 1
+            for (uint32_t q = 0; q < nblk && q < N; ++q)
+                bulk_s2g((char*)p.recv[r] + q * block_bytes + (uint64_t)base * kVecBytes,
+                         smem_u32(stage + (kOp == kCollAllGather ? q * S : 0u)), npos * (uint32_t)kVecBytes);
+            bulk_s2g_commit_wait();
+        }
+    } else if (ok) {
         if (kOp == kCollAllGather) {
 #pragma unroll 1
             for (uint32_t v = threadIdx.x; v < N * npos; v += nt) {
@@ -642,8 +658,10 @@ bool coll_has_bulk(int op, int nranks) {
     return (op == kCollAllGather || op == kCollBroadcast) && nranks <= kClusterMaxRanks;
 }
 
-const char* coll_kernel_name(int op, int nranks, bool bulk) {
+const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
     static const char* const kBulk[] = {"", "coll_bulk_kernel<all_gather>", "coll_bulk_kernel<broadcast>"};
+    static const char* const kBulkStore[] = {"", "coll_bulk_kernel<all_gather, bulk store>",
+                                             "coll_bulk_kernel<broadcast, bulk store>"};
     static const char* const kPlain[] = {"coll_kernel<reduce_scatter>", "coll_kernel<all_gather>",
                                          "coll_kernel<broadcast>", "coll_kernel<reduce>"};
     static const char* const kMulti[] = {"coll_multi_kernel<reduce_scatter>", "coll_multi_kernel<all_gather>",
@@ -651,23 +669,26 @@ const char* coll_kernel_name(int op, int nranks, bool bulk) {
     if (op < 0 || op > kCollReduceSplit) return "unknown";
     if (op == kCollBroadcastSplit) return "coll_split_kernel<broadcast>";
     if (op == kCollReduceSplit) return "coll_split_kernel<reduce>";
-    if (bulk && coll_has_bulk(op, nranks)) return kBulk[op];
+    if (bulk && coll_has_bulk(op, nranks)) return store_bulk ? kBulkStore[op] : kBulk[op];
     return nranks > kClusterMaxRanks ? kMulti[op] : kPlain[op];
 }
 
 template <typename T>
-static const void* coll_bulk_for(int op) {
-    return op == kCollAllGather ? (const void*)coll_bulk_kernel<T, kCollAllGather>
-                                : (const void*)coll_bulk_kernel<T, kCollBroadcast>;
+static const void* coll_bulk_for(int op, bool store_bulk) {
+    if (store_bulk)
+        return op == kCollAllGather ? (const void*)coll_bulk_kernel<T, kCollAllGather, true>
+                                    : (const void*)coll_bulk_kernel<T, kCollBroadcast, true>;
+    return op == kCollAllGather ? (const void*)coll_bulk_kernel<T, kCollAllGather, false>
+                                : (const void*)coll_bulk_kernel<T, kCollBroadcast, false>;
 }
 
-static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks, bool bulk) {
+static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks, bool bulk, bool store_bulk = false) {
     const bool multi = nranks > kClusterMaxRanks;
     if (bulk && coll_has_bulk(op, nranks)) {
         switch (dtype) {
-            case RRA_FP32: return coll_bulk_for<float>(op);
-            case RRA_BF16: return coll_bulk_for<__nv_bfloat16>(op);
-            case RRA_FP64: return coll_bulk_for<double>(op);
+            case RRA_FP32: return coll_bulk_for<float>(op, store_bulk);
+            case RRA_BF16: return coll_bulk_for<__nv_bfloat16>(op, store_bulk);
+            case RRA_FP64: return coll_bulk_for<double>(op, store_bulk);
         }
         return nullptr;
     }
@@ -722,7 +743,7 @@ size_t coll_stage_bytes(const Params& p, int op) {
 }
 
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl,
-                        bool bulk) {
+                        bool bulk, bool store_bulk) {
     const size_t smem = coll_stage_bytes(p, op);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kMaxRanks || p.root < 0 ||
         p.root >= p.nranks)
@@ -730,7 +751,10 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
     if ((op == kCollBroadcastSplit || op == kCollReduceSplit) && p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
     const int cdim = coll_cdim(p.nranks);
-    const void* k = coll_kernel_ptr(dtype, op, p.nranks, bulk);
+    const uint64_t es = dtype == RRA_BF16 ? 2u : dtype == RRA_FP64 ? 8u : 4u;
+    if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || (p.count * es) % kVecBytes != 0))
+        return cudaErrorInvalidValue;  // a bulk copy would write past its block
+    const void* k = coll_kernel_ptr(dtype, op, p.nranks, bulk, store_bulk);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = configure_coll(k);
     if (e != cudaSuccess) return e;

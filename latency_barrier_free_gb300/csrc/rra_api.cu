@@ -672,8 +672,8 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
 // the cluster AllReduce (one vector per thread while small, then about two
 // CTAs per SM), with at most one batch of kClusterBatch input vectors per
 // thread and the 96 KiB stage (N slots of S vectors; one slot for Broadcast).
-static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int op, int root, bool bulk, Params* p,
-                              int* threads) {
+static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int op, int root, bool bulk,
+                              bool store_bulk, Params* p, int* threads) {
     int& fits = c->coll_fits[bulk ? 1 : 0][op][(int)dtype];
     if (fits < 0) fits = rra::coll_max_active(dtype, op, c->nranks, 256, rra::kClusterStageBytes, bulk) > 0 ? 1 : 0;
     if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
@@ -711,6 +711,21 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t S;
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else if (store_bulk) {
+        // Outputs by bulk copies: the threads no longer move the data, so
+        // their count does not bound the slice.  Slices for about 8 clusters
+        // per SM's worth of CTAs, each AllGather window (N slots of S
+        // vectors) at most 32 KiB and at least 512 bytes per slot, each
+        // Broadcast slice 4-32 KiB.  (Sweeps at N = 2, 4, 8, 16 and 1-64 MiB
+        // blocks put the best slice there.)
+        const size_t target = std::max<size_t>(1, 8 * (size_t)c->sm_count / cdim);
+        if (op == rra::kCollAllGather) {
+            const size_t window = std::max<size_t>(1, (32u << 10) / rra::kVecBytes / n);
+            S = std::min<size_t>(window, std::max<size_t>(32, ceil_div(p->nvec, target)));
+        } else {
+            S = std::min<size_t>(2048, std::max<size_t>(256, ceil_div(p->nvec, target)));
+        }
+        S = std::max<size_t>(1, std::min<size_t>(S, p->nvec));
     } else {
         const size_t target = std::max<size_t>(1, 2 * (size_t)c->sm_count / cdim);
         S = std::max<size_t>(std::min<size_t>(p->nvec, std::max<size_t>(1, t / per_pos)), ceil_div(p->nvec, target));
@@ -1153,28 +1168,43 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
     const size_t es = elem_size(dtype);
     const size_t blocks = (op == rra::kCollReduceScatter || op == rra::kCollAllGather) ? (size_t)c->nranks : 1;
     if (count > c->max_bytes / es / blocks) return RRA_ERR_INVALID_ARG;
-    // Broadcast / Reduce: two hops for large messages (the root's CTA no
-    // longer carries all of a slice's traffic), one hop for small ones; the
-    // two-hop forms exist for up to 16 ranks
-    if ((op == rra::kCollBroadcast || op == rra::kCollReduce) && c->nranks <= rra::kClusterMaxRanks) {
-        const bool split = c->coll_split == 1 || (c->coll_split < 0 && c->nranks >= 3 && count * es >= (256u << 10));
-        if (split) op = op == rra::kCollBroadcast ? rra::kCollBroadcastSplit : rra::kCollReduceSplit;
-    }
     Params p;
     int threads = 0;
-    bool bulk = false;
+    bool bulk = false, store_bulk = false;
     {
         std::lock_guard<std::mutex> g(c->mu);
         // AllGather and Broadcast (up to 16 ranks) push by bulk copies from
-        // the senders' inputs, when those are device memory of this GPU
+        // the senders' inputs, when those are device memory of this GPU; and
+        // from 4 KiB blocks up (below, waiting for the copies' writes costs
+        // more than it saves) write their outputs by bulk copies too, when
+        // those are device memory of this GPU and a block is whole 16-byte
+        // vectors
         if (rra::coll_has_bulk(op, c->nranks) && c->cluster_tma != 0) {
             const int nsrc = op == rra::kCollBroadcast ? 1 : c->nranks;
             const void* const* src = op == rra::kCollBroadcast ? send + root : send;
             bulk = bulk_sources_local(c, src, nsrc, count * es);
+            if (bulk && (count * es) % rra::kVecBytes == 0 && count * es >= (4u << 10)) {
+                const void* out[RRA_MAX_RANKS];
+                for (int r = 0; r < c->nranks; ++r) out[r] = recv[r];
+                store_bulk = bulk_sources_local(c, out, c->nranks, blocks * count * es);
+            }
         }
-        rra_status_t st = plan_coll(c, count, dtype, op, root < 0 ? 0 : root, bulk, &p, &threads);
+        // Broadcast / Reduce: two hops for large messages (the root's CTA no
+        // longer carries all of a slice's traffic), one hop for small ones --
+        // except a Broadcast whose copies are all bulk copies, which stays one
+        // hop (the root's slice reaches every CTA in one multicast copy); the
+        // two-hop forms exist for up to 16 ranks
+        if ((op == rra::kCollBroadcast || op == rra::kCollReduce) && c->nranks <= rra::kClusterMaxRanks) {
+            const bool split = c->coll_split == 1 ||
+                               (c->coll_split < 0 && !store_bulk && c->nranks >= 3 && count * es >= (256u << 10));
+            if (split) {
+                op = op == rra::kCollBroadcast ? rra::kCollBroadcastSplit : rra::kCollReduceSplit;
+                bulk = store_bulk = false;
+            }
+        }
+        rra_status_t st = plan_coll(c, count, dtype, op, root < 0 ? 0 : root, bulk, store_bulk, &p, &threads);
         if (st != RRA_OK) return st;
-        c->last_kernel = rra::coll_kernel_name(op, c->nranks, bulk);
+        c->last_kernel = rra::coll_kernel_name(op, c->nranks, bulk, store_bulk);
     }
     const bool bcast = op == rra::kCollBroadcast || op == rra::kCollBroadcastSplit;
     const bool reduce = op == rra::kCollReduce || op == rra::kCollReduceSplit;
@@ -1188,7 +1218,7 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
         p.recv[r] = need_recv ? recv[r] : nullptr;
     }
     p.drop_rank = c->drop_rank;
-    cudaError_t e = rra::launch_coll(p, dtype, op, threads, (cudaStream_t)stream, c->pdl != 0, bulk);
+    cudaError_t e = rra::launch_coll(p, dtype, op, threads, (cudaStream_t)stream, c->pdl != 0, bulk, store_bulk);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return RRA_ERR_CUDA;

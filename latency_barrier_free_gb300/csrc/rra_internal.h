@@ -134,11 +134,13 @@ enum {
 size_t coll_stage_bytes(const Params& p, int op);
 // bulk: AllGather / Broadcast up to 16 ranks on the bulk-copy kernel (the
 // caller has checked that every input it reads is device memory of this GPU);
-// otherwise the st.async kernels.
+// otherwise the st.async kernels.  store_bulk (with bulk): the outputs are
+// written by bulk copies as well (the caller has checked that every output
+// is device memory of this GPU and that a block is whole 16-byte vectors).
 bool coll_has_bulk(int op, int nranks);
-const char* coll_kernel_name(int op, int nranks, bool bulk);
+const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk);
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl,
-                        bool bulk);
+                        bool bulk, bool store_bulk);
 int coll_max_active(rra_dtype_t dtype, int op, int nranks, int threads, size_t smem, bool bulk);
 // AllReduce + residual add on the public device API (fused.cu): the cluster
 // AllReduce's launch shape; cluster c handles slices c, c + G, ... of

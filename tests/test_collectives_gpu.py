@@ -13,7 +13,7 @@ from tests.gpu_util import ELEM, bits, poison_like, to_device, to_host
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-COUNTS = (1, 3, 5, 33, 4097, 20001)
+COUNTS = (1, 3, 5, 33, 4096, 4097, 20000, 20001)  # 4096, 20000: blocks of whole 16-byte vectors
 
 
 @pytest.fixture(scope="module", autouse=True)
