@@ -1175,15 +1175,16 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
         std::lock_guard<std::mutex> g(c->mu);
         // AllGather and Broadcast (up to 16 ranks) push by bulk copies from
         // the senders' inputs, when those are device memory of this GPU; and
-        // from 4 KiB blocks up (below, waiting for the copies' writes costs
-        // more than it saves) write their outputs by bulk copies too, when
-        // those are device memory of this GPU and a block is whole 16-byte
-        // vectors
+        // write their outputs by bulk copies too, when those are device
+        // memory of this GPU and a block is whole 16-byte vectors, from 4 KiB
+        // blocks (AllGather) or 256 KiB (Broadcast) up: below, the vector
+        // stores measured faster
         if (rra::coll_has_bulk(op, c->nranks) && c->cluster_tma != 0) {
             const int nsrc = op == rra::kCollBroadcast ? 1 : c->nranks;
             const void* const* src = op == rra::kCollBroadcast ? send + root : send;
             bulk = bulk_sources_local(c, src, nsrc, count * es);
-            if (bulk && (count * es) % rra::kVecBytes == 0 && count * es >= (4u << 10)) {
+            const size_t store_min = op == rra::kCollBroadcast ? (256u << 10) : (4u << 10);
+            if (bulk && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
                 const void* out[RRA_MAX_RANKS];
                 for (int r = 0; r < c->nranks; ++r) out[r] = recv[r];
                 store_bulk = bulk_sources_local(c, out, c->nranks, blocks * count * es);

@@ -104,12 +104,13 @@ def test_bulk_copy_attribute_off():
         check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
 
 
-@pytest.mark.parametrize("m", [1000, 1024, 1025])
+@pytest.mark.parametrize("m", [1000, 1024, 1025, 65536, 65537])
 def test_collectives_choose_their_push_by_source_memory(m):
     """AllGather and Broadcast push by bulk copies from device inputs, by
     st.async from inputs in host memory; with device inputs and outputs and
-    blocks of whole 16-byte vectors of at least 4 KiB (m = 1024 fp32) they
-    also write the outputs by bulk copies.  The results are the oracle's."""
+    blocks of whole 16-byte vectors of at least 4 KiB (AllGather) or 256 KiB
+    (Broadcast) they also write the outputs by bulk copies.  The results are
+    the oracle's."""
     n = 4
     small_np = [inputs.normal(inputs.rng(94, r), 1, m, "fp32")[0] for r in range(n)]
     want_ag = oracle.all_gather(small_np, "fp32")
@@ -117,14 +118,15 @@ def test_collectives_choose_their_push_by_source_memory(m):
     hs = _pinned(small_np)
     dev_host = rra.host_device_ptrs([t.data_ptr() for t in hs])
     on_device = to_device(small_np, "fp32")  # kept alive: the calls read it
-    store = ", bulk store" if m % 4 == 0 and m * 4 >= 4096 else ""
+    store_ag = ", bulk store" if m % 4 == 0 and m * 4 >= 4096 else ""
+    store_bc = ", bulk store" if m % 4 == 0 and m * 4 >= 262144 else ""
     with rra.Comm(n, n * m * 4) as comm:
         for where, src in (("device", [t.data_ptr() for t in on_device]), ("host", dev_host)):
             out = [torch.full((n * m,), float("nan"), device="cuda") for _ in range(n)]
             comm.collective_ptrs("all_gather", src, [t.data_ptr() for t in out], m, "fp32", 0)
             torch.cuda.synchronize()
             kind = comm.last_kernel()
-            assert kind == ("coll_bulk_kernel<all_gather%s>" % store if where == "device"
+            assert kind == ("coll_bulk_kernel<all_gather%s>" % store_ag if where == "device"
                             else "coll_kernel<all_gather>"), kind
             for g, w in zip(out, want_ag):
                 assert np.array_equal(bits(g.cpu().numpy()), bits(w))
@@ -132,8 +134,13 @@ def test_collectives_choose_their_push_by_source_memory(m):
             comm.collective_ptrs("broadcast", src, [t.data_ptr() for t in bc], m, "fp32", 2)
             torch.cuda.synchronize()
             kind = comm.last_kernel()
-            assert kind == ("coll_bulk_kernel<broadcast%s>" % store if where == "device"
-                            else "coll_kernel<broadcast>"), kind
+            if where == "device" and store_bc:
+                want_kind = "coll_bulk_kernel<broadcast, bulk store>"
+            elif m * 4 >= 262144:  # from 256 KiB a Broadcast without bulk stores takes two hops
+                want_kind = "coll_split_kernel<broadcast>"
+            else:
+                want_kind = "coll_bulk_kernel<broadcast>" if where == "device" else "coll_kernel<broadcast>"
+            assert kind == want_kind, kind
             for g, w in zip(bc, want_bc):
                 assert np.array_equal(bits(g.cpu().numpy()), bits(w))
         assert comm.status()[0] == rra.OK
@@ -143,7 +150,7 @@ def test_collective_outputs_in_host_memory_get_vector_stores():
     """Device inputs, outputs in pinned host memory: the push is by bulk
     copies, the outputs are written by vector stores (no bulk copy writes
     host memory)."""
-    n, m = 4, 1024
+    n, m = 4, 65536
     small_np = [inputs.normal(inputs.rng(96, r), 1, m, "fp32")[0] for r in range(n)]
     want_ag = oracle.all_gather(small_np, "fp32")
     want_bc = oracle.broadcast(small_np, "fp32", 1)
@@ -159,7 +166,7 @@ def test_collective_outputs_in_host_memory_get_vector_stores():
         assert comm.last_kernel() == "coll_bulk_kernel<all_gather>"
         comm.collective_ptrs("broadcast", src, dev_hb, m, "fp32", 1)
         torch.cuda.synchronize()
-        assert comm.last_kernel() == "coll_bulk_kernel<broadcast>"
+        assert comm.last_kernel() == "coll_split_kernel<broadcast>"  # no bulk stores: two hops at 256 KiB
         assert comm.status()[0] == rra.OK
     for g, w in zip(ho, want_ag):
         assert np.array_equal(bits(g.numpy()), bits(w))
