@@ -309,6 +309,73 @@ __global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ 
     }
 }
 
+// ReduceScatter up to 16 ranks with the push made by the TMA engine: thread
+// q of CTA r copies the slice of block q of rank r's input into slot [r] of
+// CTA q's window (one bulk copy, completing CTA q's mbarrier; q = r is the
+// own slot).  CTA q then adds its N slots in rank order into recv[q].  The
+// host chooses it only when every input is device memory of this GPU and a
+// block is a whole number of 16-byte vectors, so that every copy starts on a
+// 16-byte boundary and reads its block alone.  The CTA leaves after a
+// cluster barrier that every CTA reaches once its own bytes are in.
+template <typename T>
+__global__ void __launch_bounds__(256) coll_rs_bulk_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];  // [N][S]
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint64_t count = p.count;
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, N * npos * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = p.drop_rank;
+    cluster_wait();  // every peer's barrier exists before any copy completes on it
+    {
+        const uint32_t q = threadIdx.x;
+        if (q < N && (q == r || drop != (int32_t)r))
+            bulk_g2s_multicast(smem_u32(stage + r * S),
+                               (const char*)p.send[r] + q * count * sizeof(T) + (uint64_t)base * kVecBytes,
+                               npos * (uint32_t)kVecBytes, my_bar, (uint16_t)(1u << q));
+    }
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
+    if (ok) {
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < npos; u += nt) {
+            typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * S + u]);
+            store_block<T>(p.recv[r], 0, base + u, count, M::store(acc));
+        }
+    }
+    cluster_wait();  // every CTA's bytes are in: none of my copies is still in flight
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 // The same four collectives for nranks > 16 (clusters hold at most 16
 // CTAs): a cluster of G = 16 CTAs per slice, CTA j acting for ranks j,
 // j + G, j + 2G, ... (as the many-rank cluster AllReduce).  A push to a rank
@@ -653,13 +720,16 @@ static const void* coll_kernel_for(int op, bool multi) {
     return nullptr;
 }
 
-// AllGather and Broadcast up to 16 ranks have a bulk-copy kernel.
+// ReduceScatter, AllGather and Broadcast up to 16 ranks have a bulk-copy
+// kernel (ReduceScatter only for blocks of whole 16-byte vectors).
 bool coll_has_bulk(int op, int nranks) {
-    return (op == kCollAllGather || op == kCollBroadcast) && nranks <= kClusterMaxRanks;
+    return (op == kCollReduceScatter || op == kCollAllGather || op == kCollBroadcast) &&
+           nranks <= kClusterMaxRanks;
 }
 
 const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
-    static const char* const kBulk[] = {"", "coll_bulk_kernel<all_gather>", "coll_bulk_kernel<broadcast>"};
+    static const char* const kBulk[] = {"coll_bulk_kernel<reduce_scatter>", "coll_bulk_kernel<all_gather>",
+                                        "coll_bulk_kernel<broadcast>"};
     static const char* const kBulkStore[] = {"", "coll_bulk_kernel<all_gather, bulk store>",
                                              "coll_bulk_kernel<broadcast, bulk store>"};
     static const char* const kPlain[] = {"coll_kernel<reduce_scatter>", "coll_kernel<all_gather>",
@@ -675,6 +745,7 @@ const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
 
 template <typename T>
 static const void* coll_bulk_for(int op, bool store_bulk) {
+    if (op == kCollReduceScatter) return (const void*)coll_rs_bulk_kernel<T>;
     if (store_bulk)
         return op == kCollAllGather ? (const void*)coll_bulk_kernel<T, kCollAllGather, true>
                                     : (const void*)coll_bulk_kernel<T, kCollBroadcast, true>;
@@ -752,8 +823,11 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
         return cudaErrorInvalidValue;
     const int cdim = coll_cdim(p.nranks);
     const uint64_t es = dtype == RRA_BF16 ? 2u : dtype == RRA_FP64 ? 8u : 4u;
-    if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || (p.count * es) % kVecBytes != 0))
+    if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || op == kCollReduceScatter ||
+                       (p.count * es) % kVecBytes != 0))
         return cudaErrorInvalidValue;  // a bulk copy would write past its block
+    if (bulk && op == kCollReduceScatter && (p.count * es) % kVecBytes != 0)
+        return cudaErrorInvalidValue;  // a block would start off a 16-byte boundary
     const void* k = coll_kernel_ptr(dtype, op, p.nranks, bulk, store_bulk);
     if (k == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = configure_coll(k);

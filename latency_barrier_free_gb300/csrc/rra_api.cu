@@ -711,15 +711,16 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t S;
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
-    } else if (store_bulk) {
-        // Outputs by bulk copies: the threads no longer move the data, so
-        // their count does not bound the slice.  Slices for about 8 clusters
-        // per SM's worth of CTAs, each AllGather window (N slots of S
-        // vectors) at most 32 KiB and at least 512 bytes per slot, each
+    } else if (store_bulk || (bulk && op == rra::kCollReduceScatter)) {
+        // Outputs (AllGather, Broadcast) or inputs (ReduceScatter) moved by
+        // bulk copies: the threads no longer move that data, so their count
+        // does not bound the slice.  Slices for about 8 clusters per SM's
+        // worth of CTAs, each window of N slots of S vectors (AllGather,
+        // ReduceScatter) at most 32 KiB and at least 512 bytes per slot, each
         // Broadcast slice 4-32 KiB.  (Sweeps at N = 2, 4, 8, 16 and 1-64 MiB
         // blocks put the best slice there.)
         const size_t target = std::max<size_t>(1, 8 * (size_t)c->sm_count / cdim);
-        if (op == rra::kCollAllGather) {
+        if (op == rra::kCollAllGather || op == rra::kCollReduceScatter) {
             const size_t window = std::max<size_t>(1, (32u << 10) / rra::kVecBytes / n);
             S = std::min<size_t>(window, std::max<size_t>(32, ceil_div(p->nvec, target)));
         } else {
@@ -1179,12 +1180,15 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
         // memory of this GPU and a block is whole 16-byte vectors, from 4 KiB
         // blocks (AllGather) or 256 KiB (Broadcast) up: below, the vector
         // stores measured faster
-        if (rra::coll_has_bulk(op, c->nranks) && c->cluster_tma != 0) {
+        // ReduceScatter pushes by bulk copies as well (one per owner) when a
+        // block is whole 16-byte vectors, so that every block starts aligned.
+        const bool rs = op == rra::kCollReduceScatter;
+        if (rra::coll_has_bulk(op, c->nranks) && c->cluster_tma != 0 && (!rs || (count * es) % rra::kVecBytes == 0)) {
             const int nsrc = op == rra::kCollBroadcast ? 1 : c->nranks;
             const void* const* src = op == rra::kCollBroadcast ? send + root : send;
-            bulk = bulk_sources_local(c, src, nsrc, count * es);
+            bulk = bulk_sources_local(c, src, nsrc, (rs ? (size_t)c->nranks : 1u) * count * es);
             const size_t store_min = op == rra::kCollBroadcast ? (256u << 10) : (4u << 10);
-            if (bulk && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
+            if (bulk && !rs && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
                 const void* out[RRA_MAX_RANKS];
                 for (int r = 0; r < c->nranks; ++r) out[r] = recv[r];
                 store_bulk = bulk_sources_local(c, out, c->nranks, blocks * count * es);

@@ -132,9 +132,10 @@ enum {
     kCollReduceSplit = 5      // two hops: ReduceScatter, then every owner pushes to the root
 };
 size_t coll_stage_bytes(const Params& p, int op);
-// bulk: AllGather / Broadcast up to 16 ranks on the bulk-copy kernel (the
-// caller has checked that every input it reads is device memory of this GPU);
-// otherwise the st.async kernels.  store_bulk (with bulk): the outputs are
+// bulk: ReduceScatter / AllGather / Broadcast up to 16 ranks on the
+// bulk-copy kernels (the caller has checked that every input they read is
+// device memory of this GPU, and for ReduceScatter that a block is whole
+// 16-byte vectors); otherwise the st.async kernels.  store_bulk (with bulk): the outputs are
 // written by bulk copies as well (the caller has checked that every output
 // is device memory of this GPU and that a block is whole 16-byte vectors).
 bool coll_has_bulk(int op, int nranks);

@@ -146,6 +146,30 @@ def test_collectives_choose_their_push_by_source_memory(m):
         assert comm.status()[0] == rra.OK
 
 
+@pytest.mark.parametrize("m", [1000, 1001])
+def test_reduce_scatter_chooses_its_push_by_source_memory(m):
+    """ReduceScatter pushes by bulk copies (one per owner) from device inputs
+    whose blocks are whole 16-byte vectors (m = 1000 fp32), by st.async
+    otherwise and from host memory; the sums are the oracle's bits."""
+    n = 4
+    sends_np = inputs.normal(inputs.rng(97, m), n, n * m, "fp32")
+    want = oracle.reduce_scatter(sends_np, "fp32")
+    hs = _pinned(sends_np)
+    dev_host = rra.host_device_ptrs([t.data_ptr() for t in hs])
+    on_device = to_device(sends_np, "fp32")  # kept alive: the calls read it
+    with rra.Comm(n, n * m * 4) as comm:
+        for where, src in (("device", [t.data_ptr() for t in on_device]), ("host", dev_host)):
+            out = [torch.full((m,), float("nan"), device="cuda") for _ in range(n)]
+            comm.collective_ptrs("reduce_scatter", src, [t.data_ptr() for t in out], m, "fp32", 0)
+            torch.cuda.synchronize()
+            kind = comm.last_kernel()
+            bulk = where == "device" and m % 4 == 0
+            assert kind == ("coll_bulk_kernel<reduce_scatter>" if bulk else "coll_kernel<reduce_scatter>"), kind
+            for g, w in zip(out, want):
+                assert np.array_equal(bits(g.cpu().numpy()), bits(w))
+        assert comm.status()[0] == rra.OK
+
+
 def test_collective_outputs_in_host_memory_get_vector_stores():
     """Device inputs, outputs in pinned host memory: the push is by bulk
     copies, the outputs are written by vector stores (no bulk copy writes
