@@ -180,8 +180,9 @@ typedef enum {
                                       ReduceScatter, then every owner sends to the root):
                                       -1 (default) when nranks >= 3 and the message is at
                                       least 256 KiB, except a Broadcast that runs on bulk
-                                      copies both ways (see "The other collectives"), which
-                                      stays one hop; 0 never, 1 always; up to 16 ranks */
+                                      copies both ways and a Reduce on bulk copies (see
+                                      "The other collectives"), which stay one call of their
+                                      own shape; 0 never, 1 always; up to 16 ranks */
     RRA_ATTR_CLUSTER_TMA = 13      /* cluster one-/two-shot AllReduce (up to 16 ranks) with
                                       the push made by the TMA engine: bulk copies from a
                                       rank's input into the peers' shared memory (multicast
@@ -306,14 +307,20 @@ rra_status_t rra_allreduce_mapped(rra_comm_t comm, const void* const send[], voi
  * primitives serve these four.  Here all four run one thread-block cluster
  * of nranks CTAs per slice, CTA r acting for rank r, and exchange data
  * through distributed shared memory: a push is an st.async into a peer's
- * shared memory (AllGather and Broadcast up to 16 ranks: one TMA bulk copy
- * of the slice with cluster multicast) that completes the peer's mbarrier,
- * and the only wait is a bounded wait on one's own mbarrier (data arrival
- * is the signal).  AllGather and Broadcast on bulk copies also write their
- * outputs from shared memory by bulk copies (one per block, issued by one
- * thread) when every output is device memory of this GPU and count x
- * element size is a multiple of 16, so that no copy writes past its block;
- * otherwise every thread stores vectors.  Above
+ * shared memory that completes the peer's mbarrier, and the only wait is a
+ * bounded wait on one's own mbarrier (data arrival is the signal).  Up to 16
+ * ranks, when every input a call reads is device memory of this GPU, the
+ * pushes are TMA bulk copies straight from the inputs instead: AllGather and
+ * Broadcast one copy of the slice with cluster multicast into every CTA;
+ * ReduceScatter one copy per owner (only when count x element size is a
+ * multiple of 16, so that every block starts 16-byte aligned); Reduce one
+ * copy per partition owner, each owner then storing its rank-order sums of
+ * its partition into the root's output.  AllGather (blocks of 4 KiB and up)
+ * and Broadcast (256 KiB and up) on bulk copies also write their outputs
+ * from shared memory by bulk copies (one per block, issued by one thread)
+ * when every output is device memory of this GPU and count x element size
+ * is a multiple of 16, so that no copy writes past its block; otherwise
+ * every thread stores vectors.  Above
  * 16 ranks (the cluster limit) a cluster has 16 CTAs and CTA j acts for
  * ranks j, j + 16, j + 32, ...; pushes between ranks of one CTA are plain
  * shared-memory stores.  Nothing persists between calls.

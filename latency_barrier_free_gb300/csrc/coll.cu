@@ -376,6 +376,81 @@ __global__ void __launch_bounds__(256) coll_rs_bulk_kernel(const __grid_constant
     }
 }
 
+// Reduce up to 16 ranks with the push made by the TMA engine, in the
+// ReduceScatter pattern of the two-shot: a slice of S = N * Q vectors is
+// split into N partitions of Q, and thread q of CTA r copies partition q of
+// rank r's slice into slot [r] of CTA q's window (one bulk copy completing
+// CTA q's mbarrier; q = r is the own slot).  CTA q adds its N slots in rank
+// order and stores the sums straight into partition q of the root's output
+// (a push of the reduced partition to the root), so no CTA carries more than
+// its partition and there is no second exchange.  The input is one block at
+// send[r], so every copy starts on a 16-byte boundary; the host chooses this
+// kernel only when every input is device memory of this GPU.
+template <typename T>
+__global__ void __launch_bounds__(256) coll_reduce_bulk_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t r = cluster_ctarank();
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = S / N;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint64_t count = p.count;
+    // vectors of partition q of this slice
+    auto part_len = [&](uint32_t q) -> uint32_t { return npos > q * Q ? min(Q, npos - q * Q) : 0u; };
+    const uint32_t mine = part_len(r);
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, N * mine * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = p.drop_rank;
+    cluster_wait();  // every peer's barrier exists before any copy completes on it
+    {
+        const uint32_t q = threadIdx.x;
+        const uint32_t len = q < N ? part_len(q) : 0u;
+        if (len != 0 && (q == r || drop != (int32_t)r))
+            bulk_g2s_multicast(smem_u32(stage + r * Q),
+                               (const char*)p.send[r] + (uint64_t)(base + q * Q) * kVecBytes,
+                               len * (uint32_t)kVecBytes, my_bar, (uint16_t)(1u << q));
+    }
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)r, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
+    if (ok) {
+        void* const out = p.recv[p.root];
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * Q + u]);
+            store_block<T>(out, 0, base + r * Q + u, count, M::store(acc));
+        }
+    }
+    cluster_wait();  // every CTA's bytes are in: none of my copies is still in flight
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 // The same four collectives for nranks > 16 (clusters hold at most 16
 // CTAs): a cluster of G = 16 CTAs per slice, CTA j acting for ranks j,
 // j + G, j + 2G, ... (as the many-rank cluster AllReduce).  A push to a rank
@@ -720,18 +795,18 @@ static const void* coll_kernel_for(int op, bool multi) {
     return nullptr;
 }
 
-// ReduceScatter, AllGather and Broadcast up to 16 ranks have a bulk-copy
-// kernel (ReduceScatter only for blocks of whole 16-byte vectors).
+// ReduceScatter, AllGather, Broadcast and Reduce up to 16 ranks have a
+// bulk-copy kernel (ReduceScatter only for blocks of whole 16-byte vectors).
 bool coll_has_bulk(int op, int nranks) {
-    return (op == kCollReduceScatter || op == kCollAllGather || op == kCollBroadcast) &&
+    return (op == kCollReduceScatter || op == kCollAllGather || op == kCollBroadcast || op == kCollReduce) &&
            nranks <= kClusterMaxRanks;
 }
 
 const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
     static const char* const kBulk[] = {"coll_bulk_kernel<reduce_scatter>", "coll_bulk_kernel<all_gather>",
-                                        "coll_bulk_kernel<broadcast>"};
+                                        "coll_bulk_kernel<broadcast>", "coll_bulk_kernel<reduce>"};
     static const char* const kBulkStore[] = {"", "coll_bulk_kernel<all_gather, bulk store>",
-                                             "coll_bulk_kernel<broadcast, bulk store>"};
+                                             "coll_bulk_kernel<broadcast, bulk store>", ""};
     static const char* const kPlain[] = {"coll_kernel<reduce_scatter>", "coll_kernel<all_gather>",
                                          "coll_kernel<broadcast>", "coll_kernel<reduce>"};
     static const char* const kMulti[] = {"coll_multi_kernel<reduce_scatter>", "coll_multi_kernel<all_gather>",
@@ -746,6 +821,7 @@ const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
 template <typename T>
 static const void* coll_bulk_for(int op, bool store_bulk) {
     if (op == kCollReduceScatter) return (const void*)coll_rs_bulk_kernel<T>;
+    if (op == kCollReduce) return (const void*)coll_reduce_bulk_kernel<T>;
     if (store_bulk)
         return op == kCollAllGather ? (const void*)coll_bulk_kernel<T, kCollAllGather, true>
                                     : (const void*)coll_bulk_kernel<T, kCollBroadcast, true>;
@@ -815,15 +891,17 @@ size_t coll_stage_bytes(const Params& p, int op) {
 
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl,
                         bool bulk, bool store_bulk) {
-    const size_t smem = coll_stage_bytes(p, op);
+    // the bulk-copy Reduce holds N partitions of S / N vectors: S vectors
+    const size_t smem = bulk && op == kCollReduce ? (size_t)p.per_cta * kVecBytes : coll_stage_bytes(p, op);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kMaxRanks || p.root < 0 ||
         p.root >= p.nranks)
         return cudaErrorInvalidValue;
-    if ((op == kCollBroadcastSplit || op == kCollReduceSplit) && p.per_cta % (uint32_t)p.nranks != 0)
+    if ((op == kCollBroadcastSplit || op == kCollReduceSplit || (bulk && op == kCollReduce)) &&
+        p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
     const int cdim = coll_cdim(p.nranks);
     const uint64_t es = dtype == RRA_BF16 ? 2u : dtype == RRA_FP64 ? 8u : 4u;
-    if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || op == kCollReduceScatter ||
+    if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || op == kCollReduceScatter || op == kCollReduce ||
                        (p.count * es) % kVecBytes != 0))
         return cudaErrorInvalidValue;  // a bulk copy would write past its block
     if (bulk && op == kCollReduceScatter && (p.count * es) % kVecBytes != 0)

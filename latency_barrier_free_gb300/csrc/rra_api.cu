@@ -692,7 +692,9 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     p->chunk_vecs = p->nvec;
     p->epoch_slots = rra::kEpochSlots;
     p->root = root;
-    const bool split = op == rra::kCollBroadcastSplit || op == rra::kCollReduceSplit;
+    // the bulk-copy Reduce splits each slice into N partitions, as the split forms do
+    const bool bulk_reduce = bulk && op == rra::kCollReduce;
+    const bool split = op == rra::kCollBroadcastSplit || op == rra::kCollReduceSplit || bulk_reduce;
     // above 16 ranks a CTA hosts up to `hosted` ranks (16-CTA clusters)
     const size_t cdim = std::min<size_t>(n, rra::kClusterMaxRanks);
     const size_t hosted = ceil_div(n, cdim);
@@ -702,6 +704,7 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t smax;
     switch (op) {
         case rra::kCollBroadcast: smax = stage_vecs; break;
+        case rra::kCollReduce: smax = bulk_reduce ? stage_vecs / n * n : stage_vecs / n; break;  // S or N S vectors
         case rra::kCollBroadcastSplit: smax = stage_vecs * n / (n + 1) / n * n; break;  // (S/N + S) vectors
         case rra::kCollReduceSplit: smax = stage_vecs / 2 / n * n; break;              // 2 S vectors
         case rra::kCollReduceScatter: smax = stage_vecs / (hosted * n); break;          // N slots per hosted owner
@@ -711,18 +714,23 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t S;
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
-    } else if (store_bulk || (bulk && op == rra::kCollReduceScatter)) {
-        // Outputs (AllGather, Broadcast) or inputs (ReduceScatter) moved by
-        // bulk copies: the threads no longer move that data, so their count
-        // does not bound the slice.  Slices for about 8 clusters per SM's
-        // worth of CTAs, each window of N slots of S vectors (AllGather,
-        // ReduceScatter) at most 32 KiB and at least 512 bytes per slot, each
-        // Broadcast slice 4-32 KiB.  (Sweeps at N = 2, 4, 8, 16 and 1-64 MiB
-        // blocks put the best slice there.)
+    } else if (store_bulk || (bulk && (op == rra::kCollReduceScatter || op == rra::kCollReduce))) {
+        // Outputs (AllGather, Broadcast) or inputs (ReduceScatter, Reduce)
+        // moved by bulk copies: the threads no longer move that data, so
+        // their count does not bound the slice.  Slices for about 8 clusters
+        // per SM's worth of CTAs, each window of N slots of S vectors
+        // (AllGather, ReduceScatter) at most 32 KiB and at least 512 bytes per
+        // slot, each Broadcast slice 4-32 KiB, each Reduce slice (N
+        // partitions) at most 32 KiB and at least 512 bytes per partition.
+        // (Sweeps at N = 2, 4, 8, 16 and 1-64 MiB blocks put the best slice
+        // there.)
         const size_t target = std::max<size_t>(1, 8 * (size_t)c->sm_count / cdim);
         if (op == rra::kCollAllGather || op == rra::kCollReduceScatter) {
             const size_t window = std::max<size_t>(1, (32u << 10) / rra::kVecBytes / n);
             S = std::min<size_t>(window, std::max<size_t>(32, ceil_div(p->nvec, target)));
+        } else if (op == rra::kCollReduce) {  // N partitions of S / N vectors, S at most 32 KiB
+            S = std::min<size_t>(2048, std::max<size_t>(32 * n, ceil_div(p->nvec, target)));
+            S = std::min<size_t>(S, align_up(p->nvec, n));
         } else {
             S = std::min<size_t>(2048, std::max<size_t>(256, ceil_div(p->nvec, target)));
         }
@@ -1188,7 +1196,8 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
             const void* const* src = op == rra::kCollBroadcast ? send + root : send;
             bulk = bulk_sources_local(c, src, nsrc, (rs ? (size_t)c->nranks : 1u) * count * es);
             const size_t store_min = op == rra::kCollBroadcast ? (256u << 10) : (4u << 10);
-            if (bulk && !rs && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
+            const bool may_store = op == rra::kCollAllGather || op == rra::kCollBroadcast;
+            if (bulk && may_store && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
                 const void* out[RRA_MAX_RANKS];
                 for (int r = 0; r < c->nranks; ++r) out[r] = recv[r];
                 store_bulk = bulk_sources_local(c, out, c->nranks, blocks * count * es);
@@ -1200,8 +1209,10 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
         // hop (the root's slice reaches every CTA in one multicast copy); the
         // two-hop forms exist for up to 16 ranks
         if ((op == rra::kCollBroadcast || op == rra::kCollReduce) && c->nranks <= rra::kClusterMaxRanks) {
+            // (the bulk-copy Reduce is already spread over the cluster)
+            const bool one_hop_bulk = store_bulk || (bulk && op == rra::kCollReduce);
             const bool split = c->coll_split == 1 ||
-                               (c->coll_split < 0 && !store_bulk && c->nranks >= 3 && count * es >= (256u << 10));
+                               (c->coll_split < 0 && !one_hop_bulk && c->nranks >= 3 && count * es >= (256u << 10));
             if (split) {
                 op = op == rra::kCollBroadcast ? rra::kCollBroadcastSplit : rra::kCollReduceSplit;
                 bulk = store_bulk = false;

@@ -170,6 +170,36 @@ def test_reduce_scatter_chooses_its_push_by_source_memory(m):
         assert comm.status()[0] == rra.OK
 
 
+@pytest.mark.parametrize("m", [1000, 1001, 1024, 70001, 70000])
+def test_reduce_chooses_its_push_by_source_memory(m):
+    """Reduce pushes partition q of every rank's slice to CTA q by bulk
+    copies from device inputs (any count: each input starts aligned), the
+    owners storing their sums into the root's output; from host memory it
+    keeps the st.async kernels (two hops from 256 KiB).  The sums are the
+    oracle's bits."""
+    n, root = 4, 2
+    sends_np = inputs.normal(inputs.rng(98, m), n, m, "fp32")
+    want = oracle.reduce(sends_np, "fp32", root)
+    hs = _pinned(sends_np)
+    dev_host = rra.host_device_ptrs([t.data_ptr() for t in hs])
+    on_device = to_device(sends_np, "fp32")  # kept alive: the calls read it
+    with rra.Comm(n, m * 4) as comm:
+        for where, src in (("device", [t.data_ptr() for t in on_device]), ("host", dev_host)):
+            out = [torch.full((m,), float("nan"), device="cuda") for _ in range(n)]
+            comm.collective_ptrs("reduce", src, [t.data_ptr() for t in out], m, "fp32", root)
+            torch.cuda.synchronize()
+            kind = comm.last_kernel()
+            if where == "device":
+                assert kind == "coll_bulk_kernel<reduce>", kind
+            else:
+                assert kind == ("coll_split_kernel<reduce>" if m * 4 >= 262144 else "coll_kernel<reduce>"), kind
+            assert np.array_equal(bits(out[root].cpu().numpy()), bits(want[root]))
+            for r in range(n):  # only the root's output is written
+                if r != root:
+                    assert torch.isnan(out[r]).all()
+        assert comm.status()[0] == rra.OK
+
+
 def test_collective_outputs_in_host_memory_get_vector_stores():
     """Device inputs, outputs in pinned host memory: the push is by bulk
     copies, the outputs are written by vector stores (no bulk copy writes
