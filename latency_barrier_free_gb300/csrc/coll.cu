@@ -9,7 +9,8 @@
 // a push is an st.async into a peer's shared memory that completes the
 // peer's mbarrier, and the only wait is a bounded wait on one's own mbarrier
 // (data arrival is the signal, Sec. IV).  A CTA reads only its own rank's
-// input and writes only its own rank's output.
+// input and writes only its own rank's output -- except the bulk-copy
+// Reduce, whose partition owners push their sums into the root's output.
 //
 // Layout (v = 16-byte vector, S = slice of p.per_cta vectors, nv = p.nvec
 // vectors per block of `count` elements):
@@ -22,6 +23,9 @@
 //                  and writes its own output from registers.
 //   Reduce         every CTA but the root's pushes its slice to the root's
 //                  slot [r]; the root adds in rank order into recv[root].
+//                  With bulk copies: CTA r copies partition q of its slice
+//                  to CTA q's slot [r]; CTA q adds in rank order into
+//                  partition q of recv[root].
 // Blocks start at element q * count, which is not 16-byte aligned when count
 // is not a multiple of the elements per vector; such vectors are moved
 // element by element.
