@@ -135,7 +135,7 @@ typedef enum {
                                       step whose live ReduceScatter scratch over all windows
                                       is ~32 MiB, within the per-window scratch cap */
     RRA_ATTR_LL128_CHUNK = 4,      /* bytes per rank per LL128-atomic step; 0 = the step
-                                      whose live scratch over all windows is ~32 MiB (stays
+                                      whose live scratch over all windows is ~64 MiB (stays
                                       in L2), within the per-window scratch cap */
     RRA_ATTR_ONESHOT_CHUNK = 5,    /* bytes per rank per one-shot step, 0 = largest */
     RRA_ATTR_ONESHOT_WIDE = 6,     /* the one-shot's polls and the LL128-atomic kernel's adds

@@ -38,6 +38,12 @@ constexpr size_t kWindowAlign = 64ull << 10;
 // inputs and outputs stream through HBM (measured on GB300: a 64 MiB cap's
 // 16 MiB steps spilled scratch to DRAM, 2.3x the compulsory traffic).
 constexpr size_t kLiveScratch = 32ull << 20;
+// The LL128-atomic's step keeps about twice that live (accumulators, counters
+// and LL AllGather slots of all windows): its scratch is touched by atomics
+// and polls rather than streamed, and a 64 MiB step measured equal or faster
+// at N = 8..64 (N = 64, 256 KiB per rank: one step of 512 CTAs in 35 us
+// against two steps of 256 CTAs in 51 us).
+constexpr size_t kLiveScratchLL128 = 64ull << 20;
 
 size_t floor16(size_t x) { return x & ~(size_t)15; }
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
@@ -859,7 +865,7 @@ static rra_status_t plan_call(rra_comm* c, size_t count, rra_dtype_t dtype, rra_
             if (c->la_chunk > 0)
                 cap = std::min(cap, std::max<size_t>(1, (size_t)c->la_chunk / rra::kVecBytes / n));
             else  // live accumulators + LL AllGather slots: about 4 N^2 x part
-                cap = std::min(cap, std::max<size_t>(64, kLiveScratch / (4 * n * n) / rra::kVecBytes));
+                cap = std::min(cap, std::max<size_t>(64, kLiveScratchLL128 / (4 * n * n) / rra::kVecBytes));
             const size_t part = std::min(ceil_div(p->nvec, n), cap);
             const LaSizes s = la_sizes(L.la_part, c->nranks);
             p->chunk_vecs = (uint32_t)part;
