@@ -448,12 +448,13 @@ rra_status_t rra_comm_plan_kernel(rra_comm_t comm, size_t count, rra_dtype_t dty
  * host arithmetic).  The paper picks its kernel from measured crossovers in
  * message size and rank count (one-shot for small messages, two-shot once
  * they reach about a mebibyte at four ranks); these thresholds are the
- * crossovers measured on GB300 with CUDA-graph replay: up to 16 ranks (the
- * bulk-copy push, RRA_ATTR_CLUSTER_TMA) the cluster one-shot while
+ * crossovers measured on GB300 with CUDA-graph replay: with the bulk-copy
+ * push (RRA_ATTR_CLUSTER_TMA) the cluster one-shot, up to 16 ranks, while
  * nranks^2 * bytes <= 8 MiB at nranks <= 2, 2 MiB at nranks <= 4, 4 MiB at
- * nranks <= 8 and 8 MiB above; above 16 ranks (or with that attribute set to
- * 0 on a communicator, for that communicator's RRA_AUTO) while
- * min(nranks, 16) * nranks * bytes <= 1 MiB; the cluster two-shot above.
+ * nranks <= 8 and 8 MiB above, and above 16 ranks while 16 * nranks * bytes
+ * <= 16 MiB; with that attribute set to 0 on a communicator (for that
+ * communicator's RRA_AUTO) while min(nranks, 16) * nranks * bytes <= 1 MiB;
+ * the cluster two-shot above.
  * If the device cannot schedule the cluster shape, RRA_AUTO uses the choice
  * without cluster kernels: one-shot sentinel while nranks * bytes <= 1.5 MiB
  * (N <= 8); for N > 8 one-shot sentinel up to 4 KiB, LL128-atomic up to

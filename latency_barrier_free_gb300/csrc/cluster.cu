@@ -298,7 +298,16 @@ __global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant_
 // With kResidual (the fused AllReduce + residual add above 16 ranks), every
 // output is round(rank-order sum + that rank's residual), the residual added
 // to the running value as by the one-cluster fused kernel.
-template <typename T, bool kTwoShot, bool kResidual>
+//
+// With kBulk the pushes are TMA bulk copies straight from the hosted ranks'
+// inputs (device memory of this GPU, checked by the host): one-shot, thread
+// m copies hosted rank m's slice into its slot of every CTA with cluster
+// multicast; two-shot, thread (m, q) copies partition q of hosted rank m's
+// slice into its slot of CTA q.  Every slot then arrives by copy, the own
+// CTA's included, and a CTA leaves only after a cluster barrier that every
+// CTA reaches once its own incoming bytes are in, so that no copy it issued
+// is still in flight.
+template <typename T, bool kTwoShot, bool kResidual, bool kBulk>
 __device__ __forceinline__ void multi_body(const Params& p, const void* const* resid) {
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
@@ -319,12 +328,34 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
     if (threadIdx.x == 0) {
         mbar_init(my_bar, 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_expect_tx(my_bar, (N - hosted) * mine * (uint32_t)kVecBytes);
+        mbar_expect_tx(my_bar, (kBulk ? N : N - hosted) * mine * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
+    if (kBulk) {
+        cluster_wait();  // every peer's barrier exists before any copy completes on it
+        const uint32_t t = threadIdx.x;
+        if (kTwoShot) {
+            const uint32_t m = t / G;
+            const uint32_t q = t - m * G;
+            const uint32_t len = npos > q * Q ? min(Q, npos - q * Q) : 0u;
+            if (m < hosted && len != 0) {
+                const uint32_t rank = j + m * G;
+                if (q == j || drop != (int32_t)rank)
+                    bulk_g2s_multicast(smem_u32(stage + rank * Q),
+                                       (const char*)p.send[rank] + (uint64_t)(base + q * Q) * kVecBytes,
+                                       len * (uint32_t)kVecBytes, my_bar, (uint16_t)(1u << q));
+            }
+        } else if (t < hosted) {
+            const uint32_t rank = j + t * G;
+            const uint16_t all = (uint16_t)((1u << G) - 1u);
+            bulk_g2s_multicast(smem_u32(stage + rank * Q), (const char*)p.send[rank] + (uint64_t)base * kVecBytes,
+                               npos * (uint32_t)kVecBytes, my_bar,
+                               drop != (int32_t)rank ? all : (uint16_t)(1u << j));
+        }
+    }
     // item it = (hosted rank m, vector v)
     const uint32_t items = hosted * npos;
     uint4 x[kClusterBatch];
@@ -337,12 +368,14 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
             x[k] = load_input<T>(p.send[j + m * G], base + (it - m * npos), p.count);
         }
     };
-    load_batch(0);
-    cluster_wait();  // every peer's barrier exists before anyone stores into it
+    if (!kBulk) {
+        load_batch(0);
+        cluster_wait();  // every peer's barrier exists before anyone stores into it
+    }
 
     const uint32_t step = nt * (uint32_t)kClusterBatch;
 #pragma unroll 1
-    for (uint32_t b0 = 0; b0 < items; b0 += step) {
+    for (uint32_t b0 = 0; b0 < (kBulk ? 0u : items); b0 += step) {
         if (b0 != 0) load_batch(b0);
 #pragma unroll
         for (int k = 0; k < kClusterBatch; ++k) {
@@ -370,7 +403,7 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
             }
         }
     }
-    cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
+    if (!kBulk) cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
     int ok = 1;
     {
         Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)j, 0);
@@ -381,6 +414,7 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
             }
         }
     }
+    if (kBulk) cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
     __syncthreads();  // the hosted ranks' slots were written by other threads
     if (ok) {
 #pragma unroll 1
@@ -407,7 +441,8 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
             }
         }
     }
-    if (!__all_sync(0xffffffffu, ok)) cluster_wait();  // a thread whose wait ran out keeps the memory alive
+    if (kBulk) cluster_wait();  // every CTA's incoming bytes are in: none of my copies is still in flight
+    else if (!__all_sync(0xffffffffu, ok)) cluster_wait();  // a thread whose wait ran out keeps the memory alive
     if (p.timing != nullptr && threadIdx.x == 0) {
         const uint64_t t_end = globaltimer_ns();
         p.timing[2 * blockIdx.x] = t_start;
@@ -415,14 +450,14 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
     }
 }
 
-template <typename T, bool kTwoShot>
+template <typename T, bool kTwoShot, bool kBulk>
 __global__ void __launch_bounds__(256) cluster_multi_kernel(const __grid_constant__ Params p) {
-    multi_body<T, kTwoShot, false>(p, nullptr);
+    multi_body<T, kTwoShot, false, kBulk>(p, nullptr);
 }
 
 template <typename T, bool kTwoShot>
 __global__ void __launch_bounds__(256) residual_multi_kernel(const __grid_constant__ FusedParams f) {
-    multi_body<T, kTwoShot, true>(f.base, f.resid);
+    multi_body<T, kTwoShot, true, false>(f.base, f.resid);
 }
 
 // Persistent, double-buffered two-shot (the pages' double buffering, Sec. IV,
@@ -562,8 +597,10 @@ static const void* cluster_kernel_for(int mode) {
         case kClusterOneshot: return (const void*)cluster_kernel<T, false>;
         case kClusterTwoshot: return (const void*)cluster_kernel<T, true>;
         case kClusterTwoshotPipe: return (const void*)cluster_pipe_kernel<T>;
-        case kClusterOneshotMulti: return (const void*)cluster_multi_kernel<T, false>;
-        case kClusterTwoshotMulti: return (const void*)cluster_multi_kernel<T, true>;
+        case kClusterOneshotMulti: return (const void*)cluster_multi_kernel<T, false, false>;
+        case kClusterTwoshotMulti: return (const void*)cluster_multi_kernel<T, true, false>;
+        case kClusterOneshotMultiTma: return (const void*)cluster_multi_kernel<T, false, true>;
+        case kClusterTwoshotMultiTma: return (const void*)cluster_multi_kernel<T, true, true>;
         case kClusterOneshotMultiRes: return (const void*)residual_multi_kernel<T, false>;
         case kClusterTwoshotMultiRes: return (const void*)residual_multi_kernel<T, true>;
         case kClusterOneshotTma: return (const void*)cluster_tma_kernel<T, false>;
@@ -584,7 +621,7 @@ static const void* cluster_kernel_ptr(rra_dtype_t dtype, int mode) {
 // Opt the kernel in to the full stage and to clusters of up to 16 CTAs
 // (once per kernel; the attributes are process-wide).
 static cudaError_t configure(const void* k) {
-    static const void* done[32] = {};
+    static const void* done[64] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
@@ -608,8 +645,10 @@ size_t cluster_stage_bytes(const Params& p, int mode) {
         case kClusterTwoshotTma: return (size_t)p.per_cta / n * n * kVecBytes;
         case kClusterTwoshotPipe: return 2 * ((size_t)p.per_cta / n * n) * kVecBytes;
         case kClusterOneshotMulti:
+        case kClusterOneshotMultiTma:
         case kClusterOneshotMultiRes: return n * p.per_cta * kVecBytes;
         case kClusterTwoshotMulti:
+        case kClusterTwoshotMultiTma:
         case kClusterTwoshotMultiRes: return n * ((size_t)p.per_cta / kClusterMaxRanks) * kVecBytes;
     }
     return 0;
@@ -617,7 +656,7 @@ size_t cluster_stage_bytes(const Params& p, int mode) {
 
 static bool is_multi(int mode) {
     return mode == kClusterOneshotMulti || mode == kClusterTwoshotMulti || mode == kClusterOneshotMultiRes ||
-           mode == kClusterTwoshotMultiRes;
+           mode == kClusterTwoshotMultiRes || mode == kClusterOneshotMultiTma || mode == kClusterTwoshotMultiTma;
 }
 
 // CTAs per cluster: one per rank, or 16 hosting several ranks each.
@@ -639,9 +678,15 @@ static cudaError_t launch_cluster_args(const Params& p, void* arg, rra_dtype_t d
         return cudaErrorInvalidValue;
     if ((mode == kClusterTwoshotTma || mode == kClusterOneshotTma) && threads < p.nranks)
         return cudaErrorInvalidValue;  // the two-shot's copies are issued by threads 0..N-1
-    if ((mode == kClusterTwoshotMulti || mode == kClusterTwoshotMultiRes) &&
+    if ((mode == kClusterTwoshotMulti || mode == kClusterTwoshotMultiRes || mode == kClusterTwoshotMultiTma) &&
         p.per_cta % (uint32_t)kClusterMaxRanks != 0)
         return cudaErrorInvalidValue;
+    {   // the many-rank bulk copies are issued by threads 0 .. hosted x (16 or 1) - 1
+        const int hosted = (p.nranks + kClusterMaxRanks - 1) / kClusterMaxRanks;
+        if ((mode == kClusterTwoshotMultiTma && threads < hosted * kClusterMaxRanks) ||
+            (mode == kClusterOneshotMultiTma && threads < hosted))
+            return cudaErrorInvalidValue;
+    }
     if (mode == kClusterTwoshotPipe && p.per_cta > (uint32_t)threads * kClusterBatch) return cudaErrorInvalidValue;
     const void* k = cluster_kernel_ptr(dtype, mode);
     if (k == nullptr) return cudaErrorInvalidValue;

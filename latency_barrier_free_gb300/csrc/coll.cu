@@ -857,7 +857,7 @@ static int coll_cdim(int nranks) { return nranks < kClusterMaxRanks ? nranks : k
 // Opt a kernel in to the full stage and to clusters of up to 16 CTAs (once
 // per kernel; the attributes are process-wide).
 static cudaError_t configure_coll(const void* k) {
-    static const void* done[40] = {};
+    static const void* done[64] = {};
     for (const void* d : done)
         if (d == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);

@@ -21,7 +21,7 @@
 namespace rra {
 namespace placement {
 
-constexpr int kMaxRanks = 16;      // ranks one bulk-copy kernel serves
+constexpr int kMaxRanks = 64;      // ranks a bulk-copy kernel serves
 constexpr size_t kVecBytes = 16;   // bulk copies move whole 16-byte vectors
 
 // Source sets that passed the check, matched afterwards by address alone;

@@ -22,7 +22,7 @@
 #include "rra_internal.h"
 #include "placement.h"
 
-static_assert(rra::placement::kMaxRanks == rra::kClusterMaxRanks, "bulk-copy kernels serve up to 16 ranks");
+static_assert(rra::placement::kMaxRanks == RRA_MAX_RANKS, "bulk-copy kernels serve every rank count");
 static_assert(rra::placement::kVecBytes == (size_t)rra::kVecBytes, "one transfer vector");
 
 using rra::Ctrl;
@@ -114,7 +114,8 @@ struct rra_comm {
     int64_t cluster_tma = -1;               // cluster one-/two-shot push by bulk copies: -1 auto (default), 0, 1
     int64_t host_zero_copy = 1;             // rra_allreduce_host: run on mapped pinned buffers directly
     int cluster_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // [two-shot][dtype]: -1 not queried
-    int cluster_multi_fits[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // the same for N > 16
+    int cluster_multi_fits[2][2][3] = {{{-1, -1, -1}, {-1, -1, -1}}, {{-1, -1, -1}, {-1, -1, -1}}};
+                                            // the same for N > 16: [bulk-copy push][two-shot][dtype]
     std::map<uint64_t, int> cluster_waves;  // (dtype, threads, stage bytes) -> clusters resident at once
     int coll_fits[2][6][3] = {{{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}},
                               {{-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}, {-1, -1, -1}}};
@@ -242,10 +243,11 @@ static rra_algo_t select_global(int nranks, size_t bytes) {
 }
 
 // The cluster one-shot / two-shot crossover, measured on GB300 with CUDA-graph
-// replay (N = 2..64).  With the bulk-copy push (N <= 16) the one-shot while
-// N^2 M <= 8 MiB at N <= 2, 2 MiB at N <= 4, 4 MiB at N <= 8, 8 MiB above;
-// with st.async pushes (N > 16, or the bulk-copy push off) while
-// min(N, 16) N M <= 1 MiB.
+// replay (N = 2..64).  With the bulk-copy push, up to 16 ranks the one-shot
+// while N^2 M <= 8 MiB at N <= 2, 2 MiB at N <= 4, 4 MiB at N <= 8, 8 MiB
+// above, and above 16 ranks while 16 N M <= 16 MiB (N = 20, 32, 64: the
+// one-shot faster up to 16 KiB per rank, the two-shot from 64 KiB); with
+// st.async pushes (the bulk-copy push off) while min(N, 16) N M <= 1 MiB.
 static rra_algo_t select_cluster(int nranks, size_t bytes, bool bulk_copy) {
     const size_t n = (size_t)nranks;
     if (nranks <= rra::kClusterMaxRanks && bulk_copy) {
@@ -253,14 +255,15 @@ static rra_algo_t select_cluster(int nranks, size_t bytes, bool bulk_copy) {
         return n * n * bytes <= limit ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
     }
     const size_t g = std::min<size_t>(n, rra::kClusterMaxRanks);
-    return g * n * bytes <= (1ull << 20) ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
+    const size_t limit = bulk_copy ? (16ull << 20) : (1ull << 20);
+    return g * n * bytes <= limit ? RRA_ONESHOT_CLUSTER : RRA_TWOSHOT_CLUSTER;
 }
 
-// Whether a cluster call (N <= 16) pushes by bulk copies: unless the
-// attribute turns it off (it measured faster at every N = 2..16 and every
-// size from 128 B to 64 MiB on GB300).
+// Whether a cluster call pushes by bulk copies: unless the attribute turns
+// it off (it measured faster at every N = 2..16 and every size from 128 B
+// to 64 MiB on GB300, and above 16 ranks as well).
 static bool bulk_copy_push(const rra_comm* c) {
-    return c->nranks <= rra::kClusterMaxRanks && c->cluster_tma != 0;
+    return c->cluster_tma != 0;
 }
 
 rra_status_t rra_select_algo(int nranks, size_t bytes, rra_dtype_t dtype, rra_algo_t* out) {
@@ -525,11 +528,12 @@ rra_status_t rra_comm_get_attr(rra_comm_t c, rra_attr_t attr, int64_t* v) {
 // multiple of 16) within the 96 KiB stage.  S: the whole message while it
 // fits one slice (one-shot) or, for the two-shot, about two CTAs per SM.
 static rra_status_t plan_cluster_multi(rra_comm* c, size_t count, rra_dtype_t dtype, bool two, Params* p,
-                                       int* threads, int* mode) {
+                                       int* threads, int* mode, bool bulk) {
     const size_t n = (size_t)c->nranks;
     const size_t g = (size_t)rra::kClusterMaxRanks;
-    const int kmode = two ? rra::kClusterTwoshotMulti : rra::kClusterOneshotMulti;
-    int& fits = c->cluster_multi_fits[two ? 1 : 0][(int)dtype];
+    const int kmode = bulk ? (two ? rra::kClusterTwoshotMultiTma : rra::kClusterOneshotMultiTma)
+                           : (two ? rra::kClusterTwoshotMulti : rra::kClusterOneshotMulti);
+    int& fits = c->cluster_multi_fits[bulk ? 1 : 0][two ? 1 : 0][(int)dtype];
     if (fits < 0) fits = rra::cluster_max_active(dtype, kmode, c->nranks, 256, rra::kClusterStageBytes) > 0 ? 1 : 0;
     if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
     const size_t ve = rra::kVecBytes / elem_size(dtype);
@@ -590,7 +594,8 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
                                  int* threads, int* mode, bool host, bool local) {
     const bool two = algo == RRA_TWOSHOT_CLUSTER;
     const size_t n = (size_t)c->nranks;
-    if (c->nranks > rra::kClusterMaxRanks) return plan_cluster_multi(c, count, dtype, two, p, threads, mode);
+    if (c->nranks > rra::kClusterMaxRanks)
+        return plan_cluster_multi(c, count, dtype, two, p, threads, mode, bulk_copy_push(c) && local && !host);
     int& fits = c->cluster_fits[two ? 1 : 0][(int)dtype];
     if (fits < 0)
         fits = rra::cluster_max_active(dtype, two ? rra::kClusterTwoshot : rra::kClusterOneshot, c->nranks, 256,
@@ -968,6 +973,8 @@ static const char* kernel_name(bool cluster, int kind) {
             case rra::kClusterTwoshotPipe: return "cluster_pipe_kernel";
             case rra::kClusterOneshotMulti: return "cluster_multi_kernel<one-shot>";
             case rra::kClusterTwoshotMulti: return "cluster_multi_kernel<two-shot>";
+            case rra::kClusterOneshotMultiTma: return "cluster_multi_kernel<one-shot, bulk>";
+            case rra::kClusterTwoshotMultiTma: return "cluster_multi_kernel<two-shot, bulk>";
             case rra::kClusterOneshotTma: return "cluster_tma_kernel<one-shot>";
             case rra::kClusterTwoshotTma: return "cluster_tma_kernel<two-shot>";
         }
@@ -1290,13 +1297,13 @@ static rra_status_t plan_residual(rra_comm* c, size_t count, rra_dtype_t dtype, 
         if (fits == 0) return RRA_ERR_NOT_CORESIDENT;
         memset(f, 0, sizeof(*f));
         int mode = 0;
-        rra_status_t st = plan_cluster_multi(c, count, dtype, two, &f->base, threads, &mode);
+        rra_status_t st = plan_cluster_multi(c, count, dtype, two, &f->base, threads, &mode, false);
         if (st != RRA_OK) return st;
         *two_shot = two;
         return RRA_OK;
     }
     // shape and push as the cluster AllReduce would take them
-    const bool bulk = bulk_copy_push(c) && local;
+    const bool bulk = bulk_copy_push(c) && local && c->nranks <= rra::kClusterMaxRanks;
     const bool two = select_cluster(c->nranks, count * es, bulk) == RRA_TWOSHOT_CLUSTER;
     int& fits = c->residual_fits[bulk ? 1 : 0][two ? 1 : 0][(int)dtype];
     if (fits < 0)

@@ -113,10 +113,11 @@ cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_
 // The ...MultiRes modes are the same kernels with the residual add of
 // rra_allreduce_residual in their epilogue (launch_cluster_residual only).
 // kClusterOneshotTma / kClusterTwoshotTma: kClusterOneshot / kClusterTwoshot
-// with the push made by bulk copies (RRA_ATTR_CLUSTER_TMA).
+// with the push made by bulk copies (RRA_ATTR_CLUSTER_TMA); the ...MultiTma
+// modes the same for more than 16 ranks.
 enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2, kClusterOneshotMulti = 3,
        kClusterTwoshotMulti = 4, kClusterOneshotMultiRes = 5, kClusterTwoshotMultiRes = 6,
-       kClusterOneshotTma = 7, kClusterTwoshotTma = 8 };
+       kClusterOneshotTma = 7, kClusterTwoshotTma = 8, kClusterOneshotMultiTma = 9, kClusterTwoshotMultiTma = 10 };
 size_t cluster_stage_bytes(const Params& p, int mode);
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl);
 int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem);

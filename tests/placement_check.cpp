@@ -89,12 +89,12 @@ int main() {
         check(!q(c, false, dev4, 0, 64), "no ranks");
         check(!q(c, false, dev4, 4, 0), "no bytes");
         check(!q(c, false, nullptr, 4, 64), "no source array");
-        const void* many[17];
-        for (int r = 0; r < 17; ++r) many[r] = dev4[r % 4];
-        check(!q(c, false, many, 17, 64), "more ranks than a bulk-copy kernel serves");
+        const void* many[65];
+        for (int r = 0; r < 65; ++r) many[r] = dev4[r % 4];
+        check(!q(c, false, many, 65, 64), "more ranks than a bulk-copy kernel serves");
         check(map.queries == 0, "none of these queried the map");
-        check(q(c, false, many, 16, 64), "sixteen ranks");
-        check(!q(c, true, many, 16, 64), "another GPU in use outranks a remembered set");
+        check(q(c, false, many, 64, 64), "sixty-four ranks");
+        check(!q(c, true, many, 64, 64), "another GPU in use outranks a remembered set");
     }
     {   // the cache holds the last 8 sets
         SourceCache c;

@@ -122,13 +122,15 @@ def test_auto_selection_by_size_and_ranks():
     assert rra.select_algo(8, (64 << 10) + 16, "bf16") == "twoshot_cluster"
     assert rra.select_algo(16, 32 << 10) == "oneshot_cluster"  # 8 MiB
     assert rra.select_algo(16, 64 << 10) == "twoshot_cluster"
-    # above 16 ranks: 16-CTA clusters hosting several ranks each; min(N, 16) N M <= 1 MiB
+    # above 16 ranks: 16-CTA clusters hosting several ranks each; with the
+    # bulk-copy push the one-shot while 16 N M <= 16 MiB
     assert rra.select_algo(17, 1 << 10) == "oneshot_cluster"
-    assert rra.select_algo(64, 1 << 10) == "oneshot_cluster"
-    assert rra.select_algo(64, (1 << 10) + 16) == "twoshot_cluster"
-    assert rra.select_algo(32, 2 << 10) == "oneshot_cluster"
+    assert rra.select_algo(64, 16 << 10) == "oneshot_cluster"
+    assert rra.select_algo(64, (16 << 10) + 16) == "twoshot_cluster"
+    assert rra.select_algo(32, 32 << 10) == "oneshot_cluster"
+    assert rra.select_algo(32, (32 << 10) + 16) == "twoshot_cluster"
+    assert rra.select_algo(20, 48 << 10) == "oneshot_cluster"
     assert rra.select_algo(64, 64 << 10) == "twoshot_cluster"
-    assert rra.select_algo(32, 16 << 10) == "twoshot_cluster"
     assert rra.select_algo(64, 1 << 20) == "twoshot_cluster"
     twoshot = ("twoshot_cluster", "twoshot_direct")
     for n in (2, 4, 8, 16, 17, 64):  # once two-shot, always two-shot as the message grows

@@ -91,6 +91,37 @@ def test_mapped_host_pointers_on_the_device_entry_get_st_async():
         check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
 
 
+@pytest.mark.parametrize("n", [20, 64])
+@pytest.mark.parametrize("algo,count", [("oneshot_cluster", 40), ("twoshot_cluster", 30001), ("auto", 64)])
+def test_many_ranks_choose_their_push_by_source_memory(n, algo, count):
+    """Above 16 ranks (16-CTA clusters, each CTA hosting several ranks):
+    device inputs take the bulk copies, pinned host buffers and the
+    attribute switched off the st.async pushes; every result exact."""
+    sends_np = inputs.normal(inputs.rng(99, n, count), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.status()[0] == rra.OK
+        kind = comm.last_kernel()
+        assert kind.startswith("cluster_multi_kernel<") and kind.endswith(", bulk>"), kind
+        assert kind == comm.plan_kernel(count, "fp32", algo)
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
+        hs = _pinned(sends_np)
+        hr = [torch.full((count,), float("nan")).pin_memory() for _ in range(n)]
+        comm.allreduce_host([t.data_ptr() for t in hs], [t.data_ptr() for t in hr], count, "fp32", algo)
+        assert comm.last_kernel() == kind[:-len(", bulk>")] + ">", comm.last_kernel()
+        check_against_oracle(sends_np, [t.numpy() for t in hr], "fp32", "oneshot_cluster")
+        comm.set_attr("cluster_tma", 0)
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert comm.last_kernel() == kind[:-len(", bulk>")] + ">", comm.last_kernel()
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", "oneshot_cluster")
+        assert comm.status()[0] == rra.OK
+
+
 def test_bulk_copy_attribute_off():
     n, count = 4, 32
     sends_np = inputs.normal(inputs.rng(93, 0), n, count, "fp32")

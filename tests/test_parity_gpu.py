@@ -319,12 +319,13 @@ def test_cluster_kernels(n, dtype, algo):
 
 @pytest.mark.parametrize("algo", CLUSTER)
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
-@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 17, 32, 64])
 def test_cluster_kernels_bulk_copy_push(n, dtype, algo):
     """The cluster kernels with the push made by TMA bulk copies
-    (RRA_ATTR_CLUSTER_TMA): bit-exact for ragged sizes (a last vector only
-    partly inside the input; empty two-shot partitions), several slice
-    sizes, and in place."""
+    (RRA_ATTR_CLUSTER_TMA; above 16 ranks one copy per hosted rank and
+    owner): bit-exact for ragged sizes (a last vector only partly inside
+    the input; empty two-shot partitions), several slice sizes, and in
+    place."""
     with rra.Comm(n, 300000 * ELEM[dtype]) as comm:
         comm.set_attr("cluster_tma", 1)
         for count in (1, 7, 33, 4097, 70001, 300000):

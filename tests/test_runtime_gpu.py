@@ -274,6 +274,9 @@ def test_plan_kernel_names_the_launched_kernel():
         assert comm.plan_kernel(256, "fp32", "ll128_atomic") == "ll128_wide_kernel"
         assert comm.plan_kernel(256, "fp32", "oneshot_ll") == "oneshot_wide_kernel<LL>"
     with rra.Comm(32, 1 << 16) as comm:
+        assert comm.plan_kernel(256, "fp32", "auto") == "cluster_multi_kernel<one-shot, bulk>"
+        assert comm.plan_kernel(1 << 14, "fp32", "auto") == "cluster_multi_kernel<two-shot, bulk>"  # 16 N M = 32 MiB
+        comm.set_attr("cluster_tma", 0)
         assert comm.plan_kernel(256, "fp32", "auto") == "cluster_multi_kernel<one-shot>"
         assert comm.plan_kernel(1 << 14, "fp32", "auto") == "cluster_multi_kernel<two-shot>"
 
