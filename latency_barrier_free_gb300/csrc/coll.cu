@@ -462,7 +462,13 @@ __global__ void __launch_bounds__(256) coll_reduce_bulk_kernel(const __grid_cons
 // st.async that completes that CTA's mbarrier, which expects the bytes of
 // every rank it does not host.  Slots are indexed by rank as above; a
 // ReduceScatter CTA keeps one set of N slots per hosted owner.
-template <typename T, int kOp>
+// kBulk: every push is a TMA bulk copy from the input (device memory of this
+// GPU, checked by the host), the own CTA's slots included: ReduceScatter one
+// copy per hosted rank and owner (blocks of whole 16-byte vectors only),
+// AllGather one multicast copy per hosted rank, Broadcast one from the root's
+// CTA, Reduce one per hosted rank to the root's CTA.  Each CTA then writes
+// from its window, the root's CTA of a Broadcast included.
+template <typename T, int kOp, bool kBulk>
 __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__ Params p) {
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
@@ -488,6 +494,14 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
         case kCollAllGather: incoming = (N - hosted) * npos; items = hosted * npos; break;
         case kCollBroadcast: incoming = root_here ? 0u : npos; items = root_here ? npos : 0u; break;
         case kCollReduce: incoming = root_here ? (N - hosted) * npos : 0u; items = hosted * npos; break;
+    }
+    if (kBulk) {  // every slot arrives by copy, the own CTA's included
+        switch (kOp) {
+            case kCollReduceScatter: incoming = hosted * N * npos; break;
+            case kCollAllGather: incoming = N * npos; break;
+            case kCollBroadcast: incoming = npos; break;
+            case kCollReduce: incoming = root_here ? N * npos : 0u; break;
+        }
     }
     const uint32_t my_bar = smem_u32(&bar);
     if (threadIdx.x == 0) {
@@ -517,12 +531,47 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
             }
         }
     };
-    load_batch(0);
-    cluster_wait();  // every peer's barrier exists before anyone stores into it
+    if (kBulk) {
+        cluster_wait();  // every peer's barrier exists before any copy completes on it
+        const uint16_t all = (uint16_t)((1u << G) - 1u);
+        const uint32_t vbytes = npos * (uint32_t)kVecBytes;
+        const uint32_t ncopies = kOp == kCollReduceScatter ? hosted * N
+                                 : kOp == kCollBroadcast   ? (root_here ? 1u : 0u)
+                                                           : hosted;
+#pragma unroll 1
+        for (uint32_t c = threadIdx.x; c < ncopies; c += nt) {
+            if (kOp == kCollReduceScatter) {  // block q's slice of hosted rank m to owner q's CTA
+                const uint32_t m = c / N;
+                const uint32_t q = c - m * N;
+                const uint32_t rank = j + m * G;
+                const uint32_t dst = q % G;
+                if (dst == j || drop != (int32_t)rank)
+                    bulk_g2s_multicast(smem_u32(stage + ((q / G) * N + rank) * S),
+                                       (const char*)p.send[rank] + q * count * sizeof(T) + (uint64_t)base * kVecBytes,
+                                       vbytes, my_bar, (uint16_t)(1u << dst));
+            } else if (kOp == kCollAllGather) {  // hosted rank c's slice into its slot of every CTA
+                const uint32_t rank = j + c * G;
+                bulk_g2s_multicast(smem_u32(stage + rank * S), (const char*)p.send[rank] + (uint64_t)base * kVecBytes,
+                                   vbytes, my_bar, drop != (int32_t)rank ? all : (uint16_t)(1u << j));
+            } else if (kOp == kCollBroadcast) {  // the root's slice into slot [0] of every CTA
+                bulk_g2s_multicast(smem_u32(stage), (const char*)p.send[root] + (uint64_t)base * kVecBytes, vbytes,
+                                   my_bar, drop != (int32_t)root ? all : (uint16_t)(1u << j));
+            } else {  // Reduce: hosted rank c's slice into its slot of the root's CTA
+                const uint32_t rank = j + c * G;
+                if (root_here || drop != (int32_t)rank)
+                    bulk_g2s_multicast(smem_u32(stage + rank * S),
+                                       (const char*)p.send[rank] + (uint64_t)base * kVecBytes, vbytes, my_bar,
+                                       (uint16_t)(1u << root_cta));
+            }
+        }
+    } else {
+        load_batch(0);
+        cluster_wait();  // every peer's barrier exists before anyone stores into it
+    }
 
     const uint32_t step = nt * (uint32_t)kClusterBatch;
 #pragma unroll 1
-    for (uint32_t b0 = 0; b0 < items; b0 += step) {
+    for (uint32_t b0 = 0; b0 < (kBulk ? 0u : items); b0 += step) {
         if (b0 != 0) load_batch(b0);
 #pragma unroll
         for (int k = 0; k < kClusterBatch; ++k) {
@@ -568,7 +617,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
             }
         }
     }
-    cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
+    if (!kBulk) cluster_arrive_relaxed();  // "my pushes are issued" (orders no data)
 
     int ok = 1;
     {
@@ -580,6 +629,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
             }
         }
     }
+    if (kBulk) cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
     __syncthreads();  // slots of hosted ranks written by other threads of this CTA
     if (ok) {
         if (kOp == kCollReduceScatter) {
@@ -612,7 +662,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
                 const uint32_t u = v - q * npos;
                 store_block<T>(p.recv[j + m * G], (uint64_t)q * count, base + u, count, stage[q * S + u]);
             }
-        } else if (!root_here) {  // Broadcast
+        } else if (kBulk || !root_here) {  // Broadcast (the root's CTA wrote its outputs unless kBulk)
 #pragma unroll 1
             for (uint32_t it = threadIdx.x; it < hosted * npos; it += nt) {
                 const uint32_t m = it / npos;
@@ -777,17 +827,20 @@ __global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__
     }
 }
 
-template <typename T>
-static const void* coll_kernel_for(int op, bool multi) {
-    if (multi) {
-        switch (op) {
-            case kCollReduceScatter: return (const void*)coll_multi_kernel<T, kCollReduceScatter>;
-            case kCollAllGather: return (const void*)coll_multi_kernel<T, kCollAllGather>;
-            case kCollBroadcast: return (const void*)coll_multi_kernel<T, kCollBroadcast>;
-            case kCollReduce: return (const void*)coll_multi_kernel<T, kCollReduce>;
-        }
-        return nullptr;
+template <typename T, bool kBulk>
+static const void* coll_multi_for(int op) {
+    switch (op) {
+        case kCollReduceScatter: return (const void*)coll_multi_kernel<T, kCollReduceScatter, kBulk>;
+        case kCollAllGather: return (const void*)coll_multi_kernel<T, kCollAllGather, kBulk>;
+        case kCollBroadcast: return (const void*)coll_multi_kernel<T, kCollBroadcast, kBulk>;
+        case kCollReduce: return (const void*)coll_multi_kernel<T, kCollReduce, kBulk>;
     }
+    return nullptr;
+}
+
+template <typename T>
+static const void* coll_kernel_for(int op, bool multi, bool bulk = false) {
+    if (multi) return bulk ? coll_multi_for<T, true>(op) : coll_multi_for<T, false>(op);
     switch (op) {
         case kCollReduceScatter: return (const void*)coll_kernel<T, kCollReduceScatter>;
         case kCollAllGather: return (const void*)coll_kernel<T, kCollAllGather>;
@@ -799,11 +852,12 @@ static const void* coll_kernel_for(int op, bool multi) {
     return nullptr;
 }
 
-// ReduceScatter, AllGather, Broadcast and Reduce up to 16 ranks have a
-// bulk-copy kernel (ReduceScatter only for blocks of whole 16-byte vectors).
+// ReduceScatter, AllGather, Broadcast and Reduce have bulk-copy kernels at
+// every rank count (ReduceScatter only for blocks of whole 16-byte vectors);
+// the bulk stores of AllGather and Broadcast exist up to 16 ranks.
 bool coll_has_bulk(int op, int nranks) {
     return (op == kCollReduceScatter || op == kCollAllGather || op == kCollBroadcast || op == kCollReduce) &&
-           nranks <= kClusterMaxRanks;
+           nranks >= 2 && nranks <= kMaxRanks;
 }
 
 const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
@@ -818,6 +872,9 @@ const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
     if (op < 0 || op > kCollReduceSplit) return "unknown";
     if (op == kCollBroadcastSplit) return "coll_split_kernel<broadcast>";
     if (op == kCollReduceSplit) return "coll_split_kernel<reduce>";
+    static const char* const kMultiBulk[] = {"coll_multi_kernel<reduce_scatter, bulk>", "coll_multi_kernel<all_gather, bulk>",
+                                             "coll_multi_kernel<broadcast, bulk>", "coll_multi_kernel<reduce, bulk>"};
+    if (bulk && coll_has_bulk(op, nranks) && nranks > kClusterMaxRanks) return kMultiBulk[op];
     if (bulk && coll_has_bulk(op, nranks)) return store_bulk ? kBulkStore[op] : kBulk[op];
     return nranks > kClusterMaxRanks ? kMulti[op] : kPlain[op];
 }
@@ -835,6 +892,14 @@ static const void* coll_bulk_for(int op, bool store_bulk) {
 
 static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks, bool bulk, bool store_bulk = false) {
     const bool multi = nranks > kClusterMaxRanks;
+    if (bulk && multi && coll_has_bulk(op, nranks)) {
+        switch (dtype) {
+            case RRA_FP32: return coll_kernel_for<float>(op, true, true);
+            case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op, true, true);
+            case RRA_FP64: return coll_kernel_for<double>(op, true, true);
+        }
+        return nullptr;
+    }
     if (bulk && coll_has_bulk(op, nranks)) {
         switch (dtype) {
             case RRA_FP32: return coll_bulk_for<float>(op, store_bulk);
@@ -896,17 +961,18 @@ size_t coll_stage_bytes(const Params& p, int op) {
 cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads, cudaStream_t stream, bool pdl,
                         bool bulk, bool store_bulk) {
     // the bulk-copy Reduce holds N partitions of S / N vectors: S vectors
-    const size_t smem = bulk && op == kCollReduce ? (size_t)p.per_cta * kVecBytes : coll_stage_bytes(p, op);
+    const bool part_reduce = bulk && op == kCollReduce && p.nranks <= kClusterMaxRanks;  // coll_reduce_bulk_kernel
+    const size_t smem = part_reduce ? (size_t)p.per_cta * kVecBytes : coll_stage_bytes(p, op);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kMaxRanks || p.root < 0 ||
         p.root >= p.nranks)
         return cudaErrorInvalidValue;
-    if ((op == kCollBroadcastSplit || op == kCollReduceSplit || (bulk && op == kCollReduce)) &&
+    if ((op == kCollBroadcastSplit || op == kCollReduceSplit || part_reduce) &&
         p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
     const int cdim = coll_cdim(p.nranks);
     const uint64_t es = dtype == RRA_BF16 ? 2u : dtype == RRA_FP64 ? 8u : 4u;
     if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || op == kCollReduceScatter || op == kCollReduce ||
-                       (p.count * es) % kVecBytes != 0))
+                       p.nranks > kClusterMaxRanks || (p.count * es) % kVecBytes != 0))
         return cudaErrorInvalidValue;  // a bulk copy would write past its block
     if (bulk && op == kCollReduceScatter && (p.count * es) % kVecBytes != 0)
         return cudaErrorInvalidValue;  // a block would start off a 16-byte boundary

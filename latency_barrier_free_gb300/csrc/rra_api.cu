@@ -703,8 +703,10 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     p->chunk_vecs = p->nvec;
     p->epoch_slots = rra::kEpochSlots;
     p->root = root;
-    // the bulk-copy Reduce splits each slice into N partitions, as the split forms do
-    const bool bulk_reduce = bulk && op == rra::kCollReduce;
+    // the bulk-copy Reduce up to 16 ranks splits each slice into N partitions,
+    // as the split forms do (above 16 ranks it sends whole slices to the root)
+    const bool many = c->nranks > rra::kClusterMaxRanks;
+    const bool bulk_reduce = bulk && op == rra::kCollReduce && !many;
     const bool split = op == rra::kCollBroadcastSplit || op == rra::kCollReduceSplit || bulk_reduce;
     // above 16 ranks a CTA hosts up to `hosted` ranks (16-CTA clusters)
     const size_t cdim = std::min<size_t>(n, rra::kClusterMaxRanks);
@@ -725,7 +727,7 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t S;
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
-    } else if (store_bulk || (bulk && (op == rra::kCollReduceScatter || op == rra::kCollReduce))) {
+    } else if (!many && (store_bulk || (bulk && (op == rra::kCollReduceScatter || op == rra::kCollReduce)))) {
         // Outputs (AllGather, Broadcast) or inputs (ReduceScatter, Reduce)
         // moved by bulk copies: the threads no longer move that data, so
         // their count does not bound the slice.  Slices for about 8 clusters
@@ -1210,7 +1212,8 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
             bulk = bulk_sources_local(c, src, nsrc, (rs ? (size_t)c->nranks : 1u) * count * es);
             const size_t store_min = op == rra::kCollBroadcast ? (256u << 10) : (4u << 10);
             const bool may_store = op == rra::kCollAllGather || op == rra::kCollBroadcast;
-            if (bulk && may_store && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
+            if (bulk && may_store && c->nranks <= rra::kClusterMaxRanks && (count * es) % rra::kVecBytes == 0 &&
+                count * es >= store_min) {
                 const void* out[RRA_MAX_RANKS];
                 for (int r = 0; r < c->nranks; ++r) out[r] = recv[r];
                 store_bulk = bulk_sources_local(c, out, c->nranks, blocks * count * es);

@@ -231,6 +231,37 @@ def test_reduce_chooses_its_push_by_source_memory(m):
         assert comm.status()[0] == rra.OK
 
 
+@pytest.mark.parametrize("n", [20, 64])
+@pytest.mark.parametrize("m", [1000, 1001])
+def test_many_rank_collectives_choose_their_push(n, m):
+    """Above 16 ranks all four collectives push by bulk copies from device
+    inputs (ReduceScatter only for blocks of whole 16-byte vectors), by
+    st.async with the attribute off; the results are the oracle's bits."""
+    root = n - 3
+    rs_np = inputs.normal(inputs.rng(100, n, m), n, n * m, "fp32")
+    one_np = inputs.normal(inputs.rng(101, n, m), n, m, "fp32")
+    want = {"reduce_scatter": oracle.reduce_scatter(rs_np, "fp32"), "all_gather": oracle.all_gather(one_np, "fp32"),
+            "broadcast": oracle.broadcast(one_np, "fp32", root), "reduce": oracle.reduce(one_np, "fp32", root)}
+    rs_dev = to_device(rs_np, "fp32")
+    one_dev = to_device(one_np, "fp32")
+    with rra.Comm(n, n * m * 4) as comm:
+        for tma in (-1, 0):
+            comm.set_attr("cluster_tma", tma)
+            for op in rra.COLLECTIVES:
+                src = rs_dev if op == "reduce_scatter" else one_dev
+                out_n = n * m if op == "all_gather" else m
+                out = [torch.full((out_n,), float("nan"), device="cuda") for _ in range(n)]
+                comm.collective_ptrs(op, [t.data_ptr() for t in src], [t.data_ptr() for t in out], m, "fp32", root)
+                torch.cuda.synchronize()
+                bulk = tma != 0 and (op != "reduce_scatter" or m % 4 == 0)
+                kind = comm.last_kernel()
+                assert kind == "coll_multi_kernel<%s%s>" % (op, ", bulk" if bulk else ""), kind
+                ranks = [root] if op == "reduce" else range(n)
+                for r in ranks:
+                    assert np.array_equal(bits(out[r].cpu().numpy()), bits(want[op][r])), (op, tma, r)
+        assert comm.status()[0] == rra.OK
+
+
 def test_collective_outputs_in_host_memory_get_vector_stores():
     """Device inputs, outputs in pinned host memory: the push is by bulk
     copies, the outputs are written by vector stores (no bulk copy writes
