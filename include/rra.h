@@ -42,9 +42,11 @@
  * Bulk-copy pushes stay on one GPU.  Some cluster kernels push by TMA bulk
  * copies with cluster multicast (cp.async.bulk ... .multicast::cluster) that
  * read straight from the callers' input buffers: the cluster one-/two-shot
- * AllReduce and the fused residual AllReduce up to 16 ranks, and AllGather and
- * Broadcast up to 16 ranks.  A call uses them only when (a) every buffer such
- * a copy reads is device memory of the current GPU -- checked with
+ * AllReduce and the four collectives at every rank count, and the fused
+ * residual AllReduce up to 16 ranks; AllGather and Broadcast up to 16 ranks
+ * also write their outputs by bulk copies (then every output must be device
+ * memory of the current GPU too).  A call uses them only when (a) every
+ * buffer such a copy reads is device memory of the current GPU -- checked with
  * cudaPointerGetAttributes at both ends of the range read, the result of a
  * passing check remembered for the last 8 sets of input pointers of the
  * communicator -- and (b) the process holds no active context on any other
@@ -183,15 +185,17 @@ typedef enum {
                                       copies both ways and a Reduce on bulk copies (see
                                       "The other collectives"), which stay one call of their
                                       own shape; 0 never, 1 always; up to 16 ranks */
-    RRA_ATTR_CLUSTER_TMA = 13      /* cluster one-/two-shot AllReduce (up to 16 ranks) with
-                                      the push made by the TMA engine: bulk copies from a
-                                      rank's input into the peers' shared memory (multicast
-                                      to all N for the one-shot, one copy per partition
-                                      owner for the two-shot); also the fused residual
-                                      AllReduce, AllGather and Broadcast.  -1 (default) and
-                                      1: on (faster at every N and size measured) for calls
-                                      whose inputs pass the check of "Bulk-copy pushes"
-                                      above; 0: st.async pushes always */
+    RRA_ATTR_CLUSTER_TMA = 13      /* cluster one-/two-shot AllReduce with the push made
+                                      by the TMA engine: bulk copies from a rank's input
+                                      into the peers' shared memory (multicast to all CTAs
+                                      for the one-shot, one copy per partition owner for
+                                      the two-shot; above 16 ranks one per hosted rank);
+                                      also the fused residual AllReduce (up to 16 ranks)
+                                      and the four collectives.  -1 (default) and 1: on
+                                      (faster at every N and size measured but the
+                                      smallest two-shot calls) for calls whose inputs pass
+                                      the check of "Bulk-copy pushes" above; 0: st.async
+                                      pushes always */
 } rra_attr_t;
 
 /* Scratch layout of one window (bytes), as planned for (nranks, max_bytes).
