@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librra.so")
 
 SOURCES = ["kernels.cu", "cluster.cu", "coll.cu", "fused.cu", "rra_api.cu", "probes.cu", "rra_static.cu"]
-HEADERS = ["prims.cuh", "cluster_prims.cuh", "rra_internal.h", "placement.h"]
+HEADERS = ["prims.cuh", "cluster_prims.cuh", "rra_internal.h", "placement.h", "kernel_attrs.h"]
 PUBLIC_HEADERS = ["rra.h", "rra_probe.h", "rra_static.h", "rra_device.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -40,6 +40,7 @@
 #include "cluster_prims.cuh"
 #include "prims.cuh"
 #include "rra_internal.h"
+#include "kernel_attrs.h"
 
 namespace rra {
 
@@ -618,23 +619,8 @@ static const void* cluster_kernel_ptr(rra_dtype_t dtype, int mode) {
     return nullptr;
 }
 
-// Opt the kernel in to the full stage and to clusters of up to 16 CTAs
-// (once per kernel; the attributes are process-wide).
-static cudaError_t configure(const void* k) {
-    static const void* done[64] = {};
-    for (const void* d : done)
-        if (d == k) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    for (const void*& d : done)
-        if (d == nullptr) {
-            d = k;
-            break;
-        }
-    return cudaSuccess;
-}
+// Opt the kernel in to the full stage and to clusters of up to 16 CTAs.
+static cudaError_t configure(const void* k) { return configure_cluster_kernel(k, (int)kClusterStageBytes); }
 
 size_t cluster_stage_bytes(const Params& p, int mode) {
     const size_t n = (size_t)p.nranks;

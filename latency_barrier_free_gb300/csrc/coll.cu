@@ -35,6 +35,7 @@
 #include "cluster_prims.cuh"
 #include "prims.cuh"
 #include "rra_internal.h"
+#include "kernel_attrs.h"
 
 namespace rra {
 namespace {
@@ -919,23 +920,8 @@ static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks, bool b
 // CTAs per cluster: one per rank up to 16 ranks, 16 above.
 static int coll_cdim(int nranks) { return nranks < kClusterMaxRanks ? nranks : kClusterMaxRanks; }
 
-// Opt a kernel in to the full stage and to clusters of up to 16 CTAs (once
-// per kernel; the attributes are process-wide).
-static cudaError_t configure_coll(const void* k) {
-    static const void* done[64] = {};
-    for (const void* d : done)
-        if (d == k) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    for (const void*& d : done)
-        if (d == nullptr) {
-            d = k;
-            break;
-        }
-    return cudaSuccess;
-}
+// Opt the kernel in to the full stage and to clusters of up to 16 CTAs.
+static cudaError_t configure_coll(const void* k) { return configure_cluster_kernel(k, (int)kClusterStageBytes); }
 
 size_t coll_stage_bytes(const Params& p, int op) {
     const size_t n = (size_t)p.nranks;

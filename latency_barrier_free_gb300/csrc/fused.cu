@@ -29,6 +29,7 @@
 #include "prims.cuh"
 #include "rra_device.cuh"
 #include "rra_internal.h"
+#include "kernel_attrs.h"
 
 namespace rra {
 
@@ -225,21 +226,7 @@ static const void* residual_kernel_ptr(rra_dtype_t dtype, bool two_shot, bool bu
     return nullptr;
 }
 
-static cudaError_t configure_residual(const void* k) {
-    static const void* done[12] = {};
-    for (const void* d : done)
-        if (d == k) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterStageBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    for (const void*& d : done)
-        if (d == nullptr) {
-            d = k;
-            break;
-        }
-    return cudaSuccess;
-}
+static cudaError_t configure_residual(const void* k) { return configure_cluster_kernel(k, (int)kClusterStageBytes); }
 
 size_t residual_stage_bytes(const Params& p, bool two_shot) {
     const size_t q = two_shot ? p.per_cta / (uint32_t)p.nranks : p.per_cta;
