@@ -297,6 +297,37 @@ def test_in_kernel_timing():
         assert t[:, 1].max() - t[:, 0].min() < 10_000_000  # < 10 ms
 
 
+@pytest.mark.parametrize("algo,n", [("oneshot_ll", 2), ("oneshot_ll", 4), ("oneshot_sentinel", 2),
+                                    ("oneshot_sentinel", 4), ("oneshot_cluster", 4)])
+def test_trace_points(algo, n):
+    """rra_comm_set_trace: the call launches the traced variant, its result is
+    still exact, and every CTA's six stamps are set and in order; with the
+    buffer switched off a call leaves it untouched."""
+    count = 32
+    sends_np = inputs.normal(inputs.rng(102, n), n, count, "fp32")
+    with rra.Comm(n, count * 4) as comm:
+        grid, _ = comm.plan_call(count, "fp32", algo)
+        buf = torch.zeros(6 * grid, dtype=torch.int64, device="cuda")
+        comm.set_trace(buf.data_ptr())
+        sends = to_device(sends_np, "fp32")
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        comm.set_trace(0)
+        assert comm.status()[0] == rra.OK
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+        t = buf.view(grid, 6).cpu().numpy()
+        assert np.all(t > 0), t
+        assert np.all(np.diff(t, axis=1) >= 0), t
+        assert t[:, 5].max() - t[:, 0].min() < 10_000_000  # < 10 ms
+        buf.fill_(-1)
+        recvs = poison_like(sends)
+        comm.allreduce(sends, recvs, algo)
+        torch.cuda.synchronize()
+        assert bool((buf == -1).all())
+        check_against_oracle(sends_np, to_host(recvs, "fp32"), "fp32", algo)
+
+
 def test_probes():
     ns = rra.probe_l2_chase(4 << 20, 20000, 3)
     assert 50.0 < ns < 10000.0
