@@ -456,6 +456,81 @@ __global__ void __launch_bounds__(256) coll_reduce_bulk_kernel(const __grid_cons
     }
 }
 
+// Reduce above 16 ranks with the push made by the TMA engine, in the
+// partition pattern of coll_reduce_bulk_kernel on 16-CTA clusters: a slice of
+// S = 16 Q vectors is split into 16 partitions, and thread (m, q) of CTA j
+// copies partition q of hosted rank m's slice into slot [rank] of CTA q's
+// window; CTA q adds its N slots in rank order and stores the sums into
+// partition q of the root's output.  No CTA carries more than its partition.
+template <typename T>
+__global__ void __launch_bounds__(256) coll_reduce_multi_bulk_kernel(const __grid_constant__ Params p) {
+    using M = VecMath<T>;
+    extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
+    __shared__ __align__(8) uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t N = (uint32_t)p.nranks;
+    const uint32_t G = (uint32_t)kClusterMaxRanks;
+    const uint32_t j = cluster_ctarank();
+    const uint32_t hosted = (N - j + G - 1) / G;  // ranks j, j + G, ...
+    const uint32_t S = p.per_cta;
+    const uint32_t Q = S / G;
+    const uint32_t base = cluster_id() * S;
+    const uint32_t npos = min(S, p.nvec - base);
+    const uint32_t nt = blockDim.x;
+    const uint64_t count = p.count;
+    auto part_len = [&](uint32_t q) -> uint32_t { return npos > q * Q ? min(Q, npos - q * Q) : 0u; };
+    const uint32_t mine = part_len(j);
+    const uint32_t my_bar = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(my_bar, 1u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(my_bar, N * mine * (uint32_t)kVecBytes);
+    }
+    cluster_arrive_relaxed();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint64_t t_start = globaltimer_ns();
+    const int32_t drop = p.drop_rank;
+    cluster_wait();  // every peer's barrier exists before any copy completes on it
+#pragma unroll 1
+    for (uint32_t c = threadIdx.x; c < hosted * G; c += nt) {
+        const uint32_t m = c / G;
+        const uint32_t q = c - m * G;
+        const uint32_t rank = j + m * G;
+        const uint32_t len = part_len(q);
+        if (len != 0 && (q == j || drop != (int32_t)rank))
+            bulk_g2s_multicast(smem_u32(stage + rank * Q),
+                               (const char*)p.send[rank] + (uint64_t)(base + q * Q) * kVecBytes,
+                               len * (uint32_t)kVecBytes, my_bar, (uint16_t)(1u << q));
+    }
+    int ok = 1;
+    {
+        Waiter w = make_waiter(t_start, p.timeout_ns, p.ctrl, (int)j, 0);
+        while (!mbar_try_wait(my_bar, 0u)) {
+            if (waiter_expired(w)) {
+                ok = 0;
+                break;
+            }
+        }
+    }
+    cluster_arrive_relaxed();  // "my incoming bytes are in" (or my wait ran out)
+    if (ok) {
+        void* const out = p.recv[p.root];
+#pragma unroll 1
+        for (uint32_t u = threadIdx.x; u < mine; u += nt) {
+            typename M::Acc acc = M::load(stage[u]);
+#pragma unroll 1
+            for (uint32_t q = 1; q < N; ++q) M::add(acc, stage[q * Q + u]);
+            store_block<T>(out, 0, base + j * Q + u, count, M::store(acc));
+        }
+    }
+    cluster_wait();  // every CTA's bytes are in: none of my copies is still in flight
+    if (p.timing != nullptr && threadIdx.x == 0) {
+        const uint64_t t_end = globaltimer_ns();
+        p.timing[2 * blockIdx.x] = t_start;
+        p.timing[2 * blockIdx.x + 1] = t_end;
+    }
+}
+
 // The same four collectives for nranks > 16 (clusters hold at most 16
 // CTAs): a cluster of G = 16 CTAs per slice, CTA j acting for ranks j,
 // j + G, j + 2G, ... (as the many-rank cluster AllReduce).  A push to a rank
@@ -467,10 +542,11 @@ __global__ void __launch_bounds__(256) coll_reduce_bulk_kernel(const __grid_cons
 // GPU, checked by the host), the own CTA's slots included: ReduceScatter one
 // copy per hosted rank and owner (blocks of whole 16-byte vectors only),
 // AllGather one multicast copy per hosted rank, Broadcast one from the root's
-// CTA, Reduce one per hosted rank to the root's CTA.  Each CTA then writes
-// from its window, the root's CTA of a Broadcast included.
+// CTA.  Each CTA then writes from its window, the root's CTA of a Broadcast
+// included.  (The bulk-copy Reduce is coll_reduce_multi_bulk_kernel.)
 template <typename T, int kOp, bool kBulk>
 __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__ Params p) {
+    static_assert(!(kBulk && kOp == kCollReduce), "the bulk-copy Reduce is coll_reduce_multi_bulk_kernel");
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
@@ -501,7 +577,6 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
             case kCollReduceScatter: incoming = hosted * N * npos; break;
             case kCollAllGather: incoming = N * npos; break;
             case kCollBroadcast: incoming = npos; break;
-            case kCollReduce: incoming = root_here ? N * npos : 0u; break;
         }
     }
     const uint32_t my_bar = smem_u32(&bar);
@@ -538,7 +613,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
         const uint32_t vbytes = npos * (uint32_t)kVecBytes;
         const uint32_t ncopies = kOp == kCollReduceScatter ? hosted * N
                                  : kOp == kCollBroadcast   ? (root_here ? 1u : 0u)
-                                                           : hosted;
+                                                           : hosted;  // AllGather
 #pragma unroll 1
         for (uint32_t c = threadIdx.x; c < ncopies; c += nt) {
             if (kOp == kCollReduceScatter) {  // block q's slice of hosted rank m to owner q's CTA
@@ -557,12 +632,6 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
             } else if (kOp == kCollBroadcast) {  // the root's slice into slot [0] of every CTA
                 bulk_g2s_multicast(smem_u32(stage), (const char*)p.send[root] + (uint64_t)base * kVecBytes, vbytes,
                                    my_bar, drop != (int32_t)root ? all : (uint16_t)(1u << j));
-            } else {  // Reduce: hosted rank c's slice into its slot of the root's CTA
-                const uint32_t rank = j + c * G;
-                if (root_here || drop != (int32_t)rank)
-                    bulk_g2s_multicast(smem_u32(stage + rank * S),
-                                       (const char*)p.send[rank] + (uint64_t)base * kVecBytes, vbytes, my_bar,
-                                       (uint16_t)(1u << root_cta));
             }
         }
     } else {
@@ -834,7 +903,9 @@ static const void* coll_multi_for(int op) {
         case kCollReduceScatter: return (const void*)coll_multi_kernel<T, kCollReduceScatter, kBulk>;
         case kCollAllGather: return (const void*)coll_multi_kernel<T, kCollAllGather, kBulk>;
         case kCollBroadcast: return (const void*)coll_multi_kernel<T, kCollBroadcast, kBulk>;
-        case kCollReduce: return (const void*)coll_multi_kernel<T, kCollReduce, kBulk>;
+        case kCollReduce:
+            return kBulk ? (const void*)coll_reduce_multi_bulk_kernel<T>
+                         : (const void*)coll_multi_kernel<T, kCollReduce, false>;
     }
     return nullptr;
 }
@@ -874,7 +945,7 @@ const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
     if (op == kCollBroadcastSplit) return "coll_split_kernel<broadcast>";
     if (op == kCollReduceSplit) return "coll_split_kernel<reduce>";
     static const char* const kMultiBulk[] = {"coll_multi_kernel<reduce_scatter, bulk>", "coll_multi_kernel<all_gather, bulk>",
-                                             "coll_multi_kernel<broadcast, bulk>", "coll_multi_kernel<reduce, bulk>"};
+                                             "coll_multi_kernel<broadcast, bulk>", "coll_reduce_multi_bulk_kernel"};
     if (bulk && coll_has_bulk(op, nranks) && nranks > kClusterMaxRanks) return kMultiBulk[op];
     if (bulk && coll_has_bulk(op, nranks)) return store_bulk ? kBulkStore[op] : kBulk[op];
     return nranks > kClusterMaxRanks ? kMulti[op] : kPlain[op];
@@ -948,13 +1019,17 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
                         bool bulk, bool store_bulk) {
     // the bulk-copy Reduce holds N partitions of S / N vectors: S vectors
     const bool part_reduce = bulk && op == kCollReduce && p.nranks <= kClusterMaxRanks;  // coll_reduce_bulk_kernel
-    const size_t smem = part_reduce ? (size_t)p.per_cta * kVecBytes : coll_stage_bytes(p, op);
+    const bool multi_reduce = bulk && op == kCollReduce && p.nranks > kClusterMaxRanks;  // coll_reduce_multi_bulk_kernel
+    const size_t smem = part_reduce    ? (size_t)p.per_cta * kVecBytes
+                        : multi_reduce ? (size_t)p.nranks * (p.per_cta / kClusterMaxRanks) * kVecBytes
+                                       : coll_stage_bytes(p, op);
     if (smem == 0 || smem > kClusterStageBytes || p.nranks < 2 || p.nranks > kMaxRanks || p.root < 0 ||
         p.root >= p.nranks)
         return cudaErrorInvalidValue;
     if ((op == kCollBroadcastSplit || op == kCollReduceSplit || part_reduce) &&
         p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
+    if (multi_reduce && p.per_cta % (uint32_t)kClusterMaxRanks != 0) return cudaErrorInvalidValue;
     const int cdim = coll_cdim(p.nranks);
     const uint64_t es = dtype == RRA_BF16 ? 2u : dtype == RRA_FP64 ? 8u : 4u;
     if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || op == kCollReduceScatter || op == kCollReduce ||

@@ -707,6 +707,8 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     // as the split forms do (above 16 ranks it sends whole slices to the root)
     const bool many = c->nranks > rra::kClusterMaxRanks;
     const bool bulk_reduce = bulk && op == rra::kCollReduce && !many;
+    // above 16 ranks the bulk-copy Reduce splits a slice into 16 partitions
+    const bool multi_reduce = bulk && op == rra::kCollReduce && many;
     const bool split = op == rra::kCollBroadcastSplit || op == rra::kCollReduceSplit || bulk_reduce;
     // above 16 ranks a CTA hosts up to `hosted` ranks (16-CTA clusters)
     const size_t cdim = std::min<size_t>(n, rra::kClusterMaxRanks);
@@ -717,7 +719,9 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t smax;
     switch (op) {
         case rra::kCollBroadcast: smax = stage_vecs; break;
-        case rra::kCollReduce: smax = bulk_reduce ? stage_vecs / n * n : stage_vecs / n; break;  // S or N S vectors
+        case rra::kCollReduce:  // S, N S / 16 or N S vectors
+            smax = bulk_reduce ? stage_vecs / n * n : multi_reduce ? (stage_vecs / n) * 16 : stage_vecs / n;
+            break;
         case rra::kCollBroadcastSplit: smax = stage_vecs * n / (n + 1) / n * n; break;  // (S/N + S) vectors
         case rra::kCollReduceSplit: smax = stage_vecs / 2 / n * n; break;              // 2 S vectors
         case rra::kCollReduceScatter: smax = stage_vecs / (hosted * n); break;          // N slots per hosted owner
@@ -727,6 +731,11 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
     size_t S;
     if (c->cluster_slice > 0) {
         S = (size_t)c->cluster_slice / rra::kVecBytes;
+    } else if (multi_reduce) {
+        // as the bulk-copy Reduce below: about 8 clusters per SM's worth of
+        // slices, at least 512 bytes per partition
+        const size_t target = std::max<size_t>(1, 8 * (size_t)c->sm_count / cdim);
+        S = std::max<size_t>(32 * 16, ceil_div(p->nvec, target));
     } else if (!many && (store_bulk || (bulk && (op == rra::kCollReduceScatter || op == rra::kCollReduce)))) {
         // Outputs (AllGather, Broadcast) or inputs (ReduceScatter, Reduce)
         // moved by bulk copies: the threads no longer move that data, so
@@ -754,7 +763,8 @@ static rra_status_t plan_coll(rra_comm* c, size_t count, rra_dtype_t dtype, int 
         S = std::min<size_t>(S, std::max<size_t>(1, t * rra::kClusterBatch / per_pos));
     }
     if (split) S = align_up(S, n);  // N parts per slice
-    S = std::max<size_t>(split ? n : 1, std::min(S, smax));
+    if (multi_reduce) S = align_up(S, 16);  // 16 partitions per slice
+    S = std::max<size_t>(split ? n : multi_reduce ? 16 : 1, std::min(S, smax));
     p->per_cta = (uint32_t)S;
     p->ctas_per_rank = (int32_t)ceil_div(p->nvec, S);
     *threads = (int)std::min<size_t>(t, std::max<size_t>(32, align_up(S * per_pos, 32)));

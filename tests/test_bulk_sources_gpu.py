@@ -255,7 +255,9 @@ def test_many_rank_collectives_choose_their_push(n, m):
                 torch.cuda.synchronize()
                 bulk = tma != 0 and (op != "reduce_scatter" or m % 4 == 0)
                 kind = comm.last_kernel()
-                assert kind == "coll_multi_kernel<%s%s>" % (op, ", bulk" if bulk else ""), kind
+                want_kind = "coll_reduce_multi_bulk_kernel" if (bulk and op == "reduce") else \
+                    "coll_multi_kernel<%s%s>" % (op, ", bulk" if bulk else "")
+                assert kind == want_kind, kind
                 ranks = [root] if op == "reduce" else range(n)
                 for r in ranks:
                     assert np.array_equal(bits(out[r].cpu().numpy()), bits(want[op][r])), (op, tma, r)
