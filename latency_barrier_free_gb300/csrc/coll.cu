@@ -544,9 +544,16 @@ __global__ void __launch_bounds__(256) coll_reduce_multi_bulk_kernel(const __gri
 // AllGather one multicast copy per hosted rank, Broadcast one from the root's
 // CTA.  Each CTA then writes from its window, the root's CTA of a Broadcast
 // included.  (The bulk-copy Reduce is coll_reduce_multi_bulk_kernel.)
-template <typename T, int kOp, bool kBulk>
+// kStoreBulk (AllGather, Broadcast, with kBulk): the window goes to the
+// hosted ranks' outputs by bulk copies (one per hosted rank and block,
+// spread over the threads, each waited for by its issuing thread); the host
+// chooses it only when every output is device memory of this GPU and a
+// block is whole 16-byte vectors.
+template <typename T, int kOp, bool kBulk, bool kStoreBulk>
 __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__ Params p) {
     static_assert(!(kBulk && kOp == kCollReduce), "the bulk-copy Reduce is coll_reduce_multi_bulk_kernel");
+    static_assert(!kStoreBulk || (kBulk && (kOp == kCollAllGather || kOp == kCollBroadcast)),
+                  "bulk stores: AllGather and Broadcast on bulk copies");
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
@@ -723,6 +730,18 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
                     store_block<T>(p.recv[root], 0, base + u, count, M::store(acc));
                 }
             }
+        } else if (kStoreBulk) {  // AllGather / Broadcast: one bulk copy per hosted rank (and block)
+            fence_proxy_async_smem();
+            const uint32_t blocks = kOp == kCollAllGather ? N : 1u;
+            const uint64_t block_bytes = count * sizeof(T);
+#pragma unroll 1
+            for (uint32_t c = threadIdx.x; c < hosted * blocks; c += nt) {
+                const uint32_t m = c / blocks;
+                const uint32_t q = c - m * blocks;
+                bulk_s2g((char*)p.recv[j + m * G] + q * block_bytes + (uint64_t)base * kVecBytes,
+                         smem_u32(stage + q * S), npos * (uint32_t)kVecBytes);
+            }
+            bulk_s2g_commit_wait();
         } else if (kOp == kCollAllGather) {
 #pragma unroll 1
             for (uint32_t it = threadIdx.x; it < hosted * N * npos; it += nt) {
@@ -898,21 +917,25 @@ __global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__
 }
 
 template <typename T, bool kBulk>
-static const void* coll_multi_for(int op) {
+static const void* coll_multi_for(int op, bool store_bulk) {
     switch (op) {
-        case kCollReduceScatter: return (const void*)coll_multi_kernel<T, kCollReduceScatter, kBulk>;
-        case kCollAllGather: return (const void*)coll_multi_kernel<T, kCollAllGather, kBulk>;
-        case kCollBroadcast: return (const void*)coll_multi_kernel<T, kCollBroadcast, kBulk>;
+        case kCollReduceScatter: return (const void*)coll_multi_kernel<T, kCollReduceScatter, kBulk, false>;
+        case kCollAllGather:
+            if (kBulk && store_bulk) return (const void*)coll_multi_kernel<T, kCollAllGather, true, true>;
+            return (const void*)coll_multi_kernel<T, kCollAllGather, kBulk, false>;
+        case kCollBroadcast:
+            if (kBulk && store_bulk) return (const void*)coll_multi_kernel<T, kCollBroadcast, true, true>;
+            return (const void*)coll_multi_kernel<T, kCollBroadcast, kBulk, false>;
         case kCollReduce:
             return kBulk ? (const void*)coll_reduce_multi_bulk_kernel<T>
-                         : (const void*)coll_multi_kernel<T, kCollReduce, false>;
+                         : (const void*)coll_multi_kernel<T, kCollReduce, false, false>;
     }
     return nullptr;
 }
 
 template <typename T>
-static const void* coll_kernel_for(int op, bool multi, bool bulk = false) {
-    if (multi) return bulk ? coll_multi_for<T, true>(op) : coll_multi_for<T, false>(op);
+static const void* coll_kernel_for(int op, bool multi, bool bulk = false, bool store_bulk = false) {
+    if (multi) return bulk ? coll_multi_for<T, true>(op, store_bulk) : coll_multi_for<T, false>(op, false);
     switch (op) {
         case kCollReduceScatter: return (const void*)coll_kernel<T, kCollReduceScatter>;
         case kCollAllGather: return (const void*)coll_kernel<T, kCollAllGather>;
@@ -946,7 +969,10 @@ const char* coll_kernel_name(int op, int nranks, bool bulk, bool store_bulk) {
     if (op == kCollReduceSplit) return "coll_split_kernel<reduce>";
     static const char* const kMultiBulk[] = {"coll_multi_kernel<reduce_scatter, bulk>", "coll_multi_kernel<all_gather, bulk>",
                                              "coll_multi_kernel<broadcast, bulk>", "coll_reduce_multi_bulk_kernel"};
-    if (bulk && coll_has_bulk(op, nranks) && nranks > kClusterMaxRanks) return kMultiBulk[op];
+    static const char* const kMultiBulkStore[] = {"", "coll_multi_kernel<all_gather, bulk, bulk store>",
+                                                  "coll_multi_kernel<broadcast, bulk, bulk store>", ""};
+    if (bulk && coll_has_bulk(op, nranks) && nranks > kClusterMaxRanks)
+        return store_bulk ? kMultiBulkStore[op] : kMultiBulk[op];
     if (bulk && coll_has_bulk(op, nranks)) return store_bulk ? kBulkStore[op] : kBulk[op];
     return nranks > kClusterMaxRanks ? kMulti[op] : kPlain[op];
 }
@@ -966,9 +992,9 @@ static const void* coll_kernel_ptr(rra_dtype_t dtype, int op, int nranks, bool b
     const bool multi = nranks > kClusterMaxRanks;
     if (bulk && multi && coll_has_bulk(op, nranks)) {
         switch (dtype) {
-            case RRA_FP32: return coll_kernel_for<float>(op, true, true);
-            case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op, true, true);
-            case RRA_FP64: return coll_kernel_for<double>(op, true, true);
+            case RRA_FP32: return coll_kernel_for<float>(op, true, true, store_bulk);
+            case RRA_BF16: return coll_kernel_for<__nv_bfloat16>(op, true, true, store_bulk);
+            case RRA_FP64: return coll_kernel_for<double>(op, true, true, store_bulk);
         }
         return nullptr;
     }
@@ -1033,7 +1059,7 @@ cudaError_t launch_coll(const Params& p, rra_dtype_t dtype, int op, int threads,
     const int cdim = coll_cdim(p.nranks);
     const uint64_t es = dtype == RRA_BF16 ? 2u : dtype == RRA_FP64 ? 8u : 4u;
     if (store_bulk && (!bulk || !coll_has_bulk(op, p.nranks) || op == kCollReduceScatter || op == kCollReduce ||
-                       p.nranks > kClusterMaxRanks || (p.count * es) % kVecBytes != 0))
+                       (p.count * es) % kVecBytes != 0))
         return cudaErrorInvalidValue;  // a bulk copy would write past its block
     if (bulk && op == kCollReduceScatter && (p.count * es) % kVecBytes != 0)
         return cudaErrorInvalidValue;  // a block would start off a 16-byte boundary

@@ -1222,8 +1222,7 @@ static rra_status_t run_coll(rra_comm_t c, int op, int root, const void* const s
             bulk = bulk_sources_local(c, src, nsrc, (rs ? (size_t)c->nranks : 1u) * count * es);
             const size_t store_min = op == rra::kCollBroadcast ? (256u << 10) : (4u << 10);
             const bool may_store = op == rra::kCollAllGather || op == rra::kCollBroadcast;
-            if (bulk && may_store && c->nranks <= rra::kClusterMaxRanks && (count * es) % rra::kVecBytes == 0 &&
-                count * es >= store_min) {
+            if (bulk && may_store && (count * es) % rra::kVecBytes == 0 && count * es >= store_min) {
                 const void* out[RRA_MAX_RANKS];
                 for (int r = 0; r < c->nranks; ++r) out[r] = recv[r];
                 store_bulk = bulk_sources_local(c, out, c->nranks, blocks * count * es);

@@ -264,6 +264,26 @@ def test_many_rank_collectives_choose_their_push(n, m):
         assert comm.status()[0] == rra.OK
 
 
+def test_many_rank_bulk_stores():
+    """Above 16 ranks, AllGather (4 KiB blocks) and Broadcast (256 KiB) on
+    device buffers write their outputs by bulk copies too; the results are
+    the oracle's bits."""
+    n, root = 20, 7
+    with rra.Comm(n, n * 65536 * 4) as comm:
+        for op, m in (("all_gather", 1024), ("broadcast", 65536)):
+            src_np = [inputs.normal(inputs.rng(103, r, m), 1, m, "fp32")[0] for r in range(n)]
+            want = oracle.all_gather(src_np, "fp32") if op == "all_gather" else oracle.broadcast(src_np, "fp32", root)
+            src = to_device(src_np, "fp32")
+            out_n = n * m if op == "all_gather" else m
+            out = [torch.full((out_n,), float("nan"), device="cuda") for _ in range(n)]
+            comm.collective_ptrs(op, [t.data_ptr() for t in src], [t.data_ptr() for t in out], m, "fp32", root)
+            torch.cuda.synchronize()
+            assert comm.last_kernel() == "coll_multi_kernel<%s, bulk, bulk store>" % op, comm.last_kernel()
+            for g, w in zip(out, want):
+                assert np.array_equal(bits(g.cpu().numpy()), bits(w)), op
+        assert comm.status()[0] == rra.OK
+
+
 def test_collective_outputs_in_host_memory_get_vector_stores():
     """Device inputs, outputs in pinned host memory: the push is by bulk
     copies, the outputs are written by vector stores (no bulk copy writes
