@@ -43,9 +43,9 @@
  * copies with cluster multicast (cp.async.bulk ... .multicast::cluster) that
  * read straight from the callers' input buffers: the cluster one-/two-shot
  * AllReduce and the four collectives at every rank count, and the fused
- * residual AllReduce up to 16 ranks; AllGather and Broadcast up to 16 ranks
- * also write their outputs by bulk copies (then every output must be device
- * memory of the current GPU too).  A call uses them only when (a) every
+ * residual AllReduce up to 16 ranks; AllGather and Broadcast also write
+ * their outputs by bulk copies (then every output must be device memory of
+ * the current GPU too).  A call uses them only when (a) every
  * buffer such a copy reads is device memory of the current GPU -- checked with
  * cudaPointerGetAttributes at both ends of the range read, the result of a
  * passing check remembered for the last 8 sets of input pointers of the
