@@ -26,7 +26,13 @@ def _built():
 
 
 def _same_bits(got, expect, what):
-    assert np.array_equal(bits(got), bits(expect)), what
+    g, w = bits(got), bits(expect)
+    bad = np.nonzero(g != w)[0]
+    if bad.size:
+        poison = np.frombuffer(b"\x7f" * g.itemsize, dtype=g.dtype)[0]
+        raise AssertionError("%r: %d of %d elements differ, first at %s; got %s expect %s; %d still poison" % (
+            what, bad.size, g.size, bad[:8].tolist(), [hex(int(v)) for v in g[bad[:4]]],
+            [hex(int(v)) for v in w[bad[:4]]], int((g[bad] == poison).sum())))
 
 
 def _run(comm, op, sends_np, out_count, dtype, root=0, send_mask=None, recv_mask=None):
