@@ -13,8 +13,9 @@ launched one by one from Python are reported as stream_launch_us.
 value     mean over the 28 (dtype, size) cases of microseconds per call with
           the library's automatic choice (RRA_AUTO), lower is better; every
           algorithm's own figure on every case is reported beside it
-e2e       the same metric through rra_allreduce_host: host buffers in and out,
-          host<->device copies inside the timed region
+e2e       the same metric through the host-buffer call (pinned host buffers
+          in and out, synchronised per call), and the host link it runs over:
+          the device reading, writing, and copying pinned host memory (GB/s)
 roofline  the dominant kernel of the step against the measured HBM peak
 floor     measured single-GPU latency floor 2*L2_RTT + L_store->poll and the
           in-kernel time of the 128-byte calls
@@ -435,7 +436,7 @@ def summary_line(d, detail_path):
     if "cpu_baseline" in d:
         out["cpu_baseline"] = d["cpu_baseline"]
     e = d.get("e2e", {})
-    out["e2e"] = {k: e.get(k) for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+    out["e2e"] = {k: e.get(k) for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "host_link_GBps")}
     out["e2e"]["api"] = "rra_allreduce_mapped on pinned host buffers (zero copy), synchronised per call"
     ck = d.get("clocks", {})
     out["clocks"] = {k: ck.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}
@@ -970,8 +971,16 @@ def end_to_end(comm, rra, cases, torch, args):
         per.append((time.perf_counter() - t0) / reps * 1e6)
         h2d += NRANKS * size
         d2h += NRANKS * size
+    # The link these calls run over: the device streaming pinned host memory
+    # (N x the largest per-rank size each way, as in the largest case).  Each
+    # case moves N M bytes in and N M bytes out at once, so N M / copy rate is
+    # its link-bound time.
+    link_r, link_w, link_c = rra.probe_host_link(NRANKS * max(size for _, size in cases), 20)
+    link_us = [round(NRANKS * size / (link_c * 1e3), 2) for _, size in cases]
     return {"value": round(float(np.mean(per)), 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "host_link_GBps": {"read": round(link_r, 1), "write": round(link_w, 1), "both": round(link_c, 1)},
+            "link_bound_us": link_us,
             "api": "prepared host call (Comm.prepare_host) on pinned host buffers: resolved once by "
                    "rra_host_device_ptrs, then rra_allreduce_mapped per call, synchronised per call; the kernel "
                    "reads the inputs from and writes the outputs to host memory over NVLink-C2C (zero copy)",

@@ -14,6 +14,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <numeric>
 #include <random>
 #include <vector>
@@ -164,6 +165,51 @@ struct BigParams {
 // The launch copies the parameter block whether or not the body reads it.
 __global__ void empty_kernel_big(const __grid_constant__ BigParams p) { (void)p; }
 
+// Host-link probes: every thread streams 16-byte vectors, grid-strided, with
+// kLinkBatch loads in flight, through pinned host memory mapped into the
+// device's address space.  The read folds the vectors into one word that is
+// stored only if it matches a value no input has (so the loads stay live).
+constexpr int kLinkBatch = 4;
+
+__global__ void link_read_kernel(const uint4* __restrict__ src, size_t n, uint4* sink) {
+    uint32_t acc = 0;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += stride * kLinkBatch) {
+        uint4 v[kLinkBatch];
+#pragma unroll
+        for (int k = 0; k < kLinkBatch; ++k) {
+            const size_t i = i0 + (size_t)k * stride;
+            v[k] = i < n ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kLinkBatch; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+    }
+    if (acc == 0xFFFFFFFFu) sink[0] = make_uint4(acc, 0u, 0u, 0u);
+}
+
+__global__ void link_write_kernel(uint4* dst, size_t n) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        dst[i] = make_uint4((uint32_t)i, 0u, 0u, 0u);
+}
+
+__global__ void link_copy_kernel(const uint4* __restrict__ src, uint4* dst, size_t n) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += stride * kLinkBatch) {
+        uint4 v[kLinkBatch];
+#pragma unroll
+        for (int k = 0; k < kLinkBatch; ++k) {
+            const size_t i = i0 + (size_t)k * stride;
+            if (i < n) v[k] = src[i];
+        }
+#pragma unroll
+        for (int k = 0; k < kLinkBatch; ++k) {
+            const size_t i = i0 + (size_t)k * stride;
+            if (i < n) dst[i] = v[k];
+        }
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -310,6 +356,66 @@ rra_status_t rra_probe_launch_shape(int ctas, int threads, int big_params, int c
         return RRA_ERR_CUDA;
     }
     return RRA_OK;
+}
+
+rra_status_t rra_probe_host_link(size_t bytes, int iters, double* read_gbps, double* write_gbps,
+                                 double* copy_gbps) {
+    if (read_gbps == nullptr || write_gbps == nullptr || copy_gbps == nullptr || bytes < (64u << 10) ||
+        bytes > (1ull << 30) || bytes % 16 != 0 || iters <= 0 || iters > 10000)
+        return RRA_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    uint4 *h_src = nullptr, *h_dst = nullptr, *m_src = nullptr, *m_dst = nullptr, *sink = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    rra_status_t st = RRA_OK;
+    if (cudaHostAlloc((void**)&h_src, bytes, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostAlloc((void**)&h_dst, bytes, cudaHostAllocMapped) != cudaSuccess ||
+        cudaMalloc((void**)&sink, 16) != cudaSuccess) {
+        cudaGetLastError();
+        st = RRA_ERR_OOM;
+    }
+    if (st == RRA_OK && (cudaHostGetDevicePointer((void**)&m_src, h_src, 0) != cudaSuccess ||
+                         cudaHostGetDevicePointer((void**)&m_dst, h_dst, 0) != cudaSuccess ||
+                         cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)) {
+        cudaGetLastError();
+        st = RRA_ERR_CUDA;
+    }
+    const size_t n = bytes / 16;
+    if (st == RRA_OK) {
+        for (size_t i = 0; i < n; ++i) h_src[i] = make_uint4((uint32_t)i, 1u, 2u, 3u);
+    }
+    // two CTAs of 256 threads per SM; mean of `iters` launches after two warm-ups
+    const dim3 grid((unsigned)(2 * sms)), block(256);
+    auto measure = [&](int which, double* gbps) {
+        if (st != RRA_OK) return;
+        for (int r = -2; r < iters; ++r) {
+            if (r == 0 && cudaEventRecord(e0) != cudaSuccess) break;
+            if (which == 0) link_read_kernel<<<grid, block>>>(m_src, n, sink);
+            else if (which == 1) link_write_kernel<<<grid, block>>>(m_dst, n);
+            else link_copy_kernel<<<grid, block>>>(m_src, m_dst, n);
+        }
+        float ms = 0.f;
+        if (cudaGetLastError() != cudaSuccess || cudaEventRecord(e1) != cudaSuccess ||
+            cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.f) {
+            cudaGetLastError();
+            st = RRA_ERR_CUDA;
+            return;
+        }
+        *gbps = (double)bytes * iters / ((double)ms * 1e6);
+    };
+    measure(0, read_gbps);
+    measure(1, write_gbps);
+    measure(2, copy_gbps);
+    if (st == RRA_OK && cudaDeviceSynchronize() != cudaSuccess) st = RRA_ERR_CUDA;
+    if (st == RRA_OK && std::memcmp(h_src, h_dst, bytes) != 0) st = RRA_ERR_CUDA;  // the copy arrived whole
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (sink) cudaFree(sink);
+    if (h_src) cudaFreeHost(h_src);
+    if (h_dst) cudaFreeHost(h_dst);
+    return st;
 }
 
 }  // extern "C"

@@ -43,7 +43,7 @@ SYMBOLS = [
     "rra_version",
     "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_dsmem_pingpong", "rra_probe_empty_kernel",
     "rra_probe_launch_shape",
-    "rra_probe_sm_count",
+    "rra_probe_sm_count", "rra_probe_host_link",
     "rra_allreduce_static",
     "rra_reduce_scatter", "rra_all_gather", "rra_broadcast", "rra_reduce",
     "rra_allreduce_residual",
@@ -120,6 +120,8 @@ def load(path: str = LIB_PATH):
                                           ip, ip], i32),
             "rra_probe_empty_kernel": ([vp], i32),
             "rra_probe_sm_count": ([ip], i32),
+            "rra_probe_host_link": ([sz, i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_double)], i32),
             "rra_probe_launch_shape": ([i32, i32, i32, i32, vp], i32),
             "rra_reduce_scatter": ([vp, pp, pp, sz, i32, vp], i32),
             "rra_all_gather": ([vp, pp, pp, sz, i32, vp], i32),
@@ -509,6 +511,18 @@ def probe_sm_count() -> int:
     v = ctypes.c_int()
     _check(load().rra_probe_sm_count(ctypes.byref(v)), "rra_probe_sm_count")
     return v.value
+
+
+def probe_host_link(nbytes: int = 8 << 20, iters: int = 20):
+    """(read, write, copy) GB/s of the device streaming pinned host memory:
+    reading one buffer, writing another, and copying one into the other (each
+    direction at once)."""
+    r = ctypes.c_double()
+    w = ctypes.c_double()
+    c = ctypes.c_double()
+    _check(load().rra_probe_host_link(int(nbytes), int(iters), ctypes.byref(r), ctypes.byref(w), ctypes.byref(c)),
+           "rra_probe_host_link")
+    return r.value, w.value, c.value
 
 
 def probe_dsmem_pingpong(iters: int = 20000):

@@ -343,6 +343,18 @@ def test_probes():
     torch.cuda.synchronize()
 
 
+def test_probe_host_link():
+    """The host-link probe: three positive rates below any plausible link
+    (the probe itself checks that its copy arrived whole), and its argument
+    checks."""
+    r, w, c = rra.probe_host_link(1 << 20, 5)
+    for x in (r, w, c):
+        assert 1.0 < x < 5000.0
+    for nbytes, iters in ((1000, 5), (1 << 20, 0), ((1 << 20) + 8, 5)):
+        with pytest.raises(rra.RraError):
+            rra.probe_host_link(nbytes, iters)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("start", [2 ** 31 - 5, 2 ** 32 - 3, 3 * 2 ** 31 - 1])
 def test_epoch_scrub_at_boundary(algo, start):
