@@ -972,10 +972,9 @@ def end_to_end(comm, rra, cases, torch, args):
         h2d += NRANKS * size
         d2h += NRANKS * size
     # The link these calls run over: the device streaming pinned host memory
-    # (N x the largest per-rank size each way, as in the largest case).  Each
-    # case moves N M bytes in and N M bytes out at once, so N M / copy rate is
-    # its link-bound time.
-    link_r, link_w, link_c = rra.probe_host_link(NRANKS * max(size for _, size in cases), 20)
+    # (32 MiB buffers: the copy's steady rate).  Each case moves N M bytes in
+    # and N M bytes out at once, so N M / copy rate is its link-bound time.
+    link_r, link_w, link_c = rra.probe_host_link(32 << 20, 10)
     link_us = [round(NRANKS * size / (link_c * 1e3), 2) for _, size in cases]
     return {"value": round(float(np.mean(per)), 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,

@@ -75,12 +75,14 @@ rra_status_t rra_probe_sm_count(int* sms);
 /* The host link that the host-buffer AllReduce (rra_allreduce_host,
  * rra_allreduce_mapped, zero copy) runs over: two pinned, device-mapped host
  * buffers of `bytes` each (allocated and freed here; 64 KiB to 1 GiB, a
- * multiple of 16) streamed by 2 x SMs CTAs of 256 threads with 16-byte loads
- * and stores.  Outputs, in GB/s of `bytes` per launch (mean over `iters`
- * launches after two warm-ups): read_gbps, the device reading the first
- * buffer; write_gbps, the device writing the second; copy_gbps, the device
- * copying the first into the second (reads and writes at once: bytes per
- * second in each direction).  The copy is checked on the host afterwards.
+ * multiple of 16) streamed with 16-byte loads and stores.  Outputs, in GB/s
+ * of `bytes` per launch (mean over `iters` launches after two warm-ups):
+ * read_gbps, the device reading the first buffer; write_gbps, the device
+ * writing the second; copy_gbps, the device copying the first into the
+ * second, one vector in flight per thread, so that reads and writes overlap
+ * (bytes per second in each direction).  The copy reaches its steady rate
+ * from about 16 MiB; smaller buffers spend a larger share filling and
+ * draining.  The copy is checked on the host afterwards.
  * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_OOM, RRA_ERR_CUDA (a launch failed or
  * the copied buffer differs). */
 rra_status_t rra_probe_host_link(size_t bytes, int iters, double* read_gbps, double* write_gbps,

@@ -165,10 +165,11 @@ struct BigParams {
 // The launch copies the parameter block whether or not the body reads it.
 __global__ void empty_kernel_big(const __grid_constant__ BigParams p) { (void)p; }
 
-// Host-link probes: every thread streams 16-byte vectors, grid-strided, with
-// kLinkBatch loads in flight, through pinned host memory mapped into the
-// device's address space.  The read folds the vectors into one word that is
-// stored only if it matches a value no input has (so the loads stay live).
+// Host-link probes: threads stream 16-byte vectors, grid-strided, through
+// pinned host memory mapped into the device's address space (the reads with
+// kLinkBatch loads in flight per thread).  The read folds the vectors into
+// one word that is stored only if it matches a value no input has (so the
+// loads stay live).
 constexpr int kLinkBatch = 4;
 
 __global__ void link_read_kernel(const uint4* __restrict__ src, size_t n, uint4* sink) {
@@ -195,19 +196,7 @@ __global__ void link_write_kernel(uint4* dst, size_t n) {
 
 __global__ void link_copy_kernel(const uint4* __restrict__ src, uint4* dst, size_t n) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += stride * kLinkBatch) {
-        uint4 v[kLinkBatch];
-#pragma unroll
-        for (int k = 0; k < kLinkBatch; ++k) {
-            const size_t i = i0 + (size_t)k * stride;
-            if (i < n) v[k] = src[i];
-        }
-#pragma unroll
-        for (int k = 0; k < kLinkBatch; ++k) {
-            const size_t i = i0 + (size_t)k * stride;
-            if (i < n) dst[i] = v[k];
-        }
-    }
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = src[i];
 }
 
 }  // namespace
@@ -386,15 +375,19 @@ rra_status_t rra_probe_host_link(size_t bytes, int iters, double* read_gbps, dou
     if (st == RRA_OK) {
         for (size_t i = 0; i < n; ++i) h_src[i] = make_uint4((uint32_t)i, 1u, 2u, 3u);
     }
-    // two CTAs of 256 threads per SM; mean of `iters` launches after two warm-ups
-    const dim3 grid((unsigned)(2 * sms)), block(256);
+    // mean of `iters` launches after two warm-ups.  Read and write: two CTAs
+    // of 256 threads per SM.  Copy: one CTA of 128 threads per SM, one vector
+    // in flight per thread, so that every thread's next load overlaps other
+    // threads' stores (with all of a small buffer in flight at once, the
+    // reads and the writes would run one after the other)
+    const dim3 grid((unsigned)(2 * sms)), block(256), cgrid((unsigned)sms), cblock(128);
     auto measure = [&](int which, double* gbps) {
         if (st != RRA_OK) return;
         for (int r = -2; r < iters; ++r) {
             if (r == 0 && cudaEventRecord(e0) != cudaSuccess) break;
             if (which == 0) link_read_kernel<<<grid, block>>>(m_src, n, sink);
             else if (which == 1) link_write_kernel<<<grid, block>>>(m_dst, n);
-            else link_copy_kernel<<<grid, block>>>(m_src, m_dst, n);
+            else link_copy_kernel<<<cgrid, cblock>>>(m_src, m_dst, n);
         }
         float ms = 0.f;
         if (cudaGetLastError() != cudaSuccess || cudaEventRecord(e1) != cudaSuccess ||

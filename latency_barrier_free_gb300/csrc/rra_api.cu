@@ -631,6 +631,15 @@ static rra_status_t plan_cluster(rra_comm* c, size_t count, rra_dtype_t dtype, r
         // st.async-era shape below)
         if (!c->threads_set) T = n <= 8 ? 64 : 128;
         S = 64 * n;
+    } else if (two && host) {
+        // host buffers (zero copy): 4 KiB slices, 256 threads, one vector per
+        // thread.  Every load crosses the host link, so more, smaller slices
+        // keep more of it busy (GB300, N = 4: 4 MiB per rank in 106 us in the
+        // kernel against 154 us with the device-memory shape below, at the
+        // link's rate for reading and writing at once; 1 MiB 44 against 50 us
+        // per synchronised call)
+        if (!c->threads_set) T = 256;
+        S = 256;
     } else if (two && s_mid <= 1024) {
         // two-shot up to ~1-2 MiB per rank (latency-bound): about 512 CTAs of
         // 256 threads, 2-4 vectors per thread (GB300 sweep at N = 4, 8:

@@ -225,6 +225,29 @@ def test_host_entry_pinned_buffers(algo, zero_copy):
                 t.fill_(float("nan"))
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("n", [3, 8, 16])
+def test_host_zero_copy_two_shot(n, dtype):
+    """The cluster two-shot on pinned host buffers (zero copy) takes its own
+    slices (4 KiB, aligned up to N partitions): the oracle's result at a size
+    of many slices and a ragged tail, for N that do and do not divide a
+    slice."""
+    count = 300001
+    sends_np = inputs.normal(inputs.rng(77, n), n, count, dtype)
+    tdt = torch.float32 if dtype == "fp32" else torch.bfloat16
+    hs = [torch.from_numpy(a.view(np.int16) if dtype == "bf16" else a).view(tdt).pin_memory() for a in sends_np]
+    hr = [torch.full((count,), float("nan"), dtype=tdt).pin_memory() for _ in range(n)]
+    with rra.Comm(n, count * 4) as comm:
+        call = comm.prepare_host([t.data_ptr() for t in hs], [t.data_ptr() for t in hr], count, dtype,
+                                 "twoshot_cluster")
+        for _ in range(2):
+            call()
+            got = [t.view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else t.numpy() for t in hr]
+            check_against_oracle(sends_np, got, dtype, "twoshot_cluster")
+            for t in hr:
+                t.fill_(float("nan"))
+
+
 @pytest.mark.parametrize("algo", ["auto", "oneshot_cluster", "twoshot_cluster", "oneshot_sentinel", "ll128_atomic"])
 def test_host_buffers_resolved_once(algo):
     """Pinned host buffers resolved once (rra_host_device_ptrs), then
