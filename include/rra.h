@@ -269,7 +269,10 @@ rra_status_t rra_allreduce(rra_comm_t comm, const void* const send[], void* cons
  * is pinned host memory that the device can address (cudaHostAlloc'd or
  * registered; on GB300 the GPU reaches it over the coherent NVLink-C2C link
  * to the Grace CPU) and RRA_ATTR_HOST_ZERO_COPY is 1 (default), the kernel
- * reads the inputs and writes the outputs in host memory directly.
+ * reads the inputs and writes the outputs in host memory directly; such a
+ * call moves nranks * count elements each way over the host link, whose
+ * rates rra_probe_host_link (rra_probe.h) measures, and the cluster two-shot
+ * then takes 4 KiB slices, which keep more of that link busy.
  * Otherwise the call copies every send[r] to device staging buffers owned
  * by the communicator (allocated on first use: 2 * nranks * max_bytes), runs
  * rra_allreduce, and copies every recv[r] back (one cudaMemcpyAsync per rank
