@@ -612,6 +612,31 @@ def latency_floor(comm, rra, measure, torch, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     node_us = e0.elapsed_time(e1) * 1000.0 / (20 * 160)
+
+    # the same for an empty kernel launched as the 128-byte cluster AllReduce
+    # at N=4 is (4 CTAs of 32 threads, one cluster, programmatic dependent
+    # launch): the per-call floor of back-to-back dependent calls of that shape
+    def chain_us(cluster, pdl):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            rra.probe_launch_chain(4, 32, cluster, pdl, s)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(160):
+                    rra.probe_launch_chain(4, 32, cluster, pdl, s)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(20):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return round(e0.elapsed_time(e1) * 1000.0 / (20 * 160), 3)
+
+    chain = {"cluster4_pdl": chain_us(4, True), "cluster4": chain_us(4, False), "pdl": chain_us(1, True)}
+
     def over(key):
         ref = dsmem_floor_ns if key.endswith("cluster") else floor_ns
         return round(kern[key] / (ref / 1000.0), 3)
@@ -624,6 +649,7 @@ def latency_floor(comm, rra, measure, torch, stream):
             "in_kernel_us_128B": kern, "x_floor": {k: over(k) for k in kern}, "best_in_kernel": best_key,
             "best_over_floor": over(best_key),
             "empty_kernel_us": round(empty_us, 3), "graph_node_us": round(node_us, 3),
+            "chain_node_us": chain,
             "method": "L2 RTT: dependent ld.global.cg chase, 8 MiB random cycle; store->poll: half the mean RTT "
                       "of a fence-free ping-pong between CTA 0 and 32 CTAs on other SMs (same-die and cross-die "
                       "pairs); floor = 2 L2 RTT + store->poll for the global-memory kernels; floor_dsmem = half "

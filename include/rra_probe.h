@@ -69,6 +69,15 @@ rra_status_t rra_probe_empty_kernel(rra_stream_t stream);
  * graph-node cost by grid shape, parameter size and launch kind. */
 rra_status_t rra_probe_launch_shape(int ctas, int threads, int big_params, int cooperative, rra_stream_t stream);
 
+/* Launch one empty kernel of `ctas` x `threads` on `stream` as the AllReduce
+ * kernels launch: in clusters of `cluster` CTAs (1: no cluster; up to 8,
+ * dividing `ctas`) and, if `pdl`, with programmatic dependent launch; the
+ * kernel lets its successor launch and waits for its predecessor
+ * (griddepcontrol), nothing else.  A chain of these in a CUDA graph gives
+ * the per-call floor of back-to-back dependent calls of that shape.
+ * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_CUDA. */
+rra_status_t rra_probe_launch_chain(int ctas, int threads, int cluster, int pdl, rra_stream_t stream);
+
 /* Number of SMs of the current device. */
 rra_status_t rra_probe_sm_count(int* sms);
 

@@ -165,6 +165,14 @@ struct BigParams {
 // The launch copies the parameter block whether or not the body reads it.
 __global__ void empty_kernel_big(const __grid_constant__ BigParams p) { (void)p; }
 
+// An empty kernel shaped like the AllReduce kernels' launches: it lets the
+// next kernel launch, then waits for the previous one (programmatic
+// dependent launch), and does nothing else.
+__global__ void chain_kernel() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Host-link probes: threads stream 16-byte vectors, grid-strided, through
 // pinned host memory mapped into the device's address space (the reads with
 // kLinkBatch loads in flight per thread).  The read folds the vectors into
@@ -341,6 +349,37 @@ rra_status_t rra_probe_launch_shape(int ctas, int threads, int big_params, int c
         e = cudaLaunchKernelExC(&cfg, (const void*)empty_kernel, nullptr);
     }
     if (e != cudaSuccess) {
+        cudaGetLastError();
+        return RRA_ERR_CUDA;
+    }
+    return RRA_OK;
+}
+
+rra_status_t rra_probe_launch_chain(int ctas, int threads, int cluster, int pdl, rra_stream_t stream) {
+    if (ctas < 1 || ctas > 4096 || threads < 32 || threads > 1024 || cluster < 1 || cluster > 8 ||
+        ctas % cluster != 0)
+        return RRA_ERR_INVALID_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if (cudaLaunchKernelExC(&cfg, (const void*)chain_kernel, nullptr) != cudaSuccess) {
         cudaGetLastError();
         return RRA_ERR_CUDA;
     }

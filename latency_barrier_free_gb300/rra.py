@@ -43,7 +43,7 @@ SYMBOLS = [
     "rra_version",
     "rra_probe_l2_chase", "rra_probe_pingpong", "rra_probe_dsmem_pingpong", "rra_probe_empty_kernel",
     "rra_probe_launch_shape",
-    "rra_probe_sm_count", "rra_probe_host_link",
+    "rra_probe_sm_count", "rra_probe_host_link", "rra_probe_launch_chain",
     "rra_allreduce_static",
     "rra_reduce_scatter", "rra_all_gather", "rra_broadcast", "rra_reduce",
     "rra_allreduce_residual",
@@ -123,6 +123,7 @@ def load(path: str = LIB_PATH):
             "rra_probe_host_link": ([sz, i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_double)], i32),
             "rra_probe_launch_shape": ([i32, i32, i32, i32, vp], i32),
+            "rra_probe_launch_chain": ([i32, i32, i32, i32, vp], i32),
             "rra_reduce_scatter": ([vp, pp, pp, sz, i32, vp], i32),
             "rra_all_gather": ([vp, pp, pp, sz, i32, vp], i32),
             "rra_broadcast": ([vp, i32, pp, pp, sz, i32, vp], i32),
@@ -505,6 +506,11 @@ def probe_empty_kernel(stream=None):
 def probe_launch_shape(ctas: int, threads: int, big_params: bool, cooperative: bool, stream=None):
     _check(load().rra_probe_launch_shape(int(ctas), int(threads), int(bool(big_params)), int(bool(cooperative)),
                                          _stream_handle(stream)), "rra_probe_launch_shape")
+
+
+def probe_launch_chain(ctas: int, threads: int, cluster: int, pdl: bool, stream=None):
+    _check(load().rra_probe_launch_chain(int(ctas), int(threads), int(cluster), int(bool(pdl)),
+                                         _stream_handle(stream)), "rra_probe_launch_chain")
 
 
 def probe_sm_count() -> int:

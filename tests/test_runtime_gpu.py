@@ -366,6 +366,27 @@ def test_probes():
     torch.cuda.synchronize()
 
 
+def test_probe_launch_chain():
+    """Empty kernels launched in clusters and with programmatic dependent
+    launch run to completion on a stream and inside a captured graph; shapes
+    the probe does not take are refused."""
+    for cluster, pdl in ((4, True), (4, False), (1, True), (8, True)):
+        rra.probe_launch_chain(8, 32, cluster, pdl)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(8):
+                rra.probe_launch_chain(4, 32, 4, True, s)
+    g.replay()
+    torch.cuda.synchronize()
+    for ctas, threads, cluster in ((6, 32, 4), (4, 16, 1), (4, 32, 0), (16, 32, 16)):
+        with pytest.raises(rra.RraError):
+            rra.probe_launch_chain(ctas, threads, cluster, True)
+
+
 def test_probe_host_link():
     """The host-link probe: three positive rates below any plausible link
     (the probe itself checks that its copy arrived whole), and its argument
