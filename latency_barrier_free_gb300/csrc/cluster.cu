@@ -203,9 +203,14 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
 // its extra lanes are never stored.  Since a CTA cannot see when its own
 // copies into peers have landed, it leaves only after a cluster barrier
 // that every CTA arrives at once its own incoming bytes are in.  kTrace: as
-// for cluster_kernel.
-template <typename T, bool kTwoShot, bool kTrace>
-__global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant__ Params p) {
+// for cluster_kernel.  kResidual (one-shot only): the fused AllReduce +
+// residual add, every output round(rank-order sum + that rank's residual),
+// the residual added to the running value, one rounding.  (A two-shot form,
+// whose partition owners add every destination's residual, measured slower
+// than the device-API kernel of fused.cu at two-shot sizes.)
+template <typename T, bool kTwoShot, bool kTrace, bool kResidual>
+__device__ __forceinline__ void tma_body(const Params& p, const void* const* resid) {
+    static_assert(!(kTwoShot && kResidual), "the residual epilogue is the one-shot's");
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
@@ -237,6 +242,9 @@ __global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant_
         tr[0] = t_start;
         tr[1] = globaltimer_after((uint64_t)(uint32_t)drop);
     }
+    // the residual of this thread's first output, read while the copies fly
+    uint4 rv0 = make_uint4(0u, 0u, 0u, 0u);
+    if (kResidual && threadIdx.x < mine) rv0 = load_input<T>(resid[r], base + threadIdx.x, p.count);
     cluster_wait();  // every peer's barrier exists before any copy completes on it
     if (tr) tr[2] = globaltimer_ns();
     const bool pushes = drop != (int32_t)r;
@@ -279,6 +287,9 @@ __global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant_
                     const uint32_t d = r + k < N ? r + k : r + k - N;
                     store_output<T>(p.recv[d], pos, p.count, out);
                 }
+            } else if (kResidual) {
+                M::add(acc, u == threadIdx.x ? rv0 : load_input<T>(resid[r], base + u, p.count));
+                store_output<T>(p.recv[r], base + u, p.count, M::store(acc));
             } else {
                 store_output<T>(p.recv[r], base + u, p.count, out);
             }
@@ -291,6 +302,16 @@ __global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant_
         p.timing[2 * blockIdx.x + 1] = t_end;
     }
     if (tr) tr[5] = globaltimer_ns();
+}
+
+template <typename T, bool kTwoShot, bool kTrace>
+__global__ void __launch_bounds__(256) cluster_tma_kernel(const __grid_constant__ Params p) {
+    tma_body<T, kTwoShot, kTrace, false>(p, nullptr);
+}
+
+template <typename T, bool kTrace>
+__global__ void __launch_bounds__(256) cluster_tma_residual_kernel(const __grid_constant__ FusedParams f) {
+    tma_body<T, false, kTrace, true>(f.base, f.resid);
 }
 
 // More ranks than CTAs in a cluster (N > 16): CTA j of a cluster of G = 16
@@ -612,6 +633,7 @@ static const void* cluster_kernel_for(int mode) {
         case kClusterTwoshotMultiRes: return (const void*)residual_multi_kernel<T, true>;
         case kClusterOneshotTma: return (const void*)cluster_tma_kernel<T, false, kTrace>;
         case kClusterTwoshotTma: return (const void*)cluster_tma_kernel<T, true, kTrace>;
+        case kClusterOneshotTmaRes: return (const void*)cluster_tma_residual_kernel<T, kTrace>;
     }
     return nullptr;
 }
@@ -635,7 +657,8 @@ size_t cluster_stage_bytes(const Params& p, int mode) {
     const size_t n = (size_t)p.nranks;
     switch (mode) {
         case kClusterOneshot:
-        case kClusterOneshotTma: return n * p.per_cta * kVecBytes;
+        case kClusterOneshotTma:
+        case kClusterOneshotTmaRes: return n * p.per_cta * kVecBytes;
         case kClusterTwoshot:
         case kClusterTwoshotTma: return (size_t)p.per_cta / n * n * kVecBytes;
         case kClusterTwoshotPipe: return 2 * ((size_t)p.per_cta / n * n) * kVecBytes;
@@ -671,7 +694,8 @@ static cudaError_t launch_cluster_args(const Params& p, void* arg, rra_dtype_t d
     if ((mode == kClusterTwoshot || mode == kClusterTwoshotPipe || mode == kClusterTwoshotTma) &&
         p.per_cta % (uint32_t)p.nranks != 0)
         return cudaErrorInvalidValue;
-    if ((mode == kClusterTwoshotTma || mode == kClusterOneshotTma) && threads < p.nranks)
+    if ((mode == kClusterTwoshotTma || mode == kClusterOneshotTma || mode == kClusterOneshotTmaRes) &&
+        threads < p.nranks)
         return cudaErrorInvalidValue;  // the two-shot's copies are issued by threads 0..N-1
     if ((mode == kClusterTwoshotMulti || mode == kClusterTwoshotMultiRes || mode == kClusterTwoshotMultiTma) &&
         p.per_cta % (uint32_t)kClusterMaxRanks != 0)
@@ -712,7 +736,8 @@ static cudaError_t launch_cluster_args(const Params& p, void* arg, rra_dtype_t d
 }
 
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl) {
-    if (mode == kClusterOneshotMultiRes || mode == kClusterTwoshotMultiRes) return cudaErrorInvalidValue;
+    if (mode == kClusterOneshotMultiRes || mode == kClusterTwoshotMultiRes || mode == kClusterOneshotTmaRes)
+        return cudaErrorInvalidValue;
     return launch_cluster_args(p, (void*)&p, dtype, mode, threads, stream, pdl);
 }
 
@@ -720,6 +745,11 @@ cudaError_t launch_cluster_residual(const FusedParams& f, rra_dtype_t dtype, boo
                                     cudaStream_t stream, bool pdl) {
     const int mode = two_shot ? kClusterTwoshotMultiRes : kClusterOneshotMultiRes;
     return launch_cluster_args(f.base, (void*)&f, dtype, mode, threads, stream, pdl);
+}
+
+cudaError_t launch_cluster_tma_residual(const FusedParams& f, rra_dtype_t dtype, int threads, cudaStream_t stream,
+                                        bool pdl) {
+    return launch_cluster_args(f.base, (void*)&f, dtype, kClusterOneshotTmaRes, threads, stream, pdl);
 }
 
 // Clusters of `nranks` CTAs of this kernel, `threads` threads and `smem`

@@ -1375,16 +1375,34 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
     if (count > c->max_bytes / elem_size(dtype)) return RRA_ERR_INVALID_ARG;
     rra::FusedParams f;
     int threads = 0;
-    bool two = false, bulk = false;
+    bool two = false, bulk = false, tma_res = false;
     {
         std::lock_guard<std::mutex> g(c->mu);
-        const bool local = bulk_copy_push(c) && bulk_sources_local(c, send, c->nranks, count * elem_size(dtype));
-        rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two, &bulk, local);
-        if (st != RRA_OK) return st;
-        c->last_kernel = c->nranks > rra::kClusterMaxRanks
+        const size_t bytes = count * elem_size(dtype);
+        const bool local = bulk_copy_push(c) && bulk_sources_local(c, send, c->nranks, bytes);
+        // Up to 16 ranks, the one-shot shape on bulk copies with one slice per
+        // cluster: the cluster AllReduce's bulk-copy one-shot, planned as for
+        // rra_allreduce, with the residual add in its epilogue (N = 8, bf16
+        // [B, 8192]: B = 1 in 1.1 us in the kernel, B = 4 in 1.3 us, against
+        // 1.8 and 2.0 us for the device-API kernel below; at two-shot sizes
+        // that kernel stays faster than the same epilogue on the cluster
+        // two-shot)
+        if (c->nranks <= rra::kClusterMaxRanks && local && c->ctas_per_rank <= 0 && c->cluster_pipe == 0 &&
+            select_cluster(c->nranks, bytes, true) == RRA_ONESHOT_CLUSTER) {
+            int mode = 0;
+            rra_status_t st = plan_cluster(c, count, dtype, RRA_ONESHOT_CLUSTER, &f.base, &threads, &mode, false, true);
+            if (st != RRA_OK) return st;
+            tma_res = mode == rra::kClusterOneshotTma;
+        }
+        if (!tma_res) {
+            rra_status_t st = plan_residual(c, count, dtype, &f, &threads, &two, &bulk, local);
+            if (st != RRA_OK) return st;
+        }
+        c->last_kernel = tma_res ? "cluster_tma_kernel<one-shot, residual>"
+                         : c->nranks > rra::kClusterMaxRanks
                              ? (two ? "residual_multi_kernel<two-shot>" : "residual_multi_kernel<one-shot>")
-                             : bulk ? (two ? "residual_kernel<two-shot, bulk>" : "residual_kernel<one-shot, bulk>")
-                                    : (two ? "residual_kernel<two-shot>" : "residual_kernel<one-shot>");
+                         : bulk ? (two ? "residual_kernel<two-shot, bulk>" : "residual_kernel<one-shot, bulk>")
+                                : (two ? "residual_kernel<two-shot>" : "residual_kernel<one-shot>");
     }
     for (int r = 0; r < c->nranks; ++r) {
         if (send[r] == nullptr || residual[r] == nullptr || recv[r] == nullptr) return RRA_ERR_INVALID_ARG;
@@ -1394,7 +1412,8 @@ rra_status_t rra_allreduce_residual(rra_comm_t c, const void* const send[], cons
         f.resid[r] = residual[r];
     }
     f.base.drop_rank = c->drop_rank;
-    cudaError_t e = c->nranks > rra::kClusterMaxRanks
+    cudaError_t e = tma_res ? rra::launch_cluster_tma_residual(f, dtype, threads, (cudaStream_t)stream, c->pdl != 0)
+                    : c->nranks > rra::kClusterMaxRanks
                         ? rra::launch_cluster_residual(f, dtype, two, threads, (cudaStream_t)stream, c->pdl != 0)
                         : rra::launch_residual(f, dtype, two, bulk, threads, (cudaStream_t)stream, c->pdl != 0);
     if (e != cudaSuccess) {

@@ -114,10 +114,13 @@ cudaError_t occupancy(rra_dtype_t dtype, int kind, int threads, int* blocks_per_
 // rra_allreduce_residual in their epilogue (launch_cluster_residual only).
 // kClusterOneshotTma / kClusterTwoshotTma: kClusterOneshot / kClusterTwoshot
 // with the push made by bulk copies (RRA_ATTR_CLUSTER_TMA); the ...MultiTma
-// modes the same for more than 16 ranks.
+// modes the same for more than 16 ranks.  kClusterOneshotTmaRes:
+// kClusterOneshotTma with the residual add of rra_allreduce_residual in its
+// epilogue (launch_cluster_tma_residual only).
 enum { kClusterOneshot = 0, kClusterTwoshot = 1, kClusterTwoshotPipe = 2, kClusterOneshotMulti = 3,
        kClusterTwoshotMulti = 4, kClusterOneshotMultiRes = 5, kClusterTwoshotMultiRes = 6,
-       kClusterOneshotTma = 7, kClusterTwoshotTma = 8, kClusterOneshotMultiTma = 9, kClusterTwoshotMultiTma = 10 };
+       kClusterOneshotTma = 7, kClusterTwoshotTma = 8, kClusterOneshotMultiTma = 9, kClusterTwoshotMultiTma = 10,
+       kClusterOneshotTmaRes = 11 };
 size_t cluster_stage_bytes(const Params& p, int mode);
 cudaError_t launch_cluster(const Params& p, rra_dtype_t dtype, int mode, int threads, cudaStream_t stream, bool pdl);
 int cluster_max_active(rra_dtype_t dtype, int mode, int nranks, int threads, size_t smem);
@@ -160,6 +163,11 @@ int residual_max_active(rra_dtype_t dtype, bool two_shot, bool bulk, int nranks,
 // cluster AllReduce (kClusterOneshotMulti / kClusterTwoshotMulti).
 cudaError_t launch_cluster_residual(const FusedParams& f, rra_dtype_t dtype, bool two_shot, int threads,
                                     cudaStream_t stream, bool pdl);
+// The one-shot of up to 16 ranks on bulk copies with the residual add in its
+// epilogue (cluster.cu): f.base planned as for the cluster AllReduce's
+// kClusterOneshotTma.
+cudaError_t launch_cluster_tma_residual(const FusedParams& f, rra_dtype_t dtype, int threads, cudaStream_t stream,
+                                        bool pdl);
 cudaError_t launch_init(char* base, size_t total, const rra_layout_t& lay, int nranks,
                         cudaStream_t stream);
 

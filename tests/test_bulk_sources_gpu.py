@@ -327,8 +327,10 @@ def test_fused_residual_chooses_its_push_by_source_memory():
             comm.allreduce_residual_ptrs(src, [t.data_ptr() for t in res], [t.data_ptr() for t in out], count, "fp32")
             torch.cuda.synchronize()
             kind = comm.last_kernel()
-            assert kind.startswith("residual_kernel<")
-            assert kind.endswith(", bulk>") == (where == "device"), kind
+            # device inputs: the cluster AllReduce's bulk-copy one-shot with the
+            # residual epilogue; host inputs: the device-API kernel on st.async
+            want_kind = "cluster_tma_kernel<one-shot, residual>" if where == "device" else "residual_kernel<one-shot>"
+            assert kind == want_kind, kind
             for g, w in zip(out, want):
                 assert np.array_equal(bits(g.cpu().numpy()), bits(w))
         assert comm.status()[0] == rra.OK

@@ -1,9 +1,11 @@
 """GPU parity of rra_allreduce_residual (the AllReduce with its residual add
-fused, written on the public device API include/rra_device.cuh) against
-the oracle, bit for bit: both shapes (one-shot, two-shot), every dtype,
-ragged sizes, many epochs per cluster (sub-buffer reuse), in place, graph
-replay, and a dropped rank; above 16 ranks the many-rank cluster kernels
-with the residual add in their epilogue."""
+fused) against the oracle, bit for bit: both shapes (one-shot, two-shot),
+every dtype, ragged sizes, many epochs per cluster (sub-buffer reuse), in
+place, graph replay, and a dropped rank.  Up to 16 ranks the one-shot sizes
+run the cluster AllReduce's bulk-copy one-shot with the residual add in its
+epilogue, the rest the kernel written on the public device API
+(include/rra_device.cuh); above 16 ranks the many-rank cluster kernels with
+the residual add in their epilogue."""
 import numpy as np
 import pytest
 
@@ -75,6 +77,30 @@ def test_many_epochs_per_cluster(shape_count, clusters, threads, tma):
         for it in range(2):
             sends_np, res_np = _case(n, shape_count, dtype, clusters, threads, it, tma)
             _check(comm, sends_np, res_np, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp64"])
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
+def test_kernel_choice(n, dtype):
+    """Up to 16 ranks, device inputs at one-shot sizes run the cluster
+    AllReduce's bulk-copy one-shot with the residual epilogue; two-shot
+    sizes, capped clusters (several slices per cluster) and st.async pushes
+    run the device-API kernel.  Every form gives the oracle's bits."""
+    small, large = 333, 1200007  # one-shot, two-shot at every N and dtype here, with either push
+    with rra.Comm(n, large * ELEM[dtype]) as comm:
+        for attrs, count, want in (({}, small, "cluster_tma_kernel<one-shot, residual>"),
+                                   ({}, large, "residual_kernel<two-shot, bulk>"),
+                                   ({"ctas_per_rank": 1}, small, "residual_kernel<one-shot, bulk>"),
+                                   ({"ctas_per_rank": 2}, large, "residual_kernel<two-shot, bulk>"),
+                                   ({"cluster_tma": 0}, small, "residual_kernel<one-shot>"),
+                                   ({"cluster_tma": 0}, large, "residual_kernel<two-shot>")):
+            comm.set_attr("ctas_per_rank", 0)
+            comm.set_attr("cluster_tma", -1)
+            for k, v in attrs.items():
+                comm.set_attr(k, v)
+            sends_np, res_np = _case(n, count, dtype, 11, count, *attrs.values())
+            _check(comm, sends_np, res_np, dtype)
+            assert comm.last_kernel() == want, (attrs, count, comm.last_kernel())
 
 
 @pytest.mark.parametrize("n", [4, 40])
