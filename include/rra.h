@@ -389,7 +389,12 @@ rra_status_t rra_reduce(rra_comm_t comm, int root, const void* const send[], voi
  * output with that rank's residual (outputs and residuals are then treated
  * as registered symmetric buffers, as by RRA_TWOSHOT_DIRECT).  The shape is
  * the one RRA_AUTO's cluster AllReduce takes (rra_select_algo); the pushes
- * are the device API's bulk sends unless RRA_ATTR_CLUSTER_TMA is 0.  Above 16 ranks: the
+ * are the device API's bulk sends unless RRA_ATTR_CLUSTER_TMA is 0.  Up to
+ * 16 ranks, at one-shot sizes with the bulk-copy push and one slice per
+ * cluster (RRA_ATTR_CTAS_PER_RANK unset), the kernel is the cluster
+ * AllReduce's own bulk-copy one-shot with the residual add in its epilogue
+ * ("cluster_tma_kernel<one-shot, residual>"), not the device-API kernel.
+ * Above 16 ranks: the
  * many-rank cluster AllReduce (16-CTA clusters, CTA j acting for ranks j,
  * j + 16, ...; one-shot while 16 * nranks * count * element size <= 1 MiB)
  * with the residual add in its epilogue instead of the device-API kernel.
