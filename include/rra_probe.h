@@ -72,8 +72,9 @@ rra_status_t rra_probe_launch_shape(int ctas, int threads, int big_params, int c
 /* Launch one empty kernel of `ctas` x `threads` on `stream` as the AllReduce
  * kernels launch: in clusters of `cluster` CTAs (1: no cluster; up to 8,
  * dividing `ctas`) and, if `pdl`, with programmatic dependent launch; the
- * kernel lets its successor launch and waits for its predecessor
- * (griddepcontrol), nothing else.  A chain of these in a CUDA graph gives
+ * kernel releases its successor and waits for its predecessor as the
+ * AllReduce kernels do (griddepcontrol; a one-cluster grid releases at
+ * entry, a larger one after its wait), nothing else.  A chain of these in a CUDA graph gives
  * the per-call floor of back-to-back dependent calls of that shape.
  * Errors: RRA_ERR_INVALID_ARG, RRA_ERR_CUDA. */
 rra_status_t rra_probe_launch_chain(int ctas, int threads, int cluster, int pdl, rra_stream_t stream);

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(256) cluster_kernel(const __grid_constant__ Pa
         mbar_expect_tx(my_bar, (N - 1) * mine * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
 
     // first batch of inputs and the injected-fault word, in flight together
@@ -214,7 +214,7 @@ __device__ __forceinline__ void tma_body(const Params& p, const void* const* res
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -232,7 +232,7 @@ __device__ __forceinline__ void tma_body(const Params& p, const void* const* res
         mbar_expect_tx(my_bar, N * mine * (uint32_t)kVecBytes);  // every slot, the own one included
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     uint64_t* const tr = (kTrace && p.trace != nullptr && threadIdx.x == 0)
@@ -340,7 +340,7 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t G = (uint32_t)kClusterMaxRanks;
     const uint32_t j = cluster_ctarank();
@@ -359,7 +359,7 @@ __device__ __forceinline__ void multi_body(const Params& p, const void* const* r
         mbar_expect_tx(my_bar, (kBulk ? N : N - hosted) * mine * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     if (kBulk) {
@@ -506,8 +506,8 @@ __global__ void __launch_bounds__(256) cluster_pipe_kernel(const __grid_constant
     extern __shared__ __align__(16) uint4 stage[];  // [2][N][Q] payload vectors
     __shared__ __align__(8) uint64_t full[2];
     __shared__ __align__(8) uint64_t empty[2];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_release_early();
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();

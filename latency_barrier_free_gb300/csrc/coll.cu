@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [slots][S]
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) coll_kernel(const __grid_constant__ Param
         mbar_expect_tx(my_bar, incoming * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const void* src = p.send[r];
     const int32_t drop = p.drop_rank;
@@ -244,7 +244,7 @@ template <typename T, int kOp, bool kStoreBulk>
 __global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(16) uint4 stage[];  // AllGather [N][S], Broadcast [S]
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(256) coll_bulk_kernel(const __grid_constant__ 
         mbar_expect_tx(my_bar, incoming * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     cluster_wait();  // every peer's barrier exists before any copy completes on it
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(256) coll_rs_bulk_kernel(const __grid_constant
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [N][S]
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(256) coll_rs_bulk_kernel(const __grid_constant
         mbar_expect_tx(my_bar, N * npos * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     cluster_wait();  // every peer's barrier exists before any copy completes on it
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(256) coll_reduce_bulk_kernel(const __grid_cons
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(256) coll_reduce_bulk_kernel(const __grid_cons
         mbar_expect_tx(my_bar, N * mine * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     cluster_wait();  // every peer's barrier exists before any copy completes on it
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(256) coll_reduce_multi_bulk_kernel(const __gri
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];  // [N][Q]
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t G = (uint32_t)kClusterMaxRanks;
     const uint32_t j = cluster_ctarank();
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(256) coll_reduce_multi_bulk_kernel(const __gri
         mbar_expect_tx(my_bar, N * mine * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     cluster_wait();  // every peer's barrier exists before any copy completes on it
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
     using M = VecMath<T>;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t G = (uint32_t)kClusterMaxRanks;
     const uint32_t j = cluster_ctarank();
@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(256) coll_multi_kernel(const __grid_constant__
         mbar_expect_tx(my_bar, incoming * (uint32_t)kVecBytes);
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const int32_t drop = p.drop_rank;
     const uint32_t per_rank = kOp == kCollReduceScatter ? N * npos : npos;  // items per hosted rank
@@ -785,7 +785,7 @@ __global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__
     constexpr bool kBcast = kOp == kCollBroadcastSplit;
     extern __shared__ __align__(16) uint4 stage[];
     __shared__ __align__(8) uint64_t bars[2];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t r = cluster_ctarank();
     const uint32_t S = p.per_cta;
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(256) coll_split_kernel(const __grid_constant__
         }
     }
     cluster_arrive_relaxed();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const void* src = p.send[r];
     const bool pushes = p.drop_rank != (int32_t)r;

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
     const Params& p = f.base;
     extern __shared__ __align__(16) uint4 window[];
     __shared__ __align__(8) uint64_t bars[2];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     const uint32_t N = (uint32_t)p.nranks;
     const uint32_t S = p.per_cta;
     const uint32_t Q = kTwoShot ? S / N : S;  // slot vectors
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256) residual_kernel(const __grid_constant__ F
         t.setup(window, bars, Q, senders * mine_of(cid, r0) * (uint32_t)kVecBytes);
     }
     const uint32_t r = t.rank();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const uint64_t t_start = globaltimer_ns();
     const uint64_t deadline = t_start + p.timeout_ns;
     const void* src = p.send[r];

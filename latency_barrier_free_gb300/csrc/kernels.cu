@@ -95,14 +95,14 @@ __device__ __noinline__ bool epoch_scrub(const Params& p, int rank) {
 // so the first input loads overlap this round trip instead of waiting behind
 // a block barrier.  The barrier sits in the epilogue instead: no thread may
 // overwrite epoch slot b before every thread of the CTA has read it.
-// Programmatic dependent launch: let the next kernel on the stream be
-// scheduled now (it waits in its own griddepcontrol.wait), and wait until the
-// previous kernel has completed and its memory is visible before this one
-// touches global memory.  Both are no-ops without the launch attribute.
-// Every kernel calls this first.
+// Programmatic dependent launch (prims.cuh): release the next kernel on the
+// stream (at entry for a one-cluster grid, else after the wait), and wait
+// until the previous kernel has completed and its memory is visible before
+// this one touches global memory.  Both are no-ops without the launch
+// attribute.  Kernels without their own prologue call this first.
 __device__ __forceinline__ void pdl_entry() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_release_early();
+    pdl_wait();
 }
 
 // The parameter fields the AllReduce kernels use, read once before the kernel
@@ -489,10 +489,10 @@ __device__ __forceinline__ void prefetch_paths(const Params& p) {
 
 template <typename T, bool kLL, bool kTrace>
 __global__ void __launch_bounds__(256) oneshot_kernel(const __grid_constant__ Params p) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     warm_params(p);
     prefetch_paths<kLL>(p);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     uint4 pre;
     const bool has_pre = prefetch_first<T>(p, pre);
     const CtaState s = cta_prologue(p, kLL || p.nsteps > 1);
@@ -504,9 +504,9 @@ template <typename T, bool kLL>
 __global__ void __launch_bounds__(256) oneshot_wide_kernel(const __grid_constant__ Params p) {
     __shared__ uint4 stage[kStageVecs];
     __shared__ int fail;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     warm_params(p);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     uint4 pre;
     const bool has_pre = prefetch_first<T>(p, pre);
     if (threadIdx.x == 0) fail = 0;
@@ -956,9 +956,9 @@ __device__ __forceinline__ bool twoshot_body(const Params& p, const CtaState& s)
 
 template <typename T, bool kDirect>
 __global__ void __launch_bounds__(128, 4) twoshot_kernel(const __grid_constant__ Params p) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     warm_params(p);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     const CtaState s = cta_prologue(p, p.nsteps > 1);
     if (!s.skip) (void)twoshot_body<T, kDirect>(p, s);
     cta_epilogue(p, s);
@@ -1319,9 +1319,9 @@ __device__ __forceinline__ bool ll128_wide_body(const Params& p, const CtaState&
 
 template <typename T>
 __global__ void __launch_bounds__(256) ll128_wide_kernel(const __grid_constant__ Params p) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     warm_params(p);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     CtaState s = cta_prologue(p);
     s.skip = __syncthreads_or(s.skip) != 0;  // CTA-wide syncs follow: skip must be CTA-uniform
     if (!s.skip) (void)ll128_wide_body<T>(p, s);
@@ -1330,9 +1330,9 @@ __global__ void __launch_bounds__(256) ll128_wide_kernel(const __grid_constant__
 
 template <typename T>
 __global__ void __launch_bounds__(256) ll128_kernel(const __grid_constant__ Params p) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_release_early();
     warm_params(p);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
     CtaState s = cta_prologue(p);
     s.skip = __any_sync(0xFFFFFFFFu, s.skip) != 0;  // warp syncs follow: skip must be warp-uniform
     if (!s.skip) (void)ll128_body<T>(p, s);

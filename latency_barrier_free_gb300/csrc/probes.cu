@@ -165,12 +165,12 @@ struct BigParams {
 // The launch copies the parameter block whether or not the body reads it.
 __global__ void empty_kernel_big(const __grid_constant__ BigParams p) { (void)p; }
 
-// An empty kernel shaped like the AllReduce kernels' launches: it lets the
-// next kernel launch, then waits for the previous one (programmatic
+// An empty kernel shaped like the AllReduce kernels' launches: it releases
+// the next kernel and waits for the previous one as they do (programmatic
 // dependent launch), and does nothing else.
 __global__ void chain_kernel() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    rra::pdl_release_early();
+    rra::pdl_wait();
 }
 
 // Host-link probes: threads stream 16-byte vectors, grid-strided, through
